@@ -1,0 +1,464 @@
+"""Benchmark of the paged decode step: append the new token, then decode.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+                    [--impl ours|reference] [--no-cpu-baseline]
+
+A step is one pass of the whole path over one batch: the slot-mapped append
+of every sequence's new token, then decode attention (split-K + log-sum-exp
+combine) over every sequence's paged context.  Inputs are seeded synthetic
+data resident in HBM; the K/V pool (GBs) is far larger than the 129 MB L2,
+so no flush is needed between steps for the default workload.
+
+Prints one JSON line (rank 0).  `value` is the effective HBM throughput of the
+step in GB/s (algorithmic bytes: K/V in context, q, out, block-table entries,
+and the append's reads and writes), summed over ranks; tokens/s is reported
+beside it.  Under torchrun each rank runs its own independent batch (weak
+scaling, no collective on the data path).
+"""
+from __future__ import annotations
+
+import argparse
+import ctypes
+import hashlib
+import json
+import math
+import os
+import statistics
+import sys
+import threading
+import time
+
+import numpy as np
+import torch
+
+REPO = os.path.dirname(os.path.abspath(__file__))
+if REPO not in sys.path:
+    sys.path.insert(0, REPO)
+
+METRIC = "paged decode: effective KV HBM GB/s (% of GB300 peak) and decode tokens/sec"
+DEFAULT_WORKLOAD = "mha_fp16"
+L2_BYTES = 129 * 1024 * 1024
+FALLBACK_HBM_GBS = 6800.0
+DTYPE_NAME = {torch.float32: "f32", torch.float16: "f16", torch.bfloat16: "bf16"}
+
+
+# ---------------------------------------------------------------------------
+# helpers
+
+
+def dist_env():
+    return (int(os.environ.get("RANK", "0")), int(os.environ.get("WORLD_SIZE", "1")),
+            int(os.environ.get("LOCAL_RANK", "0")))
+
+
+def hbm_peak():
+    path = os.path.join(REPO, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            v = float(json.load(f)["hbm_gbs"])
+        return v, "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def step_bytes(w):
+    """Algorithmic bytes of one step of workload `w` at each of its steps."""
+    spec = w.spec
+    e = torch.tensor([], dtype=spec.dtype).element_size()
+    B, hq, hkv, d, bs = (spec.num_seqs, spec.num_q_heads, spec.num_kv_heads, spec.head_dim,
+                         spec.block_size)
+    out = []
+    for s in range(w.steps):
+        L = w.lens_steps[s].cpu().numpy().astype(np.int64)
+        lo = np.maximum(L - spec.window, 0) if spec.window > 0 else np.zeros_like(L)
+        ctx = int((L - lo).sum())
+        pages = int((((L - 1) // bs) - (lo // bs) + 1).clip(min=0).sum())
+        kv = ctx * 2 * hkv * d * e
+        qo = 2 * B * hq * d * e
+        meta = pages * 4 + B * 4
+        append = B * hkv * d * e * 2 * 2 + B * 8
+        out.append({"kv": kv, "decode": kv + qo + meta, "append": append,
+                    "step": kv + qo + meta + append, "tokens_kvhead": ctx * hkv})
+    return out
+
+
+class ClockSampler:
+    """Samples SM clock and clock-event reasons through NVML while running."""
+    REASONS = {0x1: "gpu_idle", 0x2: "applications_clocks_setting", 0x4: "sw_power_cap",
+               0x8: "hw_slowdown", 0x10: "sync_boost", 0x20: "sw_thermal_slowdown",
+               0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown",
+               0x100: "display_clock_setting"}
+
+    def __init__(self, index, period=0.01):
+        self.samples, self.reasons, self.max_mhz = [], 0, None
+        self.period, self._stop = period, threading.Event()
+        self.ok = False
+        try:
+            self.nvml = ctypes.CDLL("libnvidia-ml.so.1")
+            if self.nvml.nvmlInit_v2() != 0:
+                return
+            self.h = ctypes.c_void_p()
+            if self.nvml.nvmlDeviceGetHandleByIndex_v2(index, ctypes.byref(self.h)) != 0:
+                return
+            mx = ctypes.c_uint()
+            if self.nvml.nvmlDeviceGetMaxClockInfo(self.h, 1, ctypes.byref(mx)) == 0:
+                self.max_mhz = mx.value
+            self.ok = True
+        except OSError:
+            pass
+
+    def _poll(self):
+        clk, rsn = ctypes.c_uint(), ctypes.c_ulonglong()
+        while not self._stop.is_set():
+            if self.nvml.nvmlDeviceGetClockInfo(self.h, 1, ctypes.byref(clk)) == 0:
+                self.samples.append(clk.value)
+            if self.nvml.nvmlDeviceGetCurrentClocksEventReasons(self.h, ctypes.byref(rsn)) == 0:
+                self.reasons |= rsn.value
+            time.sleep(self.period)
+
+    def __enter__(self):
+        if self.ok:
+            self._t = threading.Thread(target=self._poll, daemon=True)
+            self._t.start()
+        return self
+
+    def __exit__(self, *a):
+        if self.ok:
+            self._stop.set()
+            self._t.join()
+
+    def summary(self):
+        if not self.ok:
+            return None
+        names = [n for bit, n in self.REASONS.items() if self.reasons & bit and n != "gpu_idle"]
+        return {"sm_mhz": statistics.median(self.samples) if self.samples else None,
+                "sm_max_mhz": self.max_mhz, "reasons": names, "samples": len(self.samples)}
+
+
+def kernel_source_digest():
+    h = hashlib.sha256()
+    csrc = os.path.join(REPO, "paged_kv_cache_24_gb300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        if name.startswith("pkv_decode") or name in ("pkv_device.cuh", "pkv_internal.h"):
+            with open(os.path.join(csrc, name), "rb") as f:
+                h.update(name.encode() + b"\0" + f.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(workload):
+    """DRAM bytes per decode launch from a committed ncu summary, if it still
+    describes the current kernel source (else None)."""
+    path = os.path.join(REPO, "profiles", "decode_traffic.json")
+    try:
+        with open(path) as f:
+            rec = json.load(f)
+    except Exception:
+        return None
+    ent = rec.get(workload)
+    if not ent or ent.get("kernel_digest") != kernel_source_digest():
+        return None
+    return ent.get("dram_bytes_per_launch")
+
+
+# ---------------------------------------------------------------------------
+# CPU legs: the float64 oracle as it stands
+
+
+class OracleSampler:
+    """Times the float64 oracle, as it stands, on random (sequence, query head)
+    pairs of a workload, on the host cores.  Rates are K/V bytes per second,
+    counting each pair's share (1/G) of its kv head's context."""
+
+    def __init__(self, w):
+        import oracle
+
+        self.oracle = oracle
+        self.w = w
+        spec = w.spec
+        self.e = torch.tensor([], dtype=spec.dtype).element_size()
+        self.kc, self.vc = w.k_cache.cpu(), w.v_cache.cpu()
+        self.bt = w.block_tables.cpu().numpy()
+        self.lens = w.lens_steps[0].cpu().numpy()
+        self.q = w.q_steps[0].cpu()
+        self.threads = oracle.max_threads()
+
+    def run(self, n_pairs, seed=0):
+        spec = self.w.spec
+        rng = np.random.default_rng(seed)
+        total = spec.num_seqs * spec.num_q_heads
+        flat = rng.choice(total, size=min(n_pairs, total), replace=False)
+        pairs = np.stack([flat // spec.num_q_heads, flat % spec.num_q_heads], 1).astype(np.int32)
+        t0 = time.perf_counter()
+        self.oracle.decode(self.q, self.kc, self.vc, self.bt, self.lens, spec.window,
+                           self.w.scale, pairs=pairs, threads=self.threads)
+        dt = time.perf_counter() - t0
+        L = self.lens[pairs[:, 0]].astype(np.int64)
+        lo = np.maximum(L - spec.window, 0) if spec.window > 0 else 0
+        G = spec.num_q_heads // spec.num_kv_heads
+        kvb = float(((L - lo) * 2 * spec.head_dim * self.e).sum()) / G
+        return kvb / dt, dt, len(pairs)
+
+    def rate_for(self, target_s):
+        """Grow the sample until it takes about target_s seconds."""
+        n = max(1, self.threads)
+        while True:
+            rate, dt, got = self.run(n)
+            total = self.w.spec.num_seqs * self.w.spec.num_q_heads
+            if dt >= 0.5 * target_s or got >= total:
+                return rate, dt, got
+            n = int(min(total, max(n + 1, n * target_s / max(dt, 1e-3))))
+
+
+def run_reference(args, workload):
+    """The oracle as the reference arm, on the host cores (rank 0 only)."""
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return 0
+    from paged_kv_cache_24_gb300.workloads import CONFIGS, config_spec, make_workload
+
+    spec = config_spec(CONFIGS[workload])
+    w = make_workload(spec, device="cpu", poison=True)
+    sampler = OracleSampler(w)
+    # calibrate, then size each step so that all warm-up and timed steps take
+    # about two minutes
+    _, dt, got = sampler.run(max(1, sampler.threads))
+    per_pair = dt / got
+    per_step = 120.0 / max(1, args.steps + args.warmup)
+    pairs = int(max(1, min(spec.num_seqs * spec.num_q_heads, per_step / max(per_pair, 1e-6))))
+    for i in range(args.warmup):
+        sampler.run(pairs, seed=1000 + i)
+    rates, times = [], []
+    for i in range(args.steps):
+        r, dt, _ = sampler.run(pairs, seed=i)
+        rates.append(r)
+        times.append(dt)
+    gbs = statistics.median(rates) / 1e9
+    desc = f"{pairs} random (sequence, query head) pairs per step"
+    line = {
+        "impl": "reference", "metric": METRIC, "value": gbs, "unit": "GB/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": 1e3 * statistics.median(times), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": workload, "sample": desc},
+        "cpu_baseline": {"value": gbs, "unit": "GB/s", "cores": sampler.threads,
+                         "kind": "oracle", "sample": desc},
+        "e2e": {"value": gbs, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ---------------------------------------------------------------------------
+# the GPU arm
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    args = ap.parse_args(argv)
+    args.warmup = max(args.warmup, 3)
+
+    if args.impl == "reference":
+        return run_reference(args, args.workload)
+
+    import paged_kv_cache_24_gb300 as pkv
+    from paged_kv_cache_24_gb300.workloads import CONFIGS, config_spec, make_workload
+
+    rank, world, local_rank = dist_env()
+    torch.cuda.set_device(local_rank)
+    pg = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("gloo")
+        pg = dist
+
+    base = config_spec(CONFIGS[args.workload])
+    spec = config_spec(CONFIGS[args.workload], seed=base.seed + 1000 * rank)
+    w = make_workload(spec, device="cuda", poison=True)
+    S = w.steps
+    bs = spec.block_size
+    sbytes = step_bytes(w)
+
+    stream = torch.cuda.current_stream()
+    slots = [pkv.pkv_slot_mapping(w.block_tables, w.pos_steps[s].contiguous(), bs)
+             for s in range(S)]
+    lens = [w.lens_steps[s].contiguous() for s in range(S)]
+    out = torch.empty_like(w.q_steps[0])
+    plan = pkv.pkv_decode_plan(spec.num_seqs, spec.num_q_heads, pkv.cache_layout(w.k_cache),
+                               w.max_blocks, spec.window)
+    launches_per_step = 2 + (1 if plan[1] > 1 else 0)
+
+    def step(s):
+        i = s % S
+        pkv.pkv_append(w.k_steps[i], w.v_steps[i], slots[i], w.k_cache, w.v_cache)
+        pkv.pkv_decode(w.q_steps[i], w.k_cache, w.v_cache, w.block_tables, lens[i],
+                       spec.window, w.scale, out=out)
+
+    kv_per_step = statistics.mean(b["kv"] for b in sbytes)
+    need_flush = kv_per_step < 2 * L2_BYTES
+    flush_buf = torch.empty(2 * L2_BYTES, dtype=torch.uint8, device="cuda") if need_flush else None
+
+    for s in range(args.warmup):
+        step(s)
+    torch.cuda.synchronize()
+
+    # ---- timed region: exactly K steps ----
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
+           torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    if pg:
+        pg.barrier()
+    torch.cuda.synchronize()
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    with ClockSampler(local_rank) as clocks:
+        t_start.record(stream)
+        for s in range(args.steps):
+            if need_flush:
+                flush_buf.add_(1)  # evict the previous step's working set from L2
+            i = s % S
+            ev[s][0].record(stream)
+            pkv.pkv_append(w.k_steps[i], w.v_steps[i], slots[i], w.k_cache, w.v_cache)
+            ev[s][1].record(stream)
+            pkv.pkv_decode(w.q_steps[i], w.k_cache, w.v_cache, w.block_tables, lens[i],
+                           spec.window, w.scale, out=out)
+            ev[s][2].record(stream)
+        t_end.record(stream)
+        torch.cuda.synchronize()
+    if pg:
+        pg.barrier()
+    step_ms = [ev[s][0].elapsed_time(ev[s][2]) for s in range(args.steps)]
+    dec_ms = [ev[s][1].elapsed_time(ev[s][2]) for s in range(args.steps)]
+    loop_ms = t_start.elapsed_time(t_end)
+    # the step time: whole loop / K when nothing else ran in it, else the sum of steps
+    total_ms = sum(step_ms) if need_flush else loop_ms
+    my_bytes = sum(sbytes[s % S]["step"] for s in range(args.steps))
+    my_dec_bytes = sum(sbytes[s % S]["decode"] for s in range(args.steps))
+
+    t = torch.tensor([total_ms, my_bytes, sum(dec_ms), my_dec_bytes], dtype=torch.float64)
+    if pg:
+        tmax = t.clone()
+        pg.all_reduce(tmax, op=pg.ReduceOp.MAX)
+        tsum = t.clone()
+        pg.all_reduce(tsum, op=pg.ReduceOp.SUM)
+        total_ms_all, bytes_all = float(tmax[0]), float(tsum[1])
+    else:
+        total_ms_all, bytes_all = total_ms, my_bytes
+    ms_per_step = total_ms_all / args.steps
+    value = bytes_all / (total_ms_all * 1e-3) / 1e9
+    tokens_per_s = world * spec.num_seqs * args.steps / (total_ms_all * 1e-3)
+
+    peak, peak_kind = hbm_peak()
+    dec_avg_ms = sum(dec_ms) / args.steps
+    achieved = (my_dec_bytes / args.steps) / (dec_avg_ms * 1e-3) / 1e9
+    traffic = recorded_traffic(args.workload)
+
+    # ---- end to end through the public API, host buffers ----
+    e2e = None
+    if not args.no_e2e:
+        e2e = run_e2e(pkv, w, spec, args, sbytes, pg, world)
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        sampler = OracleSampler(w)
+        rate, dt, got = sampler.rate_for(10.0)
+        cpu = {"value": rate / 1e9, "unit": "GB/s", "cores": sampler.threads, "kind": "oracle",
+               "sample": f"{got} random (sequence, query head) pairs of step 0; {dt:.1f} s of "
+                         f"float64 decode on the host cores; K/V bytes of the sample / time"}
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": DTYPE_NAME[spec.dtype], "data": "synthetic",
+            "config": {
+                "workload": args.workload, "num_seqs": spec.num_seqs,
+                "num_q_heads": spec.num_q_heads, "num_kv_heads": spec.num_kv_heads,
+                "head_dim": spec.head_dim, "block_size": spec.block_size,
+                "window": spec.window, "steps_in_workload": S,
+                "mean_context": float(w.lens_steps.float().mean()),
+                "num_blocks": w.num_blocks,
+                "tokens_per_split": plan[0], "num_splits": plan[1],
+                "l2": ("flushed between steps" if need_flush else
+                       f"inputs larger than L2 ({kv_per_step / 1e9:.2f} GB of K/V per step)"),
+                "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+            },
+            "tokens_per_s": tokens_per_s,
+            "pct_of_hbm_peak": 100.0 * value / (world * peak),
+            "roofline": {"bound": "hbm", "kernel": "decode (split-K decode + LSE combine)",
+                         "achieved": achieved, "peak": peak, "unit": "GB/s",
+                         "frac": achieved / peak, "peak_kind": peak_kind,
+                         "traffic": traffic,
+                         "algorithmic_bytes_per_launch": my_dec_bytes / args.steps,
+                         "launch_ms": dec_avg_ms},
+            "gpu_launches": launches_per_step * args.steps,
+            "clocks": clocks.summary(),
+            "e2e": e2e,
+            "cpu_baseline": cpu,
+        }
+        print(json.dumps(line), flush=True)
+    if pg:
+        pg.destroy_process_group()
+    return 0
+
+
+def run_e2e(pkv, w, spec, args, sbytes, pg, world):
+    """Same step through the public API with per-step host<->device copies:
+    q, the new K/V, positions, lengths and block tables in from pinned host
+    memory, the attention output back out, the host waiting for it."""
+    S = w.steps
+    stream = torch.cuda.current_stream()
+    host = []
+    for s in range(S):
+        host.append({k: t.cpu().pin_memory() for k, t in (
+            ("q", w.q_steps[s]), ("k", w.k_steps[s]), ("v", w.v_steps[s]),
+            ("pos", w.pos_steps[s]), ("lens", w.lens_steps[s]), ("bt", w.block_tables))})
+    dev = {k: torch.empty_like(t, device="cuda") for k, t in host[0].items()}
+    out_h = torch.empty(w.q_steps[0].shape, dtype=spec.dtype).pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in host[0].values())
+    d2h = out_h.numel() * out_h.element_size()
+
+    def step(s):
+        h = host[s % S]
+        for k in dev:
+            dev[k].copy_(h[k], non_blocking=True)
+        slots = pkv.pkv_slot_mapping(dev["bt"], dev["pos"], spec.block_size)
+        pkv.pkv_append(dev["k"], dev["v"], slots, w.k_cache, w.v_cache)
+        o = pkv.pkv_decode(dev["q"], w.k_cache, w.v_cache, dev["bt"], dev["lens"], spec.window,
+                           w.scale)
+        out_h.copy_(o, non_blocking=True)
+        stream.synchronize()  # the caller needs the result before its next step
+
+    for s in range(args.warmup):
+        step(s)
+    if pg:
+        pg.barrier()
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for s in range(args.steps):
+        step(s)
+    b.record(stream)
+    torch.cuda.synchronize()
+    ms = a.elapsed_time(b)
+    my_bytes = sum(sbytes[s % S]["step"] for s in range(args.steps))
+    t = torch.tensor([ms, my_bytes], dtype=torch.float64)
+    if pg:
+        tmax, tsum = t.clone(), t.clone()
+        pg.all_reduce(tmax, op=pg.ReduceOp.MAX)
+        pg.all_reduce(tsum, op=pg.ReduceOp.SUM)
+        ms, my_bytes = float(tmax[0]), float(tsum[1])
+    return {"value": my_bytes / (ms * 1e-3) / 1e9, "unit": "GB/s",
+            "tokens_per_s": world * spec.num_seqs * args.steps / (ms * 1e-3),
+            "ms_per_step": ms / args.steps,
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,173 @@
+/*
+ * pkv.h -- C ABI of libpkv: paged KV-cache append and single-query decode
+ * attention on NVIDIA GB300 (sm_103a).
+ *
+ * The method (blog pages on the paged KV cache, cited by title and section):
+ *   "Build a Paged KV Cache in Pure Python"
+ *     Step 1  a block holds the keys and values of block_size consecutive
+ *             token positions, for every head of one layer;
+ *     Step 2  blocks come from a shared, pre-allocated pool;
+ *     Step 3  PagedKVCache.append: the token at position pos goes to row
+ *             pos % block_size of the sequence's (pos // block_size)-th block;
+ *             retrieve: a sequence's tokens are its blocks read in list order;
+ *     Step 4  scaled_dot_product_attention: scores = scale * q.k_t over the
+ *             sequence, max-subtracted softmax, weighted sum of v_t; an empty
+ *             cache gives zeros;
+ *     Step 5  a decode step appends the new token, then attends (the token
+ *             attends to itself).
+ *   "Building a Streaming Sliding-Window Attention Engine in Pure Python"
+ *     Step 3  sliding_window_attention: with window w, attend over positions
+ *             [max(0, T - w), T) of a length-T context.
+ *
+ * Conventions shared by every entry point
+ *   - Pointers named *_cache, q, k, v, out, block_tables, context_lens,
+ *     positions and slot_mapping are DEVICE pointers on the current CUDA
+ *     device; the caller owns them.  Data pointers must be 16-byte aligned.
+ *   - `stream` is a cudaStream_t (NULL = legacy default stream).  Every call
+ *     only enqueues work on it and returns without synchronising, except
+ *     where stated.
+ *   - Return value: PKV_OK or a pkv_status code.  Arguments are checked on
+ *     the host before anything is launched; a failed check launches nothing.
+ *   - The K/V pool is HEAD-MAJOR: [num_blocks][num_kv_heads][block_size]
+ *     [head_dim], row-major.  One (block, kv head) tile is one contiguous run
+ *     of block_size * head_dim elements.  The pages store a block as
+ *     (block_size, num_heads, head_dim); the head-major order is a storage
+ *     choice that does not change what is computed.
+ */
+#ifndef PKV_H_
+#define PKV_H_
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum pkv_dtype {
+  PKV_FLOAT32 = 0,
+  PKV_FLOAT16 = 1,
+  PKV_BFLOAT16 = 2
+} pkv_dtype;
+
+typedef enum pkv_status {
+  PKV_OK = 0,
+  PKV_ERR_NULL = 1,        /* a required pointer is NULL                          */
+  PKV_ERR_SHAPE = 2,       /* a size is negative or sizes are inconsistent         */
+  PKV_ERR_DTYPE = 3,       /* unknown dtype code                                  */
+  PKV_ERR_UNSUPPORTED = 4, /* valid, not implemented (head_dim, block_size, ...)  */
+  PKV_ERR_ALIGNMENT = 5,   /* a data pointer is not 16-byte aligned              */
+  PKV_ERR_CUDA = 6,        /* a CUDA runtime call or a kernel launch failed       */
+  PKV_ERR_NOMEM = 7        /* the split-K workspace could not be allocated        */
+} pkv_status;
+
+/* Shape of one layer's K (or V) pool. */
+typedef struct pkv_cache_layout {
+  int64_t num_blocks;   /* NB: blocks in the pool                                  */
+  int32_t num_kv_heads; /* Hkv                                                     */
+  int32_t block_size;   /* bs: tokens per block; a multiple of 16, at most 256     */
+  int32_t head_dim;     /* D: 64 or 128                                            */
+  int32_t dtype;        /* pkv_dtype of the pool, and of q, k, v and out           */
+} pkv_cache_layout;
+
+/*
+ * pkv_slot_mapping -- slot of each sequence's new token.
+ *   ("Build a Paged KV Cache in Pure Python", Step 3, PagedKVCache.append)
+ *   slot_mapping[b] = block_tables[b][pos / bs] * bs + pos % bs, pos =
+ *   positions[b].  A negative position, a position at or beyond
+ *   max_blocks_per_seq * bs, or a negative block id gives -1 ("no write"
+ *   for pkv_append).
+ *   block_tables  [num_seqs][max_blocks_per_seq] int32, device
+ *   positions     [num_seqs] int64, device
+ *   slot_mapping  [num_seqs] int64, device, written
+ */
+int pkv_slot_mapping(const int32_t* block_tables, int32_t num_seqs, int32_t max_blocks_per_seq,
+                     const int64_t* positions, int32_t block_size, int64_t* slot_mapping,
+                     void* stream);
+
+/*
+ * pkv_append -- write each new token's key and value into its cache slot.
+ *   ("Build a Paged KV Cache in Pure Python", Step 3, PagedKVCache.append:
+ *   keys[offset] = key_vec in the token's physical block)
+ *   k, v          [num_tokens][num_kv_heads][head_dim], layout->dtype
+ *   slot_mapping  [num_tokens] int64: token i goes to block slot / bs, row
+ *                 slot % bs; a negative slot skips the token; a slot at or
+ *                 beyond num_blocks * bs is skipped as well (nothing is written
+ *                 out of bounds).
+ *   k_cache, v_cache  head-major pools described by *layout, updated in place.
+ *   The copy is bit-exact.  Two tokens mapped to the same slot race (the
+ *   result is one of the two rows, unspecified which).
+ */
+int pkv_append(const void* k, const void* v, const int64_t* slot_mapping, int64_t num_tokens,
+               void* k_cache, void* v_cache, const pkv_cache_layout* layout, void* stream);
+
+/*
+ * pkv_decode -- single-query attention of every (sequence, query head) over
+ * its paged context.
+ *   ("Build a Paged KV Cache in Pure Python", Step 4; "Building a Streaming
+ *   Sliding-Window Attention Engine in Pure Python", Step 3)
+ *   For sequence b with L = context_lens[b], lo = max(0, L - window) when
+ *   window > 0, else 0, and query head h reading kv head h / (Hq / Hkv):
+ *     s_t   = scale * sum_d q[b][h][d] * K[b, t][d]      for t in [lo, L)
+ *     out[b][h][:] = sum_t softmax(s)_t * V[b, t][:]     (zeros when L == lo)
+ *   where K[b, t] is row t % bs of kv head h/G in block block_tables[b][t / bs].
+ *   q    [num_seqs][num_q_heads][head_dim], layout->dtype
+ *   block_tables [num_seqs][max_blocks_per_seq] int32; entries past a
+ *                sequence's last block are never read.
+ *   context_lens [num_seqs] int32, the length including the token appended
+ *                this step.
+ *   out  [num_seqs][num_q_heads][head_dim], layout->dtype, written.
+ *   Arithmetic: products and sums in fp32 (tensor-core MMA for fp16/bf16),
+ *   online softmax in fp32, output rounded to nearest-even into the dtype.
+ *   In-kernel errors never trap: a block id outside [0, num_blocks) or a
+ *   context length outside [0, max_blocks_per_seq * bs] makes that
+ *   sequence's output rows NaN.
+ *   Long contexts are split across CTAs (flash-decoding); the partial
+ *   results go to a workspace the library allocates per (device, stream) on
+ *   first use and grows when a larger problem arrives (growth synchronises
+ *   `stream`).  Issue the largest call once before capturing a CUDA graph.
+ *   Calls on one stream share that stream's workspace and are ordered by the
+ *   stream; calls on different streams never share one.
+ */
+int pkv_decode(const void* q, int32_t num_seqs, int32_t num_q_heads,
+               const void* k_cache, const void* v_cache, const pkv_cache_layout* layout,
+               const int32_t* block_tables, int32_t max_blocks_per_seq,
+               const int32_t* context_lens, int32_t window, float scale, void* out,
+               void* stream);
+
+/*
+ * pkv_decode_split -- pkv_decode with an explicit context split.
+ *   tokens_per_split: a positive multiple of 16 (each CTA handles at most that
+ *   many tokens of one sequence), or 0 to let the library choose (exactly
+ *   what pkv_decode does).  The result is the same up to fp32 rounding
+ *   order for every choice.
+ */
+int pkv_decode_split(const void* q, int32_t num_seqs, int32_t num_q_heads,
+                     const void* k_cache, const void* v_cache, const pkv_cache_layout* layout,
+                     const int32_t* block_tables, int32_t max_blocks_per_seq,
+                     const int32_t* context_lens, int32_t window, float scale, void* out,
+                     int32_t tokens_per_split, void* stream);
+
+/*
+ * pkv_decode_plan -- the split pkv_decode_split would use (host only, no GPU
+ * work).  num_sms: streaming multiprocessors to plan for (<= 0: query the
+ * current device).  Writes the tokens per split and the number of splits
+ * the grid provides for the longest possible context.
+ */
+int pkv_decode_plan(int32_t num_seqs, int32_t num_q_heads, const pkv_cache_layout* layout,
+                    int32_t max_blocks_per_seq, int32_t window, int32_t tokens_per_split,
+                    int32_t num_sms, int32_t* tokens_per_split_out, int32_t* num_splits_out);
+
+/* Human-readable name of a pkv_status code (static storage). */
+const char* pkv_status_string(int status);
+
+/*
+ * pkv_release_workspaces -- free every split-K workspace the library holds.
+ * Synchronises the device; call it only when no pkv_decode is in flight.
+ */
+int pkv_release_workspaces(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PKV_H_ */

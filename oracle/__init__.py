@@ -211,6 +211,8 @@ def decode(q, k_cache, v_cache, block_tables, context_lens, window: int, scale: 
     else:
         pairs_arr = _int_array(pairs, np.int32).reshape(-1, 2)
         n = pairs_arr.shape[0]
+        if n == 0:
+            return np.empty((0, D), dtype=np.float64)
     out = np.empty((n, D), dtype=np.float64)
     rc = _load().oracle_decode(_ptr(qr), B, Hq, _ptr(kc), _ptr(vc), nb, hkv, bs, D, qd,
                                _ptr(bt), bt.shape[1] if bt.ndim == 2 else 0, _ptr(lens),

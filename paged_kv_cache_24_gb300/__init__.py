@@ -1,0 +1,25 @@
+"""paged_kv_cache_24_gb300 -- paged KV-cache decode attention for GB300 (sm_103a).
+
+Public API (thin wrappers over the C ABI of ``libpkv.so``, see include/pkv.h):
+
+* ``pkv_slot_mapping(block_tables, positions, block_size)`` -- slot of each
+  sequence's new token;
+* ``pkv_append(k, v, slot_mapping, k_cache, v_cache)`` -- write the new
+  tokens' K/V into their slots;
+* ``pkv_decode(q, k_cache, v_cache, block_tables, context_lens, window, scale,
+  out)`` -- single-query attention over each sequence's paged context,
+  optionally limited to a sliding window.
+
+All tensors live on the GPU; PyTorch provides the memory and the stream.
+``workloads`` builds the seeded synthetic inputs used by the tests and the
+benchmark.
+"""
+from ._binding import (CacheLayout, PkvError, cache_layout, library_path, load_library,
+                       pkv_append, pkv_decode, pkv_decode_plan, pkv_release_workspaces,
+                       pkv_slot_mapping, status_string)
+
+__all__ = [
+    "CacheLayout", "PkvError", "cache_layout", "library_path", "load_library", "pkv_append",
+    "pkv_decode", "pkv_decode_plan", "pkv_release_workspaces", "pkv_slot_mapping",
+    "status_string",
+]

@@ -1,0 +1,195 @@
+"""ctypes binding of libpkv (the C ABI in include/pkv.h).
+
+Argument marshalling only: shapes and dtypes are read off torch tensors,
+pointers are passed through, and every step of the computation runs in the
+library's CUDA kernels.  There is no fallback: if ``_lib/libpkv.so`` is
+missing or a call fails, an exception is raised.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+from . import _build
+
+PKV_OK = 0
+_DTYPES = {torch.float32: 0, torch.float16: 1, torch.bfloat16: 2}
+
+
+class PkvError(RuntimeError):
+    """A libpkv call returned a non-zero pkv_status."""
+
+    def __init__(self, fn: str, status: int, message: str):
+        super().__init__(f"{fn} failed: {message} (status {status})")
+        self.status = status
+
+
+class CacheLayout(ctypes.Structure):
+    """Mirror of ``pkv_cache_layout``."""
+    _fields_ = [("num_blocks", ctypes.c_int64), ("num_kv_heads", ctypes.c_int32),
+                ("block_size", ctypes.c_int32), ("head_dim", ctypes.c_int32),
+                ("dtype", ctypes.c_int32)]
+
+
+_lock = threading.Lock()
+_lib = None
+
+
+def library_path() -> str:
+    return _build.LIB_PATH
+
+
+def load_library():
+    """Load libpkv.so (built by ``paged_kv_cache_24_gb300._build``); raise if absent."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        path = library_path()
+        if not os.path.exists(path):
+            raise RuntimeError(
+                f"libpkv.so not found at {path}; build it with "
+                "`python -m paged_kv_cache_24_gb300._build` (there is no CPU fallback)")
+        lib = ctypes.CDLL(path)
+        vp, i32, i64, f32 = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_float
+        lay = ctypes.POINTER(CacheLayout)
+        sig = {
+            "pkv_slot_mapping": [vp, i32, i32, vp, i32, vp, vp],
+            "pkv_append": [vp, vp, vp, i64, vp, vp, lay, vp],
+            "pkv_decode": [vp, i32, i32, vp, vp, lay, vp, i32, vp, i32, f32, vp, vp],
+            "pkv_decode_split": [vp, i32, i32, vp, vp, lay, vp, i32, vp, i32, f32, vp, i32, vp],
+            "pkv_decode_plan": [i32, i32, lay, i32, i32, i32, i32, ctypes.POINTER(i32),
+                                ctypes.POINTER(i32)],
+            "pkv_release_workspaces": [],
+        }
+        for name, args in sig.items():
+            fn = getattr(lib, name)
+            fn.argtypes = args
+            fn.restype = ctypes.c_int
+        lib.pkv_status_string.argtypes = [ctypes.c_int]
+        lib.pkv_status_string.restype = ctypes.c_char_p
+        _lib = lib
+        return lib
+
+
+def _check(name: str, status: int) -> None:
+    if status != PKV_OK:
+        msg = load_library().pkv_status_string(status).decode()
+        raise PkvError(name, status, msg)
+
+
+def status_string(status: int) -> str:
+    return load_library().pkv_status_string(status).decode()
+
+
+def _ptr(t) -> int:
+    return 0 if t is None else t.data_ptr()
+
+
+def _stream(stream) -> int:
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def cache_layout(cache: torch.Tensor) -> CacheLayout:
+    """Layout of a head-major pool tensor [num_blocks, num_kv_heads, block_size, head_dim]."""
+    if cache.dim() != 4:
+        raise ValueError("cache must be [num_blocks, num_kv_heads, block_size, head_dim]")
+    if cache.dtype not in _DTYPES:
+        raise TypeError(f"unsupported cache dtype {cache.dtype}")
+    if not cache.is_contiguous():
+        raise ValueError("cache must be contiguous")
+    nb, hkv, bs, d = cache.shape
+    return CacheLayout(nb, hkv, bs, d, _DTYPES[cache.dtype])
+
+
+def _require(cond: bool, msg: str) -> None:
+    if not cond:
+        raise ValueError(msg)
+
+
+def _on_cuda(*ts) -> None:
+    for t in ts:
+        if t is not None and t.device.type != "cuda":
+            raise ValueError("libpkv operates on CUDA tensors only")
+
+
+def pkv_slot_mapping(block_tables: torch.Tensor, positions: torch.Tensor, block_size: int,
+                     out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """Slots of each sequence's new token (int64 [B], -1 = no slot)."""
+    _on_cuda(block_tables, positions, out)
+    _require(block_tables.dtype == torch.int32 and block_tables.dim() == 2
+             and block_tables.is_contiguous(), "block_tables must be contiguous int32 [B, MB]")
+    _require(positions.dtype == torch.int64 and positions.is_contiguous()
+             and positions.numel() == block_tables.shape[0], "positions must be int64 [B]")
+    if out is None:
+        out = torch.empty(block_tables.shape[0], dtype=torch.int64, device=block_tables.device)
+    _check("pkv_slot_mapping", load_library().pkv_slot_mapping(
+        _ptr(block_tables), block_tables.shape[0], block_tables.shape[1], _ptr(positions),
+        int(block_size), _ptr(out), _stream(stream)))
+    return out
+
+
+def pkv_append(k: torch.Tensor, v: torch.Tensor, slot_mapping: torch.Tensor,
+               k_cache: torch.Tensor, v_cache: torch.Tensor, stream=None) -> None:
+    """Write k[i], v[i] ([T, Hkv, D]) into cache slot slot_mapping[i] (int64, <0 skips)."""
+    _on_cuda(k, v, slot_mapping, k_cache, v_cache)
+    layout = cache_layout(k_cache)
+    _require(v_cache.shape == k_cache.shape and v_cache.dtype == k_cache.dtype
+             and v_cache.is_contiguous(), "v_cache must match k_cache")
+    T = k.shape[0]
+    shape = (T, layout.num_kv_heads, layout.head_dim)
+    _require(tuple(k.shape) == shape and tuple(v.shape) == shape, f"k and v must be {shape}")
+    _require(k.dtype == k_cache.dtype and v.dtype == k_cache.dtype, "k/v dtype must match cache")
+    _require(k.is_contiguous() and v.is_contiguous(), "k and v must be contiguous")
+    _require(slot_mapping.dtype == torch.int64 and slot_mapping.numel() == T
+             and slot_mapping.is_contiguous(), "slot_mapping must be int64 [T]")
+    _check("pkv_append", load_library().pkv_append(
+        _ptr(k), _ptr(v), _ptr(slot_mapping), T, _ptr(k_cache), _ptr(v_cache),
+        ctypes.byref(layout), _stream(stream)))
+
+
+def pkv_decode(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
+               block_tables: torch.Tensor, context_lens: torch.Tensor, window: int,
+               scale: float, out: torch.Tensor | None = None, tokens_per_split: int = 0,
+               stream=None) -> torch.Tensor:
+    """Decode attention of q [B, Hq, D] over the paged context; returns out [B, Hq, D]."""
+    _on_cuda(q, k_cache, v_cache, block_tables, context_lens, out)
+    layout = cache_layout(k_cache)
+    _require(v_cache.shape == k_cache.shape and v_cache.dtype == k_cache.dtype
+             and v_cache.is_contiguous(), "v_cache must match k_cache")
+    _require(q.dim() == 3 and q.shape[2] == layout.head_dim and q.is_contiguous()
+             and q.dtype == k_cache.dtype, "q must be contiguous [B, Hq, D] of the cache dtype")
+    B, Hq, D = q.shape
+    _require(block_tables.dtype == torch.int32 and block_tables.dim() == 2
+             and block_tables.shape[0] == B and block_tables.is_contiguous(),
+             "block_tables must be contiguous int32 [B, MB]")
+    _require(context_lens.dtype == torch.int32 and context_lens.numel() == B
+             and context_lens.is_contiguous(), "context_lens must be int32 [B]")
+    if out is None:
+        out = torch.empty_like(q)
+    _require(out.shape == q.shape and out.dtype == q.dtype and out.is_contiguous(),
+             "out must be contiguous and shaped like q")
+    _check("pkv_decode", load_library().pkv_decode_split(
+        _ptr(q), B, Hq, _ptr(k_cache), _ptr(v_cache), ctypes.byref(layout),
+        _ptr(block_tables), block_tables.shape[1], _ptr(context_lens), int(window),
+        float(scale), _ptr(out), int(tokens_per_split), _stream(stream)))
+    return out
+
+
+def pkv_decode_plan(num_seqs: int, num_q_heads: int, layout: CacheLayout, max_blocks: int,
+                    window: int, tokens_per_split: int = 0, num_sms: int = 0):
+    """(tokens_per_split, num_splits) the library would use; host only."""
+    tps, ns = ctypes.c_int32(0), ctypes.c_int32(0)
+    _check("pkv_decode_plan", load_library().pkv_decode_plan(
+        num_seqs, num_q_heads, ctypes.byref(layout), max_blocks, window, tokens_per_split,
+        num_sms, ctypes.byref(tps), ctypes.byref(ns)))
+    return tps.value, ns.value
+
+
+def pkv_release_workspaces() -> None:
+    _check("pkv_release_workspaces", load_library().pkv_release_workspaces())

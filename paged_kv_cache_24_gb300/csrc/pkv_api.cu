@@ -1,0 +1,345 @@
+// pkv_api.cu -- the C ABI of libpkv (declared in include/pkv.h): argument
+// checks, split planning, the per-(device, stream) split-K workspace, TMA
+// descriptor encoding and kernel dispatch.
+#include <cudaTypedefs.h>
+
+#include <map>
+#include <mutex>
+#include <utility>
+
+#include "pkv.h"
+#include "pkv_internal.h"
+
+namespace {
+
+using pkv::DecodeParams;
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+bool aligned4(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0; }
+
+int elem_bytes(int dtype) { return dtype == PKV_FLOAT32 ? 4 : 2; }
+
+// Layout checks.  `for_decode` adds the tile constraints of the decode kernels.
+int check_layout(const pkv_cache_layout* L, bool for_decode) {
+  if (!L) return PKV_ERR_NULL;
+  if (L->dtype < PKV_FLOAT32 || L->dtype > PKV_BFLOAT16) return PKV_ERR_DTYPE;
+  if (L->num_blocks < 0 || L->num_kv_heads <= 0 || L->block_size <= 0 || L->head_dim <= 0)
+    return PKV_ERR_SHAPE;
+  if ((L->head_dim * elem_bytes(L->dtype)) % 16 != 0) return PKV_ERR_UNSUPPORTED;
+  if (for_decode) {
+    if (L->head_dim != 64 && L->head_dim != 128) return PKV_ERR_UNSUPPORTED;
+    if (L->block_size % pkv::kUnitTokens != 0 || L->block_size > 256) return PKV_ERR_UNSUPPORTED;
+    // TMA row coordinates are 32-bit
+    if (L->num_blocks * L->num_kv_heads * static_cast<int64_t>(L->block_size) > 0x7fffffffLL)
+      return PKV_ERR_UNSUPPORTED;
+  }
+  return PKV_OK;
+}
+
+int to_status(cudaError_t e) {
+  if (e == cudaSuccess) return PKV_OK;
+  if (e == cudaErrorMemoryAllocation) return PKV_ERR_NOMEM;
+  return PKV_ERR_CUDA;
+}
+
+// ---- split-K workspace, one per (device, stream) ---------------------------
+
+struct Workspace {
+  void* ptr = nullptr;
+  size_t bytes = 0;
+};
+std::mutex g_ws_mutex;
+std::map<std::pair<int, cudaStream_t>, Workspace> g_ws;
+
+int get_workspace(int device, cudaStream_t stream, size_t need, void** out) {
+  std::lock_guard<std::mutex> lock(g_ws_mutex);
+  Workspace& ws = g_ws[{device, stream}];
+  if (ws.bytes < need) {
+    if (ws.ptr) {
+      // earlier calls on this stream may still read the old buffer
+      cudaError_t e = cudaStreamSynchronize(stream);
+      if (e != cudaSuccess) return to_status(e);
+      cudaFree(ws.ptr);
+      ws.ptr = nullptr;
+      ws.bytes = 0;
+    }
+    size_t bytes = need < (size_t(1) << 20) ? (size_t(1) << 20) : need;
+    cudaError_t e = cudaMalloc(&ws.ptr, bytes);
+    if (e != cudaSuccess) {
+      cudaGetLastError();  // clear the sticky-free allocation error
+      ws.ptr = nullptr;
+      return PKV_ERR_NOMEM;
+    }
+    ws.bytes = bytes;
+  }
+  *out = ws.ptr;
+  return PKV_OK;
+}
+
+// ---- TMA descriptors --------------------------------------------------------
+
+PFN_cuTensorMapEncodeTiled_v12000 get_encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault,
+                                         &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      f = nullptr;
+    return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+  }();
+  return fn;
+}
+
+// The pool viewed as a 2-D tensor [NB * Hkv * bs rows][D columns]; one box is
+// 16 rows x 64 columns (128 bytes) with the 128-byte swizzle.
+int encode_pool_map(CUtensorMap* map, const void* pool, const pkv_cache_layout* L) {
+  auto fn = get_encode_fn();
+  if (!fn) return PKV_ERR_CUDA;
+  const cuuint64_t rows = static_cast<cuuint64_t>(L->num_blocks) * L->num_kv_heads * L->block_size;
+  cuuint64_t dims[2] = {static_cast<cuuint64_t>(L->head_dim), rows > 0 ? rows : 1};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(L->head_dim) * 2};
+  cuuint32_t box[2] = {64, static_cast<cuuint32_t>(pkv::kUnitTokens)};
+  cuuint32_t estr[2] = {1, 1};
+  CUtensorMapDataType dt =
+      L->dtype == PKV_FLOAT16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+  CUresult r = fn(map, dt, 2, const_cast<void*>(pool), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? PKV_OK : PKV_ERR_CUDA;
+}
+
+// ---- planning -----------------------------------------------------------------
+
+struct Plan {
+  int head_chunk, num_head_chunks, ntiles;
+  int units_per_split, num_splits;
+};
+
+int sm_count_of_current_device() {
+  int dev = 0, n = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+  return n;
+}
+
+int make_plan(int num_seqs, int num_q_heads, const pkv_cache_layout* L, int max_blocks,
+              int window, int tokens_per_split, int num_sms, Plan* plan) {
+  const int group = num_q_heads / L->num_kv_heads;
+  const int cap = L->dtype == PKV_FLOAT32 ? 8 : 16;  // query heads per CTA
+  plan->head_chunk = group < cap ? group : cap;
+  plan->num_head_chunks = (group + plan->head_chunk - 1) / plan->head_chunk;
+  plan->ntiles = plan->head_chunk <= 8 ? 1 : 2;
+  if (static_cast<int64_t>(L->num_kv_heads) * plan->num_head_chunks > 65535) return PKV_ERR_UNSUPPORTED;
+
+  const int64_t total_units =
+      static_cast<int64_t>(max_blocks) * L->block_size / pkv::kUnitTokens;
+  int64_t max_units = total_units;
+  if (window > 0) {
+    const int64_t wu = (static_cast<int64_t>(window) - 1) / pkv::kUnitTokens + 2;
+    if (wu < max_units) max_units = wu;
+  }
+  // Each warp resolves its units' pages with one lane per unit: at most 32
+  // units per warp, i.e. 2048 tokens per split.
+  const int max_ups = 32 * pkv::kDecodeWarps;
+  int ups;
+  if (tokens_per_split > 0) {
+    if (tokens_per_split % pkv::kUnitTokens != 0) return PKV_ERR_SHAPE;
+    ups = tokens_per_split / pkv::kUnitTokens;
+    if (ups > max_ups) return PKV_ERR_UNSUPPORTED;
+  } else {
+    // 512-token splits by default; shorten them (down to 128 tokens) while
+    // the grid would not give every SM several CTAs.
+    if (num_sms <= 0) num_sms = 148;
+    const int64_t pairs = static_cast<int64_t>(num_seqs) * L->num_kv_heads * plan->num_head_chunks;
+    const int64_t target = static_cast<int64_t>(num_sms) * 8;
+    ups = 32;
+    while (ups > 8 && pairs * ((max_units + ups - 1) / ups) < target) ups /= 2;
+  }
+  int64_t ns = (max_units + ups - 1) / ups;
+  if (ns < 1) ns = 1;
+  if (ns > 0x7fffffffLL) return PKV_ERR_UNSUPPORTED;
+  plan->units_per_split = ups;
+  plan->num_splits = static_cast<int>(ns);
+  return PKV_OK;
+}
+
+int check_decode_args(const void* q, int32_t num_seqs, int32_t num_q_heads, const void* k_cache,
+                      const void* v_cache, const pkv_cache_layout* layout,
+                      const int32_t* block_tables, int32_t max_blocks,
+                      const int32_t* context_lens, const void* out) {
+  int rc = check_layout(layout, true);
+  if (rc != PKV_OK) return rc;
+  if (num_seqs < 0 || num_q_heads <= 0 || max_blocks < 0) return PKV_ERR_SHAPE;
+  if (num_q_heads % layout->num_kv_heads != 0) return PKV_ERR_SHAPE;
+  if (num_seqs > 65535) return PKV_ERR_UNSUPPORTED;
+  if (static_cast<int64_t>(max_blocks) * layout->block_size > 0x7fffffffLL) return PKV_ERR_UNSUPPORTED;
+  if (num_seqs == 0) return PKV_OK;
+  if (!q || !k_cache || !v_cache || !block_tables || !context_lens || !out) return PKV_ERR_NULL;
+  if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(out) ||
+      !aligned4(block_tables) || !aligned4(context_lens))
+    return PKV_ERR_ALIGNMENT;
+  return PKV_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* pkv_status_string(int status) {
+  switch (status) {
+    case PKV_OK: return "PKV_OK";
+    case PKV_ERR_NULL: return "PKV_ERR_NULL: a required pointer is NULL";
+    case PKV_ERR_SHAPE: return "PKV_ERR_SHAPE: negative or inconsistent sizes";
+    case PKV_ERR_DTYPE: return "PKV_ERR_DTYPE: unknown dtype code";
+    case PKV_ERR_UNSUPPORTED: return "PKV_ERR_UNSUPPORTED: shape or size not supported";
+    case PKV_ERR_ALIGNMENT: return "PKV_ERR_ALIGNMENT: data pointer not 16-byte aligned";
+    case PKV_ERR_CUDA: return "PKV_ERR_CUDA: a CUDA call or kernel launch failed";
+    case PKV_ERR_NOMEM: return "PKV_ERR_NOMEM: workspace allocation failed";
+    default: return "unknown pkv status";
+  }
+}
+
+int pkv_slot_mapping(const int32_t* block_tables, int32_t num_seqs, int32_t max_blocks_per_seq,
+                     const int64_t* positions, int32_t block_size, int64_t* slot_mapping,
+                     void* stream) {
+  if (num_seqs < 0 || max_blocks_per_seq < 0 || block_size <= 0) return PKV_ERR_SHAPE;
+  if (num_seqs == 0) return PKV_OK;
+  if (!block_tables || !positions || !slot_mapping) return PKV_ERR_NULL;
+  if (!aligned4(block_tables) || (reinterpret_cast<uintptr_t>(positions) & 7u) ||
+      (reinterpret_cast<uintptr_t>(slot_mapping) & 7u))
+    return PKV_ERR_ALIGNMENT;
+  return to_status(pkv::launch_slot_mapping(block_tables, num_seqs, max_blocks_per_seq, positions,
+                                            block_size, slot_mapping,
+                                            static_cast<cudaStream_t>(stream)));
+}
+
+int pkv_append(const void* k, const void* v, const int64_t* slot_mapping, int64_t num_tokens,
+               void* k_cache, void* v_cache, const pkv_cache_layout* layout, void* stream) {
+  int rc = check_layout(layout, false);
+  if (rc != PKV_OK) return rc;
+  if (num_tokens < 0) return PKV_ERR_SHAPE;
+  if (num_tokens == 0) return PKV_OK;
+  if (!k || !v || !slot_mapping || !k_cache || !v_cache) return PKV_ERR_NULL;
+  if (!aligned16(k) || !aligned16(v) || !aligned16(k_cache) || !aligned16(v_cache) ||
+      (reinterpret_cast<uintptr_t>(slot_mapping) & 7u))
+    return PKV_ERR_ALIGNMENT;
+  return to_status(pkv::launch_append(elem_bytes(layout->dtype), k, v, slot_mapping, num_tokens,
+                                      k_cache, v_cache, layout->num_blocks, layout->num_kv_heads,
+                                      layout->block_size, layout->head_dim,
+                                      static_cast<cudaStream_t>(stream)));
+}
+
+int pkv_decode_plan(int32_t num_seqs, int32_t num_q_heads, const pkv_cache_layout* layout,
+                    int32_t max_blocks_per_seq, int32_t window, int32_t tokens_per_split,
+                    int32_t num_sms, int32_t* tokens_per_split_out, int32_t* num_splits_out) {
+  int rc = check_layout(layout, true);
+  if (rc != PKV_OK) return rc;
+  if (num_seqs < 0 || num_q_heads <= 0 || max_blocks_per_seq < 0 ||
+      num_q_heads % layout->num_kv_heads != 0)
+    return PKV_ERR_SHAPE;
+  Plan plan;
+  rc = make_plan(num_seqs, num_q_heads, layout, max_blocks_per_seq, window, tokens_per_split,
+                 num_sms > 0 ? num_sms : sm_count_of_current_device(), &plan);
+  if (rc != PKV_OK) return rc;
+  if (tokens_per_split_out) *tokens_per_split_out = plan.units_per_split * pkv::kUnitTokens;
+  if (num_splits_out) *num_splits_out = plan.num_splits;
+  return PKV_OK;
+}
+
+int pkv_decode_split(const void* q, int32_t num_seqs, int32_t num_q_heads,
+                     const void* k_cache, const void* v_cache, const pkv_cache_layout* layout,
+                     const int32_t* block_tables, int32_t max_blocks_per_seq,
+                     const int32_t* context_lens, int32_t window, float scale, void* out,
+                     int32_t tokens_per_split, void* stream) {
+  int rc = check_decode_args(q, num_seqs, num_q_heads, k_cache, v_cache, layout, block_tables,
+                             max_blocks_per_seq, context_lens, out);
+  if (rc != PKV_OK) return rc;
+  if (tokens_per_split < 0 || tokens_per_split % pkv::kUnitTokens != 0) return PKV_ERR_SHAPE;
+  if (tokens_per_split > 32 * pkv::kDecodeWarps * pkv::kUnitTokens) return PKV_ERR_UNSUPPORTED;
+  if (num_seqs == 0) return PKV_OK;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+
+  int device = 0;
+  if (cudaGetDevice(&device) != cudaSuccess) return PKV_ERR_CUDA;
+  Plan plan;
+  rc = make_plan(num_seqs, num_q_heads, layout, max_blocks_per_seq, window, tokens_per_split,
+                 sm_count_of_current_device(), &plan);
+  if (rc != PKV_OK) return rc;
+
+  DecodeParams p{};
+  p.q = q;
+  p.out = out;
+  p.k_cache = k_cache;
+  p.v_cache = v_cache;
+  p.block_tables = block_tables;
+  p.context_lens = context_lens;
+  p.num_blocks = layout->num_blocks;
+  p.num_seqs = num_seqs;
+  p.num_q_heads = num_q_heads;
+  p.num_kv_heads = layout->num_kv_heads;
+  p.group = num_q_heads / layout->num_kv_heads;
+  p.head_chunk = plan.head_chunk;
+  p.num_head_chunks = plan.num_head_chunks;
+  p.max_blocks = max_blocks_per_seq;
+  p.block_size = layout->block_size;
+  p.window = window;
+  p.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
+  p.units_per_split = plan.units_per_split;
+  p.num_splits = plan.num_splits;
+
+  if (plan.num_splits > 1) {
+    const size_t rows = static_cast<size_t>(num_seqs) * num_q_heads * plan.num_splits;
+    const size_t o_bytes = rows * layout->head_dim * sizeof(float);
+    void* ws = nullptr;
+    rc = get_workspace(device, st, o_bytes + rows * sizeof(float2), &ws);
+    if (rc != PKV_OK) return rc;
+    p.part_o = static_cast<float*>(ws);
+    p.part_ml = reinterpret_cast<float2*>(static_cast<char*>(ws) + o_bytes);
+  }
+
+  cudaError_t e;
+  if (layout->dtype == PKV_FLOAT32) {
+    e = pkv::launch_decode_f32(layout->head_dim, p, st);
+  } else {
+    CUtensorMap kmap, vmap;
+    rc = encode_pool_map(&kmap, k_cache, layout);
+    if (rc != PKV_OK) return rc;
+    rc = encode_pool_map(&vmap, v_cache, layout);
+    if (rc != PKV_OK) return rc;
+    e = pkv::launch_decode_16bit(layout->dtype, layout->head_dim, plan.ntiles, kmap, vmap, p, st);
+  }
+  if (e != cudaSuccess) return to_status(e);
+  if (plan.num_splits > 1) {
+    e = pkv::launch_combine(layout->dtype, layout->head_dim, p, st);
+    if (e != cudaSuccess) return to_status(e);
+  }
+  return PKV_OK;
+}
+
+int pkv_decode(const void* q, int32_t num_seqs, int32_t num_q_heads, const void* k_cache,
+               const void* v_cache, const pkv_cache_layout* layout, const int32_t* block_tables,
+               int32_t max_blocks_per_seq, const int32_t* context_lens, int32_t window,
+               float scale, void* out, void* stream) {
+  return pkv_decode_split(q, num_seqs, num_q_heads, k_cache, v_cache, layout, block_tables,
+                          max_blocks_per_seq, context_lens, window, scale, out, 0, stream);
+}
+
+int pkv_release_workspaces(void) {
+  std::lock_guard<std::mutex> lock(g_ws_mutex);
+  int rc = PKV_OK;
+  if (!g_ws.empty() && cudaDeviceSynchronize() != cudaSuccess) rc = PKV_ERR_CUDA;
+  for (auto& kv : g_ws) {
+    if (kv.second.ptr) {
+      int prev = 0;
+      cudaGetDevice(&prev);
+      cudaSetDevice(kv.first.first);
+      cudaFree(kv.second.ptr);
+      cudaSetDevice(prev);
+    }
+  }
+  g_ws.clear();
+  return rc;
+}
+
+}  // extern "C"

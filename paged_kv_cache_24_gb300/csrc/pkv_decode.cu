@@ -1,0 +1,650 @@
+// pkv_decode.cu -- single-query decode attention over a paged K/V pool.
+//
+// What is computed ("Build a Paged KV Cache in Pure Python", Step 4,
+// scaled_dot_product_attention; "Building a Streaming Sliding-Window
+// Attention Engine in Pure Python", Step 3, sliding_window_attention): for
+// each sequence b and query head h (kv head h / G),
+//     out = sum_t softmax_t(scale * q . K_t) V_t,   t in [lo, L),
+// with K_t, V_t found through the block table (Step 3, retrieve).
+//
+// How (GB300 design):
+//  * Work item = (sequence, kv head, head chunk, context split).  One CTA of
+//    four warps per item; the split covers a fixed number of 16-token units
+//    so every CTA streams the same number of bytes (flash-decoding split-K).
+//  * Each warp owns a ring of shared-memory stages.  Lane 0 reads the block
+//    table and issues TMA tile loads (cp.async.bulk.tensor, 128-byte swizzle)
+//    of the unit's K and V rows straight from the page; completion arrives on
+//    the stage's mbarrier.  Nothing is gathered through registers.
+//  * 16-bit pools: S^T = K Q^T and O^T += V^T P^T on the tensor cores
+//    (mma.m16n8k16, fp32 accumulate): 16 context tokens form the M side, the
+//    G query heads of the group (padded to 8) the N side, so one page read
+//    serves the whole GQA group.  P is carried as a hi + lo pair of 16-bit
+//    values, so the weights keep ~fp32 precision.  The softmax is online in
+//    fp32 (log2 domain), with lazy rescaling of the accumulator.
+//  * fp32 pools: the same split structure on CUDA cores (float4 loads,
+//    shuffle reductions).
+//  * Every CTA ends with a cross-warp merge; a sequence with one split writes
+//    its output directly, otherwise the unnormalised partial (m, l, o) goes to
+//    the workspace and the combine kernel applies the log-sum-exp merge.
+#include <math.h>
+
+#include "pkv_device.cuh"
+#include "pkv_internal.h"
+
+namespace pkv {
+namespace {
+
+constexpr int kThreads = kDecodeWarps * 32;
+constexpr int kBoxBytes = kUnitTokens * 128;  // one TMA box: 16 rows x 128 bytes
+constexpr float kRescaleThreshold = 8.0f;     // log2 units: weights stay <= 2^8
+
+template <int D>
+struct Tile16 {
+  static constexpr int kBoxes = D / 64;                     // 64 16-bit columns per box
+  static constexpr int kTileBytes = kBoxes * kBoxBytes;     // K (or V) rows of one unit
+  static constexpr int kUnitBytes = 2 * kTileBytes;         // K + V
+  static constexpr int kStages = D == 128 ? kStagesD128 : kStagesD64;
+  static constexpr int kRingBytes = kStages * kUnitBytes;   // per warp
+  static constexpr int kSmemBytes = kDecodeWarps * kRingBytes + 1024;  // + alignment slack
+};
+
+// Byte offset of 16-byte chunk `chunk` (0 .. D/8-1) of tile row `row` in a
+// TMA tile written with CU_TENSOR_MAP_SWIZZLE_128B: the chunk index inside a
+// 128-byte row is XORed with (row mod 8).
+__device__ __forceinline__ uint32_t swz(int row, int chunk) {
+  return static_cast<uint32_t>((chunk >> 3) * kBoxBytes + row * 128 +
+                               (((chunk & 7) ^ (row & 7)) << 4));
+}
+
+// Per-CTA bookkeeping shared by both decode kernels.
+struct WorkItem {
+  int b, hkv, h0, nh, split;
+  int L, lo, nsplit;
+  int u0, u1;  // units of this CTA
+  bool len_ok, empty;
+};
+
+__device__ __forceinline__ WorkItem make_work_item(const DecodeParams& p) {
+  WorkItem w;
+  w.split = blockIdx.x;
+  w.hkv = blockIdx.y / p.num_head_chunks;
+  const int chunk = blockIdx.y - w.hkv * p.num_head_chunks;
+  w.b = blockIdx.z;
+  w.h0 = w.hkv * p.group + chunk * p.head_chunk;
+  w.nh = min(p.head_chunk, p.group - chunk * p.head_chunk);
+  w.L = p.context_lens[w.b];
+  w.len_ok = w.L >= 0 && static_cast<int64_t>(w.L) <= static_cast<int64_t>(p.max_blocks) * p.block_size;
+  int first, end;
+  unit_range(w.len_ok ? w.L : 0, p.window, &first, &end);
+  w.lo = window_start(w.len_ok ? w.L : 0, p.window);
+  w.empty = end == first;
+  w.nsplit = (!w.len_ok || w.empty) ? 1 : splits_for(end - first, p.units_per_split);
+  w.u0 = first + w.split * p.units_per_split;
+  w.u1 = min(w.u0 + p.units_per_split, end);
+  return w;
+}
+
+// Rows of an invalid (NaN) or empty (zero) context, written by split 0.
+template <typename T, int D>
+__device__ void write_trivial_rows(const DecodeParams& p, const WorkItem& w) {
+  const float val = w.len_ok ? 0.0f : __int_as_float(0x7fc00000);
+  T* out = static_cast<T*>(p.out);
+  for (int i = threadIdx.x; i < w.nh * D; i += blockDim.x) {
+    const int qi = i / D, d = i - qi * D;
+    out[(static_cast<int64_t>(w.b) * p.num_q_heads + w.h0 + qi) * D + d] = from_f32<T>(val);
+  }
+}
+
+// Merge the per-warp softmax states held in shared memory and store either
+// the final rows (single split) or this split's unnormalised partial.
+//   so[w][q][DP] partial O, sm[w][q] running max (log2 units), sl[w][q] sum.
+template <typename T, int D, int QT, int DP>
+__device__ void merge_and_store(const float* so, const float* sm, const float* sl,
+                                const DecodeParams& p, const WorkItem& w, bool bad) {
+  const float nanf_ = __int_as_float(0x7fc00000);
+  for (int i = threadIdx.x; i < w.nh * D; i += blockDim.x) {
+    const int qi = i / D, d = i - qi * D;
+    float M = -INFINITY;
+#pragma unroll
+    for (int k = 0; k < kDecodeWarps; ++k) M = fmaxf(M, sm[k * QT + qi]);
+    float acc = 0.f, lsum = 0.f;
+#pragma unroll
+    for (int k = 0; k < kDecodeWarps; ++k) {
+      const float mk = sm[k * QT + qi];
+      const float f = (mk == -INFINITY) ? 0.f : ex2(mk - M);
+      acc = fmaf(f, so[(k * QT + qi) * DP + d], acc);
+      lsum = fmaf(f, sl[k * QT + qi], lsum);
+    }
+    const int64_t row = static_cast<int64_t>(w.b) * p.num_q_heads + (w.h0 + qi);
+    if (w.nsplit == 1) {
+      static_cast<T*>(p.out)[row * D + d] = from_f32<T>(bad ? nanf_ : acc / lsum);
+    } else {
+      const int64_t slot = row * p.num_splits + w.split;
+      p.part_o[slot * D + d] = bad ? nanf_ : acc;
+      if (d == 0) p.part_ml[slot] = make_float2(M, lsum);
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------
+// 16-bit pools: TMA-staged pages, tensor-core QK^T and PV.
+
+template <typename T, int D, int NT>
+__global__ void __launch_bounds__(kThreads, 2)
+decode16_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
+                const DecodeParams p) {
+  using Cfg = Tile16<D>;
+  constexpr int QT = 8 * NT;        // query columns per CTA (padded group)
+  constexpr int KS = D / 16;        // k-steps of QK^T == m-tiles of PV
+  constexpr int DP = D + 4;         // padded row stride of the merge buffer
+  constexpr int S = Cfg::kStages;
+  static_assert(kDecodeWarps * QT * (DP + 2) * 4 <= kDecodeWarps * Cfg::kRingBytes,
+                "merge buffer must fit in the staging ring");
+
+  extern __shared__ uint8_t smem_raw[];
+  __shared__ __align__(8) uint64_t bars[kDecodeWarps][S];
+  __shared__ int s_bad;
+
+  const int lane = threadIdx.x & 31;
+  const int warp = threadIdx.x >> 5;
+  const WorkItem w = make_work_item(p);
+  if (!w.len_ok || w.empty) {
+    if (w.split == 0) write_trivial_rows<T, D>(p, w);
+    return;
+  }
+  if (w.split >= w.nsplit) return;
+
+  const uint32_t raw_addr = smem_u32(smem_raw);
+  const uint32_t base_addr = (raw_addr + 1023u) & ~1023u;  // 128B-swizzle tiles need 1 KB alignment
+  uint8_t* base = smem_raw + (base_addr - raw_addr);
+  const uint32_t ring = base_addr + warp * Cfg::kRingBytes;
+
+  if (threadIdx.x == 0) s_bad = 0;
+  if (lane == 0) {
+    if (warp == 0) {
+      tma_prefetch_desc(&kmap);
+      tma_prefetch_desc(&vmap);
+    }
+#pragma unroll
+    for (int s = 0; s < S; ++s) mbar_init(smem_u32(&bars[warp][s]), 1);
+    fence_mbar_init();
+  }
+  __syncthreads();
+
+  // Units of this warp: u = u0 + warp + j * kDecodeWarps.  Lane j resolves
+  // unit j's page through the block table once, up front.
+  const int span = w.u1 - w.u0;
+  const int my_n = span > warp ? (span - warp + kDecodeWarps - 1) / kDecodeWarps : 0;
+  int my_y = -1;  // TMA row coordinate of the unit's first token, -1 = bad block id
+  if (lane < my_n) {
+    const int t0 = (w.u0 + warp + lane * kDecodeWarps) * kUnitTokens;
+    const int32_t pb = __ldg(p.block_tables + static_cast<int64_t>(w.b) * p.max_blocks +
+                             t0 / p.block_size);
+    if (pb >= 0 && pb < p.num_blocks)
+      my_y = (pb * p.num_kv_heads + w.hkv) * p.block_size + (t0 % p.block_size);
+  }
+
+  auto issue = [&](int stage, int y) {
+    const uint32_t bar = smem_u32(&bars[warp][stage]);
+    const uint32_t kdst = ring + stage * Cfg::kUnitBytes;
+    const uint32_t vdst = kdst + Cfg::kTileBytes;
+    if (y >= 0) {
+      mbar_arrive_expect_tx(bar, Cfg::kUnitBytes);
+#pragma unroll
+      for (int bx = 0; bx < Cfg::kBoxes; ++bx) {
+        tma_load_2d(kdst + bx * kBoxBytes, &kmap, bx * 64, y, bar);
+        tma_load_2d(vdst + bx * kBoxBytes, &vmap, bx * 64, y, bar);
+      }
+    } else {
+      mbar_arrive(bar);  // nothing to fetch: complete the phase, the unit is flagged bad
+    }
+  };
+
+#pragma unroll
+  for (int j = 0; j < S; ++j) {
+    const int y = __shfl_sync(0xffffffffu, my_y, j);
+    if (lane == 0 && j < my_n) issue(j, y);
+  }
+
+  // Q fragments: B operand of S^T = K Q^T.  Lane holds q[n = lane/4] at
+  // d = 16 kk + 2 (lane % 4) + {0, 1} (register 0) and + 8 (register 1).
+  uint32_t qf[NT][KS][2];
+  const int g = lane >> 2, tig = lane & 3;
+#pragma unroll
+  for (int nt = 0; nt < NT; ++nt) {
+    const int qi = nt * 8 + g;
+    const uint32_t* qrow = reinterpret_cast<const uint32_t*>(
+        static_cast<const T*>(p.q) + (static_cast<int64_t>(w.b) * p.num_q_heads + w.h0 + qi) * D);
+#pragma unroll
+    for (int kk = 0; kk < KS; ++kk) {
+      qf[nt][kk][0] = qi < w.nh ? __ldg(qrow + kk * 8 + tig) : 0u;
+      qf[nt][kk][1] = qi < w.nh ? __ldg(qrow + kk * 8 + 4 + tig) : 0u;
+    }
+  }
+
+  float o[KS][NT][4];
+  float m_run[NT][2], l_run[NT][2];
+#pragma unroll
+  for (int nt = 0; nt < NT; ++nt) {
+#pragma unroll
+    for (int jj = 0; jj < 2; ++jj) {
+      m_run[nt][jj] = -INFINITY;
+      l_run[nt][jj] = 0.f;
+    }
+#pragma unroll
+    for (int mt = 0; mt < KS; ++mt)
+#pragma unroll
+      for (int r = 0; r < 4; ++r) o[mt][nt][r] = 0.f;
+  }
+  bool bad = false;
+
+  for (int j = 0; j < my_n; ++j) {
+    const int stage = j % S;
+    const uint32_t parity = (j / S) & 1;
+    const int yj = __shfl_sync(0xffffffffu, my_y, j);
+    const bool ok = mbar_wait_bounded(smem_u32(&bars[warp][stage]), parity, kWaitLimit);
+    if (!__all_sync(0xffffffffu, ok)) {
+      bad = true;  // the copy never landed; stop using this ring
+      break;
+    }
+    if (yj < 0) bad = true;
+
+    const uint32_t kt = ring + stage * Cfg::kUnitBytes;
+    const uint32_t vt = kt + Cfg::kTileBytes;
+    const int t0 = (w.u0 + warp + j * kDecodeWarps) * kUnitTokens;
+
+    // ---- S^T[16 tok x 8 NT q] = K[16 x D] . Q^T[D x 8 NT] ----
+    float s[NT][4];
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+      for (int r = 0; r < 4; ++r) s[nt][r] = 0.f;
+#pragma unroll
+    for (int kk = 0; kk < KS; ++kk) {
+      uint32_t a0, a1, a2, a3;
+      ldmatrix_x4(kt + swz(lane & 15, kk * 2 + (lane >> 4)), a0, a1, a2, a3);
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt) Mma<T>::run(s[nt], a0, a1, a2, a3, qf[nt][kk][0], qf[nt][kk][1]);
+    }
+
+    // ---- scale into log2 units; mask tokens outside [lo, L) ----
+    const bool edge = (t0 < w.lo) || (t0 + kUnitTokens > w.L);
+    const int ta = t0 + g, tb = ta + 8;  // tokens of rows g and g + 8
+    const bool va = !edge || (ta >= w.lo && ta < w.L);
+    const bool vb = !edge || (tb >= w.lo && tb < w.L);
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+      s[nt][0] = va ? s[nt][0] * p.scale_log2 : -INFINITY;
+      s[nt][1] = va ? s[nt][1] * p.scale_log2 : -INFINITY;
+      s[nt][2] = vb ? s[nt][2] * p.scale_log2 : -INFINITY;
+      s[nt][3] = vb ? s[nt][3] * p.scale_log2 : -INFINITY;
+    }
+
+    // ---- column (query) maxima over the 16 tokens ----
+    float mx[NT][2];
+    bool need = false;
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+      for (int jj = 0; jj < 2; ++jj) {
+        float v = fmaxf(s[nt][jj], s[nt][2 + jj]);
+        v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 4));
+        v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 8));
+        v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 16));
+        mx[nt][jj] = v;
+        need |= v > m_run[nt][jj] + kRescaleThreshold;
+      }
+    // Lazy online softmax: move the reference max only when the new tile
+    // exceeds it by more than the threshold (exact: every weight and the
+    // accumulator share the reference).
+    if (__any_sync(0xffffffffu, need)) {
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+        for (int jj = 0; jj < 2; ++jj) {
+          const float mnew = mx[nt][jj] > m_run[nt][jj] + kRescaleThreshold ? mx[nt][jj] : m_run[nt][jj];
+          const float alpha = ex2(m_run[nt][jj] - mnew);
+          m_run[nt][jj] = mnew;
+          l_run[nt][jj] *= alpha;
+#pragma unroll
+          for (int mt = 0; mt < KS; ++mt) {
+            o[mt][nt][jj] *= alpha;
+            o[mt][nt][2 + jj] *= alpha;
+          }
+        }
+    }
+
+    // ---- weights P = 2^(s - m), split into hi + lo 16-bit parts, transposed ----
+    uint32_t bh[NT][2], bl[NT][2];
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+      const float p0 = ex2(s[nt][0] - m_run[nt][0]);
+      const float p1 = ex2(s[nt][1] - m_run[nt][1]);
+      const float p2 = ex2(s[nt][2] - m_run[nt][0]);
+      const float p3 = ex2(s[nt][3] - m_run[nt][1]);
+      l_run[nt][0] += p0 + p2;
+      l_run[nt][1] += p1 + p3;
+      const uint32_t htop = Mma<T>::pack(p0, p1), hbot = Mma<T>::pack(p2, p3);
+      const uint32_t ltop = Mma<T>::pack(p0 - Mma<T>::lo_f32(htop), p1 - Mma<T>::hi_f32(htop));
+      const uint32_t lbot = Mma<T>::pack(p2 - Mma<T>::lo_f32(hbot), p3 - Mma<T>::hi_f32(hbot));
+      bh[nt][0] = movmatrix_trans(htop);
+      bh[nt][1] = movmatrix_trans(hbot);
+      bl[nt][0] = movmatrix_trans(ltop);
+      bl[nt][1] = movmatrix_trans(lbot);
+    }
+
+    // ---- O^T[D x 8 NT] += V^T[D x 16] . P^T[16 x 8 NT] ----
+    // Rows of V outside [lo, L) may hold anything (even NaN): zero them in
+    // the fragment so that 0 * garbage cannot leak into the sum.
+    uint32_t mlo = 0xffffffffu, mhi = 0xffffffffu;
+    if (edge) {
+      const int tk = t0 + 2 * tig;
+      mlo = ((tk >= w.lo && tk < w.L) ? 0x0000ffffu : 0u) |
+            ((tk + 1 >= w.lo && tk + 1 < w.L) ? 0xffff0000u : 0u);
+      mhi = ((tk + 8 >= w.lo && tk + 8 < w.L) ? 0x0000ffffu : 0u) |
+            ((tk + 9 >= w.lo && tk + 9 < w.L) ? 0xffff0000u : 0u);
+    }
+#pragma unroll
+    for (int mt = 0; mt < KS; ++mt) {
+      uint32_t a0, a1, a2, a3;
+      const int tok = (lane & 7) + ((lane >> 4) << 3);
+      ldmatrix_x4_trans(vt + swz(tok, mt * 2 + ((lane >> 3) & 1)), a0, a1, a2, a3);
+      a0 &= mlo;
+      a1 &= mlo;
+      a2 &= mhi;
+      a3 &= mhi;
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt) {
+        Mma<T>::run(o[mt][nt], a0, a1, a2, a3, bh[nt][0], bh[nt][1]);
+        Mma<T>::run(o[mt][nt], a0, a1, a2, a3, bl[nt][0], bl[nt][1]);
+      }
+    }
+
+    // ---- recycle the stage ----
+    __syncwarp();
+    if (j + S < my_n) {
+      const int yn = __shfl_sync(0xffffffffu, my_y, j + S);
+      if (lane == 0) {
+        fence_proxy_async_smem();
+        issue(stage, yn);
+      }
+    }
+  }
+
+  // ---- per-warp state -> shared memory -> CTA merge ----
+#pragma unroll
+  for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+    for (int jj = 0; jj < 2; ++jj) {
+      float v = l_run[nt][jj];
+      v += __shfl_xor_sync(0xffffffffu, v, 4);
+      v += __shfl_xor_sync(0xffffffffu, v, 8);
+      v += __shfl_xor_sync(0xffffffffu, v, 16);
+      l_run[nt][jj] = v;
+    }
+  if (bad) s_bad = 1;
+  __syncthreads();  // every warp is done with its ring; reuse it for the merge
+
+  float* so = reinterpret_cast<float*>(base);
+  float* sm = so + kDecodeWarps * QT * DP;
+  float* sl = sm + kDecodeWarps * QT;
+#pragma unroll
+  for (int mt = 0; mt < KS; ++mt)
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+      for (int r = 0; r < 4; ++r) {
+        const int d = mt * 16 + g + ((r >> 1) << 3);
+        const int q = nt * 8 + 2 * tig + (r & 1);
+        so[(warp * QT + q) * DP + d] = o[mt][nt][r];
+      }
+  if (g == 0) {
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+      for (int jj = 0; jj < 2; ++jj) {
+        sm[warp * QT + nt * 8 + 2 * tig + jj] = m_run[nt][jj];
+        sl[warp * QT + nt * 8 + 2 * tig + jj] = l_run[nt][jj];
+      }
+  }
+  __syncthreads();
+  merge_and_store<T, D, QT, DP>(so, sm, sl, p, w, s_bad != 0);
+}
+
+// ---------------------------------------------------------------------------
+// fp32 pools: CUDA-core path with the same work split.
+
+template <int D>
+__global__ void __launch_bounds__(kThreads)
+decode_f32_kernel(const DecodeParams p) {
+  constexpr int QT = 8;          // query heads per CTA
+  constexpr int LPR = D / 4;     // lanes per context row (one float4 each)
+  constexpr int RPW = 32 / LPR;  // rows per warp step
+  constexpr int DP = D + 4;
+  __shared__ float so[kDecodeWarps * QT * DP];
+  __shared__ float sm[kDecodeWarps * QT];
+  __shared__ float sl[kDecodeWarps * QT];
+  __shared__ int s_bad;
+
+  const int lane = threadIdx.x & 31;
+  const int warp = threadIdx.x >> 5;
+  const WorkItem w = make_work_item(p);
+  if (!w.len_ok || w.empty) {
+    if (w.split == 0) write_trivial_rows<float, D>(p, w);
+    return;
+  }
+  if (w.split >= w.nsplit) return;
+  if (threadIdx.x == 0) s_bad = 0;
+  __syncthreads();
+
+  const int sub = lane / LPR;  // which row of the warp step
+  const int li = lane % LPR;   // float4 column
+  float4 qv[QT];
+#pragma unroll
+  for (int qi = 0; qi < QT; ++qi) {
+    qv[qi] = qi < w.nh
+                 ? __ldg(reinterpret_cast<const float4*>(
+                             static_cast<const float*>(p.q) +
+                             (static_cast<int64_t>(w.b) * p.num_q_heads + w.h0 + qi) * D) + li)
+                 : make_float4(0.f, 0.f, 0.f, 0.f);
+  }
+  float m[QT], l[QT];
+  float4 acc[QT];
+#pragma unroll
+  for (int qi = 0; qi < QT; ++qi) {
+    m[qi] = -INFINITY;
+    l[qi] = 0.f;
+    acc[qi] = make_float4(0.f, 0.f, 0.f, 0.f);
+  }
+  bool bad = false;
+  const float* kc = static_cast<const float*>(p.k_cache);
+  const float* vc = static_cast<const float*>(p.v_cache);
+
+  for (int u = w.u0 + warp; u < w.u1; u += kDecodeWarps) {
+    const int t0 = u * kUnitTokens;
+    const int32_t pb = __ldg(p.block_tables + static_cast<int64_t>(w.b) * p.max_blocks +
+                             t0 / p.block_size);
+    if (pb < 0 || pb >= p.num_blocks) {
+      bad = true;
+      continue;
+    }
+    const int64_t tile = ((static_cast<int64_t>(pb) * p.num_kv_heads + w.hkv) * p.block_size +
+                          (t0 % p.block_size)) * D;
+    for (int r = sub; r < kUnitTokens; r += RPW) {
+      const int t = t0 + r;
+      const bool valid = t >= w.lo && t < w.L;
+      float4 k4 = make_float4(0.f, 0.f, 0.f, 0.f), v4 = k4;
+      if (valid) {
+        k4 = __ldg(reinterpret_cast<const float4*>(kc + tile + r * D) + li);
+        v4 = __ldg(reinterpret_cast<const float4*>(vc + tile + r * D) + li);
+      }
+#pragma unroll
+      for (int qi = 0; qi < QT; ++qi) {
+        float part = qv[qi].x * k4.x + qv[qi].y * k4.y + qv[qi].z * k4.z + qv[qi].w * k4.w;
+#pragma unroll
+        for (int off = 1; off < LPR; off <<= 1) part += __shfl_xor_sync(0xffffffffu, part, off);
+        if (valid) {
+          const float sc = part * p.scale_log2;
+          const float mnew = fmaxf(m[qi], sc);
+          const float alpha = ex2(m[qi] - mnew);
+          const float pw = ex2(sc - mnew);
+          m[qi] = mnew;
+          l[qi] = l[qi] * alpha + pw;
+          acc[qi].x = acc[qi].x * alpha + pw * v4.x;
+          acc[qi].y = acc[qi].y * alpha + pw * v4.y;
+          acc[qi].z = acc[qi].z * alpha + pw * v4.z;
+          acc[qi].w = acc[qi].w * alpha + pw * v4.w;
+        }
+      }
+    }
+  }
+  // merge the row groups of the warp (RPW == 2 for D == 64)
+  if (RPW == 2) {
+#pragma unroll
+    for (int qi = 0; qi < QT; ++qi) {
+      const float mo = __shfl_xor_sync(0xffffffffu, m[qi], 16);
+      const float lo_ = __shfl_xor_sync(0xffffffffu, l[qi], 16);
+      float4 ao;
+      ao.x = __shfl_xor_sync(0xffffffffu, acc[qi].x, 16);
+      ao.y = __shfl_xor_sync(0xffffffffu, acc[qi].y, 16);
+      ao.z = __shfl_xor_sync(0xffffffffu, acc[qi].z, 16);
+      ao.w = __shfl_xor_sync(0xffffffffu, acc[qi].w, 16);
+      const float M = fmaxf(m[qi], mo);
+      const float fa = m[qi] == -INFINITY ? 0.f : ex2(m[qi] - M);
+      const float fb = mo == -INFINITY ? 0.f : ex2(mo - M);
+      m[qi] = M;
+      l[qi] = l[qi] * fa + lo_ * fb;
+      acc[qi].x = acc[qi].x * fa + ao.x * fb;
+      acc[qi].y = acc[qi].y * fa + ao.y * fb;
+      acc[qi].z = acc[qi].z * fa + ao.z * fb;
+      acc[qi].w = acc[qi].w * fa + ao.w * fb;
+    }
+  }
+  if (bad) s_bad = 1;
+  if (sub == 0) {
+#pragma unroll
+    for (int qi = 0; qi < QT; ++qi) {
+      float* dst = so + (warp * QT + qi) * DP + li * 4;
+      dst[0] = acc[qi].x;
+      dst[1] = acc[qi].y;
+      dst[2] = acc[qi].z;
+      dst[3] = acc[qi].w;
+      if (li == 0) {
+        sm[warp * QT + qi] = m[qi];
+        sl[warp * QT + qi] = l[qi];
+      }
+    }
+  }
+  __syncthreads();
+  merge_and_store<float, D, QT, DP>(so, sm, sl, p, w, s_bad != 0);
+}
+
+// ---------------------------------------------------------------------------
+// Log-sum-exp combine of the split partials: one warp per (sequence, head).
+//   M = max_s m_s,  out = sum_s 2^(m_s - M) o_s / sum_s 2^(m_s - M) l_s.
+
+template <typename T, int D>
+__global__ void __launch_bounds__(128)
+combine_kernel(const DecodeParams p) {
+  constexpr int PER = D / 32;
+  const int lane = threadIdx.x & 31;
+  const int64_t item = static_cast<int64_t>(blockIdx.x) * 4 + (threadIdx.x >> 5);
+  if (item >= static_cast<int64_t>(p.num_seqs) * p.num_q_heads) return;
+  const int b = static_cast<int>(item / p.num_q_heads);
+  const int L = p.context_lens[b];
+  if (L < 0 || static_cast<int64_t>(L) > static_cast<int64_t>(p.max_blocks) * p.block_size) return;
+  int first, end;
+  unit_range(L, p.window, &first, &end);
+  const int nsplit = splits_for(end - first, p.units_per_split);
+  if (nsplit <= 1) return;  // written directly by the decode kernel
+
+  const float2* ml = p.part_ml + item * p.num_splits;
+  const float* po = p.part_o + item * p.num_splits * D;
+  float M = -INFINITY;
+  for (int s = lane; s < nsplit; s += 32) M = fmaxf(M, ml[s].x);
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
+
+  float acc[PER];
+#pragma unroll
+  for (int i = 0; i < PER; ++i) acc[i] = 0.f;
+  float lsum = 0.f;
+  for (int s = 0; s < nsplit; ++s) {
+    const float2 v = ml[s];
+    const float f = v.x == -INFINITY ? 0.f : ex2(v.x - M);
+    lsum = fmaf(f, v.y, lsum);
+    const float* src = po + static_cast<int64_t>(s) * D + lane * PER;
+#pragma unroll
+    for (int i = 0; i < PER; ++i) acc[i] = fmaf(f, src[i], acc[i]);
+  }
+  T* out = static_cast<T*>(p.out) + item * D + lane * PER;
+#pragma unroll
+  for (int i = 0; i < PER; ++i) out[i] = from_f32<T>(acc[i] / lsum);
+}
+
+template <typename T, int D, int NT>
+cudaError_t launch16(const CUtensorMap& kmap, const CUtensorMap& vmap, const DecodeParams& p,
+                     cudaStream_t stream) {
+  auto kern = decode16_kernel<T, D, NT>;
+  const int smem = Tile16<D>::kSmemBytes;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  dim3 grid(p.num_splits, p.num_kv_heads * p.num_head_chunks, p.num_seqs);
+  kern<<<grid, kThreads, smem, stream>>>(kmap, vmap, p);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+size_t decode_16bit_smem_bytes(int head_dim) {
+  return head_dim == 128 ? Tile16<128>::kSmemBytes : Tile16<64>::kSmemBytes;
+}
+
+cudaError_t launch_decode_16bit(int dtype, int head_dim, int ntiles, const CUtensorMap& kmap,
+                                const CUtensorMap& vmap, const DecodeParams& p,
+                                cudaStream_t stream) {
+  // dtype: 1 = fp16, 2 = bf16
+#define PKV_LAUNCH16(T, D, NT) return launch16<T, D, NT>(kmap, vmap, p, stream)
+  if (dtype == 1) {
+    if (head_dim == 128) {
+      if (ntiles == 1) PKV_LAUNCH16(__half, 128, 1);
+      PKV_LAUNCH16(__half, 128, 2);
+    }
+    if (ntiles == 1) PKV_LAUNCH16(__half, 64, 1);
+    PKV_LAUNCH16(__half, 64, 2);
+  }
+  if (head_dim == 128) {
+    if (ntiles == 1) PKV_LAUNCH16(__nv_bfloat16, 128, 1);
+    PKV_LAUNCH16(__nv_bfloat16, 128, 2);
+  }
+  if (ntiles == 1) PKV_LAUNCH16(__nv_bfloat16, 64, 1);
+  PKV_LAUNCH16(__nv_bfloat16, 64, 2);
+#undef PKV_LAUNCH16
+}
+
+cudaError_t launch_decode_f32(int head_dim, const DecodeParams& p, cudaStream_t stream) {
+  dim3 grid(p.num_splits, p.num_kv_heads * p.num_head_chunks, p.num_seqs);
+  if (head_dim == 128)
+    decode_f32_kernel<128><<<grid, kThreads, 0, stream>>>(p);
+  else
+    decode_f32_kernel<64><<<grid, kThreads, 0, stream>>>(p);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_combine(int dtype, int head_dim, const DecodeParams& p, cudaStream_t stream) {
+  const int64_t items = static_cast<int64_t>(p.num_seqs) * p.num_q_heads;
+  if (items == 0) return cudaSuccess;
+  const unsigned blocks = static_cast<unsigned>((items + 3) / 4);
+#define PKV_COMBINE(T, D) combine_kernel<T, D><<<blocks, 128, 0, stream>>>(p)
+  if (dtype == 0) {
+    if (head_dim == 128) PKV_COMBINE(float, 128); else PKV_COMBINE(float, 64);
+  } else if (dtype == 1) {
+    if (head_dim == 128) PKV_COMBINE(__half, 128); else PKV_COMBINE(__half, 64);
+  } else {
+    if (head_dim == 128) PKV_COMBINE(__nv_bfloat16, 128); else PKV_COMBINE(__nv_bfloat16, 64);
+  }
+#undef PKV_COMBINE
+  return cudaGetLastError();
+}
+
+}  // namespace pkv

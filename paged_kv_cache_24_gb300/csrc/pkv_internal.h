@@ -1,0 +1,81 @@
+// pkv_internal.h -- shared definitions between the C-ABI layer and the kernels.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace pkv {
+
+// Tokens per work unit: one 16-row MMA tile of the context.
+constexpr int kUnitTokens = 16;
+// Warps per decode CTA; each warp streams its own units through its own
+// shared-memory ring, and the warps merge their softmax states at the end.
+constexpr int kDecodeWarps = 4;
+// Ring depth (units in flight per warp) by head_dim, for 16-bit pools.
+constexpr int kStagesD128 = 3;
+constexpr int kStagesD64 = 4;
+// Bounded mbarrier wait (polls); a TMA that has not landed by then is treated
+// as an error (output NaN), never as a reason to spin forever.
+constexpr uint32_t kWaitLimit = 1u << 20;
+
+// First position a length-L context attends with window `window`
+// (window <= 0: no window).
+__host__ __device__ __forceinline__ int window_start(int L, int window) {
+  if (window <= 0) return 0;
+  int lo = L - window;
+  return lo > 0 ? lo : 0;
+}
+
+// Units [first, end) covering the attended positions [lo, L).
+__host__ __device__ __forceinline__ void unit_range(int L, int window, int* first, int* end) {
+  if (L <= 0) {
+    *first = *end = 0;
+    return;
+  }
+  *first = window_start(L, window) / kUnitTokens;
+  *end = (L + kUnitTokens - 1) / kUnitTokens;
+}
+
+__host__ __device__ __forceinline__ int splits_for(int n_units, int units_per_split) {
+  return (n_units + units_per_split - 1) / units_per_split;
+}
+
+struct DecodeParams {
+  const void* q;               // [B][Hq][D]
+  void* out;                   // [B][Hq][D]
+  const void* k_cache;         // fp32 path reads the pools directly
+  const void* v_cache;
+  const int32_t* block_tables; // [B][MB]
+  const int32_t* context_lens; // [B]
+  float* part_o;               // [B][Hq][S][D]  unnormalised partial outputs
+  float2* part_ml;             // [B][Hq][S]     (running max in log2 units, sum)
+  int64_t num_blocks;
+  int num_seqs, num_q_heads, num_kv_heads, group;  // group = Hq / Hkv
+  int head_chunk;              // query heads per CTA (<= 8 * NT)
+  int num_head_chunks;         // ceil(group / head_chunk)
+  int max_blocks;              // MB
+  int block_size;              // bs
+  int window;
+  float scale_log2;            // scale * log2(e)
+  int units_per_split;
+  int num_splits;              // grid.x
+};
+
+// Launchers (return cudaGetLastError of the launch).
+cudaError_t launch_decode_16bit(int dtype, int head_dim, int ntiles, const CUtensorMap& kmap,
+                                const CUtensorMap& vmap, const DecodeParams& p,
+                                cudaStream_t stream);
+cudaError_t launch_decode_f32(int head_dim, const DecodeParams& p, cudaStream_t stream);
+cudaError_t launch_combine(int dtype, int head_dim, const DecodeParams& p, cudaStream_t stream);
+cudaError_t launch_append(int elem_bytes, const void* k, const void* v, const int64_t* slots,
+                          int64_t num_tokens, void* k_cache, void* v_cache, int64_t num_blocks,
+                          int num_kv_heads, int block_size, int head_dim, cudaStream_t stream);
+cudaError_t launch_slot_mapping(const int32_t* block_tables, int num_seqs, int max_blocks,
+                                const int64_t* positions, int block_size, int64_t* slots,
+                                cudaStream_t stream);
+
+// Dynamic shared memory the 16-bit decode kernel needs for a head_dim.
+size_t decode_16bit_smem_bytes(int head_dim);
+
+}  // namespace pkv

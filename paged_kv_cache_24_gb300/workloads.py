@@ -1,0 +1,293 @@
+"""Seeded synthetic workloads for paged decode attention.
+
+This module produces inputs only: context lengths, block tables drawn from a
+shuffled or fragmented block pool, a prefilled K/V pool, and the per-step new
+tokens.  It holds none of the attention arithmetic and no slot arithmetic
+(each side -- the CUDA library and the float64 oracle -- maps positions to
+slots with its own code), so it can feed both without coupling them.
+
+Workload recipes follow the five benchmark configurations of this project
+(tiny fp32 / MHA fp16 / GQA bf16 / sliding-window bf16 / serving mix fp16).
+The block pool and its LIFO free list follow the block allocator of
+"Build a Paged KV Cache in Pure Python", Step 2 (``BlockAllocator``: a stack of
+free block ids, ``pop()`` to allocate, ``MemoryError`` when exhausted).
+
+Poisoning: every pool slot that no sequence's context covers holds NaN (and,
+with ``poison_outside_window``, every slot before a sequence's window start),
+so a kernel that reads a slot it should not shows NaN in its output.  The slot
+each step's append will write also starts as NaN.
+"""
+from __future__ import annotations
+
+import math
+from dataclasses import dataclass, field
+from typing import List, Optional
+
+import numpy as np
+import torch
+
+__all__ = [
+    "BlockAllocator", "WorkloadSpec", "Workload", "make_workload", "CONFIGS", "config_spec",
+]
+
+
+class BlockAllocator:
+    """Fixed pool of block ids with a LIFO free list (stack), like a page allocator.
+
+    ``allocate`` pops ids from the end of the free list and raises ``MemoryError``
+    when the pool cannot satisfy the request; ``deallocate`` pushes a sequence's
+    ids back.  Pure host bookkeeping: it never touches K/V data.
+    """
+
+    def __init__(self, total_blocks: int, free_list: Optional[List[int]] = None):
+        self.total_blocks = int(total_blocks)
+        self.free_list: List[int] = (list(range(total_blocks)) if free_list is None
+                                     else [int(x) for x in free_list])
+        self.used_map: dict = {}
+
+    def allocate(self, seq_id: int, num_blocks: int = 1) -> List[int]:
+        if len(self.free_list) < num_blocks:
+            raise MemoryError(
+                f"KV cache out of memory: need {num_blocks} blocks, "
+                f"only {len(self.free_list)} free of {self.total_blocks} total.")
+        got = [self.free_list.pop() for _ in range(num_blocks)]
+        self.used_map.setdefault(seq_id, []).extend(got)
+        return got
+
+    def deallocate(self, seq_id: int) -> None:
+        for idx in self.used_map.pop(seq_id, []):
+            self.free_list.append(idx)
+
+    @property
+    def free_blocks(self) -> int:
+        return len(self.free_list)
+
+    def used_blocks(self) -> int:
+        return sum(len(v) for v in self.used_map.values())
+
+
+@dataclass
+class WorkloadSpec:
+    name: str
+    dtype: torch.dtype
+    num_seqs: int
+    num_q_heads: int
+    num_kv_heads: int
+    head_dim: int
+    block_size: int
+    # Lengths: either explicit, or drawn by `len_dist` in [len_lo, len_hi].
+    # For single-step workloads the lengths are the decode lengths (the step's
+    # appended token included); for multi-step ones they are the lengths before
+    # the first step's append.
+    lens: Optional[List[int]] = None
+    len_dist: str = "uniform"  # "uniform" | "geometric"
+    len_lo: int = 1
+    len_hi: int = 1
+    geom_mean: float = 512.0
+    lens_are_pre_append: bool = False
+    window: int = 0
+    steps: int = 1
+    pool_factor: float = 1.2          # pool = ceil(factor * blocks needed), shuffled ids
+    explicit_pool: Optional[int] = None
+    occupancy: Optional[float] = None  # serving: fraction of the pool held at step 0
+    prefix_group: int = 0             # serving: sequences per shared-prefix group
+    prefix_tokens: int = 0            # serving: shared prefix length in tokens
+    seed: int = 0
+
+
+def config_spec(idx: int, **overrides) -> WorkloadSpec:
+    """The five benchmark workloads (index 0..4), optionally resized for tests."""
+    base = {
+        0: dict(name="tiny_fp32", dtype=torch.float32, num_seqs=4, num_q_heads=8, num_kv_heads=8,
+                head_dim=64, block_size=16, lens=[17, 33, 64, 100], lens_are_pre_append=True,
+                explicit_pool=32, seed=0),
+        1: dict(name="mha_fp16", dtype=torch.float16, num_seqs=64, num_q_heads=32, num_kv_heads=32,
+                head_dim=128, block_size=16, len_lo=512, len_hi=4096, seed=1),
+        2: dict(name="gqa_bf16", dtype=torch.bfloat16, num_seqs=256, num_q_heads=32,
+                num_kv_heads=8, head_dim=128, block_size=32, len_lo=1024, len_hi=8192, seed=2),
+        3: dict(name="sliding_bf16", dtype=torch.bfloat16, num_seqs=16, num_q_heads=32,
+                num_kv_heads=8, head_dim=128, block_size=16, len_lo=16384, len_hi=32768,
+                window=4096, seed=3),
+        4: dict(name="serving_fp16", dtype=torch.float16, num_seqs=1024, num_q_heads=32,
+                num_kv_heads=8, head_dim=128, block_size=16, len_dist="geometric", len_lo=128,
+                len_hi=2048, geom_mean=512.0, lens_are_pre_append=True, steps=32,
+                occupancy=0.7, prefix_group=16, prefix_tokens=256, seed=4),
+    }[idx]
+    base.update(overrides)
+    return WorkloadSpec(**base)
+
+
+CONFIGS = {config_spec(i).name: i for i in range(5)}
+
+
+@dataclass
+class Workload:
+    spec: WorkloadSpec
+    scale: float                 # float32-rounded 1/sqrt(head_dim)
+    num_blocks: int
+    block_tables: torch.Tensor   # [B, MB] int32; -1 where a sequence has no block
+    lens_steps: torch.Tensor     # [S, B] int32 decode length at each step (append included)
+    pos_steps: torch.Tensor      # [S, B] int64 position of each step's new token
+    q_steps: torch.Tensor        # [S, B, Hq, D]
+    k_steps: torch.Tensor        # [S, B, Hkv, D]
+    v_steps: torch.Tensor        # [S, B, Hkv, D]
+    k_cache: torch.Tensor        # [NB, Hkv, bs, D]
+    v_cache: torch.Tensor        # [NB, Hkv, bs, D]
+    unique_blocks: int = 0       # distinct physical blocks referenced at step 0
+    free_list_after: List[int] = field(default_factory=list)
+
+    @property
+    def steps(self) -> int:
+        return self.lens_steps.shape[0]
+
+    @property
+    def max_blocks(self) -> int:
+        return self.block_tables.shape[1]
+
+
+def _draw_lengths(spec: WorkloadSpec, rng: np.random.Generator) -> np.ndarray:
+    if spec.lens is not None:
+        return np.asarray(spec.lens, dtype=np.int64)
+    if spec.len_dist == "uniform":
+        return rng.integers(spec.len_lo, spec.len_hi + 1, size=spec.num_seqs).astype(np.int64)
+    if spec.len_dist == "geometric":
+        # geometric on {1, 2, ...} with success probability 1/mean, then clipped
+        raw = rng.geometric(1.0 / spec.geom_mean, size=spec.num_seqs)
+        return np.clip(raw, spec.len_lo, spec.len_hi).astype(np.int64)
+    raise ValueError(spec.len_dist)
+
+
+def _fill_random(t: torch.Tensor, gen: torch.Generator, chunk_elems: int = 1 << 26) -> None:
+    """t <- N(0, 1) drawn in fp32 and rounded to t's dtype, in chunks (bounded temporaries)."""
+    flat = t.view(-1)
+    for s in range(0, flat.numel(), chunk_elems):
+        e = min(flat.numel(), s + chunk_elems)
+        flat[s:e] = torch.randn(e - s, generator=gen, device=t.device, dtype=torch.float32)
+
+
+def make_workload(spec: WorkloadSpec, device="cpu", poison: bool = True,
+                  poison_outside_window: bool = False) -> Workload:
+    """Build the seeded inputs of one workload on `device`.
+
+    Host-side planning (lengths, block ids) uses numpy's PCG64 seeded with
+    ``spec.seed``; tensor data uses a torch generator on ``device`` with the same
+    seed.  The cache holds every sequence's tokens [0, L-1) of the first step;
+    each step's append writes position ``pos_steps[s, b]``.
+    """
+    device = torch.device(device)
+    rng = np.random.default_rng(spec.seed)
+    B, Hq, Hkv, D, bs = (spec.num_seqs, spec.num_q_heads, spec.num_kv_heads, spec.head_dim,
+                         spec.block_size)
+    if Hq % Hkv:
+        raise ValueError("num_q_heads must be a multiple of num_kv_heads")
+    S = spec.steps
+    lens0 = _draw_lengths(spec, rng)
+    if len(lens0) != B:
+        raise ValueError("lens must have num_seqs entries")
+    if spec.lens_are_pre_append:
+        pre = lens0                      # tokens already cached before step 0
+    else:
+        pre = np.maximum(lens0 - 1, 0)   # the first step appends token L-1
+    # position of each step's new token and decode length after it
+    pos = pre[None, :] + np.arange(S, dtype=np.int64)[:, None]          # [S, B]
+    lens_steps = pos + 1
+    final_len = lens_steps[-1]
+    need_final = (final_len + bs - 1) // bs                             # blocks by the last step
+    MB = int(need_final.max()) if B else 0
+    block_tables = np.full((B, max(MB, 1)), -1, dtype=np.int64)
+
+    if spec.occupancy is None:
+        # Shuffled pool: ids from a random permutation, taken consecutively per sequence.
+        total_need = int(need_final.sum())
+        nb = spec.explicit_pool if spec.explicit_pool is not None else int(
+            math.ceil(spec.pool_factor * total_need))
+        if nb < total_need:
+            raise ValueError("pool smaller than the blocks the workload needs")
+        perm = rng.permutation(nb)
+        cursor = 0
+        for b in range(B):
+            n = int(need_final[b])
+            block_tables[b, :n] = perm[cursor:cursor + n]
+            cursor += n
+        unique = total_need
+        free_after: List[int] = [int(x) for x in perm[cursor:]]
+    else:
+        # Serving mix: groups of `prefix_group` consecutive sequences share their
+        # leading full blocks (identical block ids); the rest is private.  The
+        # pool is sized so the step-0 blocks fill `occupancy` of it, at random
+        # ids; the remaining ids form a shuffled free list popped LIFO.
+        need0 = (pre + bs - 1) // bs
+        shared_per_seq = np.zeros(B, dtype=np.int64)
+        if spec.prefix_group > 0 and spec.prefix_tokens > 0:
+            cap = spec.prefix_tokens // bs
+            shared_per_seq = np.minimum(cap, pre // bs)
+        groups = []
+        for g0 in range(0, B, max(spec.prefix_group, 1) if spec.prefix_group else B):
+            members = list(range(g0, min(B, g0 + (spec.prefix_group or B))))
+            groups.append(members)
+        n_shared = [int(shared_per_seq[m].max()) if m else 0 for m in groups]
+        unique = int(sum(n_shared) + sum(int(need0[b] - shared_per_seq[b]) for b in range(B)))
+        nb = int(math.ceil(unique / spec.occupancy))
+        ids = rng.permutation(nb)
+        occupied, free = ids[:unique], ids[unique:]
+        cursor = 0
+        for members, ns in zip(groups, n_shared):
+            shared_ids = occupied[cursor:cursor + ns]
+            cursor += ns
+            for b in members:
+                block_tables[b, :shared_per_seq[b]] = shared_ids[:shared_per_seq[b]]
+        for b in range(B):
+            n = int(need0[b] - shared_per_seq[b])
+            block_tables[b, shared_per_seq[b]:need0[b]] = occupied[cursor:cursor + n]
+            cursor += n
+        alloc = BlockAllocator(nb, free_list=list(free))
+        held = need0.copy()
+        for s in range(S):                      # blocks the 32 steps need, in step order
+            for b in range(B):
+                while held[b] * bs <= pos[s, b]:
+                    block_tables[b, held[b]] = alloc.allocate(b, 1)[0]
+                    held[b] += 1
+        free_after = list(alloc.free_list)
+
+    # ---- tensors ---------------------------------------------------------
+    gen = torch.Generator(device=device)
+    gen.manual_seed(spec.seed)
+    dt = spec.dtype
+    k_cache = torch.empty((nb, Hkv, bs, D), dtype=dt, device=device)
+    v_cache = torch.empty((nb, Hkv, bs, D), dtype=dt, device=device)
+    _fill_random(k_cache, gen)
+    _fill_random(v_cache, gen)
+    q_steps = torch.empty((S, B, Hq, D), dtype=dt, device=device)
+    k_steps = torch.empty((S, B, Hkv, D), dtype=dt, device=device)
+    v_steps = torch.empty((S, B, Hkv, D), dtype=dt, device=device)
+    for t in (q_steps, k_steps, v_steps):
+        _fill_random(t, gen)
+
+    if poison:
+        # valid[slot] = some sequence holds a token there before step 0
+        valid = np.zeros(nb * bs, dtype=bool)
+        for b in range(B):
+            lo = 0
+            if poison_outside_window and spec.window > 0:
+                lo = max(0, int(lens_steps[0, b]) - spec.window)
+            t = np.arange(lo, int(pre[b]), dtype=np.int64)
+            if t.size:
+                valid[block_tables[b, t // bs] * bs + t % bs] = True
+        bad = torch.from_numpy(np.nonzero(~valid)[0]).to(device)
+        if bad.numel():
+            blk, row = bad // bs, bad % bs
+            k_cache[blk, :, row, :] = float("nan")
+            v_cache[blk, :, row, :] = float("nan")
+
+    return Workload(
+        spec=spec,
+        scale=float(np.float32(1.0 / math.sqrt(D))),
+        num_blocks=nb,
+        block_tables=torch.from_numpy(block_tables.astype(np.int32)).to(device),
+        lens_steps=torch.from_numpy(lens_steps.astype(np.int32)).to(device),
+        pos_steps=torch.from_numpy(pos.astype(np.int64)).to(device),
+        q_steps=q_steps, k_steps=k_steps, v_steps=v_steps,
+        k_cache=k_cache, v_cache=v_cache,
+        unique_blocks=unique,
+        free_list_after=free_after,
+    )

@@ -1,0 +1,124 @@
+"""The C ABI on the host: every declared symbol is exported, and argument checks
+return their status codes before anything touches a GPU."""
+import ctypes
+import os
+import re
+
+import pytest
+
+REPO = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(REPO, "include", "pkv.h")
+
+OK, NULL, SHAPE, DTYPE, UNSUP, ALIGN = 0, 1, 2, 3, 4, 5
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?\w+\s*\*?\s*(pkv_\w+)\s*\(", text, flags=re.M)))
+
+
+def test_header_declares_the_two_calls_of_the_method():
+    names = declared_functions()
+    assert "pkv_append" in names and "pkv_decode" in names
+
+
+def test_library_exports_every_declared_symbol(pkv_lib):
+    lib = ctypes.CDLL(pkv_lib.library_path())
+    missing = [n for n in declared_functions() if not hasattr(lib, n)]
+    assert not missing, f"not exported: {missing}"
+
+
+def test_status_strings(pkv_lib):
+    for code in range(8):
+        assert pkv_lib.status_string(code).startswith("PKV_")
+    assert "unknown" in pkv_lib.status_string(99)
+
+
+def _layout(pkv, nb=64, hkv=8, bs=16, d=128, dt=1):
+    return pkv.CacheLayout(nb, hkv, bs, d, dt)
+
+
+FAKE = 0x100000  # a 16-byte aligned address that is never dereferenced
+
+
+def _decode(pkv, layout, q=FAKE, k=FAKE, v=FAKE, bt=FAKE, lens=FAKE, out=FAKE, B=4, hq=32,
+            mb=8, window=0, tps=0):
+    lib = pkv.load_library()
+    return lib.pkv_decode_split(q, B, hq, k, v, ctypes.byref(layout), bt, mb, lens, window,
+                                0.1, out, tps, None)
+
+
+def test_decode_argument_checks(pkv_lib):
+    pkv = pkv_lib
+    assert _decode(pkv, _layout(pkv), q=0) == NULL
+    assert _decode(pkv, _layout(pkv), out=0) == NULL
+    assert _decode(pkv, _layout(pkv, dt=7)) == DTYPE
+    assert _decode(pkv, _layout(pkv, d=96)) == UNSUP
+    assert _decode(pkv, _layout(pkv, bs=8)) == UNSUP
+    assert _decode(pkv, _layout(pkv, bs=24)) == UNSUP
+    assert _decode(pkv, _layout(pkv), hq=12) == SHAPE           # 12 % 8 != 0
+    assert _decode(pkv, _layout(pkv), B=-1) == SHAPE
+    assert _decode(pkv, _layout(pkv, hkv=0)) == SHAPE
+    assert _decode(pkv, _layout(pkv), q=FAKE + 8) == ALIGN
+    assert _decode(pkv, _layout(pkv), lens=FAKE + 2) == ALIGN
+    assert _decode(pkv, _layout(pkv), tps=24) == SHAPE          # not a multiple of 16
+    assert _decode(pkv, _layout(pkv), tps=4096) == UNSUP        # more than 2048 per split
+    assert _decode(pkv, _layout(pkv, nb=1 << 30)) == UNSUP      # TMA rows exceed int32
+    # nothing to do: succeeds without touching the device
+    assert _decode(pkv, _layout(pkv), B=0, q=0, out=0) == OK
+
+
+def test_append_argument_checks(pkv_lib):
+    pkv = pkv_lib
+    lib = pkv.load_library()
+    lay = _layout(pkv)
+
+    def call(k=FAKE, v=FAKE, slots=FAKE, n=3, kc=FAKE, vc=FAKE, layout=lay):
+        return lib.pkv_append(k, v, slots, n, kc, vc, ctypes.byref(layout), None)
+
+    assert call(k=0) == NULL
+    assert call(slots=0) == NULL
+    assert call(n=-1) == SHAPE
+    assert call(n=0, k=0, v=0) == OK
+    assert call(layout=_layout(pkv, dt=-1)) == DTYPE
+    assert call(layout=_layout(pkv, d=4)) == UNSUP   # 4 fp16 = 8 bytes: not 16-byte rows
+    assert call(v=FAKE + 4) == ALIGN
+    assert call(slots=FAKE + 4) == ALIGN
+
+
+def test_slot_mapping_argument_checks(pkv_lib):
+    lib = pkv_lib.load_library()
+    assert lib.pkv_slot_mapping(FAKE, 4, 8, FAKE, 0, FAKE, None) == SHAPE
+    assert lib.pkv_slot_mapping(0, 4, 8, FAKE, 16, FAKE, None) == NULL
+    assert lib.pkv_slot_mapping(FAKE, 4, 8, FAKE + 4, 16, FAKE, None) == ALIGN
+    assert lib.pkv_slot_mapping(0, 0, 8, 0, 16, 0, None) == OK
+
+
+@pytest.mark.parametrize("cfg,expect", [
+    # (num_seqs, hq, layout args, max_blocks, window) -> (tokens_per_split, num_splits)
+    ((64, 32, (10000, 32, 16, 128, 1), 256, 0), (512, 8)),
+    ((256, 32, (44000, 8, 32, 128, 2), 256, 0), (512, 16)),
+    ((16, 32, (30000, 8, 16, 128, 2), 2048, 4096), (256, 17)),
+    ((4, 8, (32, 8, 16, 64, 0), 7, 0), (128, 1)),
+])
+def test_plan(pkv_lib, cfg, expect):
+    B, hq, lay, mb, window = cfg
+    assert pkv_lib.pkv_decode_plan(B, hq, pkv_lib.CacheLayout(*lay), mb, window,
+                                   num_sms=152) == expect
+
+
+def test_plan_covers_every_length(pkv_lib):
+    """The grid's split count bounds the splits any valid length needs."""
+    lay = pkv_lib.CacheLayout(5000, 8, 32, 128, 2)
+    for mb in (1, 3, 17, 64):
+        for window in (0, 1, 15, 16, 17, 100, 4096):
+            for tps in (0, 16, 64, 2048):
+                t, ns = pkv_lib.pkv_decode_plan(8, 32, lay, mb, window, tps, num_sms=152)
+                units = t // 16
+                worst = 0
+                for L in range(0, mb * 32 + 1):
+                    lo = max(0, L - window) if window > 0 else 0
+                    n = 0 if L == 0 else (L + 15) // 16 - lo // 16
+                    worst = max(worst, -(-n // units))
+                assert worst <= ns
