@@ -314,7 +314,7 @@ def main(argv=None):
                        spec.window, w.scale, out=out)
 
     kv_per_step = statistics.mean(b["kv"] for b in sbytes)
-    need_flush = kv_per_step < 2 * L2_BYTES
+    need_flush = kv_per_step < 4 * L2_BYTES
     flush_buf = torch.empty(2 * L2_BYTES, dtype=torch.uint8, device="cuda") if need_flush else None
 
     for s in range(args.warmup):
