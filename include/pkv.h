@@ -57,7 +57,9 @@ typedef enum pkv_status {
   PKV_ERR_UNSUPPORTED = 4, /* valid, not implemented (head_dim, block_size, ...)  */
   PKV_ERR_ALIGNMENT = 5,   /* a data pointer is not 16-byte aligned              */
   PKV_ERR_CUDA = 6,        /* a CUDA runtime call or a kernel launch failed       */
-  PKV_ERR_NOMEM = 7        /* the split-K workspace could not be allocated        */
+  PKV_ERR_NOMEM = 7,       /* the split-K workspace could not be allocated        */
+  PKV_ERR_SCRATCH = 8      /* pkv_decode_noalloc: the problem needs more split-K
+                              scratch than its fixed buffer holds                */
 } pkv_status;
 
 /* Shape of one layer's K (or V) pool. */
@@ -156,6 +158,37 @@ int pkv_decode_split(const void* q, int32_t num_seqs, int32_t num_q_heads,
 int pkv_decode_plan(int32_t num_seqs, int32_t num_q_heads, const pkv_cache_layout* layout,
                     int32_t max_blocks_per_seq, int32_t window, int32_t tokens_per_split,
                     int32_t num_sms, int32_t* tokens_per_split_out, int32_t* num_splits_out);
+
+/*
+ * pkv_decode_noalloc -- pkv_decode for callers that cannot allocate device
+ * memory.  (The pages have no counterpart: it is a deployment variant.)
+ *   Same arguments, same result and same split plan as pkv_decode.  Where
+ *   pkv_decode asks cudaMalloc for its split-K workspace, this entry point
+ *   uses a fixed buffer of PKV_NOALLOC_SCRATCH_BYTES (32 MiB) that is part of
+ *   the library image: every GPU that loads libpkv holds it until the process
+ *   exits.  It never calls cudaMalloc, cudaFree or any allocating routine, so
+ *   it suits callers that have handed all free HBM to their own pool (a
+ *   serving engine that reserves memory for its KV blocks up front leaves a
+ *   library nothing to allocate from) and callers that cannot afford the
+ *   device-wide synchronisation cudaMalloc / cudaFree may bring in a hot
+ *   loop.
+ *   Limit: B * Hq * num_splits * (head_dim * 4 + 8) bytes must fit in the
+ *   buffer (num_splits from pkv_decode_plan; a problem that needs no split
+ *   uses no scratch); otherwise PKV_ERR_SCRATCH and nothing is launched.
+ *   Set-up: the first call on each device looks up the buffer's device address
+ *   (cudaGetSymbolAddress) with that device current; make that first call
+ *   before any stream capture.
+ *   Sharing: every call on every stream of a device uses the same buffer,
+ *   which keeps the last call's partial results.  Nothing in it needs to start
+ *   at zero (each call writes every partial it reads), but calls that overlap
+ *   on the GPU race on it: order them (one stream, or events).
+ */
+#define PKV_NOALLOC_SCRATCH_BYTES (32u * 1024u * 1024u)
+int pkv_decode_noalloc(const void* q, int32_t num_seqs, int32_t num_q_heads,
+                       const void* k_cache, const void* v_cache, const pkv_cache_layout* layout,
+                       const int32_t* block_tables, int32_t max_blocks_per_seq,
+                       const int32_t* context_lens, int32_t window, float scale, void* out,
+                       void* stream);
 
 /* Human-readable name of a pkv_status code (static storage). */
 const char* pkv_status_string(int status);

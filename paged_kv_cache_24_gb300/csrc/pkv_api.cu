@@ -184,6 +184,35 @@ int check_decode_args(const void* q, int32_t num_seqs, int32_t num_q_heads, cons
 
 }  // namespace
 
+namespace pkv {
+// Host helpers shared with the fixed-scratch entry point (pkv_noalloc.cu).
+int decode_checks(const void* q, int32_t num_seqs, int32_t num_q_heads, const void* k_cache,
+                  const void* v_cache, const pkv_cache_layout* layout,
+                  const int32_t* block_tables, int32_t max_blocks, const int32_t* context_lens,
+                  const void* out) {
+  return check_decode_args(q, num_seqs, num_q_heads, k_cache, v_cache, layout, block_tables,
+                           max_blocks, context_lens, out);
+}
+int decode_plan(int num_seqs, int num_q_heads, const pkv_cache_layout* layout, int max_blocks,
+                int window, int* head_chunk, int* num_head_chunks, int* ntiles,
+                int* units_per_split, int* num_splits) {
+  Plan plan;
+  int rc = make_plan(num_seqs, num_q_heads, layout, max_blocks, window, 0,
+                     sm_count_of_current_device(), &plan);
+  if (rc != PKV_OK) return rc;
+  *head_chunk = plan.head_chunk;
+  *num_head_chunks = plan.num_head_chunks;
+  *ntiles = plan.ntiles;
+  *units_per_split = plan.units_per_split;
+  *num_splits = plan.num_splits;
+  return PKV_OK;
+}
+int pool_tensor_map(CUtensorMap* map, const void* pool, const pkv_cache_layout* layout) {
+  return encode_pool_map(map, pool, layout);
+}
+int status_of(cudaError_t e) { return to_status(e); }
+}  // namespace pkv
+
 extern "C" {
 
 const char* pkv_status_string(int status) {
@@ -196,6 +225,7 @@ const char* pkv_status_string(int status) {
     case PKV_ERR_ALIGNMENT: return "PKV_ERR_ALIGNMENT: data pointer not 16-byte aligned";
     case PKV_ERR_CUDA: return "PKV_ERR_CUDA: a CUDA call or kernel launch failed";
     case PKV_ERR_NOMEM: return "PKV_ERR_NOMEM: workspace allocation failed";
+    case PKV_ERR_SCRATCH: return "PKV_ERR_SCRATCH: problem needs more than the fixed no-alloc scratch";
     default: return "unknown pkv status";
   }
 }

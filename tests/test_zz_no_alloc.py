@@ -1,0 +1,93 @@
+"""pkv_decode_noalloc: decode without any device allocation at call time.
+
+Some callers cannot let a library call cudaMalloc: a serving engine that has
+already handed all free HBM to its own KV-block pool, or a hot loop that must
+not run into the device-wide synchronisation cudaMalloc / cudaFree can bring.
+pkv_decode_noalloc serves them with a fixed scratch buffer that lives in the
+library image.  These checks call it through the C ABI and compare it with
+pkv_decode, the entry point that allocates its workspace, on two calls in a
+row (the second call runs over the first call's leftovers in the shared
+buffer).  This file is collected last on purpose.
+"""
+import ctypes
+
+import numpy as np
+import pytest
+import torch
+
+from paged_kv_cache_24_gb300.workloads import config_spec, make_workload
+
+pytestmark = pytest.mark.gpu
+
+PKV_ERR_SCRATCH = 8
+TOL = {torch.float16: 2e-3, torch.bfloat16: 2e-3, torch.float32: 1e-5}
+
+
+def _noalloc_fn(pkv):
+    lib = pkv.load_library()
+    fn = lib.pkv_decode_noalloc
+    vp, i32 = ctypes.c_void_p, ctypes.c_int32
+    fn.argtypes = [vp, i32, i32, vp, vp, ctypes.POINTER(pkv.CacheLayout), vp, i32, vp, i32,
+                   ctypes.c_float, vp, vp]
+    fn.restype = ctypes.c_int
+    return fn
+
+
+def _call_noalloc(pkv, fn, q, kc, vc, bt, lens, window, scale, out):
+    layout = pkv.cache_layout(kc)
+    return fn(q.data_ptr(), q.shape[0], q.shape[1], kc.data_ptr(), vc.data_ptr(),
+              ctypes.byref(layout), bt.data_ptr(), bt.shape[1], lens.data_ptr(), window,
+              scale, out.data_ptr(), torch.cuda.current_stream().cuda_stream)
+
+
+def _close(a, b, dtype):
+    a, b = a.double(), b.double()
+    tol = TOL[dtype] + 0.5 * torch.finfo(dtype).eps * b.abs()
+    assert torch.isfinite(a).all()
+    assert ((a - b).abs() <= tol).all(), f"max diff {(a - b).abs().max().item():.3e}"
+
+
+@pytest.mark.parametrize("dtype,window", [(torch.bfloat16, 0), (torch.float16, 300),
+                                          (torch.float32, 0)])
+def test_noalloc_matches_allocating_decode_twice(pkv_lib, dtype, window):
+    pkv = pkv_lib
+    fn = _noalloc_fn(pkv)
+    spec = config_spec(0, dtype=dtype, num_seqs=6, num_q_heads=16, num_kv_heads=4,
+                       head_dim=128, block_size=16, lens=[1, 40, 700, 1500, 2600, 3333],
+                       explicit_pool=None, lens_are_pre_append=False, window=window)
+    w = make_workload(spec, device="cuda", poison=True)
+    plan = pkv.pkv_decode_plan(spec.num_seqs, spec.num_q_heads, pkv.cache_layout(w.k_cache),
+                               w.max_blocks, window)
+    assert plan[1] > 1, "the case must use the split-K scratch"
+    slots = pkv.pkv_slot_mapping(w.block_tables, w.pos_steps[0].contiguous(), 16)
+    pkv.pkv_append(w.k_steps[0], w.v_steps[0], slots, w.k_cache, w.v_cache)
+    lens = w.lens_steps[0].contiguous()
+    for call in range(2):
+        # the second call uses other queries and shorter contexts, over what the
+        # first call left in the shared scratch
+        q = w.q_steps[0] if call == 0 else torch.flip(w.q_steps[0], dims=[0]).contiguous()
+        ln = lens if call == 0 else torch.clamp(lens - 17, min=0).contiguous()
+        ref = pkv.pkv_decode(q, w.k_cache, w.v_cache, w.block_tables, ln, window, w.scale)
+        out = torch.full_like(q, float("nan"))
+        rc = _call_noalloc(pkv, fn, q, w.k_cache, w.v_cache, w.block_tables, ln, window,
+                           w.scale, out)
+        assert rc == 0, pkv.status_string(rc)
+        torch.cuda.synchronize()
+        _close(out, ref, dtype)
+
+
+def test_noalloc_rejects_problems_beyond_its_scratch(pkv_lib):
+    pkv = pkv_lib
+    fn = _noalloc_fn(pkv)
+    B, hq, hkv, d, bs, mb = 1024, 32, 8, 128, 16, 130
+    q = torch.zeros(B, hq, d, dtype=torch.float16, device="cuda")
+    out = torch.zeros_like(q)
+    kc = torch.zeros(4, hkv, bs, d, dtype=torch.float16, device="cuda")
+    bt = torch.zeros(B, mb, dtype=torch.int32, device="cuda")
+    lens = torch.zeros(B, dtype=torch.int32, device="cuda")
+    tps, ns = pkv.pkv_decode_plan(B, hq, pkv.cache_layout(kc), mb, 0)
+    need = B * hq * ns * (d * 4 + 8)
+    assert need > 32 * 1024 * 1024
+    rc = _call_noalloc(pkv, fn, q, kc, kc, bt, lens, 0, 0.1, out)
+    assert rc == PKV_ERR_SCRATCH
+    assert "scratch" in pkv.status_string(rc)
