@@ -4,6 +4,7 @@
 // token at position pos is written to row pos % block_size of the sequence's
 // (pos // block_size)-th block.  Here the write is a pure 16-byte vector copy
 // per thread, so the cache holds exactly the bits it was given.
+#include "pkv_device.cuh"
 #include "pkv_internal.h"
 
 namespace pkv {
@@ -12,6 +13,8 @@ namespace {
 __global__ void slot_mapping_kernel(const int32_t* __restrict__ block_tables, int num_seqs,
                                     int max_blocks, const int64_t* __restrict__ positions,
                                     int block_size, int64_t* __restrict__ slots) {
+  pdl_launch_dependents();
+  pdl_wait_prior();
   const int b = blockIdx.x * blockDim.x + threadIdx.x;
   if (b >= num_seqs) return;
   const int64_t pos = positions[b];
@@ -29,6 +32,8 @@ __global__ void append_kernel(const uint4* __restrict__ k, const uint4* __restri
                               uint4* __restrict__ k_cache, uint4* __restrict__ v_cache,
                               int64_t num_blocks, int num_kv_heads, int block_size,
                               int chunks_per_row) {
+  pdl_launch_dependents();
+  pdl_wait_prior();
   const int64_t idx = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
   const int64_t per_token = static_cast<int64_t>(num_kv_heads) * chunks_per_row;
   if (idx >= num_tokens * per_token) return;
@@ -56,9 +61,8 @@ cudaError_t launch_slot_mapping(const int32_t* block_tables, int num_seqs, int m
   if (num_seqs == 0) return cudaSuccess;
   const int threads = 128;
   const int blocks = (num_seqs + threads - 1) / threads;
-  slot_mapping_kernel<<<blocks, threads, 0, stream>>>(block_tables, num_seqs, max_blocks,
-                                                      positions, block_size, slots);
-  return cudaGetLastError();
+  return launch_pdl(slot_mapping_kernel, dim3(blocks), dim3(threads), 0, stream, block_tables,
+                    num_seqs, max_blocks, positions, block_size, slots);
 }
 
 cudaError_t launch_append(int elem_bytes, const void* k, const void* v, const int64_t* slots,
@@ -70,11 +74,10 @@ cudaError_t launch_append(int elem_bytes, const void* k, const void* v, const in
   const int threads = 256;
   const int64_t blocks = (total + threads - 1) / threads;
   if (blocks > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
-  append_kernel<<<static_cast<unsigned>(blocks), threads, 0, stream>>>(
-      static_cast<const uint4*>(k), static_cast<const uint4*>(v), slots, num_tokens,
-      static_cast<uint4*>(k_cache), static_cast<uint4*>(v_cache), num_blocks, num_kv_heads,
-      block_size, chunks_per_row);
-  return cudaGetLastError();
+  return launch_pdl(append_kernel, dim3(static_cast<unsigned>(blocks)), dim3(threads), 0, stream,
+                    static_cast<const uint4*>(k), static_cast<const uint4*>(v), slots,
+                    num_tokens, static_cast<uint4*>(k_cache), static_cast<uint4*>(v_cache),
+                    num_blocks, num_kv_heads, block_size, chunks_per_row);
 }
 
 }  // namespace pkv

@@ -28,6 +28,8 @@
 //    the workspace and the combine kernel applies the log-sum-exp merge.
 #include <math.h>
 
+#include <atomic>
+
 #include "pkv_device.cuh"
 #include "pkv_internal.h"
 
@@ -147,6 +149,8 @@ decode16_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant_
 
   const int lane = threadIdx.x & 31;
   const int warp = threadIdx.x >> 5;
+  pdl_launch_dependents();
+  pdl_wait_prior();
   const WorkItem w = make_work_item(p);
   if (!w.len_ok || w.empty) {
     if (w.split == 0) write_trivial_rows<T, D>(p, w);
@@ -428,6 +432,8 @@ decode_f32_kernel(const DecodeParams p) {
 
   const int lane = threadIdx.x & 31;
   const int warp = threadIdx.x >> 5;
+  pdl_launch_dependents();
+  pdl_wait_prior();
   const WorkItem w = make_work_item(p);
   if (!w.len_ok || w.empty) {
     if (w.split == 0) write_trivial_rows<float, D>(p, w);
@@ -548,6 +554,8 @@ __global__ void __launch_bounds__(128)
 combine_kernel(const DecodeParams p) {
   constexpr int PER = D / 32;
   const int lane = threadIdx.x & 31;
+  pdl_launch_dependents();
+  pdl_wait_prior();
   const int64_t item = static_cast<int64_t>(blockIdx.x) * 4 + (threadIdx.x >> 5);
   if (item >= static_cast<int64_t>(p.num_seqs) * p.num_q_heads) return;
   const int b = static_cast<int>(item / p.num_q_heads);
@@ -587,11 +595,19 @@ cudaError_t launch16(const CUtensorMap& kmap, const CUtensorMap& vmap, const Dec
                      cudaStream_t stream) {
   auto kern = decode16_kernel<T, D, NT>;
   const int smem = Tile16<D>::kSmemBytes;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  // the shared-memory opt-in is per device; set it once for each
+  static std::atomic<uint64_t> configured{0};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
+  const uint64_t bit = dev < 64 ? (uint64_t(1) << dev) : 0;
+  if (!bit || !(configured.load(std::memory_order_acquire) & bit)) {
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    configured.fetch_or(bit, std::memory_order_acq_rel);
+  }
   dim3 grid(p.num_splits, p.num_kv_heads * p.num_head_chunks, p.num_seqs);
-  kern<<<grid, kThreads, smem, stream>>>(kmap, vmap, p);
-  return cudaGetLastError();
+  return launch_pdl(kern, grid, dim3(kThreads), smem, stream, kmap, vmap, p);
 }
 
 }  // namespace
@@ -625,26 +641,27 @@ cudaError_t launch_decode_16bit(int dtype, int head_dim, int ntiles, const CUten
 cudaError_t launch_decode_f32(int head_dim, const DecodeParams& p, cudaStream_t stream) {
   dim3 grid(p.num_splits, p.num_kv_heads * p.num_head_chunks, p.num_seqs);
   if (head_dim == 128)
-    decode_f32_kernel<128><<<grid, kThreads, 0, stream>>>(p);
-  else
-    decode_f32_kernel<64><<<grid, kThreads, 0, stream>>>(p);
-  return cudaGetLastError();
+    return launch_pdl(decode_f32_kernel<128>, grid, dim3(kThreads), 0, stream, p);
+  return launch_pdl(decode_f32_kernel<64>, grid, dim3(kThreads), 0, stream, p);
 }
 
 cudaError_t launch_combine(int dtype, int head_dim, const DecodeParams& p, cudaStream_t stream) {
   const int64_t items = static_cast<int64_t>(p.num_seqs) * p.num_q_heads;
   if (items == 0) return cudaSuccess;
   const unsigned blocks = static_cast<unsigned>((items + 3) / 4);
-#define PKV_COMBINE(T, D) combine_kernel<T, D><<<blocks, 128, 0, stream>>>(p)
+#define PKV_COMBINE(T, D) \
+  return launch_pdl(combine_kernel<T, D>, dim3(blocks), dim3(128), 0, stream, p)
   if (dtype == 0) {
-    if (head_dim == 128) PKV_COMBINE(float, 128); else PKV_COMBINE(float, 64);
-  } else if (dtype == 1) {
-    if (head_dim == 128) PKV_COMBINE(__half, 128); else PKV_COMBINE(__half, 64);
-  } else {
-    if (head_dim == 128) PKV_COMBINE(__nv_bfloat16, 128); else PKV_COMBINE(__nv_bfloat16, 64);
+    if (head_dim == 128) PKV_COMBINE(float, 128);
+    PKV_COMBINE(float, 64);
   }
+  if (dtype == 1) {
+    if (head_dim == 128) PKV_COMBINE(__half, 128);
+    PKV_COMBINE(__half, 64);
+  }
+  if (head_dim == 128) PKV_COMBINE(__nv_bfloat16, 128);
+  PKV_COMBINE(__nv_bfloat16, 64);
 #undef PKV_COMBINE
-  return cudaGetLastError();
 }
 
 }  // namespace pkv

@@ -5,6 +5,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <utility>
+
 namespace pkv {
 
 // Tokens per work unit: one 16-row MMA tile of the context.
@@ -39,6 +41,26 @@ __host__ __device__ __forceinline__ void unit_range(int L, int window, int* firs
 
 __host__ __device__ __forceinline__ int splits_for(int n_units, int units_per_split) {
   return (n_units + units_per_split - 1) / units_per_split;
+}
+
+// Launch `kernel` so that it may be scheduled while the previous kernel in
+// the stream finishes (programmatic stream serialisation).  Every kernel of
+// this library calls pdl_wait_prior() before it reads global memory, so the
+// overlap only hides launch latency.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                       cudaStream_t stream, Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
 }
 
 struct DecodeParams {
