@@ -148,12 +148,13 @@ int make_plan(int num_seqs, int num_q_heads, const pkv_cache_layout* L, int max_
     ups = tokens_per_split / pkv::kUnitTokens;
     if (ups > max_ups) return PKV_ERR_UNSUPPORTED;
   } else {
-    // 512-token splits by default; shorten them (down to 128 tokens) while
-    // the grid would not give every SM several CTAs.
+    // Long splits cost the least per byte (each CTA pays its pipeline fill
+    // and merge once): start at 2048 tokens and halve (down to 128) only
+    // while the grid would give the SMs fewer than 4 CTAs each.
     if (num_sms <= 0) num_sms = 148;
     const int64_t pairs = static_cast<int64_t>(num_seqs) * L->num_kv_heads * plan->num_head_chunks;
-    const int64_t target = static_cast<int64_t>(num_sms) * 8;
-    ups = 32;
+    const int64_t target = static_cast<int64_t>(num_sms) * 4;
+    ups = max_ups;
     while (ups > 8 && pairs * ((max_units + ups - 1) / ups) < target) ups /= 2;
   }
   int64_t ns = (max_units + ups - 1) / ups;

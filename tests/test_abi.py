@@ -97,10 +97,11 @@ def test_slot_mapping_argument_checks(pkv_lib):
 
 @pytest.mark.parametrize("cfg,expect", [
     # (num_seqs, hq, layout args, max_blocks, window) -> (tokens_per_split, num_splits)
-    ((64, 32, (10000, 32, 16, 128, 1), 256, 0), (512, 8)),
-    ((256, 32, (44000, 8, 32, 128, 2), 256, 0), (512, 16)),
-    ((16, 32, (30000, 8, 16, 128, 2), 2048, 4096), (256, 17)),
+    ((64, 32, (10000, 32, 16, 128, 1), 256, 0), (2048, 2)),
+    ((256, 32, (44000, 8, 32, 128, 2), 256, 0), (2048, 4)),
+    ((16, 32, (30000, 8, 16, 128, 2), 2048, 4096), (1024, 5)),
     ((4, 8, (32, 8, 16, 64, 0), 7, 0), (128, 1)),
+    ((1, 8, (4096, 8, 16, 128, 1), 2048, 0), (256, 128)),
 ])
 def test_plan(pkv_lib, cfg, expect):
     B, hq, lay, mb, window = cfg

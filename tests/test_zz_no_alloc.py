@@ -79,7 +79,7 @@ def test_noalloc_matches_allocating_decode_twice(pkv_lib, dtype, window):
 def test_noalloc_rejects_problems_beyond_its_scratch(pkv_lib):
     pkv = pkv_lib
     fn = _noalloc_fn(pkv)
-    B, hq, hkv, d, bs, mb = 1024, 32, 8, 128, 16, 130
+    B, hq, hkv, d, bs, mb = 1024, 32, 8, 128, 16, 300
     q = torch.zeros(B, hq, d, dtype=torch.float16, device="cuda")
     out = torch.zeros_like(q)
     kc = torch.zeros(4, hkv, bs, d, dtype=torch.float16, device="cuda")
