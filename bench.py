@@ -423,44 +423,31 @@ def main(argv=None):
 
 
 def run_e2e(pkv, w, spec, args, sbytes, pg, world):
-    """Same step through the public API with per-step host<->device copies:
-    q, the new K/V, positions, lengths and block tables in from pinned host
-    memory, the attention output back out, the host waiting for it."""
+    """Same step through the public API (DecodeStep) with host buffers: every
+    step copies its staged inputs -- q, the new K/V, positions, lengths and the
+    block tables -- from pinned host memory to the device, replays slot
+    mapping + append + decode as one CUDA graph, copies the attention output
+    back, and the host waits for it."""
     S = w.steps
-    stream = torch.cuda.current_stream()
-    host = []
+    step = pkv.DecodeStep(w.k_cache, w.v_cache, spec.num_seqs, spec.num_q_heads, w.max_blocks,
+                          spec.window, w.scale, copy_block_tables=True, num_buffers=S)
     for s in range(S):
-        host.append({k: t.cpu().pin_memory() for k, t in (
-            ("q", w.q_steps[s]), ("k", w.k_steps[s]), ("v", w.v_steps[s]),
-            ("pos", w.pos_steps[s]), ("lens", w.lens_steps[s]), ("bt", w.block_tables))})
-    dev = {k: torch.empty_like(t, device="cuda") for k, t in host[0].items()}
-    out_h = torch.empty(w.q_steps[0].shape, dtype=spec.dtype).pin_memory()
-    h2d = sum(t.numel() * t.element_size() for t in host[0].values())
-    d2h = out_h.numel() * out_h.element_size()
-
-    def step(s):
-        h = host[s % S]
-        for k in dev:
-            dev[k].copy_(h[k], non_blocking=True)
-        slots = pkv.pkv_slot_mapping(dev["bt"], dev["pos"], spec.block_size)
-        pkv.pkv_append(dev["k"], dev["v"], slots, w.k_cache, w.v_cache)
-        o = pkv.pkv_decode(dev["q"], w.k_cache, w.v_cache, dev["bt"], dev["lens"], spec.window,
-                           w.scale)
-        out_h.copy_(o, non_blocking=True)
-        stream.synchronize()  # the caller needs the result before its next step
-
+        h = step.host[s]
+        h["q"].copy_(w.q_steps[s])
+        h["k"].copy_(w.k_steps[s])
+        h["v"].copy_(w.v_steps[s])
+        h["positions"].copy_(w.pos_steps[s])
+        h["context_lens"].copy_(w.lens_steps[s])
+        h["block_tables"].copy_(w.block_tables)
     for s in range(args.warmup):
-        step(s)
+        step.run(s % S)
     if pg:
         pg.barrier()
     torch.cuda.synchronize()
-    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    a.record(stream)
+    t0 = time.perf_counter()
     for s in range(args.steps):
-        step(s)
-    b.record(stream)
-    torch.cuda.synchronize()
-    ms = a.elapsed_time(b)
+        step.run(s % S)
+    ms = (time.perf_counter() - t0) * 1e3
     my_bytes = sum(sbytes[s % S]["step"] for s in range(args.steps))
     t = torch.tensor([ms, my_bytes], dtype=torch.float64)
     if pg:
@@ -471,7 +458,8 @@ def run_e2e(pkv, w, spec, args, sbytes, pg, world):
     return {"value": my_bytes / (ms * 1e-3) / 1e9, "unit": "GB/s",
             "tokens_per_s": world * spec.num_seqs * args.steps / (ms * 1e-3),
             "ms_per_step": ms / args.steps,
-            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+            "h2d_bytes_per_step": step.h2d_bytes, "d2h_bytes_per_step": step.d2h_bytes,
+            "api": "DecodeStep (one CUDA graph per step, host waits each step)"}
 
 
 if __name__ == "__main__":

@@ -124,11 +124,14 @@ int pkv_append(const void* k, const void* v, const int64_t* slot_mapping, int64_
  *   context length outside [0, max_blocks_per_seq * bs] makes that
  *   sequence's output rows NaN.
  *   Long contexts are split across CTAs (flash-decoding); the partial
- *   results go to a workspace the library allocates per (device, stream) on
- *   first use and grows when a larger problem arrives (growth synchronises
- *   `stream`).  Issue the largest call once before capturing a CUDA graph.
- *   Calls on one stream share that stream's workspace and are ordered by the
- *   stream; calls on different streams never share one.
+ *   results go to a workspace the library allocates (cudaMalloc) per
+ *   (device, stream) on first use and replaces with a larger one when a
+ *   larger problem arrives; outgrown buffers stay allocated (queued work or a
+ *   captured CUDA graph may still use them) until pkv_release_workspaces.
+ *   Issue the largest call once before capturing a CUDA graph, so that no
+ *   allocation happens during capture.  Calls on one stream share that
+ *   stream's workspace and are ordered by the stream; calls on different
+ *   streams never share one.
  */
 int pkv_decode(const void* q, int32_t num_seqs, int32_t num_q_heads,
                const void* k_cache, const void* v_cache, const pkv_cache_layout* layout,
@@ -194,8 +197,10 @@ int pkv_decode_noalloc(const void* q, int32_t num_seqs, int32_t num_q_heads,
 const char* pkv_status_string(int status);
 
 /*
- * pkv_release_workspaces -- free every split-K workspace the library holds.
- * Synchronises the device; call it only when no pkv_decode is in flight.
+ * pkv_release_workspaces -- free every split-K workspace the library holds,
+ * outgrown ones included.  Synchronises the device; call it only when no
+ * pkv_decode is in flight and no captured graph that contains one will run
+ * again.
  */
 int pkv_release_workspaces(void);
 

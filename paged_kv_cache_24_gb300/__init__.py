@@ -10,6 +10,9 @@ Public API (thin wrappers over the C ABI of ``libpkv.so``, see include/pkv.h):
   out)`` -- single-query attention over each sequence's paged context,
   optionally limited to a sliding window.
 
+``DecodeStep`` packages one serving step (slot mapping, append, decode) as a
+CUDA graph fed from a pinned host staging buffer.
+
 All tensors live on the GPU; PyTorch provides the memory and the stream.
 ``workloads`` builds the seeded synthetic inputs used by the tests and the
 benchmark.
@@ -17,9 +20,10 @@ benchmark.
 from ._binding import (CacheLayout, PkvError, cache_layout, library_path, load_library,
                        pkv_append, pkv_decode, pkv_decode_plan, pkv_release_workspaces,
                        pkv_slot_mapping, status_string)
+from .step import DecodeStep
 
 __all__ = [
-    "CacheLayout", "PkvError", "cache_layout", "library_path", "load_library", "pkv_append",
+    "DecodeStep", "CacheLayout", "PkvError", "cache_layout", "library_path", "load_library", "pkv_append",
     "pkv_decode", "pkv_decode_plan", "pkv_release_workspaces", "pkv_slot_mapping",
     "status_string",
 ]

@@ -6,6 +6,7 @@
 #include <map>
 #include <mutex>
 #include <utility>
+#include <vector>
 
 #include "pkv.h"
 #include "pkv_internal.h"
@@ -47,29 +48,27 @@ int to_status(cudaError_t e) {
 struct Workspace {
   void* ptr = nullptr;
   size_t bytes = 0;
+  std::vector<void*> retired;  // outgrown buffers, kept until pkv_release_workspaces
 };
 std::mutex g_ws_mutex;
 std::map<std::pair<int, cudaStream_t>, Workspace> g_ws;
 
+// The stream's workspace, grown to `need` bytes.  An outgrown buffer is not
+// freed: work already queued (or captured into a CUDA graph) may still use
+// it, so it is retired and released only by pkv_release_workspaces.
 int get_workspace(int device, cudaStream_t stream, size_t need, void** out) {
   std::lock_guard<std::mutex> lock(g_ws_mutex);
   Workspace& ws = g_ws[{device, stream}];
   if (ws.bytes < need) {
-    if (ws.ptr) {
-      // earlier calls on this stream may still read the old buffer
-      cudaError_t e = cudaStreamSynchronize(stream);
-      if (e != cudaSuccess) return to_status(e);
-      cudaFree(ws.ptr);
-      ws.ptr = nullptr;
-      ws.bytes = 0;
-    }
     size_t bytes = need < (size_t(1) << 20) ? (size_t(1) << 20) : need;
-    cudaError_t e = cudaMalloc(&ws.ptr, bytes);
+    void* fresh = nullptr;
+    cudaError_t e = cudaMalloc(&fresh, bytes);
     if (e != cudaSuccess) {
-      cudaGetLastError();  // clear the sticky-free allocation error
-      ws.ptr = nullptr;
+      cudaGetLastError();  // clear the allocation error so later calls are unaffected
       return PKV_ERR_NOMEM;
     }
+    if (ws.ptr) ws.retired.push_back(ws.ptr);
+    ws.ptr = fresh;
     ws.bytes = bytes;
   }
   *out = ws.ptr;
@@ -360,15 +359,14 @@ int pkv_release_workspaces(void) {
   std::lock_guard<std::mutex> lock(g_ws_mutex);
   int rc = PKV_OK;
   if (!g_ws.empty() && cudaDeviceSynchronize() != cudaSuccess) rc = PKV_ERR_CUDA;
+  int prev = 0;
+  cudaGetDevice(&prev);
   for (auto& kv : g_ws) {
-    if (kv.second.ptr) {
-      int prev = 0;
-      cudaGetDevice(&prev);
-      cudaSetDevice(kv.first.first);
-      cudaFree(kv.second.ptr);
-      cudaSetDevice(prev);
-    }
+    cudaSetDevice(kv.first.first);
+    if (kv.second.ptr) cudaFree(kv.second.ptr);
+    for (void* r : kv.second.retired) cudaFree(r);
   }
+  cudaSetDevice(prev);
   g_ws.clear();
   return rc;
 }

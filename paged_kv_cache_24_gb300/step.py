@@ -1,0 +1,112 @@
+"""DecodeStep: one serving decode step (slot mapping, append, decode) as a
+replayable CUDA graph fed from pinned host memory.
+
+A step's host inputs -- the queries, the new tokens' K and V, their positions,
+the context lengths and (optionally) the block tables -- are packed into one
+pinned staging buffer and reach the device in a single copy; the attention
+output comes back in another.  Between them the graph replays
+``pkv_slot_mapping``, ``pkv_append`` and ``pkv_decode`` exactly as the eager
+calls would run them.  The K/V pools stay resident on the device.
+
+Several staging buffers can be kept (``num_buffers``), one graph each, so a
+caller can fill the next step's inputs while the current one runs.
+
+Usage::
+
+    step = DecodeStep(k_cache, v_cache, num_seqs, num_q_heads, max_blocks,
+                      window=0, scale=1 / math.sqrt(head_dim))
+    step.host[0]["q"].copy_(q_cpu); step.host[0]["k"].copy_(k_cpu); ...
+    out_cpu = step.run(0)          # waits for the result
+"""
+from __future__ import annotations
+
+import torch
+
+from ._binding import cache_layout, pkv_append, pkv_decode, pkv_slot_mapping
+
+_ALIGN = 256
+
+
+class DecodeStep:
+    def __init__(self, k_cache: torch.Tensor, v_cache: torch.Tensor, num_seqs: int,
+                 num_q_heads: int, max_blocks: int, window: int, scale: float,
+                 copy_block_tables: bool = True, num_buffers: int = 1, use_graph: bool = True):
+        layout = cache_layout(k_cache)
+        self.k_cache, self.v_cache = k_cache, v_cache
+        self.window, self.scale = int(window), float(scale)
+        self.block_size = layout.block_size
+        dt, dev = k_cache.dtype, k_cache.device
+        B, hq, hkv, d = num_seqs, num_q_heads, layout.num_kv_heads, layout.head_dim
+        shapes = {
+            "q": ((B, hq, d), dt), "k": ((B, hkv, d), dt), "v": ((B, hkv, d), dt),
+            "positions": ((B,), torch.int64), "context_lens": ((B,), torch.int32),
+            "block_tables": ((B, max_blocks), torch.int32),
+        }
+        offsets, cur = {}, 0
+        for name, (shape, t) in shapes.items():
+            n = 1
+            for s in shape:
+                n *= s
+            nbytes = n * torch.tensor([], dtype=t).element_size()
+            offsets[name] = (cur, nbytes, shape, t)
+            cur += (nbytes + _ALIGN - 1) // _ALIGN * _ALIGN
+        # block tables sit last so that leaving them out shortens the copy
+        self._staged_bytes = cur if copy_block_tables else offsets["block_tables"][0]
+
+        def views(buf):
+            return {name: buf[o:o + nb].view(t).view(shape)
+                    for name, (o, nb, shape, t) in offsets.items()}
+
+        self._host_bufs = [torch.empty(cur, dtype=torch.uint8).pin_memory()
+                           for _ in range(num_buffers)]
+        self.host = [views(b) for b in self._host_bufs]   # fill these, then run(i)
+        self._dev_buf = torch.empty(cur, dtype=torch.uint8, device=dev)
+        self.device = views(self._dev_buf)
+        self.slots = torch.empty(B, dtype=torch.int64, device=dev)
+        self.out = torch.empty((B, hq, d), dtype=dt, device=dev)
+        self.host_out = torch.empty((B, hq, d), dtype=dt).pin_memory()
+        self.h2d_bytes = self._staged_bytes
+        self.d2h_bytes = self.host_out.numel() * self.host_out.element_size()
+        self.stream = torch.cuda.Stream(device=dev)
+        self.graphs = None
+        if use_graph:
+            # an eager pass with empty contexts and no writes sizes the decode
+            # workspace before capture
+            for h in self.host:
+                h["context_lens"].zero_()
+                h["positions"].fill_(-1)
+            self.stream.wait_stream(torch.cuda.current_stream(dev))
+            with torch.cuda.stream(self.stream):
+                self._enqueue(0)
+            self.stream.synchronize()
+            self.graphs = []
+            for i in range(num_buffers):
+                g = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(g, stream=self.stream):
+                    self._enqueue(i)
+                self.graphs.append(g)
+
+    def _enqueue(self, i):
+        n = self._staged_bytes
+        self._dev_buf[:n].copy_(self._host_bufs[i][:n], non_blocking=True)
+        dv = self.device
+        pkv_slot_mapping(dv["block_tables"], dv["positions"], self.block_size, out=self.slots)
+        pkv_append(dv["k"], dv["v"], self.slots, self.k_cache, self.v_cache)
+        pkv_decode(dv["q"], self.k_cache, self.v_cache, dv["block_tables"], dv["context_lens"],
+                   self.window, self.scale, out=self.out)
+        self.host_out.copy_(self.out, non_blocking=True)
+
+    def run(self, i: int = 0, wait: bool = True) -> torch.Tensor:
+        """Copy staging buffer i in, run the step, copy the output back."""
+        caller = torch.cuda.current_stream(self.stream.device)
+        self.stream.wait_stream(caller)   # after whatever the caller queued on the pools
+        with torch.cuda.stream(self.stream):
+            if self.graphs is not None:
+                self.graphs[i].replay()
+            else:
+                self._enqueue(i)
+        if wait:
+            self.stream.synchronize()
+        else:
+            caller.wait_stream(self.stream)
+        return self.host_out
