@@ -271,6 +271,8 @@ def main(argv=None):
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--path", default="fused", choices=["fused", "separate"],
+                    help="fused: pkv_append_decode (one launch); separate: pkv_append + pkv_decode")
     ap.add_argument("--num-seqs", type=int, default=0,
                     help="profiling only: shrink the workload's batch (not a bench line)")
     args = ap.parse_args(argv)
@@ -305,13 +307,25 @@ def main(argv=None):
     out = torch.empty_like(w.q_steps[0])
     plan = pkv.pkv_decode_plan(spec.num_seqs, spec.num_q_heads, pkv.cache_layout(w.k_cache),
                                w.max_blocks, spec.window)
-    launches_per_step = 2 + (1 if plan[1] > 1 else 0)
+    fused = args.path == "fused"
+    launches_per_step = (1 if fused else 2) + (1 if plan[1] > 1 else 0)
+
+    def do_append(i):
+        if not fused:
+            pkv.pkv_append(w.k_steps[i], w.v_steps[i], slots[i], w.k_cache, w.v_cache)
+
+    def do_decode(i):
+        if fused:
+            pkv.pkv_append_decode(w.q_steps[i], w.k_steps[i], w.v_steps[i], w.k_cache,
+                                  w.v_cache, w.block_tables, lens[i], spec.window, w.scale,
+                                  out=out)
+        else:
+            pkv.pkv_decode(w.q_steps[i], w.k_cache, w.v_cache, w.block_tables, lens[i],
+                           spec.window, w.scale, out=out)
 
     def step(s):
-        i = s % S
-        pkv.pkv_append(w.k_steps[i], w.v_steps[i], slots[i], w.k_cache, w.v_cache)
-        pkv.pkv_decode(w.q_steps[i], w.k_cache, w.v_cache, w.block_tables, lens[i],
-                       spec.window, w.scale, out=out)
+        do_append(s % S)
+        do_decode(s % S)
 
     kv_per_step = statistics.mean(b["kv"] for b in sbytes)
     need_flush = kv_per_step < 4 * L2_BYTES
@@ -336,10 +350,9 @@ def main(argv=None):
                 flush_buf.add_(1)  # evict the previous step's working set from L2
             i = s % S
             ev[s][0].record(stream)
-            pkv.pkv_append(w.k_steps[i], w.v_steps[i], slots[i], w.k_cache, w.v_cache)
+            do_append(i)
             ev[s][1].record(stream)
-            pkv.pkv_decode(w.q_steps[i], w.k_cache, w.v_cache, w.block_tables, lens[i],
-                           spec.window, w.scale, out=out)
+            do_decode(i)
             ev[s][2].record(stream)
         t_end.record(stream)
         torch.cuda.synchronize()
@@ -351,7 +364,8 @@ def main(argv=None):
     # the step time: whole loop / K when nothing else ran in it, else the sum of steps
     total_ms = sum(step_ms) if need_flush else loop_ms
     my_bytes = sum(sbytes[s % S]["step"] for s in range(args.steps))
-    my_dec_bytes = sum(sbytes[s % S]["decode"] for s in range(args.steps))
+    dec_key = "step" if fused else "decode"  # the fused launch also does the append
+    my_dec_bytes = sum(sbytes[s % S][dec_key] for s in range(args.steps))
 
     t = torch.tensor([total_ms, my_bytes, sum(dec_ms), my_dec_bytes], dtype=torch.float64)
     if pg:
@@ -405,7 +419,10 @@ def main(argv=None):
             },
             "tokens_per_s": tokens_per_s,
             "pct_of_hbm_peak": 100.0 * value / (world * peak),
-            "roofline": {"bound": "hbm", "kernel": "decode (split-K decode + LSE combine)",
+            "path": args.path,
+            "roofline": {"bound": "hbm",
+                         "kernel": ("fused append + decode (split-K) + LSE combine" if fused
+                                    else "decode (split-K decode + LSE combine)"),
                          "achieved": achieved, "peak": peak, "unit": "GB/s",
                          "frac": achieved / peak, "peak_kind": peak_kind,
                          "traffic": traffic,
@@ -430,7 +447,8 @@ def run_e2e(pkv, w, spec, args, sbytes, pg, world):
     back, and the host waits for it."""
     S = w.steps
     step = pkv.DecodeStep(w.k_cache, w.v_cache, spec.num_seqs, spec.num_q_heads, w.max_blocks,
-                          spec.window, w.scale, copy_block_tables=True, num_buffers=S)
+                          spec.window, w.scale, copy_block_tables=True, num_buffers=S,
+                          fused=args.path == "fused")
     for s in range(S):
         h = step.host[s]
         h["q"].copy_(w.q_steps[s])

@@ -153,6 +153,28 @@ int pkv_decode_split(const void* q, int32_t num_seqs, int32_t num_q_heads,
                      int32_t tokens_per_split, void* stream);
 
 /*
+ * pkv_append_decode -- one decode step in one launch: pkv_append of every
+ * sequence's new token, then pkv_decode, fused.
+ *   ("Build a Paged KV Cache in Pure Python", Step 5: append the new token,
+ *   then attend, so it attends to itself.)
+ *   The new token of sequence b sits at position L - 1, L = context_lens[b]
+ *   (the length after the append): its K and V rows, k_new[b][h][:] and
+ *   v_new[b][h][:] ([num_seqs][num_kv_heads][head_dim], layout->dtype), are
+ *   written to row (L-1) % bs of block block_tables[b][(L-1) / bs] and used
+ *   for that position.  Sequences with L == 0 have no new token.  The pools and
+ *   the output end up bit-identical to pkv_slot_mapping(positions = L - 1) +
+ *   pkv_append + pkv_decode_split with the same tokens_per_split.
+ *   Precondition: no other sequence of the call reads the block that receives
+ *   a sequence's new token (true whenever the block holding a sequence's
+ *   last position is private to it); otherwise use the separate calls.
+ */
+int pkv_append_decode(const void* q, const void* k_new, const void* v_new, int32_t num_seqs,
+                      int32_t num_q_heads, void* k_cache, void* v_cache,
+                      const pkv_cache_layout* layout, const int32_t* block_tables,
+                      int32_t max_blocks_per_seq, const int32_t* context_lens, int32_t window,
+                      float scale, void* out, int32_t tokens_per_split, void* stream);
+
+/*
  * pkv_decode_plan -- the split pkv_decode_split would use (host only, no GPU
  * work).  num_sms: streaming multiprocessors to plan for (<= 0: query the
  * current device).  Writes the tokens per split and the number of splits

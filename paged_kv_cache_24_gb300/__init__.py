@@ -8,7 +8,9 @@ Public API (thin wrappers over the C ABI of ``libpkv.so``, see include/pkv.h):
   tokens' K/V into their slots;
 * ``pkv_decode(q, k_cache, v_cache, block_tables, context_lens, window, scale,
   out)`` -- single-query attention over each sequence's paged context,
-  optionally limited to a sliding window.
+  optionally limited to a sliding window;
+* ``pkv_append_decode(q, k_new, v_new, k_cache, v_cache, block_tables,
+  context_lens, window, scale)`` -- both in one launch.
 
 ``DecodeStep`` packages one serving step (slot mapping, append, decode) as a
 CUDA graph fed from a pinned host staging buffer.
@@ -18,12 +20,13 @@ All tensors live on the GPU; PyTorch provides the memory and the stream.
 benchmark.
 """
 from ._binding import (CacheLayout, PkvError, cache_layout, library_path, load_library,
-                       pkv_append, pkv_decode, pkv_decode_plan, pkv_release_workspaces,
+                       pkv_append, pkv_append_decode, pkv_decode, pkv_decode_plan, pkv_release_workspaces,
                        pkv_slot_mapping, status_string)
 from .step import DecodeStep
 
 __all__ = [
     "DecodeStep", "CacheLayout", "PkvError", "cache_layout", "library_path", "load_library", "pkv_append",
+    "pkv_append_decode",
     "pkv_decode", "pkv_decode_plan", "pkv_release_workspaces", "pkv_slot_mapping",
     "status_string",
 ]

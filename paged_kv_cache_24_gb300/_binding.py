@@ -61,6 +61,8 @@ def load_library():
             "pkv_append": [vp, vp, vp, i64, vp, vp, lay, vp],
             "pkv_decode": [vp, i32, i32, vp, vp, lay, vp, i32, vp, i32, f32, vp, vp],
             "pkv_decode_split": [vp, i32, i32, vp, vp, lay, vp, i32, vp, i32, f32, vp, i32, vp],
+            "pkv_append_decode": [vp, vp, vp, i32, i32, vp, vp, lay, vp, i32, vp, i32, f32, vp,
+                                  i32, vp],
             "pkv_decode_plan": [i32, i32, lay, i32, i32, i32, i32, ctypes.POINTER(i32),
                                 ctypes.POINTER(i32)],
             "pkv_release_workspaces": [],
@@ -178,6 +180,41 @@ def pkv_decode(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
         _ptr(q), B, Hq, _ptr(k_cache), _ptr(v_cache), ctypes.byref(layout),
         _ptr(block_tables), block_tables.shape[1], _ptr(context_lens), int(window),
         float(scale), _ptr(out), int(tokens_per_split), _stream(stream)))
+    return out
+
+
+def pkv_append_decode(q: torch.Tensor, k_new: torch.Tensor, v_new: torch.Tensor,
+                      k_cache: torch.Tensor, v_cache: torch.Tensor, block_tables: torch.Tensor,
+                      context_lens: torch.Tensor, window: int, scale: float,
+                      out: torch.Tensor | None = None, tokens_per_split: int = 0,
+                      stream=None) -> torch.Tensor:
+    """Append each sequence's new token (at position context_lens[b] - 1) and
+    decode, in one launch; same result as the separate calls."""
+    _on_cuda(q, k_new, v_new, k_cache, v_cache, block_tables, context_lens, out)
+    layout = cache_layout(k_cache)
+    _require(v_cache.shape == k_cache.shape and v_cache.dtype == k_cache.dtype
+             and v_cache.is_contiguous(), "v_cache must match k_cache")
+    _require(q.dim() == 3 and q.shape[2] == layout.head_dim and q.is_contiguous()
+             and q.dtype == k_cache.dtype, "q must be contiguous [B, Hq, D] of the cache dtype")
+    B, Hq, D = q.shape
+    shape = (B, layout.num_kv_heads, layout.head_dim)
+    _require(tuple(k_new.shape) == shape and tuple(v_new.shape) == shape
+             and k_new.dtype == q.dtype and v_new.dtype == q.dtype
+             and k_new.is_contiguous() and v_new.is_contiguous(),
+             f"k_new and v_new must be contiguous {shape} of the cache dtype")
+    _require(block_tables.dtype == torch.int32 and block_tables.dim() == 2
+             and block_tables.shape[0] == B and block_tables.is_contiguous(),
+             "block_tables must be contiguous int32 [B, MB]")
+    _require(context_lens.dtype == torch.int32 and context_lens.numel() == B
+             and context_lens.is_contiguous(), "context_lens must be int32 [B]")
+    if out is None:
+        out = torch.empty_like(q)
+    _require(out.shape == q.shape and out.dtype == q.dtype and out.is_contiguous(),
+             "out must be contiguous and shaped like q")
+    _check("pkv_append_decode", load_library().pkv_append_decode(
+        _ptr(q), _ptr(k_new), _ptr(v_new), B, Hq, _ptr(k_cache), _ptr(v_cache),
+        ctypes.byref(layout), _ptr(block_tables), block_tables.shape[1], _ptr(context_lens),
+        int(window), float(scale), _ptr(out), int(tokens_per_split), _stream(stream)))
     return out
 
 

@@ -182,6 +182,82 @@ int check_decode_args(const void* q, int32_t num_seqs, int32_t num_q_heads, cons
   return PKV_OK;
 }
 
+// pkv_decode_split, optionally with the fused append of each sequence's token
+// at position context_lens[b] - 1 (k_new / v_new non-null).
+int decode_impl(const void* q, const void* k_new, const void* v_new, int32_t num_seqs,
+                int32_t num_q_heads, const void* k_cache, const void* v_cache,
+                const pkv_cache_layout* layout, const int32_t* block_tables,
+                int32_t max_blocks_per_seq, const int32_t* context_lens, int32_t window,
+                float scale, void* out, int32_t tokens_per_split, void* stream) {
+  int rc = check_decode_args(q, num_seqs, num_q_heads, k_cache, v_cache, layout, block_tables,
+                             max_blocks_per_seq, context_lens, out);
+  if (rc != PKV_OK) return rc;
+  if (tokens_per_split < 0 || tokens_per_split % pkv::kUnitTokens != 0) return PKV_ERR_SHAPE;
+  if (tokens_per_split > 32 * pkv::kDecodeWarps * pkv::kUnitTokens) return PKV_ERR_UNSUPPORTED;
+  if (num_seqs == 0) return PKV_OK;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+
+  int device = 0;
+  if (cudaGetDevice(&device) != cudaSuccess) return PKV_ERR_CUDA;
+  Plan plan;
+  rc = make_plan(num_seqs, num_q_heads, layout, max_blocks_per_seq, window, tokens_per_split,
+                 sm_count_of_current_device(), &plan);
+  if (rc != PKV_OK) return rc;
+
+  DecodeParams p{};
+  p.q = q;
+  p.out = out;
+  p.k_cache = k_cache;
+  p.v_cache = v_cache;
+  p.block_tables = block_tables;
+  p.context_lens = context_lens;
+  p.k_new = k_new;
+  p.v_new = v_new;
+  p.k_dst = const_cast<void*>(k_cache);
+  p.v_dst = const_cast<void*>(v_cache);
+  p.num_blocks = layout->num_blocks;
+  p.num_seqs = num_seqs;
+  p.num_q_heads = num_q_heads;
+  p.num_kv_heads = layout->num_kv_heads;
+  p.group = num_q_heads / layout->num_kv_heads;
+  p.head_chunk = plan.head_chunk;
+  p.num_head_chunks = plan.num_head_chunks;
+  p.max_blocks = max_blocks_per_seq;
+  p.block_size = layout->block_size;
+  p.window = window;
+  p.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
+  p.units_per_split = plan.units_per_split;
+  p.num_splits = plan.num_splits;
+
+  if (plan.num_splits > 1) {
+    const size_t rows = static_cast<size_t>(num_seqs) * num_q_heads * plan.num_splits;
+    const size_t o_bytes = rows * layout->head_dim * sizeof(float);
+    void* ws = nullptr;
+    rc = get_workspace(device, st, o_bytes + rows * sizeof(float2), &ws);
+    if (rc != PKV_OK) return rc;
+    p.part_o = static_cast<float*>(ws);
+    p.part_ml = reinterpret_cast<float2*>(static_cast<char*>(ws) + o_bytes);
+  }
+
+  cudaError_t e;
+  if (layout->dtype == PKV_FLOAT32) {
+    e = pkv::launch_decode_f32(layout->head_dim, p, st);
+  } else {
+    CUtensorMap kmap, vmap;
+    rc = encode_pool_map(&kmap, k_cache, layout);
+    if (rc != PKV_OK) return rc;
+    rc = encode_pool_map(&vmap, v_cache, layout);
+    if (rc != PKV_OK) return rc;
+    e = pkv::launch_decode_16bit(layout->dtype, layout->head_dim, plan.ntiles, kmap, vmap, p, st);
+  }
+  if (e != cudaSuccess) return to_status(e);
+  if (plan.num_splits > 1) {
+    e = pkv::launch_combine(layout->dtype, layout->head_dim, p, st);
+    if (e != cudaSuccess) return to_status(e);
+  }
+  return PKV_OK;
+}
+
 }  // namespace
 
 namespace pkv {
@@ -282,69 +358,23 @@ int pkv_decode_split(const void* q, int32_t num_seqs, int32_t num_q_heads,
                      const int32_t* block_tables, int32_t max_blocks_per_seq,
                      const int32_t* context_lens, int32_t window, float scale, void* out,
                      int32_t tokens_per_split, void* stream) {
-  int rc = check_decode_args(q, num_seqs, num_q_heads, k_cache, v_cache, layout, block_tables,
-                             max_blocks_per_seq, context_lens, out);
-  if (rc != PKV_OK) return rc;
-  if (tokens_per_split < 0 || tokens_per_split % pkv::kUnitTokens != 0) return PKV_ERR_SHAPE;
-  if (tokens_per_split > 32 * pkv::kDecodeWarps * pkv::kUnitTokens) return PKV_ERR_UNSUPPORTED;
-  if (num_seqs == 0) return PKV_OK;
-  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  return decode_impl(q, nullptr, nullptr, num_seqs, num_q_heads, k_cache, v_cache, layout,
+                     block_tables, max_blocks_per_seq, context_lens, window, scale, out,
+                     tokens_per_split, stream);
+}
 
-  int device = 0;
-  if (cudaGetDevice(&device) != cudaSuccess) return PKV_ERR_CUDA;
-  Plan plan;
-  rc = make_plan(num_seqs, num_q_heads, layout, max_blocks_per_seq, window, tokens_per_split,
-                 sm_count_of_current_device(), &plan);
-  if (rc != PKV_OK) return rc;
-
-  DecodeParams p{};
-  p.q = q;
-  p.out = out;
-  p.k_cache = k_cache;
-  p.v_cache = v_cache;
-  p.block_tables = block_tables;
-  p.context_lens = context_lens;
-  p.num_blocks = layout->num_blocks;
-  p.num_seqs = num_seqs;
-  p.num_q_heads = num_q_heads;
-  p.num_kv_heads = layout->num_kv_heads;
-  p.group = num_q_heads / layout->num_kv_heads;
-  p.head_chunk = plan.head_chunk;
-  p.num_head_chunks = plan.num_head_chunks;
-  p.max_blocks = max_blocks_per_seq;
-  p.block_size = layout->block_size;
-  p.window = window;
-  p.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
-  p.units_per_split = plan.units_per_split;
-  p.num_splits = plan.num_splits;
-
-  if (plan.num_splits > 1) {
-    const size_t rows = static_cast<size_t>(num_seqs) * num_q_heads * plan.num_splits;
-    const size_t o_bytes = rows * layout->head_dim * sizeof(float);
-    void* ws = nullptr;
-    rc = get_workspace(device, st, o_bytes + rows * sizeof(float2), &ws);
-    if (rc != PKV_OK) return rc;
-    p.part_o = static_cast<float*>(ws);
-    p.part_ml = reinterpret_cast<float2*>(static_cast<char*>(ws) + o_bytes);
+int pkv_append_decode(const void* q, const void* k_new, const void* v_new, int32_t num_seqs,
+                      int32_t num_q_heads, void* k_cache, void* v_cache,
+                      const pkv_cache_layout* layout, const int32_t* block_tables,
+                      int32_t max_blocks_per_seq, const int32_t* context_lens, int32_t window,
+                      float scale, void* out, int32_t tokens_per_split, void* stream) {
+  if (num_seqs > 0) {
+    if (!k_new || !v_new) return PKV_ERR_NULL;
+    if (!aligned16(k_new) || !aligned16(v_new)) return PKV_ERR_ALIGNMENT;
   }
-
-  cudaError_t e;
-  if (layout->dtype == PKV_FLOAT32) {
-    e = pkv::launch_decode_f32(layout->head_dim, p, st);
-  } else {
-    CUtensorMap kmap, vmap;
-    rc = encode_pool_map(&kmap, k_cache, layout);
-    if (rc != PKV_OK) return rc;
-    rc = encode_pool_map(&vmap, v_cache, layout);
-    if (rc != PKV_OK) return rc;
-    e = pkv::launch_decode_16bit(layout->dtype, layout->head_dim, plan.ntiles, kmap, vmap, p, st);
-  }
-  if (e != cudaSuccess) return to_status(e);
-  if (plan.num_splits > 1) {
-    e = pkv::launch_combine(layout->dtype, layout->head_dim, p, st);
-    if (e != cudaSuccess) return to_status(e);
-  }
-  return PKV_OK;
+  return decode_impl(q, k_new, v_new, num_seqs, num_q_heads, k_cache, v_cache, layout,
+                     block_tables, max_blocks_per_seq, context_lens, window, scale, out,
+                     tokens_per_split, stream);
 }
 
 int pkv_decode(const void* q, int32_t num_seqs, int32_t num_q_heads, const void* k_cache,

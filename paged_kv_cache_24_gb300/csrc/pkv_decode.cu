@@ -242,6 +242,22 @@ decode16_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant_
   }
   bool bad = false;
 
+  // Fused append: the warp that streams the unit holding position L-1 puts the
+  // new token's K and V into that unit's staged rows -- so the token attends
+  // to the new values -- and (head chunk 0 only) stores them to the pool slot.
+  constexpr int CPR = D / 8;  // 16-byte chunks per row
+  const int t_new = w.L - 1;
+  const int rel_new = t_new / kUnitTokens - w.u0 - warp;
+  const bool own_new = p.k_new != nullptr && t_new >= 0 && rel_new >= 0 &&
+                       t_new / kUnitTokens < w.u1 && rel_new % kDecodeWarps == 0;
+  const int j_new = own_new ? rel_new / kDecodeWarps : -1;
+  uint4 new_row = make_uint4(0u, 0u, 0u, 0u);
+  if (own_new && lane < 2 * CPR) {
+    const T* src = static_cast<const T*>(lane < CPR ? p.k_new : p.v_new) +
+                   (static_cast<int64_t>(w.b) * p.num_kv_heads + w.hkv) * D;
+    new_row = __ldg(reinterpret_cast<const uint4*>(src) + (lane % CPR));
+  }
+
   for (int j = 0; j < my_n; ++j) {
     const int stage = j % S;
     const uint32_t parity = (j / S) & 1;
@@ -256,6 +272,21 @@ decode16_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant_
     const uint32_t kt = ring + stage * Cfg::kUnitBytes;
     const uint32_t vt = kt + Cfg::kTileBytes;
     const int t0 = (w.u0 + warp + j * kDecodeWarps) * kUnitTokens;
+
+    if (j == j_new) {
+      const int r = t_new % kUnitTokens;
+      if (lane < 2 * CPR) {
+        const int c = lane % CPR;
+        st_shared_v4((lane < CPR ? kt : vt) + swz(r, c), new_row);
+        if (yj >= 0 && w.h0 == w.hkv * p.group) {
+          T* dst = static_cast<T*>(lane < CPR ? p.k_dst : p.v_dst) +
+                   (static_cast<int64_t>(yj) + r) * D;
+          reinterpret_cast<uint4*>(dst)[c] = new_row;
+        }
+      }
+      fence_proxy_async_smem();  // these generic writes precede the stage's next TMA fill
+      __syncwarp();
+    }
 
     // ---- S^T[16 tok x 8 NT q] = K[16 x D] . Q^T[D x 8 NT] ----
     float s[NT][4];
@@ -480,7 +511,16 @@ decode_f32_kernel(const DecodeParams p) {
       const int t = t0 + r;
       const bool valid = t >= w.lo && t < w.L;
       float4 k4 = make_float4(0.f, 0.f, 0.f, 0.f), v4 = k4;
-      if (valid) {
+      if (valid && p.k_new != nullptr && t == w.L - 1) {
+        // fused append: attend to the new token and store it to its slot
+        const int64_t src = (static_cast<int64_t>(w.b) * p.num_kv_heads + w.hkv) * D;
+        k4 = __ldg(reinterpret_cast<const float4*>(static_cast<const float*>(p.k_new) + src) + li);
+        v4 = __ldg(reinterpret_cast<const float4*>(static_cast<const float*>(p.v_new) + src) + li);
+        if (w.h0 == w.hkv * p.group) {
+          reinterpret_cast<float4*>(static_cast<float*>(p.k_dst) + tile + r * D)[li] = k4;
+          reinterpret_cast<float4*>(static_cast<float*>(p.v_dst) + tile + r * D)[li] = v4;
+        }
+      } else if (valid) {
         k4 = __ldg(reinterpret_cast<const float4*>(kc + tile + r * D) + li);
         v4 = __ldg(reinterpret_cast<const float4*>(vc + tile + r * D) + li);
       }

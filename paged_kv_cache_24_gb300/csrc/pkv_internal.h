@@ -70,6 +70,10 @@ struct DecodeParams {
   const void* v_cache;
   const int32_t* block_tables; // [B][MB]
   const int32_t* context_lens; // [B]
+  const void* k_new;           // fused append: [B][Hkv][D] new keys (nullptr: decode only)
+  const void* v_new;           //               [B][Hkv][D] new values
+  void* k_dst;                 //               pools the new token is written to
+  void* v_dst;
   float* part_o;               // [B][Hq][S][D]  unnormalised partial outputs
   float2* part_ml;             // [B][Hq][S]     (running max in log2 units, sum)
   int64_t num_blocks;

@@ -1,6 +1,10 @@
 """DecodeStep: one serving decode step (slot mapping, append, decode) as a
 replayable CUDA graph fed from pinned host memory.
 
+With ``fused=True`` (the default) the step is ``pkv_append_decode`` -- the
+new token of each sequence sits at position ``context_lens - 1`` -- in one
+launch; ``fused=False`` runs the three separate calls.
+
 A step's host inputs -- the queries, the new tokens' K and V, their positions,
 the context lengths and (optionally) the block tables -- are packed into one
 pinned staging buffer and reach the device in a single copy; the attention
@@ -22,7 +26,8 @@ from __future__ import annotations
 
 import torch
 
-from ._binding import cache_layout, pkv_append, pkv_decode, pkv_slot_mapping
+from ._binding import (cache_layout, pkv_append, pkv_append_decode, pkv_decode,
+                       pkv_slot_mapping)
 
 _ALIGN = 256
 
@@ -30,11 +35,13 @@ _ALIGN = 256
 class DecodeStep:
     def __init__(self, k_cache: torch.Tensor, v_cache: torch.Tensor, num_seqs: int,
                  num_q_heads: int, max_blocks: int, window: int, scale: float,
-                 copy_block_tables: bool = True, num_buffers: int = 1, use_graph: bool = True):
+                 copy_block_tables: bool = True, num_buffers: int = 1, use_graph: bool = True,
+                 fused: bool = True):
         layout = cache_layout(k_cache)
         self.k_cache, self.v_cache = k_cache, v_cache
         self.window, self.scale = int(window), float(scale)
         self.block_size = layout.block_size
+        self.fused = fused
         dt, dev = k_cache.dtype, k_cache.device
         B, hq, hkv, d = num_seqs, num_q_heads, layout.num_kv_heads, layout.head_dim
         shapes = {
@@ -90,10 +97,17 @@ class DecodeStep:
         n = self._staged_bytes
         self._dev_buf[:n].copy_(self._host_bufs[i][:n], non_blocking=True)
         dv = self.device
-        pkv_slot_mapping(dv["block_tables"], dv["positions"], self.block_size, out=self.slots)
-        pkv_append(dv["k"], dv["v"], self.slots, self.k_cache, self.v_cache)
-        pkv_decode(dv["q"], self.k_cache, self.v_cache, dv["block_tables"], dv["context_lens"],
-                   self.window, self.scale, out=self.out)
+        if self.fused:
+            # the new token sits at position context_lens - 1: one launch
+            pkv_append_decode(dv["q"], dv["k"], dv["v"], self.k_cache, self.v_cache,
+                              dv["block_tables"], dv["context_lens"], self.window, self.scale,
+                              out=self.out)
+        else:
+            pkv_slot_mapping(dv["block_tables"], dv["positions"], self.block_size,
+                             out=self.slots)
+            pkv_append(dv["k"], dv["v"], self.slots, self.k_cache, self.v_cache)
+            pkv_decode(dv["q"], self.k_cache, self.v_cache, dv["block_tables"],
+                       dv["context_lens"], self.window, self.scale, out=self.out)
         self.host_out.copy_(self.out, non_blocking=True)
 
     def run(self, i: int = 0, wait: bool = True) -> torch.Tensor:
