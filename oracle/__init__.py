@@ -11,7 +11,9 @@ The arithmetic lives in ``pkv_oracle.c`` (plain C, double precision, libm
 * "Build a Paged KV Cache in Pure Python", Step 3 (``PagedKVCache.append`` and
   ``retrieve``) and Step 4 (``scaled_dot_product_attention``);
 * "Building a Streaming Sliding-Window Attention Engine in Pure Python",
-  Step 3 (``sliding_window_attention``: attend over ``[max(0, T - w), T)``).
+  Step 3 (``sliding_window_attention``: attend over ``[max(0, T - w), T)``)
+  and the StreamingLLM item of its "Extending" list (attention sinks: the
+  first tokens are kept regardless of the window).
 
 This module only marshals numpy / torch-CPU arrays into that library.
 """
@@ -75,8 +77,8 @@ def _load():
         lib.oracle_attend.argtypes = [c_vp, c_vp, c_vp, c_i64, c_i32, c_dbl, c_vp]
         lib.oracle_decode.restype = ctypes.c_int
         lib.oracle_decode.argtypes = [c_vp, c_i32, c_i32, c_vp, c_vp, c_i64, c_i32, c_i32, c_i32,
-                                      c_i32, c_vp, c_i32, c_vp, c_i32, c_dbl, c_vp, c_i64, c_vp,
-                                      c_i32]
+                                      c_i32, c_vp, c_i32, c_vp, c_i32, c_i32, c_dbl, c_vp, c_i64,
+                                      c_vp, c_i32]
         lib.oracle_max_threads.restype = ctypes.c_int
         lib.oracle_max_threads.argtypes = []
         _lib = lib
@@ -186,11 +188,12 @@ def attend(q: np.ndarray, K: np.ndarray, V: np.ndarray, scale: float) -> np.ndar
 
 
 def decode(q, k_cache, v_cache, block_tables, context_lens, window: int, scale: float,
-           pairs=None, threads: int = 0, check: bool = True) -> np.ndarray:
+           pairs=None, threads: int = 0, check: bool = True, num_sinks: int = 0) -> np.ndarray:
     """Paged decode attention in float64.
 
     ``q`` [B, Hq, D]; caches [NB, Hkv, bs, D]; ``block_tables`` [B, MB] int32;
-    ``context_lens`` [B] int32 (after the append); ``window`` <= 0 for none.
+    ``context_lens`` [B] int32 (after the append); ``window`` <= 0 for none;
+    ``num_sinks``: with a window, positions [0, num_sinks) are attended too.
     ``scale`` is used exactly as given (pass the float32 value the GPU sees).
     ``pairs``: optional [n, 2] array of (b, h); returns [n, D], else [B, Hq, D].
     """
@@ -216,7 +219,7 @@ def decode(q, k_cache, v_cache, block_tables, context_lens, window: int, scale: 
     out = np.empty((n, D), dtype=np.float64)
     rc = _load().oracle_decode(_ptr(qr), B, Hq, _ptr(kc), _ptr(vc), nb, hkv, bs, D, qd,
                                _ptr(bt), bt.shape[1] if bt.ndim == 2 else 0, _ptr(lens),
-                               int(window), float(scale),
+                               int(window), int(num_sinks), float(scale),
                                None if pairs_arr is None else _ptr(pairs_arr), n, _ptr(out),
                                int(threads))
     if check and rc != 0:

@@ -28,6 +28,10 @@
  *   - Grouped-query attention: query head h reads kv head h / (Hq / Hkv).
  *   - window <= 0 means no window; otherwise attend over the last `window`
  *     tokens, current token included.
+ *   - Attention sinks ([P3] "Extending" list, the StreamingLLM item: keep
+ *     the first 4 tokens regardless of the window): with a window and
+ *     num_sinks > 0, positions [0, num_sinks) are attended as well as the
+ *     window; num_sinks = 0 is the plain window.
  *   - Inputs of type fp16 / bf16 are widened exactly to double; all
  *     arithmetic is in double with libm exp().
  *
@@ -180,6 +184,7 @@ typedef struct {
   int32_t max_blocks;
   const int32_t* context_lens;
   int32_t window;
+  int32_t num_sinks;
   double scale;
 } decode_problem;
 
@@ -202,7 +207,10 @@ static int decode_one(const decode_problem* p, int32_t b, int32_t h, double* out
     return ORACLE_ERR_LENGTH;
   }
   const int64_t lo = window_start(L, p->window);
-  const int64_t T = L - lo;
+  /* sink positions before the window: [0, min(num_sinks, lo)) */
+  int64_t n_sink = 0;
+  if (p->window > 0 && p->num_sinks > 0) n_sink = p->num_sinks < lo ? p->num_sinks : lo;
+  const int64_t T = n_sink + (L - lo);
 
   double* q = (double*)malloc((size_t)D * sizeof(double));
   double* K = (double*)malloc((size_t)(T > 0 ? T : 1) * D * sizeof(double));
@@ -216,7 +224,10 @@ static int decode_one(const decode_problem* p, int32_t b, int32_t h, double* out
 
   const int32_t* table = p->block_tables + (int64_t)b * p->max_blocks;
   int rc = ORACLE_OK;
-  for (int64_t t = lo; t < L; ++t) {
+  /* the attended positions, in order: the sinks, then the window */
+  int64_t i = 0;
+  for (int64_t t = 0; t < L && rc == ORACLE_OK; ++t) {
+    if (!(t < n_sink || t >= lo)) continue;
     int64_t physical = table[t / p->block_size];
     int64_t row = t % p->block_size;
     if (physical < 0 || physical >= p->num_blocks) {
@@ -225,9 +236,10 @@ static int decode_one(const decode_problem* p, int32_t b, int32_t h, double* out
     }
     int64_t base = ((physical * p->num_kv_heads + hk) * p->block_size + row) * D;
     for (int32_t d = 0; d < D; ++d) {
-      K[(t - lo) * D + d] = load_elem(p->k_cache, base + d, p->dtype);
-      V[(t - lo) * D + d] = load_elem(p->v_cache, base + d, p->dtype);
+      K[i * D + d] = load_elem(p->k_cache, base + d, p->dtype);
+      V[i * D + d] = load_elem(p->v_cache, base + d, p->dtype);
     }
+    ++i;
   }
   if (rc == ORACLE_OK) {
     oracle_attend(q, K, V, T, D, p->scale, out);
@@ -243,6 +255,7 @@ static int decode_one(const decode_problem* p, int32_t b, int32_t h, double* out
  *   k/v_cache    [num_blocks][num_kv_heads][block_size][head_dim] dtype
  *   block_tables [num_seqs][max_blocks] int32
  *   context_lens [num_seqs] int32 (length after the step's append)
+ *   window, num_sinks: see the readings at the top of this file
  *   pairs        [n_pairs][2] = (b, h); NULL means every pair in (b, h) order
  *   out          [n_pairs][head_dim] double
  * Returns ORACLE_OK or the first error met (the affected rows hold NaN). */
@@ -250,15 +263,15 @@ int oracle_decode(const void* q, int32_t num_seqs, int32_t num_q_heads,
                   const void* k_cache, const void* v_cache, int64_t num_blocks,
                   int32_t num_kv_heads, int32_t block_size, int32_t head_dim, int32_t dtype,
                   const int32_t* block_tables, int32_t max_blocks, const int32_t* context_lens,
-                  int32_t window, double scale, const int32_t* pairs, int64_t n_pairs,
-                  double* out, int32_t num_threads) {
+                  int32_t window, int32_t num_sinks, double scale, const int32_t* pairs,
+                  int64_t n_pairs, double* out, int32_t num_threads) {
   if (!q || !k_cache || !v_cache || !block_tables || !context_lens || !out) return ORACLE_ERR_ARG;
   if (num_seqs < 0 || num_q_heads <= 0 || num_kv_heads <= 0 || head_dim <= 0 || block_size <= 0 ||
       max_blocks < 0 || num_q_heads % num_kv_heads != 0 || dtype < 0 || dtype > 2)
     return ORACLE_ERR_ARG;
   decode_problem p = {q, num_seqs, num_q_heads, k_cache, v_cache, num_blocks, num_kv_heads,
                       block_size, head_dim, dtype, block_tables, max_blocks, context_lens,
-                      window, scale};
+                      window, num_sinks, scale};
   const int64_t total = pairs ? n_pairs : (int64_t)num_seqs * num_q_heads;
   int rc = ORACLE_OK;
 #ifdef _OPENMP

@@ -84,7 +84,8 @@ def test_closed_form_cases(oracle_lib, case):
     kc = paged_from_logical(K, table[0], bs, nb)
     vc = paged_from_logical(V, table[0], bs, nb)
     q = np.asarray(case["q"], dtype=np.float32).reshape(1, 1, d)
-    out = oracle.decode(q, kc, vc, table, np.array([L], np.int32), case["window"], case["scale"])
+    out = oracle.decode(q, kc, vc, table, np.array([L], np.int32), case["window"], case["scale"],
+                        num_sinks=case.get("sinks", 0))
     np.testing.assert_allclose(out[0, 0], case["expected"], rtol=0, atol=case["tol"])
 
 
@@ -128,7 +129,7 @@ def _random_problem(rng, B, hq, hkv, d, bs, lens, dtype, nb_extra=3):
     return qt, kt, vt, table, logical_t
 
 
-def _sdpa_reference(q_b, Kl, Vl, G, window, scale):
+def _sdpa_reference(q_b, Kl, Vl, G, window, scale, sinks=0):
     """torch float64 SDPA of one sequence: q_b [Hq, D], Kl/Vl [L, Hkv, D]."""
     L = Kl.shape[0]
     hq, d = q_b.shape
@@ -138,7 +139,8 @@ def _sdpa_reference(q_b, Kl, Vl, G, window, scale):
     Vh = Vl.permute(1, 0, 2).repeat_interleave(G, dim=0)
     mask = None
     if window > 0:
-        mask = torch.arange(L) >= max(0, L - window)
+        pos = torch.arange(L)
+        mask = (pos >= max(0, L - window)) | (pos < sinks)
         mask = mask.view(1, 1, 1, L)
     out = torch.nn.functional.scaled_dot_product_attention(
         q_b.view(1, hq, 1, d), Kh.unsqueeze(0), Vh.unsqueeze(0), attn_mask=mask, scale=scale)
@@ -146,17 +148,21 @@ def _sdpa_reference(q_b, Kl, Vl, G, window, scale):
 
 
 @pytest.mark.parametrize("dtype", ["f32", "f16", "bf16"])
-@pytest.mark.parametrize("hq,hkv,window,bs", [(4, 4, 0, 4), (8, 2, 0, 8), (6, 2, 5, 4),
-                                               (4, 1, 3, 16), (3, 3, 100, 2)])
-def test_matches_torch_sdpa(oracle_lib, dtype, hq, hkv, window, bs):
+@pytest.mark.parametrize("hq,hkv,window,bs,sinks", [(4, 4, 0, 4, 0), (8, 2, 0, 8, 0),
+                                                     (6, 2, 5, 4, 0), (4, 1, 3, 16, 0),
+                                                     (3, 3, 100, 2, 0), (4, 2, 6, 4, 4),
+                                                     (2, 1, 9, 8, 2), (4, 4, 0, 4, 3)])
+def test_matches_torch_sdpa(oracle_lib, dtype, hq, hkv, window, bs, sinks):
     rng = np.random.default_rng(zlib.crc32(repr((dtype, hq, hkv, window, bs)).encode()))
     lens = [1, 7, 13, 0, 29]
     d = 16
     scale = float(np.float32(1 / math.sqrt(d)))
     q, kc, vc, table, logical = _random_problem(rng, len(lens), hq, hkv, d, bs, lens, dtype)
-    out = oracle.decode(q, kc, vc, table, np.array(lens, np.int32), window, scale)
+    out = oracle.decode(q, kc, vc, table, np.array(lens, np.int32), window, scale,
+                        num_sinks=sinks)
     for b, L in enumerate(lens):
-        ref = _sdpa_reference(q[b].double(), *logical[b], hq // hkv, window, scale).numpy()
+        ref = _sdpa_reference(q[b].double(), *logical[b], hq // hkv, window, scale,
+                              sinks).numpy()
         np.testing.assert_allclose(out[b], ref, rtol=1e-12, atol=1e-12)
 
 

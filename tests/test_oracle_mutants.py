@@ -4,10 +4,10 @@ Each case plants one mistake in a temporary copy of oracle/pkv_oracle.c (on the
 CPU, never in the product), rebuilds it, and runs tests/test_oracle.py against
 the copy: the pin suite has to fail.  The mistakes are the ones a careful
 reader of the pages could still make: a wrong GQA head mapping, a flipped or
-missing max-subtraction, an off-by-one window start, swapped K and V, wrong
-row/block or head-major indexing, a squared scale, wrong element decoding, a
-wrong slot, a wrong append destination, the wrong query head, and a non-zero
-empty context.
+missing max-subtraction, an off-by-one window start, a wrong attention-sink
+count or ignored sinks, swapped K and V, wrong row/block or head-major
+indexing, a squared scale, wrong element decoding, a wrong slot, a wrong
+append destination, the wrong query head, and a non-zero empty context.
 """
 import os
 import shutil
@@ -23,8 +23,11 @@ MUTANTS = {
     "exp_sign": ("s[t] = exp(s[t] - m);", "s[t] = exp(m - s[t]);"),
     "no_max_subtraction": ("s[t] = exp(s[t] - m);", "s[t] = exp(s[t]);"),
     "window_off_by_one": ("int64_t lo = L - window;", "int64_t lo = L - window + 1;"),
-    "k_v_swapped": ("V[(t - lo) * D + d] = load_elem(p->v_cache",
-                    "V[(t - lo) * D + d] = load_elem(p->k_cache"),
+    "sink_count_off_by_one": (
+        "if (p->window > 0 && p->num_sinks > 0) n_sink = p->num_sinks < lo ? p->num_sinks : lo;",
+        "if (p->window > 0 && p->num_sinks > 0) n_sink = p->num_sinks + 1 < lo ? p->num_sinks + 1 : lo;"),
+    "sinks_ignored": ("if (!(t < n_sink || t >= lo)) continue;", "if (!(t >= lo)) continue;"),
+    "k_v_swapped": ("V[i * D + d] = load_elem(p->v_cache", "V[i * D + d] = load_elem(p->k_cache"),
     "row_index": ("int64_t row = t % p->block_size;",
                   "int64_t row = (t / p->block_size) % p->block_size;"),
     "token_major_offset": (
