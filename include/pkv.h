@@ -174,15 +174,41 @@ int pkv_append_decode(const void* q, const void* k_new, const void* v_new, int32
                       int32_t max_blocks_per_seq, const int32_t* context_lens, int32_t window,
                       float scale, void* out, int32_t tokens_per_split, void* stream);
 
+/* Options of pkv_decode_ex. */
+typedef struct pkv_decode_options {
+  int32_t window;           /* <= 0: no window                                        */
+  int32_t num_sinks;        /* with window > 0, positions [0, num_sinks) are attended
+                               as well (attention sinks); 0: plain window             */
+  int32_t tokens_per_split; /* a multiple of 16 up to 2048, or 0 for the library plan */
+  const void* k_new;        /* both non-NULL: fused append of position L-1, as in    */
+  const void* v_new;        /* pkv_append_decode; both NULL: decode only             */
+} pkv_decode_options;
+
 /*
- * pkv_decode_plan -- the split pkv_decode_split would use (host only, no GPU
+ * pkv_decode_ex -- pkv_decode with every option.
+ *   ("Building a Streaming Sliding-Window Attention Engine in Pure Python",
+ *   Step 3 for the window and the StreamingLLM item of its "Extending" list
+ *   for the sinks: the first tokens are kept regardless of the window.)
+ *   With window w > 0 and num_sinks s > 0 a length-L context attends the
+ *   positions [0, min(s, lo)) and [lo, L), lo = max(0, L - w).  The other
+ *   arguments, the errors and the workspace are those of pkv_decode; k_cache
+ *   and v_cache are written only with the fused append.
+ */
+int pkv_decode_ex(const void* q, int32_t num_seqs, int32_t num_q_heads, void* k_cache,
+                  void* v_cache, const pkv_cache_layout* layout, const int32_t* block_tables,
+                  int32_t max_blocks_per_seq, const int32_t* context_lens, float scale, void* out,
+                  const pkv_decode_options* options, void* stream);
+
+/*
+ * pkv_decode_plan -- the split pkv_decode_ex would use (host only, no GPU
  * work).  num_sms: streaming multiprocessors to plan for (<= 0: query the
  * current device).  Writes the tokens per split and the number of splits
  * the grid provides for the longest possible context.
  */
 int pkv_decode_plan(int32_t num_seqs, int32_t num_q_heads, const pkv_cache_layout* layout,
-                    int32_t max_blocks_per_seq, int32_t window, int32_t tokens_per_split,
-                    int32_t num_sms, int32_t* tokens_per_split_out, int32_t* num_splits_out);
+                    int32_t max_blocks_per_seq, int32_t window, int32_t num_sinks,
+                    int32_t tokens_per_split, int32_t num_sms, int32_t* tokens_per_split_out,
+                    int32_t* num_splits_out);
 
 /*
  * pkv_decode_noalloc -- pkv_decode for callers that cannot allocate device

@@ -19,13 +19,13 @@ All tensors live on the GPU; PyTorch provides the memory and the stream.
 ``workloads`` builds the seeded synthetic inputs used by the tests and the
 benchmark.
 """
-from ._binding import (CacheLayout, PkvError, cache_layout, library_path, load_library,
+from ._binding import (CacheLayout, DecodeOptions, PkvError, cache_layout, library_path, load_library,
                        pkv_append, pkv_append_decode, pkv_decode, pkv_decode_plan, pkv_release_workspaces,
                        pkv_slot_mapping, status_string)
 from .step import DecodeStep
 
 __all__ = [
-    "DecodeStep", "CacheLayout", "PkvError", "cache_layout", "library_path", "load_library", "pkv_append",
+    "DecodeStep", "DecodeOptions", "CacheLayout", "PkvError", "cache_layout", "library_path", "load_library", "pkv_append",
     "pkv_append_decode",
     "pkv_decode", "pkv_decode_plan", "pkv_release_workspaces", "pkv_slot_mapping",
     "status_string",

@@ -27,6 +27,13 @@ class PkvError(RuntimeError):
         self.status = status
 
 
+class DecodeOptions(ctypes.Structure):
+    """Mirror of ``pkv_decode_options``."""
+    _fields_ = [("window", ctypes.c_int32), ("num_sinks", ctypes.c_int32),
+                ("tokens_per_split", ctypes.c_int32), ("k_new", ctypes.c_void_p),
+                ("v_new", ctypes.c_void_p)]
+
+
 class CacheLayout(ctypes.Structure):
     """Mirror of ``pkv_cache_layout``."""
     _fields_ = [("num_blocks", ctypes.c_int64), ("num_kv_heads", ctypes.c_int32),
@@ -63,7 +70,9 @@ def load_library():
             "pkv_decode_split": [vp, i32, i32, vp, vp, lay, vp, i32, vp, i32, f32, vp, i32, vp],
             "pkv_append_decode": [vp, vp, vp, i32, i32, vp, vp, lay, vp, i32, vp, i32, f32, vp,
                                   i32, vp],
-            "pkv_decode_plan": [i32, i32, lay, i32, i32, i32, i32, ctypes.POINTER(i32),
+            "pkv_decode_ex": [vp, i32, i32, vp, vp, lay, vp, i32, vp, f32, vp,
+                              ctypes.POINTER(DecodeOptions), vp],
+            "pkv_decode_plan": [i32, i32, lay, i32, i32, i32, i32, i32, ctypes.POINTER(i32),
                                 ctypes.POINTER(i32)],
             "pkv_release_workspaces": [],
         }
@@ -158,8 +167,9 @@ def pkv_append(k: torch.Tensor, v: torch.Tensor, slot_mapping: torch.Tensor,
 def pkv_decode(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
                block_tables: torch.Tensor, context_lens: torch.Tensor, window: int,
                scale: float, out: torch.Tensor | None = None, tokens_per_split: int = 0,
-               stream=None) -> torch.Tensor:
-    """Decode attention of q [B, Hq, D] over the paged context; returns out [B, Hq, D]."""
+               stream=None, num_sinks: int = 0) -> torch.Tensor:
+    """Decode attention of q [B, Hq, D] over the paged context; returns out [B, Hq, D].
+    With a window, ``num_sinks`` first positions are attended as well."""
     _on_cuda(q, k_cache, v_cache, block_tables, context_lens, out)
     layout = cache_layout(k_cache)
     _require(v_cache.shape == k_cache.shape and v_cache.dtype == k_cache.dtype
@@ -176,10 +186,11 @@ def pkv_decode(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
         out = torch.empty_like(q)
     _require(out.shape == q.shape and out.dtype == q.dtype and out.is_contiguous(),
              "out must be contiguous and shaped like q")
-    _check("pkv_decode", load_library().pkv_decode_split(
+    opts = DecodeOptions(int(window), int(num_sinks), int(tokens_per_split), None, None)
+    _check("pkv_decode", load_library().pkv_decode_ex(
         _ptr(q), B, Hq, _ptr(k_cache), _ptr(v_cache), ctypes.byref(layout),
-        _ptr(block_tables), block_tables.shape[1], _ptr(context_lens), int(window),
-        float(scale), _ptr(out), int(tokens_per_split), _stream(stream)))
+        _ptr(block_tables), block_tables.shape[1], _ptr(context_lens), float(scale), _ptr(out),
+        ctypes.byref(opts), _stream(stream)))
     return out
 
 
@@ -187,7 +198,7 @@ def pkv_append_decode(q: torch.Tensor, k_new: torch.Tensor, v_new: torch.Tensor,
                       k_cache: torch.Tensor, v_cache: torch.Tensor, block_tables: torch.Tensor,
                       context_lens: torch.Tensor, window: int, scale: float,
                       out: torch.Tensor | None = None, tokens_per_split: int = 0,
-                      stream=None) -> torch.Tensor:
+                      stream=None, num_sinks: int = 0) -> torch.Tensor:
     """Append each sequence's new token (at position context_lens[b] - 1) and
     decode, in one launch; same result as the separate calls."""
     _on_cuda(q, k_new, v_new, k_cache, v_cache, block_tables, context_lens, out)
@@ -211,20 +222,23 @@ def pkv_append_decode(q: torch.Tensor, k_new: torch.Tensor, v_new: torch.Tensor,
         out = torch.empty_like(q)
     _require(out.shape == q.shape and out.dtype == q.dtype and out.is_contiguous(),
              "out must be contiguous and shaped like q")
-    _check("pkv_append_decode", load_library().pkv_append_decode(
-        _ptr(q), _ptr(k_new), _ptr(v_new), B, Hq, _ptr(k_cache), _ptr(v_cache),
-        ctypes.byref(layout), _ptr(block_tables), block_tables.shape[1], _ptr(context_lens),
-        int(window), float(scale), _ptr(out), int(tokens_per_split), _stream(stream)))
+    opts = DecodeOptions(int(window), int(num_sinks), int(tokens_per_split), _ptr(k_new),
+                         _ptr(v_new))
+    _check("pkv_append_decode", load_library().pkv_decode_ex(
+        _ptr(q), B, Hq, _ptr(k_cache), _ptr(v_cache), ctypes.byref(layout), _ptr(block_tables),
+        block_tables.shape[1], _ptr(context_lens), float(scale), _ptr(out), ctypes.byref(opts),
+        _stream(stream)))
     return out
 
 
 def pkv_decode_plan(num_seqs: int, num_q_heads: int, layout: CacheLayout, max_blocks: int,
-                    window: int, tokens_per_split: int = 0, num_sms: int = 0):
+                    window: int, tokens_per_split: int = 0, num_sms: int = 0,
+                    num_sinks: int = 0):
     """(tokens_per_split, num_splits) the library would use; host only."""
     tps, ns = ctypes.c_int32(0), ctypes.c_int32(0)
     _check("pkv_decode_plan", load_library().pkv_decode_plan(
-        num_seqs, num_q_heads, ctypes.byref(layout), max_blocks, window, tokens_per_split,
-        num_sms, ctypes.byref(tps), ctypes.byref(ns)))
+        num_seqs, num_q_heads, ctypes.byref(layout), max_blocks, window, num_sinks,
+        tokens_per_split, num_sms, ctypes.byref(tps), ctypes.byref(ns)))
     return tps.value, ns.value
 
 

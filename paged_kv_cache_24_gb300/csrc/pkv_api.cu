@@ -123,7 +123,7 @@ int sm_count_of_current_device() {
 }
 
 int make_plan(int num_seqs, int num_q_heads, const pkv_cache_layout* L, int max_blocks,
-              int window, int tokens_per_split, int num_sms, Plan* plan) {
+              int window, int num_sinks, int tokens_per_split, int num_sms, Plan* plan) {
   const int group = num_q_heads / L->num_kv_heads;
   const int cap = L->dtype == PKV_FLOAT32 ? 8 : 16;  // query heads per CTA
   plan->head_chunk = group < cap ? group : cap;
@@ -135,7 +135,11 @@ int make_plan(int num_seqs, int num_q_heads, const pkv_cache_layout* L, int max_
       static_cast<int64_t>(max_blocks) * L->block_size / pkv::kUnitTokens;
   int64_t max_units = total_units;
   if (window > 0) {
-    const int64_t wu = (static_cast<int64_t>(window) - 1) / pkv::kUnitTokens + 2;
+    // a window spans at most (w-1)/16 + 2 units; sinks add theirs in front
+    const int64_t sink_units =
+        num_sinks > 0 ? (static_cast<int64_t>(num_sinks) + pkv::kUnitTokens - 1) / pkv::kUnitTokens
+                      : 0;
+    const int64_t wu = (static_cast<int64_t>(window) - 1) / pkv::kUnitTokens + 2 + sink_units;
     if (wu < max_units) max_units = wu;
   }
   // Each warp resolves its units' pages with one lane per unit: at most 32
@@ -188,11 +192,13 @@ int decode_impl(const void* q, const void* k_new, const void* v_new, int32_t num
                 int32_t num_q_heads, const void* k_cache, const void* v_cache,
                 const pkv_cache_layout* layout, const int32_t* block_tables,
                 int32_t max_blocks_per_seq, const int32_t* context_lens, int32_t window,
-                float scale, void* out, int32_t tokens_per_split, void* stream) {
+                int32_t num_sinks, float scale, void* out, int32_t tokens_per_split,
+                void* stream) {
   int rc = check_decode_args(q, num_seqs, num_q_heads, k_cache, v_cache, layout, block_tables,
                              max_blocks_per_seq, context_lens, out);
   if (rc != PKV_OK) return rc;
   if (tokens_per_split < 0 || tokens_per_split % pkv::kUnitTokens != 0) return PKV_ERR_SHAPE;
+  if (num_sinks < 0) return PKV_ERR_SHAPE;
   if (tokens_per_split > 32 * pkv::kDecodeWarps * pkv::kUnitTokens) return PKV_ERR_UNSUPPORTED;
   if (num_seqs == 0) return PKV_OK;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
@@ -200,8 +206,8 @@ int decode_impl(const void* q, const void* k_new, const void* v_new, int32_t num
   int device = 0;
   if (cudaGetDevice(&device) != cudaSuccess) return PKV_ERR_CUDA;
   Plan plan;
-  rc = make_plan(num_seqs, num_q_heads, layout, max_blocks_per_seq, window, tokens_per_split,
-                 sm_count_of_current_device(), &plan);
+  rc = make_plan(num_seqs, num_q_heads, layout, max_blocks_per_seq, window, num_sinks,
+                 tokens_per_split, sm_count_of_current_device(), &plan);
   if (rc != PKV_OK) return rc;
 
   DecodeParams p{};
@@ -225,6 +231,7 @@ int decode_impl(const void* q, const void* k_new, const void* v_new, int32_t num
   p.max_blocks = max_blocks_per_seq;
   p.block_size = layout->block_size;
   p.window = window;
+  p.num_sinks = num_sinks;
   p.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
   p.units_per_split = plan.units_per_split;
   p.num_splits = plan.num_splits;
@@ -270,10 +277,10 @@ int decode_checks(const void* q, int32_t num_seqs, int32_t num_q_heads, const vo
                            max_blocks, context_lens, out);
 }
 int decode_plan(int num_seqs, int num_q_heads, const pkv_cache_layout* layout, int max_blocks,
-                int window, int* head_chunk, int* num_head_chunks, int* ntiles,
+                int window, int num_sinks, int* head_chunk, int* num_head_chunks, int* ntiles,
                 int* units_per_split, int* num_splits) {
   Plan plan;
-  int rc = make_plan(num_seqs, num_q_heads, layout, max_blocks, window, 0,
+  int rc = make_plan(num_seqs, num_q_heads, layout, max_blocks, window, num_sinks, 0,
                      sm_count_of_current_device(), &plan);
   if (rc != PKV_OK) return rc;
   *head_chunk = plan.head_chunk;
@@ -337,16 +344,18 @@ int pkv_append(const void* k, const void* v, const int64_t* slot_mapping, int64_
 }
 
 int pkv_decode_plan(int32_t num_seqs, int32_t num_q_heads, const pkv_cache_layout* layout,
-                    int32_t max_blocks_per_seq, int32_t window, int32_t tokens_per_split,
-                    int32_t num_sms, int32_t* tokens_per_split_out, int32_t* num_splits_out) {
+                    int32_t max_blocks_per_seq, int32_t window, int32_t num_sinks,
+                    int32_t tokens_per_split, int32_t num_sms, int32_t* tokens_per_split_out,
+                    int32_t* num_splits_out) {
   int rc = check_layout(layout, true);
   if (rc != PKV_OK) return rc;
   if (num_seqs < 0 || num_q_heads <= 0 || max_blocks_per_seq < 0 ||
       num_q_heads % layout->num_kv_heads != 0)
     return PKV_ERR_SHAPE;
+  if (num_sinks < 0) return PKV_ERR_SHAPE;
   Plan plan;
-  rc = make_plan(num_seqs, num_q_heads, layout, max_blocks_per_seq, window, tokens_per_split,
-                 num_sms > 0 ? num_sms : sm_count_of_current_device(), &plan);
+  rc = make_plan(num_seqs, num_q_heads, layout, max_blocks_per_seq, window, num_sinks,
+                 tokens_per_split, num_sms > 0 ? num_sms : sm_count_of_current_device(), &plan);
   if (rc != PKV_OK) return rc;
   if (tokens_per_split_out) *tokens_per_split_out = plan.units_per_split * pkv::kUnitTokens;
   if (num_splits_out) *num_splits_out = plan.num_splits;
@@ -359,8 +368,23 @@ int pkv_decode_split(const void* q, int32_t num_seqs, int32_t num_q_heads,
                      const int32_t* context_lens, int32_t window, float scale, void* out,
                      int32_t tokens_per_split, void* stream) {
   return decode_impl(q, nullptr, nullptr, num_seqs, num_q_heads, k_cache, v_cache, layout,
-                     block_tables, max_blocks_per_seq, context_lens, window, scale, out,
+                     block_tables, max_blocks_per_seq, context_lens, window, 0, scale, out,
                      tokens_per_split, stream);
+}
+
+int pkv_decode_ex(const void* q, int32_t num_seqs, int32_t num_q_heads, void* k_cache,
+                  void* v_cache, const pkv_cache_layout* layout, const int32_t* block_tables,
+                  int32_t max_blocks_per_seq, const int32_t* context_lens, float scale, void* out,
+                  const pkv_decode_options* options, void* stream) {
+  if (!options) return PKV_ERR_NULL;
+  if (num_seqs > 0 && (options->k_new != nullptr) != (options->v_new != nullptr))
+    return PKV_ERR_NULL;
+  if (num_seqs > 0 && options->k_new &&
+      (!aligned16(options->k_new) || !aligned16(options->v_new)))
+    return PKV_ERR_ALIGNMENT;
+  return decode_impl(q, options->k_new, options->v_new, num_seqs, num_q_heads, k_cache, v_cache,
+                     layout, block_tables, max_blocks_per_seq, context_lens, options->window,
+                     options->num_sinks, scale, out, options->tokens_per_split, stream);
 }
 
 int pkv_append_decode(const void* q, const void* k_new, const void* v_new, int32_t num_seqs,
@@ -373,7 +397,7 @@ int pkv_append_decode(const void* q, const void* k_new, const void* v_new, int32
     if (!aligned16(k_new) || !aligned16(v_new)) return PKV_ERR_ALIGNMENT;
   }
   return decode_impl(q, k_new, v_new, num_seqs, num_q_heads, k_cache, v_cache, layout,
-                     block_tables, max_blocks_per_seq, context_lens, window, scale, out,
+                     block_tables, max_blocks_per_seq, context_lens, window, 0, scale, out,
                      tokens_per_split, stream);
 }
 

@@ -62,7 +62,8 @@ __device__ __forceinline__ uint32_t swz(int row, int chunk) {
 struct WorkItem {
   int b, hkv, h0, nh, split;
   int L, lo, nsplit;
-  int u0, u1;  // units of this CTA
+  int u0, u1;  // virtual units of this CTA (see SeqUnits)
+  SeqUnits su;
   bool len_ok, empty;
 };
 
@@ -76,13 +77,12 @@ __device__ __forceinline__ WorkItem make_work_item(const DecodeParams& p) {
   w.nh = min(p.head_chunk, p.group - chunk * p.head_chunk);
   w.L = p.context_lens[w.b];
   w.len_ok = w.L >= 0 && static_cast<int64_t>(w.L) <= static_cast<int64_t>(p.max_blocks) * p.block_size;
-  int first, end;
-  unit_range(w.len_ok ? w.L : 0, p.window, &first, &end);
-  w.lo = window_start(w.len_ok ? w.L : 0, p.window);
-  w.empty = end == first;
-  w.nsplit = (!w.len_ok || w.empty) ? 1 : splits_for(end - first, p.units_per_split);
-  w.u0 = first + w.split * p.units_per_split;
-  w.u1 = min(w.u0 + p.units_per_split, end);
+  w.su = seq_units(w.len_ok ? w.L : 0, p.window, p.num_sinks);
+  w.lo = w.su.lo;
+  w.empty = w.su.n_units == 0;
+  w.nsplit = (!w.len_ok || w.empty) ? 1 : splits_for(w.su.n_units, p.units_per_split);
+  w.u0 = w.split * p.units_per_split;
+  w.u1 = min(w.u0 + p.units_per_split, w.su.n_units);
   return w;
 }
 
@@ -181,7 +181,7 @@ decode16_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant_
   const int my_n = span > warp ? (span - warp + kDecodeWarps - 1) / kDecodeWarps : 0;
   int my_y = -1;  // TMA row coordinate of the unit's first token, -1 = bad block id
   if (lane < my_n) {
-    const int t0 = (w.u0 + warp + lane * kDecodeWarps) * kUnitTokens;
+    const int t0 = phys_unit(w.su, w.u0 + warp + lane * kDecodeWarps) * kUnitTokens;
     const int32_t pb = __ldg(p.block_tables + static_cast<int64_t>(w.b) * p.max_blocks +
                              t0 / p.block_size);
     if (pb >= 0 && pb < p.num_blocks)
@@ -246,10 +246,11 @@ decode16_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant_
   // new token's K and V into that unit's staged rows -- so the token attends
   // to the new values -- and (head chunk 0 only) stores them to the pool slot.
   constexpr int CPR = D / 8;  // 16-byte chunks per row
-  const int t_new = w.L - 1;
-  const int rel_new = t_new / kUnitTokens - w.u0 - warp;
-  const bool own_new = p.k_new != nullptr && t_new >= 0 && rel_new >= 0 &&
-                       t_new / kUnitTokens < w.u1 && rel_new % kDecodeWarps == 0;
+  const int t_new = w.L - 1;  // always inside the window part
+  const int v_new = w.su.n_sink_u + t_new / kUnitTokens - w.su.win_u0;
+  const int rel_new = v_new - w.u0 - warp;
+  const bool own_new = p.k_new != nullptr && t_new >= 0 && rel_new >= 0 && v_new < w.u1 &&
+                       rel_new % kDecodeWarps == 0;
   const int j_new = own_new ? rel_new / kDecodeWarps : -1;
   uint4 new_row = make_uint4(0u, 0u, 0u, 0u);
   if (own_new && lane < 2 * CPR) {
@@ -271,7 +272,7 @@ decode16_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant_
 
     const uint32_t kt = ring + stage * Cfg::kUnitBytes;
     const uint32_t vt = kt + Cfg::kTileBytes;
-    const int t0 = (w.u0 + warp + j * kDecodeWarps) * kUnitTokens;
+    const int t0 = phys_unit(w.su, w.u0 + warp + j * kDecodeWarps) * kUnitTokens;
 
     if (j == j_new) {
       const int r = t_new % kUnitTokens;
@@ -302,11 +303,12 @@ decode16_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant_
       for (int nt = 0; nt < NT; ++nt) Mma<T>::run(s[nt], a0, a1, a2, a3, qf[nt][kk][0], qf[nt][kk][1]);
     }
 
-    // ---- scale into log2 units; mask tokens outside [lo, L) ----
-    const bool edge = (t0 < w.lo) || (t0 + kUnitTokens > w.L);
+    // ---- scale into log2 units; mask tokens that are not attended ----
+    const bool edge = !(t0 + kUnitTokens <= w.L &&
+                        (t0 >= w.lo || t0 + kUnitTokens <= w.su.sinks));
     const int ta = t0 + g, tb = ta + 8;  // tokens of rows g and g + 8
-    const bool va = !edge || (ta >= w.lo && ta < w.L);
-    const bool vb = !edge || (tb >= w.lo && tb < w.L);
+    const bool va = !edge || attended(w.su, w.L, ta);
+    const bool vb = !edge || attended(w.su, w.L, tb);
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) {
       s[nt][0] = va ? s[nt][0] * p.scale_log2 : -INFINITY;
@@ -374,10 +376,10 @@ decode16_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant_
     uint32_t mlo = 0xffffffffu, mhi = 0xffffffffu;
     if (edge) {
       const int tk = t0 + 2 * tig;
-      mlo = ((tk >= w.lo && tk < w.L) ? 0x0000ffffu : 0u) |
-            ((tk + 1 >= w.lo && tk + 1 < w.L) ? 0xffff0000u : 0u);
-      mhi = ((tk + 8 >= w.lo && tk + 8 < w.L) ? 0x0000ffffu : 0u) |
-            ((tk + 9 >= w.lo && tk + 9 < w.L) ? 0xffff0000u : 0u);
+      mlo = (attended(w.su, w.L, tk) ? 0x0000ffffu : 0u) |
+            (attended(w.su, w.L, tk + 1) ? 0xffff0000u : 0u);
+      mhi = (attended(w.su, w.L, tk + 8) ? 0x0000ffffu : 0u) |
+            (attended(w.su, w.L, tk + 9) ? 0xffff0000u : 0u);
     }
 #pragma unroll
     for (int mt = 0; mt < KS; ++mt) {
@@ -498,7 +500,7 @@ decode_f32_kernel(const DecodeParams p) {
   const float* vc = static_cast<const float*>(p.v_cache);
 
   for (int u = w.u0 + warp; u < w.u1; u += kDecodeWarps) {
-    const int t0 = u * kUnitTokens;
+    const int t0 = phys_unit(w.su, u) * kUnitTokens;
     const int32_t pb = __ldg(p.block_tables + static_cast<int64_t>(w.b) * p.max_blocks +
                              t0 / p.block_size);
     if (pb < 0 || pb >= p.num_blocks) {
@@ -509,7 +511,7 @@ decode_f32_kernel(const DecodeParams p) {
                           (t0 % p.block_size)) * D;
     for (int r = sub; r < kUnitTokens; r += RPW) {
       const int t = t0 + r;
-      const bool valid = t >= w.lo && t < w.L;
+      const bool valid = attended(w.su, w.L, t);
       float4 k4 = make_float4(0.f, 0.f, 0.f, 0.f), v4 = k4;
       if (valid && p.k_new != nullptr && t == w.L - 1) {
         // fused append: attend to the new token and store it to its slot
@@ -601,9 +603,7 @@ combine_kernel(const DecodeParams p) {
   const int b = static_cast<int>(item / p.num_q_heads);
   const int L = p.context_lens[b];
   if (L < 0 || static_cast<int64_t>(L) > static_cast<int64_t>(p.max_blocks) * p.block_size) return;
-  int first, end;
-  unit_range(L, p.window, &first, &end);
-  const int nsplit = splits_for(end - first, p.units_per_split);
+  const int nsplit = splits_for(seq_units(L, p.window, p.num_sinks).n_units, p.units_per_split);
   if (nsplit <= 1) return;  // written directly by the decode kernel
 
   const float2* ml = p.part_ml + item * p.num_splits;

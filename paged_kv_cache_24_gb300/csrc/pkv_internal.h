@@ -29,14 +29,37 @@ __host__ __device__ __forceinline__ int window_start(int L, int window) {
   return lo > 0 ? lo : 0;
 }
 
-// Units [first, end) covering the attended positions [lo, L).
-__host__ __device__ __forceinline__ void unit_range(int L, int window, int* first, int* end) {
-  if (L <= 0) {
-    *first = *end = 0;
-    return;
-  }
-  *first = window_start(L, window) / kUnitTokens;
-  *end = (L + kUnitTokens - 1) / kUnitTokens;
+// The 16-token units a length-L context attends, as a virtual sequence
+// 0 .. n_units-1: first the units holding the attention sinks [0, sinks),
+// then the units of the window [lo, L).  When the two meet, one range from
+// unit 0 covers both (tokens in a gap between them are masked per token).
+struct SeqUnits {
+  int lo;        // window start
+  int sinks;     // sink positions before the window: [0, sinks)
+  int n_sink_u;  // virtual units 0 .. n_sink_u-1 are physical units 0 .. n_sink_u-1
+  int win_u0;    // virtual unit n_sink_u + i is physical unit win_u0 + i
+  int n_units;
+};
+
+__host__ __device__ __forceinline__ SeqUnits seq_units(int L, int window, int num_sinks) {
+  SeqUnits r{0, 0, 0, 0, 0};
+  if (L <= 0) return r;
+  r.lo = window_start(L, window);
+  r.sinks = (window > 0 && num_sinks > 0) ? (num_sinks < r.lo ? num_sinks : r.lo) : 0;
+  r.n_sink_u = (r.sinks + kUnitTokens - 1) / kUnitTokens;
+  r.win_u0 = r.lo / kUnitTokens;
+  if (r.n_sink_u >= r.win_u0) r.n_sink_u = r.win_u0 = 0;
+  r.n_units = r.n_sink_u + (L + kUnitTokens - 1) / kUnitTokens - r.win_u0;
+  return r;
+}
+
+__host__ __device__ __forceinline__ int phys_unit(const SeqUnits& r, int v) {
+  return v < r.n_sink_u ? v : r.win_u0 + (v - r.n_sink_u);
+}
+
+// Is position t (0 <= t) attended by a length-L context?
+__host__ __device__ __forceinline__ bool attended(const SeqUnits& r, int L, int t) {
+  return t < L && (t >= r.lo || t < r.sinks);
 }
 
 __host__ __device__ __forceinline__ int splits_for(int n_units, int units_per_split) {
@@ -83,6 +106,7 @@ struct DecodeParams {
   int max_blocks;              // MB
   int block_size;              // bs
   int window;
+  int num_sinks;               // attention sinks kept besides the window
   float scale_log2;            // scale * log2(e)
   int units_per_split;
   int num_splits;              // grid.x
@@ -116,7 +140,7 @@ int decode_checks(const void* q, int32_t num_seqs, int32_t num_q_heads, const vo
                   const int32_t* block_tables, int32_t max_blocks, const int32_t* context_lens,
                   const void* out);
 int decode_plan(int num_seqs, int num_q_heads, const pkv_cache_layout* layout, int max_blocks,
-                int window, int* head_chunk, int* num_head_chunks, int* ntiles,
+                int window, int num_sinks, int* head_chunk, int* num_head_chunks, int* ntiles,
                 int* units_per_split, int* num_splits);
 int pool_tensor_map(CUtensorMap* map, const void* pool, const pkv_cache_layout* layout);
 int status_of(cudaError_t e);

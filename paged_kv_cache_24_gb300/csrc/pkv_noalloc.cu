@@ -61,8 +61,9 @@ extern "C" int pkv_decode_noalloc(const void* q, int32_t num_seqs, int32_t num_q
   if (cudaGetDevice(&device) != cudaSuccess) return PKV_ERR_CUDA;
   pkv::DecodeParams p{};
   int ntiles = 1;
-  rc = pkv::decode_plan(num_seqs, num_q_heads, layout, max_blocks_per_seq, window, &p.head_chunk,
-                        &p.num_head_chunks, &ntiles, &p.units_per_split, &p.num_splits);
+  rc = pkv::decode_plan(num_seqs, num_q_heads, layout, max_blocks_per_seq, window, 0,
+                        &p.head_chunk, &p.num_head_chunks, &ntiles, &p.units_per_split,
+                        &p.num_splits);
   if (rc != PKV_OK) return rc;
 
   if (p.num_splits > 1) {

@@ -13,7 +13,8 @@ The block pool and its LIFO free list follow the block allocator of
 free block ids, ``pop()`` to allocate, ``MemoryError`` when exhausted).
 
 Poisoning: every pool slot that no sequence's context covers holds NaN (and,
-with ``poison_outside_window``, every slot before a sequence's window start),
+with ``poison_outside_window``, every slot before a sequence's window start
+other than its attention sinks),
 so a kernel that reads a slot it should not shows NaN in its output.  The slot
 each step's append will write also starts as NaN.
 """
@@ -86,6 +87,7 @@ class WorkloadSpec:
     geom_mean: float = 512.0
     lens_are_pre_append: bool = False
     window: int = 0
+    num_sinks: int = 0                # with a window: first positions kept (attention sinks)
     steps: int = 1
     pool_factor: float = 1.2          # pool = ceil(factor * blocks needed), shuffled ids
     explicit_pool: Optional[int] = None
@@ -270,7 +272,9 @@ def make_workload(spec: WorkloadSpec, device="cpu", poison: bool = True,
             lo = 0
             if poison_outside_window and spec.window > 0:
                 lo = max(0, int(lens_steps[0, b]) - spec.window)
-            t = np.arange(lo, int(pre[b]), dtype=np.int64)
+            keep = np.arange(0, min(lo, spec.num_sinks), dtype=np.int64)  # sink positions
+            t = np.concatenate([keep, np.arange(lo, int(pre[b]), dtype=np.int64)])
+            t = t[t < int(pre[b])]
             if t.size:
                 valid[block_tables[b, t // bs] * bs + t % bs] = True
         bad = torch.from_numpy(np.nonzero(~valid)[0]).to(device)

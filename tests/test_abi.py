@@ -109,17 +109,29 @@ def test_plan(pkv_lib, cfg, expect):
                                    num_sms=152) == expect
 
 
+def _units_needed(L, window, sinks):
+    """Units a length-L context attends: the sink units, then the window units
+    (one range from unit 0 when they meet)."""
+    if L == 0:
+        return 0
+    lo = max(0, L - window) if window > 0 else 0
+    s = min(sinks, lo) if window > 0 else 0
+    su, wu0 = -(-s // 16), lo // 16
+    if su >= wu0:
+        su = wu0 = 0
+    return su + (L + 15) // 16 - wu0
+
+
 def test_plan_covers_every_length(pkv_lib):
     """The grid's split count bounds the splits any valid length needs."""
     lay = pkv_lib.CacheLayout(5000, 8, 32, 128, 2)
     for mb in (1, 3, 17, 64):
         for window in (0, 1, 15, 16, 17, 100, 4096):
-            for tps in (0, 16, 64, 2048):
-                t, ns = pkv_lib.pkv_decode_plan(8, 32, lay, mb, window, tps, num_sms=152)
-                units = t // 16
-                worst = 0
-                for L in range(0, mb * 32 + 1):
-                    lo = max(0, L - window) if window > 0 else 0
-                    n = 0 if L == 0 else (L + 15) // 16 - lo // 16
-                    worst = max(worst, -(-n // units))
-                assert worst <= ns
+            for sinks in (0, 4, 16, 40):
+                for tps in (0, 16, 64, 2048):
+                    t, ns = pkv_lib.pkv_decode_plan(8, 32, lay, mb, window, tps, num_sms=152,
+                                                    num_sinks=sinks)
+                    units = t // 16
+                    worst = max(-(-_units_needed(L, window, sinks) // units)
+                                for L in range(0, mb * 32 + 1))
+                    assert worst <= ns

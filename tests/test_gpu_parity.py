@@ -127,6 +127,48 @@ def test_small_cases_all_outputs(pkv_lib, oracle_lib, name, over, splits):
         check_close(out, ref, spec.dtype)
 
 
+SINKS = [
+    # name, spec overrides, num_sinks, tokens_per_split values
+    ("bf16_g4_w37_s4", dict(dtype=torch.bfloat16, num_seqs=8, num_q_heads=8, num_kv_heads=2,
+                            head_dim=128, block_size=16,
+                            lens=[1, 5, 20, 37, 38, 41, 700, 2000], window=37), 4, (0, 16, 64)),
+    ("fp16_d64_bs32_w100_s20", dict(dtype=torch.float16, num_seqs=5, num_q_heads=4,
+                                    num_kv_heads=4, head_dim=64, block_size=32,
+                                    lens=[19, 110, 121, 130, 1500], window=100), 20, (0, 32)),
+    ("fp32_w16_s4", dict(dtype=torch.float32, num_seqs=4, num_q_heads=8, num_kv_heads=2,
+                         head_dim=128, lens=[3, 17, 21, 400], window=16), 4, (0, 16)),
+    ("bf16_s16_aligned", dict(dtype=torch.bfloat16, num_seqs=3, num_q_heads=32, num_kv_heads=2,
+                              head_dim=128, lens=[33, 64, 999], window=32), 16, (0, 16)),
+]
+
+
+@pytest.mark.parametrize("name,over,sinks,splits", SINKS, ids=[c[0] for c in SINKS])
+def test_attention_sinks(pkv_lib, oracle_lib, name, over, sinks, splits):
+    spec = config_spec(0, explicit_pool=None, lens_are_pre_append=False, num_sinks=sinks,
+                       **over)
+    w = make_workload(spec, device="cuda", poison_outside_window=True)
+    slots = pkv_lib.pkv_slot_mapping(w.block_tables, w.pos_steps[0].contiguous(),
+                                     spec.block_size)
+    pkv_lib.pkv_append(w.k_steps[0], w.v_steps[0], slots, w.k_cache, w.v_cache)
+    kc_h, vc_h = w.k_cache.cpu(), w.v_cache.cpu()
+    ref = oracle.decode(w.q_steps[0].cpu(), kc_h, vc_h, w.block_tables.cpu().numpy(),
+                        w.lens_steps[0].cpu().numpy(), spec.window, w.scale, num_sinks=sinks)
+    for tps in splits:
+        out = pkv_lib.pkv_decode(w.q_steps[0], w.k_cache, w.v_cache, w.block_tables,
+                                 w.lens_steps[0].contiguous(), spec.window, w.scale,
+                                 tokens_per_split=tps, num_sinks=sinks)
+        torch.cuda.synchronize()
+        check_close(out, ref, spec.dtype)
+    # fused append + decode with sinks, from the pre-append pool
+    w2 = make_workload(spec, device="cuda", poison_outside_window=True)
+    out = pkv_lib.pkv_append_decode(w2.q_steps[0], w2.k_steps[0], w2.v_steps[0], w2.k_cache,
+                                    w2.v_cache, w2.block_tables, w2.lens_steps[0].contiguous(),
+                                    spec.window, w2.scale, num_sinks=sinks)
+    torch.cuda.synchronize()
+    check_close(out, ref, spec.dtype)
+    assert torch.equal(_bits(w2.k_cache.cpu()), _bits(kc_h))
+
+
 def test_single_token_is_exact(pkv_lib, oracle_lib):
     for dt in (torch.float16, torch.bfloat16, torch.float32):
         spec = config_spec(0, dtype=dt, num_seqs=3, num_q_heads=4, num_kv_heads=2,
