@@ -79,6 +79,19 @@ def _load():
         lib.oracle_decode.argtypes = [c_vp, c_i32, c_i32, c_vp, c_vp, c_i64, c_i32, c_i32, c_i32,
                                       c_i32, c_vp, c_i32, c_vp, c_i32, c_i32, c_dbl, c_vp, c_i64,
                                       c_vp, c_i32]
+        lib.oracle_e4m3_to_double.restype = c_dbl
+        lib.oracle_e4m3_to_double.argtypes = [ctypes.c_uint8]
+        lib.oracle_encode_e4m3.restype = None
+        lib.oracle_encode_e4m3.argtypes = [c_vp, c_i64, c_vp]
+        lib.oracle_quantize_row.restype = ctypes.c_float
+        lib.oracle_quantize_row.argtypes = [c_vp, c_i32, c_vp]
+        lib.oracle_append_fp8.restype = ctypes.c_int
+        lib.oracle_append_fp8.argtypes = [c_vp, c_vp, c_i32, c_vp, c_i64, c_vp, c_vp, c_vp, c_vp,
+                                          c_i64, c_i32, c_i32, c_i32]
+        lib.oracle_decode_fp8.restype = ctypes.c_int
+        lib.oracle_decode_fp8.argtypes = [c_vp, c_i32, c_i32, c_i32, c_vp, c_vp, c_vp, c_vp,
+                                          c_i64, c_i32, c_i32, c_i32, c_vp, c_i32, c_vp, c_i32,
+                                          c_i32, c_dbl, c_vp, c_i64, c_vp, c_i32]
         lib.oracle_max_threads.restype = ctypes.c_int
         lib.oracle_max_threads.argtypes = []
         _lib = lib
@@ -224,4 +237,110 @@ def decode(q, k_cache, v_cache, block_tables, context_lens, window: int, scale: 
                                int(threads))
     if check and rc != 0:
         raise ValueError(f"oracle_decode failed with code {rc}")
+    return out if pairs is not None else out.reshape(B, Hq, D)
+
+
+# ---------------------------------------------------------------------------
+# FP8 (E4M3) cache: codes + one float32 scale per (token, kv head) row
+
+
+F8 = 3
+
+
+def _u8(x):
+    if type(x).__module__.startswith("torch"):
+        import torch
+        x = x.contiguous()
+        if x.dtype != torch.uint8:
+            x = x.view(torch.uint8)
+        return x.numpy()
+    x = np.ascontiguousarray(x)
+    if x.dtype != np.uint8:
+        raise TypeError("FP8 codes must be uint8")
+    return x
+
+
+def _f32(x):
+    if type(x).__module__.startswith("torch"):
+        x = x.contiguous().numpy()
+    x = np.ascontiguousarray(x)
+    if x.dtype != np.float32:
+        raise TypeError("expected float32")
+    return x
+
+
+def e4m3_to_double(codes) -> np.ndarray:
+    """Value of each E4M3 code (uint8 array) in float64."""
+    return decode_elements(_u8(codes), F8)
+
+
+def encode_e4m3(x) -> np.ndarray:
+    """Nearest E4M3 code (ties to even, saturating) of each float32."""
+    x = np.ascontiguousarray(x, dtype=np.float32)
+    out = np.empty(x.shape, dtype=np.uint8)
+    _load().oracle_encode_e4m3(_ptr(x), x.size, _ptr(out))
+    return out
+
+
+def quantize_rows(x):
+    """Quantise each row of a float32 matrix [n, D]: (codes uint8 [n, D], scales float32 [n])."""
+    x = np.ascontiguousarray(x, dtype=np.float32)
+    n, d = x.shape
+    codes = np.empty((n, d), dtype=np.uint8)
+    scales = np.empty(n, dtype=np.float32)
+    lib = _load()
+    for i in range(n):
+        scales[i] = lib.oracle_quantize_row(_ptr(x[i]), d, codes[i].ctypes.data)
+    return codes, scales
+
+
+def append_fp8(k, v, slot_mapping_, k_codes, v_codes, k_scale, v_scale) -> None:
+    """Quantise and write each token's K/V rows ([T, Hkv, D], fp16/bf16/fp32) into
+    FP8 pools ([NB, Hkv, bs, D] uint8 codes, [NB, Hkv, bs] float32 scales), in place."""
+    kr, kd = _as_raw(k)
+    vr, vd = _as_raw(v)
+    if kd != vd:
+        raise TypeError("k and v dtypes differ")
+    for c in (k_codes, v_codes, k_scale, v_scale):
+        contiguous = c.is_contiguous() if hasattr(c, "is_contiguous") else c.flags.c_contiguous
+        if not contiguous:
+            raise ValueError("pools must be contiguous so they can be written in place")
+    kc, vc = _u8(k_codes), _u8(v_codes)
+    ks, vs = _f32(k_scale), _f32(v_scale)
+    slots = _int_array(slot_mapping_, np.int64)
+    nb, hkv, bs, d = kc.shape
+    rc = _load().oracle_append_fp8(_ptr(kr), _ptr(vr), kd, _ptr(slots), slots.size, _ptr(kc),
+                                   _ptr(vc), _ptr(ks), _ptr(vs), nb, hkv, bs, d)
+    if rc != 0:
+        raise ValueError(f"oracle_append_fp8 failed with code {rc}")
+
+
+def decode_fp8(q, k_codes, v_codes, k_scale, v_scale, block_tables, context_lens, window: int,
+               scale: float, pairs=None, threads: int = 0, check: bool = True,
+               num_sinks: int = 0) -> np.ndarray:
+    """Paged decode over FP8 pools (stored value = code * row scale), in float64."""
+    qr, qd = _as_raw(q)
+    kc, vc = _u8(k_codes), _u8(v_codes)
+    ks, vs = _f32(k_scale), _f32(v_scale)
+    bt = _int_array(block_tables, np.int32)
+    lens = _int_array(context_lens, np.int32)
+    B, Hq, D = qr.shape
+    nb, hkv, bs, d2 = kc.shape
+    if d2 != D:
+        raise ValueError("head_dim mismatch")
+    if pairs is None:
+        pairs_arr, n = None, B * Hq
+    else:
+        pairs_arr = _int_array(pairs, np.int32).reshape(-1, 2)
+        n = pairs_arr.shape[0]
+        if n == 0:
+            return np.empty((0, D), dtype=np.float64)
+    out = np.empty((n, D), dtype=np.float64)
+    rc = _load().oracle_decode_fp8(_ptr(qr), qd, B, Hq, _ptr(kc), _ptr(vc), _ptr(ks), _ptr(vs),
+                                   nb, hkv, bs, D, _ptr(bt), bt.shape[1], _ptr(lens),
+                                   int(window), int(num_sinks), float(scale),
+                                   None if pairs_arr is None else _ptr(pairs_arr), n, _ptr(out),
+                                   int(threads))
+    if check and rc != 0:
+        raise ValueError(f"oracle_decode_fp8 failed with code {rc}")
     return out if pairs is not None else out.reshape(B, Hq, D)

@@ -34,6 +34,15 @@
  *     window; num_sinks = 0 is the plain window.
  *   - Inputs of type fp16 / bf16 are widened exactly to double; all
  *     arithmetic is in double with libm exp().
+ *   - Quantised cache ("Building a Memory-Compressed Attention Engine with
+ *     KV Caching", Extending, item 2: INT8 or FP8 quantisation of the cached
+ *     keys and values): FP8 E4M3 codes with one float32 scale per (token, kv
+ *     head) row, stored value = code * scale.  A row is quantised when it is
+ *     appended: scale = absmax / 448 (448 = largest E4M3 value), code =
+ *     E4M3(x * (448 / absmax)) rounded to nearest, ties to even, saturating;
+ *     an all-zero row gets scale 1.  The divisions and the product are single
+ *     IEEE float32 operations.  Decoding over such a cache attends over the
+ *     stored values code * scale, widened to double.
  *
  * Build: gcc -O2 -fopenmp -shared -fPIC pkv_oracle.c -o liboracle.so -lm
  * (no fast-math: the reference arithmetic must stay IEEE double).
@@ -46,7 +55,7 @@
 #include <omp.h>
 #endif
 
-enum { ORACLE_F32 = 0, ORACLE_F16 = 1, ORACLE_BF16 = 2 };
+enum { ORACLE_F32 = 0, ORACLE_F16 = 1, ORACLE_BF16 = 2, ORACLE_FP8 = 3 };
 
 enum {
   ORACLE_OK = 0,
@@ -82,6 +91,58 @@ double oracle_bf16_to_double(uint16_t bits) {
   return (double)f;
 }
 
+/* FP8 E4M3 ("fn" variant): 1 sign bit, 4 exponent bits (bias 7), 3 fraction
+ * bits; exponent 0 is subnormal (frac * 2^-9); S.1111.111 is NaN; there is no
+ * infinity.  Largest finite magnitude: 1.75 * 2^8 = 448. */
+double oracle_e4m3_to_double(uint8_t code) {
+  int sign = (code >> 7) & 1;
+  int expo = (code >> 3) & 0xf;
+  int frac = code & 0x7;
+  double mag;
+  if (expo == 15 && frac == 7) return NAN;
+  if (expo == 0) mag = ldexp((double)frac, -9);
+  else mag = ldexp((double)(8 + frac), expo - 10); /* (1 + frac/8) * 2^(e-7) */
+  return sign ? -mag : mag;
+}
+
+/* Nearest E4M3 code to a float32, ties to the even code, saturating to +-448:
+ * a brute-force search over the 127 finite non-negative codes. */
+uint8_t oracle_float_to_e4m3(float x) {
+  if (x != x) return 0x7f;
+  uint8_t sign = (x < 0.0f || (x == 0.0f && 1.0f / x < 0.0f)) ? 0x80 : 0x00;
+  double a = fabs((double)x);
+  int best = 0;
+  double best_err = INFINITY;
+  for (int c = 0; c <= 126; ++c) {
+    double err = fabs(oracle_e4m3_to_double((uint8_t)c) - a);
+    if (err < best_err || (err == best_err && (c & 1) == 0)) {
+      best = c;
+      best_err = err;
+    }
+  }
+  return (uint8_t)(sign | best);
+}
+
+/* Quantise one row of n float32 values: writes n codes, returns the scale. */
+float oracle_quantize_row(const float* x, int32_t n, uint8_t* codes) {
+  float absmax = 0.0f;
+  for (int32_t i = 0; i < n; ++i) {
+    float a = fabsf(x[i]);
+    if (a > absmax) absmax = a;
+  }
+  float scale = 1.0f, inv = 1.0f;
+  if (absmax > 0.0f) {
+    volatile float num = 448.0f; /* single float32 divisions, as the reading states */
+    scale = absmax / num;
+    inv = num / absmax;
+  }
+  for (int32_t i = 0; i < n; ++i) {
+    volatile float prod = x[i] * inv;
+    codes[i] = oracle_float_to_e4m3(prod);
+  }
+  return scale;
+}
+
 static double load_elem(const void* base, int64_t idx, int dtype) {
   switch (dtype) {
     case ORACLE_F32: return (double)((const float*)base)[idx];
@@ -92,7 +153,13 @@ static double load_elem(const void* base, int64_t idx, int dtype) {
 
 /* Vector forms, used by the tests to pin the decoders. */
 void oracle_decode_elements(const void* src, int64_t n, int32_t dtype, double* dst) {
-  for (int64_t i = 0; i < n; ++i) dst[i] = load_elem(src, i, dtype);
+  for (int64_t i = 0; i < n; ++i)
+    dst[i] = dtype == ORACLE_FP8 ? oracle_e4m3_to_double(((const uint8_t*)src)[i])
+                                 : load_elem(src, i, dtype);
+}
+
+void oracle_encode_e4m3(const float* src, int64_t n, uint8_t* dst) {
+  for (int64_t i = 0; i < n; ++i) dst[i] = oracle_float_to_e4m3(src[i]);
 }
 
 /* ---- slot mapping and append ([P2] Step 3, PagedKVCache.append) ---------- */
@@ -139,6 +206,42 @@ int oracle_append(const void* k, const void* v, const int64_t* slot_mapping, int
   return ORACLE_OK;
 }
 
+/* Append into an FP8 pool: each (token, kv head) row of k / v (fp16 / bf16 /
+ * fp32, `dtype`) is quantised on its own (see the reading at the top) and its
+ * codes and scale written to the slot; negative slots are skipped. */
+int oracle_append_fp8(const void* k, const void* v, int32_t dtype, const int64_t* slot_mapping,
+                      int64_t num_tokens, uint8_t* k_codes, uint8_t* v_codes, float* k_scale,
+                      float* v_scale, int64_t num_blocks, int32_t num_kv_heads,
+                      int32_t block_size, int32_t head_dim) {
+  if (!k || !v || !slot_mapping || !k_codes || !v_codes || !k_scale || !v_scale)
+    return ORACLE_ERR_ARG;
+  float* row = (float*)malloc((size_t)head_dim * sizeof(float));
+  if (!row) return ORACLE_ERR_NOMEM;
+  int rc = ORACLE_OK;
+  for (int64_t i = 0; i < num_tokens && rc == ORACLE_OK; ++i) {
+    int64_t slot = slot_mapping[i];
+    if (slot < 0) continue;
+    int64_t block = slot / block_size, r = slot % block_size;
+    if (block >= num_blocks) {
+      rc = ORACLE_ERR_BLOCK_ID;
+      break;
+    }
+    for (int32_t h = 0; h < num_kv_heads; ++h) {
+      int64_t dst_row = ((block * num_kv_heads + h) * block_size + r);
+      int64_t src = ((int64_t)i * num_kv_heads + h) * head_dim;
+      for (int pass = 0; pass < 2; ++pass) {
+        const void* x = pass ? v : k;
+        for (int32_t d = 0; d < head_dim; ++d) row[d] = (float)load_elem(x, src + d, dtype);
+        uint8_t* codes = (pass ? v_codes : k_codes) + dst_row * head_dim;
+        float sc = oracle_quantize_row(row, head_dim, codes);
+        (pass ? v_scale : k_scale)[dst_row] = sc;
+      }
+    }
+  }
+  free(row);
+  return rc;
+}
+
 /* ---- attention over a contiguous cache ([P2] Step 4, [P3] Step 3) -------- */
 
 /* out[d] = sum_t softmax_t(scale * q.K[t]) * V[t][d] for t in [0, T).
@@ -178,8 +281,10 @@ typedef struct {
   int32_t num_seqs, num_q_heads;
   const void* k_cache;
   const void* v_cache;
+  const float* k_scale; /* FP8 pools: per-row scales, else NULL */
+  const float* v_scale;
   int64_t num_blocks;
-  int32_t num_kv_heads, block_size, head_dim, dtype;
+  int32_t num_kv_heads, block_size, head_dim, dtype, kv_dtype;
   const int32_t* block_tables;
   int32_t max_blocks;
   const int32_t* context_lens;
@@ -234,10 +339,20 @@ static int decode_one(const decode_problem* p, int32_t b, int32_t h, double* out
       rc = ORACLE_ERR_BLOCK_ID;
       break;
     }
-    int64_t base = ((physical * p->num_kv_heads + hk) * p->block_size + row) * D;
-    for (int32_t d = 0; d < D; ++d) {
-      K[i * D + d] = load_elem(p->k_cache, base + d, p->dtype);
-      V[i * D + d] = load_elem(p->v_cache, base + d, p->dtype);
+    int64_t prow = (physical * p->num_kv_heads + hk) * p->block_size + row;
+    int64_t base = prow * D;
+    if (p->kv_dtype == ORACLE_FP8) {
+      /* stored value = code * scale of its row */
+      double ks = (double)p->k_scale[prow], vs = (double)p->v_scale[prow];
+      for (int32_t d = 0; d < D; ++d) {
+        K[i * D + d] = oracle_e4m3_to_double(((const uint8_t*)p->k_cache)[base + d]) * ks;
+        V[i * D + d] = oracle_e4m3_to_double(((const uint8_t*)p->v_cache)[base + d]) * vs;
+      }
+    } else {
+      for (int32_t d = 0; d < D; ++d) {
+        K[i * D + d] = load_elem(p->k_cache, base + d, p->kv_dtype);
+        V[i * D + d] = load_elem(p->v_cache, base + d, p->kv_dtype);
+      }
     }
     ++i;
   }
@@ -249,6 +364,9 @@ static int decode_one(const decode_problem* p, int32_t b, int32_t h, double* out
   free(q); free(K); free(V);
   return rc;
 }
+
+static int decode_pairs(const decode_problem* p, const int32_t* pairs, int64_t n_pairs,
+                        double* out, int32_t num_threads);
 
 /* Decode attention for a list of (sequence, query head) pairs.
  *   q            [num_seqs][num_q_heads][head_dim]        dtype
@@ -269,9 +387,38 @@ int oracle_decode(const void* q, int32_t num_seqs, int32_t num_q_heads,
   if (num_seqs < 0 || num_q_heads <= 0 || num_kv_heads <= 0 || head_dim <= 0 || block_size <= 0 ||
       max_blocks < 0 || num_q_heads % num_kv_heads != 0 || dtype < 0 || dtype > 2)
     return ORACLE_ERR_ARG;
-  decode_problem p = {q, num_seqs, num_q_heads, k_cache, v_cache, num_blocks, num_kv_heads,
-                      block_size, head_dim, dtype, block_tables, max_blocks, context_lens,
-                      window, num_sinks, scale};
+  decode_problem p = {q, num_seqs, num_q_heads, k_cache, v_cache, NULL, NULL, num_blocks,
+                      num_kv_heads, block_size, head_dim, dtype, dtype, block_tables,
+                      max_blocks, context_lens, window, num_sinks, scale};
+  return decode_pairs(&p, pairs, n_pairs, out, num_threads);
+}
+
+/* Decode over FP8 pools: k_codes / v_codes [NB][Hkv][bs][D] E4M3 codes,
+ * k_scale / v_scale [NB][Hkv][bs] float32; q has dtype q_dtype (fp16 / bf16 /
+ * fp32).  Otherwise as oracle_decode. */
+int oracle_decode_fp8(const void* q, int32_t q_dtype, int32_t num_seqs, int32_t num_q_heads,
+                      const uint8_t* k_codes, const uint8_t* v_codes, const float* k_scale,
+                      const float* v_scale, int64_t num_blocks, int32_t num_kv_heads,
+                      int32_t block_size, int32_t head_dim, const int32_t* block_tables,
+                      int32_t max_blocks, const int32_t* context_lens, int32_t window,
+                      int32_t num_sinks, double scale, const int32_t* pairs, int64_t n_pairs,
+                      double* out, int32_t num_threads) {
+  if (!q || !k_codes || !v_codes || !k_scale || !v_scale || !block_tables || !context_lens ||
+      !out)
+    return ORACLE_ERR_ARG;
+  if (num_seqs < 0 || num_q_heads <= 0 || num_kv_heads <= 0 || head_dim <= 0 || block_size <= 0 ||
+      max_blocks < 0 || num_q_heads % num_kv_heads != 0 || q_dtype < 0 || q_dtype > 2)
+    return ORACLE_ERR_ARG;
+  decode_problem p = {q, num_seqs, num_q_heads, k_codes, v_codes, k_scale, v_scale, num_blocks,
+                      num_kv_heads, block_size, head_dim, q_dtype, ORACLE_FP8, block_tables,
+                      max_blocks, context_lens, window, num_sinks, scale};
+  return decode_pairs(&p, pairs, n_pairs, out, num_threads);
+}
+
+static int decode_pairs(const decode_problem* pp, const int32_t* pairs, int64_t n_pairs,
+                        double* out, int32_t num_threads) {
+  const decode_problem p = *pp;
+  const int32_t num_seqs = p.num_seqs, num_q_heads = p.num_q_heads, head_dim = p.head_dim;
   const int64_t total = pairs ? n_pairs : (int64_t)num_seqs * num_q_heads;
   int rc = ORACLE_OK;
 #ifdef _OPENMP
