@@ -33,8 +33,8 @@ MUTANTS = {
     "row_index": ("int64_t row = t % p->block_size;",
                   "int64_t row = (t / p->block_size) % p->block_size;"),
     "token_major_offset": (
-        "int64_t base = ((physical * p->num_kv_heads + hk) * p->block_size + row) * D;",
-        "int64_t base = ((physical * p->block_size + row) * p->num_kv_heads + hk) * D;"),
+        "int64_t prow = (physical * p->num_kv_heads + hk) * p->block_size + row;",
+        "int64_t prow = (physical * p->block_size + row) * p->num_kv_heads + hk;"),
     "scale_squared": ("s[t] = scale * dot;", "s[t] = scale * scale * dot;"),
     "f16_exponent_bias": ("mag = ldexp((double)(1024 + frac), expo - 25);",
                           "mag = ldexp((double)(1024 + frac), expo - 24);"),
