@@ -64,7 +64,8 @@ def hbm_peak():
 def step_bytes(w):
     """Algorithmic bytes of one step of workload `w` at each of its steps."""
     spec = w.spec
-    e = torch.tensor([], dtype=spec.dtype).element_size()
+    e = torch.tensor([], dtype=spec.dtype).element_size()   # q / out / new tokens
+    row = d_row = spec.head_dim * (1 if spec.kv_fp8 else e) + (4 if spec.kv_fp8 else 0)
     B, hq, hkv, d, bs = (spec.num_seqs, spec.num_q_heads, spec.num_kv_heads, spec.head_dim,
                          spec.block_size)
     out = []
@@ -73,10 +74,10 @@ def step_bytes(w):
         lo = np.maximum(L - spec.window, 0) if spec.window > 0 else np.zeros_like(L)
         ctx = int((L - lo).sum())
         pages = int((((L - 1) // bs) - (lo // bs) + 1).clip(min=0).sum())
-        kv = ctx * 2 * hkv * d * e
+        kv = ctx * 2 * hkv * row            # one K row and one V row per (token, kv head)
         qo = 2 * B * hq * d * e
         meta = pages * 4 + B * 4
-        append = B * hkv * d * e * 2 * 2 + B * 8
+        append = B * hkv * (d * e + d_row) * 2 + B * 8  # new rows read, pool rows written
         out.append({"kv": kv, "decode": kv + qo + meta, "append": append,
                     "step": kv + qo + meta + append, "tokens_kvhead": ctx * hkv})
     return out
@@ -177,6 +178,8 @@ class OracleSampler:
         spec = w.spec
         self.e = torch.tensor([], dtype=spec.dtype).element_size()
         self.kc, self.vc = w.k_cache.cpu(), w.v_cache.cpu()
+        self.ks = w.k_scale.cpu() if w.k_scale is not None else None
+        self.vs = w.v_scale.cpu() if w.v_scale is not None else None
         self.bt = w.block_tables.cpu().numpy()
         self.lens = w.lens_steps[0].cpu().numpy()
         self.q = w.q_steps[0].cpu()
@@ -189,13 +192,18 @@ class OracleSampler:
         flat = rng.choice(total, size=min(n_pairs, total), replace=False)
         pairs = np.stack([flat // spec.num_q_heads, flat % spec.num_q_heads], 1).astype(np.int32)
         t0 = time.perf_counter()
-        self.oracle.decode(self.q, self.kc, self.vc, self.bt, self.lens, spec.window,
-                           self.w.scale, pairs=pairs, threads=self.threads)
+        if spec.kv_fp8:
+            self.oracle.decode_fp8(self.q, self.kc, self.vc, self.ks, self.vs, self.bt, self.lens,
+                                   spec.window, self.w.scale, pairs=pairs, threads=self.threads)
+        else:
+            self.oracle.decode(self.q, self.kc, self.vc, self.bt, self.lens, spec.window,
+                               self.w.scale, pairs=pairs, threads=self.threads)
         dt = time.perf_counter() - t0
         L = self.lens[pairs[:, 0]].astype(np.int64)
         lo = np.maximum(L - spec.window, 0) if spec.window > 0 else 0
         G = spec.num_q_heads // spec.num_kv_heads
-        kvb = float(((L - lo) * 2 * spec.head_dim * self.e).sum()) / G
+        row = spec.head_dim + 4 if spec.kv_fp8 else spec.head_dim * self.e
+        kvb = float(((L - lo) * 2 * row).sum()) / G
         return kvb / dt, dt, len(pairs)
 
     def rate_for(self, target_s):
@@ -307,11 +315,17 @@ def main(argv=None):
     out = torch.empty_like(w.q_steps[0])
     plan = pkv.pkv_decode_plan(spec.num_seqs, spec.num_q_heads, pkv.cache_layout(w.k_cache),
                                w.max_blocks, spec.window)
-    fused = args.path == "fused"
+    # FP8 pools append through the quantising kernel (no fused form)
+    fused = args.path == "fused" and not spec.kv_fp8
     launches_per_step = (1 if fused else 2) + (1 if plan[1] > 1 else 0)
 
     def do_append(i):
-        if not fused:
+        if fused:
+            return
+        if spec.kv_fp8:
+            pkv.pkv_append_fp8(w.k_steps[i], w.v_steps[i], slots[i], w.k_cache, w.v_cache,
+                               w.k_scale, w.v_scale)
+        else:
             pkv.pkv_append(w.k_steps[i], w.v_steps[i], slots[i], w.k_cache, w.v_cache)
 
     def do_decode(i):
@@ -321,7 +335,7 @@ def main(argv=None):
                                   out=out)
         else:
             pkv.pkv_decode(w.q_steps[i], w.k_cache, w.v_cache, w.block_tables, lens[i],
-                           spec.window, w.scale, out=out)
+                           spec.window, w.scale, out=out, k_scale=w.k_scale, v_scale=w.v_scale)
 
     def step(s):
         do_append(s % S)
@@ -403,7 +417,7 @@ def main(argv=None):
             "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-            "dtype": DTYPE_NAME[spec.dtype], "data": "synthetic",
+            "dtype": "e4m3+f16" if spec.kv_fp8 else DTYPE_NAME[spec.dtype], "data": "synthetic",
             "config": {
                 "workload": args.workload + ("" if not over else "-reduced"),
                 "num_seqs": spec.num_seqs,
@@ -419,7 +433,7 @@ def main(argv=None):
             },
             "tokens_per_s": tokens_per_s,
             "pct_of_hbm_peak": 100.0 * value / (world * peak),
-            "path": args.path,
+            "path": "fused" if fused else "separate",
             "roofline": {"bound": "hbm",
                          "kernel": ("fused append + decode (split-K) + LSE combine" if fused
                                     else "decode (split-K decode + LSE combine)"),
@@ -448,7 +462,8 @@ def run_e2e(pkv, w, spec, args, sbytes, pg, world):
     S = w.steps
     step = pkv.DecodeStep(w.k_cache, w.v_cache, spec.num_seqs, spec.num_q_heads, w.max_blocks,
                           spec.window, w.scale, copy_block_tables=True, num_buffers=S,
-                          fused=args.path == "fused")
+                          fused=args.path == "fused" and not spec.kv_fp8,
+                          k_scale=w.k_scale, v_scale=w.v_scale)
     for s in range(S):
         h = step.host[s]
         h["q"].copy_(w.q_steps[s])

@@ -46,7 +46,9 @@ extern "C" {
 typedef enum pkv_dtype {
   PKV_FLOAT32 = 0,
   PKV_FLOAT16 = 1,
-  PKV_BFLOAT16 = 2
+  PKV_BFLOAT16 = 2,
+  PKV_FP8_E4M3 = 3  /* pools only: E4M3 codes + one float32 scale per (token, kv head)
+                       row; see pkv_append_fp8.  q, out, k_new, v_new are then fp16. */
 } pkv_dtype;
 
 typedef enum pkv_status {
@@ -182,7 +184,29 @@ typedef struct pkv_decode_options {
   int32_t tokens_per_split; /* a multiple of 16 up to 2048, or 0 for the library plan */
   const void* k_new;        /* both non-NULL: fused append of position L-1, as in    */
   const void* v_new;        /* pkv_append_decode; both NULL: decode only             */
+  const float* k_scale;     /* FP8 pools: [NB][Hkv][bs] row scales, 16-byte aligned;  */
+  const float* v_scale;     /* NULL otherwise                                         */
 } pkv_decode_options;
+
+/*
+ * pkv_append_fp8 -- quantise each new token's K and V rows into FP8 pools.
+ *   ("Building a Memory-Compressed Attention Engine with KV Caching",
+ *   Extending, item 2: INT8 or FP8 quantisation of the cached keys and
+ *   values cuts the cache's memory traffic.)
+ *   k, v        [num_tokens][num_kv_heads][head_dim], dtype in_dtype (fp32, fp16
+ *               or bf16)
+ *   slot_mapping as in pkv_append (negative or out-of-pool slots are skipped)
+ *   k_cache, v_cache  E4M3 code pools [NB][Hkv][bs][D] (layout->dtype ==
+ *               PKV_FP8_E4M3), k_scale, v_scale [NB][Hkv][bs] float32.
+ *   Each (token, kv head) row is quantised on its own: scale = absmax / 448,
+ *   code_d = E4M3(x_d * (448 / absmax)) rounded to nearest even, saturating;
+ *   an all-zero row gets scale 1.  The stored value is code * scale.  Division
+ *   and product are single IEEE float32 operations, so the codes are exactly
+ *   reproducible.  head_dim 64 or 128.
+ */
+int pkv_append_fp8(const void* k, const void* v, int32_t in_dtype, const int64_t* slot_mapping,
+                   int64_t num_tokens, void* k_cache, void* v_cache, float* k_scale,
+                   float* v_scale, const pkv_cache_layout* layout, void* stream);
 
 /*
  * pkv_decode_ex -- pkv_decode with every option.
@@ -193,6 +217,9 @@ typedef struct pkv_decode_options {
  *   positions [0, min(s, lo)) and [lo, L), lo = max(0, L - w).  The other
  *   arguments, the errors and the workspace are those of pkv_decode; k_cache
  *   and v_cache are written only with the fused append.
+ *   FP8 pools (layout->dtype == PKV_FP8_E4M3, head_dim 128): the attended
+ *   values are code * row scale; q and out are fp16; k_scale and v_scale are
+ *   required; the fused append is not available for them (PKV_ERR_UNSUPPORTED).
  */
 int pkv_decode_ex(const void* q, int32_t num_seqs, int32_t num_q_heads, void* k_cache,
                   void* v_cache, const pkv_cache_layout* layout, const int32_t* block_tables,

@@ -16,7 +16,9 @@ import torch
 from . import _build
 
 PKV_OK = 0
+PKV_FP8_E4M3 = 3
 _DTYPES = {torch.float32: 0, torch.float16: 1, torch.bfloat16: 2}
+_POOL_DTYPES = {**_DTYPES, torch.uint8: PKV_FP8_E4M3}  # uint8 pools hold E4M3 codes
 
 
 class PkvError(RuntimeError):
@@ -31,7 +33,8 @@ class DecodeOptions(ctypes.Structure):
     """Mirror of ``pkv_decode_options``."""
     _fields_ = [("window", ctypes.c_int32), ("num_sinks", ctypes.c_int32),
                 ("tokens_per_split", ctypes.c_int32), ("k_new", ctypes.c_void_p),
-                ("v_new", ctypes.c_void_p)]
+                ("v_new", ctypes.c_void_p), ("k_scale", ctypes.c_void_p),
+                ("v_scale", ctypes.c_void_p)]
 
 
 class CacheLayout(ctypes.Structure):
@@ -72,6 +75,7 @@ def load_library():
                                   i32, vp],
             "pkv_decode_ex": [vp, i32, i32, vp, vp, lay, vp, i32, vp, f32, vp,
                               ctypes.POINTER(DecodeOptions), vp],
+            "pkv_append_fp8": [vp, vp, i32, vp, i64, vp, vp, vp, vp, lay, vp],
             "pkv_decode_plan": [i32, i32, lay, i32, i32, i32, i32, i32, ctypes.POINTER(i32),
                                 ctypes.POINTER(i32)],
             "pkv_release_workspaces": [],
@@ -107,15 +111,32 @@ def _stream(stream) -> int:
 
 
 def cache_layout(cache: torch.Tensor) -> CacheLayout:
-    """Layout of a head-major pool tensor [num_blocks, num_kv_heads, block_size, head_dim]."""
+    """Layout of a head-major pool tensor [num_blocks, num_kv_heads, block_size, head_dim]
+    (a uint8 pool holds FP8 E4M3 codes)."""
     if cache.dim() != 4:
         raise ValueError("cache must be [num_blocks, num_kv_heads, block_size, head_dim]")
-    if cache.dtype not in _DTYPES:
+    if cache.dtype not in _POOL_DTYPES:
         raise TypeError(f"unsupported cache dtype {cache.dtype}")
     if not cache.is_contiguous():
         raise ValueError("cache must be contiguous")
     nb, hkv, bs, d = cache.shape
-    return CacheLayout(nb, hkv, bs, d, _DTYPES[cache.dtype])
+    return CacheLayout(nb, hkv, bs, d, _POOL_DTYPES[cache.dtype])
+
+
+def _compute_dtype(cache: torch.Tensor):
+    """dtype of q / out / new tokens for a pool (fp16 for FP8 pools)."""
+    return torch.float16 if cache.dtype == torch.uint8 else cache.dtype
+
+
+def _check_scales(k_cache, k_scale, v_scale):
+    if k_cache.dtype != torch.uint8:
+        _require(k_scale is None and v_scale is None, "scales are only for FP8 (uint8) pools")
+        return
+    shape = tuple(k_cache.shape[:3])
+    for sc in (k_scale, v_scale):
+        _require(sc is not None and sc.dtype == torch.float32 and tuple(sc.shape) == shape
+                 and sc.is_contiguous() and sc.device.type == "cuda",
+                 f"FP8 pools need contiguous float32 scales of shape {shape}")
 
 
 def _require(cond: bool, msg: str) -> None:
@@ -167,15 +188,19 @@ def pkv_append(k: torch.Tensor, v: torch.Tensor, slot_mapping: torch.Tensor,
 def pkv_decode(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
                block_tables: torch.Tensor, context_lens: torch.Tensor, window: int,
                scale: float, out: torch.Tensor | None = None, tokens_per_split: int = 0,
-               stream=None, num_sinks: int = 0) -> torch.Tensor:
+               stream=None, num_sinks: int = 0, k_scale: torch.Tensor | None = None,
+               v_scale: torch.Tensor | None = None) -> torch.Tensor:
     """Decode attention of q [B, Hq, D] over the paged context; returns out [B, Hq, D].
-    With a window, ``num_sinks`` first positions are attended as well."""
-    _on_cuda(q, k_cache, v_cache, block_tables, context_lens, out)
+    With a window, ``num_sinks`` first positions are attended as well.  FP8 pools
+    (uint8 codes) take their row scales and fp16 q."""
+    _on_cuda(q, k_cache, v_cache, block_tables, context_lens, out, k_scale, v_scale)
     layout = cache_layout(k_cache)
     _require(v_cache.shape == k_cache.shape and v_cache.dtype == k_cache.dtype
              and v_cache.is_contiguous(), "v_cache must match k_cache")
+    _check_scales(k_cache, k_scale, v_scale)
     _require(q.dim() == 3 and q.shape[2] == layout.head_dim and q.is_contiguous()
-             and q.dtype == k_cache.dtype, "q must be contiguous [B, Hq, D] of the cache dtype")
+             and q.dtype == _compute_dtype(k_cache),
+             "q must be contiguous [B, Hq, D] of the cache's compute dtype")
     B, Hq, D = q.shape
     _require(block_tables.dtype == torch.int32 and block_tables.dim() == 2
              and block_tables.shape[0] == B and block_tables.is_contiguous(),
@@ -186,12 +211,36 @@ def pkv_decode(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
         out = torch.empty_like(q)
     _require(out.shape == q.shape and out.dtype == q.dtype and out.is_contiguous(),
              "out must be contiguous and shaped like q")
-    opts = DecodeOptions(int(window), int(num_sinks), int(tokens_per_split), None, None)
+    opts = DecodeOptions(int(window), int(num_sinks), int(tokens_per_split), None, None,
+                         _ptr(k_scale) or None, _ptr(v_scale) or None)
     _check("pkv_decode", load_library().pkv_decode_ex(
         _ptr(q), B, Hq, _ptr(k_cache), _ptr(v_cache), ctypes.byref(layout),
         _ptr(block_tables), block_tables.shape[1], _ptr(context_lens), float(scale), _ptr(out),
         ctypes.byref(opts), _stream(stream)))
     return out
+
+
+def pkv_append_fp8(k: torch.Tensor, v: torch.Tensor, slot_mapping: torch.Tensor,
+                   k_cache: torch.Tensor, v_cache: torch.Tensor, k_scale: torch.Tensor,
+                   v_scale: torch.Tensor, stream=None) -> None:
+    """Quantise k[i], v[i] ([T, Hkv, D], fp32/fp16/bf16) into the FP8 pools (uint8
+    codes [NB, Hkv, bs, D], float32 row scales [NB, Hkv, bs]) at slot_mapping[i]."""
+    _on_cuda(k, v, slot_mapping, k_cache, v_cache, k_scale, v_scale)
+    layout = cache_layout(k_cache)
+    _require(k_cache.dtype == torch.uint8, "pkv_append_fp8 writes uint8 (E4M3) pools")
+    _require(v_cache.shape == k_cache.shape and v_cache.dtype == torch.uint8
+             and v_cache.is_contiguous(), "v_cache must match k_cache")
+    _check_scales(k_cache, k_scale, v_scale)
+    T = k.shape[0]
+    shape = (T, layout.num_kv_heads, layout.head_dim)
+    _require(tuple(k.shape) == shape and tuple(v.shape) == shape and k.dtype == v.dtype
+             and k.dtype in _DTYPES and k.is_contiguous() and v.is_contiguous(),
+             f"k and v must be contiguous {shape} fp32/fp16/bf16")
+    _require(slot_mapping.dtype == torch.int64 and slot_mapping.numel() == T
+             and slot_mapping.is_contiguous(), "slot_mapping must be int64 [T]")
+    _check("pkv_append_fp8", load_library().pkv_append_fp8(
+        _ptr(k), _ptr(v), _DTYPES[k.dtype], _ptr(slot_mapping), T, _ptr(k_cache), _ptr(v_cache),
+        _ptr(k_scale), _ptr(v_scale), ctypes.byref(layout), _stream(stream)))
 
 
 def pkv_append_decode(q: torch.Tensor, k_new: torch.Tensor, v_new: torch.Tensor,
@@ -223,7 +272,7 @@ def pkv_append_decode(q: torch.Tensor, k_new: torch.Tensor, v_new: torch.Tensor,
     _require(out.shape == q.shape and out.dtype == q.dtype and out.is_contiguous(),
              "out must be contiguous and shaped like q")
     opts = DecodeOptions(int(window), int(num_sinks), int(tokens_per_split), _ptr(k_new),
-                         _ptr(v_new))
+                         _ptr(v_new), None, None)
     _check("pkv_append_decode", load_library().pkv_decode_ex(
         _ptr(q), B, Hq, _ptr(k_cache), _ptr(v_cache), ctypes.byref(layout), _ptr(block_tables),
         block_tables.shape[1], _ptr(context_lens), float(scale), _ptr(out), ctypes.byref(opts),

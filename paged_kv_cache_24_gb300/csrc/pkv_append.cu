@@ -53,7 +53,89 @@ __global__ void append_kernel(const uint4* __restrict__ k, const uint4* __restri
   v_cache[dst] = vv;
 }
 
+// FP8 pools: one warp per (token, kv head) row.  The row is quantised on its
+// own -- scale = absmax / 448, codes = E4M3(x * (448 / absmax)), round to
+// nearest even, saturating; an all-zero row gets scale 1 -- with IEEE float32
+// divisions and products, so the codes are reproducible bit for bit.
+template <typename Tin, int D>
+__global__ void append_fp8_kernel(const Tin* __restrict__ k, const Tin* __restrict__ v,
+                                  const int64_t* __restrict__ slots, int64_t num_tokens,
+                                  uint8_t* __restrict__ k_codes, uint8_t* __restrict__ v_codes,
+                                  float* __restrict__ k_scale, float* __restrict__ v_scale,
+                                  int64_t num_blocks, int num_kv_heads, int block_size) {
+  constexpr int PER = D / 32;  // elements per lane
+  pdl_launch_dependents();
+  pdl_wait_prior();
+  const int lane = threadIdx.x & 31;
+  const int64_t row = static_cast<int64_t>(blockIdx.x) * (blockDim.x / 32) + (threadIdx.x >> 5);
+  if (row >= num_tokens * num_kv_heads) return;
+  const int64_t tok = row / num_kv_heads;
+  const int h = static_cast<int>(row - tok * num_kv_heads);
+  const int64_t slot = slots[tok];
+  if (slot < 0 || slot >= num_blocks * block_size) return;
+  const int64_t blk = slot / block_size;
+  const int64_t dst_row = (blk * num_kv_heads + h) * block_size + (slot - blk * block_size);
+#pragma unroll
+  for (int pass = 0; pass < 2; ++pass) {
+    const Tin* src = (pass ? v : k) + row * D + lane * PER;
+    float x[PER];
+    float amax = 0.f;
+#pragma unroll
+    for (int i = 0; i < PER; ++i) {
+      x[i] = to_f32<Tin>(src[i]);
+      amax = fmaxf(amax, fabsf(x[i]));
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
+    float scale = 1.f, inv = 1.f;
+    if (amax > 0.f) {
+      scale = __fdiv_rn(amax, 448.f);
+      inv = __fdiv_rn(448.f, amax);
+    }
+    uint32_t packed = 0;
+#pragma unroll
+    for (int i = 0; i < PER; i += 2)
+      packed |= f32x2_to_e4m3x2(__fmul_rn(x[i], inv), __fmul_rn(x[i + 1], inv)) << (8 * i);
+    uint8_t* dst = (pass ? v_codes : k_codes) + dst_row * D + lane * PER;
+    if constexpr (PER == 4) {
+      *reinterpret_cast<uint32_t*>(dst) = packed;
+    } else {
+      *reinterpret_cast<uint16_t*>(dst) = static_cast<uint16_t>(packed);
+    }
+    if (lane == 0) (pass ? v_scale : k_scale)[dst_row] = scale;
+  }
+}
+
 }  // namespace
+
+cudaError_t launch_append_fp8(int in_dtype, const void* k, const void* v, const int64_t* slots,
+                              int64_t num_tokens, void* k_codes, void* v_codes, float* k_scale,
+                              float* v_scale, int64_t num_blocks, int num_kv_heads,
+                              int block_size, int head_dim, cudaStream_t stream) {
+  if (num_tokens == 0) return cudaSuccess;
+  const int64_t rows = num_tokens * num_kv_heads;
+  const int warps = 8;
+  const int64_t blocks = (rows + warps - 1) / warps;
+  if (blocks > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+  auto* kc = static_cast<uint8_t*>(k_codes);
+  auto* vc = static_cast<uint8_t*>(v_codes);
+#define PKV_APPEND8(T, D)                                                                  \
+  return launch_pdl(append_fp8_kernel<T, D>, dim3(static_cast<unsigned>(blocks)),          \
+                    dim3(warps * 32), 0, stream, static_cast<const T*>(k),                 \
+                    static_cast<const T*>(v), slots, num_tokens, kc, vc, k_scale, v_scale, \
+                    num_blocks, num_kv_heads, block_size)
+  if (in_dtype == 0) {
+    if (head_dim == 128) PKV_APPEND8(float, 128);
+    PKV_APPEND8(float, 64);
+  }
+  if (in_dtype == 1) {
+    if (head_dim == 128) PKV_APPEND8(__half, 128);
+    PKV_APPEND8(__half, 64);
+  }
+  if (head_dim == 128) PKV_APPEND8(__nv_bfloat16, 128);
+  PKV_APPEND8(__nv_bfloat16, 64);
+#undef PKV_APPEND8
+}
 
 cudaError_t launch_slot_mapping(const int32_t* block_tables, int num_seqs, int max_blocks,
                                 const int64_t* positions, int block_size, int64_t* slots,

@@ -40,15 +40,53 @@ constexpr int kThreads = kDecodeWarps * 32;
 constexpr int kBoxBytes = kUnitTokens * 128;  // one TMA box: 16 rows x 128 bytes
 constexpr float kRescaleThreshold = 8.0f;     // log2 units: weights stay <= 2^8
 
-template <int D>
+// Shared-memory plan of the tensor-core decode kernel.
+//  16-bit pools: each warp's ring stage holds a unit's K and V tiles (16 rows
+//    x D, 128-byte swizzled boxes), read by ldmatrix in place.
+//  FP8 pools (KV8): a stage holds the unit's K and V code tiles (16 rows x D
+//    bytes, one swizzled box each) and 2 x 16 row scales; the warp dequantises
+//    the codes into its own fp16 tile pair (same layout as the 16-bit tiles)
+//    and releases the stage before computing.
+template <int D, bool KV8>
 struct Tile16 {
   static constexpr int kBoxes = D / 64;                     // 64 16-bit columns per box
-  static constexpr int kTileBytes = kBoxes * kBoxBytes;     // K (or V) rows of one unit
-  static constexpr int kUnitBytes = 2 * kTileBytes;         // K + V
-  static constexpr int kStages = D == 128 ? kStagesD128 : kStagesD64;
-  static constexpr int kRingBytes = kStages * kUnitBytes;   // per warp
-  static constexpr int kSmemBytes = kDecodeWarps * kRingBytes + 1024;  // + alignment slack
+  static constexpr int kTileBytes = kBoxes * kBoxBytes;     // fp16 K (or V) rows of one unit
+  static constexpr int kCodeTileBytes = KV8 ? D * kUnitTokens : 0;
+  static constexpr int kStageBytes = KV8 ? 2 * kCodeTileBytes : 2 * kTileBytes;
+  static constexpr int kStages = KV8 ? kStagesFp8 : (D == 128 ? kStagesD128 : kStagesD64);
+  static constexpr int kRingBytes = kStages * kStageBytes;  // per warp
+  static constexpr int kConvBytes = KV8 ? 2 * kTileBytes : 0;  // per warp
+  static constexpr int kWarpBytes = kRingBytes + kConvBytes;  // multiple of 1 KB
+  static constexpr int kScaleBytes = KV8 ? kStages * 2 * kUnitTokens * 4 : 0;  // per warp
+  static constexpr int kTxBytes = KV8 ? 2 * kCodeTileBytes + 2 * kUnitTokens * 4 : kStageBytes;
+  static constexpr int kSmemBytes = kDecodeWarps * (kWarpBytes + kScaleBytes) + 1024;
+  static_assert(kWarpBytes % 1024 == 0, "swizzled tiles need 1 KB alignment");
 };
+
+// FP8 code tile (16 rows of D = 128 codes, 128-byte swizzle) -> fp16 tile in
+// the 16-bit layout.  Item i = (row i / 8, 16-code chunk i % 8); 4 per lane.
+__device__ __forceinline__ void dequant_tile_e4m3(uint32_t src, uint32_t dst, int lane) {
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    const int i = lane + 32 * k;
+    const int r = i >> 3, c8 = i & 7;
+    const uint4 w = ld_shared_v4(src + r * 128 + ((c8 ^ (r & 7)) << 4));
+    uint4 lo, hi;
+    lo.x = e4m3x2_to_f16x2(w.x);
+    lo.y = e4m3x2_to_f16x2(w.x >> 16);
+    lo.z = e4m3x2_to_f16x2(w.y);
+    lo.w = e4m3x2_to_f16x2(w.y >> 16);
+    hi.x = e4m3x2_to_f16x2(w.z);
+    hi.y = e4m3x2_to_f16x2(w.z >> 16);
+    hi.z = e4m3x2_to_f16x2(w.w);
+    hi.w = e4m3x2_to_f16x2(w.w >> 16);
+    const uint32_t rowbase = static_cast<uint32_t>(r * 128);
+    // chunks 2 c8 and 2 c8 + 1 of the fp16 row (box c8 / 4)
+    const uint32_t box = static_cast<uint32_t>((c8 >> 2) * kBoxBytes);
+    st_shared_v4(dst + box + rowbase + ((((2 * c8) & 7) ^ (r & 7)) << 4), lo);
+    st_shared_v4(dst + box + rowbase + ((((2 * c8 + 1) & 7) ^ (r & 7)) << 4), hi);
+  }
+}
 
 // Byte offset of 16-byte chunk `chunk` (0 .. D/8-1) of tile row `row` in a
 // TMA tile written with CU_TENSOR_MAP_SWIZZLE_128B: the chunk index inside a
@@ -131,17 +169,18 @@ __device__ void merge_and_store(const float* so, const float* sm, const float* s
 // ---------------------------------------------------------------------------
 // 16-bit pools: TMA-staged pages, tensor-core QK^T and PV.
 
-template <typename T, int D, int NT>
+template <typename T, int D, int NT, bool KV8>
 __global__ void __launch_bounds__(kThreads, 2)
 decode16_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
                 const DecodeParams p) {
-  using Cfg = Tile16<D>;
+  using Cfg = Tile16<D, KV8>;
   constexpr int QT = 8 * NT;        // query columns per CTA (padded group)
   constexpr int KS = D / 16;        // k-steps of QK^T == m-tiles of PV
   constexpr int DP = D + 4;         // padded row stride of the merge buffer
   constexpr int S = Cfg::kStages;
-  static_assert(kDecodeWarps * QT * (DP + 2) * 4 <= kDecodeWarps * Cfg::kRingBytes,
-                "merge buffer must fit in the staging ring");
+  static_assert(kDecodeWarps * QT * (DP + 2) * 4 <= kDecodeWarps * Cfg::kWarpBytes,
+                "merge buffer must fit in the staging rings");
+  static_assert(!KV8 || D == 128, "FP8 pools: head_dim 128");
 
   extern __shared__ uint8_t smem_raw[];
   __shared__ __align__(8) uint64_t bars[kDecodeWarps][S];
@@ -161,7 +200,9 @@ decode16_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant_
   const uint32_t raw_addr = smem_u32(smem_raw);
   const uint32_t base_addr = (raw_addr + 1023u) & ~1023u;  // 128B-swizzle tiles need 1 KB alignment
   uint8_t* base = smem_raw + (base_addr - raw_addr);
-  const uint32_t ring = base_addr + warp * Cfg::kRingBytes;
+  const uint32_t ring = base_addr + warp * Cfg::kWarpBytes;
+  const uint32_t conv = ring + Cfg::kRingBytes;  // FP8: dequantised K tile, then V tile
+  const uint32_t scales = base_addr + kDecodeWarps * Cfg::kWarpBytes + warp * Cfg::kScaleBytes;
 
   if (threadIdx.x == 0) s_bad = 0;
   if (lane == 0) {
@@ -190,14 +231,22 @@ decode16_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant_
 
   auto issue = [&](int stage, int y) {
     const uint32_t bar = smem_u32(&bars[warp][stage]);
-    const uint32_t kdst = ring + stage * Cfg::kUnitBytes;
-    const uint32_t vdst = kdst + Cfg::kTileBytes;
+    const uint32_t kdst = ring + stage * Cfg::kStageBytes;
+    const uint32_t vdst = kdst + Cfg::kStageBytes / 2;
     if (y >= 0) {
-      mbar_arrive_expect_tx(bar, Cfg::kUnitBytes);
+      mbar_arrive_expect_tx(bar, Cfg::kTxBytes);
+      if constexpr (KV8) {
+        tma_load_2d(kdst, &kmap, 0, y, bar);  // 16 rows x 128 codes
+        tma_load_2d(vdst, &vmap, 0, y, bar);
+        const uint32_t sdst = scales + stage * 2 * kUnitTokens * 4;
+        bulk_load(sdst, p.k_scale + y, kUnitTokens * 4, bar);
+        bulk_load(sdst + kUnitTokens * 4, p.v_scale + y, kUnitTokens * 4, bar);
+      } else {
 #pragma unroll
-      for (int bx = 0; bx < Cfg::kBoxes; ++bx) {
-        tma_load_2d(kdst + bx * kBoxBytes, &kmap, bx * 64, y, bar);
-        tma_load_2d(vdst + bx * kBoxBytes, &vmap, bx * 64, y, bar);
+        for (int bx = 0; bx < Cfg::kBoxes; ++bx) {
+          tma_load_2d(kdst + bx * kBoxBytes, &kmap, bx * 64, y, bar);
+          tma_load_2d(vdst + bx * kBoxBytes, &vmap, bx * 64, y, bar);
+        }
       }
     } else {
       mbar_arrive(bar);  // nothing to fetch: complete the phase, the unit is flagged bad
@@ -270,11 +319,32 @@ decode16_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant_
     }
     if (yj < 0) bad = true;
 
-    const uint32_t kt = ring + stage * Cfg::kUnitBytes;
-    const uint32_t vt = kt + Cfg::kTileBytes;
+    uint32_t kt = ring + stage * Cfg::kStageBytes;
+    uint32_t vt = kt + Cfg::kTileBytes;
     const int t0 = phys_unit(w.su, w.u0 + warp + j * kDecodeWarps) * kUnitTokens;
+    // per-row scales of the unit (FP8 pools; 1 otherwise): K rows g, g+8; V rows g, g+8
+    float ksa = 1.f, ksb = 1.f, vsa = 1.f, vsb = 1.f;
+    if constexpr (KV8) {
+      const uint32_t sc = scales + stage * 2 * kUnitTokens * 4;
+      ksa = ld_shared_f32(sc + (g << 2));
+      ksb = ld_shared_f32(sc + ((g + 8) << 2));
+      vsa = ld_shared_f32(sc + ((kUnitTokens + g) << 2));
+      vsb = ld_shared_f32(sc + ((kUnitTokens + g + 8) << 2));
+      dequant_tile_e4m3(kt, conv, lane);
+      dequant_tile_e4m3(kt + Cfg::kCodeTileBytes, conv + Cfg::kTileBytes, lane);
+      kt = conv;
+      vt = conv + Cfg::kTileBytes;
+      // the codes and scales are consumed: refill the stage now (every lane
+      // orders its reads of the stage before the asynchronous refill)
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (j + S < my_n) {
+        const int yn = __shfl_sync(0xffffffffu, my_y, j + S);
+        if (lane == 0) issue(stage, yn);
+      }
+    }
 
-    if (j == j_new) {
+    if (!KV8 && j == j_new) {
       const int r = t_new % kUnitTokens;
       if (lane < 2 * CPR) {
         const int c = lane % CPR;
@@ -309,12 +379,13 @@ decode16_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant_
     const int ta = t0 + g, tb = ta + 8;  // tokens of rows g and g + 8
     const bool va = !edge || attended(w.su, w.L, ta);
     const bool vb = !edge || attended(w.su, w.L, tb);
+    const float fa = ksa * p.scale_log2, fb = ksb * p.scale_log2;
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) {
-      s[nt][0] = va ? s[nt][0] * p.scale_log2 : -INFINITY;
-      s[nt][1] = va ? s[nt][1] * p.scale_log2 : -INFINITY;
-      s[nt][2] = vb ? s[nt][2] * p.scale_log2 : -INFINITY;
-      s[nt][3] = vb ? s[nt][3] * p.scale_log2 : -INFINITY;
+      s[nt][0] = va ? s[nt][0] * fa : -INFINITY;
+      s[nt][1] = va ? s[nt][1] * fa : -INFINITY;
+      s[nt][2] = vb ? s[nt][2] * fb : -INFINITY;
+      s[nt][3] = vb ? s[nt][3] * fb : -INFINITY;
     }
 
     // ---- column (query) maxima over the 16 tokens ----
@@ -355,12 +426,20 @@ decode16_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant_
     uint32_t bh[NT][2], bl[NT][2];
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) {
-      const float p0 = ex2(s[nt][0] - m_run[nt][0]);
-      const float p1 = ex2(s[nt][1] - m_run[nt][1]);
-      const float p2 = ex2(s[nt][2] - m_run[nt][0]);
-      const float p3 = ex2(s[nt][3] - m_run[nt][1]);
+      float p0 = ex2(s[nt][0] - m_run[nt][0]);
+      float p1 = ex2(s[nt][1] - m_run[nt][1]);
+      float p2 = ex2(s[nt][2] - m_run[nt][0]);
+      float p3 = ex2(s[nt][3] - m_run[nt][1]);
       l_run[nt][0] += p0 + p2;
       l_run[nt][1] += p1 + p3;
+      if constexpr (KV8) {
+        // fold the V row scales into the weights (masked rows have weight 0
+        // and may carry a NaN scale)
+        p0 = va ? p0 * vsa : 0.f;
+        p1 = va ? p1 * vsa : 0.f;
+        p2 = vb ? p2 * vsb : 0.f;
+        p3 = vb ? p3 * vsb : 0.f;
+      }
       const uint32_t htop = Mma<T>::pack(p0, p1), hbot = Mma<T>::pack(p2, p3);
       const uint32_t ltop = Mma<T>::pack(p0 - Mma<T>::lo_f32(htop), p1 - Mma<T>::hi_f32(htop));
       const uint32_t lbot = Mma<T>::pack(p2 - Mma<T>::lo_f32(hbot), p3 - Mma<T>::hi_f32(hbot));
@@ -397,14 +476,16 @@ decode16_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant_
       }
     }
 
-    // ---- recycle the stage ----
-    __syncwarp();
-    if (j + S < my_n) {
-      const int yn = __shfl_sync(0xffffffffu, my_y, j + S);
-      if (lane == 0) {
-        fence_proxy_async_smem();
-        issue(stage, yn);
+    // ---- recycle the stage (16-bit pools: the tiles were read in place) ----
+    if constexpr (!KV8) {
+      fence_proxy_async_smem();  // this lane's reads of the stage precede the refill
+      __syncwarp();
+      if (j + S < my_n) {
+        const int yn = __shfl_sync(0xffffffffu, my_y, j + S);
+        if (lane == 0) issue(stage, yn);
       }
+    } else {
+      __syncwarp();  // the fp16 tiles are rewritten by the next unit
     }
   }
 
@@ -630,11 +711,11 @@ combine_kernel(const DecodeParams p) {
   for (int i = 0; i < PER; ++i) out[i] = from_f32<T>(acc[i] / lsum);
 }
 
-template <typename T, int D, int NT>
+template <typename T, int D, int NT, bool KV8 = false>
 cudaError_t launch16(const CUtensorMap& kmap, const CUtensorMap& vmap, const DecodeParams& p,
                      cudaStream_t stream) {
-  auto kern = decode16_kernel<T, D, NT>;
-  const int smem = Tile16<D>::kSmemBytes;
+  auto kern = decode16_kernel<T, D, NT, KV8>;
+  const int smem = Tile16<D, KV8>::kSmemBytes;
   // the shared-memory opt-in is per device; set it once for each
   static std::atomic<uint64_t> configured{0};
   int dev = 0;
@@ -653,7 +734,13 @@ cudaError_t launch16(const CUtensorMap& kmap, const CUtensorMap& vmap, const Dec
 }  // namespace
 
 size_t decode_16bit_smem_bytes(int head_dim) {
-  return head_dim == 128 ? Tile16<128>::kSmemBytes : Tile16<64>::kSmemBytes;
+  return head_dim == 128 ? Tile16<128, false>::kSmemBytes : Tile16<64, false>::kSmemBytes;
+}
+
+cudaError_t launch_decode_fp8(int ntiles, const CUtensorMap& kmap, const CUtensorMap& vmap,
+                              const DecodeParams& p, cudaStream_t stream) {
+  if (ntiles == 1) return launch16<__half, 128, 1, true>(kmap, vmap, p, stream);
+  return launch16<__half, 128, 2, true>(kmap, vmap, p, stream);
 }
 
 cudaError_t launch_decode_16bit(int dtype, int head_dim, int ntiles, const CUtensorMap& kmap,

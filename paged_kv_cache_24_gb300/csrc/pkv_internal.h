@@ -17,6 +17,7 @@ constexpr int kDecodeWarps = 4;
 // Ring depth (units in flight per warp) by head_dim, for 16-bit pools.
 constexpr int kStagesD128 = 3;
 constexpr int kStagesD64 = 4;
+constexpr int kStagesFp8 = 4;  // FP8 pools: 4 KB of codes + 128 B of scales per unit
 // Bounded mbarrier wait (polls); a TMA that has not landed by then is treated
 // as an error (output NaN), never as a reason to spin forever.
 constexpr uint32_t kWaitLimit = 1u << 20;
@@ -97,6 +98,8 @@ struct DecodeParams {
   const void* v_new;           //               [B][Hkv][D] new values
   void* k_dst;                 //               pools the new token is written to
   void* v_dst;
+  const float* k_scale;        // FP8 pools: [NB][Hkv][bs] row scales (stored = code * scale)
+  const float* v_scale;
   float* part_o;               // [B][Hq][S][D]  unnormalised partial outputs
   float2* part_ml;             // [B][Hq][S]     (running max in log2 units, sum)
   int64_t num_blocks;
@@ -116,6 +119,13 @@ struct DecodeParams {
 cudaError_t launch_decode_16bit(int dtype, int head_dim, int ntiles, const CUtensorMap& kmap,
                                 const CUtensorMap& vmap, const DecodeParams& p,
                                 cudaStream_t stream);
+// FP8 E4M3 pools (head_dim 128), fp16 q / out; kmap / vmap describe the code pools.
+cudaError_t launch_decode_fp8(int ntiles, const CUtensorMap& kmap, const CUtensorMap& vmap,
+                              const DecodeParams& p, cudaStream_t stream);
+cudaError_t launch_append_fp8(int in_dtype, const void* k, const void* v, const int64_t* slots,
+                              int64_t num_tokens, void* k_codes, void* v_codes, float* k_scale,
+                              float* v_scale, int64_t num_blocks, int num_kv_heads,
+                              int block_size, int head_dim, cudaStream_t stream);
 cudaError_t launch_decode_f32(int head_dim, const DecodeParams& p, cudaStream_t stream);
 cudaError_t launch_combine(int dtype, int head_dim, const DecodeParams& p, cudaStream_t stream);
 cudaError_t launch_append(int elem_bytes, const void* k, const void* v, const int64_t* slots,

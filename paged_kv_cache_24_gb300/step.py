@@ -26,8 +26,8 @@ from __future__ import annotations
 
 import torch
 
-from ._binding import (cache_layout, pkv_append, pkv_append_decode, pkv_decode,
-                       pkv_slot_mapping)
+from ._binding import (cache_layout, pkv_append, pkv_append_decode, pkv_append_fp8,
+                       pkv_decode, pkv_slot_mapping)
 
 _ALIGN = 256
 
@@ -36,13 +36,19 @@ class DecodeStep:
     def __init__(self, k_cache: torch.Tensor, v_cache: torch.Tensor, num_seqs: int,
                  num_q_heads: int, max_blocks: int, window: int, scale: float,
                  copy_block_tables: bool = True, num_buffers: int = 1, use_graph: bool = True,
-                 fused: bool = True):
+                 fused: bool = True, k_scale: torch.Tensor | None = None,
+                 v_scale: torch.Tensor | None = None):
         layout = cache_layout(k_cache)
         self.k_cache, self.v_cache = k_cache, v_cache
         self.window, self.scale = int(window), float(scale)
         self.block_size = layout.block_size
+        self.fp8 = k_cache.dtype == torch.uint8
+        if self.fp8 and fused:
+            raise ValueError("FP8 pools append through pkv_append_fp8: use fused=False")
+        self.k_scale, self.v_scale = k_scale, v_scale
         self.fused = fused
-        dt, dev = k_cache.dtype, k_cache.device
+        dev = k_cache.device
+        dt = torch.float16 if k_cache.dtype == torch.uint8 else k_cache.dtype
         B, hq, hkv, d = num_seqs, num_q_heads, layout.num_kv_heads, layout.head_dim
         shapes = {
             "q": ((B, hq, d), dt), "k": ((B, hkv, d), dt), "v": ((B, hkv, d), dt),
@@ -105,9 +111,14 @@ class DecodeStep:
         else:
             pkv_slot_mapping(dv["block_tables"], dv["positions"], self.block_size,
                              out=self.slots)
-            pkv_append(dv["k"], dv["v"], self.slots, self.k_cache, self.v_cache)
+            if self.fp8:
+                pkv_append_fp8(dv["k"], dv["v"], self.slots, self.k_cache, self.v_cache,
+                               self.k_scale, self.v_scale)
+            else:
+                pkv_append(dv["k"], dv["v"], self.slots, self.k_cache, self.v_cache)
             pkv_decode(dv["q"], self.k_cache, self.v_cache, dv["block_tables"],
-                       dv["context_lens"], self.window, self.scale, out=self.out)
+                       dv["context_lens"], self.window, self.scale, out=self.out,
+                       k_scale=self.k_scale, v_scale=self.v_scale)
         self.host_out.copy_(self.out, non_blocking=True)
 
     def run(self, i: int = 0, wait: bool = True) -> torch.Tensor:

@@ -88,6 +88,7 @@ class WorkloadSpec:
     lens_are_pre_append: bool = False
     window: int = 0
     num_sinks: int = 0                # with a window: first positions kept (attention sinks)
+    kv_fp8: bool = False              # pools of FP8 E4M3 codes + float32 row scales
     steps: int = 1
     pool_factor: float = 1.2          # pool = ceil(factor * blocks needed), shuffled ids
     explicit_pool: Optional[int] = None
@@ -98,8 +99,9 @@ class WorkloadSpec:
 
 
 def config_spec(idx: int, **overrides) -> WorkloadSpec:
-    """The five benchmark workloads (index 0..4), optionally resized for tests."""
-    base = {
+    """The five benchmark workloads (index 0..4) and FP8-pool variants of the MHA
+    and GQA ones (5, 6), optionally resized for tests."""
+    table = {
         0: dict(name="tiny_fp32", dtype=torch.float32, num_seqs=4, num_q_heads=8, num_kv_heads=8,
                 head_dim=64, block_size=16, lens=[17, 33, 64, 100], lens_are_pre_append=True,
                 explicit_pool=32, seed=0),
@@ -114,12 +116,16 @@ def config_spec(idx: int, **overrides) -> WorkloadSpec:
                 num_kv_heads=8, head_dim=128, block_size=16, len_dist="geometric", len_lo=128,
                 len_hi=2048, geom_mean=512.0, lens_are_pre_append=True, steps=32,
                 occupancy=0.7, prefix_group=16, prefix_tokens=256, seed=4),
-    }[idx]
+    }
+    # the MHA and GQA shapes over FP8 E4M3 pools (fp16 queries and new tokens)
+    table[5] = dict(table[1], name="mha_fp8", kv_fp8=True, seed=5)
+    table[6] = dict(table[2], name="gqa_fp8", dtype=torch.float16, kv_fp8=True, seed=6)
+    base = dict(table[idx])
     base.update(overrides)
     return WorkloadSpec(**base)
 
 
-CONFIGS = {config_spec(i).name: i for i in range(5)}
+CONFIGS = {config_spec(i).name: i for i in range(7)}
 
 
 @dataclass
@@ -133,8 +139,10 @@ class Workload:
     q_steps: torch.Tensor        # [S, B, Hq, D]
     k_steps: torch.Tensor        # [S, B, Hkv, D]
     v_steps: torch.Tensor        # [S, B, Hkv, D]
-    k_cache: torch.Tensor        # [NB, Hkv, bs, D]
+    k_cache: torch.Tensor        # [NB, Hkv, bs, D] (uint8 E4M3 codes for FP8 pools)
     v_cache: torch.Tensor        # [NB, Hkv, bs, D]
+    k_scale: Optional[torch.Tensor] = None  # FP8 pools: [NB, Hkv, bs] float32 row scales
+    v_scale: Optional[torch.Tensor] = None
     unique_blocks: int = 0       # distinct physical blocks referenced at step 0
     free_list_after: List[int] = field(default_factory=list)
 
@@ -255,10 +263,23 @@ def make_workload(spec: WorkloadSpec, device="cpu", poison: bool = True,
     gen = torch.Generator(device=device)
     gen.manual_seed(spec.seed)
     dt = spec.dtype
-    k_cache = torch.empty((nb, Hkv, bs, D), dtype=dt, device=device)
-    v_cache = torch.empty((nb, Hkv, bs, D), dtype=dt, device=device)
-    _fill_random(k_cache, gen)
-    _fill_random(v_cache, gen)
+    k_scale = v_scale = None
+    if spec.kv_fp8:
+        # E4M3 codes of N(0, 1) * 64 (torch's float8 cast) and row scales around 1/64
+        k_cache = torch.empty((nb, Hkv, bs, D), dtype=torch.uint8, device=device)
+        v_cache = torch.empty((nb, Hkv, bs, D), dtype=torch.uint8, device=device)
+        for c in (k_cache, v_cache):
+            tmp = torch.empty(c.shape, dtype=torch.float32, device=device)
+            _fill_random(tmp, gen)
+            c.copy_((tmp * 64.0).to(torch.float8_e4m3fn).view(torch.uint8))
+            del tmp
+        k_scale = torch.rand((nb, Hkv, bs), generator=gen, device=device) * (1 / 64) + 1 / 128
+        v_scale = torch.rand((nb, Hkv, bs), generator=gen, device=device) * (1 / 64) + 1 / 128
+    else:
+        k_cache = torch.empty((nb, Hkv, bs, D), dtype=dt, device=device)
+        v_cache = torch.empty((nb, Hkv, bs, D), dtype=dt, device=device)
+        _fill_random(k_cache, gen)
+        _fill_random(v_cache, gen)
     q_steps = torch.empty((S, B, Hq, D), dtype=dt, device=device)
     k_steps = torch.empty((S, B, Hkv, D), dtype=dt, device=device)
     v_steps = torch.empty((S, B, Hkv, D), dtype=dt, device=device)
@@ -280,8 +301,14 @@ def make_workload(spec: WorkloadSpec, device="cpu", poison: bool = True,
         bad = torch.from_numpy(np.nonzero(~valid)[0]).to(device)
         if bad.numel():
             blk, row = bad // bs, bad % bs
-            k_cache[blk, :, row, :] = float("nan")
-            v_cache[blk, :, row, :] = float("nan")
+            if spec.kv_fp8:
+                k_cache[blk, :, row, :] = 0x7F  # E4M3 NaN code
+                v_cache[blk, :, row, :] = 0x7F
+                k_scale[blk, :, row] = float("nan")
+                v_scale[blk, :, row] = float("nan")
+            else:
+                k_cache[blk, :, row, :] = float("nan")
+                v_cache[blk, :, row, :] = float("nan")
 
     return Workload(
         spec=spec,
@@ -291,7 +318,7 @@ def make_workload(spec: WorkloadSpec, device="cpu", poison: bool = True,
         lens_steps=torch.from_numpy(lens_steps.astype(np.int32)).to(device),
         pos_steps=torch.from_numpy(pos.astype(np.int64)).to(device),
         q_steps=q_steps, k_steps=k_steps, v_steps=v_steps,
-        k_cache=k_cache, v_cache=v_cache,
+        k_cache=k_cache, v_cache=v_cache, k_scale=k_scale, v_scale=v_scale,
         unique_blocks=unique,
         free_list_after=free_after,
     )
