@@ -44,9 +44,9 @@ constexpr float kRescaleThreshold = 8.0f;     // log2 units: weights stay <= 2^8
 //  16-bit pools: each warp's ring stage holds a unit's K and V tiles (16 rows
 //    x D, 128-byte swizzled boxes), read by ldmatrix in place.
 //  FP8 pools (KV8): a stage holds the unit's K and V code tiles (16 rows x D
-//    bytes, one swizzled box each) and 2 x 16 row scales; the warp dequantises
-//    the codes into its own fp16 tile pair (same layout as the 16-bit tiles)
-//    and releases the stage before computing.
+//    bytes, one swizzled box each); the 2 x 16 row scales sit in a separate
+//    per-warp array.  ldmatrix reads the codes in place and the warp turns
+//    them into fp16 fragments in registers.
 template <int D, bool KV8>
 struct Tile16 {
   static constexpr int kBoxes = D / 64;                     // 64 16-bit columns per box
@@ -55,37 +55,23 @@ struct Tile16 {
   static constexpr int kStageBytes = KV8 ? 2 * kCodeTileBytes : 2 * kTileBytes;
   static constexpr int kStages = KV8 ? kStagesFp8 : (D == 128 ? kStagesD128 : kStagesD64);
   static constexpr int kRingBytes = kStages * kStageBytes;  // per warp
-  static constexpr int kConvBytes = KV8 ? 2 * kTileBytes : 0;  // per warp
-  static constexpr int kWarpBytes = kRingBytes + kConvBytes;  // multiple of 1 KB
+  static constexpr int kWarpBytes = kRingBytes;             // multiple of 1 KB
   static constexpr int kScaleBytes = KV8 ? kStages * 2 * kUnitTokens * 4 : 0;  // per warp
   static constexpr int kTxBytes = KV8 ? 2 * kCodeTileBytes + 2 * kUnitTokens * 4 : kStageBytes;
   static constexpr int kSmemBytes = kDecodeWarps * (kWarpBytes + kScaleBytes) + 1024;
   static_assert(kWarpBytes % 1024 == 0, "swizzled tiles need 1 KB alignment");
 };
 
-// FP8 code tile (16 rows of D = 128 codes, 128-byte swizzle) -> fp16 tile in
-// the 16-bit layout.  Item i = (row i / 8, 16-code chunk i % 8); 4 per lane.
-__device__ __forceinline__ void dequant_tile_e4m3(uint32_t src, uint32_t dst, int lane) {
-#pragma unroll
-  for (int k = 0; k < 4; ++k) {
-    const int i = lane + 32 * k;
-    const int r = i >> 3, c8 = i & 7;
-    const uint4 w = ld_shared_v4(src + r * 128 + ((c8 ^ (r & 7)) << 4));
-    uint4 lo, hi;
-    lo.x = e4m3x2_to_f16x2(w.x);
-    lo.y = e4m3x2_to_f16x2(w.x >> 16);
-    lo.z = e4m3x2_to_f16x2(w.y);
-    lo.w = e4m3x2_to_f16x2(w.y >> 16);
-    hi.x = e4m3x2_to_f16x2(w.z);
-    hi.y = e4m3x2_to_f16x2(w.z >> 16);
-    hi.z = e4m3x2_to_f16x2(w.w);
-    hi.w = e4m3x2_to_f16x2(w.w >> 16);
-    const uint32_t rowbase = static_cast<uint32_t>(r * 128);
-    // chunks 2 c8 and 2 c8 + 1 of the fp16 row (box c8 / 4)
-    const uint32_t box = static_cast<uint32_t>((c8 >> 2) * kBoxBytes);
-    st_shared_v4(dst + box + rowbase + ((((2 * c8) & 7) ^ (r & 7)) << 4), lo);
-    st_shared_v4(dst + box + rowbase + ((((2 * c8 + 1) & 7) ^ (r & 7)) << 4), hi);
-  }
+// Head-dim index of accumulator element r of m-tile mt held by lane group g.
+//  16-bit pools: m-tile mt covers d = 16 mt .. 16 mt + 15 in order.
+//  FP8 pools: m-tiles come in even / odd pairs over 32 d values: tile 2c + e
+//  holds d = 32 c + e + 2 g (rows g) and 32 c + 16 + e + 2 g (rows g + 8).
+template <bool KV8>
+__device__ __forceinline__ int acc_dim(int mt, int r, int g) {
+  if constexpr (KV8)
+    return 32 * (mt >> 1) + (mt & 1) + 2 * g + ((r >> 1) << 4);
+  else
+    return mt * 16 + g + ((r >> 1) << 3);
 }
 
 // Byte offset of 16-byte chunk `chunk` (0 .. D/8-1) of tile row `row` in a
@@ -170,7 +156,7 @@ __device__ void merge_and_store(const float* so, const float* sm, const float* s
 // 16-bit pools: TMA-staged pages, tensor-core QK^T and PV.
 
 template <typename T, int D, int NT, bool KV8>
-__global__ void __launch_bounds__(kThreads, 2)
+__global__ void __launch_bounds__(kThreads, (KV8 && NT == 1) ? 3 : 2)
 decode16_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
                 const DecodeParams p) {
   using Cfg = Tile16<D, KV8>;
@@ -201,7 +187,6 @@ decode16_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant_
   const uint32_t base_addr = (raw_addr + 1023u) & ~1023u;  // 128B-swizzle tiles need 1 KB alignment
   uint8_t* base = smem_raw + (base_addr - raw_addr);
   const uint32_t ring = base_addr + warp * Cfg::kWarpBytes;
-  const uint32_t conv = ring + Cfg::kRingBytes;  // FP8: dequantised K tile, then V tile
   const uint32_t scales = base_addr + kDecodeWarps * Cfg::kWarpBytes + warp * Cfg::kScaleBytes;
 
   if (threadIdx.x == 0) s_bad = 0;
@@ -270,8 +255,16 @@ decode16_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant_
         static_cast<const T*>(p.q) + (static_cast<int64_t>(w.b) * p.num_q_heads + w.h0 + qi) * D);
 #pragma unroll
     for (int kk = 0; kk < KS; ++kk) {
-      qf[nt][kk][0] = qi < w.nh ? __ldg(qrow + kk * 8 + tig) : 0u;
-      qf[nt][kk][1] = qi < w.nh ? __ldg(qrow + kk * 8 + 4 + tig) : 0u;
+      if constexpr (KV8) {
+        // the FP8 K fragments carry d = 16 kk + 4 tig + {0, 1} | + {2, 3}: match them
+        const uint2 v2 = qi < w.nh ? __ldg(reinterpret_cast<const uint2*>(qrow + kk * 8) + tig)
+                                   : make_uint2(0u, 0u);
+        qf[nt][kk][0] = v2.x;
+        qf[nt][kk][1] = v2.y;
+      } else {
+        qf[nt][kk][0] = qi < w.nh ? __ldg(qrow + kk * 8 + tig) : 0u;
+        qf[nt][kk][1] = qi < w.nh ? __ldg(qrow + kk * 8 + 4 + tig) : 0u;
+      }
     }
   }
 
@@ -319,8 +312,8 @@ decode16_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant_
     }
     if (yj < 0) bad = true;
 
-    uint32_t kt = ring + stage * Cfg::kStageBytes;
-    uint32_t vt = kt + Cfg::kTileBytes;
+    const uint32_t kt = ring + stage * Cfg::kStageBytes;
+    const uint32_t vt = kt + Cfg::kStageBytes / 2;
     const int t0 = phys_unit(w.su, w.u0 + warp + j * kDecodeWarps) * kUnitTokens;
     // per-row scales of the unit (FP8 pools; 1 otherwise): K rows g, g+8; V rows g, g+8
     float ksa = 1.f, ksb = 1.f, vsa = 1.f, vsb = 1.f;
@@ -330,18 +323,6 @@ decode16_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant_
       ksb = ld_shared_f32(sc + ((g + 8) << 2));
       vsa = ld_shared_f32(sc + ((kUnitTokens + g) << 2));
       vsb = ld_shared_f32(sc + ((kUnitTokens + g + 8) << 2));
-      dequant_tile_e4m3(kt, conv, lane);
-      dequant_tile_e4m3(kt + Cfg::kCodeTileBytes, conv + Cfg::kTileBytes, lane);
-      kt = conv;
-      vt = conv + Cfg::kTileBytes;
-      // the codes and scales are consumed: refill the stage now (every lane
-      // orders its reads of the stage before the asynchronous refill)
-      fence_proxy_async_smem();
-      __syncwarp();
-      if (j + S < my_n) {
-        const int yn = __shfl_sync(0xffffffffu, my_y, j + S);
-        if (lane == 0) issue(stage, yn);
-      }
     }
 
     if (!KV8 && j == j_new) {
@@ -365,12 +346,33 @@ decode16_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant_
     for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
       for (int r = 0; r < 4; ++r) s[nt][r] = 0.f;
+    if constexpr (KV8) {
+      // one ldmatrix.x4 of codes = two k-steps of 16 d values for the 16 rows;
+      // each 32-bit register holds 4 consecutive codes of one row
 #pragma unroll
-    for (int kk = 0; kk < KS; ++kk) {
-      uint32_t a0, a1, a2, a3;
-      ldmatrix_x4(kt + swz(lane & 15, kk * 2 + (lane >> 4)), a0, a1, a2, a3);
+      for (int c = 0; c < KS / 2; ++c) {
+        const int row = lane & 15, chunk = 2 * c + (lane >> 4);
+        uint32_t r0, r1, r2, r3;
+        ldmatrix_x4(kt + row * 128 + ((chunk ^ (row & 7)) << 4), r0, r1, r2, r3);
+        const uint32_t a0 = e4m3x2_to_f16x2(r0), a1 = e4m3x2_to_f16x2(r1);
+        const uint32_t a2 = e4m3x2_to_f16x2(r0 >> 16), a3 = e4m3x2_to_f16x2(r1 >> 16);
+        const uint32_t b0 = e4m3x2_to_f16x2(r2), b1 = e4m3x2_to_f16x2(r3);
+        const uint32_t b2 = e4m3x2_to_f16x2(r2 >> 16), b3 = e4m3x2_to_f16x2(r3 >> 16);
 #pragma unroll
-      for (int nt = 0; nt < NT; ++nt) Mma<T>::run(s[nt], a0, a1, a2, a3, qf[nt][kk][0], qf[nt][kk][1]);
+        for (int nt = 0; nt < NT; ++nt) {
+          Mma<T>::run(s[nt], a0, a1, a2, a3, qf[nt][2 * c][0], qf[nt][2 * c][1]);
+          Mma<T>::run(s[nt], b0, b1, b2, b3, qf[nt][2 * c + 1][0], qf[nt][2 * c + 1][1]);
+        }
+      }
+    } else {
+#pragma unroll
+      for (int kk = 0; kk < KS; ++kk) {
+        uint32_t a0, a1, a2, a3;
+        ldmatrix_x4(kt + swz(lane & 15, kk * 2 + (lane >> 4)), a0, a1, a2, a3);
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt)
+          Mma<T>::run(s[nt], a0, a1, a2, a3, qf[nt][kk][0], qf[nt][kk][1]);
+      }
     }
 
     // ---- scale into log2 units; mask tokens that are not attended ----
@@ -460,32 +462,59 @@ decode16_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant_
       mhi = (attended(w.su, w.L, tk + 8) ? 0x0000ffffu : 0u) |
             (attended(w.su, w.L, tk + 9) ? 0xffff0000u : 0u);
     }
+    if constexpr (KV8) {
+      // ldmatrix.trans on the code tile viewed as 16-bit pairs: a register
+      // holds tokens (2 tig, 2 tig + 1) x dims (2 g, 2 g + 1) of one 16-d
+      // chunk; one byte permute separates the even-d pair from the odd-d pair,
+      // which feed the even and odd m-tiles of the 32-d block.
 #pragma unroll
-    for (int mt = 0; mt < KS; ++mt) {
-      uint32_t a0, a1, a2, a3;
-      const int tok = (lane & 7) + ((lane >> 4) << 3);
-      ldmatrix_x4_trans(vt + swz(tok, mt * 2 + ((lane >> 3) & 1)), a0, a1, a2, a3);
-      a0 &= mlo;
-      a1 &= mlo;
-      a2 &= mhi;
-      a3 &= mhi;
+      for (int c = 0; c < KS / 2; ++c) {
+        const int tok = (lane & 7) + ((lane >> 4) << 3);
+        const int chunk = 2 * c + ((lane >> 3) & 1);
+        uint32_t r0, r1, r2, r3;
+        ldmatrix_x4_trans(vt + tok * 128 + ((chunk ^ (tok & 7)) << 4), r0, r1, r2, r3);
+        r0 = __byte_perm(r0, 0u, 0x3120);
+        r1 = __byte_perm(r1, 0u, 0x3120);
+        r2 = __byte_perm(r2, 0u, 0x3120);
+        r3 = __byte_perm(r3, 0u, 0x3120);
 #pragma unroll
-      for (int nt = 0; nt < NT; ++nt) {
-        Mma<T>::run(o[mt][nt], a0, a1, a2, a3, bh[nt][0], bh[nt][1]);
-        Mma<T>::run(o[mt][nt], a0, a1, a2, a3, bl[nt][0], bl[nt][1]);
+        for (int e = 0; e < 2; ++e) {
+          const int sh = 16 * e;
+          const uint32_t a0 = e4m3x2_to_f16x2(r0 >> sh) & mlo;
+          const uint32_t a1 = e4m3x2_to_f16x2(r1 >> sh) & mlo;
+          const uint32_t a2 = e4m3x2_to_f16x2(r2 >> sh) & mhi;
+          const uint32_t a3 = e4m3x2_to_f16x2(r3 >> sh) & mhi;
+#pragma unroll
+          for (int nt = 0; nt < NT; ++nt) {
+            Mma<T>::run(o[2 * c + e][nt], a0, a1, a2, a3, bh[nt][0], bh[nt][1]);
+            Mma<T>::run(o[2 * c + e][nt], a0, a1, a2, a3, bl[nt][0], bl[nt][1]);
+          }
+        }
+      }
+    } else {
+#pragma unroll
+      for (int mt = 0; mt < KS; ++mt) {
+        uint32_t a0, a1, a2, a3;
+        const int tok = (lane & 7) + ((lane >> 4) << 3);
+        ldmatrix_x4_trans(vt + swz(tok, mt * 2 + ((lane >> 3) & 1)), a0, a1, a2, a3);
+        a0 &= mlo;
+        a1 &= mlo;
+        a2 &= mhi;
+        a3 &= mhi;
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+          Mma<T>::run(o[mt][nt], a0, a1, a2, a3, bh[nt][0], bh[nt][1]);
+          Mma<T>::run(o[mt][nt], a0, a1, a2, a3, bl[nt][0], bl[nt][1]);
+        }
       }
     }
 
-    // ---- recycle the stage (16-bit pools: the tiles were read in place) ----
-    if constexpr (!KV8) {
-      fence_proxy_async_smem();  // this lane's reads of the stage precede the refill
-      __syncwarp();
-      if (j + S < my_n) {
-        const int yn = __shfl_sync(0xffffffffu, my_y, j + S);
-        if (lane == 0) issue(stage, yn);
-      }
-    } else {
-      __syncwarp();  // the fp16 tiles are rewritten by the next unit
+    // ---- recycle the stage ----
+    fence_proxy_async_smem();  // this lane's reads of the stage precede the refill
+    __syncwarp();
+    if (j + S < my_n) {
+      const int yn = __shfl_sync(0xffffffffu, my_y, j + S);
+      if (lane == 0) issue(stage, yn);
     }
   }
 
@@ -512,7 +541,7 @@ decode16_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant_
     for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
       for (int r = 0; r < 4; ++r) {
-        const int d = mt * 16 + g + ((r >> 1) << 3);
+        const int d = acc_dim<KV8>(mt, r, g);
         const int q = nt * 8 + 2 * tig + (r & 1);
         so[(warp * QT + q) * DP + d] = o[mt][nt][r];
       }
