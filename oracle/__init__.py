@@ -92,6 +92,9 @@ def _load():
         lib.oracle_decode_fp8.argtypes = [c_vp, c_i32, c_i32, c_i32, c_vp, c_vp, c_vp, c_vp,
                                           c_i64, c_i32, c_i32, c_i32, c_vp, c_i32, c_vp, c_i32,
                                           c_i32, c_dbl, c_vp, c_i64, c_vp, c_i32]
+        lib.oracle_prefill.restype = ctypes.c_int
+        lib.oracle_prefill.argtypes = [c_vp, c_i32, c_vp, c_i32, c_i32, c_vp, c_vp, c_i64, c_i32,
+                                       c_i32, c_i32, c_vp, c_i32, c_vp, c_i32, c_dbl, c_vp, c_i32]
         lib.oracle_max_threads.restype = ctypes.c_int
         lib.oracle_max_threads.argtypes = []
         _lib = lib
@@ -344,3 +347,30 @@ def decode_fp8(q, k_codes, v_codes, k_scale, v_scale, block_tables, context_lens
     if check and rc != 0:
         raise ValueError(f"oracle_decode_fp8 failed with code {rc}")
     return out if pairs is not None else out.reshape(B, Hq, D)
+
+
+def prefill(q, cu_q, k_cache, v_cache, block_tables, context_lens, window: int, scale: float,
+            threads: int = 0, check: bool = True) -> np.ndarray:
+    """Chunked prefill over a paged cache (chunk already appended), float64.
+
+    ``q`` [T, Hq, D] packed chunk queries; ``cu_q`` [B + 1] chunk offsets;
+    ``context_lens`` [B] lengths including the chunk.  Query token at position
+    p attends positions j <= p (and p - j < window when window > 0).
+    Returns [T, Hq, D]."""
+    qr, qd = _as_raw(q)
+    kc, kd = _as_raw(k_cache)
+    vc, vd = _as_raw(v_cache)
+    if not (qd == kd == vd):
+        raise TypeError("q, k_cache and v_cache must share a dtype")
+    cu = _int_array(cu_q, np.int32)
+    bt = _int_array(block_tables, np.int32)
+    lens = _int_array(context_lens, np.int32)
+    T, Hq, D = qr.shape
+    nb, hkv, bs, d2 = kc.shape
+    out = np.empty((T, Hq, D), dtype=np.float64)
+    rc = _load().oracle_prefill(_ptr(qr), qd, _ptr(cu), len(cu) - 1, Hq, _ptr(kc), _ptr(vc), nb,
+                                hkv, bs, D, _ptr(bt), bt.shape[1], _ptr(lens), int(window),
+                                float(scale), _ptr(out), int(threads))
+    if check and rc != 0:
+        raise ValueError(f"oracle_prefill failed with code {rc}")
+    return out

@@ -445,6 +445,60 @@ static int decode_pairs(const decode_problem* pp, const int32_t* pairs, int64_t 
   return rc;
 }
 
+/* ---- paged (chunked) prefill ([P3] Step 3, prefill_attention) ------------- */
+
+/* Prefill of a chunk of new tokens per sequence over a paged cache that holds
+ * the sequence's earlier tokens and the chunk itself (appended beforehand).
+ * Sequence b's chunk is tokens cu_q[b] .. cu_q[b+1]-1 of the packed q / out,
+ * at positions L_b - n_b .. L_b - 1 (L_b = context_lens[b], n_b the chunk
+ * size).  Query token at position p attends the positions j with j <= p and,
+ * when window > 0, p - j < window: the mask of prefill_attention, with the
+ * softmax taken per query row.  That is a decode of length p + 1 with the same
+ * window, which is how it is computed here.
+ *   q   [T][Hq][D] (dtype), out [T][Hq][D] double, T = cu_q[num_seqs]. */
+int oracle_prefill(const void* q, int32_t dtype, const int32_t* cu_q, int32_t num_seqs,
+                   int32_t num_q_heads, const void* k_cache, const void* v_cache,
+                   int64_t num_blocks, int32_t num_kv_heads, int32_t block_size,
+                   int32_t head_dim, const int32_t* block_tables, int32_t max_blocks,
+                   const int32_t* context_lens, int32_t window, double scale, double* out,
+                   int32_t num_threads) {
+  if (!q || !cu_q || !k_cache || !v_cache || !block_tables || !context_lens || !out)
+    return ORACLE_ERR_ARG;
+  if (num_seqs < 0 || num_q_heads <= 0 || num_kv_heads <= 0 || num_q_heads % num_kv_heads ||
+      dtype < 0 || dtype > 2)
+    return ORACLE_ERR_ARG;
+  const int64_t T = cu_q[num_seqs];
+  int rc = ORACLE_OK;
+#ifdef _OPENMP
+  if (num_threads <= 0) num_threads = omp_get_max_threads();
+#pragma omp parallel for schedule(dynamic, 1) num_threads(num_threads)
+#endif
+  for (int64_t t = 0; t < T; ++t) {
+    int32_t b = 0;
+    while (b + 1 < num_seqs && cu_q[b + 1] <= t) ++b; /* the sequence holding token t */
+    const int64_t n = cu_q[b + 1] - cu_q[b];
+    const int64_t p = context_lens[b] - n + (t - cu_q[b]); /* its position */
+    /* one query row: a decode problem of a single sequence with length p + 1 */
+    int32_t len = (int32_t)(p + 1);
+    decode_problem dp = {(const char*)q + t * (int64_t)num_q_heads * head_dim *
+                                              (dtype == ORACLE_F32 ? 4 : 2),
+                         1, num_q_heads, k_cache, v_cache, NULL, NULL, num_blocks,
+                         num_kv_heads, block_size, head_dim, dtype, dtype,
+                         block_tables + (int64_t)b * max_blocks, max_blocks, &len, window, 0,
+                         scale};
+    for (int32_t h = 0; h < num_q_heads; ++h) {
+      int r = p < 0 ? ORACLE_ERR_LENGTH : decode_one(&dp, 0, h, out + (t * num_q_heads + h) * head_dim);
+      if (r != ORACLE_OK) {
+#ifdef _OPENMP
+#pragma omp critical
+#endif
+        if (rc == ORACLE_OK) rc = r;
+      }
+    }
+  }
+  return rc;
+}
+
 /* Number of threads the OpenMP runtime would use (1 without OpenMP). */
 int oracle_max_threads(void) {
 #ifdef _OPENMP

@@ -1,15 +1,16 @@
 """The oracle's pins must catch plausible mistakes in the oracle.
 
 Each case plants one mistake in a temporary copy of oracle/pkv_oracle.c (on the
-CPU, never in the product), rebuilds it, and runs tests/test_oracle.py and
-tests/test_oracle_fp8.py against the copy: the pin suite has to fail.  The mistakes are the ones a careful
+CPU, never in the product), rebuilds it, and runs the oracle pin files
+(tests/test_oracle*.py) against the copy: the pin suite has to fail.  The mistakes are the ones a careful
 reader of the pages could still make: a wrong GQA head mapping, a flipped or
 missing max-subtraction, an off-by-one window start, a wrong attention-sink
 count or ignored sinks, swapped K and V, wrong row/block or head-major
 indexing, a squared scale, wrong element decoding, a wrong slot, a wrong
 append destination, the wrong query head, a non-zero empty context, and in the
 FP8 cache a wrong exponent bias, ties broken to odd, a dropped sign, a wrong
-quantisation constant, or an ignored row scale.
+quantisation constant, or an ignored row scale, and in the prefill a query
+position off by one or a missing causal limit.
 """
 import os
 import shutil
@@ -55,6 +56,10 @@ MUTANTS = {
     "fp8_scale_constant": ("volatile float num = 448.0f;", "volatile float num = 480.0f;"),
     "fp8_scale_ignored": ("double ks = (double)p->k_scale[prow], vs = (double)p->v_scale[prow];",
                           "double ks = 1.0, vs = (double)p->v_scale[prow];"),
+    "prefill_position_off_by_one": (
+        "const int64_t p = context_lens[b] - n + (t - cu_q[b]); /* its position */",
+        "const int64_t p = context_lens[b] - n + (t - cu_q[b]) + 1; /* its position */"),
+    "prefill_not_causal": ("int32_t len = (int32_t)(p + 1);", "int32_t len = context_lens[b];"),
     "empty_context_not_zero": (
         "for (int32_t d = 0; d < D; ++d) out[d] = 0.0;\n  if (T <= 0) return;",
         "for (int32_t d = 0; d < D; ++d) out[d] = 0.0;\n  if (T <= 0) { out[0] = 1.0; return; }"),
@@ -75,6 +80,7 @@ def test_pins_catch_planted_mistake(name, tmp_path, oracle_lib):
                     ignore=shutil.ignore_patterns("__pycache__", "test_oracle_mutants.py",
                                                   "test_gpu*", "test_zz*"))
     r = subprocess.run([sys.executable, "-m", "pytest", "-q", "-x", "-p", "no:cacheprovider",
-                        "tests/test_oracle.py", "tests/test_oracle_fp8.py"], cwd=tmp_path,
+                        "tests/test_oracle.py", "tests/test_oracle_fp8.py",
+                        "tests/test_oracle_prefill.py"], cwd=tmp_path,
                        capture_output=True, text=True, timeout=600)
     assert r.returncode == 1, f"pins did not catch '{name}':\n{r.stdout[-2000:]}"
