@@ -189,6 +189,31 @@ typedef struct pkv_decode_options {
 } pkv_decode_options;
 
 /*
+ * pkv_prefill -- append a chunk of new tokens per sequence and compute their
+ * attention (chunked prefill over a paged cache).
+ *   ("Building a Streaming Sliding-Window Attention Engine in Pure Python",
+ *   Step 3, prefill_attention: query i attends key j when j <= i and, with a
+ *   window, i - j < window; softmax per query row.)
+ *   The chunks are packed: sequence b owns tokens cu_q[b] .. cu_q[b+1]-1
+ *   (cu_q [num_seqs + 1] int32, device; n_b = cu_q[b+1] - cu_q[b] <= max_chunk).
+ *   q    [T][num_q_heads][head_dim], k, v [T][num_kv_heads][head_dim] (T =
+ *        cu_q[num_seqs]), layout->dtype (fp16 or bf16)
+ *   context_lens [num_seqs]: L_b, the length after the chunk; the chunk sits at
+ *        positions L_b - n_b .. L_b - 1, the tokens before it are in the pools.
+ *   First the chunk's K/V rows are written to their slots (block_tables as in
+ *   pkv_decode); then the query at position p attends positions j <= p (and
+ *   p - j < window when window > 0) of the pools, which hold the prefix and
+ *   the chunk.  out [T][num_q_heads][head_dim].
+ *   Limits: head_dim 64 or 128, max_blocks_per_seq * block_size <= 262,144.
+ *   In-kernel errors (bad block id, L_b < n_b) make the affected rows NaN.
+ */
+int pkv_prefill(const void* q, const void* k, const void* v, const int32_t* cu_q,
+                int32_t num_seqs, int32_t num_q_heads, int32_t max_chunk, void* k_cache,
+                void* v_cache, const pkv_cache_layout* layout, const int32_t* block_tables,
+                int32_t max_blocks_per_seq, const int32_t* context_lens, int32_t window,
+                float scale, void* out, void* stream);
+
+/*
  * pkv_append_fp8 -- quantise each new token's K and V rows into FP8 pools.
  *   ("Building a Memory-Compressed Attention Engine with KV Caching",
  *   Extending, item 2: INT8 or FP8 quantisation of the cached keys and

@@ -76,6 +76,8 @@ def load_library():
             "pkv_decode_ex": [vp, i32, i32, vp, vp, lay, vp, i32, vp, f32, vp,
                               ctypes.POINTER(DecodeOptions), vp],
             "pkv_append_fp8": [vp, vp, i32, vp, i64, vp, vp, vp, vp, lay, vp],
+            "pkv_prefill": [vp, vp, vp, vp, i32, i32, i32, vp, vp, lay, vp, i32, vp, i32, f32,
+                            vp, vp],
             "pkv_decode_plan": [i32, i32, lay, i32, i32, i32, i32, i32, ctypes.POINTER(i32),
                                 ctypes.POINTER(i32)],
             "pkv_release_workspaces": [],
@@ -241,6 +243,41 @@ def pkv_append_fp8(k: torch.Tensor, v: torch.Tensor, slot_mapping: torch.Tensor,
     _check("pkv_append_fp8", load_library().pkv_append_fp8(
         _ptr(k), _ptr(v), _DTYPES[k.dtype], _ptr(slot_mapping), T, _ptr(k_cache), _ptr(v_cache),
         _ptr(k_scale), _ptr(v_scale), ctypes.byref(layout), _stream(stream)))
+
+
+def pkv_prefill(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, cu_q: torch.Tensor,
+                k_cache: torch.Tensor, v_cache: torch.Tensor, block_tables: torch.Tensor,
+                context_lens: torch.Tensor, window: int, scale: float, max_chunk: int,
+                out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """Append each sequence's chunk (packed q/k/v, offsets cu_q) and compute its
+    causal (optionally windowed) attention over the paged cache; returns out like q."""
+    _on_cuda(q, k, v, cu_q, k_cache, v_cache, block_tables, context_lens, out)
+    layout = cache_layout(k_cache)
+    _require(v_cache.shape == k_cache.shape and v_cache.dtype == k_cache.dtype
+             and v_cache.is_contiguous(), "v_cache must match k_cache")
+    T = q.shape[0]
+    _require(q.dim() == 3 and q.shape[2] == layout.head_dim and q.dtype == k_cache.dtype
+             and q.is_contiguous(), "q must be contiguous [T, Hq, D] of the cache dtype")
+    shape = (T, layout.num_kv_heads, layout.head_dim)
+    _require(tuple(k.shape) == shape and tuple(v.shape) == shape and k.dtype == q.dtype
+             and v.dtype == q.dtype and k.is_contiguous() and v.is_contiguous(),
+             f"k and v must be contiguous {shape}")
+    B = block_tables.shape[0]
+    _require(cu_q.dtype == torch.int32 and cu_q.numel() == B + 1 and cu_q.is_contiguous(),
+             "cu_q must be int32 [B + 1]")
+    _require(block_tables.dtype == torch.int32 and block_tables.dim() == 2
+             and block_tables.is_contiguous(), "block_tables must be contiguous int32 [B, MB]")
+    _require(context_lens.dtype == torch.int32 and context_lens.numel() == B
+             and context_lens.is_contiguous(), "context_lens must be int32 [B]")
+    if out is None:
+        out = torch.empty_like(q)
+    _require(out.shape == q.shape and out.dtype == q.dtype and out.is_contiguous(),
+             "out must be contiguous and shaped like q")
+    _check("pkv_prefill", load_library().pkv_prefill(
+        _ptr(q), _ptr(k), _ptr(v), _ptr(cu_q), B, q.shape[1], int(max_chunk), _ptr(k_cache),
+        _ptr(v_cache), ctypes.byref(layout), _ptr(block_tables), block_tables.shape[1],
+        _ptr(context_lens), int(window), float(scale), _ptr(out), _stream(stream)))
+    return out
 
 
 def pkv_append_decode(q: torch.Tensor, k_new: torch.Tensor, v_new: torch.Tensor,

@@ -408,6 +408,39 @@ int pkv_decode_ex(const void* q, int32_t num_seqs, int32_t num_q_heads, void* k_
                      options->k_scale, options->v_scale);
 }
 
+int pkv_prefill(const void* q, const void* k, const void* v, const int32_t* cu_q,
+                int32_t num_seqs, int32_t num_q_heads, int32_t max_chunk, void* k_cache,
+                void* v_cache, const pkv_cache_layout* layout, const int32_t* block_tables,
+                int32_t max_blocks_per_seq, const int32_t* context_lens, int32_t window,
+                float scale, void* out, void* stream) {
+  int rc = check_layout(layout, true);
+  if (rc != PKV_OK) return rc;
+  if (layout->dtype != PKV_FLOAT16 && layout->dtype != PKV_BFLOAT16) return PKV_ERR_UNSUPPORTED;
+  if (num_seqs < 0 || num_q_heads <= 0 || max_chunk < 0 || max_blocks_per_seq < 0 ||
+      num_q_heads % layout->num_kv_heads != 0)
+    return PKV_ERR_SHAPE;
+  if (num_seqs > 65535) return PKV_ERR_UNSUPPORTED;
+  const int64_t max_units = static_cast<int64_t>(max_blocks_per_seq) * layout->block_size / 16;
+  if (max_units > 16384) return PKV_ERR_UNSUPPORTED;  // page-row table lives in shared memory
+  if (num_seqs == 0 || max_chunk == 0) return PKV_OK;
+  if (!q || !k || !v || !cu_q || !k_cache || !v_cache || !block_tables || !context_lens || !out)
+    return PKV_ERR_NULL;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(k_cache) ||
+      !aligned16(v_cache) || !aligned16(out) || !aligned4(cu_q) || !aligned4(block_tables) ||
+      !aligned4(context_lens))
+    return PKV_ERR_ALIGNMENT;
+  CUtensorMap kmap, vmap;
+  rc = encode_pool_map(&kmap, k_cache, layout);
+  if (rc != PKV_OK) return rc;
+  rc = encode_pool_map(&vmap, v_cache, layout);
+  if (rc != PKV_OK) return rc;
+  return to_status(pkv::launch_prefill(
+      layout->dtype, layout->head_dim, q, k, v, cu_q, num_seqs, num_q_heads, max_chunk, k_cache,
+      v_cache, layout->num_blocks, layout->num_kv_heads, layout->block_size, block_tables,
+      max_blocks_per_seq, context_lens, window, scale, out, kmap, vmap,
+      static_cast<cudaStream_t>(stream)));
+}
+
 int pkv_append_fp8(const void* k, const void* v, int32_t in_dtype, const int64_t* slot_mapping,
                    int64_t num_tokens, void* k_cache, void* v_cache, float* k_scale,
                    float* v_scale, const pkv_cache_layout* layout, void* stream) {

@@ -1,0 +1,100 @@
+"""pkv_prefill (chunked prefill over the paged cache) against the oracle: the
+chunk's rows land bit-exactly in their slots, and every query row's output is
+within the fp16 / bf16 tolerance of the oracle's prefill."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from paged_kv_cache_24_gb300.workloads import config_spec, make_workload
+
+pytestmark = pytest.mark.gpu
+
+
+def _bits(t):
+    return t.view(torch.int16)
+
+
+def _prefill_case(dtype, hq, hkv, d, bs, prefixes, chunks, window, seed):
+    """Pools holding each sequence's prefix (everything else NaN) and the packed chunk."""
+    lens = [p + n for p, n in zip(prefixes, chunks)]
+    spec = config_spec(0, dtype=dtype, num_seqs=len(lens), num_q_heads=hq, num_kv_heads=hkv,
+                       head_dim=d, block_size=bs, lens=lens, explicit_pool=None,
+                       lens_are_pre_append=False, window=0, seed=seed)
+    w = make_workload(spec, device="cuda")
+    bt = w.block_tables.cpu().numpy()
+    # positions prefix .. L-1 belong to the chunk: poison them before the call
+    kc, vc = w.k_cache, w.v_cache
+    for b, (p, L) in enumerate(zip(prefixes, lens)):
+        for t in range(p, L):
+            s = oracle.slot_for_position(bt[b], bs, t)
+            kc[s // bs, :, s % bs] = float("nan")
+            vc[s // bs, :, s % bs] = float("nan")
+    g = torch.Generator(device="cuda").manual_seed(seed + 7)
+    T = sum(chunks)
+    q = torch.randn(T, hq, d, generator=g, device="cuda").to(dtype)
+    k = torch.randn(T, hkv, d, generator=g, device="cuda").to(dtype)
+    v = torch.randn(T, hkv, d, generator=g, device="cuda").to(dtype)
+    cu = torch.tensor(np.concatenate([[0], np.cumsum(chunks)]), dtype=torch.int32, device="cuda")
+    return w, q, k, v, cu, torch.tensor(lens, dtype=torch.int32, device="cuda")
+
+
+def _oracle_prefill(w, q, k, v, cu, lens, chunks, window):
+    kc, vc = w.k_cache.cpu(), w.v_cache.cpu()
+    bt = w.block_tables.cpu().numpy()
+    cu_h, lens_h = cu.cpu().numpy(), lens.cpu().numpy()
+    slots = []
+    for b, n in enumerate(chunks):
+        for i in range(n):
+            slots.append(oracle.slot_for_position(bt[b], w.spec.block_size, lens_h[b] - n + i))
+    oracle.append(k.cpu(), v.cpu(), np.array(slots, np.int64), kc, vc)
+    out = oracle.prefill(q.cpu(), cu_h, kc, vc, bt, lens_h, window, w.scale)
+    return out, kc, vc
+
+
+CASES = [
+    # name, dtype, hq, hkv, d, bs, prefixes, chunks, window
+    ("mha_pure", torch.float16, 4, 4, 128, 16, [0, 0, 0], [1, 70, 129], 0),
+    ("mha_chunked", torch.float16, 4, 4, 128, 16, [15, 300, 2], [17, 64, 200], 0),
+    ("gqa4_bs32", torch.bfloat16, 8, 2, 128, 32, [0, 33, 500], [50, 31, 100], 0),
+    ("gqa8", torch.bfloat16, 8, 1, 128, 16, [7, 100], [9, 40], 0),
+    ("g6_chunks", torch.float16, 12, 2, 128, 16, [20, 0], [13, 30], 0),
+    ("g32", torch.bfloat16, 32, 1, 128, 16, [40, 5], [11, 6], 0),
+    ("d64", torch.bfloat16, 8, 4, 64, 16, [3, 90], [60, 45], 0),
+    ("window37", torch.bfloat16, 8, 2, 128, 16, [0, 100, 7], [80, 50, 30], 37),
+    ("window1", torch.float16, 4, 4, 128, 16, [5, 0], [20, 33], 1),
+    ("window_large", torch.float16, 4, 2, 128, 16, [10, 60], [30, 20], 5000),
+]
+
+
+@pytest.mark.parametrize("name,dtype,hq,hkv,d,bs,prefixes,chunks,window", CASES,
+                         ids=[c[0] for c in CASES])
+def test_prefill_matches_oracle(pkv_lib, oracle_lib, name, dtype, hq, hkv, d, bs, prefixes,
+                                chunks, window):
+    w, q, k, v, cu, lens = _prefill_case(dtype, hq, hkv, d, bs, prefixes, chunks, window,
+                                         seed=len(name))
+    ref, kc_h, vc_h = _oracle_prefill(w, q, k, v, cu, lens, chunks, window)
+    out = pkv_lib.pkv_prefill(q, k, v, cu, w.k_cache, w.v_cache, w.block_tables, lens, window,
+                              w.scale, max_chunk=max(chunks))
+    torch.cuda.synchronize()
+    assert torch.equal(_bits(w.k_cache.cpu()), _bits(kc_h))
+    assert torch.equal(_bits(w.v_cache.cpu()), _bits(vc_h))
+    g = out.double().cpu().numpy()
+    assert not np.isnan(g).any()
+    err = np.abs(g - ref)
+    tol = 2e-3 + 0.5 * torch.finfo(dtype).eps * np.abs(ref)
+    assert (err <= tol).all(), f"max err {err.max():.3e}"
+
+
+def test_prefill_last_row_equals_decode(pkv_lib):
+    """The last chunk token attends exactly what a decode of length L attends."""
+    w, q, k, v, cu, lens = _prefill_case(torch.bfloat16, 8, 2, 128, 16, [100, 37], [40, 12], 0,
+                                         seed=3)
+    out = pkv_lib.pkv_prefill(q, k, v, cu, w.k_cache, w.v_cache, w.block_tables, lens, 0,
+                              w.scale, max_chunk=40)
+    last = cu[1:].long() - 1
+    dec = pkv_lib.pkv_decode(q[last].contiguous(), w.k_cache, w.v_cache, w.block_tables, lens, 0,
+                             w.scale)
+    torch.cuda.synchronize()
+    diff = (out[last].double() - dec.double()).abs().max().item()
+    assert diff <= 2e-3 + 0.5 * torch.finfo(torch.bfloat16).eps * dec.double().abs().max().item()
