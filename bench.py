@@ -267,6 +267,80 @@ def run_reference(args, workload):
 
 
 # ---------------------------------------------------------------------------
+# chunked prefill (a separate workload: tensor-core bound, reported in TFLOP/s)
+
+PREFILL = {
+    # batch of sequences with a cached prefix and a 1024-token chunk each
+    "prefill_bf16": dict(dtype=torch.bfloat16, num_seqs=4, num_q_heads=32, num_kv_heads=8,
+                         head_dim=128, block_size=16, chunk=1024, prefix_lo=2048,
+                         prefix_hi=6144, seed=11),
+}
+
+
+def run_prefill(args, pkv):
+    from paged_kv_cache_24_gb300.workloads import config_spec, make_workload
+
+    c = PREFILL[args.workload]
+    rng = np.random.default_rng(c["seed"])
+    B, chunk = c["num_seqs"], c["chunk"]
+    prefix = rng.integers(c["prefix_lo"], c["prefix_hi"] + 1, B)
+    lens = (prefix + chunk).tolist()
+    spec = config_spec(0, dtype=c["dtype"], num_seqs=B, num_q_heads=c["num_q_heads"],
+                       num_kv_heads=c["num_kv_heads"], head_dim=c["head_dim"],
+                       block_size=c["block_size"], lens=lens, explicit_pool=None,
+                       lens_are_pre_append=False, seed=c["seed"])
+    w = make_workload(spec, device="cuda", poison=False)
+    g = torch.Generator(device="cuda").manual_seed(c["seed"])
+    T, hq, hkv, d = B * chunk, spec.num_q_heads, spec.num_kv_heads, spec.head_dim
+    q = torch.randn(T, hq, d, generator=g, device="cuda").to(spec.dtype)
+    k = torch.randn(T, hkv, d, generator=g, device="cuda").to(spec.dtype)
+    v = torch.randn(T, hkv, d, generator=g, device="cuda").to(spec.dtype)
+    cu = torch.arange(0, T + 1, chunk, dtype=torch.int32, device="cuda")
+    L = torch.tensor(lens, dtype=torch.int32, device="cuda")
+    out = torch.empty_like(q)
+    # algorithmic flops: every (query row, attended key) pair costs 2 D (QK) + 2 D (PV)
+    flops = float(sum(int(chunk) * int(p) + chunk * (chunk + 1) // 2 for p in prefix)) * hq * 4 * d
+
+    def step():
+        pkv.pkv_prefill(q, k, v, cu, w.k_cache, w.v_cache, w.block_tables, L, 0, w.scale,
+                        max_chunk=chunk, out=out)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(0) as clocks:
+        a.record()
+        for _ in range(args.steps):
+            step()
+        b.record()
+        torch.cuda.synchronize()
+    ms = a.elapsed_time(b) / args.steps
+    tflops = flops / (ms * 1e-3) / 1e12
+    peak = None
+    try:
+        with open(os.path.join(REPO, "MEASURED_PEAKS.json")) as f:
+            peak = float(json.load(f)["bf16_tflops"])
+        peak_kind = "measured"
+    except Exception:
+        peak, peak_kind = 1900.0, "fallback"
+    print(json.dumps({
+        "metric": "paged chunked prefill: attention TFLOP/s", "value": tflops,
+        "unit": "TFLOP/s", "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": DTYPE_NAME[spec.dtype], "data": "synthetic",
+        "config": {"workload": args.workload, "num_seqs": B, "chunk": chunk,
+                   "mean_prefix": float(prefix.mean()), "num_q_heads": hq, "num_kv_heads": hkv,
+                   "head_dim": d, "block_size": spec.block_size},
+        "tokens_per_s": T / (ms * 1e-3),
+        "roofline": {"bound": "tensor", "kernel": "prefill (chunk append + attention)",
+                     "achieved": tflops, "peak": peak, "unit": "TFLOP/s", "frac": tflops / peak,
+                     "peak_kind": peak_kind, "traffic": None},
+        "gpu_launches": 2 * args.steps, "clocks": clocks.summary()}), flush=True)
+    return 0
+
+
+# ---------------------------------------------------------------------------
 # the GPU arm
 
 
@@ -294,6 +368,8 @@ def main(argv=None):
 
     rank, world, local_rank = dist_env()
     torch.cuda.set_device(local_rank)
+    if args.workload in PREFILL:
+        return run_prefill(args, pkv)
     pg = None
     if world > 1:
         import torch.distributed as dist
