@@ -437,7 +437,7 @@ int pkv_prefill(const void* q, const void* k, const void* v, const int32_t* cu_q
   return to_status(pkv::launch_prefill(
       layout->dtype, layout->head_dim, q, k, v, cu_q, num_seqs, num_q_heads, max_chunk, k_cache,
       v_cache, layout->num_blocks, layout->num_kv_heads, layout->block_size, block_tables,
-      max_blocks_per_seq, context_lens, window, scale, out, kmap, vmap,
+      max_blocks_per_seq, context_lens, window, scale, out, kmap, vmap, true,
       static_cast<cudaStream_t>(stream)));
 }
 

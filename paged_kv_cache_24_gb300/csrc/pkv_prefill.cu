@@ -369,7 +369,8 @@ cudaError_t launch_prefill(int dtype, int head_dim, const void* q, const void* k
                            void* k_cache, void* v_cache, int64_t num_blocks, int num_kv_heads,
                            int block_size, const int32_t* block_tables, int max_blocks,
                            const int32_t* context_lens, int window, float scale, void* out,
-                           const CUtensorMap& kmap, const CUtensorMap& vmap, cudaStream_t stream) {
+                           const CUtensorMap& kmap, const CUtensorMap& vmap, bool tensor_memory,
+                           cudaStream_t stream) {
   if (num_seqs == 0 || max_chunk == 0) return cudaSuccess;
   // 1) the chunk's rows to their slots
   const int cpr = head_dim * 2 / 16;
@@ -382,6 +383,10 @@ cudaError_t launch_prefill(int dtype, int head_dim, const void* q, const void* k
                              static_cast<uint4*>(v_cache));
   if (e != cudaSuccess) return e;
   // 2) attention over prefix + chunk
+  if (tensor_memory)
+    return launch_prefill_tc(dtype, head_dim, q, cu_q, num_seqs, num_q_heads, max_chunk,
+                             num_blocks, num_kv_heads, block_size, block_tables, max_blocks,
+                             context_lens, window, scale, out, kmap, vmap, stream);
   PrefillParams p{};
   p.q = q;
   p.out = out;
