@@ -1,28 +1,30 @@
 // pkv_prefill_tc.cu -- chunked prefill attention on the 5th-generation tensor
-// cores (tcgen05, accumulators in tensor memory).
+// cores (tcgen05, accumulators and probabilities in tensor memory).
 //
 // What is computed: see pkv_prefill.cu ("Building a Streaming Sliding-Window
-// Attention Engine in Pure Python", Step 3, prefill_attention: query at
+// Attention Engine in Pure Python", Step 3, prefill_attention: the query at
 // position p attends keys j <= p with p - j < window, softmax per row).
 //
-// How: a CTA of 128 threads owns 128 query rows of one (sequence, kv head):
-// (token, GQA head) pairs, so every K/V page read serves the whole group.
-// Thread t owns row t, which is also TMEM lane t.  Per tile of 64 keys:
-//   1. TMA brings the four 16-key K and V units of the tile (128-byte swizzle)
-//      into one of two stages;
-//   2. thread 0 issues S = Q K^T (M = 128, N = 64, K = head_dim; both operands
-//      K-major in shared memory) into TMEM;
-//   3. every thread loads its S row from TMEM and runs the online softmax on
-//      it alone -- row maxima and sums need no shuffles;
-//   4. P is written to shared memory as a K-major operand, split into a hi
-//      and a lo 16-bit part (so the weights keep ~fp32 precision), and thread
-//      0 issues O += P_hi V + P_lo V (N = head_dim, V read MN-major straight
-//      from its TMA tile) into TMEM;
-//   5. when a row's running maximum moves by more than 2^8, the row's O in
-//      TMEM is rescaled in place (lazy rescaling).
-// V rows of keys that no query of the CTA may see are zeroed before the
+// How.  A CTA owns 256 query rows of one (sequence, kv head): (token, GQA
+// head) pairs, so every K/V page it reads serves the whole group.  The rows
+// form two tiles of 128 (one per TMEM lane), worked on in ping-pong:
+//   warp 9      (load)    TMA of the 16-key K and V units of each 64-key tile
+//                         into a ring of stages (128-byte swizzle);
+//   warp 8      (MMA)     one thread issues S_t = Q_t K^T (M 128, N 64, both
+//                         operands K-major in shared memory) and
+//                         O_t += P_t V (A = P_t read from TMEM, B = V read
+//                         MN-major straight from its TMA tile);
+//   warps 0-3 / 4-7       tile 0 / tile 1 softmax: each thread owns one row
+//                         (its TMEM lane), loads its 64 scores, masks, keeps
+//                         the running maximum and sum, writes P back to TMEM
+//                         and, when the maximum moved by more than 2^8,
+//                         rescales its O row in TMEM (lazy rescaling).
+// While one tile's rows are in the softmax, the tensor cores work on the
+// other tile's products.  P is kept as one 16-bit part or, for bf16, as a
+// hi and a lo part (so the weights keep ~16 significant bits).
+// V rows of keys that no row of the CTA may see are zeroed before the
 // products, so garbage (even NaN) in unused slots cannot leak.
-#include <limits.h>
+#include <atomic>
 #include <math.h>
 
 #include "pkv_device.cuh"
@@ -31,10 +33,12 @@
 namespace pkv {
 namespace {
 
-constexpr int kTRows = 128;       // query rows per CTA == TMEM lanes
-constexpr int kTKeys = 64;        // keys per tile
+constexpr int kQT = 128;          // rows per Q tile == TMEM lanes
+constexpr int kRowsCta = 2 * kQT;
+constexpr int kTKeys = 64;        // keys per K/V tile
 constexpr int kTUnits = kTKeys / kUnitTokens;
-constexpr int kTThreads = 128;
+constexpr int kMmaWarp = 8, kLoadWarp = 9;
+constexpr int kTThreads = 320;
 constexpr float kTRescale = 8.0f;
 
 struct TcParams {
@@ -47,56 +51,59 @@ struct TcParams {
   int num_q_heads, num_kv_heads, group;
   int head_chunk_log2, num_head_chunks;
   int max_blocks, block_size, window;
-  int max_units;
   float scale_log2;
 };
 
 template <int D>
 struct TcLayout {
-  static constexpr int kStages = D == 128 ? 3 : 4;
-  static constexpr int kKBlocks = D / 64;                  // 128-byte column blocks
-  static constexpr int kQBytes = kKBlocks * kTRows * 128;
-  static constexpr int kKVTile = kKBlocks * kTKeys * 128;  // K (or V) of one tile
+  static constexpr int kStages = D == 128 ? 4 : 6;
+  static constexpr int kKBlocks = D / 64;                   // 128-byte column blocks
+  static constexpr int kQTileBytes = kKBlocks * kQT * 128;
+  static constexpr int kKVTile = kKBlocks * kTKeys * 128;   // K (or V) of one tile
   static constexpr int kStageBytes = 2 * kKVTile;
-  static constexpr int kPBytes = kTRows * 128;             // 64 keys x 2 bytes per row
-  static constexpr int kQOff = 0;
-  static constexpr int kStageOff = kQBytes;
-  static constexpr int kPOff = kStageOff + kStages * kStageBytes;
-  static constexpr int kYOff = kPOff + 2 * kPBytes;
-  static constexpr uint32_t kTmemCols = (64 + D) <= 128 ? 128 : 256;  // S: 64, O: D
+  static constexpr int kStageOff = 2 * kQTileBytes;
+  static constexpr int kSmemBytes = kStageOff + kStages * kStageBytes;
+  // TMEM columns: O_t at t*D, S_t at 2D + 64t, P_t at 2D + 128 + 64t (hi, then lo)
+  static constexpr uint32_t o_col(int t) { return static_cast<uint32_t>(t * D); }
+  static constexpr uint32_t s_col(int t) { return static_cast<uint32_t>(2 * D + 64 * t); }
+  static constexpr uint32_t p_col(int t) { return static_cast<uint32_t>(2 * D + 128 + 64 * t); }
+  static constexpr uint32_t kTmemCols = 512;
+  static_assert(2 * D + 256 <= 512, "TMEM columns");
 };
 
 __device__ __forceinline__ uint32_t sw128(int row, int chunk) {
   return static_cast<uint32_t>(row * 128 + (((chunk & 7) ^ (row & 7)) << 4));
 }
 
-template <typename T, int D>
+template <typename T, int D, bool PLO>
 __global__ void __launch_bounds__(kTThreads, 1)
 prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
                   const TcParams p) {
   using Lay = TcLayout<D>;
   constexpr int S = Lay::kStages;
   constexpr uint32_t kFmt = __is_same(T, __nv_bfloat16) ? 1u : 0u;
-  constexpr uint32_t kIdS = umma_idesc_f16(kFmt, kTRows, kTKeys, 0);
-  constexpr uint32_t kIdO = umma_idesc_f16(kFmt, kTRows, D, 1);
+  constexpr uint32_t kIdS = umma_idesc_f16(kFmt, kQT, kTKeys, 0);
+  constexpr uint32_t kIdO = umma_idesc_f16(kFmt, kQT, D, 1);
 
   extern __shared__ uint8_t smem_raw[];
-  __shared__ __align__(8) uint64_t full_bar[S];
-  __shared__ __align__(8) uint64_t s_bar, pv_bar, done_bar;
+  __shared__ __align__(8) uint64_t kv_full[S], kv_empty[S];
+  __shared__ __align__(8) uint64_t s_full[2], p_full[2], o_done[2], done_bar;
   __shared__ uint32_t tmem_base_s;
+  __shared__ int s_bad;
 
-  const int tid = threadIdx.x, warp = tid >> 5;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   pdl_launch_dependents();
   pdl_wait_prior();
 
   const int b = blockIdx.z;
   const int hkv = blockIdx.y / p.num_head_chunks;
   const int chunk = blockIdx.y - hkv * p.num_head_chunks;
-  const int gc = 1 << p.head_chunk_log2;
-  const int tok_per_cta = kTRows >> p.head_chunk_log2;
+  const int lg = p.head_chunk_log2, gc = 1 << lg;
+  const int tok_per_cta = kRowsCta >> lg;
   const int start = p.cu_q[b];
   const int n = p.cu_q[b + 1] - start;
-  const int tile0 = blockIdx.x * tok_per_cta;
+  // the latest tokens (longest key ranges) first
+  const int tile0 = (gridDim.x - 1 - blockIdx.x) * tok_per_cta;
   if (tile0 >= n) return;
   const int L = p.context_lens[b];
   const int tile_n = min(tok_per_cta, n - tile0);
@@ -106,268 +113,348 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
   const int k_lo = (p.window > 0) ? max(0, pos0 - p.window + 1) : 0;
   const int u_first = k_lo / kUnitTokens;
   const int n_units = len_ok ? pos1 / kUnitTokens - u_first + 1 : 0;
+  const int n_tiles = (n_units + kTUnits - 1) / kTUnits;
 
   const uint32_t raw_addr = smem_u32(smem_raw);
   const uint32_t base = (raw_addr + 1023u) & ~1023u;
-  int* ys = reinterpret_cast<int*>(smem_raw + (base - raw_addr) + Lay::kYOff);
 
-  // ---- set-up: TMEM, barriers, page rows of the key range, the Q tile ----
+  // ---- set-up: TMEM, barriers, the Q tiles ----
   if (warp == 0) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
                      smem_u32(&tmem_base_s)),
                  "r"(Lay::kTmemCols));
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
   }
-  if (tid == 0) {
-    tma_prefetch_desc(&kmap);
-    tma_prefetch_desc(&vmap);
-    for (int s = 0; s < S; ++s) mbar_init(smem_u32(&full_bar[s]), 1);
-    mbar_init(smem_u32(&s_bar), 1);
-    mbar_init(smem_u32(&pv_bar), 1);
+  if (tid == kMmaWarp * 32) {
+    for (int s = 0; s < S; ++s) {
+      mbar_init(smem_u32(&kv_full[s]), 1);
+      mbar_init(smem_u32(&kv_empty[s]), 1);
+    }
+    for (int t = 0; t < 2; ++t) {
+      mbar_init(smem_u32(&s_full[t]), 1);
+      mbar_init(smem_u32(&p_full[t]), kQT);
+      mbar_init(smem_u32(&o_done[t]), 1);
+    }
     mbar_init(smem_u32(&done_bar), 1);
+    s_bad = len_ok ? 0 : 1;
     fence_mbar_init();
   }
-  bool bad = !(len_ok && n_units <= p.max_units);
-  const int n_load = min(n_units, p.max_units);
-  for (int u = tid; u < n_load; u += kTThreads) {
-    const int t0 = (u_first + u) * kUnitTokens;
-    const int32_t pb = __ldg(p.block_tables + static_cast<int64_t>(b) * p.max_blocks +
-                             t0 / p.block_size);
-    const bool ok = pb >= 0 && pb < p.num_blocks;
-    ys[u] = ok ? (pb * p.num_kv_heads + hkv) * p.block_size + (t0 % p.block_size) : -1;
-    if (!ok) bad = true;
-  }
-  // this thread's query row: token ti of the tile, head hi of the chunk
-  const int ti = tid >> p.head_chunk_log2, hi = tid & (gc - 1);
-  const bool row_ok = ti < tile_n;
+  // softmax threads: row `row` of Q tile `wg` (token ti of the CTA, head hi of the chunk)
+  const int wg = warp >> 2, row = tid & (kQT - 1);
+  const int r_cta = wg * kQT + row;
+  const int ti = r_cta >> lg, hi = r_cta & (gc - 1);
+  const bool row_ok = warp < 8 && ti < tile_n;
   const int rpos = row_ok ? pos0 + ti : -1;
-  {
-    const uint4* qrow = reinterpret_cast<const uint4*>(
-        static_cast<const T*>(p.q) +
-        (static_cast<int64_t>(start + tile0 + (row_ok ? ti : 0)) * p.num_q_heads +
-         hkv * p.group + chunk * gc + hi) * D);
+  const int64_t qo_row = (static_cast<int64_t>(start + tile0 + (row_ok ? ti : 0)) * p.num_q_heads +
+                          hkv * p.group + chunk * gc + hi) * D;
+  if (warp < 8) {
+    const uint4* qrow = reinterpret_cast<const uint4*>(static_cast<const T*>(p.q) + qo_row);
+    const uint32_t qt = base + wg * Lay::kQTileBytes;
 #pragma unroll
     for (int c16 = 0; c16 < D / 8; ++c16) {
       const uint4 v = row_ok ? __ldg(qrow + c16) : make_uint4(0u, 0u, 0u, 0u);
-      st_shared_v4(base + Lay::kQOff + (c16 >> 3) * kTRows * 128 + sw128(tid, c16), v);
+      st_shared_v4(qt + (c16 >> 3) * kQT * 128 + sw128(row, c16), v);
     }
+    fence_proxy_async_smem();
   }
-  fence_proxy_async_smem();
   tc_fence_before();
-  const bool bad_cta = __syncthreads_or(bad) != 0;
+  __syncthreads();
   tc_fence_after();
-  bad = bad_cta;
   const uint32_t tmem = tmem_base_s;
-  const uint32_t tS = tmem, tO = tmem + 64;
-  const uint32_t lane_off = static_cast<uint32_t>(warp * 32) << 16;
-  const int n_tiles = bad_cta ? 0 : (n_units + kTUnits - 1) / kTUnits;
+  bool bad = false;
 
-  // TMA of the units of tile j that exist (thread 0 only)
-  auto issue = [&](int j) {
-    const int stage = j % S;
-    const uint32_t bar = smem_u32(&full_bar[stage]);
-    const uint32_t kdst = base + Lay::kStageOff + stage * Lay::kStageBytes;
-    const uint32_t vdst = kdst + Lay::kKVTile;
-    const int units = min(kTUnits, n_units - j * kTUnits);
-    mbar_arrive_expect_tx(bar, units * 2 * Lay::kKBlocks * kUnitTokens * 128);
-    for (int i = 0; i < units; ++i) {
-      const int y = ys[j * kTUnits + i];
+  if (warp == kLoadWarp) {
+    // ================= load warp: K/V units of each tile into the ring =================
+    if (lane == 0) {
+      tma_prefetch_desc(&kmap);
+      tma_prefetch_desc(&vmap);
+    }
+    // page row of unit u of the key range: -1 past the range, -2 invalid page
+    auto page_row = [&](int u) -> int {
+      if (u >= n_units) return -1;
+      const int t0 = (u_first + u) * kUnitTokens;
+      const int32_t pb = __ldg(p.block_tables + static_cast<int64_t>(b) * p.max_blocks +
+                               t0 / p.block_size);
+      if (pb < 0 || pb >= p.num_blocks) return -2;
+      return (pb * p.num_kv_heads + hkv) * p.block_size + (t0 % p.block_size);
+    };
+    int y_next = (lane < kTUnits && n_tiles > 0) ? page_row(lane) : -1;
+    for (int j = 0; j < n_tiles; ++j) {
+      const int y_cur = y_next;
+      if (j + 1 < n_tiles) y_next = lane < kTUnits ? page_row((j + 1) * kTUnits + lane) : -1;
+      const int stage = j % S;
+      if (j >= S && !mbar_wait_bounded(smem_u32(&kv_empty[stage]), ((j / S) - 1) & 1, kWaitLimit))
+        bad = true;
+      int ys[kTUnits];
 #pragma unroll
-      for (int kb = 0; kb < Lay::kKBlocks; ++kb) {
-        const uint32_t off = kb * kTKeys * 128 + i * kUnitTokens * 128;
-        tma_load_2d(kdst + off, &kmap, kb * 64, y, bar);
-        tma_load_2d(vdst + off, &vmap, kb * 64, y, bar);
+      for (int i = 0; i < kTUnits; ++i) ys[i] = __shfl_sync(0xffffffffu, y_cur, i);
+      if (lane == 0) {
+        const uint32_t bar = smem_u32(&kv_full[stage]);
+        const uint32_t kdst = base + Lay::kStageOff + stage * Lay::kStageBytes;
+        int loaded = 0;
+#pragma unroll
+        for (int i = 0; i < kTUnits; ++i) {
+          if (ys[i] >= 0) ++loaded;
+          if (ys[i] == -2) bad = true;
+        }
+        if (loaded == 0) {
+          mbar_arrive(bar);
+        } else {
+          mbar_arrive_expect_tx(bar, loaded * 2 * Lay::kKBlocks * kUnitTokens * 128);
+#pragma unroll
+          for (int i = 0; i < kTUnits; ++i) {
+            if (ys[i] < 0) continue;
+#pragma unroll
+            for (int kb = 0; kb < Lay::kKBlocks; ++kb) {
+              const uint32_t off = kb * kTKeys * 128 + i * kUnitTokens * 128;
+              tma_load_2d(kdst + off, &kmap, kb * 64, ys[i], bar);
+              tma_load_2d(kdst + Lay::kKVTile + off, &vmap, kb * 64, ys[i], bar);
+            }
+          }
+        }
       }
     }
-  };
-  int issued = 0;
-  if (tid == 0)
-    for (; issued < min(S, n_tiles); ++issued) issue(issued);
-
-  float m_run = -INFINITY, l_run = 0.f;
-  const uint32_t ph = base + Lay::kPOff, pl = ph + Lay::kPBytes;
-  int j = 0;
-  for (; j < n_tiles; ++j) {
-    const int stage = j % S;
-    const uint32_t kst = base + Lay::kStageOff + stage * Lay::kStageBytes;
-    const uint32_t vst = kst + Lay::kKVTile;
-    const int t0 = (u_first + j * kTUnits) * kUnitTokens;
-    if (!mbar_wait_bounded(smem_u32(&full_bar[stage]), (j / S) & 1, kWaitLimit)) bad = true;
-
-    // ---- S = Q K^T into TMEM columns [0, 64) ----
-    // (every thread read S(j-1) before the last barrier, so it may be overwritten)
-    if (tid == 0) {
+    // every copy started has landed (already waited for unless a wait ran out)
+    if (lane == 0)
+      for (int t = max(0, n_tiles - S); t < n_tiles; ++t)
+        if (!mbar_wait_bounded(smem_u32(&kv_full[t % S]), (t / S) & 1, kWaitLimit)) bad = true;
+  } else if (warp == kMmaWarp) {
+    // ================= MMA warp =================
+    auto stage_addr = [&](int j) { return base + Lay::kStageOff + (j % S) * Lay::kStageBytes; };
+    auto wait_full = [&](int j) {
+      if (!mbar_wait_bounded(smem_u32(&kv_full[j % S]), (j / S) & 1, kWaitLimit)) bad = true;
+      tc_fence_after();
+    };
+    auto issue_s = [&](int t, int j) {
+      if (lane == 0) {
+        const uint32_t qt = base + t * Lay::kQTileBytes, kt = stage_addr(j);
 #pragma unroll
-      for (int kk = 0; kk < D / 16; ++kk) {
-        const uint64_t ad =
-            umma_sdesc_sw128(base + Lay::kQOff + (kk >> 2) * kTRows * 128 + (kk & 3) * 32, 16, 1024);
-        const uint64_t bd = umma_sdesc_sw128(kst + (kk >> 2) * kTKeys * 128 + (kk & 3) * 32, 16, 1024);
-        umma_f16(tS, ad, bd, kIdS, kk > 0 ? 1u : 0u);
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint64_t ad = umma_sdesc_sw128(qt + (kk >> 2) * kQT * 128 + (kk & 3) * 32, 16, 1024);
+          const uint64_t bd = umma_sdesc_sw128(kt + (kk >> 2) * kTKeys * 128 + (kk & 3) * 32, 16, 1024);
+          umma_f16(tmem + Lay::s_col(t), ad, bd, kIdS, kk > 0 ? 1u : 0u);
+        }
+        umma_commit(smem_u32(&s_full[t]));
       }
-      umma_commit(smem_u32(&s_bar));
-    }
-
-    // V rows of keys outside [k_lo, pos1] (before the window of every row, past
-    // the chunk, or never loaded) may hold anything, even NaN: zero them so that
-    // their zero weights give exact zeros
-    if ((t0 < k_lo || t0 + kTKeys - 1 > pos1) && tid < kTKeys) {
-      const int kp = t0 + tid;
-      if (kp < k_lo || kp > pos1) {
+      __syncwarp();
+    };
+    // V rows of keys outside [k_lo, pos1] (before every row's window, past
+    // the chunk, never loaded) may hold anything: zero them
+    auto zero_v = [&](int j) {
+      const int t0 = (u_first + j * kTUnits) * kUnitTokens;
+      if (t0 >= k_lo && t0 + kTKeys - 1 <= pos1) return;
+      const uint32_t vt = stage_addr(j) + Lay::kKVTile;
+      for (int r = lane; r < kTKeys; r += 32) {
+        const int kp = t0 + r;
+        if (kp >= k_lo && kp <= pos1) continue;
 #pragma unroll
         for (int kb = 0; kb < Lay::kKBlocks; ++kb)
 #pragma unroll
           for (int c = 0; c < 8; ++c)
-            st_shared_v4(vst + kb * kTKeys * 128 + tid * 128 + c * 16, make_uint4(0u, 0u, 0u, 0u));
+            st_shared_v4(vt + kb * kTKeys * 128 + r * 128 + c * 16, make_uint4(0u, 0u, 0u, 0u));
       }
+      fence_proxy_async_smem();
+      __syncwarp();
+    };
+    if (n_tiles > 0) {
+      wait_full(0);
+      issue_s(0, 0);
+      issue_s(1, 0);
+      zero_v(0);
     }
-
-    if (!mbar_wait_bounded(smem_u32(&s_bar), j & 1, kWaitLimit)) bad = true;
-    tc_fence_after();
-
-    // ---- the row's scores: mask, log2 scale, maximum ----
-    float s[kTKeys];
+    for (int j = 0; j < n_tiles; ++j) {
+      const uint32_t vt = stage_addr(j) + Lay::kKVTile;
 #pragma unroll
-    for (int c = 0; c < kTKeys; c += 16) {
-      float v[16];
-      tmem_ld16(tS + lane_off + c, v);
+      for (int t = 0; t < 2; ++t) {
+        if (!mbar_wait_bounded(smem_u32(&p_full[t]), j & 1, kWaitLimit)) bad = true;
+        tc_fence_after();
+        if (lane == 0) {
 #pragma unroll
-      for (int i = 0; i < 16; ++i) s[c + i] = v[i];
-    }
-    float mx = -INFINITY;
+          for (int part = 0; part < (PLO ? 2 : 1); ++part) {
 #pragma unroll
-    for (int c = 0; c < kTKeys; ++c) {
-      const int kp = t0 + c;
-      const bool valid = kp <= rpos && (p.window <= 0 || rpos - kp < p.window);
-      s[c] = valid ? s[c] * p.scale_log2 : -INFINITY;
-      mx = fmaxf(mx, s[c]);
-    }
-    const float m_old = m_run;
-    const bool need = mx > m_old + kTRescale;
-    if (need) m_run = mx;
-    const bool rescale = need && m_old != -INFINITY;
-    const float alpha = rescale ? ex2(m_old - m_run) : 1.f;
-    l_run *= alpha;
-
-    // P and O are free once the previous PV product completed; so is the stage
-    // tile j-1 used, which takes tile j-1+S
-    if (j > 0) {
-      if (!mbar_wait_bounded(smem_u32(&pv_bar), (j - 1) & 1, kWaitLimit)) bad = true;
-      tc_fence_after();
-      if (tid == 0 && issued < n_tiles && !bad) issue(issued++);
-    }
-
-    // ---- P rows (hi, lo) as K-major operands ----
-#pragma unroll
-    for (int c8 = 0; c8 < kTKeys / 8; ++c8) {
-      uint32_t hw[4], lw[4];
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const float p0 = ex2(s[c8 * 8 + 2 * e] - m_run);
-        const float p1 = ex2(s[c8 * 8 + 2 * e + 1] - m_run);
-        l_run += p0 + p1;
-        hw[e] = Mma<T>::pack(p0, p1);
-        lw[e] = Mma<T>::pack(p0 - Mma<T>::lo_f32(hw[e]), p1 - Mma<T>::hi_f32(hw[e]));
-      }
-      st_shared_v4(ph + sw128(tid, c8), make_uint4(hw[0], hw[1], hw[2], hw[3]));
-      st_shared_v4(pl + sw128(tid, c8), make_uint4(lw[0], lw[1], lw[2], lw[3]));
-    }
-    // ---- lazy rescale of the row's O (after PV(j-1), before PV(j)) ----
-    if (j > 0 && __any_sync(0xffffffffu, rescale)) {
-#pragma unroll
-      for (int c = 0; c < D; c += 16) {
-        float v[16];
-        tmem_ld16(tO + lane_off + c, v);
-#pragma unroll
-        for (int i = 0; i < 16; ++i) v[i] *= alpha;
-        tmem_st16(tO + lane_off + c, v);
-      }
-    }
-    fence_proxy_async_smem();
-    tc_fence_before();
-    if (__syncthreads_or(bad)) {
-      bad = true;
-      break;
-    }
-    tc_fence_after();
-
-    // ---- O += P_hi V + P_lo V into TMEM columns [64, 64 + D) ----
-    if (tid == 0) {
-#pragma unroll
-      for (int part = 0; part < 2; ++part) {
-#pragma unroll
-        for (int kk = 0; kk < kTKeys / 16; ++kk) {
-          const uint64_t ad = umma_sdesc_sw128((part ? pl : ph) + kk * 32, 16, 1024);
-          // V: keys are the K dimension (8-row groups 1 KB apart, 16 keys per
-          // step), head dims the N dimension (64-column blocks one tile apart)
-          const uint64_t bd = umma_sdesc_sw128(vst + kk * 16 * 128, kTKeys * 128, 1024);
-          umma_f16(tO, ad, bd, kIdO, (j > 0 || kk > 0 || part > 0) ? 1u : 0u);
+            for (int kk = 0; kk < kTKeys / 16; ++kk) {
+              // V: keys are the K dimension (8-row groups 1 KB apart, 16 keys a
+              // step), head dims the N dimension (64-column blocks a tile apart)
+              const uint64_t bd = umma_sdesc_sw128(vt + kk * 16 * 128, kTKeys * 128, 1024);
+              umma_f16_ts(tmem + Lay::o_col(t), tmem + Lay::p_col(t) + part * 32 + kk * 8, bd,
+                          kIdO, (j > 0 || kk > 0 || part > 0) ? 1u : 0u);
+            }
+          }
+          umma_commit(smem_u32(&o_done[t]));
+          if (t == 1) umma_commit(smem_u32(&kv_empty[j % S]));
+        }
+        __syncwarp();
+        if (j + 1 < n_tiles) {
+          if (t == 0) wait_full(j + 1);
+          issue_s(t, j + 1);
+          if (t == 1) zero_v(j + 1);
         }
       }
-      umma_commit(smem_u32(&pv_bar));
     }
-  }
+    // every product issued has completed
+    if (n_tiles > 0) {
+      if (lane == 0) umma_commit(smem_u32(&done_bar));
+      __syncwarp();
+      if (!mbar_wait_bounded(smem_u32(&done_bar), 0, kWaitLimit)) bad = true;
+    }
+  } else {
+    // ================= softmax warps: one row per thread =================
+    const int t = wg;
+    const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
+    const uint32_t tS = tmem + Lay::s_col(t) + lane_off;
+    const uint32_t tP = tmem + Lay::p_col(t) + lane_off;
+    const uint32_t tO = tmem + Lay::o_col(t) + lane_off;
+    float m_run = -INFINITY, l_run = 0.f;
+    for (int j = 0; j < n_tiles; ++j) {
+      const int t0 = (u_first + j * kTUnits) * kUnitTokens;
+      if (!mbar_wait_bounded(smem_u32(&s_full[t]), j & 1, kWaitLimit)) bad = true;
+      tc_fence_after();
+      float s[kTKeys];
+      tmem_ld64(tS, s);
+      // scores in the log2 domain; keys this row may not see -> -inf
+      float mx = -INFINITY;
+      const bool edge = t0 + kTKeys - 1 > rpos || (p.window > 0 && t0 <= rpos - p.window);
+      if (__any_sync(0xffffffffu, edge)) {
+#pragma unroll
+        for (int c = 0; c < kTKeys; ++c) {
+          const int kp = t0 + c;
+          const bool valid = kp <= rpos && (p.window <= 0 || rpos - kp < p.window);
+          s[c] = valid ? s[c] * p.scale_log2 : -INFINITY;
+          mx = fmaxf(mx, s[c]);
+        }
+      } else {
+#pragma unroll
+        for (int c = 0; c < kTKeys; ++c) {
+          s[c] *= p.scale_log2;
+          mx = fmaxf(mx, s[c]);
+        }
+      }
+      const float m_old = m_run;
+      if (mx > m_old + kTRescale) m_run = mx;
+      const bool rescale = m_run != m_old && m_old != -INFINITY;
+      const float alpha = rescale ? ex2(m_old - m_run) : 1.f;
+      l_run *= alpha;
+      const float m_use = m_run == -INFINITY ? 0.f : m_run;  // nothing visible yet: p = 0
 
-  // ---- drain: every product and every copy this CTA started has landed ----
-  // (products were issued iff there was a tile)
-  if (tid == 0) {
-    if (n_tiles > 0) umma_commit(smem_u32(&done_bar));
-    for (int t = j; t < issued; ++t)
-      if (!mbar_wait_bounded(smem_u32(&full_bar[t % S]), (t / S) & 1, kWaitLimit)) bad = true;
-  }
-  if (n_tiles > 0 && !mbar_wait_bounded(smem_u32(&done_bar), 0, kWaitLimit)) bad = true;
-  tc_fence_after();
-  const bool nan_out = __syncthreads_or(bad) != 0;
+      // P_t and O_t are free once the previous PV product of this tile completed
+      if (j > 0) {
+        if (!mbar_wait_bounded(smem_u32(&o_done[t]), (j - 1) & 1, kWaitLimit)) bad = true;
+        tc_fence_after();
+        if (__any_sync(0xffffffffu, rescale)) {
+#pragma unroll
+          for (int c = 0; c < D; c += 16) {
+            float v[16];
+            tmem_ld16(tO + c, v);
+#pragma unroll
+            for (int i = 0; i < 16; ++i) v[i] *= alpha;
+            tmem_st16(tO + c, v);
+          }
+        }
+      }
+      uint32_t hw[kTKeys / 2];
+#pragma unroll
+      for (int c2 = 0; c2 < kTKeys / 2; ++c2) {
+        const float p0 = ex2(s[2 * c2] - m_use);
+        const float p1 = ex2(s[2 * c2 + 1] - m_use);
+        l_run += p0 + p1;
+        hw[c2] = Mma<T>::pack(p0, p1);
+        if (PLO) {
+          // the lo part takes the place of the spent scores
+          s[2 * c2] = p0 - Mma<T>::lo_f32(hw[c2]);
+          s[2 * c2 + 1] = p1 - Mma<T>::hi_f32(hw[c2]);
+        }
+      }
+      {
+        uint32_t w[16];
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+#pragma unroll
+          for (int i = 0; i < 16; ++i) w[i] = hw[h * 16 + i];
+          tmem_st16u(tP + h * 16, w);
+        }
+        if (PLO) {
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+#pragma unroll
+            for (int i = 0; i < 16; ++i)
+              w[i] = Mma<T>::pack(s[2 * (h * 16 + i)], s[2 * (h * 16 + i) + 1]);
+            tmem_st16u(tP + 32 + h * 16, w);
+          }
+        }
+      }
+      tmem_wait_st();
+      tc_fence_before();
+      mbar_arrive(smem_u32(&p_full[t]));
+    }
+    if (n_tiles > 0) {
+      if (!mbar_wait_bounded(smem_u32(&o_done[t]), (n_tiles - 1) & 1, kWaitLimit)) bad = true;
+      tc_fence_after();
+    }
 
-  // ---- epilogue: O / l to the output rows (TMEM loads are warp-wide) ----
-  T* dst = static_cast<T*>(p.out) +
-           (static_cast<int64_t>(start + tile0 + (row_ok ? ti : 0)) * p.num_q_heads +
-            hkv * p.group + chunk * gc + hi) * D;
-  const float inv = nan_out ? __int_as_float(0x7fc00000) : 1.f / l_run;
+    // ---- join, then O / l to the output rows (TMEM loads are warp-wide) ----
+    if (bad) s_bad = 1;
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const bool nan_out = s_bad != 0;
+    T* dst = static_cast<T*>(p.out) + qo_row;
+    const float inv = nan_out ? __int_as_float(0x7fc00000) : 1.f / l_run;
 #pragma unroll
-  for (int c = 0; c < D; c += 16) {
-    float v[16];
-    if (!nan_out) {
-      tmem_ld16(tO + lane_off + c, v);
-    } else {
+    for (int c = 0; c < D; c += 16) {
+      float v[16];
+      if (!nan_out) {
+        tmem_ld16(tO + c, v);
+      } else {
 #pragma unroll
-      for (int i = 0; i < 16; ++i) v[i] = 0.f;
+        for (int i = 0; i < 16; ++i) v[i] = 0.f;
+      }
+      if (row_ok) {
+        uint32_t w[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) w[i] = Mma<T>::pack(v[2 * i] * inv, v[2 * i + 1] * inv);
+        reinterpret_cast<uint4*>(dst + c)[0] = make_uint4(w[0], w[1], w[2], w[3]);
+        reinterpret_cast<uint4*>(dst + c)[1] = make_uint4(w[4], w[5], w[6], w[7]);
+      }
     }
-    if (row_ok) {
-      uint32_t w[8];
-#pragma unroll
-      for (int i = 0; i < 8; ++i) w[i] = Mma<T>::pack(v[2 * i] * inv, v[2 * i + 1] * inv);
-      reinterpret_cast<uint4*>(dst + c)[0] = make_uint4(w[0], w[1], w[2], w[3]);
-      reinterpret_cast<uint4*>(dst + c)[1] = make_uint4(w[4], w[5], w[6], w[7]);
-    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0)
+      asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
+                   "r"(Lay::kTmemCols));
+    return;
   }
+  // load and MMA warps: the softmax warps' join and final barriers
+  if (bad) s_bad = 1;
   tc_fence_before();
   __syncthreads();
-  if (warp == 0)
-    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
-                 "r"(Lay::kTmemCols));
+  tc_fence_after();
+  __syncthreads();
 }
 
-template <typename T, int D>
+template <typename T, int D, bool PLO>
 cudaError_t launch_t(const CUtensorMap& kmap, const CUtensorMap& vmap, const TcParams& p,
                      int max_chunk, int num_seqs, cudaStream_t stream) {
   using Lay = TcLayout<D>;
-  auto kern = prefill_tc_kernel<T, D>;
-  const size_t smem = 1024 + Lay::kYOff + sizeof(int) * p.max_units;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       static_cast<int>(smem));
+  auto kern = prefill_tc_kernel<T, D, PLO>;
+  const int smem = 1024 + Lay::kSmemBytes;
+  // the shared-memory opt-in is per device; set it once for each
+  static std::atomic<uint64_t> configured{0};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
-  const int tok_per_cta = kTRows >> p.head_chunk_log2;
+  const uint64_t bit = dev < 64 ? (uint64_t(1) << dev) : 0;
+  if (!bit || !(configured.load(std::memory_order_acquire) & bit)) {
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    configured.fetch_or(bit, std::memory_order_acq_rel);
+  }
+  const int tok_per_cta = kRowsCta >> p.head_chunk_log2;
   dim3 grid((max_chunk + tok_per_cta - 1) / tok_per_cta, p.num_kv_heads * p.num_head_chunks,
             num_seqs);
   return launch_pdl(kern, grid, dim3(kTThreads), smem, stream, kmap, vmap, p);
 }
 
 }  // namespace
-
-size_t prefill_tc_smem_bytes(int head_dim, int max_units) {
-  const int y = head_dim == 128 ? TcLayout<128>::kYOff : TcLayout<64>::kYOff;
-  return 1024 + y + sizeof(int) * static_cast<size_t>(max_units);
-}
 
 cudaError_t launch_prefill_tc(int dtype, int head_dim, const void* q, const int32_t* cu_q,
                               int num_seqs, int num_q_heads, int max_chunk, int64_t num_blocks,
@@ -386,7 +473,7 @@ cudaError_t launch_prefill_tc(int dtype, int head_dim, const void* q, const int3
   p.num_kv_heads = num_kv_heads;
   p.group = num_q_heads / num_kv_heads;
   int gc = 1;
-  while (gc * 2 <= 16 && p.group % (gc * 2) == 0) gc *= 2;
+  while (gc * 2 <= 16 && p.group % (gc * 2) == 0) gc *= 2;  // largest power of two dividing G
   int lg = 0;
   while ((1 << lg) < gc) ++lg;
   p.head_chunk_log2 = lg;
@@ -394,15 +481,17 @@ cudaError_t launch_prefill_tc(int dtype, int head_dim, const void* q, const int3
   p.max_blocks = max_blocks;
   p.block_size = block_size;
   p.window = window;
-  p.max_units = static_cast<int>(static_cast<int64_t>(max_blocks) * block_size / kUnitTokens) + 1;
   p.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
+  // fp16 weights carry 11 significant bits, enough alone; bf16 ones (8 bits)
+  // get a second, lo part
   if (dtype == 1) {
-    if (head_dim == 128) return launch_t<__half, 128>(kmap, vmap, p, max_chunk, num_seqs, stream);
-    return launch_t<__half, 64>(kmap, vmap, p, max_chunk, num_seqs, stream);
+    if (head_dim == 128)
+      return launch_t<__half, 128, false>(kmap, vmap, p, max_chunk, num_seqs, stream);
+    return launch_t<__half, 64, false>(kmap, vmap, p, max_chunk, num_seqs, stream);
   }
   if (head_dim == 128)
-    return launch_t<__nv_bfloat16, 128>(kmap, vmap, p, max_chunk, num_seqs, stream);
-  return launch_t<__nv_bfloat16, 64>(kmap, vmap, p, max_chunk, num_seqs, stream);
+    return launch_t<__nv_bfloat16, 128, true>(kmap, vmap, p, max_chunk, num_seqs, stream);
+  return launch_t<__nv_bfloat16, 64, true>(kmap, vmap, p, max_chunk, num_seqs, stream);
 }
 
 }  // namespace pkv

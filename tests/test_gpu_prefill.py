@@ -64,6 +64,12 @@ CASES = [
     ("window37", torch.bfloat16, 8, 2, 128, 16, [0, 100, 7], [80, 50, 30], 37),
     ("window1", torch.float16, 4, 4, 128, 16, [5, 0], [20, 33], 1),
     ("window_large", torch.float16, 4, 2, 128, 16, [10, 60], [30, 20], 5000),
+    # rows whose first key tiles are wholly outside their window
+    ("window5_long", torch.bfloat16, 4, 4, 128, 16, [0, 200], [300, 260], 5),
+    ("window16_d64", torch.float16, 8, 2, 64, 16, [100], [500], 16),
+    # many key tiles, several CTAs per (sequence, kv head)
+    ("long_prefix", torch.bfloat16, 8, 2, 128, 16, [3000, 1], [300, 700], 0),
+    ("long_prefix_fp16", torch.float16, 16, 2, 128, 32, [2047], [513], 0),
 ]
 
 
