@@ -304,6 +304,10 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
     const uint32_t tS = tmem + Lay::s_col(t) + lane_off;
     const uint32_t tP = tmem + Lay::p_col(t) + lane_off;
     const uint32_t tO = tmem + Lay::o_col(t) + lane_off;
+    // a positive scale lets the maximum be taken on the raw scores and the
+    // scaling ride in the exponent's FFMA; otherwise scores are scaled first
+    const bool raw_max = p.scale_log2 > 0.f;
+    const float sl = raw_max ? p.scale_log2 : 1.f;
     float m_run = -INFINITY, l_run = 0.f;
     for (int j = 0; j < n_tiles; ++j) {
       const int t0 = (u_first + j * kTUnits) * kUnitTokens;
@@ -311,30 +315,33 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
       tc_fence_after();
       float s[kTKeys];
       tmem_ld64(tS, s);
-      // scores in the log2 domain; keys this row may not see -> -inf
-      float mx = -INFINITY;
+      if (!raw_max) {
+#pragma unroll
+        for (int c = 0; c < kTKeys; ++c) s[c] *= p.scale_log2;
+      }
+      // keys this row may not see -> -inf
       const bool edge = t0 + kTKeys - 1 > rpos || (p.window > 0 && t0 <= rpos - p.window);
       if (__any_sync(0xffffffffu, edge)) {
 #pragma unroll
         for (int c = 0; c < kTKeys; ++c) {
           const int kp = t0 + c;
           const bool valid = kp <= rpos && (p.window <= 0 || rpos - kp < p.window);
-          s[c] = valid ? s[c] * p.scale_log2 : -INFINITY;
-          mx = fmaxf(mx, s[c]);
-        }
-      } else {
-#pragma unroll
-        for (int c = 0; c < kTKeys; ++c) {
-          s[c] *= p.scale_log2;
-          mx = fmaxf(mx, s[c]);
+          s[c] = valid ? s[c] : -INFINITY;
         }
       }
+      float mp[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) mp[i] = s[i];
+#pragma unroll
+      for (int c = 8; c < kTKeys; ++c) mp[c & 7] = fmaxf(mp[c & 7], s[c]);
+      const float mx =
+          fmaxf(fmaxf(fmaxf(mp[0], mp[1]), fmaxf(mp[2], mp[3])),
+                fmaxf(fmaxf(mp[4], mp[5]), fmaxf(mp[6], mp[7]))) * sl;
       const float m_old = m_run;
       if (mx > m_old + kTRescale) m_run = mx;
       const bool rescale = m_run != m_old && m_old != -INFINITY;
       const float alpha = rescale ? ex2(m_old - m_run) : 1.f;
-      l_run *= alpha;
-      const float m_use = m_run == -INFINITY ? 0.f : m_run;  // nothing visible yet: p = 0
+      const float neg_m = m_run == -INFINITY ? 0.f : -m_run;  // nothing visible yet: p = 0
 
       // P_t and O_t are free once the previous PV product of this tile completed
       if (j > 0) {
@@ -351,37 +358,23 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
           }
         }
       }
-      uint32_t hw[kTKeys / 2];
+      // P = 2^(s*sl - m), written to TMEM 32 keys at a time
+      float ls[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-      for (int c2 = 0; c2 < kTKeys / 2; ++c2) {
-        const float p0 = ex2(s[2 * c2] - m_use);
-        const float p1 = ex2(s[2 * c2 + 1] - m_use);
-        l_run += p0 + p1;
-        hw[c2] = Mma<T>::pack(p0, p1);
-        if (PLO) {
-          // the lo part takes the place of the spent scores
-          s[2 * c2] = p0 - Mma<T>::lo_f32(hw[c2]);
-          s[2 * c2 + 1] = p1 - Mma<T>::hi_f32(hw[c2]);
+      for (int h = 0; h < 2; ++h) {
+        uint32_t w[16], wl[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          const float p0 = ex2(fmaf(s[h * 32 + 2 * i], sl, neg_m));
+          const float p1 = ex2(fmaf(s[h * 32 + 2 * i + 1], sl, neg_m));
+          ls[i & 3] += p0 + p1;
+          w[i] = Mma<T>::pack(p0, p1);
+          if (PLO) wl[i] = Mma<T>::pack(p0 - Mma<T>::lo_f32(w[i]), p1 - Mma<T>::hi_f32(w[i]));
         }
+        tmem_st16u(tP + h * 16, w);
+        if (PLO) tmem_st16u(tP + 32 + h * 16, wl);
       }
-      {
-        uint32_t w[16];
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-#pragma unroll
-          for (int i = 0; i < 16; ++i) w[i] = hw[h * 16 + i];
-          tmem_st16u(tP + h * 16, w);
-        }
-        if (PLO) {
-#pragma unroll
-          for (int h = 0; h < 2; ++h) {
-#pragma unroll
-            for (int i = 0; i < 16; ++i)
-              w[i] = Mma<T>::pack(s[2 * (h * 16 + i)], s[2 * (h * 16 + i) + 1]);
-            tmem_st16u(tP + 32 + h * 16, w);
-          }
-        }
-      }
+      l_run = l_run * alpha + ((ls[0] + ls[1]) + (ls[2] + ls[3]));
       tmem_wait_st();
       tc_fence_before();
       mbar_arrive(smem_u32(&p_full[t]));

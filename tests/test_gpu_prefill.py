@@ -104,3 +104,25 @@ def test_prefill_last_row_equals_decode(pkv_lib):
     torch.cuda.synchronize()
     diff = (out[last].double() - dec.double()).abs().max().item()
     assert diff <= 2e-3 + 0.5 * torch.finfo(torch.bfloat16).eps * dec.double().abs().max().item()
+
+
+@pytest.mark.parametrize("scale", [0.0, -0.0625])
+def test_prefill_nonpositive_scale(pkv_lib, oracle_lib, scale):
+    """A zero scale gives the mean of the visible V rows; a negative one flips
+    which keys dominate.  Both take the kernel's scale-first path."""
+    chunks, prefixes = [70, 130], [40, 0]
+    w, q, k, v, cu, lens = _prefill_case(torch.bfloat16, 8, 2, 128, 16, prefixes, chunks, 0,
+                                         seed=11)
+    kc, vc = w.k_cache.cpu(), w.v_cache.cpu()
+    bt = w.block_tables.cpu().numpy()
+    lens_h = lens.cpu().numpy()
+    slots = [oracle.slot_for_position(bt[b], w.spec.block_size, lens_h[b] - n + i)
+             for b, n in enumerate(chunks) for i in range(n)]
+    oracle.append(k.cpu(), v.cpu(), np.array(slots, np.int64), kc, vc)
+    ref = oracle.prefill(q.cpu(), cu.cpu().numpy(), kc, vc, bt, lens_h, 0, scale)
+    out = pkv_lib.pkv_prefill(q, k, v, cu, w.k_cache, w.v_cache, w.block_tables, lens, 0, scale,
+                              max_chunk=max(chunks))
+    torch.cuda.synchronize()
+    g = out.double().cpu().numpy()
+    err = np.abs(g - ref)
+    assert (err <= 2e-3 + 0.5 * torch.finfo(torch.bfloat16).eps * np.abs(ref)).all(), err.max()
