@@ -7,23 +7,27 @@
 //
 // How.  A CTA owns 256 query rows of one (sequence, kv head): (token, GQA
 // head) pairs, so every K/V page it reads serves the whole group.  The rows
-// form two tiles of 128 (one per TMEM lane), worked on in ping-pong:
-//   warp 9      (load)    TMA of the 16-key K and V units of each 64-key tile
-//                         into a ring of stages (128-byte swizzle);
-//   warp 8      (MMA)     one thread issues S_t = Q_t K^T (M 128, N 64, both
-//                         operands K-major in shared memory) and
-//                         O_t += P_t V (A = P_t read from TMEM, B = V read
-//                         MN-major straight from its TMA tile);
-//   warps 0-3 / 4-7       tile 0 / tile 1 softmax: each thread owns one row
-//                         (its TMEM lane), loads its 64 scores, masks, keeps
-//                         the running maximum and sum, writes P back to TMEM
-//                         and, when the maximum moved by more than 2^8,
-//                         rescales its O row in TMEM (lazy rescaling).
+// form two tiles of 128 (one per TMEM lane), worked on in ping-pong over
+// tiles of 128 keys:
+//   warp 9       (load)    TMA of the 16-key K and V units of each key tile
+//                          into two rings of stages (128-byte swizzle);
+//   warps 10-11  (V prep)  turn each landed V tile into fp16 in place (bf16
+//                          caches) and zero the rows of keys no row of the CTA
+//                          may see, so garbage (even NaN) in unused slots
+//                          cannot leak through a zero weight;
+//   warp 8       (MMA)     one thread issues S_t = Q_t K^T (M 128, N 128, both
+//                          operands K-major in shared memory) and
+//                          O_t += P_t V (A = P_t read from TMEM, B = V read
+//                          MN-major from its stage);
+//   warps 0-3 / 4-7        tile 0 / tile 1 softmax: each thread owns one row
+//                          (its TMEM lane), loads its 128 scores, masks, keeps
+//                          the running maximum and sum, writes P as fp16 over
+//                          the scores it came from, and, when the maximum
+//                          moved by more than 2^8, rescales its O row in TMEM
+//                          (lazy rescaling).
 // While one tile's rows are in the softmax, the tensor cores work on the
-// other tile's products.  P is kept as one 16-bit part or, for bf16, as a
-// hi and a lo part (so the weights keep ~16 significant bits).
-// V rows of keys that no row of the CTA may see are zeroed before the
-// products, so garbage (even NaN) in unused slots cannot leak.
+// other tile's products.  The softmax warpgroups take registers from the
+// others (setmaxnreg).
 #include <atomic>
 #include <math.h>
 
@@ -35,11 +39,15 @@ namespace {
 
 constexpr int kQT = 128;          // rows per Q tile == TMEM lanes
 constexpr int kRowsCta = 2 * kQT;
-constexpr int kTKeys = 64;        // keys per K/V tile
+constexpr int kTKeys = 128;       // keys per K/V tile
 constexpr int kTUnits = kTKeys / kUnitTokens;
-constexpr int kMmaWarp = 8, kLoadWarp = 9;
-constexpr int kTThreads = 320;
+constexpr int kMmaWarp = 8, kLoadWarp = 9, kPrepWarp0 = 10;
+constexpr int kPrepThreads = 64;
+constexpr int kTThreads = 384;
 constexpr float kTRescale = 8.0f;
+// register split: the two softmax warpgroups grow, the third shrinks; the sum
+// must not exceed what the block is launched with (checked on the host)
+constexpr int kSoftmaxRegs = 200, kOtherRegs = 104;
 
 struct TcParams {
   const void* q;
@@ -56,17 +64,16 @@ struct TcParams {
 
 template <int D>
 struct TcLayout {
-  static constexpr int kStages = D == 128 ? 4 : 6;
+  static constexpr int kStages = D == 128 ? 2 : 3;          // per ring (K, V)
   static constexpr int kKBlocks = D / 64;                   // 128-byte column blocks
   static constexpr int kQTileBytes = kKBlocks * kQT * 128;
-  static constexpr int kKVTile = kKBlocks * kTKeys * 128;   // K (or V) of one tile
-  static constexpr int kStageBytes = 2 * kKVTile;
-  static constexpr int kStageOff = 2 * kQTileBytes;
-  static constexpr int kSmemBytes = kStageOff + kStages * kStageBytes;
-  // TMEM columns: O_t at t*D, S_t at 2D + 64t, P_t at 2D + 128 + 64t (hi, then lo)
+  static constexpr int kKVTile = kKBlocks * kTKeys * 128;   // K (or V) of one key tile
+  static constexpr int kKOff = 2 * kQTileBytes;
+  static constexpr int kVOff = kKOff + kStages * kKVTile;
+  static constexpr int kSmemBytes = kVOff + kStages * kKVTile;
+  // TMEM columns: O_t at t*D, S_t (and P_t over its first 64) at 2D + 128t
   static constexpr uint32_t o_col(int t) { return static_cast<uint32_t>(t * D); }
-  static constexpr uint32_t s_col(int t) { return static_cast<uint32_t>(2 * D + 64 * t); }
-  static constexpr uint32_t p_col(int t) { return static_cast<uint32_t>(2 * D + 128 + 64 * t); }
+  static constexpr uint32_t s_col(int t) { return static_cast<uint32_t>(2 * D + 128 * t); }
   static constexpr uint32_t kTmemCols = 512;
   static_assert(2 * D + 256 <= 512, "TMEM columns");
 };
@@ -75,18 +82,26 @@ __device__ __forceinline__ uint32_t sw128(int row, int chunk) {
   return static_cast<uint32_t>(row * 128 + (((chunk & 7) ^ (row & 7)) << 4));
 }
 
-template <typename T, int D, bool PLO>
+// two bf16 (low half first) -> two fp16; `inf_flag` collects fp16 overflow
+__device__ __forceinline__ uint32_t bf16x2_to_f16x2(uint32_t w, uint32_t& inf_flag) {
+  const float lo = __uint_as_float(w << 16), hi = __uint_as_float(w & 0xffff0000u);
+  const uint32_t h = Mma<__half>::pack(lo, hi);
+  inf_flag |= ((h & 0x7c007c00u) + 0x04000400u) & 0x80008000u;  // exponent all ones
+  return h;
+}
+
+template <typename T, int D>
 __global__ void __launch_bounds__(kTThreads, 1)
 prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
                   const TcParams p) {
   using Lay = TcLayout<D>;
   constexpr int S = Lay::kStages;
-  constexpr uint32_t kFmt = __is_same(T, __nv_bfloat16) ? 1u : 0u;
-  constexpr uint32_t kIdS = umma_idesc_f16(kFmt, kQT, kTKeys, 0);
-  constexpr uint32_t kIdO = umma_idesc_f16(kFmt, kQT, D, 1);
+  constexpr bool kBf16 = __is_same(T, __nv_bfloat16);
+  constexpr uint32_t kIdS = umma_idesc_f16(kBf16 ? 1u : 0u, kQT, kTKeys, 0);
+  constexpr uint32_t kIdO = umma_idesc_f16(0u, kQT, D, 1);  // P and V in fp16
 
   extern __shared__ uint8_t smem_raw[];
-  __shared__ __align__(8) uint64_t kv_full[S], kv_empty[S];
+  __shared__ __align__(8) uint64_t k_full[S], k_empty[S], v_full[S], v_ready[S], v_empty[S];
   __shared__ __align__(8) uint64_t s_full[2], p_full[2], o_done[2], done_bar;
   __shared__ uint32_t tmem_base_s;
   __shared__ int s_bad;
@@ -127,8 +142,11 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
   }
   if (tid == kMmaWarp * 32) {
     for (int s = 0; s < S; ++s) {
-      mbar_init(smem_u32(&kv_full[s]), 1);
-      mbar_init(smem_u32(&kv_empty[s]), 1);
+      mbar_init(smem_u32(&k_full[s]), 1);
+      mbar_init(smem_u32(&k_empty[s]), 1);
+      mbar_init(smem_u32(&v_full[s]), 1);
+      mbar_init(smem_u32(&v_ready[s]), kPrepThreads);
+      mbar_init(smem_u32(&v_empty[s]), 1);
     }
     for (int t = 0; t < 2; ++t) {
       mbar_init(smem_u32(&s_full[t]), 1);
@@ -162,281 +180,312 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
   tc_fence_after();
   const uint32_t tmem = tmem_base_s;
   bool bad = false;
+  auto k_addr = [&](int j) { return base + Lay::kKOff + (j % S) * Lay::kKVTile; };
+  auto v_addr = [&](int j) { return base + Lay::kVOff + (j % S) * Lay::kKVTile; };
 
-  if (warp == kLoadWarp) {
-    // ================= load warp: K/V units of each tile into the ring =================
-    if (lane == 0) {
-      tma_prefetch_desc(&kmap);
-      tma_prefetch_desc(&vmap);
-    }
-    // page row of unit u of the key range: -1 past the range, -2 invalid page
-    auto page_row = [&](int u) -> int {
-      if (u >= n_units) return -1;
-      const int t0 = (u_first + u) * kUnitTokens;
-      const int32_t pb = __ldg(p.block_tables + static_cast<int64_t>(b) * p.max_blocks +
-                               t0 / p.block_size);
-      if (pb < 0 || pb >= p.num_blocks) return -2;
-      return (pb * p.num_kv_heads + hkv) * p.block_size + (t0 % p.block_size);
-    };
-    int y_next = (lane < kTUnits && n_tiles > 0) ? page_row(lane) : -1;
-    for (int j = 0; j < n_tiles; ++j) {
-      const int y_cur = y_next;
-      if (j + 1 < n_tiles) y_next = lane < kTUnits ? page_row((j + 1) * kTUnits + lane) : -1;
-      const int stage = j % S;
-      if (j >= S && !mbar_wait_bounded(smem_u32(&kv_empty[stage]), ((j / S) - 1) & 1, kWaitLimit))
-        bad = true;
-      int ys[kTUnits];
-#pragma unroll
-      for (int i = 0; i < kTUnits; ++i) ys[i] = __shfl_sync(0xffffffffu, y_cur, i);
+  if (warp >= 8) {
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kOtherRegs));
+    if (warp == kLoadWarp) {
+      // ============ load warp: K and V units of each key tile into their rings ============
       if (lane == 0) {
-        const uint32_t bar = smem_u32(&kv_full[stage]);
-        const uint32_t kdst = base + Lay::kStageOff + stage * Lay::kStageBytes;
+        tma_prefetch_desc(&kmap);
+        tma_prefetch_desc(&vmap);
+      }
+      // page row of unit u of the key range: -1 past the range, -2 invalid page
+      auto page_row = [&](int u) -> int {
+        if (u >= n_units) return -1;
+        const int t0 = (u_first + u) * kUnitTokens;
+        const int32_t pb = __ldg(p.block_tables + static_cast<int64_t>(b) * p.max_blocks +
+                                 t0 / p.block_size);
+        if (pb < 0 || pb >= p.num_blocks) return -2;
+        return (pb * p.num_kv_heads + hkv) * p.block_size + (t0 % p.block_size);
+      };
+      auto issue = [&](const CUtensorMap* map, uint32_t bar, uint32_t dst, const int (&ys)[kTUnits],
+                       int loaded) {
+        if (loaded == 0) {
+          mbar_arrive(bar);
+          return;
+        }
+        mbar_arrive_expect_tx(bar, loaded * Lay::kKBlocks * kUnitTokens * 128);
+#pragma unroll
+        for (int i = 0; i < kTUnits; ++i) {
+          if (ys[i] < 0) continue;
+#pragma unroll
+          for (int kb = 0; kb < Lay::kKBlocks; ++kb)
+            tma_load_2d(dst + kb * kTKeys * 128 + i * kUnitTokens * 128, map, kb * 64, ys[i], bar);
+        }
+      };
+      int y_next = (lane < kTUnits && n_tiles > 0) ? page_row(lane) : -1;
+      for (int j = 0; j < n_tiles; ++j) {
+        const int y_cur = y_next;
+        if (j + 1 < n_tiles) y_next = lane < kTUnits ? page_row((j + 1) * kTUnits + lane) : -1;
+        int ys[kTUnits];
         int loaded = 0;
 #pragma unroll
         for (int i = 0; i < kTUnits; ++i) {
+          ys[i] = __shfl_sync(0xffffffffu, y_cur, i);
           if (ys[i] >= 0) ++loaded;
           if (ys[i] == -2) bad = true;
         }
-        if (loaded == 0) {
-          mbar_arrive(bar);
-        } else {
-          mbar_arrive_expect_tx(bar, loaded * 2 * Lay::kKBlocks * kUnitTokens * 128);
-#pragma unroll
-          for (int i = 0; i < kTUnits; ++i) {
-            if (ys[i] < 0) continue;
-#pragma unroll
-            for (int kb = 0; kb < Lay::kKBlocks; ++kb) {
-              const uint32_t off = kb * kTKeys * 128 + i * kUnitTokens * 128;
-              tma_load_2d(kdst + off, &kmap, kb * 64, ys[i], bar);
-              tma_load_2d(kdst + Lay::kKVTile + off, &vmap, kb * 64, ys[i], bar);
+        if (j >= S && !mbar_wait_bounded(smem_u32(&k_empty[j % S]), ((j / S) - 1) & 1, kWaitLimit))
+          bad = true;
+        if (lane == 0) issue(&kmap, smem_u32(&k_full[j % S]), k_addr(j), ys, loaded);
+        if (j >= S && !mbar_wait_bounded(smem_u32(&v_empty[j % S]), ((j / S) - 1) & 1, kWaitLimit))
+          bad = true;
+        if (lane == 0) issue(&vmap, smem_u32(&v_full[j % S]), v_addr(j), ys, loaded);
+      }
+      // every copy started has landed (already waited for unless a wait ran out)
+      if (lane == 0)
+        for (int t = max(0, n_tiles - S); t < n_tiles; ++t) {
+          if (!mbar_wait_bounded(smem_u32(&k_full[t % S]), (t / S) & 1, kWaitLimit)) bad = true;
+          if (!mbar_wait_bounded(smem_u32(&v_full[t % S]), (t / S) & 1, kWaitLimit)) bad = true;
+        }
+    } else if (warp >= kPrepWarp0) {
+      // ============ V prep: fp16 in place (bf16 caches), unseen keys zeroed ============
+      const int ct = tid - kPrepWarp0 * 32;
+      uint32_t inf_flag = 0;
+      for (int j = 0; j < n_tiles; ++j) {
+        if (!mbar_wait_bounded(smem_u32(&v_full[j % S]), (j / S) & 1, kWaitLimit)) bad = true;
+        const int t0 = (u_first + j * kTUnits) * kUnitTokens;
+        const uint32_t vt = v_addr(j);
+        if (kBf16) {
+#pragma unroll 4
+          for (int i = 0; i < Lay::kKVTile / 16 / kPrepThreads; ++i) {
+            const int u = ct + kPrepThreads * i;  // 16-byte chunk of the tile
+            const int kp = t0 + ((u & (kTKeys * 8 - 1)) >> 3);
+            uint4 x = ld_shared_v4(vt + u * 16);
+            if (kp < k_lo || kp > pos1) {
+              x = make_uint4(0u, 0u, 0u, 0u);
+            } else {
+              x.x = bf16x2_to_f16x2(x.x, inf_flag);
+              x.y = bf16x2_to_f16x2(x.y, inf_flag);
+              x.z = bf16x2_to_f16x2(x.z, inf_flag);
+              x.w = bf16x2_to_f16x2(x.w, inf_flag);
             }
+            st_shared_v4(vt + u * 16, x);
+          }
+        } else if (t0 < k_lo || t0 + kTKeys - 1 > pos1) {
+          for (int r = ct; r < kTKeys; r += kPrepThreads) {
+            const int kp = t0 + r;
+            if (kp >= k_lo && kp <= pos1) continue;
+#pragma unroll
+            for (int kb = 0; kb < Lay::kKBlocks; ++kb)
+#pragma unroll
+              for (int c = 0; c < 8; ++c)
+                st_shared_v4(vt + kb * kTKeys * 128 + r * 128 + c * 16, make_uint4(0u, 0u, 0u, 0u));
           }
         }
+        fence_proxy_async_smem();
+        mbar_arrive(smem_u32(&v_ready[j % S]));
       }
-    }
-    // every copy started has landed (already waited for unless a wait ran out)
-    if (lane == 0)
-      for (int t = max(0, n_tiles - S); t < n_tiles; ++t)
-        if (!mbar_wait_bounded(smem_u32(&kv_full[t % S]), (t / S) & 1, kWaitLimit)) bad = true;
-  } else if (warp == kMmaWarp) {
-    // ================= MMA warp =================
-    auto stage_addr = [&](int j) { return base + Lay::kStageOff + (j % S) * Lay::kStageBytes; };
-    auto wait_full = [&](int j) {
-      if (!mbar_wait_bounded(smem_u32(&kv_full[j % S]), (j / S) & 1, kWaitLimit)) bad = true;
-      tc_fence_after();
-    };
-    auto issue_s = [&](int t, int j) {
-      if (lane == 0) {
-        const uint32_t qt = base + t * Lay::kQTileBytes, kt = stage_addr(j);
-#pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint64_t ad = umma_sdesc_sw128(qt + (kk >> 2) * kQT * 128 + (kk & 3) * 32, 16, 1024);
-          const uint64_t bd = umma_sdesc_sw128(kt + (kk >> 2) * kTKeys * 128 + (kk & 3) * 32, 16, 1024);
-          umma_f16(tmem + Lay::s_col(t), ad, bd, kIdS, kk > 0 ? 1u : 0u);
-        }
-        umma_commit(smem_u32(&s_full[t]));
-      }
-      __syncwarp();
-    };
-    // V rows of keys outside [k_lo, pos1] (before every row's window, past
-    // the chunk, never loaded) may hold anything: zero them
-    auto zero_v = [&](int j) {
-      const int t0 = (u_first + j * kTUnits) * kUnitTokens;
-      if (t0 >= k_lo && t0 + kTKeys - 1 <= pos1) return;
-      const uint32_t vt = stage_addr(j) + Lay::kKVTile;
-      for (int r = lane; r < kTKeys; r += 32) {
-        const int kp = t0 + r;
-        if (kp >= k_lo && kp <= pos1) continue;
-#pragma unroll
-        for (int kb = 0; kb < Lay::kKBlocks; ++kb)
-#pragma unroll
-          for (int c = 0; c < 8; ++c)
-            st_shared_v4(vt + kb * kTKeys * 128 + r * 128 + c * 16, make_uint4(0u, 0u, 0u, 0u));
-      }
-      fence_proxy_async_smem();
-      __syncwarp();
-    };
-    if (n_tiles > 0) {
-      wait_full(0);
-      issue_s(0, 0);
-      issue_s(1, 0);
-      zero_v(0);
-    }
-    for (int j = 0; j < n_tiles; ++j) {
-      const uint32_t vt = stage_addr(j) + Lay::kKVTile;
-#pragma unroll
-      for (int t = 0; t < 2; ++t) {
-        if (!mbar_wait_bounded(smem_u32(&p_full[t]), j & 1, kWaitLimit)) bad = true;
-        tc_fence_after();
+      // a bf16 value beyond the fp16 range cannot take part in the fp16 product
+      if (inf_flag) bad = true;
+    } else {
+      // ============ MMA warp ============
+      auto issue_s = [&](int t, int j) {
         if (lane == 0) {
+          const uint32_t qt = base + t * Lay::kQTileBytes, kt = k_addr(j);
 #pragma unroll
-          for (int part = 0; part < (PLO ? 2 : 1); ++part) {
+          for (int kk = 0; kk < D / 16; ++kk) {
+            const uint64_t ad =
+                umma_sdesc_sw128(qt + (kk >> 2) * kQT * 128 + (kk & 3) * 32, 16, 1024);
+            const uint64_t bd =
+                umma_sdesc_sw128(kt + (kk >> 2) * kTKeys * 128 + (kk & 3) * 32, 16, 1024);
+            umma_f16(tmem + Lay::s_col(t), ad, bd, kIdS, kk > 0 ? 1u : 0u);
+          }
+          umma_commit(smem_u32(&s_full[t]));
+        }
+        __syncwarp();
+      };
+      auto wait_k = [&](int j) {
+        if (!mbar_wait_bounded(smem_u32(&k_full[j % S]), (j / S) & 1, kWaitLimit)) bad = true;
+        tc_fence_after();
+      };
+      if (n_tiles > 0) {
+        wait_k(0);
+        issue_s(0, 0);
+        issue_s(1, 0);
+        if (lane == 0) umma_commit(smem_u32(&k_empty[0]));
+      }
+      for (int j = 0; j < n_tiles; ++j) {
+        if (!mbar_wait_bounded(smem_u32(&v_ready[j % S]), (j / S) & 1, kWaitLimit)) bad = true;
+        const uint32_t vt = v_addr(j);
+#pragma unroll
+        for (int t = 0; t < 2; ++t) {
+          if (!mbar_wait_bounded(smem_u32(&p_full[t]), j & 1, kWaitLimit)) bad = true;
+          tc_fence_after();
+          if (lane == 0) {
 #pragma unroll
             for (int kk = 0; kk < kTKeys / 16; ++kk) {
               // V: keys are the K dimension (8-row groups 1 KB apart, 16 keys a
               // step), head dims the N dimension (64-column blocks a tile apart)
               const uint64_t bd = umma_sdesc_sw128(vt + kk * 16 * 128, kTKeys * 128, 1024);
-              umma_f16_ts(tmem + Lay::o_col(t), tmem + Lay::p_col(t) + part * 32 + kk * 8, bd,
-                          kIdO, (j > 0 || kk > 0 || part > 0) ? 1u : 0u);
+              umma_f16_ts(tmem + Lay::o_col(t), tmem + Lay::s_col(t) + kk * 8, bd, kIdO,
+                          (j > 0 || kk > 0) ? 1u : 0u);
             }
+            umma_commit(smem_u32(&o_done[t]));
+            if (t == 1) umma_commit(smem_u32(&v_empty[j % S]));
           }
-          umma_commit(smem_u32(&o_done[t]));
-          if (t == 1) umma_commit(smem_u32(&kv_empty[j % S]));
+          __syncwarp();
+          if (j + 1 < n_tiles) {
+            // S_t(j+1) overwrites P_t(j) after the product above read it (one
+            // issuing thread: the tensor pipe takes them in order)
+            if (t == 0) wait_k(j + 1);
+            issue_s(t, j + 1);
+            if (t == 1 && lane == 0) umma_commit(smem_u32(&k_empty[(j + 1) % S]));
+            __syncwarp();
+          }
         }
+      }
+      // every product issued has completed
+      if (n_tiles > 0) {
+        if (lane == 0) umma_commit(smem_u32(&done_bar));
         __syncwarp();
-        if (j + 1 < n_tiles) {
-          if (t == 0) wait_full(j + 1);
-          issue_s(t, j + 1);
-          if (t == 1) zero_v(j + 1);
-        }
+        if (!mbar_wait_bounded(smem_u32(&done_bar), 0, kWaitLimit)) bad = true;
       }
     }
-    // every product issued has completed
-    if (n_tiles > 0) {
-      if (lane == 0) umma_commit(smem_u32(&done_bar));
-      __syncwarp();
-      if (!mbar_wait_bounded(smem_u32(&done_bar), 0, kWaitLimit)) bad = true;
-    }
-  } else {
-    // ================= softmax warps: one row per thread =================
-    const int t = wg;
-    const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
-    const uint32_t tS = tmem + Lay::s_col(t) + lane_off;
-    const uint32_t tP = tmem + Lay::p_col(t) + lane_off;
-    const uint32_t tO = tmem + Lay::o_col(t) + lane_off;
-    // a positive scale lets the maximum be taken on the raw scores and the
-    // scaling ride in the exponent's FFMA; otherwise scores are scaled first
-    const bool raw_max = p.scale_log2 > 0.f;
-    const float sl = raw_max ? p.scale_log2 : 1.f;
-    float m_run = -INFINITY, l_run = 0.f;
-    for (int j = 0; j < n_tiles; ++j) {
-      const int t0 = (u_first + j * kTUnits) * kUnitTokens;
-      if (!mbar_wait_bounded(smem_u32(&s_full[t]), j & 1, kWaitLimit)) bad = true;
-      tc_fence_after();
-      float s[kTKeys];
-      tmem_ld64(tS, s);
-      if (!raw_max) {
-#pragma unroll
-        for (int c = 0; c < kTKeys; ++c) s[c] *= p.scale_log2;
-      }
-      // keys this row may not see -> -inf
-      const bool edge = t0 + kTKeys - 1 > rpos || (p.window > 0 && t0 <= rpos - p.window);
-      if (__any_sync(0xffffffffu, edge)) {
-#pragma unroll
-        for (int c = 0; c < kTKeys; ++c) {
-          const int kp = t0 + c;
-          const bool valid = kp <= rpos && (p.window <= 0 || rpos - kp < p.window);
-          s[c] = valid ? s[c] : -INFINITY;
-        }
-      }
-      float mp[8];
-#pragma unroll
-      for (int i = 0; i < 8; ++i) mp[i] = s[i];
-#pragma unroll
-      for (int c = 8; c < kTKeys; ++c) mp[c & 7] = fmaxf(mp[c & 7], s[c]);
-      const float mx =
-          fmaxf(fmaxf(fmaxf(mp[0], mp[1]), fmaxf(mp[2], mp[3])),
-                fmaxf(fmaxf(mp[4], mp[5]), fmaxf(mp[6], mp[7]))) * sl;
-      const float m_old = m_run;
-      if (mx > m_old + kTRescale) m_run = mx;
-      const bool rescale = m_run != m_old && m_old != -INFINITY;
-      const float alpha = rescale ? ex2(m_old - m_run) : 1.f;
-      const float neg_m = m_run == -INFINITY ? 0.f : -m_run;  // nothing visible yet: p = 0
-
-      // P_t and O_t are free once the previous PV product of this tile completed
-      if (j > 0) {
-        if (!mbar_wait_bounded(smem_u32(&o_done[t]), (j - 1) & 1, kWaitLimit)) bad = true;
-        tc_fence_after();
-        if (__any_sync(0xffffffffu, rescale)) {
-#pragma unroll
-          for (int c = 0; c < D; c += 16) {
-            float v[16];
-            tmem_ld16(tO + c, v);
-#pragma unroll
-            for (int i = 0; i < 16; ++i) v[i] *= alpha;
-            tmem_st16(tO + c, v);
-          }
-        }
-      }
-      // P = 2^(s*sl - m), written to TMEM 32 keys at a time
-      float ls[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        uint32_t w[16], wl[16];
-#pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          const float p0 = ex2(fmaf(s[h * 32 + 2 * i], sl, neg_m));
-          const float p1 = ex2(fmaf(s[h * 32 + 2 * i + 1], sl, neg_m));
-          ls[i & 3] += p0 + p1;
-          w[i] = Mma<T>::pack(p0, p1);
-          if (PLO) wl[i] = Mma<T>::pack(p0 - Mma<T>::lo_f32(w[i]), p1 - Mma<T>::hi_f32(w[i]));
-        }
-        tmem_st16u(tP + h * 16, w);
-        if (PLO) tmem_st16u(tP + 32 + h * 16, wl);
-      }
-      l_run = l_run * alpha + ((ls[0] + ls[1]) + (ls[2] + ls[3]));
-      tmem_wait_st();
-      tc_fence_before();
-      mbar_arrive(smem_u32(&p_full[t]));
-    }
-    if (n_tiles > 0) {
-      if (!mbar_wait_bounded(smem_u32(&o_done[t]), (n_tiles - 1) & 1, kWaitLimit)) bad = true;
-      tc_fence_after();
-    }
-
-    // ---- join, then O / l to the output rows (TMEM loads are warp-wide) ----
+    // the softmax warps' join and final barriers
     if (bad) s_bad = 1;
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    const bool nan_out = s_bad != 0;
-    T* dst = static_cast<T*>(p.out) + qo_row;
-    const float inv = nan_out ? __int_as_float(0x7fc00000) : 1.f / l_run;
-#pragma unroll
-    for (int c = 0; c < D; c += 16) {
-      float v[16];
-      if (!nan_out) {
-        tmem_ld16(tO + c, v);
-      } else {
-#pragma unroll
-        for (int i = 0; i < 16; ++i) v[i] = 0.f;
-      }
-      if (row_ok) {
-        uint32_t w[8];
-#pragma unroll
-        for (int i = 0; i < 8; ++i) w[i] = Mma<T>::pack(v[2 * i] * inv, v[2 * i + 1] * inv);
-        reinterpret_cast<uint4*>(dst + c)[0] = make_uint4(w[0], w[1], w[2], w[3]);
-        reinterpret_cast<uint4*>(dst + c)[1] = make_uint4(w[4], w[5], w[6], w[7]);
-      }
-    }
-    tc_fence_before();
     __syncthreads();
-    if (warp == 0)
-      asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
-                   "r"(Lay::kTmemCols));
     return;
   }
-  // load and MMA warps: the softmax warps' join and final barriers
+
+  // ================= softmax warps: one row per thread =================
+  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kSoftmaxRegs));
+  const int t = wg;
+  const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
+  const uint32_t tS = tmem + Lay::s_col(t) + lane_off;
+  const uint32_t tO = tmem + Lay::o_col(t) + lane_off;
+  // a positive scale lets the maximum be taken on the raw scores and the
+  // scaling ride in the exponent's FFMA; otherwise scores are scaled first
+  const bool raw_max = p.scale_log2 > 0.f;
+  const float sl = raw_max ? p.scale_log2 : 1.f;
+  float m_run = -INFINITY, l_run = 0.f;
+  for (int j = 0; j < n_tiles; ++j) {
+    const int t0 = (u_first + j * kTUnits) * kUnitTokens;
+    if (!mbar_wait_bounded(smem_u32(&s_full[t]), j & 1, kWaitLimit)) bad = true;
+    tc_fence_after();
+    float s[kTKeys];
+    tmem_ld128(tS, s);
+    if (!raw_max) {
+#pragma unroll
+      for (int c = 0; c < kTKeys; ++c) s[c] *= p.scale_log2;
+    }
+    // keys this row may not see -> -inf
+    const bool edge = t0 + kTKeys - 1 > rpos || (p.window > 0 && t0 <= rpos - p.window);
+    if (__any_sync(0xffffffffu, edge)) {
+#pragma unroll
+      for (int c = 0; c < kTKeys; ++c) {
+        const int kp = t0 + c;
+        const bool valid = kp <= rpos && (p.window <= 0 || rpos - kp < p.window);
+        s[c] = valid ? s[c] : -INFINITY;
+      }
+    }
+    float mp[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) mp[i] = s[i];
+#pragma unroll
+    for (int c = 8; c < kTKeys; ++c) mp[c & 7] = fmaxf(mp[c & 7], s[c]);
+    const float mx = fmaxf(fmaxf(fmaxf(mp[0], mp[1]), fmaxf(mp[2], mp[3])),
+                           fmaxf(fmaxf(mp[4], mp[5]), fmaxf(mp[6], mp[7]))) * sl;
+    const float m_old = m_run;
+    if (mx > m_old + kTRescale) m_run = mx;
+    const bool rescale = m_run != m_old && m_old != -INFINITY;
+    const float alpha = rescale ? ex2(m_old - m_run) : 1.f;
+    const float neg_m = m_run == -INFINITY ? 0.f : -m_run;  // nothing visible yet: p = 0
+
+    // S_t(j) completing means O_t += P_t(j-1) V completed too (issued before it)
+    if (__any_sync(0xffffffffu, rescale)) {
+#pragma unroll
+      for (int c = 0; c < D; c += 16) {
+        float v[16];
+        tmem_ld16(tO + c, v);
+#pragma unroll
+        for (int i = 0; i < 16; ++i) v[i] *= alpha;
+        tmem_st16(tO + c, v);
+      }
+    }
+    // P = 2^(s*sl - m) as fp16 over the first 64 columns of S_t
+    float2 acc[4] = {{0.f, 0.f}, {0.f, 0.f}, {0.f, 0.f}, {0.f, 0.f}};
+    const float2 sl2 = make_float2(sl, sl), nm2 = make_float2(neg_m, neg_m);
+#pragma unroll
+    for (int h = 0; h < kTKeys / 32; ++h) {
+      uint32_t w[16];
+#pragma unroll
+      for (int i = 0; i < 16; ++i) {
+        const float2 x = ffma2(make_float2(s[h * 32 + 2 * i], s[h * 32 + 2 * i + 1]), sl2, nm2);
+        const float2 pr = make_float2(ex2(x.x), ex2(x.y));
+        acc[i & 3] = fadd2(acc[i & 3], pr);
+        w[i] = Mma<__half>::pack(pr.x, pr.y);
+      }
+      tmem_st16u(tS + h * 16, w);
+    }
+    const float2 a01 = fadd2(acc[0], acc[1]), a23 = fadd2(acc[2], acc[3]);
+    l_run = l_run * alpha + ((a01.x + a01.y) + (a23.x + a23.y));
+    tmem_wait_st();
+    tc_fence_before();
+    mbar_arrive(smem_u32(&p_full[t]));
+  }
+  if (n_tiles > 0) {
+    if (!mbar_wait_bounded(smem_u32(&o_done[t]), (n_tiles - 1) & 1, kWaitLimit)) bad = true;
+    tc_fence_after();
+  }
+
+  // ---- join, then O / l to the output rows (TMEM loads are warp-wide) ----
   if (bad) s_bad = 1;
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  const bool nan_out = s_bad != 0;
+  T* dst = static_cast<T*>(p.out) + qo_row;
+  const float inv = nan_out ? __int_as_float(0x7fc00000) : 1.f / l_run;
+#pragma unroll
+  for (int c = 0; c < D; c += 16) {
+    float v[16];
+    if (!nan_out) {
+      tmem_ld16(tO + c, v);
+    } else {
+#pragma unroll
+      for (int i = 0; i < 16; ++i) v[i] = 0.f;
+    }
+    if (row_ok) {
+      uint32_t w[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) w[i] = Mma<T>::pack(v[2 * i] * inv, v[2 * i + 1] * inv);
+      reinterpret_cast<uint4*>(dst + c)[0] = make_uint4(w[0], w[1], w[2], w[3]);
+      reinterpret_cast<uint4*>(dst + c)[1] = make_uint4(w[4], w[5], w[6], w[7]);
+    }
+  }
+  tc_fence_before();
   __syncthreads();
+  if (warp == 0)
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
+                 "r"(Lay::kTmemCols));
 }
 
-template <typename T, int D, bool PLO>
+template <typename T, int D>
 cudaError_t launch_t(const CUtensorMap& kmap, const CUtensorMap& vmap, const TcParams& p,
                      int max_chunk, int num_seqs, cudaStream_t stream) {
   using Lay = TcLayout<D>;
-  auto kern = prefill_tc_kernel<T, D, PLO>;
+  auto kern = prefill_tc_kernel<T, D>;
   const int smem = 1024 + Lay::kSmemBytes;
-  // the shared-memory opt-in is per device; set it once for each
+  // per device, once: the shared-memory opt-in, and a check that the block
+  // is launched with the registers the warpgroups' split hands out (a larger
+  // split would leave setmaxnreg.inc waiting)
   static std::atomic<uint64_t> configured{0};
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   const uint64_t bit = dev < 64 ? (uint64_t(1) << dev) : 0;
   if (!bit || !(configured.load(std::memory_order_acquire) & bit)) {
+    cudaFuncAttributes attr{};
+    e = cudaFuncGetAttributes(&attr, kern);
+    if (e != cudaSuccess) return e;
+    if (attr.numRegs * kTThreads < 2 * kQT * kSoftmaxRegs + 4 * 32 * kOtherRegs)
+      return cudaErrorInvalidConfiguration;
     e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     configured.fetch_or(bit, std::memory_order_acq_rel);
@@ -475,16 +524,13 @@ cudaError_t launch_prefill_tc(int dtype, int head_dim, const void* q, const int3
   p.block_size = block_size;
   p.window = window;
   p.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
-  // fp16 weights carry 11 significant bits, enough alone; bf16 ones (8 bits)
-  // get a second, lo part
   if (dtype == 1) {
-    if (head_dim == 128)
-      return launch_t<__half, 128, false>(kmap, vmap, p, max_chunk, num_seqs, stream);
-    return launch_t<__half, 64, false>(kmap, vmap, p, max_chunk, num_seqs, stream);
+    if (head_dim == 128) return launch_t<__half, 128>(kmap, vmap, p, max_chunk, num_seqs, stream);
+    return launch_t<__half, 64>(kmap, vmap, p, max_chunk, num_seqs, stream);
   }
   if (head_dim == 128)
-    return launch_t<__nv_bfloat16, 128, true>(kmap, vmap, p, max_chunk, num_seqs, stream);
-  return launch_t<__nv_bfloat16, 64, true>(kmap, vmap, p, max_chunk, num_seqs, stream);
+    return launch_t<__nv_bfloat16, 128>(kmap, vmap, p, max_chunk, num_seqs, stream);
+  return launch_t<__nv_bfloat16, 64>(kmap, vmap, p, max_chunk, num_seqs, stream);
 }
 
 }  // namespace pkv
