@@ -274,6 +274,9 @@ PREFILL = {
     "prefill_bf16": dict(dtype=torch.bfloat16, num_seqs=4, num_q_heads=32, num_kv_heads=8,
                          head_dim=128, block_size=16, chunk=1024, prefix_lo=2048,
                          prefix_hi=6144, seed=11),
+    "prefill_fp16": dict(dtype=torch.float16, num_seqs=4, num_q_heads=32, num_kv_heads=8,
+                         head_dim=128, block_size=16, chunk=1024, prefix_lo=2048,
+                         prefix_hi=6144, seed=11),
 }
 
 

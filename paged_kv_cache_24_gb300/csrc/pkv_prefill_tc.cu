@@ -42,8 +42,8 @@ constexpr int kRowsCta = 2 * kQT;
 constexpr int kTKeys = 128;       // keys per K/V tile
 constexpr int kTUnits = kTKeys / kUnitTokens;
 constexpr int kMmaWarp = 8, kLoadWarp = 9, kPrepWarp0 = 10;
-constexpr int kPrepThreads = 64;
 constexpr int kTThreads = 384;
+constexpr int kPrepThreads = kTThreads - kPrepWarp0 * 32;
 constexpr float kTRescale = 8.0f;
 // register split: the two softmax warpgroups grow, the third shrinks; the sum
 // must not exceed what the block is launched with (checked on the host)
@@ -64,13 +64,14 @@ struct TcParams {
 
 template <int D>
 struct TcLayout {
-  static constexpr int kStages = D == 128 ? 2 : 3;          // per ring (K, V)
+  static constexpr int kKStages = D == 128 ? 2 : 3;  // stages per ring
+  static constexpr int kVStages = kKStages;
   static constexpr int kKBlocks = D / 64;                   // 128-byte column blocks
   static constexpr int kQTileBytes = kKBlocks * kQT * 128;
   static constexpr int kKVTile = kKBlocks * kTKeys * 128;   // K (or V) of one key tile
   static constexpr int kKOff = 2 * kQTileBytes;
-  static constexpr int kVOff = kKOff + kStages * kKVTile;
-  static constexpr int kSmemBytes = kVOff + kStages * kKVTile;
+  static constexpr int kVOff = kKOff + kKStages * kKVTile;
+  static constexpr int kSmemBytes = kVOff + kVStages * kKVTile;
   // TMEM columns: O_t at t*D, S_t (and P_t over its first 64) at 2D + 128t
   static constexpr uint32_t o_col(int t) { return static_cast<uint32_t>(t * D); }
   static constexpr uint32_t s_col(int t) { return static_cast<uint32_t>(2 * D + 128 * t); }
@@ -82,11 +83,12 @@ __device__ __forceinline__ uint32_t sw128(int row, int chunk) {
   return static_cast<uint32_t>(row * 128 + (((chunk & 7) ^ (row & 7)) << 4));
 }
 
-// two bf16 (low half first) -> two fp16; `inf_flag` collects fp16 overflow
-__device__ __forceinline__ uint32_t bf16x2_to_f16x2(uint32_t w, uint32_t& inf_flag) {
+// two bf16 (low half first) -> two fp16; `amax` keeps the largest magnitudes
+// (an infinity there means a value beyond the fp16 range)
+__device__ __forceinline__ uint32_t bf16x2_to_f16x2(uint32_t w, __half2& amax) {
   const float lo = __uint_as_float(w << 16), hi = __uint_as_float(w & 0xffff0000u);
   const uint32_t h = Mma<__half>::pack(lo, hi);
-  inf_flag |= ((h & 0x7c007c00u) + 0x04000400u) & 0x80008000u;  // exponent all ones
+  amax = __hmax2(amax, __habs2(*reinterpret_cast<const __half2*>(&h)));
   return h;
 }
 
@@ -95,13 +97,13 @@ __global__ void __launch_bounds__(kTThreads, 1)
 prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
                   const TcParams p) {
   using Lay = TcLayout<D>;
-  constexpr int S = Lay::kStages;
+  constexpr int SK = Lay::kKStages, SV = Lay::kVStages;
   constexpr bool kBf16 = __is_same(T, __nv_bfloat16);
   constexpr uint32_t kIdS = umma_idesc_f16(kBf16 ? 1u : 0u, kQT, kTKeys, 0);
   constexpr uint32_t kIdO = umma_idesc_f16(0u, kQT, D, 1);  // P and V in fp16
 
   extern __shared__ uint8_t smem_raw[];
-  __shared__ __align__(8) uint64_t k_full[S], k_empty[S], v_full[S], v_ready[S], v_empty[S];
+  __shared__ __align__(8) uint64_t k_full[SK], k_empty[SK], v_full[SV], v_ready[SV], v_empty[SV];
   __shared__ __align__(8) uint64_t s_full[2], p_full[2], o_done[2], done_bar;
   __shared__ uint32_t tmem_base_s;
   __shared__ int s_bad;
@@ -141,9 +143,11 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
   }
   if (tid == kMmaWarp * 32) {
-    for (int s = 0; s < S; ++s) {
+    for (int s = 0; s < SK; ++s) {
       mbar_init(smem_u32(&k_full[s]), 1);
       mbar_init(smem_u32(&k_empty[s]), 1);
+    }
+    for (int s = 0; s < SV; ++s) {
       mbar_init(smem_u32(&v_full[s]), 1);
       mbar_init(smem_u32(&v_ready[s]), kPrepThreads);
       mbar_init(smem_u32(&v_empty[s]), 1);
@@ -180,8 +184,8 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
   tc_fence_after();
   const uint32_t tmem = tmem_base_s;
   bool bad = false;
-  auto k_addr = [&](int j) { return base + Lay::kKOff + (j % S) * Lay::kKVTile; };
-  auto v_addr = [&](int j) { return base + Lay::kVOff + (j % S) * Lay::kKVTile; };
+  auto k_addr = [&](int j) { return base + Lay::kKOff + (j % SK) * Lay::kKVTile; };
+  auto v_addr = [&](int j) { return base + Lay::kVOff + (j % SV) * Lay::kKVTile; };
 
   if (warp >= 8) {
     asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kOtherRegs));
@@ -227,40 +231,42 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
           if (ys[i] >= 0) ++loaded;
           if (ys[i] == -2) bad = true;
         }
-        if (j >= S && !mbar_wait_bounded(smem_u32(&k_empty[j % S]), ((j / S) - 1) & 1, kWaitLimit))
+        if (j >= SK &&
+            !mbar_wait_bounded(smem_u32(&k_empty[j % SK]), ((j / SK) - 1) & 1, kWaitLimit))
           bad = true;
-        if (lane == 0) issue(&kmap, smem_u32(&k_full[j % S]), k_addr(j), ys, loaded);
-        if (j >= S && !mbar_wait_bounded(smem_u32(&v_empty[j % S]), ((j / S) - 1) & 1, kWaitLimit))
+        if (lane == 0) issue(&kmap, smem_u32(&k_full[j % SK]), k_addr(j), ys, loaded);
+        if (j >= SV &&
+            !mbar_wait_bounded(smem_u32(&v_empty[j % SV]), ((j / SV) - 1) & 1, kWaitLimit))
           bad = true;
-        if (lane == 0) issue(&vmap, smem_u32(&v_full[j % S]), v_addr(j), ys, loaded);
+        if (lane == 0) issue(&vmap, smem_u32(&v_full[j % SV]), v_addr(j), ys, loaded);
       }
       // every copy started has landed (already waited for unless a wait ran out)
-      if (lane == 0)
-        for (int t = max(0, n_tiles - S); t < n_tiles; ++t) {
-          if (!mbar_wait_bounded(smem_u32(&k_full[t % S]), (t / S) & 1, kWaitLimit)) bad = true;
-          if (!mbar_wait_bounded(smem_u32(&v_full[t % S]), (t / S) & 1, kWaitLimit)) bad = true;
-        }
+      if (lane == 0) {
+        for (int t = max(0, n_tiles - SK); t < n_tiles; ++t)
+          if (!mbar_wait_bounded(smem_u32(&k_full[t % SK]), (t / SK) & 1, kWaitLimit)) bad = true;
+        for (int t = max(0, n_tiles - SV); t < n_tiles; ++t)
+          if (!mbar_wait_bounded(smem_u32(&v_full[t % SV]), (t / SV) & 1, kWaitLimit)) bad = true;
+      }
     } else if (warp >= kPrepWarp0) {
       // ============ V prep: fp16 in place (bf16 caches), unseen keys zeroed ============
       const int ct = tid - kPrepWarp0 * 32;
-      uint32_t inf_flag = 0;
+      __half2 amax = __float2half2_rn(0.f);
       for (int j = 0; j < n_tiles; ++j) {
-        if (!mbar_wait_bounded(smem_u32(&v_full[j % S]), (j / S) & 1, kWaitLimit)) bad = true;
+        if (!mbar_wait_bounded(smem_u32(&v_full[j % SV]), (j / SV) & 1, kWaitLimit)) bad = true;
         const int t0 = (u_first + j * kTUnits) * kUnitTokens;
         const uint32_t vt = v_addr(j);
         if (kBf16) {
 #pragma unroll 4
-          for (int i = 0; i < Lay::kKVTile / 16 / kPrepThreads; ++i) {
-            const int u = ct + kPrepThreads * i;  // 16-byte chunk of the tile
+          for (int u = ct; u < Lay::kKVTile / 16; u += kPrepThreads) {  // 16-byte chunks
             const int kp = t0 + ((u & (kTKeys * 8 - 1)) >> 3);
             uint4 x = ld_shared_v4(vt + u * 16);
             if (kp < k_lo || kp > pos1) {
               x = make_uint4(0u, 0u, 0u, 0u);
             } else {
-              x.x = bf16x2_to_f16x2(x.x, inf_flag);
-              x.y = bf16x2_to_f16x2(x.y, inf_flag);
-              x.z = bf16x2_to_f16x2(x.z, inf_flag);
-              x.w = bf16x2_to_f16x2(x.w, inf_flag);
+              x.x = bf16x2_to_f16x2(x.x, amax);
+              x.y = bf16x2_to_f16x2(x.y, amax);
+              x.z = bf16x2_to_f16x2(x.z, amax);
+              x.w = bf16x2_to_f16x2(x.w, amax);
             }
             st_shared_v4(vt + u * 16, x);
           }
@@ -276,10 +282,10 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
           }
         }
         fence_proxy_async_smem();
-        mbar_arrive(smem_u32(&v_ready[j % S]));
+        mbar_arrive(smem_u32(&v_ready[j % SV]));
       }
       // a bf16 value beyond the fp16 range cannot take part in the fp16 product
-      if (inf_flag) bad = true;
+      if (__hisinf(__low2half(amax)) || __hisinf(__high2half(amax))) bad = true;
     } else {
       // ============ MMA warp ============
       auto issue_s = [&](int t, int j) {
@@ -298,7 +304,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
         __syncwarp();
       };
       auto wait_k = [&](int j) {
-        if (!mbar_wait_bounded(smem_u32(&k_full[j % S]), (j / S) & 1, kWaitLimit)) bad = true;
+        if (!mbar_wait_bounded(smem_u32(&k_full[j % SK]), (j / SK) & 1, kWaitLimit)) bad = true;
         tc_fence_after();
       };
       if (n_tiles > 0) {
@@ -308,7 +314,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
         if (lane == 0) umma_commit(smem_u32(&k_empty[0]));
       }
       for (int j = 0; j < n_tiles; ++j) {
-        if (!mbar_wait_bounded(smem_u32(&v_ready[j % S]), (j / S) & 1, kWaitLimit)) bad = true;
+        if (!mbar_wait_bounded(smem_u32(&v_ready[j % SV]), (j / SV) & 1, kWaitLimit)) bad = true;
         const uint32_t vt = v_addr(j);
 #pragma unroll
         for (int t = 0; t < 2; ++t) {
@@ -324,7 +330,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
                           (j > 0 || kk > 0) ? 1u : 0u);
             }
             umma_commit(smem_u32(&o_done[t]));
-            if (t == 1) umma_commit(smem_u32(&v_empty[j % S]));
+            if (t == 1) umma_commit(smem_u32(&v_empty[j % SV]));
           }
           __syncwarp();
           if (j + 1 < n_tiles) {
@@ -332,7 +338,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
             // issuing thread: the tensor pipe takes them in order)
             if (t == 0) wait_k(j + 1);
             issue_s(t, j + 1);
-            if (t == 1 && lane == 0) umma_commit(smem_u32(&k_empty[(j + 1) % S]));
+            if (t == 1 && lane == 0) umma_commit(smem_u32(&k_empty[(j + 1) % SK]));
             __syncwarp();
           }
         }
@@ -484,7 +490,7 @@ cudaError_t launch_t(const CUtensorMap& kmap, const CUtensorMap& vmap, const TcP
     cudaFuncAttributes attr{};
     e = cudaFuncGetAttributes(&attr, kern);
     if (e != cudaSuccess) return e;
-    if (attr.numRegs * kTThreads < 2 * kQT * kSoftmaxRegs + 4 * 32 * kOtherRegs)
+    if (attr.numRegs * kTThreads < 2 * kQT * kSoftmaxRegs + (kTThreads - 2 * kQT) * kOtherRegs)
       return cudaErrorInvalidConfiguration;
     e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
