@@ -204,8 +204,11 @@ typedef struct pkv_decode_options {
  *   pkv_decode); then the query at position p attends positions j <= p (and
  *   p - j < window when window > 0) of the pools, which hold the prefix and
  *   the chunk.  out [T][num_q_heads][head_dim].
- *   Limits: head_dim 64 or 128, max_blocks_per_seq * block_size <= 262,144.
- *   In-kernel errors (bad block id, L_b < n_b) make the affected rows NaN.
+ *   Limits: head_dim 64 or 128.  The P.V product runs in fp16: with a bf16
+ *   cache, V values beyond the fp16 range (|v| > 65504) are an error.
+ *   In-kernel errors (bad block id, L_b < n_b, V out of range) make the rows
+ *   of the affected work item NaN: up to 256 (token, query head) rows of one
+ *   sequence and kv head.
  */
 int pkv_prefill(const void* q, const void* k, const void* v, const int32_t* cu_q,
                 int32_t num_seqs, int32_t num_q_heads, int32_t max_chunk, void* k_cache,

@@ -10,6 +10,7 @@
 
 #include "pkv.h"
 #include "pkv_internal.h"
+#include "pkv_prefill.h"
 
 namespace {
 
@@ -420,8 +421,8 @@ int pkv_prefill(const void* q, const void* k, const void* v, const int32_t* cu_q
       num_q_heads % layout->num_kv_heads != 0)
     return PKV_ERR_SHAPE;
   if (num_seqs > 65535) return PKV_ERR_UNSUPPORTED;
-  const int64_t max_units = static_cast<int64_t>(max_blocks_per_seq) * layout->block_size / 16;
-  if (max_units > 16384) return PKV_ERR_UNSUPPORTED;  // page-row table lives in shared memory
+  if (static_cast<int64_t>(max_blocks_per_seq) * layout->block_size > 0x7fffffffLL)
+    return PKV_ERR_UNSUPPORTED;  // positions are 32-bit
   if (num_seqs == 0 || max_chunk == 0) return PKV_OK;
   if (!q || !k || !v || !cu_q || !k_cache || !v_cache || !block_tables || !context_lens || !out)
     return PKV_ERR_NULL;
@@ -437,7 +438,7 @@ int pkv_prefill(const void* q, const void* k, const void* v, const int32_t* cu_q
   return to_status(pkv::launch_prefill(
       layout->dtype, layout->head_dim, q, k, v, cu_q, num_seqs, num_q_heads, max_chunk, k_cache,
       v_cache, layout->num_blocks, layout->num_kv_heads, layout->block_size, block_tables,
-      max_blocks_per_seq, context_lens, window, scale, out, kmap, vmap, true,
+      max_blocks_per_seq, context_lens, window, scale, out, kmap, vmap,
       static_cast<cudaStream_t>(stream)));
 }
 

@@ -131,22 +131,6 @@ cudaError_t launch_combine(int dtype, int head_dim, const DecodeParams& p, cudaS
 cudaError_t launch_append(int elem_bytes, const void* k, const void* v, const int64_t* slots,
                           int64_t num_tokens, void* k_cache, void* v_cache, int64_t num_blocks,
                           int num_kv_heads, int block_size, int head_dim, cudaStream_t stream);
-// Chunked prefill: the chunk's rows to their slots, then attention.
-cudaError_t launch_prefill(int dtype, int head_dim, const void* q, const void* k, const void* v,
-                           const int32_t* cu_q, int num_seqs, int num_q_heads, int max_chunk,
-                           void* k_cache, void* v_cache, int64_t num_blocks, int num_kv_heads,
-                           int block_size, const int32_t* block_tables, int max_blocks,
-                           const int32_t* context_lens, int window, float scale, void* out,
-                           const CUtensorMap& kmap, const CUtensorMap& vmap, bool tensor_memory,
-                           cudaStream_t stream);
-// Attention half of the chunked prefill on the tcgen05 tensor cores (the
-// chunk's rows must already be in the pool).
-cudaError_t launch_prefill_tc(int dtype, int head_dim, const void* q, const int32_t* cu_q,
-                              int num_seqs, int num_q_heads, int max_chunk, int64_t num_blocks,
-                              int num_kv_heads, int block_size, const int32_t* block_tables,
-                              int max_blocks, const int32_t* context_lens, int window,
-                              float scale, void* out, const CUtensorMap& kmap,
-                              const CUtensorMap& vmap, cudaStream_t stream);
 cudaError_t launch_slot_mapping(const int32_t* block_tables, int num_seqs, int max_blocks,
                                 const int64_t* positions, int block_size, int64_t* slots,
                                 cudaStream_t stream);

@@ -33,6 +33,8 @@
 
 #include "pkv_device.cuh"
 #include "pkv_internal.h"
+#include "pkv_prefill.h"
+#include "pkv_tcgen05.cuh"
 
 namespace pkv {
 namespace {
