@@ -92,6 +92,12 @@ def _load():
         lib.oracle_decode_fp8.argtypes = [c_vp, c_i32, c_i32, c_i32, c_vp, c_vp, c_vp, c_vp,
                                           c_i64, c_i32, c_i32, c_i32, c_vp, c_i32, c_vp, c_i32,
                                           c_i32, c_dbl, c_vp, c_i64, c_vp, c_i32]
+        lib.oracle_quantize_row_int8.restype = ctypes.c_float
+        lib.oracle_quantize_row_int8.argtypes = [c_vp, c_i32, c_vp]
+        lib.oracle_append_int8.restype = ctypes.c_int
+        lib.oracle_append_int8.argtypes = lib.oracle_append_fp8.argtypes
+        lib.oracle_decode_int8.restype = ctypes.c_int
+        lib.oracle_decode_int8.argtypes = lib.oracle_decode_fp8.argtypes
         lib.oracle_prefill.restype = ctypes.c_int
         lib.oracle_prefill.argtypes = [c_vp, c_i32, c_vp, c_i32, c_i32, c_vp, c_vp, c_i64, c_i32,
                                        c_i32, c_i32, c_vp, c_i32, c_vp, c_i32, c_dbl, c_vp, c_i32]
@@ -316,6 +322,88 @@ def append_fp8(k, v, slot_mapping_, k_codes, v_codes, k_scale, v_scale) -> None:
                                    _ptr(vc), _ptr(ks), _ptr(vs), nb, hkv, bs, d)
     if rc != 0:
         raise ValueError(f"oracle_append_fp8 failed with code {rc}")
+
+
+def _codes8(x):
+    """Raw bytes of an FP8 or INT8 code array (torch or numpy), sharing memory."""
+    if type(x).__module__.startswith("torch"):
+        import torch
+        x = x.contiguous()
+        return x.view(torch.uint8).numpy() if x.dtype != torch.uint8 else x.numpy()
+    x = np.ascontiguousarray(x)
+    if x.dtype not in (np.uint8, np.int8):
+        raise TypeError("codes must be uint8 or int8")
+    return x.view(np.uint8)
+
+
+def quantize_rows_int8(x):
+    """INT8-quantise each row of a float32 matrix [n, D]: (codes int8 [n, D], scales float32 [n])."""
+    x = np.ascontiguousarray(x, dtype=np.float32)
+    n, d = x.shape
+    codes = np.empty((n, d), dtype=np.int8)
+    scales = np.empty(n, dtype=np.float32)
+    lib = _load()
+    for i in range(n):
+        scales[i] = lib.oracle_quantize_row_int8(_ptr(x[i]), d, codes[i].ctypes.data)
+    return codes, scales
+
+
+def append_int8(k, v, slot_mapping_, k_codes, v_codes, k_scale, v_scale) -> None:
+    """Quantise and write each token's K/V rows ([T, Hkv, D], fp16/bf16/fp32) into
+    INT8 pools ([NB, Hkv, bs, D] int8 codes, [NB, Hkv, bs] float32 scales), in place."""
+    kr, kd = _as_raw(k)
+    vr, vd = _as_raw(v)
+    if kd != vd:
+        raise TypeError("k and v dtypes differ")
+    for c in (k_codes, v_codes, k_scale, v_scale):
+        contiguous = c.is_contiguous() if hasattr(c, "is_contiguous") else c.flags.c_contiguous
+        if not contiguous:
+            raise ValueError("pools must be contiguous so they can be written in place")
+    kc, vc = _codes8(k_codes), _codes8(v_codes)
+    ks, vs = _f32(k_scale), _f32(v_scale)
+    slots = _int_array(slot_mapping_, np.int64)
+    nb, hkv, bs, d = kc.shape
+    rc = _load().oracle_append_int8(_ptr(kr), _ptr(vr), kd, _ptr(slots), slots.size, _ptr(kc),
+                                    _ptr(vc), _ptr(ks), _ptr(vs), nb, hkv, bs, d)
+    if rc != 0:
+        raise ValueError(f"oracle_append_int8 failed with code {rc}")
+
+
+def decode_int8(q, k_codes, v_codes, k_scale, v_scale, block_tables, context_lens, window: int,
+                scale: float, pairs=None, threads: int = 0, check: bool = True,
+                num_sinks: int = 0) -> np.ndarray:
+    """Paged decode over INT8 pools (stored value = code * row scale), in float64."""
+    return _decode_codes("oracle_decode_int8", q, _codes8(k_codes), _codes8(v_codes), k_scale,
+                         v_scale, block_tables, context_lens, window, scale, pairs, threads,
+                         check, num_sinks)
+
+
+def _decode_codes(fn, q, kc, vc, k_scale, v_scale, block_tables, context_lens, window, scale,
+                  pairs, threads, check, num_sinks):
+    qr, qd = _as_raw(q)
+    ks, vs = _f32(k_scale), _f32(v_scale)
+    bt = _int_array(block_tables, np.int32)
+    lens = _int_array(context_lens, np.int32)
+    B, Hq, D = qr.shape
+    nb, hkv, bs, d2 = kc.shape
+    if d2 != D:
+        raise ValueError("head_dim mismatch")
+    if pairs is None:
+        pairs_arr, n = None, B * Hq
+    else:
+        pairs_arr = _int_array(pairs, np.int32).reshape(-1, 2)
+        n = pairs_arr.shape[0]
+        if n == 0:
+            return np.empty((0, D), dtype=np.float64)
+    out = np.empty((n, D), dtype=np.float64)
+    rc = getattr(_load(), fn)(_ptr(qr), qd, B, Hq, _ptr(kc), _ptr(vc), _ptr(ks), _ptr(vs),
+                              nb, hkv, bs, D, _ptr(bt), bt.shape[1], _ptr(lens), int(window),
+                              int(num_sinks), float(scale),
+                              None if pairs_arr is None else _ptr(pairs_arr), n, _ptr(out),
+                              int(threads))
+    if check and rc != 0:
+        raise ValueError(f"{fn} failed with code {rc}")
+    return out if pairs is not None else out.reshape(B, Hq, D)
 
 
 def decode_fp8(q, k_codes, v_codes, k_scale, v_scale, block_tables, context_lens, window: int,

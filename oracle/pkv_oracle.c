@@ -43,6 +43,12 @@
  *     an all-zero row gets scale 1.  The divisions and the product are single
  *     IEEE float32 operations.  Decoding over such a cache attends over the
  *     stored values code * scale, widened to double.
+ *   - INT8 codes (same page and item): two's complement int8 with one float32
+ *     scale per row, stored value = code * scale; scale = absmax / 127, code =
+ *     x * (127 / absmax) rounded to the nearest integer, ties to even, and
+ *     clamped to [-127, 127] (the symmetric range: -128 is never produced);
+ *     an all-zero row gets scale 1; a NaN element gets code 0.  Single IEEE
+ *     float32 divisions and products, as for FP8.
  *
  * Build: gcc -O2 -fopenmp -shared -fPIC pkv_oracle.c -o liboracle.so -lm
  * (no fast-math: the reference arithmetic must stay IEEE double).
@@ -55,7 +61,7 @@
 #include <omp.h>
 #endif
 
-enum { ORACLE_F32 = 0, ORACLE_F16 = 1, ORACLE_BF16 = 2, ORACLE_FP8 = 3 };
+enum { ORACLE_F32 = 0, ORACLE_F16 = 1, ORACLE_BF16 = 2, ORACLE_FP8 = 3, ORACLE_I8 = 4 };
 
 enum {
   ORACLE_OK = 0,
@@ -143,6 +149,34 @@ float oracle_quantize_row(const float* x, int32_t n, uint8_t* codes) {
   return scale;
 }
 
+/* INT8 row quantiser (see the reading at the top): writes n codes, returns
+ * the scale. */
+float oracle_quantize_row_int8(const float* x, int32_t n, int8_t* codes) {
+  float absmax = 0.0f;
+  for (int32_t i = 0; i < n; ++i) {
+    float a = fabsf(x[i]);
+    if (a > absmax) absmax = a;
+  }
+  float scale = 1.0f, inv = 1.0f;
+  if (absmax > 0.0f) {
+    volatile float top = 127.0f; /* single float32 divisions */
+    scale = absmax / top;
+    inv = top / absmax;
+  }
+  for (int32_t i = 0; i < n; ++i) {
+    volatile float prod = x[i] * inv;
+    if (prod != prod) {
+      codes[i] = 0;
+      continue;
+    }
+    double r = nearbyint((double)prod); /* default rounding: to nearest, ties to even */
+    if (r > 127.0) r = 127.0;
+    if (r < -127.0) r = -127.0;
+    codes[i] = (int8_t)r;
+  }
+  return scale;
+}
+
 static double load_elem(const void* base, int64_t idx, int dtype) {
   switch (dtype) {
     case ORACLE_F32: return (double)((const float*)base)[idx];
@@ -206,13 +240,15 @@ int oracle_append(const void* k, const void* v, const int64_t* slot_mapping, int
   return ORACLE_OK;
 }
 
-/* Append into an FP8 pool: each (token, kv head) row of k / v (fp16 / bf16 /
- * fp32, `dtype`) is quantised on its own (see the reading at the top) and its
- * codes and scale written to the slot; negative slots are skipped. */
-int oracle_append_fp8(const void* k, const void* v, int32_t dtype, const int64_t* slot_mapping,
-                      int64_t num_tokens, uint8_t* k_codes, uint8_t* v_codes, float* k_scale,
-                      float* v_scale, int64_t num_blocks, int32_t num_kv_heads,
-                      int32_t block_size, int32_t head_dim) {
+/* Append into a quantised pool (kind ORACLE_FP8 or ORACLE_I8): each (token,
+ * kv head) row of k / v (fp16 / bf16 / fp32, `dtype`) is quantised on its own
+ * (see the readings at the top) and its codes and scale written to the slot;
+ * negative slots are skipped. */
+static int append_quantised(const void* k, const void* v, int32_t dtype,
+                            const int64_t* slot_mapping, int64_t num_tokens, uint8_t* k_codes,
+                            uint8_t* v_codes, float* k_scale, float* v_scale, int64_t num_blocks,
+                            int32_t num_kv_heads, int32_t block_size, int32_t head_dim,
+                            int kind) {
   if (!k || !v || !slot_mapping || !k_codes || !v_codes || !k_scale || !v_scale)
     return ORACLE_ERR_ARG;
   float* row = (float*)malloc((size_t)head_dim * sizeof(float));
@@ -233,13 +269,31 @@ int oracle_append_fp8(const void* k, const void* v, int32_t dtype, const int64_t
         const void* x = pass ? v : k;
         for (int32_t d = 0; d < head_dim; ++d) row[d] = (float)load_elem(x, src + d, dtype);
         uint8_t* codes = (pass ? v_codes : k_codes) + dst_row * head_dim;
-        float sc = oracle_quantize_row(row, head_dim, codes);
+        float sc = kind == ORACLE_I8 ? oracle_quantize_row_int8(row, head_dim, (int8_t*)codes)
+                                     : oracle_quantize_row(row, head_dim, codes);
         (pass ? v_scale : k_scale)[dst_row] = sc;
       }
     }
   }
   free(row);
   return rc;
+}
+
+int oracle_append_fp8(const void* k, const void* v, int32_t dtype, const int64_t* slot_mapping,
+                      int64_t num_tokens, uint8_t* k_codes, uint8_t* v_codes, float* k_scale,
+                      float* v_scale, int64_t num_blocks, int32_t num_kv_heads,
+                      int32_t block_size, int32_t head_dim) {
+  return append_quantised(k, v, dtype, slot_mapping, num_tokens, k_codes, v_codes, k_scale,
+                          v_scale, num_blocks, num_kv_heads, block_size, head_dim, ORACLE_FP8);
+}
+
+int oracle_append_int8(const void* k, const void* v, int32_t dtype, const int64_t* slot_mapping,
+                       int64_t num_tokens, int8_t* k_codes, int8_t* v_codes, float* k_scale,
+                       float* v_scale, int64_t num_blocks, int32_t num_kv_heads,
+                       int32_t block_size, int32_t head_dim) {
+  return append_quantised(k, v, dtype, slot_mapping, num_tokens, (uint8_t*)k_codes,
+                          (uint8_t*)v_codes, k_scale, v_scale, num_blocks, num_kv_heads,
+                          block_size, head_dim, ORACLE_I8);
 }
 
 /* ---- attention over a contiguous cache ([P2] Step 4, [P3] Step 3) -------- */
@@ -281,7 +335,7 @@ typedef struct {
   int32_t num_seqs, num_q_heads;
   const void* k_cache;
   const void* v_cache;
-  const float* k_scale; /* FP8 pools: per-row scales, else NULL */
+  const float* k_scale; /* FP8 / INT8 pools: per-row scales, else NULL */
   const float* v_scale;
   int64_t num_blocks;
   int32_t num_kv_heads, block_size, head_dim, dtype, kv_dtype;
@@ -341,12 +395,20 @@ static int decode_one(const decode_problem* p, int32_t b, int32_t h, double* out
     }
     int64_t prow = (physical * p->num_kv_heads + hk) * p->block_size + row;
     int64_t base = prow * D;
-    if (p->kv_dtype == ORACLE_FP8) {
+    if (p->kv_dtype == ORACLE_FP8 || p->kv_dtype == ORACLE_I8) {
       /* stored value = code * scale of its row */
       double ks = (double)p->k_scale[prow], vs = (double)p->v_scale[prow];
       for (int32_t d = 0; d < D; ++d) {
-        K[i * D + d] = oracle_e4m3_to_double(((const uint8_t*)p->k_cache)[base + d]) * ks;
-        V[i * D + d] = oracle_e4m3_to_double(((const uint8_t*)p->v_cache)[base + d]) * vs;
+        double kc, vc;
+        if (p->kv_dtype == ORACLE_FP8) {
+          kc = oracle_e4m3_to_double(((const uint8_t*)p->k_cache)[base + d]);
+          vc = oracle_e4m3_to_double(((const uint8_t*)p->v_cache)[base + d]);
+        } else {
+          kc = (double)((const int8_t*)p->k_cache)[base + d];
+          vc = (double)((const int8_t*)p->v_cache)[base + d];
+        }
+        K[i * D + d] = kc * ks;
+        V[i * D + d] = vc * vs;
       }
     } else {
       for (int32_t d = 0; d < D; ++d) {
@@ -411,6 +473,26 @@ int oracle_decode_fp8(const void* q, int32_t q_dtype, int32_t num_seqs, int32_t 
     return ORACLE_ERR_ARG;
   decode_problem p = {q, num_seqs, num_q_heads, k_codes, v_codes, k_scale, v_scale, num_blocks,
                       num_kv_heads, block_size, head_dim, q_dtype, ORACLE_FP8, block_tables,
+                      max_blocks, context_lens, window, num_sinks, scale};
+  return decode_pairs(&p, pairs, n_pairs, out, num_threads);
+}
+
+/* Decode over INT8 pools: as oracle_decode_fp8 with int8 codes. */
+int oracle_decode_int8(const void* q, int32_t q_dtype, int32_t num_seqs, int32_t num_q_heads,
+                       const int8_t* k_codes, const int8_t* v_codes, const float* k_scale,
+                       const float* v_scale, int64_t num_blocks, int32_t num_kv_heads,
+                       int32_t block_size, int32_t head_dim, const int32_t* block_tables,
+                       int32_t max_blocks, const int32_t* context_lens, int32_t window,
+                       int32_t num_sinks, double scale, const int32_t* pairs, int64_t n_pairs,
+                       double* out, int32_t num_threads) {
+  if (!q || !k_codes || !v_codes || !k_scale || !v_scale || !block_tables || !context_lens ||
+      !out)
+    return ORACLE_ERR_ARG;
+  if (num_seqs < 0 || num_q_heads <= 0 || num_kv_heads <= 0 || head_dim <= 0 || block_size <= 0 ||
+      max_blocks < 0 || num_q_heads % num_kv_heads != 0 || q_dtype < 0 || q_dtype > 2)
+    return ORACLE_ERR_ARG;
+  decode_problem p = {q, num_seqs, num_q_heads, k_codes, v_codes, k_scale, v_scale, num_blocks,
+                      num_kv_heads, block_size, head_dim, q_dtype, ORACLE_I8, block_tables,
                       max_blocks, context_lens, window, num_sinks, scale};
   return decode_pairs(&p, pairs, n_pairs, out, num_threads);
 }

@@ -9,8 +9,10 @@ count or ignored sinks, swapped K and V, wrong row/block or head-major
 indexing, a squared scale, wrong element decoding, a wrong slot, a wrong
 append destination, the wrong query head, a non-zero empty context, and in the
 FP8 cache a wrong exponent bias, ties broken to odd, a dropped sign, a wrong
-quantisation constant, or an ignored row scale, and in the prefill a query
-position off by one or a missing causal limit.
+quantisation constant, or an ignored row scale, in the INT8 cache a wrong
+scale constant, truncation or ties away from zero instead of ties to even, or
+codes read as unsigned, and in the prefill a query position off by one or a
+missing causal limit.
 """
 import os
 import shutil
@@ -56,6 +58,13 @@ MUTANTS = {
     "fp8_scale_constant": ("volatile float num = 448.0f;", "volatile float num = 480.0f;"),
     "fp8_scale_ignored": ("double ks = (double)p->k_scale[prow], vs = (double)p->v_scale[prow];",
                           "double ks = 1.0, vs = (double)p->v_scale[prow];"),
+    "int8_scale_constant": ("volatile float top = 127.0f;", "volatile float top = 128.0f;"),
+    "int8_round_truncates": ("double r = nearbyint((double)prod);",
+                             "double r = trunc((double)prod);"),
+    "int8_ties_away_from_zero": ("double r = nearbyint((double)prod);",
+                                 "double r = round((double)prod);"),
+    "int8_codes_unsigned": ("kc = (double)((const int8_t*)p->k_cache)[base + d];",
+                            "kc = (double)((const uint8_t*)p->k_cache)[base + d];"),
     "prefill_position_off_by_one": (
         "const int64_t p = context_lens[b] - n + (t - cu_q[b]); /* its position */",
         "const int64_t p = context_lens[b] - n + (t - cu_q[b]) + 1; /* its position */"),
@@ -81,6 +90,7 @@ def test_pins_catch_planted_mistake(name, tmp_path, oracle_lib):
                                                   "test_gpu*", "test_zz*"))
     r = subprocess.run([sys.executable, "-m", "pytest", "-q", "-x", "-p", "no:cacheprovider",
                         "tests/test_oracle.py", "tests/test_oracle_fp8.py",
-                        "tests/test_oracle_prefill.py"], cwd=tmp_path,
+                        "tests/test_oracle_int8.py", "tests/test_oracle_prefill.py"],
+                       cwd=tmp_path,
                        capture_output=True, text=True, timeout=600)
     assert r.returncode == 1, f"pins did not catch '{name}':\n{r.stdout[-2000:]}"
