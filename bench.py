@@ -65,7 +65,8 @@ def step_bytes(w):
     """Algorithmic bytes of one step of workload `w` at each of its steps."""
     spec = w.spec
     e = torch.tensor([], dtype=spec.dtype).element_size()   # q / out / new tokens
-    row = d_row = spec.head_dim * (1 if spec.kv_fp8 else e) + (4 if spec.kv_fp8 else 0)
+    q8 = spec.kv_fp8 or spec.kv_int8
+    row = d_row = spec.head_dim * (1 if q8 else e) + (4 if q8 else 0)
     B, hq, hkv, d, bs = (spec.num_seqs, spec.num_q_heads, spec.num_kv_heads, spec.head_dim,
                          spec.block_size)
     out = []
@@ -192,9 +193,10 @@ class OracleSampler:
         flat = rng.choice(total, size=min(n_pairs, total), replace=False)
         pairs = np.stack([flat // spec.num_q_heads, flat % spec.num_q_heads], 1).astype(np.int32)
         t0 = time.perf_counter()
-        if spec.kv_fp8:
-            self.oracle.decode_fp8(self.q, self.kc, self.vc, self.ks, self.vs, self.bt, self.lens,
-                                   spec.window, self.w.scale, pairs=pairs, threads=self.threads)
+        if spec.kv_fp8 or spec.kv_int8:
+            decode = self.oracle.decode_fp8 if spec.kv_fp8 else self.oracle.decode_int8
+            decode(self.q, self.kc, self.vc, self.ks, self.vs, self.bt, self.lens, spec.window,
+                   self.w.scale, pairs=pairs, threads=self.threads)
         else:
             self.oracle.decode(self.q, self.kc, self.vc, self.bt, self.lens, spec.window,
                                self.w.scale, pairs=pairs, threads=self.threads)
@@ -202,7 +204,7 @@ class OracleSampler:
         L = self.lens[pairs[:, 0]].astype(np.int64)
         lo = np.maximum(L - spec.window, 0) if spec.window > 0 else 0
         G = spec.num_q_heads // spec.num_kv_heads
-        row = spec.head_dim + 4 if spec.kv_fp8 else spec.head_dim * self.e
+        row = spec.head_dim + 4 if (spec.kv_fp8 or spec.kv_int8) else spec.head_dim * self.e
         kvb = float(((L - lo) * 2 * row).sum()) / G
         return kvb / dt, dt, len(pairs)
 
@@ -395,15 +397,17 @@ def main(argv=None):
     plan = pkv.pkv_decode_plan(spec.num_seqs, spec.num_q_heads, pkv.cache_layout(w.k_cache),
                                w.max_blocks, spec.window)
     # FP8 pools append through the quantising kernel (no fused form)
-    fused = args.path == "fused" and not spec.kv_fp8
+    q8 = spec.kv_fp8 or spec.kv_int8
+    fused = args.path == "fused" and not q8
     launches_per_step = (1 if fused else 2) + (1 if plan[1] > 1 else 0)
 
     def do_append(i):
         if fused:
             return
-        if spec.kv_fp8:
-            pkv.pkv_append_fp8(w.k_steps[i], w.v_steps[i], slots[i], w.k_cache, w.v_cache,
-                               w.k_scale, w.v_scale)
+        if q8:
+            append = pkv.pkv_append_fp8 if spec.kv_fp8 else pkv.pkv_append_int8
+            append(w.k_steps[i], w.v_steps[i], slots[i], w.k_cache, w.v_cache, w.k_scale,
+                   w.v_scale)
         else:
             pkv.pkv_append(w.k_steps[i], w.v_steps[i], slots[i], w.k_cache, w.v_cache)
 
@@ -523,7 +527,8 @@ def main(argv=None):
             "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-            "dtype": "e4m3+f16" if spec.kv_fp8 else DTYPE_NAME[spec.dtype], "data": "synthetic",
+            "dtype": ("e4m3+f16" if spec.kv_fp8 else "i8+f16" if spec.kv_int8
+                      else DTYPE_NAME[spec.dtype]), "data": "synthetic",
             "config": {
                 "workload": args.workload + ("" if not over else "-reduced"),
                 "num_seqs": spec.num_seqs,
@@ -568,7 +573,7 @@ def run_e2e(pkv, w, spec, args, sbytes, pg, world):
     S = w.steps
     step = pkv.DecodeStep(w.k_cache, w.v_cache, spec.num_seqs, spec.num_q_heads, w.max_blocks,
                           spec.window, w.scale, copy_block_tables=True, num_buffers=S,
-                          fused=args.path == "fused" and not spec.kv_fp8,
+                          fused=args.path == "fused" and not (spec.kv_fp8 or spec.kv_int8),
                           k_scale=w.k_scale, v_scale=w.v_scale)
     for s in range(S):
         h = step.host[s]

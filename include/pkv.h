@@ -47,8 +47,10 @@ typedef enum pkv_dtype {
   PKV_FLOAT32 = 0,
   PKV_FLOAT16 = 1,
   PKV_BFLOAT16 = 2,
-  PKV_FP8_E4M3 = 3  /* pools only: E4M3 codes + one float32 scale per (token, kv head)
+  PKV_FP8_E4M3 = 3, /* pools only: E4M3 codes + one float32 scale per (token, kv head)
                        row; see pkv_append_fp8.  q, out, k_new, v_new are then fp16. */
+  PKV_INT8 = 4      /* pools only: int8 codes + one float32 scale per row; see
+                       pkv_append_int8.  q and out are then fp16. */
 } pkv_dtype;
 
 typedef enum pkv_status {
@@ -184,7 +186,7 @@ typedef struct pkv_decode_options {
   int32_t tokens_per_split; /* a multiple of 16 up to 2048, or 0 for the library plan */
   const void* k_new;        /* both non-NULL: fused append of position L-1, as in    */
   const void* v_new;        /* pkv_append_decode; both NULL: decode only             */
-  const float* k_scale;     /* FP8 pools: [NB][Hkv][bs] row scales, 16-byte aligned;  */
+  const float* k_scale;     /* 8-bit pools: [NB][Hkv][bs] row scales, 16-byte aligned; */
   const float* v_scale;     /* NULL otherwise                                         */
 } pkv_decode_options;
 
@@ -237,6 +239,22 @@ int pkv_append_fp8(const void* k, const void* v, int32_t in_dtype, const int64_t
                    float* v_scale, const pkv_cache_layout* layout, void* stream);
 
 /*
+ * pkv_append_int8 -- quantise each new token's K and V rows into INT8 pools.
+ *   (Same passage as pkv_append_fp8: INT8 or FP8 quantisation of the cached
+ *   keys and values.)
+ *   Arguments as pkv_append_fp8, with int8 code pools (layout->dtype ==
+ *   PKV_INT8).  Each (token, kv head) row is quantised on its own: scale =
+ *   absmax / 127, code_d = x_d * (127 / absmax) rounded to the nearest
+ *   integer, ties to even, clamped to [-127, 127] (-128 is never written; a
+ *   NaN product gives 0); an all-zero row gets scale 1.  The stored value is
+ *   code * scale; single IEEE float32 division and product, so the codes are
+ *   exactly reproducible.  head_dim 64 or 128 (decode: 128).
+ */
+int pkv_append_int8(const void* k, const void* v, int32_t in_dtype, const int64_t* slot_mapping,
+                    int64_t num_tokens, void* k_cache, void* v_cache, float* k_scale,
+                    float* v_scale, const pkv_cache_layout* layout, void* stream);
+
+/*
  * pkv_decode_ex -- pkv_decode with every option.
  *   ("Building a Streaming Sliding-Window Attention Engine in Pure Python",
  *   Step 3 for the window and the StreamingLLM item of its "Extending" list
@@ -245,9 +263,10 @@ int pkv_append_fp8(const void* k, const void* v, int32_t in_dtype, const int64_t
  *   positions [0, min(s, lo)) and [lo, L), lo = max(0, L - w).  The other
  *   arguments, the errors and the workspace are those of pkv_decode; k_cache
  *   and v_cache are written only with the fused append.
- *   FP8 pools (layout->dtype == PKV_FP8_E4M3, head_dim 128): the attended
- *   values are code * row scale; q and out are fp16; k_scale and v_scale are
- *   required; the fused append is not available for them (PKV_ERR_UNSUPPORTED).
+ *   8-bit pools (layout->dtype == PKV_FP8_E4M3 or PKV_INT8, head_dim 128):
+ *   the attended values are code * row scale; q and out are fp16; k_scale and
+ *   v_scale are required; the fused append is not available for them
+ *   (PKV_ERR_UNSUPPORTED).
  */
 int pkv_decode_ex(const void* q, int32_t num_seqs, int32_t num_q_heads, void* k_cache,
                   void* v_cache, const pkv_cache_layout* layout, const int32_t* block_tables,
@@ -281,6 +300,8 @@ int pkv_decode_plan(int32_t num_seqs, int32_t num_q_heads, const pkv_cache_layou
  *   Limit: B * Hq * num_splits * (head_dim * 4 + 8) bytes must fit in the
  *   buffer (num_splits from pkv_decode_plan; a problem that needs no split
  *   uses no scratch); otherwise PKV_ERR_SCRATCH and nothing is launched.
+ *   8-bit pools (FP8, INT8) need row scales this call does not take:
+ *   PKV_ERR_UNSUPPORTED.
  *   Set-up: the first call on each device looks up the buffer's device address
  *   (cudaGetSymbolAddress) with that device current; make that first call
  *   before any stream capture.

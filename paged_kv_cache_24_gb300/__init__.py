@@ -12,8 +12,8 @@ Public API (thin wrappers over the C ABI of ``libpkv.so``, see include/pkv.h):
 * ``pkv_append_decode(q, k_new, v_new, k_cache, v_cache, block_tables,
   context_lens, window, scale)`` -- both in one launch;
 * ``pkv_append_fp8(k, v, slot_mapping, k_codes, v_codes, k_scale, v_scale)``
-  -- quantising append into FP8 E4M3 pools, which ``pkv_decode`` reads when
-  given the row scales;
+  and ``pkv_append_int8(...)`` -- quantising append into FP8 E4M3 (uint8) or
+  INT8 (int8) pools, which ``pkv_decode`` reads when given the row scales;
 * ``pkv_prefill(q, k, v, cu_q, k_cache, v_cache, block_tables, context_lens,
   window, scale, max_chunk)`` -- chunked prefill: append packed chunks and
   compute their causal (windowed) attention over the paged cache.
@@ -26,13 +26,13 @@ All tensors live on the GPU; PyTorch provides the memory and the stream.
 benchmark.
 """
 from ._binding import (CacheLayout, DecodeOptions, PkvError, cache_layout, library_path, load_library,
-                       pkv_append, pkv_append_decode, pkv_append_fp8, pkv_decode, pkv_prefill, pkv_decode_plan, pkv_release_workspaces,
+                       pkv_append, pkv_append_decode, pkv_append_fp8, pkv_append_int8, pkv_decode, pkv_prefill, pkv_decode_plan, pkv_release_workspaces,
                        pkv_slot_mapping, status_string)
 from .step import DecodeStep
 
 __all__ = [
     "DecodeStep", "DecodeOptions", "CacheLayout", "PkvError", "cache_layout", "library_path", "load_library", "pkv_append",
-    "pkv_append_decode", "pkv_append_fp8", "pkv_prefill",
+    "pkv_append_decode", "pkv_append_fp8", "pkv_append_int8", "pkv_prefill",
     "pkv_decode", "pkv_decode_plan", "pkv_release_workspaces", "pkv_slot_mapping",
     "status_string",
 ]

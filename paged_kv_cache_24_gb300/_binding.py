@@ -17,8 +17,11 @@ from . import _build
 
 PKV_OK = 0
 PKV_FP8_E4M3 = 3
+PKV_INT8 = 4
 _DTYPES = {torch.float32: 0, torch.float16: 1, torch.bfloat16: 2}
-_POOL_DTYPES = {**_DTYPES, torch.uint8: PKV_FP8_E4M3}  # uint8 pools hold E4M3 codes
+# 8-bit pools: uint8 tensors hold E4M3 codes, int8 tensors int8 codes
+_POOL_DTYPES = {**_DTYPES, torch.uint8: PKV_FP8_E4M3, torch.int8: PKV_INT8}
+_CODE_DTYPES = (torch.uint8, torch.int8)
 
 
 class PkvError(RuntimeError):
@@ -76,6 +79,7 @@ def load_library():
             "pkv_decode_ex": [vp, i32, i32, vp, vp, lay, vp, i32, vp, f32, vp,
                               ctypes.POINTER(DecodeOptions), vp],
             "pkv_append_fp8": [vp, vp, i32, vp, i64, vp, vp, vp, vp, lay, vp],
+            "pkv_append_int8": [vp, vp, i32, vp, i64, vp, vp, vp, vp, lay, vp],
             "pkv_prefill": [vp, vp, vp, vp, i32, i32, i32, vp, vp, lay, vp, i32, vp, i32, f32,
                             vp, vp],
             "pkv_decode_plan": [i32, i32, lay, i32, i32, i32, i32, i32, ctypes.POINTER(i32),
@@ -114,7 +118,7 @@ def _stream(stream) -> int:
 
 def cache_layout(cache: torch.Tensor) -> CacheLayout:
     """Layout of a head-major pool tensor [num_blocks, num_kv_heads, block_size, head_dim]
-    (a uint8 pool holds FP8 E4M3 codes)."""
+    (a uint8 pool holds FP8 E4M3 codes, an int8 pool int8 codes)."""
     if cache.dim() != 4:
         raise ValueError("cache must be [num_blocks, num_kv_heads, block_size, head_dim]")
     if cache.dtype not in _POOL_DTYPES:
@@ -126,19 +130,19 @@ def cache_layout(cache: torch.Tensor) -> CacheLayout:
 
 
 def _compute_dtype(cache: torch.Tensor):
-    """dtype of q / out / new tokens for a pool (fp16 for FP8 pools)."""
-    return torch.float16 if cache.dtype == torch.uint8 else cache.dtype
+    """dtype of q / out / new tokens for a pool (fp16 for 8-bit pools)."""
+    return torch.float16 if cache.dtype in _CODE_DTYPES else cache.dtype
 
 
 def _check_scales(k_cache, k_scale, v_scale):
-    if k_cache.dtype != torch.uint8:
-        _require(k_scale is None and v_scale is None, "scales are only for FP8 (uint8) pools")
+    if k_cache.dtype not in _CODE_DTYPES:
+        _require(k_scale is None and v_scale is None, "scales are only for 8-bit pools")
         return
     shape = tuple(k_cache.shape[:3])
     for sc in (k_scale, v_scale):
         _require(sc is not None and sc.dtype == torch.float32 and tuple(sc.shape) == shape
                  and sc.is_contiguous() and sc.device.type == "cuda",
-                 f"FP8 pools need contiguous float32 scales of shape {shape}")
+                 f"8-bit pools need contiguous float32 scales of shape {shape}")
 
 
 def _require(cond: bool, msg: str) -> None:
@@ -193,8 +197,8 @@ def pkv_decode(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
                stream=None, num_sinks: int = 0, k_scale: torch.Tensor | None = None,
                v_scale: torch.Tensor | None = None) -> torch.Tensor:
     """Decode attention of q [B, Hq, D] over the paged context; returns out [B, Hq, D].
-    With a window, ``num_sinks`` first positions are attended as well.  FP8 pools
-    (uint8 codes) take their row scales and fp16 q."""
+    With a window, ``num_sinks`` first positions are attended as well.  8-bit pools
+    (uint8 E4M3 or int8 codes) take their row scales and fp16 q."""
     _on_cuda(q, k_cache, v_cache, block_tables, context_lens, out, k_scale, v_scale)
     layout = cache_layout(k_cache)
     _require(v_cache.shape == k_cache.shape and v_cache.dtype == k_cache.dtype
@@ -222,15 +226,12 @@ def pkv_decode(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
     return out
 
 
-def pkv_append_fp8(k: torch.Tensor, v: torch.Tensor, slot_mapping: torch.Tensor,
-                   k_cache: torch.Tensor, v_cache: torch.Tensor, k_scale: torch.Tensor,
-                   v_scale: torch.Tensor, stream=None) -> None:
-    """Quantise k[i], v[i] ([T, Hkv, D], fp32/fp16/bf16) into the FP8 pools (uint8
-    codes [NB, Hkv, bs, D], float32 row scales [NB, Hkv, bs]) at slot_mapping[i]."""
+def _append_q8(fn: str, code_dtype, k, v, slot_mapping, k_cache, v_cache, k_scale, v_scale,
+               stream) -> None:
     _on_cuda(k, v, slot_mapping, k_cache, v_cache, k_scale, v_scale)
     layout = cache_layout(k_cache)
-    _require(k_cache.dtype == torch.uint8, "pkv_append_fp8 writes uint8 (E4M3) pools")
-    _require(v_cache.shape == k_cache.shape and v_cache.dtype == torch.uint8
+    _require(k_cache.dtype == code_dtype, f"{fn} writes {code_dtype} pools")
+    _require(v_cache.shape == k_cache.shape and v_cache.dtype == code_dtype
              and v_cache.is_contiguous(), "v_cache must match k_cache")
     _check_scales(k_cache, k_scale, v_scale)
     T = k.shape[0]
@@ -240,9 +241,27 @@ def pkv_append_fp8(k: torch.Tensor, v: torch.Tensor, slot_mapping: torch.Tensor,
              f"k and v must be contiguous {shape} fp32/fp16/bf16")
     _require(slot_mapping.dtype == torch.int64 and slot_mapping.numel() == T
              and slot_mapping.is_contiguous(), "slot_mapping must be int64 [T]")
-    _check("pkv_append_fp8", load_library().pkv_append_fp8(
+    _check(fn, getattr(load_library(), fn)(
         _ptr(k), _ptr(v), _DTYPES[k.dtype], _ptr(slot_mapping), T, _ptr(k_cache), _ptr(v_cache),
         _ptr(k_scale), _ptr(v_scale), ctypes.byref(layout), _stream(stream)))
+
+
+def pkv_append_fp8(k: torch.Tensor, v: torch.Tensor, slot_mapping: torch.Tensor,
+                   k_cache: torch.Tensor, v_cache: torch.Tensor, k_scale: torch.Tensor,
+                   v_scale: torch.Tensor, stream=None) -> None:
+    """Quantise k[i], v[i] ([T, Hkv, D], fp32/fp16/bf16) into the FP8 pools (uint8
+    codes [NB, Hkv, bs, D], float32 row scales [NB, Hkv, bs]) at slot_mapping[i]."""
+    _append_q8("pkv_append_fp8", torch.uint8, k, v, slot_mapping, k_cache, v_cache, k_scale,
+               v_scale, stream)
+
+
+def pkv_append_int8(k: torch.Tensor, v: torch.Tensor, slot_mapping: torch.Tensor,
+                    k_cache: torch.Tensor, v_cache: torch.Tensor, k_scale: torch.Tensor,
+                    v_scale: torch.Tensor, stream=None) -> None:
+    """Quantise k[i], v[i] ([T, Hkv, D], fp32/fp16/bf16) into the INT8 pools (int8
+    codes [NB, Hkv, bs, D], float32 row scales [NB, Hkv, bs]) at slot_mapping[i]."""
+    _append_q8("pkv_append_int8", torch.int8, k, v, slot_mapping, k_cache, v_cache, k_scale,
+               v_scale, stream)
 
 
 def pkv_prefill(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, cu_q: torch.Tensor,

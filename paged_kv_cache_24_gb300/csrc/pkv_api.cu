@@ -20,19 +20,20 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 bool aligned4(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0; }
 
 int elem_bytes(int dtype) {
-  return dtype == PKV_FLOAT32 ? 4 : (dtype == PKV_FP8_E4M3 ? 1 : 2);
+  return dtype == PKV_FLOAT32 ? 4 : ((dtype == PKV_FP8_E4M3 || dtype == PKV_INT8) ? 1 : 2);
 }
 
 // Layout checks.  `for_decode` adds the tile constraints of the decode kernels.
 int check_layout(const pkv_cache_layout* L, bool for_decode) {
   if (!L) return PKV_ERR_NULL;
-  if (L->dtype < PKV_FLOAT32 || L->dtype > PKV_FP8_E4M3) return PKV_ERR_DTYPE;
+  if (L->dtype < PKV_FLOAT32 || L->dtype > PKV_INT8) return PKV_ERR_DTYPE;
   if (L->num_blocks < 0 || L->num_kv_heads <= 0 || L->block_size <= 0 || L->head_dim <= 0)
     return PKV_ERR_SHAPE;
   if ((L->head_dim * elem_bytes(L->dtype)) % 16 != 0) return PKV_ERR_UNSUPPORTED;
   if (for_decode) {
     if (L->head_dim != 64 && L->head_dim != 128) return PKV_ERR_UNSUPPORTED;
-    if (L->dtype == PKV_FP8_E4M3 && L->head_dim != 128) return PKV_ERR_UNSUPPORTED;
+    if ((L->dtype == PKV_FP8_E4M3 || L->dtype == PKV_INT8) && L->head_dim != 128)
+      return PKV_ERR_UNSUPPORTED;
     if (L->block_size % pkv::kUnitTokens != 0 || L->block_size > 256) return PKV_ERR_UNSUPPORTED;
     // TMA row coordinates are 32-bit
     if (L->num_blocks * L->num_kv_heads * static_cast<int64_t>(L->block_size) > 0x7fffffffLL)
@@ -106,7 +107,7 @@ int encode_pool_map(CUtensorMap* map, const void* pool, const pkv_cache_layout* 
   cuuint32_t estr[2] = {1, 1};
   CUtensorMapDataType dt =
       L->dtype == PKV_FLOAT16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
-  if (L->dtype == PKV_FP8_E4M3) {
+  if (L->dtype == PKV_FP8_E4M3 || L->dtype == PKV_INT8) {
     // code pools: one 128-byte box row per token row (head_dim 128)
     dt = CU_TENSOR_MAP_DATA_TYPE_UINT8;
     strides[0] = static_cast<cuuint64_t>(L->head_dim);
@@ -210,8 +211,8 @@ int decode_impl(const void* q, const void* k_new, const void* v_new, int32_t num
   if (tokens_per_split < 0 || tokens_per_split % pkv::kUnitTokens != 0) return PKV_ERR_SHAPE;
   if (num_sinks < 0) return PKV_ERR_SHAPE;
   if (tokens_per_split > 32 * pkv::kDecodeWarps * pkv::kUnitTokens) return PKV_ERR_UNSUPPORTED;
-  const bool fp8 = layout->dtype == PKV_FP8_E4M3;
-  if (fp8 && num_seqs > 0) {
+  const bool q8 = layout->dtype == PKV_FP8_E4M3 || layout->dtype == PKV_INT8;
+  if (q8 && num_seqs > 0) {
     if (!k_scale || !v_scale) return PKV_ERR_NULL;
     if (!aligned16(k_scale) || !aligned16(v_scale)) return PKV_ERR_ALIGNMENT;
     if (k_new) return PKV_ERR_UNSUPPORTED;
@@ -273,14 +274,14 @@ int decode_impl(const void* q, const void* k_new, const void* v_new, int32_t num
     if (rc != PKV_OK) return rc;
     rc = encode_pool_map(&vmap, v_cache, layout);
     if (rc != PKV_OK) return rc;
-    e = fp8 ? pkv::launch_decode_fp8(plan.ntiles, kmap, vmap, p, st)
+    e = q8 ? pkv::launch_decode_q8(layout->dtype == PKV_INT8, plan.ntiles, kmap, vmap, p, st)
             : pkv::launch_decode_16bit(layout->dtype, layout->head_dim, plan.ntiles, kmap, vmap,
                                        p, st);
   }
   if (e != cudaSuccess) return to_status(e);
   if (plan.num_splits > 1) {
-    // FP8 pools decode into fp16 outputs
-    e = pkv::launch_combine(fp8 ? PKV_FLOAT16 : layout->dtype, layout->head_dim, p, st);
+    // 8-bit pools decode into fp16 outputs
+    e = pkv::launch_combine(q8 ? PKV_FLOAT16 : layout->dtype, layout->head_dim, p, st);
     if (e != cudaSuccess) return to_status(e);
   }
   return PKV_OK;
@@ -316,6 +317,31 @@ int pool_tensor_map(CUtensorMap* map, const void* pool, const pkv_cache_layout* 
 }
 int status_of(cudaError_t e) { return to_status(e); }
 }  // namespace pkv
+
+// Quantising append into an 8-bit pool (E4M3 or int8 codes).
+static int append_q8(bool int8, const void* k, const void* v, int32_t in_dtype,
+                     const int64_t* slot_mapping, int64_t num_tokens, void* k_cache,
+                     void* v_cache, float* k_scale, float* v_scale,
+                     const pkv_cache_layout* layout, void* stream) {
+  int rc = check_layout(layout, false);
+  if (rc != PKV_OK) return rc;
+  if (layout->dtype != (int8 ? PKV_INT8 : PKV_FP8_E4M3)) return PKV_ERR_DTYPE;
+  if (in_dtype < PKV_FLOAT32 || in_dtype > PKV_BFLOAT16) return PKV_ERR_DTYPE;
+  if (layout->head_dim != 64 && layout->head_dim != 128) return PKV_ERR_UNSUPPORTED;
+  if (num_tokens < 0) return PKV_ERR_SHAPE;
+  if (num_tokens == 0) return PKV_OK;
+  if (!k || !v || !slot_mapping || !k_cache || !v_cache || !k_scale || !v_scale)
+    return PKV_ERR_NULL;
+  if (!aligned16(k) || !aligned16(v) || !aligned16(k_cache) || !aligned16(v_cache) ||
+      !aligned4(k_scale) || !aligned4(v_scale) ||
+      (reinterpret_cast<uintptr_t>(slot_mapping) & 7u))
+    return PKV_ERR_ALIGNMENT;
+  return to_status(pkv::launch_append_q8(int8, in_dtype, k, v, slot_mapping, num_tokens, k_cache,
+                                         v_cache, k_scale, v_scale, layout->num_blocks,
+                                         layout->num_kv_heads, layout->block_size,
+                                         layout->head_dim, static_cast<cudaStream_t>(stream)));
+}
+
 
 extern "C" {
 
@@ -445,23 +471,15 @@ int pkv_prefill(const void* q, const void* k, const void* v, const int32_t* cu_q
 int pkv_append_fp8(const void* k, const void* v, int32_t in_dtype, const int64_t* slot_mapping,
                    int64_t num_tokens, void* k_cache, void* v_cache, float* k_scale,
                    float* v_scale, const pkv_cache_layout* layout, void* stream) {
-  int rc = check_layout(layout, false);
-  if (rc != PKV_OK) return rc;
-  if (layout->dtype != PKV_FP8_E4M3) return PKV_ERR_DTYPE;
-  if (in_dtype < PKV_FLOAT32 || in_dtype > PKV_BFLOAT16) return PKV_ERR_DTYPE;
-  if (layout->head_dim != 64 && layout->head_dim != 128) return PKV_ERR_UNSUPPORTED;
-  if (num_tokens < 0) return PKV_ERR_SHAPE;
-  if (num_tokens == 0) return PKV_OK;
-  if (!k || !v || !slot_mapping || !k_cache || !v_cache || !k_scale || !v_scale)
-    return PKV_ERR_NULL;
-  if (!aligned16(k) || !aligned16(v) || !aligned16(k_cache) || !aligned16(v_cache) ||
-      !aligned4(k_scale) || !aligned4(v_scale) ||
-      (reinterpret_cast<uintptr_t>(slot_mapping) & 7u))
-    return PKV_ERR_ALIGNMENT;
-  return to_status(pkv::launch_append_fp8(in_dtype, k, v, slot_mapping, num_tokens, k_cache,
-                                          v_cache, k_scale, v_scale, layout->num_blocks,
-                                          layout->num_kv_heads, layout->block_size,
-                                          layout->head_dim, static_cast<cudaStream_t>(stream)));
+  return append_q8(false, k, v, in_dtype, slot_mapping, num_tokens, k_cache, v_cache, k_scale,
+                   v_scale, layout, stream);
+}
+
+int pkv_append_int8(const void* k, const void* v, int32_t in_dtype, const int64_t* slot_mapping,
+                    int64_t num_tokens, void* k_cache, void* v_cache, float* k_scale,
+                    float* v_scale, const pkv_cache_layout* layout, void* stream) {
+  return append_q8(true, k, v, in_dtype, slot_mapping, num_tokens, k_cache, v_cache, k_scale,
+                   v_scale, layout, stream);
 }
 
 int pkv_append_decode(const void* q, const void* k_new, const void* v_new, int32_t num_seqs,

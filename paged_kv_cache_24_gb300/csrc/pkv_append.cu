@@ -53,12 +53,15 @@ __global__ void append_kernel(const uint4* __restrict__ k, const uint4* __restri
   v_cache[dst] = vv;
 }
 
-// FP8 pools: one warp per (token, kv head) row.  The row is quantised on its
-// own -- scale = absmax / 448, codes = E4M3(x * (448 / absmax)), round to
-// nearest even, saturating; an all-zero row gets scale 1 -- with IEEE float32
-// divisions and products, so the codes are reproducible bit for bit.
-template <typename Tin, int D>
-__global__ void append_fp8_kernel(const Tin* __restrict__ k, const Tin* __restrict__ v,
+// 8-bit pools: one warp per (token, kv head) row.  The row is quantised on
+// its own; an all-zero row gets scale 1.  FP8: scale = absmax / 448, codes =
+// E4M3(x * (448 / absmax)), round to nearest even, saturating.  INT8 (I8):
+// scale = absmax / 127, codes = x * (127 / absmax) rounded to the nearest
+// integer, ties to even, clamped to [-127, 127] (a NaN product gives 0).
+// IEEE float32 divisions and products, so the codes are reproducible bit for
+// bit.
+template <typename Tin, int D, bool I8>
+__global__ void append_q8_kernel(const Tin* __restrict__ k, const Tin* __restrict__ v,
                                   const int64_t* __restrict__ slots, int64_t num_tokens,
                                   uint8_t* __restrict__ k_codes, uint8_t* __restrict__ v_codes,
                                   float* __restrict__ k_scale, float* __restrict__ v_scale,
@@ -87,15 +90,25 @@ __global__ void append_fp8_kernel(const Tin* __restrict__ k, const Tin* __restri
     }
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
+    constexpr float kTop = I8 ? 127.f : 448.f;
     float scale = 1.f, inv = 1.f;
     if (amax > 0.f) {
-      scale = __fdiv_rn(amax, 448.f);
-      inv = __fdiv_rn(448.f, amax);
+      scale = __fdiv_rn(amax, kTop);
+      inv = __fdiv_rn(kTop, amax);
     }
     uint32_t packed = 0;
+    if constexpr (I8) {
 #pragma unroll
-    for (int i = 0; i < PER; i += 2)
-      packed |= f32x2_to_e4m3x2(__fmul_rn(x[i], inv), __fmul_rn(x[i + 1], inv)) << (8 * i);
+      for (int i = 0; i < PER; ++i) {
+        const float pr = __fmul_rn(x[i], inv);
+        const int c = pr != pr ? 0 : min(max(__float2int_rn(pr), -127), 127);
+        packed |= (static_cast<uint32_t>(c) & 0xffu) << (8 * i);
+      }
+    } else {
+#pragma unroll
+      for (int i = 0; i < PER; i += 2)
+        packed |= f32x2_to_e4m3x2(__fmul_rn(x[i], inv), __fmul_rn(x[i + 1], inv)) << (8 * i);
+    }
     uint8_t* dst = (pass ? v_codes : k_codes) + dst_row * D + lane * PER;
     if constexpr (PER == 4) {
       *reinterpret_cast<uint32_t*>(dst) = packed;
@@ -108,10 +121,11 @@ __global__ void append_fp8_kernel(const Tin* __restrict__ k, const Tin* __restri
 
 }  // namespace
 
-cudaError_t launch_append_fp8(int in_dtype, const void* k, const void* v, const int64_t* slots,
-                              int64_t num_tokens, void* k_codes, void* v_codes, float* k_scale,
-                              float* v_scale, int64_t num_blocks, int num_kv_heads,
-                              int block_size, int head_dim, cudaStream_t stream) {
+cudaError_t launch_append_q8(bool int8, int in_dtype, const void* k, const void* v,
+                             const int64_t* slots, int64_t num_tokens, void* k_codes,
+                             void* v_codes, float* k_scale, float* v_scale, int64_t num_blocks,
+                             int num_kv_heads, int block_size, int head_dim,
+                             cudaStream_t stream) {
   if (num_tokens == 0) return cudaSuccess;
   const int64_t rows = num_tokens * num_kv_heads;
   const int warps = 8;
@@ -119,11 +133,12 @@ cudaError_t launch_append_fp8(int in_dtype, const void* k, const void* v, const 
   if (blocks > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
   auto* kc = static_cast<uint8_t*>(k_codes);
   auto* vc = static_cast<uint8_t*>(v_codes);
-#define PKV_APPEND8(T, D)                                                                  \
-  return launch_pdl(append_fp8_kernel<T, D>, dim3(static_cast<unsigned>(blocks)),          \
-                    dim3(warps * 32), 0, stream, static_cast<const T*>(k),                 \
-                    static_cast<const T*>(v), slots, num_tokens, kc, vc, k_scale, v_scale, \
-                    num_blocks, num_kv_heads, block_size)
+#define PKV_APPEND8_K(T, D, I8)                                                        \
+  launch_pdl(append_q8_kernel<T, D, I8>, dim3(static_cast<unsigned>(blocks)),             \
+             dim3(warps * 32), 0, stream, static_cast<const T*>(k), static_cast<const T*>(v), \
+             slots, num_tokens, kc, vc, k_scale, v_scale, num_blocks, num_kv_heads,       \
+             block_size)
+#define PKV_APPEND8(T, D) return int8 ? PKV_APPEND8_K(T, D, true) : PKV_APPEND8_K(T, D, false)
   if (in_dtype == 0) {
     if (head_dim == 128) PKV_APPEND8(float, 128);
     PKV_APPEND8(float, 64);
@@ -135,6 +150,7 @@ cudaError_t launch_append_fp8(int in_dtype, const void* k, const void* v, const 
   if (head_dim == 128) PKV_APPEND8(__nv_bfloat16, 128);
   PKV_APPEND8(__nv_bfloat16, 64);
 #undef PKV_APPEND8
+#undef PKV_APPEND8_K
 }
 
 cudaError_t launch_slot_mapping(const int32_t* block_tables, int num_seqs, int max_blocks,

@@ -155,7 +155,7 @@ __device__ void merge_and_store(const float* so, const float* sm, const float* s
 // ---------------------------------------------------------------------------
 // 16-bit pools: TMA-staged pages, tensor-core QK^T and PV.
 
-template <typename T, int D, int NT, bool KV8>
+template <typename T, int D, int NT, bool KV8, bool I8 = false>
 __global__ void __launch_bounds__(kThreads, (KV8 && NT == 1) ? 3 : 2)
 decode16_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
                 const DecodeParams p) {
@@ -354,10 +354,22 @@ decode16_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant_
         const int row = lane & 15, chunk = 2 * c + (lane >> 4);
         uint32_t r0, r1, r2, r3;
         ldmatrix_x4(kt + row * 128 + ((chunk ^ (row & 7)) << 4), r0, r1, r2, r3);
-        const uint32_t a0 = e4m3x2_to_f16x2(r0), a1 = e4m3x2_to_f16x2(r1);
-        const uint32_t a2 = e4m3x2_to_f16x2(r0 >> 16), a3 = e4m3x2_to_f16x2(r1 >> 16);
-        const uint32_t b0 = e4m3x2_to_f16x2(r2), b1 = e4m3x2_to_f16x2(r3);
-        const uint32_t b2 = e4m3x2_to_f16x2(r2 >> 16), b3 = e4m3x2_to_f16x2(r3 >> 16);
+        uint32_t a0, a1, a2, a3, b0, b1, b2, b3;
+        if constexpr (I8) {
+          r0 ^= 0x80808080u;
+          r1 ^= 0x80808080u;
+          r2 ^= 0x80808080u;
+          r3 ^= 0x80808080u;
+          a0 = s8pair_to_f16x2<0x5140>(r0), a1 = s8pair_to_f16x2<0x5140>(r1);
+          a2 = s8pair_to_f16x2<0x5342>(r0), a3 = s8pair_to_f16x2<0x5342>(r1);
+          b0 = s8pair_to_f16x2<0x5140>(r2), b1 = s8pair_to_f16x2<0x5140>(r3);
+          b2 = s8pair_to_f16x2<0x5342>(r2), b3 = s8pair_to_f16x2<0x5342>(r3);
+        } else {
+          a0 = e4m3x2_to_f16x2(r0), a1 = e4m3x2_to_f16x2(r1);
+          a2 = e4m3x2_to_f16x2(r0 >> 16), a3 = e4m3x2_to_f16x2(r1 >> 16);
+          b0 = e4m3x2_to_f16x2(r2), b1 = e4m3x2_to_f16x2(r3);
+          b2 = e4m3x2_to_f16x2(r2 >> 16), b3 = e4m3x2_to_f16x2(r3 >> 16);
+        }
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt) {
           Mma<T>::run(s[nt], a0, a1, a2, a3, qf[nt][2 * c][0], qf[nt][2 * c][1]);
@@ -473,17 +485,32 @@ decode16_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant_
         const int chunk = 2 * c + ((lane >> 3) & 1);
         uint32_t r0, r1, r2, r3;
         ldmatrix_x4_trans(vt + tok * 128 + ((chunk ^ (tok & 7)) << 4), r0, r1, r2, r3);
-        r0 = __byte_perm(r0, 0u, 0x3120);
-        r1 = __byte_perm(r1, 0u, 0x3120);
-        r2 = __byte_perm(r2, 0u, 0x3120);
-        r3 = __byte_perm(r3, 0u, 0x3120);
+        if constexpr (I8) {
+          r0 ^= 0x80808080u;
+          r1 ^= 0x80808080u;
+          r2 ^= 0x80808080u;
+          r3 ^= 0x80808080u;
+        } else {
+          r0 = __byte_perm(r0, 0u, 0x3120);
+          r1 = __byte_perm(r1, 0u, 0x3120);
+          r2 = __byte_perm(r2, 0u, 0x3120);
+          r3 = __byte_perm(r3, 0u, 0x3120);
+        }
 #pragma unroll
         for (int e = 0; e < 2; ++e) {
           const int sh = 16 * e;
-          const uint32_t a0 = e4m3x2_to_f16x2(r0 >> sh) & mlo;
-          const uint32_t a1 = e4m3x2_to_f16x2(r1 >> sh) & mlo;
-          const uint32_t a2 = e4m3x2_to_f16x2(r2 >> sh) & mhi;
-          const uint32_t a3 = e4m3x2_to_f16x2(r3 >> sh) & mhi;
+          uint32_t a0, a1, a2, a3;
+          if constexpr (I8) {  // even d: bytes 0, 2; odd d: bytes 1, 3
+            a0 = (e ? s8pair_to_f16x2<0x5341>(r0) : s8pair_to_f16x2<0x5240>(r0)) & mlo;
+            a1 = (e ? s8pair_to_f16x2<0x5341>(r1) : s8pair_to_f16x2<0x5240>(r1)) & mlo;
+            a2 = (e ? s8pair_to_f16x2<0x5341>(r2) : s8pair_to_f16x2<0x5240>(r2)) & mhi;
+            a3 = (e ? s8pair_to_f16x2<0x5341>(r3) : s8pair_to_f16x2<0x5240>(r3)) & mhi;
+          } else {
+            a0 = e4m3x2_to_f16x2(r0 >> sh) & mlo;
+            a1 = e4m3x2_to_f16x2(r1 >> sh) & mlo;
+            a2 = e4m3x2_to_f16x2(r2 >> sh) & mhi;
+            a3 = e4m3x2_to_f16x2(r3 >> sh) & mhi;
+          }
 #pragma unroll
           for (int nt = 0; nt < NT; ++nt) {
             Mma<T>::run(o[2 * c + e][nt], a0, a1, a2, a3, bh[nt][0], bh[nt][1]);
@@ -740,10 +767,10 @@ combine_kernel(const DecodeParams p) {
   for (int i = 0; i < PER; ++i) out[i] = from_f32<T>(acc[i] / lsum);
 }
 
-template <typename T, int D, int NT, bool KV8 = false>
+template <typename T, int D, int NT, bool KV8 = false, bool I8 = false>
 cudaError_t launch16(const CUtensorMap& kmap, const CUtensorMap& vmap, const DecodeParams& p,
                      cudaStream_t stream) {
-  auto kern = decode16_kernel<T, D, NT, KV8>;
+  auto kern = decode16_kernel<T, D, NT, KV8, I8>;
   const int smem = Tile16<D, KV8>::kSmemBytes;
   // the shared-memory opt-in is per device; set it once for each
   static std::atomic<uint64_t> configured{0};
@@ -766,8 +793,12 @@ size_t decode_16bit_smem_bytes(int head_dim) {
   return head_dim == 128 ? Tile16<128, false>::kSmemBytes : Tile16<64, false>::kSmemBytes;
 }
 
-cudaError_t launch_decode_fp8(int ntiles, const CUtensorMap& kmap, const CUtensorMap& vmap,
-                              const DecodeParams& p, cudaStream_t stream) {
+cudaError_t launch_decode_q8(bool int8, int ntiles, const CUtensorMap& kmap,
+                             const CUtensorMap& vmap, const DecodeParams& p, cudaStream_t stream) {
+  if (int8) {
+    if (ntiles == 1) return launch16<__half, 128, 1, true, true>(kmap, vmap, p, stream);
+    return launch16<__half, 128, 2, true, true>(kmap, vmap, p, stream);
+  }
   if (ntiles == 1) return launch16<__half, 128, 1, true>(kmap, vmap, p, stream);
   return launch16<__half, 128, 2, true>(kmap, vmap, p, stream);
 }

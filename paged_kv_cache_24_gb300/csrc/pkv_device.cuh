@@ -82,6 +82,20 @@ __device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t two_codes) {
   return d;
 }
 
+// Two int8 codes to two fp16 values, exactly.  `biased` holds four codes with
+// their sign bits flipped (code + 128, as unsigned bytes; one XOR with
+// 0x80808080 per register); the byte selector `sel` places two of them as the
+// low bytes of halves whose high byte is 0x64 (value 1024 + code + 128), and
+// 1152 is subtracted.  sel 0x5140 takes bytes 0, 1; 0x5342 bytes 2, 3;
+// 0x5240 bytes 0, 2; 0x5341 bytes 1, 3 (low half first).
+template <uint32_t kSel>
+__device__ __forceinline__ uint32_t s8pair_to_f16x2(uint32_t biased) {
+  const uint32_t h = __byte_perm(biased, 0x6464u, kSel);
+  uint32_t d;
+  asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(d) : "r"(h), "r"(0x64806480u));
+  return d;
+}
+
 // Two floats to two FP8 E4M3 codes (round to nearest even, saturating);
 // lo -> bits 0..7, hi -> bits 8..15.
 __device__ __forceinline__ uint32_t f32x2_to_e4m3x2(float lo, float hi) {

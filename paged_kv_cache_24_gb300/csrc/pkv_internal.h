@@ -120,12 +120,14 @@ cudaError_t launch_decode_16bit(int dtype, int head_dim, int ntiles, const CUten
                                 const CUtensorMap& vmap, const DecodeParams& p,
                                 cudaStream_t stream);
 // FP8 E4M3 pools (head_dim 128), fp16 q / out; kmap / vmap describe the code pools.
-cudaError_t launch_decode_fp8(int ntiles, const CUtensorMap& kmap, const CUtensorMap& vmap,
-                              const DecodeParams& p, cudaStream_t stream);
-cudaError_t launch_append_fp8(int in_dtype, const void* k, const void* v, const int64_t* slots,
-                              int64_t num_tokens, void* k_codes, void* v_codes, float* k_scale,
-                              float* v_scale, int64_t num_blocks, int num_kv_heads,
-                              int block_size, int head_dim, cudaStream_t stream);
+// 8-bit pools (E4M3 codes, or int8 codes when `int8`), head_dim 128.
+cudaError_t launch_decode_q8(bool int8, int ntiles, const CUtensorMap& kmap,
+                             const CUtensorMap& vmap, const DecodeParams& p, cudaStream_t stream);
+cudaError_t launch_append_q8(bool int8, int in_dtype, const void* k, const void* v,
+                             const int64_t* slots, int64_t num_tokens, void* k_codes,
+                             void* v_codes, float* k_scale, float* v_scale, int64_t num_blocks,
+                             int num_kv_heads, int block_size, int head_dim,
+                             cudaStream_t stream);
 cudaError_t launch_decode_f32(int head_dim, const DecodeParams& p, cudaStream_t stream);
 cudaError_t launch_combine(int dtype, int head_dim, const DecodeParams& p, cudaStream_t stream);
 cudaError_t launch_append(int elem_bytes, const void* k, const void* v, const int64_t* slots,

@@ -54,6 +54,8 @@ extern "C" int pkv_decode_noalloc(const void* q, int32_t num_seqs, int32_t num_q
   int rc = pkv::decode_checks(q, num_seqs, num_q_heads, k_cache, v_cache, layout, block_tables,
                               max_blocks_per_seq, context_lens, out);
   if (rc != PKV_OK) return rc;
+  // 8-bit pools need row scales, which this entry point does not take
+  if (layout->dtype == PKV_FP8_E4M3 || layout->dtype == PKV_INT8) return PKV_ERR_UNSUPPORTED;
   if (num_seqs == 0) return PKV_OK;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
 

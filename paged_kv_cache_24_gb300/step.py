@@ -27,6 +27,7 @@ from __future__ import annotations
 import torch
 
 from ._binding import (cache_layout, pkv_append, pkv_append_decode, pkv_append_fp8,
+                       pkv_append_int8,
                        pkv_decode, pkv_slot_mapping)
 
 _ALIGN = 256
@@ -42,13 +43,15 @@ class DecodeStep:
         self.k_cache, self.v_cache = k_cache, v_cache
         self.window, self.scale = int(window), float(scale)
         self.block_size = layout.block_size
-        self.fp8 = k_cache.dtype == torch.uint8
-        if self.fp8 and fused:
-            raise ValueError("FP8 pools append through pkv_append_fp8: use fused=False")
+        # 8-bit pools (uint8 E4M3 / int8 codes) append through the quantising call
+        self.q8 = k_cache.dtype in (torch.uint8, torch.int8)
+        if self.q8 and fused:
+            raise ValueError("8-bit pools append through pkv_append_fp8 / pkv_append_int8: "
+                             "use fused=False")
         self.k_scale, self.v_scale = k_scale, v_scale
         self.fused = fused
         dev = k_cache.device
-        dt = torch.float16 if k_cache.dtype == torch.uint8 else k_cache.dtype
+        dt = torch.float16 if self.q8 else k_cache.dtype
         B, hq, hkv, d = num_seqs, num_q_heads, layout.num_kv_heads, layout.head_dim
         shapes = {
             "q": ((B, hq, d), dt), "k": ((B, hkv, d), dt), "v": ((B, hkv, d), dt),
@@ -111,9 +114,10 @@ class DecodeStep:
         else:
             pkv_slot_mapping(dv["block_tables"], dv["positions"], self.block_size,
                              out=self.slots)
-            if self.fp8:
-                pkv_append_fp8(dv["k"], dv["v"], self.slots, self.k_cache, self.v_cache,
-                               self.k_scale, self.v_scale)
+            if self.q8:
+                append = pkv_append_int8 if self.k_cache.dtype == torch.int8 else pkv_append_fp8
+                append(dv["k"], dv["v"], self.slots, self.k_cache, self.v_cache, self.k_scale,
+                       self.v_scale)
             else:
                 pkv_append(dv["k"], dv["v"], self.slots, self.k_cache, self.v_cache)
             pkv_decode(dv["q"], self.k_cache, self.v_cache, dv["block_tables"],

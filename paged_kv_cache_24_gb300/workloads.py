@@ -89,6 +89,7 @@ class WorkloadSpec:
     window: int = 0
     num_sinks: int = 0                # with a window: first positions kept (attention sinks)
     kv_fp8: bool = False              # pools of FP8 E4M3 codes + float32 row scales
+    kv_int8: bool = False             # pools of int8 codes + float32 row scales
     steps: int = 1
     pool_factor: float = 1.2          # pool = ceil(factor * blocks needed), shuffled ids
     explicit_pool: Optional[int] = None
@@ -99,8 +100,8 @@ class WorkloadSpec:
 
 
 def config_spec(idx: int, **overrides) -> WorkloadSpec:
-    """The five benchmark workloads (index 0..4) and FP8-pool variants of the MHA
-    and GQA ones (5, 6), optionally resized for tests."""
+    """The five benchmark workloads (index 0..4) and FP8-pool (5, 6) and INT8-pool
+    (7, 8) variants of the MHA and GQA ones, optionally resized for tests."""
     table = {
         0: dict(name="tiny_fp32", dtype=torch.float32, num_seqs=4, num_q_heads=8, num_kv_heads=8,
                 head_dim=64, block_size=16, lens=[17, 33, 64, 100], lens_are_pre_append=True,
@@ -120,12 +121,15 @@ def config_spec(idx: int, **overrides) -> WorkloadSpec:
     # the MHA and GQA shapes over FP8 E4M3 pools (fp16 queries and new tokens)
     table[5] = dict(table[1], name="mha_fp8", kv_fp8=True, seed=5)
     table[6] = dict(table[2], name="gqa_fp8", dtype=torch.float16, kv_fp8=True, seed=6)
+    # the same shapes over INT8 pools
+    table[7] = dict(table[1], name="mha_int8", kv_int8=True, seed=7)
+    table[8] = dict(table[2], name="gqa_int8", dtype=torch.float16, kv_int8=True, seed=8)
     base = dict(table[idx])
     base.update(overrides)
     return WorkloadSpec(**base)
 
 
-CONFIGS = {config_spec(i).name: i for i in range(7)}
+CONFIGS = {config_spec(i).name: i for i in range(9)}
 
 
 @dataclass
@@ -275,6 +279,17 @@ def make_workload(spec: WorkloadSpec, device="cpu", poison: bool = True,
             del tmp
         k_scale = torch.rand((nb, Hkv, bs), generator=gen, device=device) * (1 / 64) + 1 / 128
         v_scale = torch.rand((nb, Hkv, bs), generator=gen, device=device) * (1 / 64) + 1 / 128
+    elif spec.kv_int8:
+        # int8 codes of N(0, 1) * 32 (rounded, clamped to +-127) and row scales around 1/64
+        k_cache = torch.empty((nb, Hkv, bs, D), dtype=torch.int8, device=device)
+        v_cache = torch.empty((nb, Hkv, bs, D), dtype=torch.int8, device=device)
+        for c in (k_cache, v_cache):
+            tmp = torch.empty(c.shape, dtype=torch.float32, device=device)
+            _fill_random(tmp, gen)
+            c.copy_((tmp * 32.0).round().clamp(-127, 127).to(torch.int8))
+            del tmp
+        k_scale = torch.rand((nb, Hkv, bs), generator=gen, device=device) * (1 / 64) + 1 / 128
+        v_scale = torch.rand((nb, Hkv, bs), generator=gen, device=device) * (1 / 64) + 1 / 128
     else:
         k_cache = torch.empty((nb, Hkv, bs, D), dtype=dt, device=device)
         v_cache = torch.empty((nb, Hkv, bs, D), dtype=dt, device=device)
@@ -301,9 +316,10 @@ def make_workload(spec: WorkloadSpec, device="cpu", poison: bool = True,
         bad = torch.from_numpy(np.nonzero(~valid)[0]).to(device)
         if bad.numel():
             blk, row = bad // bs, bad % bs
-            if spec.kv_fp8:
-                k_cache[blk, :, row, :] = 0x7F  # E4M3 NaN code
-                v_cache[blk, :, row, :] = 0x7F
+            if spec.kv_fp8 or spec.kv_int8:
+                code = 0x7F if spec.kv_fp8 else -128  # E4M3 NaN / never-written int8 code
+                k_cache[blk, :, row, :] = code
+                v_cache[blk, :, row, :] = code
                 k_scale[blk, :, row] = float("nan")
                 v_scale[blk, :, row] = float("nan")
             else:

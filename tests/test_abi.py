@@ -135,3 +135,31 @@ def test_plan_covers_every_length(pkv_lib):
                     worst = max(-(-_units_needed(L, window, sinks) // units)
                                 for L in range(0, mb * 32 + 1))
                     assert worst <= ns
+
+
+def test_quantised_pool_argument_checks(pkv_lib):
+    """8-bit pools (FP8 = 3, INT8 = 4): decode only at head_dim 128 and with row
+    scales, appends only into the matching code format, no fixed-scratch decode."""
+    pkv = pkv_lib
+    lib = pkv.load_library()
+    for dt in (3, 4):
+        assert _decode(pkv, _layout(pkv, dt=dt, d=64)) == UNSUP
+        assert _decode(pkv, _layout(pkv, dt=dt)) == NULL         # no scales given
+        vp = ctypes.c_void_p
+        assert lib.pkv_decode_noalloc(vp(FAKE), 4, 32, vp(FAKE), vp(FAKE),
+                                      ctypes.byref(_layout(pkv, dt=dt)), vp(FAKE), 8, vp(FAKE),
+                                      0, ctypes.c_float(0.1), vp(FAKE), None) == UNSUP
+
+    def app(fn, dt, in_dtype=1, ks=FAKE, n=3):
+        lay = _layout(pkv, dt=dt)
+        return getattr(lib, fn)(FAKE, FAKE, in_dtype, FAKE, n, FAKE, FAKE, ks, FAKE,
+                                ctypes.byref(lay), None)
+
+    assert app("pkv_append_int8", 3) == DTYPE      # an FP8 pool
+    assert app("pkv_append_fp8", 4) == DTYPE       # an INT8 pool
+    assert app("pkv_append_int8", 1) == DTYPE      # a 16-bit pool
+    assert app("pkv_append_int8", 4, in_dtype=3) == DTYPE
+    assert app("pkv_append_int8", 4, ks=0) == NULL
+    assert app("pkv_append_int8", 4, n=-1) == SHAPE
+    assert app("pkv_append_int8", 4, n=0) == OK
+    assert _decode(pkv, _layout(pkv, dt=5)) == DTYPE
