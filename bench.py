@@ -51,6 +51,28 @@ def dist_env():
             int(os.environ.get("LOCAL_RANK", "0")))
 
 
+def reduce_over_ranks(pg, ms, nbytes):
+    """Whole-job time and bytes: the slowest rank's time, all ranks' bytes
+    (weak scaling: every rank runs its own batch).  pg is torch.distributed
+    with an initialised process group, or None for one process."""
+    if pg is None:
+        return ms, nbytes
+    t = torch.tensor([ms, nbytes], dtype=torch.float64)
+    tmax, tsum = t.clone(), t.clone()
+    pg.all_reduce(tmax, op=pg.ReduceOp.MAX)
+    pg.all_reduce(tsum, op=pg.ReduceOp.SUM)
+    return float(tmax[0]), float(tsum[1])
+
+
+def rank_spec(workload, rank, num_seqs=0):
+    """The workload spec of one rank: same shapes, a seed of its own."""
+    from paged_kv_cache_24_gb300.workloads import CONFIGS, config_spec
+
+    base = config_spec(CONFIGS[workload])
+    over = {"num_seqs": num_seqs} if num_seqs > 0 else {}
+    return config_spec(CONFIGS[workload], seed=base.seed + 1000 * rank, **over)
+
+
 def hbm_peak():
     path = os.path.join(REPO, "MEASURED_PEAKS.json")
     try:
@@ -240,10 +262,10 @@ def run_reference(args, workload):
     w = make_workload(spec, device="cpu", poison=True)
     sampler = OracleSampler(w)
     # calibrate, then size each step so that all warm-up and timed steps take
-    # about two minutes
+    # about --reference-seconds (two minutes by default)
     _, dt, got = sampler.run(max(1, sampler.threads))
     per_pair = dt / got
-    per_step = 120.0 / max(1, args.steps + args.warmup)
+    per_step = args.reference_seconds / max(1, args.steps + args.warmup)
     pairs = int(max(1, min(spec.num_seqs * spec.num_q_heads, per_step / max(per_pair, 1e-6))))
     for i in range(args.warmup):
         sampler.run(pairs, seed=1000 + i)
@@ -360,6 +382,8 @@ def main(argv=None):
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--path", default="fused", choices=["fused", "separate"],
                     help="fused: pkv_append_decode (one launch); separate: pkv_append + pkv_decode")
+    ap.add_argument("--reference-seconds", type=float, default=120.0,
+                    help="--impl reference: host time of all warm-up and timed steps")
     ap.add_argument("--num-seqs", type=int, default=0,
                     help="profiling only: shrink the workload's batch (not a bench line)")
     args = ap.parse_args(argv)
@@ -381,9 +405,8 @@ def main(argv=None):
         dist.init_process_group("gloo")
         pg = dist
 
-    base = config_spec(CONFIGS[args.workload])
     over = {"num_seqs": args.num_seqs} if args.num_seqs > 0 else {}
-    spec = config_spec(CONFIGS[args.workload], seed=base.seed + 1000 * rank, **over)
+    spec = rank_spec(args.workload, rank, args.num_seqs)
     w = make_workload(spec, device="cuda", poison=True)
     S = w.steps
     bs = spec.block_size
@@ -491,15 +514,7 @@ def main(argv=None):
     dec_key = "step" if fused else "decode"  # the fused launch also does the append
     my_dec_bytes = sum(sbytes[s % S][dec_key] for s in range(args.steps))
 
-    t = torch.tensor([total_ms, my_bytes, sum(dec_ms), my_dec_bytes], dtype=torch.float64)
-    if pg:
-        tmax = t.clone()
-        pg.all_reduce(tmax, op=pg.ReduceOp.MAX)
-        tsum = t.clone()
-        pg.all_reduce(tsum, op=pg.ReduceOp.SUM)
-        total_ms_all, bytes_all = float(tmax[0]), float(tsum[1])
-    else:
-        total_ms_all, bytes_all = total_ms, my_bytes
+    total_ms_all, bytes_all = reduce_over_ranks(pg, total_ms, my_bytes)
     ms_per_step = total_ms_all / args.steps
     value = bytes_all / (total_ms_all * 1e-3) / 1e9
     tokens_per_s = world * spec.num_seqs * args.steps / (total_ms_all * 1e-3)
@@ -593,12 +608,7 @@ def run_e2e(pkv, w, spec, args, sbytes, pg, world):
         step.run(s % S)
     ms = (time.perf_counter() - t0) * 1e3
     my_bytes = sum(sbytes[s % S]["step"] for s in range(args.steps))
-    t = torch.tensor([ms, my_bytes], dtype=torch.float64)
-    if pg:
-        tmax, tsum = t.clone(), t.clone()
-        pg.all_reduce(tmax, op=pg.ReduceOp.MAX)
-        pg.all_reduce(tsum, op=pg.ReduceOp.SUM)
-        ms, my_bytes = float(tmax[0]), float(tsum[1])
+    ms, my_bytes = reduce_over_ranks(pg, ms, my_bytes)
     return {"value": my_bytes / (ms * 1e-3) / 1e9, "unit": "GB/s",
             "tokens_per_s": world * spec.num_seqs * args.steps / (ms * 1e-3),
             "ms_per_step": ms / args.steps,
