@@ -29,6 +29,7 @@
 #include <math.h>
 
 #include <atomic>
+#include <type_traits>
 
 #include "pkv_device.cuh"
 #include "pkv_internal.h"
@@ -478,45 +479,60 @@ decode16_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant_
       // ldmatrix.trans on the code tile viewed as 16-bit pairs: a register
       // holds tokens (2 tig, 2 tig + 1) x dims (2 g, 2 g + 1) of one 16-d
       // chunk; one byte permute separates the even-d pair from the odd-d pair,
-      // which feed the even and odd m-tiles of the 32-d block.
+      // which feed the even and odd m-tiles of the 32-d block.  Units wholly
+      // inside the context skip the masks (a second copy of the loop).
+      auto v_products = [&](auto masked_tag) {
+        constexpr bool kMasked = decltype(masked_tag)::value;
 #pragma unroll
-      for (int c = 0; c < KS / 2; ++c) {
-        const int tok = (lane & 7) + ((lane >> 4) << 3);
-        const int chunk = 2 * c + ((lane >> 3) & 1);
-        uint32_t r0, r1, r2, r3;
-        ldmatrix_x4_trans(vt + tok * 128 + ((chunk ^ (tok & 7)) << 4), r0, r1, r2, r3);
-        if constexpr (I8) {
-          r0 ^= 0x80808080u;
-          r1 ^= 0x80808080u;
-          r2 ^= 0x80808080u;
-          r3 ^= 0x80808080u;
-        } else {
-          r0 = __byte_perm(r0, 0u, 0x3120);
-          r1 = __byte_perm(r1, 0u, 0x3120);
-          r2 = __byte_perm(r2, 0u, 0x3120);
-          r3 = __byte_perm(r3, 0u, 0x3120);
-        }
-#pragma unroll
-        for (int e = 0; e < 2; ++e) {
-          const int sh = 16 * e;
-          uint32_t a0, a1, a2, a3;
-          if constexpr (I8) {  // even d: bytes 0, 2; odd d: bytes 1, 3
-            a0 = (e ? s8pair_to_f16x2<0x5341>(r0) : s8pair_to_f16x2<0x5240>(r0)) & mlo;
-            a1 = (e ? s8pair_to_f16x2<0x5341>(r1) : s8pair_to_f16x2<0x5240>(r1)) & mlo;
-            a2 = (e ? s8pair_to_f16x2<0x5341>(r2) : s8pair_to_f16x2<0x5240>(r2)) & mhi;
-            a3 = (e ? s8pair_to_f16x2<0x5341>(r3) : s8pair_to_f16x2<0x5240>(r3)) & mhi;
+        for (int c = 0; c < KS / 2; ++c) {
+          const int tok = (lane & 7) + ((lane >> 4) << 3);
+          const int chunk = 2 * c + ((lane >> 3) & 1);
+          uint32_t r0, r1, r2, r3;
+          ldmatrix_x4_trans(vt + tok * 128 + ((chunk ^ (tok & 7)) << 4), r0, r1, r2, r3);
+          if constexpr (I8) {
+            r0 ^= 0x80808080u;
+            r1 ^= 0x80808080u;
+            r2 ^= 0x80808080u;
+            r3 ^= 0x80808080u;
           } else {
-            a0 = e4m3x2_to_f16x2(r0 >> sh) & mlo;
-            a1 = e4m3x2_to_f16x2(r1 >> sh) & mlo;
-            a2 = e4m3x2_to_f16x2(r2 >> sh) & mhi;
-            a3 = e4m3x2_to_f16x2(r3 >> sh) & mhi;
+            r0 = __byte_perm(r0, 0u, 0x3120);
+            r1 = __byte_perm(r1, 0u, 0x3120);
+            r2 = __byte_perm(r2, 0u, 0x3120);
+            r3 = __byte_perm(r3, 0u, 0x3120);
           }
 #pragma unroll
-          for (int nt = 0; nt < NT; ++nt) {
-            Mma<T>::run(o[2 * c + e][nt], a0, a1, a2, a3, bh[nt][0], bh[nt][1]);
-            Mma<T>::run(o[2 * c + e][nt], a0, a1, a2, a3, bl[nt][0], bl[nt][1]);
+          for (int e = 0; e < 2; ++e) {
+            uint32_t a0, a1, a2, a3;
+            if constexpr (I8) {  // even d: bytes 0, 2; odd d: bytes 1, 3
+              a0 = e ? s8pair_to_f16x2<0x5341>(r0) : s8pair_to_f16x2<0x5240>(r0);
+              a1 = e ? s8pair_to_f16x2<0x5341>(r1) : s8pair_to_f16x2<0x5240>(r1);
+              a2 = e ? s8pair_to_f16x2<0x5341>(r2) : s8pair_to_f16x2<0x5240>(r2);
+              a3 = e ? s8pair_to_f16x2<0x5341>(r3) : s8pair_to_f16x2<0x5240>(r3);
+            } else {
+              const int sh = 16 * e;
+              a0 = e4m3x2_to_f16x2(r0 >> sh);
+              a1 = e4m3x2_to_f16x2(r1 >> sh);
+              a2 = e4m3x2_to_f16x2(r2 >> sh);
+              a3 = e4m3x2_to_f16x2(r3 >> sh);
+            }
+            if constexpr (kMasked) {
+              a0 &= mlo;
+              a1 &= mlo;
+              a2 &= mhi;
+              a3 &= mhi;
+            }
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt) {
+              Mma<T>::run(o[2 * c + e][nt], a0, a1, a2, a3, bh[nt][0], bh[nt][1]);
+              Mma<T>::run(o[2 * c + e][nt], a0, a1, a2, a3, bl[nt][0], bl[nt][1]);
+            }
           }
         }
+      };
+      if (edge) {
+        v_products(std::true_type{});
+      } else {
+        v_products(std::false_type{});
       }
     } else {
 #pragma unroll
