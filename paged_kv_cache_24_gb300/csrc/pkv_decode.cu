@@ -535,20 +535,30 @@ decode16_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant_
         v_products(std::false_type{});
       }
     } else {
+      auto v_products = [&](auto masked_tag) {
+        constexpr bool kMasked = decltype(masked_tag)::value;
 #pragma unroll
-      for (int mt = 0; mt < KS; ++mt) {
-        uint32_t a0, a1, a2, a3;
-        const int tok = (lane & 7) + ((lane >> 4) << 3);
-        ldmatrix_x4_trans(vt + swz(tok, mt * 2 + ((lane >> 3) & 1)), a0, a1, a2, a3);
-        a0 &= mlo;
-        a1 &= mlo;
-        a2 &= mhi;
-        a3 &= mhi;
+        for (int mt = 0; mt < KS; ++mt) {
+          uint32_t a0, a1, a2, a3;
+          const int tok = (lane & 7) + ((lane >> 4) << 3);
+          ldmatrix_x4_trans(vt + swz(tok, mt * 2 + ((lane >> 3) & 1)), a0, a1, a2, a3);
+          if constexpr (kMasked) {
+            a0 &= mlo;
+            a1 &= mlo;
+            a2 &= mhi;
+            a3 &= mhi;
+          }
 #pragma unroll
-        for (int nt = 0; nt < NT; ++nt) {
-          Mma<T>::run(o[mt][nt], a0, a1, a2, a3, bh[nt][0], bh[nt][1]);
-          Mma<T>::run(o[mt][nt], a0, a1, a2, a3, bl[nt][0], bl[nt][1]);
+          for (int nt = 0; nt < NT; ++nt) {
+            Mma<T>::run(o[mt][nt], a0, a1, a2, a3, bh[nt][0], bh[nt][1]);
+            Mma<T>::run(o[mt][nt], a0, a1, a2, a3, bl[nt][0], bl[nt][1]);
+          }
         }
+      };
+      if (edge) {
+        v_products(std::true_type{});
+      } else {
+        v_products(std::false_type{});
       }
     }
 
