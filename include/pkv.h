@@ -206,8 +206,11 @@ typedef struct pkv_decode_options {
  *   pkv_decode); then the query at position p attends positions j <= p (and
  *   p - j < window when window > 0) of the pools, which hold the prefix and
  *   the chunk.  out [T][num_q_heads][head_dim].
- *   Limits: head_dim 64 or 128.  The P.V product runs in fp16: with a bf16
- *   cache, V values beyond the fp16 range (|v| > 65504) are an error.
+ *   Limits: head_dim 64 or 128; num_seqs <= 65534.  The P.V product runs in
+ *   fp16: with a bf16 cache, V values beyond the fp16 range (|v| > 65504) are
+ *   an error.  Uses the stream's workspace (as pkv_decode's split-K) for the
+ *   order of its work items, 4 bytes per (sequence, token chunk); may return
+ *   PKV_ERR_NOMEM when that has to grow.
  *   In-kernel errors (bad block id, L_b < n_b, V out of range) make the rows
  *   of the affected work item NaN: up to 256 (token, query head) rows of one
  *   sequence and kv head.

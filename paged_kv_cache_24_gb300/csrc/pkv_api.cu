@@ -446,10 +446,17 @@ int pkv_prefill(const void* q, const void* k, const void* v, const int32_t* cu_q
   if (num_seqs < 0 || num_q_heads <= 0 || max_chunk < 0 || max_blocks_per_seq < 0 ||
       num_q_heads % layout->num_kv_heads != 0)
     return PKV_ERR_SHAPE;
-  if (num_seqs > 65535) return PKV_ERR_UNSUPPORTED;
+  if (num_seqs > 65534) return PKV_ERR_UNSUPPORTED;
   if (static_cast<int64_t>(max_blocks_per_seq) * layout->block_size > 0x7fffffffLL)
     return PKV_ERR_UNSUPPORTED;  // positions are 32-bit
   if (num_seqs == 0 || max_chunk == 0) return PKV_OK;
+  // work items (sequence, token chunk) and their CTAs (one per kv head and head chunk)
+  const int group = num_q_heads / layout->num_kv_heads;
+  const int heads_log2 = pkv::prefill_heads_log2(group);
+  const int tok_per_cta = pkv::kPrefillRowsCta >> heads_log2;
+  const int64_t items = static_cast<int64_t>(num_seqs) * ((max_chunk + tok_per_cta - 1) / tok_per_cta);
+  if (items * layout->num_kv_heads * (group >> heads_log2) > 0x7fffffffLL)
+    return PKV_ERR_UNSUPPORTED;
   if (!q || !k || !v || !cu_q || !k_cache || !v_cache || !block_tables || !context_lens || !out)
     return PKV_ERR_NULL;
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(k_cache) ||
@@ -461,11 +468,17 @@ int pkv_prefill(const void* q, const void* k, const void* v, const int32_t* cu_q
   if (rc != PKV_OK) return rc;
   rc = encode_pool_map(&vmap, v_cache, layout);
   if (rc != PKV_OK) return rc;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  int device = 0;
+  if (cudaGetDevice(&device) != cudaSuccess) return PKV_ERR_CUDA;
+  void* order = nullptr;  // the items' order, written and read on this stream
+  rc = get_workspace(device, st, static_cast<size_t>(items) * sizeof(int32_t), &order);
+  if (rc != PKV_OK) return rc;
   return to_status(pkv::launch_prefill(
       layout->dtype, layout->head_dim, q, k, v, cu_q, num_seqs, num_q_heads, max_chunk, k_cache,
       v_cache, layout->num_blocks, layout->num_kv_heads, layout->block_size, block_tables,
-      max_blocks_per_seq, context_lens, window, scale, out, kmap, vmap,
-      static_cast<cudaStream_t>(stream)));
+      max_blocks_per_seq, context_lens, window, scale, out, static_cast<int32_t*>(order), kmap,
+      vmap, st));
 }
 
 int pkv_append_fp8(const void* k, const void* v, int32_t in_dtype, const int64_t* slot_mapping,

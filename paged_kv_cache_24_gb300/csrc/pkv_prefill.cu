@@ -8,8 +8,8 @@
 // when window > 0) of the paged cache -- the cached prefix and the chunk.
 //
 // How: the chunk's K/V rows are first written to their slots (the kernel
-// below), then the attention runs on the tcgen05 tensor cores
-// (pkv_prefill_tc.cu).
+// below, whose extra block also orders the attention's work items), then the
+// attention runs on the tcgen05 tensor cores (pkv_prefill_tc.cu).
 #include "pkv_device.cuh"
 #include "pkv_internal.h"
 #include "pkv_prefill.h"
@@ -17,17 +17,81 @@
 namespace pkv {
 namespace {
 
+constexpr int kAppendThreads = 256;
+constexpr int kPlanBins = 4096;  // work sizes 0 .. 4095 key tiles (larger ones share the top bin)
+
+struct PlanArgs {
+  int32_t* order;
+  int chunks_per_seq, tok_per_cta, window;
+};
+
+// Work items (sequence b, token chunk c), item id b * chunks_per_seq + c, in
+// descending order of their key tiles: a counting sort over the work sizes in
+// one block (histogram, exclusive scan, scatter).  Items of equal size come
+// in any order; each item's result does not depend on when it runs.
+__device__ void plan_items(const int32_t* __restrict__ cu_q,
+                           const int32_t* __restrict__ context_lens, int num_seqs,
+                           int max_blocks, int block_size, const PlanArgs& pa) {
+  static_assert(kPlanBins % kAppendThreads == 0, "bins per thread");
+  constexpr int kPer = kPlanBins / kAppendThreads;
+  __shared__ int bins[kPlanBins];
+  __shared__ int warp_sum[kAppendThreads / 32];
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  for (int i = tid; i < kPlanBins; i += kAppendThreads) bins[i] = 0;
+  __syncthreads();
+  const int64_t n_items = static_cast<int64_t>(num_seqs) * pa.chunks_per_seq;
+  auto bin_of = [&](int64_t i) {
+    const int b = static_cast<int>(i / pa.chunks_per_seq);
+    const int c = static_cast<int>(i - static_cast<int64_t>(b) * pa.chunks_per_seq);
+    const PrefillItem it = prefill_item(cu_q, context_lens, b, c, pa.tok_per_cta, pa.window,
+                                        max_blocks, block_size);
+    const int w = it.empty ? 0 : min(it.n_tiles, kPlanBins - 1);
+    return kPlanBins - 1 - w;  // the largest work first
+  };
+  for (int64_t i = tid; i < n_items; i += kAppendThreads) atomicAdd(&bins[bin_of(i)], 1);
+  __syncthreads();
+  // exclusive scan: thread t owns bins t*kPer .. t*kPer + kPer - 1
+  int local = 0;
+#pragma unroll
+  for (int k = 0; k < kPer; ++k) local += bins[tid * kPer + k];
+  int incl = local;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int y = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += y;
+  }
+  if (lane == 31) warp_sum[warp] = incl;
+  __syncthreads();
+  int run = incl - local;
+  for (int w = 0; w < warp; ++w) run += warp_sum[w];
+#pragma unroll
+  for (int k = 0; k < kPer; ++k) {
+    const int h = bins[tid * kPer + k];
+    bins[tid * kPer + k] = run;
+    run += h;
+  }
+  __syncthreads();
+  for (int64_t i = tid; i < n_items; i += kAppendThreads)
+    pa.order[atomicAdd(&bins[bin_of(i)], 1)] = static_cast<int32_t>(i);
+}
+
 // The chunk's K/V rows to their slots: token i of sequence b sits at position
 // L_b - n_b + i.  One thread per 16-byte chunk of a (token, kv head) row.
-__global__ void chunk_append_kernel(const uint4* __restrict__ k, const uint4* __restrict__ v,
-                                    const int32_t* __restrict__ cu_q,
-                                    const int32_t* __restrict__ context_lens,
-                                    const int32_t* __restrict__ block_tables, int max_blocks,
-                                    int block_size, int64_t num_blocks, int num_kv_heads,
-                                    int chunks_per_row, uint4* __restrict__ k_cache,
-                                    uint4* __restrict__ v_cache) {
+// Block (0, num_seqs) orders the attention's work items instead.
+__global__ void __launch_bounds__(kAppendThreads)
+chunk_append_kernel(const uint4* __restrict__ k, const uint4* __restrict__ v,
+                    const int32_t* __restrict__ cu_q, const int32_t* __restrict__ context_lens,
+                    const int32_t* __restrict__ block_tables, int max_blocks, int block_size,
+                    int64_t num_blocks, int num_kv_heads, int chunks_per_row,
+                    uint4* __restrict__ k_cache, uint4* __restrict__ v_cache, int num_seqs,
+                    const PlanArgs pa) {
   pdl_launch_dependents();
   pdl_wait_prior();
+  if (static_cast<int>(blockIdx.y) == num_seqs) {
+    if (blockIdx.x == 0)
+      plan_items(cu_q, context_lens, num_seqs, max_blocks, block_size, pa);
+    return;
+  }
   const int b = blockIdx.y;
   const int start = cu_q[b];
   const int n = cu_q[b + 1] - start;
@@ -55,22 +119,29 @@ cudaError_t launch_prefill(int dtype, int head_dim, const void* q, const void* k
                            void* k_cache, void* v_cache, int64_t num_blocks, int num_kv_heads,
                            int block_size, const int32_t* block_tables, int max_blocks,
                            const int32_t* context_lens, int window, float scale, void* out,
-                           const CUtensorMap& kmap, const CUtensorMap& vmap, cudaStream_t stream) {
+                           int32_t* order, const CUtensorMap& kmap, const CUtensorMap& vmap,
+                           cudaStream_t stream) {
   if (num_seqs == 0 || max_chunk == 0) return cudaSuccess;
-  // 1) the chunk's rows to their slots
+  // 1) the chunk's rows to their slots; the work items' order
   const int cpr = head_dim * 2 / 16;
   const int64_t per_seq = static_cast<int64_t>(max_chunk) * num_kv_heads * cpr;
-  dim3 agrid(static_cast<unsigned>((per_seq + 255) / 256), num_seqs);
-  cudaError_t e = launch_pdl(chunk_append_kernel, agrid, dim3(256), 0, stream,
+  PlanArgs pa;
+  pa.order = order;
+  pa.tok_per_cta = kPrefillRowsCta >> prefill_heads_log2(num_q_heads / num_kv_heads);
+  pa.chunks_per_seq = (max_chunk + pa.tok_per_cta - 1) / pa.tok_per_cta;
+  pa.window = window;
+  dim3 agrid(static_cast<unsigned>((per_seq + kAppendThreads - 1) / kAppendThreads),
+             num_seqs + 1);
+  cudaError_t e = launch_pdl(chunk_append_kernel, agrid, dim3(kAppendThreads), 0, stream,
                              static_cast<const uint4*>(k), static_cast<const uint4*>(v), cu_q,
                              context_lens, block_tables, max_blocks, block_size, num_blocks,
                              num_kv_heads, cpr, static_cast<uint4*>(k_cache),
-                             static_cast<uint4*>(v_cache));
+                             static_cast<uint4*>(v_cache), num_seqs, pa);
   if (e != cudaSuccess) return e;
-  // 2) attention over prefix + chunk on the tensor cores
+  // 2) attention over prefix + chunk on the tensor cores, items in that order
   return launch_prefill_tc(dtype, head_dim, q, cu_q, num_seqs, num_q_heads, max_chunk,
                            num_blocks, num_kv_heads, block_size, block_tables, max_blocks,
-                           context_lens, window, scale, out, kmap, vmap, stream);
+                           context_lens, window, scale, out, order, kmap, vmap, stream);
 }
 
 }  // namespace pkv

@@ -7,13 +7,66 @@
 
 namespace pkv {
 
-// Chunked prefill: the chunk's rows to their slots, then attention.
+// Keys per tile of the tensor-core prefill, and query rows per CTA.
+constexpr int kPrefillTileKeys = 128;
+constexpr int kPrefillRowsCta = 256;
+
+// A CTA's rows are (token, GQA head) pairs of one kv head: the largest power
+// of two (at most 16) dividing the group size G is the number of heads per
+// token, 256 / that the tokens per CTA.
+__host__ __device__ __forceinline__ int prefill_heads_log2(int group) {
+  int lg = 0;
+  while (lg < 4 && group % (2 << lg) == 0) ++lg;
+  return lg;
+}
+
+#ifdef __CUDACC__
+// Work item (sequence b, token chunk c) of the prefill: the chunk's tokens
+// tile0 .. tile0 + tile_n - 1 sit at positions pos0 .. pos1 and attend keys
+// k_lo .. pos1, read in units of 16 keys from unit u_first on and in tiles of
+// kPrefillTileKeys keys.  `empty`: the chunk has no token there; `len_ok`
+// false: the sequence's lengths are inconsistent (its rows become NaN).
+struct PrefillItem {
+  int start, n, tile0, tile_n, pos0, pos1, k_lo, u_first, n_units, n_tiles;
+  bool empty, len_ok;
+};
+
+__device__ __forceinline__ PrefillItem prefill_item(const int32_t* cu_q, const int32_t* lens,
+                                                    int b, int c, int tok_per_cta, int window,
+                                                    int max_blocks, int block_size) {
+  PrefillItem it{};
+  it.start = cu_q[b];
+  it.n = cu_q[b + 1] - it.start;
+  it.tile0 = c * tok_per_cta;
+  it.empty = it.tile0 >= it.n;
+  if (it.empty) return it;
+  const int L = lens[b];
+  it.tile_n = min(tok_per_cta, it.n - it.tile0);
+  it.pos0 = L - it.n + it.tile0;
+  it.pos1 = it.pos0 + it.tile_n - 1;
+  it.len_ok = L >= it.n && it.pos0 >= 0 &&
+              static_cast<int64_t>(L) <= static_cast<int64_t>(max_blocks) * block_size;
+  it.k_lo = window > 0 ? max(0, it.pos0 - window + 1) : 0;
+  it.u_first = it.k_lo / 16;
+  it.n_units = it.len_ok ? it.pos1 / 16 - it.u_first + 1 : 0;
+  it.n_tiles = (it.n_units + kPrefillTileKeys / 16 - 1) / (kPrefillTileKeys / 16);
+  return it;
+}
+#endif
+
+// Chunked prefill: the chunk's rows to their slots, then attention.  The
+// append launch also orders the work items (sequence, token chunk) by their
+// number of key tiles, longest first, into `order` (num_seqs * chunks per
+// sequence entries, device memory), and the attention CTAs take the items in
+// that order: the hardware starts CTAs in index order, so the long items
+// start first and the short ones fill the end (longest-processing-time-first).
 cudaError_t launch_prefill(int dtype, int head_dim, const void* q, const void* k, const void* v,
                            const int32_t* cu_q, int num_seqs, int num_q_heads, int max_chunk,
                            void* k_cache, void* v_cache, int64_t num_blocks, int num_kv_heads,
                            int block_size, const int32_t* block_tables, int max_blocks,
                            const int32_t* context_lens, int window, float scale, void* out,
-                           const CUtensorMap& kmap, const CUtensorMap& vmap, cudaStream_t stream);
+                           int32_t* order, const CUtensorMap& kmap, const CUtensorMap& vmap,
+                           cudaStream_t stream);
 
 // Attention half of the chunked prefill on the tcgen05 tensor cores (the
 // chunk's rows must already be in the pools).
@@ -21,7 +74,8 @@ cudaError_t launch_prefill_tc(int dtype, int head_dim, const void* q, const int3
                               int num_seqs, int num_q_heads, int max_chunk, int64_t num_blocks,
                               int num_kv_heads, int block_size, const int32_t* block_tables,
                               int max_blocks, const int32_t* context_lens, int window,
-                              float scale, void* out, const CUtensorMap& kmap,
-                              const CUtensorMap& vmap, cudaStream_t stream);
+                              float scale, void* out, const int32_t* order,
+                              const CUtensorMap& kmap, const CUtensorMap& vmap,
+                              cudaStream_t stream);
 
 }  // namespace pkv

@@ -6,7 +6,9 @@
 // position p attends keys j <= p with p - j < window, softmax per row).
 //
 // How.  A CTA owns 256 query rows of one (sequence, kv head): (token, GQA
-// head) pairs, so every K/V page it reads serves the whole group.  The rows
+// head) pairs, so every K/V page it reads serves the whole group.  CTAs take
+// the (sequence, token chunk) items in the order the planner gave them
+// (most key tiles first), the kv heads of one item side by side.  The rows
 // form two tiles of 128 (one per TMEM lane), worked on in ping-pong over
 // tiles of 128 keys:
 //   warp 9       (load)    TMA of the 16-key K and V units of each key tile
@@ -40,8 +42,9 @@ namespace pkv {
 namespace {
 
 constexpr int kQT = 128;          // rows per Q tile == TMEM lanes
-constexpr int kRowsCta = 2 * kQT;
-constexpr int kTKeys = 128;       // keys per K/V tile
+constexpr int kRowsCta = kPrefillRowsCta;
+constexpr int kTKeys = kPrefillTileKeys;  // keys per K/V tile
+static_assert(kRowsCta == 2 * kQT && kUnitTokens == 16, "tile shapes");
 constexpr int kTUnits = kTKeys / kUnitTokens;
 constexpr int kMmaWarp = 8, kLoadWarp = 9, kPrepWarp0 = 10;
 constexpr int kTThreads = 384;
@@ -55,11 +58,12 @@ struct TcParams {
   const void* q;
   void* out;
   const int32_t* cu_q;
+  const int32_t* order;  // work items, most key tiles first
   const int32_t* block_tables;
   const int32_t* context_lens;
   int64_t num_blocks;
   int num_q_heads, num_kv_heads, group;
-  int head_chunk_log2, num_head_chunks;
+  int head_chunk_log2, num_head_chunks, chunks_per_seq;
   int max_blocks, block_size, window;
   float scale_log2;
 };
@@ -114,25 +118,22 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
   pdl_launch_dependents();
   pdl_wait_prior();
 
-  const int b = blockIdx.z;
-  const int hkv = blockIdx.y / p.num_head_chunks;
-  const int chunk = blockIdx.y - hkv * p.num_head_chunks;
+  const int hh_count = p.num_kv_heads * p.num_head_chunks;
+  const int slot = static_cast<int>(blockIdx.x / hh_count);
+  const int hh = static_cast<int>(blockIdx.x - static_cast<unsigned>(slot) * hh_count);
+  const int item = p.order[slot];
+  const int b = item / p.chunks_per_seq;
+  const int hkv = hh / p.num_head_chunks;
+  const int chunk = hh - hkv * p.num_head_chunks;
   const int lg = p.head_chunk_log2, gc = 1 << lg;
   const int tok_per_cta = kRowsCta >> lg;
-  const int start = p.cu_q[b];
-  const int n = p.cu_q[b + 1] - start;
-  // the latest tokens (longest key ranges) first
-  const int tile0 = (gridDim.x - 1 - blockIdx.x) * tok_per_cta;
-  if (tile0 >= n) return;
-  const int L = p.context_lens[b];
-  const int tile_n = min(tok_per_cta, n - tile0);
-  const int pos0 = L - n + tile0, pos1 = pos0 + tile_n - 1;
-  const bool len_ok = L >= n && pos0 >= 0 &&
-                      static_cast<int64_t>(L) <= static_cast<int64_t>(p.max_blocks) * p.block_size;
-  const int k_lo = (p.window > 0) ? max(0, pos0 - p.window + 1) : 0;
-  const int u_first = k_lo / kUnitTokens;
-  const int n_units = len_ok ? pos1 / kUnitTokens - u_first + 1 : 0;
-  const int n_tiles = (n_units + kTUnits - 1) / kTUnits;
+  const PrefillItem it = prefill_item(p.cu_q, p.context_lens, b, item - b * p.chunks_per_seq,
+                                      tok_per_cta, p.window, p.max_blocks, p.block_size);
+  if (it.empty) return;
+  const int start = it.start, tile0 = it.tile0, tile_n = it.tile_n;
+  const int pos0 = it.pos0, pos1 = it.pos1, k_lo = it.k_lo, u_first = it.u_first;
+  const int n_units = it.n_units, n_tiles = it.n_tiles;
+  const bool len_ok = it.len_ok;
 
   const uint32_t raw_addr = smem_u32(smem_raw);
   const uint32_t base = (raw_addr + 1023u) & ~1023u;
@@ -498,10 +499,11 @@ cudaError_t launch_t(const CUtensorMap& kmap, const CUtensorMap& vmap, const TcP
     if (e != cudaSuccess) return e;
     configured.fetch_or(bit, std::memory_order_acq_rel);
   }
-  const int tok_per_cta = kRowsCta >> p.head_chunk_log2;
-  dim3 grid((max_chunk + tok_per_cta - 1) / tok_per_cta, p.num_kv_heads * p.num_head_chunks,
-            num_seqs);
-  return launch_pdl(kern, grid, dim3(kTThreads), smem, stream, kmap, vmap, p);
+  const int64_t ctas = static_cast<int64_t>(num_seqs) * p.chunks_per_seq * p.num_kv_heads *
+                       p.num_head_chunks;
+  if (ctas > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+  return launch_pdl(kern, dim3(static_cast<unsigned>(ctas)), dim3(kTThreads), smem, stream, kmap,
+                    vmap, p);
 }
 
 }  // namespace
@@ -510,24 +512,24 @@ cudaError_t launch_prefill_tc(int dtype, int head_dim, const void* q, const int3
                               int num_seqs, int num_q_heads, int max_chunk, int64_t num_blocks,
                               int num_kv_heads, int block_size, const int32_t* block_tables,
                               int max_blocks, const int32_t* context_lens, int window,
-                              float scale, void* out, const CUtensorMap& kmap,
-                              const CUtensorMap& vmap, cudaStream_t stream) {
+                              float scale, void* out, const int32_t* order,
+                              const CUtensorMap& kmap, const CUtensorMap& vmap,
+                              cudaStream_t stream) {
   TcParams p{};
   p.q = q;
   p.out = out;
   p.cu_q = cu_q;
+  p.order = order;
   p.block_tables = block_tables;
   p.context_lens = context_lens;
   p.num_blocks = num_blocks;
   p.num_q_heads = num_q_heads;
   p.num_kv_heads = num_kv_heads;
   p.group = num_q_heads / num_kv_heads;
-  int gc = 1;
-  while (gc * 2 <= 16 && p.group % (gc * 2) == 0) gc *= 2;  // largest power of two dividing G
-  int lg = 0;
-  while ((1 << lg) < gc) ++lg;
-  p.head_chunk_log2 = lg;
-  p.num_head_chunks = p.group / gc;
+  p.head_chunk_log2 = prefill_heads_log2(p.group);
+  p.num_head_chunks = p.group >> p.head_chunk_log2;
+  const int tok_per_cta = kRowsCta >> p.head_chunk_log2;
+  p.chunks_per_seq = (max_chunk + tok_per_cta - 1) / tok_per_cta;
   p.max_blocks = max_blocks;
   p.block_size = block_size;
   p.window = window;

@@ -71,6 +71,11 @@ CASES = [
     ("long_prefix", torch.bfloat16, 8, 2, 128, 16, [3000, 1], [300, 700], 0),
     ("long_prefix_fp16", torch.float16, 16, 2, 128, 32, [2047], [513], 0),
 ]
+# more (sequence, token chunk) work items than the planner's block has threads,
+# of many different sizes, so its counting sort loops and fills many bins
+_r = np.random.default_rng(29)
+CASES.append(("many_seqs", torch.float16, 8, 2, 128, 16, _r.integers(0, 600, 300).tolist(),
+              _r.integers(1, 140, 300).tolist(), 0))
 
 
 @pytest.mark.parametrize("name,dtype,hq,hkv,d,bs,prefixes,chunks,window", CASES,
@@ -80,8 +85,10 @@ def test_prefill_matches_oracle(pkv_lib, oracle_lib, name, dtype, hq, hkv, d, bs
     w, q, k, v, cu, lens = _prefill_case(dtype, hq, hkv, d, bs, prefixes, chunks, window,
                                          seed=len(name))
     ref, kc_h, vc_h = _oracle_prefill(w, q, k, v, cu, lens, chunks, window)
-    out = pkv_lib.pkv_prefill(q, k, v, cu, w.k_cache, w.v_cache, w.block_tables, lens, window,
-                              w.scale, max_chunk=max(chunks))
+    # every row must be written: a work item left out would leave NaN behind
+    out = torch.full_like(q, float("nan"))
+    pkv_lib.pkv_prefill(q, k, v, cu, w.k_cache, w.v_cache, w.block_tables, lens, window,
+                        w.scale, max_chunk=max(chunks), out=out)
     torch.cuda.synchronize()
     assert torch.equal(_bits(w.k_cache.cpu()), _bits(kc_h))
     assert torch.equal(_bits(w.v_cache.cpu()), _bits(vc_h))
