@@ -207,41 +207,38 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
         if (pb < 0 || pb >= p.num_blocks) return -2;
         return (pb * p.num_kv_heads + hkv) * p.block_size + (t0 % p.block_size);
       };
-      auto issue = [&](const CUtensorMap* map, uint32_t bar, uint32_t dst, const int (&ys)[kTUnits],
-                       int loaded) {
-        if (loaded == 0) {
-          mbar_arrive(bar);
-          return;
+      // Lane 0 posts the tile's byte count, then lane i copies unit i (its
+      // K or V rows, one box per 64 columns): a copy takes tens of cycles to
+      // issue, so the eight units go out side by side.
+      auto issue = [&](const CUtensorMap* map, uint32_t bar, uint32_t dst, int y, int loaded) {
+        if (lane == 0) {
+          if (loaded == 0)
+            mbar_arrive(bar);
+          else
+            mbar_arrive_expect_tx(bar, loaded * Lay::kKBlocks * kUnitTokens * 128);
         }
-        mbar_arrive_expect_tx(bar, loaded * Lay::kKBlocks * kUnitTokens * 128);
-#pragma unroll
-        for (int i = 0; i < kTUnits; ++i) {
-          if (ys[i] < 0) continue;
+        __syncwarp();
+        if (y >= 0) {
 #pragma unroll
           for (int kb = 0; kb < Lay::kKBlocks; ++kb)
-            tma_load_2d(dst + kb * kTKeys * 128 + i * kUnitTokens * 128, map, kb * 64, ys[i], bar);
+            tma_load_2d(dst + kb * kTKeys * 128 + lane * kUnitTokens * 128, map, kb * 64, y, bar);
         }
       };
+      // lane i < 8 holds the page row of unit i of the tile (-1 elsewhere)
       int y_next = (lane < kTUnits && n_tiles > 0) ? page_row(lane) : -1;
       for (int j = 0; j < n_tiles; ++j) {
         const int y_cur = y_next;
         if (j + 1 < n_tiles) y_next = lane < kTUnits ? page_row((j + 1) * kTUnits + lane) : -1;
-        int ys[kTUnits];
-        int loaded = 0;
-#pragma unroll
-        for (int i = 0; i < kTUnits; ++i) {
-          ys[i] = __shfl_sync(0xffffffffu, y_cur, i);
-          if (ys[i] >= 0) ++loaded;
-          if (ys[i] == -2) bad = true;
-        }
+        const int loaded = __popc(__ballot_sync(0xffffffffu, y_cur >= 0));
+        if (y_cur == -2) bad = true;
         if (j >= SK &&
             !mbar_wait_bounded(smem_u32(&k_empty[j % SK]), ((j / SK) - 1) & 1, kWaitLimit))
           bad = true;
-        if (lane == 0) issue(&kmap, smem_u32(&k_full[j % SK]), k_addr(j), ys, loaded);
+        issue(&kmap, smem_u32(&k_full[j % SK]), k_addr(j), y_cur, loaded);
         if (j >= SV &&
             !mbar_wait_bounded(smem_u32(&v_empty[j % SV]), ((j / SV) - 1) & 1, kWaitLimit))
           bad = true;
-        if (lane == 0) issue(&vmap, smem_u32(&v_full[j % SV]), v_addr(j), ys, loaded);
+        issue(&vmap, smem_u32(&v_full[j % SV]), v_addr(j), y_cur, loaded);
       }
       // every copy started has landed (already waited for unless a wait ran out)
       if (lane == 0) {
@@ -290,9 +287,11 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
       // a bf16 value beyond the fp16 range cannot take part in the fp16 product
       if (__hisinf(__low2half(amax)) || __hisinf(__high2half(amax))) bad = true;
     } else {
-      // ============ MMA warp ============
-      auto issue_s = [&](int t, int j) {
-        if (lane == 0) {
+      // ============ MMA warp: one thread waits and issues ============
+      // (the role uses no warp-collective instruction; the other lanes wait
+      // at the warp's join)
+      if (lane == 0) {
+        auto issue_s = [&](int t, int j) {
           const uint32_t qt = base + t * Lay::kQTileBytes, kt = k_addr(j);
 #pragma unroll
           for (int kk = 0; kk < D / 16; ++kk) {
@@ -303,27 +302,24 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
             umma_f16(tmem + Lay::s_col(t), ad, bd, kIdS, kk > 0 ? 1u : 0u);
           }
           umma_commit(smem_u32(&s_full[t]));
-        }
-        __syncwarp();
-      };
-      auto wait_k = [&](int j) {
-        if (!mbar_wait_bounded(smem_u32(&k_full[j % SK]), (j / SK) & 1, kWaitLimit)) bad = true;
-        tc_fence_after();
-      };
-      if (n_tiles > 0) {
-        wait_k(0);
-        issue_s(0, 0);
-        issue_s(1, 0);
-        if (lane == 0) umma_commit(smem_u32(&k_empty[0]));
-      }
-      for (int j = 0; j < n_tiles; ++j) {
-        if (!mbar_wait_bounded(smem_u32(&v_ready[j % SV]), (j / SV) & 1, kWaitLimit)) bad = true;
-        const uint32_t vt = v_addr(j);
-#pragma unroll
-        for (int t = 0; t < 2; ++t) {
-          if (!mbar_wait_bounded(smem_u32(&p_full[t]), j & 1, kWaitLimit)) bad = true;
+        };
+        auto wait_k = [&](int j) {
+          if (!mbar_wait_bounded(smem_u32(&k_full[j % SK]), (j / SK) & 1, kWaitLimit)) bad = true;
           tc_fence_after();
-          if (lane == 0) {
+        };
+        if (n_tiles > 0) {
+          wait_k(0);
+          issue_s(0, 0);
+          issue_s(1, 0);
+          umma_commit(smem_u32(&k_empty[0]));
+        }
+        for (int j = 0; j < n_tiles; ++j) {
+          if (!mbar_wait_bounded(smem_u32(&v_ready[j % SV]), (j / SV) & 1, kWaitLimit)) bad = true;
+          const uint32_t vt = v_addr(j);
+#pragma unroll
+          for (int t = 0; t < 2; ++t) {
+            if (!mbar_wait_bounded(smem_u32(&p_full[t]), j & 1, kWaitLimit)) bad = true;
+            tc_fence_after();
 #pragma unroll
             for (int kk = 0; kk < kTKeys / 16; ++kk) {
               // V: keys are the K dimension (8-row groups 1 KB apart, 16 keys a
@@ -334,24 +330,22 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
             }
             umma_commit(smem_u32(&o_done[t]));
             if (t == 1) umma_commit(smem_u32(&v_empty[j % SV]));
-          }
-          __syncwarp();
-          if (j + 1 < n_tiles) {
-            // S_t(j+1) overwrites P_t(j) after the product above read it (one
-            // issuing thread: the tensor pipe takes them in order)
-            if (t == 0) wait_k(j + 1);
-            issue_s(t, j + 1);
-            if (t == 1 && lane == 0) umma_commit(smem_u32(&k_empty[(j + 1) % SK]));
-            __syncwarp();
+            if (j + 1 < n_tiles) {
+              // S_t(j+1) overwrites P_t(j) after the product above read it (one
+              // issuing thread: the tensor pipe takes them in order)
+              if (t == 0) wait_k(j + 1);
+              issue_s(t, j + 1);
+              if (t == 1) umma_commit(smem_u32(&k_empty[(j + 1) % SK]));
+            }
           }
         }
+        // every product issued has completed
+        if (n_tiles > 0) {
+          umma_commit(smem_u32(&done_bar));
+          if (!mbar_wait_bounded(smem_u32(&done_bar), 0, kWaitLimit)) bad = true;
+        }
       }
-      // every product issued has completed
-      if (n_tiles > 0) {
-        if (lane == 0) umma_commit(smem_u32(&done_bar));
-        __syncwarp();
-        if (!mbar_wait_bounded(smem_u32(&done_bar), 0, kWaitLimit)) bad = true;
-      }
+      __syncwarp();
     }
     // the softmax warps' join and final barriers
     if (bad) s_bad = 1;
