@@ -105,29 +105,12 @@ __device__ __forceinline__ void tmem_ld128(uint32_t taddr, float (&v)[128]) {
   for (int i = 0; i < 128; ++i) v[i] = __uint_as_float(r[i]);
 }
 
-// Packed fp32 pairs (Blackwell FFMA2 / FADD2): d = a * b + c, d = a + b.
+// Packed fp32 pairs (Blackwell FFMA2 / FADD2): d = a * b + c, d = a + b,
+// through CUDA's float2 intrinsics so the compiler picks the register pairs.
 __device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c) {
-  uint64_t d;
-  asm("{\n\t.reg .b64 ra, rb, rc;\n\t"
-      "mov.b64 ra, {%1, %2};\n\tmov.b64 rb, {%3, %4};\n\tmov.b64 rc, {%5, %6};\n\t"
-      "fma.rn.f32x2 %0, ra, rb, rc;\n\t}"
-      : "=l"(d)
-      : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y), "f"(c.x), "f"(c.y));
-  float2 r;
-  asm("mov.b64 {%0, %1}, %2;" : "=f"(r.x), "=f"(r.y) : "l"(d));
-  return r;
+  return __ffma2_rn(a, b, c);
 }
-__device__ __forceinline__ float2 fadd2(float2 a, float2 b) {
-  uint64_t d;
-  asm("{\n\t.reg .b64 ra, rb;\n\t"
-      "mov.b64 ra, {%1, %2};\n\tmov.b64 rb, {%3, %4};\n\t"
-      "add.rn.f32x2 %0, ra, rb;\n\t}"
-      : "=l"(d)
-      : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
-  float2 r;
-  asm("mov.b64 {%0, %1}, %2;" : "=f"(r.x), "=f"(r.y) : "l"(d));
-  return r;
-}
+__device__ __forceinline__ float2 fadd2(float2 a, float2 b) { return __fadd2_rn(a, b); }
 
 // 16 consecutive 32-bit columns of this thread's TMEM lane; not waited for
 // (tmem_wait_st makes the stores visible to later tcgen05 operations).
