@@ -159,27 +159,29 @@ class ClockSampler:
                 "sm_max_mhz": self.max_mhz, "reasons": names, "samples": len(self.samples)}
 
 
-def kernel_source_digest():
+def kernel_source_digest(kind="decode"):
+    """Digest of the sources of the decode kernels or of the prefill kernels."""
     h = hashlib.sha256()
     csrc = os.path.join(REPO, "paged_kv_cache_24_gb300", "csrc")
+    own = ("pkv_decode",) if kind == "decode" else ("pkv_prefill", "pkv_tcgen05")
     for name in sorted(os.listdir(csrc)):
-        if name.startswith("pkv_decode") or name in ("pkv_device.cuh", "pkv_internal.h"):
+        if name.startswith(own) or name in ("pkv_device.cuh", "pkv_internal.h"):
             with open(os.path.join(csrc, name), "rb") as f:
                 h.update(name.encode() + b"\0" + f.read())
     return h.hexdigest()[:16]
 
 
-def recorded_traffic(workload):
-    """DRAM bytes per decode launch from a committed ncu summary, if it still
-    describes the current kernel source (else None)."""
-    path = os.path.join(REPO, "profiles", "decode_traffic.json")
+def recorded_traffic(workload, kind="decode"):
+    """DRAM bytes per launch of the dominant kernel from a committed ncu
+    summary, if it still describes the current kernel source (else None)."""
+    path = os.path.join(REPO, "profiles", f"{kind}_traffic.json")
     try:
         with open(path) as f:
             rec = json.load(f)
     except Exception:
         return None
     ent = rec.get(workload)
-    if not ent or ent.get("kernel_digest") != kernel_source_digest():
+    if not ent or ent.get("kernel_digest") != kernel_source_digest(kind):
         return None
     return ent.get("dram_bytes_per_launch")
 
@@ -332,17 +334,33 @@ def run_prefill(args, pkv):
         pkv.pkv_prefill(q, k, v, cu, w.k_cache, w.v_cache, w.block_tables, L, 0, w.scale,
                         max_chunk=chunk, out=out)
 
-    for _ in range(args.warmup):
+    # The K/V the step reads (tens of MB) fits in L2: L2 is flushed before
+    # every timed step (outside its events), as for the decode lines.
+    flush_buf = torch.empty(2 * L2_BYTES, dtype=torch.uint8, device="cuda")
+    clean_buf = torch.zeros(2 * L2_BYTES // 4, dtype=torch.int32, device="cuda")
+    # warm-up on the capture stream (the stream's workspace then exists), then
+    # the timed steps replay a CUDA graph of the same C-ABI call
+    gstream = torch.cuda.Stream()
+    gstream.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(gstream):
+        for _ in range(args.warmup):
+            step()
+    gstream.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=gstream):
         step()
     torch.cuda.synchronize()
-    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    with ClockSampler(0) as clocks:
-        a.record()
-        for _ in range(args.steps):
-            step()
-        b.record()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(args.steps)]
+    with ClockSampler(0) as clocks, torch.cuda.stream(gstream):
+        for s in range(args.steps):
+            flush_buf.add_(1)
+            clean_buf.amax()
+            ev[s][0].record(gstream)
+            graph.replay()
+            ev[s][1].record(gstream)
         torch.cuda.synchronize()
-    ms = a.elapsed_time(b) / args.steps
+    ms = sum(a.elapsed_time(b) for a, b in ev) / args.steps
     tflops = flops / (ms * 1e-3) / 1e12
     peak = None
     try:
@@ -358,11 +376,13 @@ def run_prefill(args, pkv):
         "dtype": DTYPE_NAME[spec.dtype], "data": "synthetic",
         "config": {"workload": args.workload, "num_seqs": B, "chunk": chunk,
                    "mean_prefix": float(prefix.mean()), "num_q_heads": hq, "num_kv_heads": hkv,
-                   "head_dim": d, "block_size": spec.block_size},
+                   "head_dim": d, "block_size": spec.block_size,
+                   "l2": "flushed between steps (2x L2 written, then 2x L2 read)"},
         "tokens_per_s": T / (ms * 1e-3),
         "roofline": {"bound": "tensor", "kernel": "prefill (chunk append + attention)",
                      "achieved": tflops, "peak": peak, "unit": "TFLOP/s", "frac": tflops / peak,
-                     "peak_kind": peak_kind, "traffic": None},
+                     "peak_kind": peak_kind,
+                     "traffic": recorded_traffic(args.workload, "prefill")},
         "gpu_launches": 2 * args.steps, "clocks": clocks.summary()}), flush=True)
     return 0
 
