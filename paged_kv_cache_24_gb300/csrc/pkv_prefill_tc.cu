@@ -291,15 +291,18 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
       // (the role uses no warp-collective instruction; the other lanes wait
       // at the warp's join)
       if (lane == 0) {
+        // A descriptor is built once per operand tile; a step inside the tile
+        // adds its byte offset / 16 to the start-address field (shared
+        // memory addresses stay below 256 KB, so the field cannot carry).
         auto issue_s = [&](int t, int j) {
-          const uint32_t qt = base + t * Lay::kQTileBytes, kt = k_addr(j);
+          const uint64_t a0 = umma_sdesc_sw128(base + t * Lay::kQTileBytes, 16, 1024);
+          const uint64_t b0 = umma_sdesc_sw128(k_addr(j), 16, 1024);
 #pragma unroll
           for (int kk = 0; kk < D / 16; ++kk) {
-            const uint64_t ad =
-                umma_sdesc_sw128(qt + (kk >> 2) * kQT * 128 + (kk & 3) * 32, 16, 1024);
-            const uint64_t bd =
-                umma_sdesc_sw128(kt + (kk >> 2) * kTKeys * 128 + (kk & 3) * 32, 16, 1024);
-            umma_f16(tmem + Lay::s_col(t), ad, bd, kIdS, kk > 0 ? 1u : 0u);
+            // 16 columns a step: 32 bytes inside a 128-byte block, blocks a tile apart
+            const uint64_t step = static_cast<uint64_t>(((kk >> 2) * kQT * 128 + (kk & 3) * 32) >> 4);
+            static_assert(kQT == kTKeys, "Q and K tiles share their step offsets");
+            umma_f16(tmem + Lay::s_col(t), a0 + step, b0 + step, kIdS, kk > 0 ? 1u : 0u);
           }
           umma_commit(smem_u32(&s_full[t]));
         };
@@ -315,19 +318,18 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
         }
         for (int j = 0; j < n_tiles; ++j) {
           if (!mbar_wait_bounded(smem_u32(&v_ready[j % SV]), (j / SV) & 1, kWaitLimit)) bad = true;
-          const uint32_t vt = v_addr(j);
+          // V: keys are the K dimension (8-row groups 1 KB apart, 16 keys a
+          // step), head dims the N dimension (64-column blocks a tile apart)
+          const uint64_t v0 = umma_sdesc_sw128(v_addr(j), kTKeys * 128, 1024);
 #pragma unroll
           for (int t = 0; t < 2; ++t) {
             if (!mbar_wait_bounded(smem_u32(&p_full[t]), j & 1, kWaitLimit)) bad = true;
             tc_fence_after();
 #pragma unroll
-            for (int kk = 0; kk < kTKeys / 16; ++kk) {
-              // V: keys are the K dimension (8-row groups 1 KB apart, 16 keys a
-              // step), head dims the N dimension (64-column blocks a tile apart)
-              const uint64_t bd = umma_sdesc_sw128(vt + kk * 16 * 128, kTKeys * 128, 1024);
-              umma_f16_ts(tmem + Lay::o_col(t), tmem + Lay::s_col(t) + kk * 8, bd, kIdO,
+            for (int kk = 0; kk < kTKeys / 16; ++kk)
+              umma_f16_ts(tmem + Lay::o_col(t), tmem + Lay::s_col(t) + kk * 8,
+                          v0 + static_cast<uint64_t>((kk * 16 * 128) >> 4), kIdO,
                           (j > 0 || kk > 0) ? 1u : 0u);
-            }
             umma_commit(smem_u32(&o_done[t]));
             if (t == 1) umma_commit(smem_u32(&v_empty[j % SV]));
             if (j + 1 < n_tiles) {
