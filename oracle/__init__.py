@@ -100,7 +100,8 @@ def _load():
         lib.oracle_decode_int8.argtypes = lib.oracle_decode_fp8.argtypes
         lib.oracle_prefill.restype = ctypes.c_int
         lib.oracle_prefill.argtypes = [c_vp, c_i32, c_vp, c_i32, c_i32, c_vp, c_vp, c_i64, c_i32,
-                                       c_i32, c_i32, c_vp, c_i32, c_vp, c_i32, c_dbl, c_vp, c_i32]
+                                       c_i32, c_i32, c_vp, c_i32, c_vp, c_i32, c_i32, c_dbl, c_vp,
+                                       c_i32]
         lib.oracle_max_threads.restype = ctypes.c_int
         lib.oracle_max_threads.argtypes = []
         _lib = lib
@@ -438,12 +439,13 @@ def decode_fp8(q, k_codes, v_codes, k_scale, v_scale, block_tables, context_lens
 
 
 def prefill(q, cu_q, k_cache, v_cache, block_tables, context_lens, window: int, scale: float,
-            threads: int = 0, check: bool = True) -> np.ndarray:
+            threads: int = 0, check: bool = True, num_sinks: int = 0) -> np.ndarray:
     """Chunked prefill over a paged cache (chunk already appended), float64.
 
     ``q`` [T, Hq, D] packed chunk queries; ``cu_q`` [B + 1] chunk offsets;
     ``context_lens`` [B] lengths including the chunk.  Query token at position
-    p attends positions j <= p (and p - j < window when window > 0).
+    p attends positions j <= p with p - j < window when window > 0, and, with a
+    window, also the positions j < num_sinks (attention sinks).
     Returns [T, Hq, D]."""
     qr, qd = _as_raw(q)
     kc, kd = _as_raw(k_cache)
@@ -458,7 +460,7 @@ def prefill(q, cu_q, k_cache, v_cache, block_tables, context_lens, window: int, 
     out = np.empty((T, Hq, D), dtype=np.float64)
     rc = _load().oracle_prefill(_ptr(qr), qd, _ptr(cu), len(cu) - 1, Hq, _ptr(kc), _ptr(vc), nb,
                                 hkv, bs, D, _ptr(bt), bt.shape[1], _ptr(lens), int(window),
-                                float(scale), _ptr(out), int(threads))
+                                int(num_sinks), float(scale), _ptr(out), int(threads))
     if check and rc != 0:
         raise ValueError(f"oracle_prefill failed with code {rc}")
     return out

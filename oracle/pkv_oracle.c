@@ -535,14 +535,17 @@ static int decode_pairs(const decode_problem* pp, const int32_t* pairs, int64_t 
  * at positions L_b - n_b .. L_b - 1 (L_b = context_lens[b], n_b the chunk
  * size).  Query token at position p attends the positions j with j <= p and,
  * when window > 0, p - j < window: the mask of prefill_attention, with the
- * softmax taken per query row.  That is a decode of length p + 1 with the same
- * window, which is how it is computed here.
+ * softmax taken per query row.  With a window and num_sinks > 0 the positions
+ * j < num_sinks (j <= p) are attended as well (the attention-sink policy, as
+ * in decode).  That is a decode of length p + 1 with the same window and
+ * sinks, which is how it is computed here.
  *   q   [T][Hq][D] (dtype), out [T][Hq][D] double, T = cu_q[num_seqs]. */
 int oracle_prefill(const void* q, int32_t dtype, const int32_t* cu_q, int32_t num_seqs,
                    int32_t num_q_heads, const void* k_cache, const void* v_cache,
                    int64_t num_blocks, int32_t num_kv_heads, int32_t block_size,
                    int32_t head_dim, const int32_t* block_tables, int32_t max_blocks,
-                   const int32_t* context_lens, int32_t window, double scale, double* out,
+                   const int32_t* context_lens, int32_t window, int32_t num_sinks,
+                   double scale, double* out,
                    int32_t num_threads) {
   if (!q || !cu_q || !k_cache || !v_cache || !block_tables || !context_lens || !out)
     return ORACLE_ERR_ARG;
@@ -566,8 +569,8 @@ int oracle_prefill(const void* q, int32_t dtype, const int32_t* cu_q, int32_t nu
                                               (dtype == ORACLE_F32 ? 4 : 2),
                          1, num_q_heads, k_cache, v_cache, NULL, NULL, num_blocks,
                          num_kv_heads, block_size, head_dim, dtype, dtype,
-                         block_tables + (int64_t)b * max_blocks, max_blocks, &len, window, 0,
-                         scale};
+                         block_tables + (int64_t)b * max_blocks, max_blocks, &len, window,
+                         num_sinks, scale};
     for (int32_t h = 0; h < num_q_heads; ++h) {
       int r = p < 0 ? ORACLE_ERR_LENGTH : decode_one(&dp, 0, h, out + (t * num_q_heads + h) * head_dim);
       if (r != ORACLE_OK) {

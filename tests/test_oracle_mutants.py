@@ -11,8 +11,8 @@ append destination, the wrong query head, a non-zero empty context, and in the
 FP8 cache a wrong exponent bias, ties broken to odd, a dropped sign, a wrong
 quantisation constant, or an ignored row scale, in the INT8 cache a wrong
 scale constant, truncation or ties away from zero instead of ties to even, or
-codes read as unsigned, and in the prefill a query position off by one or a
-missing causal limit.
+codes read as unsigned, and in the prefill a query position off by one, a
+missing causal limit or ignored attention sinks.
 """
 import os
 import shutil
@@ -69,6 +69,8 @@ MUTANTS = {
         "const int64_t p = context_lens[b] - n + (t - cu_q[b]); /* its position */",
         "const int64_t p = context_lens[b] - n + (t - cu_q[b]) + 1; /* its position */"),
     "prefill_not_causal": ("int32_t len = (int32_t)(p + 1);", "int32_t len = context_lens[b];"),
+    "prefill_ignores_sinks": ("max_blocks, &len, window,\n                         num_sinks, scale};",
+                              "max_blocks, &len, window,\n                         0, scale};"),
     "empty_context_not_zero": (
         "for (int32_t d = 0; d < D; ++d) out[d] = 0.0;\n  if (T <= 0) return;",
         "for (int32_t d = 0; d < D; ++d) out[d] = 0.0;\n  if (T <= 0) { out[0] = 1.0; return; }"),
