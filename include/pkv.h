@@ -205,7 +205,11 @@ typedef struct pkv_decode_options {
  *   First the chunk's K/V rows are written to their slots (block_tables as in
  *   pkv_decode); then the query at position p attends positions j <= p (and
  *   p - j < window when window > 0) of the pools, which hold the prefix and
- *   the chunk.  out [T][num_q_heads][head_dim].
+ *   the chunk.  With window > 0 and num_sinks > 0 the positions j <
+ *   num_sinks (j <= p) are attended as well, as in pkv_decode_ex ("...
+ *   Sliding-Window Attention Engine", Extending: attention sinks); num_sinks
+ *   is ignored without a window and must not be negative.
+ *   out [T][num_q_heads][head_dim].
  *   Limits: head_dim 64 or 128; num_seqs <= 65534.  The P.V product runs in
  *   fp16: with a bf16 cache, V values beyond the fp16 range (|v| > 65504) are
  *   an error.  Uses the stream's workspace (as pkv_decode's split-K) for the
@@ -219,7 +223,7 @@ int pkv_prefill(const void* q, const void* k, const void* v, const int32_t* cu_q
                 int32_t num_seqs, int32_t num_q_heads, int32_t max_chunk, void* k_cache,
                 void* v_cache, const pkv_cache_layout* layout, const int32_t* block_tables,
                 int32_t max_blocks_per_seq, const int32_t* context_lens, int32_t window,
-                float scale, void* out, void* stream);
+                int32_t num_sinks, float scale, void* out, void* stream);
 
 /*
  * pkv_append_fp8 -- quantise each new token's K and V rows into FP8 pools.

@@ -80,8 +80,8 @@ def load_library():
                               ctypes.POINTER(DecodeOptions), vp],
             "pkv_append_fp8": [vp, vp, i32, vp, i64, vp, vp, vp, vp, lay, vp],
             "pkv_append_int8": [vp, vp, i32, vp, i64, vp, vp, vp, vp, lay, vp],
-            "pkv_prefill": [vp, vp, vp, vp, i32, i32, i32, vp, vp, lay, vp, i32, vp, i32, f32,
-                            vp, vp],
+            "pkv_prefill": [vp, vp, vp, vp, i32, i32, i32, vp, vp, lay, vp, i32, vp, i32, i32,
+                            f32, vp, vp],
             "pkv_decode_plan": [i32, i32, lay, i32, i32, i32, i32, i32, ctypes.POINTER(i32),
                                 ctypes.POINTER(i32)],
             "pkv_release_workspaces": [],
@@ -267,9 +267,11 @@ def pkv_append_int8(k: torch.Tensor, v: torch.Tensor, slot_mapping: torch.Tensor
 def pkv_prefill(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, cu_q: torch.Tensor,
                 k_cache: torch.Tensor, v_cache: torch.Tensor, block_tables: torch.Tensor,
                 context_lens: torch.Tensor, window: int, scale: float, max_chunk: int,
-                out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+                out: torch.Tensor | None = None, stream=None,
+                num_sinks: int = 0) -> torch.Tensor:
     """Append each sequence's chunk (packed q/k/v, offsets cu_q) and compute its
-    causal (optionally windowed) attention over the paged cache; returns out like q."""
+    causal (optionally windowed, with attention sinks) attention over the
+    paged cache; returns out like q."""
     _on_cuda(q, k, v, cu_q, k_cache, v_cache, block_tables, context_lens, out)
     layout = cache_layout(k_cache)
     _require(v_cache.shape == k_cache.shape and v_cache.dtype == k_cache.dtype
@@ -295,7 +297,8 @@ def pkv_prefill(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, cu_q: torch.T
     _check("pkv_prefill", load_library().pkv_prefill(
         _ptr(q), _ptr(k), _ptr(v), _ptr(cu_q), B, q.shape[1], int(max_chunk), _ptr(k_cache),
         _ptr(v_cache), ctypes.byref(layout), _ptr(block_tables), block_tables.shape[1],
-        _ptr(context_lens), int(window), float(scale), _ptr(out), _stream(stream)))
+        _ptr(context_lens), int(window), int(num_sinks), float(scale), _ptr(out),
+        _stream(stream)))
     return out
 
 

@@ -439,12 +439,12 @@ int pkv_prefill(const void* q, const void* k, const void* v, const int32_t* cu_q
                 int32_t num_seqs, int32_t num_q_heads, int32_t max_chunk, void* k_cache,
                 void* v_cache, const pkv_cache_layout* layout, const int32_t* block_tables,
                 int32_t max_blocks_per_seq, const int32_t* context_lens, int32_t window,
-                float scale, void* out, void* stream) {
+                int32_t num_sinks, float scale, void* out, void* stream) {
   int rc = check_layout(layout, true);
   if (rc != PKV_OK) return rc;
   if (layout->dtype != PKV_FLOAT16 && layout->dtype != PKV_BFLOAT16) return PKV_ERR_UNSUPPORTED;
   if (num_seqs < 0 || num_q_heads <= 0 || max_chunk < 0 || max_blocks_per_seq < 0 ||
-      num_q_heads % layout->num_kv_heads != 0)
+      num_sinks < 0 || num_q_heads % layout->num_kv_heads != 0)
     return PKV_ERR_SHAPE;
   if (num_seqs > 65534) return PKV_ERR_UNSUPPORTED;
   if (static_cast<int64_t>(max_blocks_per_seq) * layout->block_size > 0x7fffffffLL)
@@ -477,8 +477,8 @@ int pkv_prefill(const void* q, const void* k, const void* v, const int32_t* cu_q
   return to_status(pkv::launch_prefill(
       layout->dtype, layout->head_dim, q, k, v, cu_q, num_seqs, num_q_heads, max_chunk, k_cache,
       v_cache, layout->num_blocks, layout->num_kv_heads, layout->block_size, block_tables,
-      max_blocks_per_seq, context_lens, window, scale, out, static_cast<int32_t*>(order), kmap,
-      vmap, st));
+      max_blocks_per_seq, context_lens, window, num_sinks, scale, out,
+      static_cast<int32_t*>(order), kmap, vmap, st));
 }
 
 int pkv_append_fp8(const void* k, const void* v, int32_t in_dtype, const int64_t* slot_mapping,

@@ -6,6 +6,9 @@
 // n_b new ones was appended at positions L_b - n_b .. L_b - 1; the query of
 // the chunk token at position p attends positions j <= p (and p - j < window
 // when window > 0) of the paged cache -- the cached prefix and the chunk.
+// With a window, the first num_sinks positions stay attended as well
+// ("Building a Streaming Sliding-Window Attention Engine in Pure Python",
+// Extending: the StreamingLLM attention-sink item).
 //
 // How: the chunk's K/V rows are first written to their slots (the kernel
 // below, whose extra block also orders the attention's work items), then the
@@ -22,7 +25,7 @@ constexpr int kPlanBins = 4096;  // work sizes 0 .. 4095 key tiles (larger ones 
 
 struct PlanArgs {
   int32_t* order;
-  int chunks_per_seq, tok_per_cta, window;
+  int chunks_per_seq, tok_per_cta, window, num_sinks;
 };
 
 // Work items (sequence b, token chunk c), item id b * chunks_per_seq + c, in
@@ -44,7 +47,7 @@ __device__ void plan_items(const int32_t* __restrict__ cu_q,
     const int b = static_cast<int>(i / pa.chunks_per_seq);
     const int c = static_cast<int>(i - static_cast<int64_t>(b) * pa.chunks_per_seq);
     const PrefillItem it = prefill_item(cu_q, context_lens, b, c, pa.tok_per_cta, pa.window,
-                                        max_blocks, block_size);
+                                        pa.num_sinks, max_blocks, block_size);
     const int w = it.empty ? 0 : min(it.n_tiles, kPlanBins - 1);
     return kPlanBins - 1 - w;  // the largest work first
   };
@@ -118,9 +121,9 @@ cudaError_t launch_prefill(int dtype, int head_dim, const void* q, const void* k
                            const int32_t* cu_q, int num_seqs, int num_q_heads, int max_chunk,
                            void* k_cache, void* v_cache, int64_t num_blocks, int num_kv_heads,
                            int block_size, const int32_t* block_tables, int max_blocks,
-                           const int32_t* context_lens, int window, float scale, void* out,
-                           int32_t* order, const CUtensorMap& kmap, const CUtensorMap& vmap,
-                           cudaStream_t stream) {
+                           const int32_t* context_lens, int window, int num_sinks, float scale,
+                           void* out, int32_t* order, const CUtensorMap& kmap,
+                           const CUtensorMap& vmap, cudaStream_t stream) {
   if (num_seqs == 0 || max_chunk == 0) return cudaSuccess;
   // 1) the chunk's rows to their slots; the work items' order
   const int cpr = head_dim * 2 / 16;
@@ -130,6 +133,7 @@ cudaError_t launch_prefill(int dtype, int head_dim, const void* q, const void* k
   pa.tok_per_cta = kPrefillRowsCta >> prefill_heads_log2(num_q_heads / num_kv_heads);
   pa.chunks_per_seq = (max_chunk + pa.tok_per_cta - 1) / pa.tok_per_cta;
   pa.window = window;
+  pa.num_sinks = num_sinks;
   dim3 agrid(static_cast<unsigned>((per_seq + kAppendThreads - 1) / kAppendThreads),
              num_seqs + 1);
   cudaError_t e = launch_pdl(chunk_append_kernel, agrid, dim3(kAppendThreads), 0, stream,
@@ -141,7 +145,8 @@ cudaError_t launch_prefill(int dtype, int head_dim, const void* q, const void* k
   // 2) attention over prefix + chunk on the tensor cores, items in that order
   return launch_prefill_tc(dtype, head_dim, q, cu_q, num_seqs, num_q_heads, max_chunk,
                            num_blocks, num_kv_heads, block_size, block_tables, max_blocks,
-                           context_lens, window, scale, out, order, kmap, vmap, stream);
+                           context_lens, window, num_sinks, scale, out, order, kmap, vmap,
+                           stream);
 }
 
 }  // namespace pkv

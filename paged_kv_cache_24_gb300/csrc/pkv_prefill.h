@@ -22,18 +22,27 @@ __host__ __device__ __forceinline__ int prefill_heads_log2(int group) {
 
 #ifdef __CUDACC__
 // Work item (sequence b, token chunk c) of the prefill: the chunk's tokens
-// tile0 .. tile0 + tile_n - 1 sit at positions pos0 .. pos1 and attend keys
-// k_lo .. pos1, read in units of 16 keys from unit u_first on and in tiles of
-// kPrefillTileKeys keys.  `empty`: the chunk has no token there; `len_ok`
-// false: the sequence's lengths are inconsistent (its rows become NaN).
+// tile0 .. tile0 + tile_n - 1 sit at positions pos0 .. pos1.  Their keys come
+// in two sections of 128-key tiles, each tile holding consecutive positions:
+//   sinks   (window > 0, num_sinks > 0): units 0 .. sink_units-1, which hold
+//           the sink positions before the first row's window start k_lo,
+//           padded to sink_tiles whole tiles;
+//   window  units win_u0 .. pos1 / 16 (n_win_units of them), win_u0 =
+//           max(k_lo / 16, sink_units), so that no unit is in both.
+// `empty`: the chunk has no token there; `len_ok` false: the sequence's
+// lengths are inconsistent (its rows become NaN).
 struct PrefillItem {
-  int start, n, tile0, tile_n, pos0, pos1, k_lo, u_first, n_units, n_tiles;
+  int start, n, tile0, tile_n, pos0, pos1, k_lo;
+  int sink_units, sink_tiles, win_u0, n_win_units;
+  int n_units, n_tiles;  // virtual units (sink tiles' units + window units), key tiles
   bool empty, len_ok;
 };
 
 __device__ __forceinline__ PrefillItem prefill_item(const int32_t* cu_q, const int32_t* lens,
                                                     int b, int c, int tok_per_cta, int window,
-                                                    int max_blocks, int block_size) {
+                                                    int num_sinks, int max_blocks,
+                                                    int block_size) {
+  constexpr int kTU = kPrefillTileKeys / 16;  // units per tile
   PrefillItem it{};
   it.start = cu_q[b];
   it.n = cu_q[b + 1] - it.start;
@@ -47,9 +56,14 @@ __device__ __forceinline__ PrefillItem prefill_item(const int32_t* cu_q, const i
   it.len_ok = L >= it.n && it.pos0 >= 0 &&
               static_cast<int64_t>(L) <= static_cast<int64_t>(max_blocks) * block_size;
   it.k_lo = window > 0 ? max(0, it.pos0 - window + 1) : 0;
-  it.u_first = it.k_lo / 16;
-  it.n_units = it.len_ok ? it.pos1 / 16 - it.u_first + 1 : 0;
-  it.n_tiles = (it.n_units + kPrefillTileKeys / 16 - 1) / (kPrefillTileKeys / 16);
+  if (!it.len_ok) return it;
+  const int sink_keys = (window > 0 && num_sinks > 0) ? min(num_sinks, it.k_lo) : 0;
+  it.sink_units = (sink_keys + 15) / 16;
+  it.sink_tiles = (it.sink_units + kTU - 1) / kTU;
+  it.win_u0 = max(it.k_lo / 16, it.sink_units);
+  it.n_win_units = it.pos1 / 16 - it.win_u0 + 1;  // >= 0: sink_units <= pos1 / 16 + 1
+  it.n_units = it.sink_tiles * kTU + it.n_win_units;
+  it.n_tiles = (it.n_units + kTU - 1) / kTU;
   return it;
 }
 #endif
@@ -64,9 +78,9 @@ cudaError_t launch_prefill(int dtype, int head_dim, const void* q, const void* k
                            const int32_t* cu_q, int num_seqs, int num_q_heads, int max_chunk,
                            void* k_cache, void* v_cache, int64_t num_blocks, int num_kv_heads,
                            int block_size, const int32_t* block_tables, int max_blocks,
-                           const int32_t* context_lens, int window, float scale, void* out,
-                           int32_t* order, const CUtensorMap& kmap, const CUtensorMap& vmap,
-                           cudaStream_t stream);
+                           const int32_t* context_lens, int window, int num_sinks, float scale,
+                           void* out, int32_t* order, const CUtensorMap& kmap,
+                           const CUtensorMap& vmap, cudaStream_t stream);
 
 // Attention half of the chunked prefill on the tcgen05 tensor cores (the
 // chunk's rows must already be in the pools).
@@ -74,7 +88,7 @@ cudaError_t launch_prefill_tc(int dtype, int head_dim, const void* q, const int3
                               int num_seqs, int num_q_heads, int max_chunk, int64_t num_blocks,
                               int num_kv_heads, int block_size, const int32_t* block_tables,
                               int max_blocks, const int32_t* context_lens, int window,
-                              float scale, void* out, const int32_t* order,
+                              int num_sinks, float scale, void* out, const int32_t* order,
                               const CUtensorMap& kmap, const CUtensorMap& vmap,
                               cudaStream_t stream);
 

@@ -64,6 +64,7 @@ struct TcParams {
   int64_t num_blocks;
   int num_q_heads, num_kv_heads, group;
   int head_chunk_log2, num_head_chunks, chunks_per_seq;
+  int num_sinks;  // attention sinks (0 without a window)
   int max_blocks, block_size, window;
   float scale_log2;
 };
@@ -98,7 +99,9 @@ __device__ __forceinline__ uint32_t bf16x2_to_f16x2(uint32_t w, __half2& amax) {
   return h;
 }
 
-template <typename T, int D>
+// kSinks: the key range has a sink section (window > 0, num_sinks > 0); the
+// instantiation without it compiles the sink tests away.
+template <typename T, int D, bool kSinks>
 __global__ void __launch_bounds__(kTThreads, 1)
 prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
                   const TcParams p) {
@@ -128,12 +131,27 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
   const int lg = p.head_chunk_log2, gc = 1 << lg;
   const int tok_per_cta = kRowsCta >> lg;
   const PrefillItem it = prefill_item(p.cu_q, p.context_lens, b, item - b * p.chunks_per_seq,
-                                      tok_per_cta, p.window, p.max_blocks, p.block_size);
+                                      tok_per_cta, p.window, p.num_sinks, p.max_blocks,
+                                      p.block_size);
   if (it.empty) return;
   const int start = it.start, tile0 = it.tile0, tile_n = it.tile_n;
-  const int pos0 = it.pos0, pos1 = it.pos1, k_lo = it.k_lo, u_first = it.u_first;
+  const int pos0 = it.pos0, pos1 = it.pos1, k_lo = it.k_lo;
   const int n_units = it.n_units, n_tiles = it.n_tiles;
+  const int sink_tiles = kSinks ? it.sink_tiles : 0, sink_units = kSinks ? it.sink_units : 0;
+  const int win_u0 = it.win_u0;
+  const int sink_end = sink_units * kUnitTokens;  // keys of the sink section
+  const int num_sinks = kSinks ? p.num_sinks : 0;
   const bool len_ok = it.len_ok;
+  // first key position of key tile j (the sink tiles, then the window tiles)
+  auto tile_t0 = [&](int j) {
+    return j < sink_tiles ? j * kTKeys : (win_u0 + (j - sink_tiles) * kTUnits) * kUnitTokens;
+  };
+  // keys some row of the CTA attends and tile j holds: at most pos1, inside the
+  // window of some row or a sink, and (sink tiles) inside the sink section
+  auto key_kept = [&](int j, int kp) {
+    return kp <= pos1 && (j >= sink_tiles || kp < sink_end) &&
+           (p.window <= 0 || kp >= k_lo || kp < num_sinks);
+  };
 
   const uint32_t raw_addr = smem_u32(smem_raw);
   const uint32_t base = (raw_addr + 1023u) & ~1023u;
@@ -198,10 +216,18 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
         tma_prefetch_desc(&kmap);
         tma_prefetch_desc(&vmap);
       }
-      // page row of unit u of the key range: -1 past the range, -2 invalid page
+      // page row of virtual unit u (the sink tiles' units, then the window's):
+      // -1 past the range or in the sink tiles' padding, -2 invalid page
       auto page_row = [&](int u) -> int {
         if (u >= n_units) return -1;
-        const int t0 = (u_first + u) * kUnitTokens;
+        int t0;
+        if constexpr (kSinks) {
+          const int su = sink_tiles * kTUnits;
+          if (u < su && u >= sink_units) return -1;
+          t0 = (u < su ? u : win_u0 + (u - su)) * kUnitTokens;
+        } else {
+          t0 = (win_u0 + u) * kUnitTokens;
+        }
         const int32_t pb = __ldg(p.block_tables + static_cast<int64_t>(b) * p.max_blocks +
                                  t0 / p.block_size);
         if (pb < 0 || pb >= p.num_blocks) return -2;
@@ -253,14 +279,16 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
       __half2 amax = __float2half2_rn(0.f);
       for (int j = 0; j < n_tiles; ++j) {
         if (!mbar_wait_bounded(smem_u32(&v_full[j % SV]), (j / SV) & 1, kWaitLimit)) bad = true;
-        const int t0 = (u_first + j * kTUnits) * kUnitTokens;
+        const int t0 = tile_t0(j);
         const uint32_t vt = v_addr(j);
+        // a window tile wholly inside [k_lo, pos1] keeps every key
+        const bool whole = j >= sink_tiles && t0 >= k_lo && t0 + kTKeys - 1 <= pos1;
         if (kBf16) {
 #pragma unroll 4
           for (int u = ct; u < Lay::kKVTile / 16; u += kPrepThreads) {  // 16-byte chunks
             const int kp = t0 + ((u & (kTKeys * 8 - 1)) >> 3);
             uint4 x = ld_shared_v4(vt + u * 16);
-            if (kp < k_lo || kp > pos1) {
+            if (!whole && (kSinks ? !key_kept(j, kp) : (kp < k_lo || kp > pos1))) {
               x = make_uint4(0u, 0u, 0u, 0u);
             } else {
               x.x = bf16x2_to_f16x2(x.x, amax);
@@ -270,10 +298,10 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
             }
             st_shared_v4(vt + u * 16, x);
           }
-        } else if (t0 < k_lo || t0 + kTKeys - 1 > pos1) {
+        } else if (!whole) {
           for (int r = ct; r < kTKeys; r += kPrepThreads) {
             const int kp = t0 + r;
-            if (kp >= k_lo && kp <= pos1) continue;
+            if (kSinks ? key_kept(j, kp) : (kp >= k_lo && kp <= pos1)) continue;
 #pragma unroll
             for (int kb = 0; kb < Lay::kKBlocks; ++kb)
 #pragma unroll
@@ -370,7 +398,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
   const float sl = raw_max ? p.scale_log2 : 1.f;
   float m_run = -INFINITY, l_run = 0.f;
   for (int j = 0; j < n_tiles; ++j) {
-    const int t0 = (u_first + j * kTUnits) * kUnitTokens;
+    const int t0 = kSinks ? tile_t0(j) : (win_u0 + j * kTUnits) * kUnitTokens;
     if (!mbar_wait_bounded(smem_u32(&s_full[t]), j & 1, kWaitLimit)) bad = true;
     tc_fence_after();
     float s[kTKeys];
@@ -380,13 +408,27 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
       for (int c = 0; c < kTKeys; ++c) s[c] *= p.scale_log2;
     }
     // keys this row may not see -> -inf
-    const bool edge = t0 + kTKeys - 1 > rpos || (p.window > 0 && t0 <= rpos - p.window);
+    // (sink tiles always take the masked path; for the window tiles the test
+    // below ignores the sinks, which can only keep keys it would mask)
+    const bool edge = (kSinks && j < sink_tiles) || t0 + kTKeys - 1 > rpos ||
+                      (p.window > 0 && t0 <= rpos - p.window);
     if (__any_sync(0xffffffffu, edge)) {
+      if constexpr (kSinks) {
+        const int kend = j < sink_tiles ? sink_end : 0x7fffffff;  // past the sink section
 #pragma unroll
-      for (int c = 0; c < kTKeys; ++c) {
-        const int kp = t0 + c;
-        const bool valid = kp <= rpos && (p.window <= 0 || rpos - kp < p.window);
-        s[c] = valid ? s[c] : -INFINITY;
+        for (int c = 0; c < kTKeys; ++c) {
+          const int kp = t0 + c;
+          const bool valid = kp <= rpos && kp < kend &&
+                             (p.window <= 0 || rpos - kp < p.window || kp < num_sinks);
+          s[c] = valid ? s[c] : -INFINITY;
+        }
+      } else {
+#pragma unroll
+        for (int c = 0; c < kTKeys; ++c) {
+          const int kp = t0 + c;
+          const bool valid = kp <= rpos && (p.window <= 0 || rpos - kp < p.window);
+          s[c] = valid ? s[c] : -INFINITY;
+        }
       }
     }
     float mp[8];
@@ -471,11 +513,11 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
                  "r"(Lay::kTmemCols));
 }
 
-template <typename T, int D>
+template <typename T, int D, bool kSinks>
 cudaError_t launch_t(const CUtensorMap& kmap, const CUtensorMap& vmap, const TcParams& p,
                      int max_chunk, int num_seqs, cudaStream_t stream) {
   using Lay = TcLayout<D>;
-  auto kern = prefill_tc_kernel<T, D>;
+  auto kern = prefill_tc_kernel<T, D, kSinks>;
   const int smem = 1024 + Lay::kSmemBytes;
   // per device, once: the shared-memory opt-in, and a check that the block
   // is launched with the registers the warpgroups' split hands out (a larger
@@ -508,7 +550,7 @@ cudaError_t launch_prefill_tc(int dtype, int head_dim, const void* q, const int3
                               int num_seqs, int num_q_heads, int max_chunk, int64_t num_blocks,
                               int num_kv_heads, int block_size, const int32_t* block_tables,
                               int max_blocks, const int32_t* context_lens, int window,
-                              float scale, void* out, const int32_t* order,
+                              int num_sinks, float scale, void* out, const int32_t* order,
                               const CUtensorMap& kmap, const CUtensorMap& vmap,
                               cudaStream_t stream) {
   TcParams p{};
@@ -529,14 +571,21 @@ cudaError_t launch_prefill_tc(int dtype, int head_dim, const void* q, const int3
   p.max_blocks = max_blocks;
   p.block_size = block_size;
   p.window = window;
+  p.num_sinks = window > 0 ? num_sinks : 0;
+  const bool sinks = p.num_sinks > 0;
   p.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
   if (dtype == 1) {
-    if (head_dim == 128) return launch_t<__half, 128>(kmap, vmap, p, max_chunk, num_seqs, stream);
-    return launch_t<__half, 64>(kmap, vmap, p, max_chunk, num_seqs, stream);
+    if (head_dim == 128)
+      return sinks ? launch_t<__half, 128, true>(kmap, vmap, p, max_chunk, num_seqs, stream)
+                   : launch_t<__half, 128, false>(kmap, vmap, p, max_chunk, num_seqs, stream);
+    return sinks ? launch_t<__half, 64, true>(kmap, vmap, p, max_chunk, num_seqs, stream)
+                 : launch_t<__half, 64, false>(kmap, vmap, p, max_chunk, num_seqs, stream);
   }
   if (head_dim == 128)
-    return launch_t<__nv_bfloat16, 128>(kmap, vmap, p, max_chunk, num_seqs, stream);
-  return launch_t<__nv_bfloat16, 64>(kmap, vmap, p, max_chunk, num_seqs, stream);
+    return sinks ? launch_t<__nv_bfloat16, 128, true>(kmap, vmap, p, max_chunk, num_seqs, stream)
+                 : launch_t<__nv_bfloat16, 128, false>(kmap, vmap, p, max_chunk, num_seqs, stream);
+  return sinks ? launch_t<__nv_bfloat16, 64, true>(kmap, vmap, p, max_chunk, num_seqs, stream)
+               : launch_t<__nv_bfloat16, 64, false>(kmap, vmap, p, max_chunk, num_seqs, stream);
 }
 
 }  // namespace pkv

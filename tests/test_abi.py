@@ -163,3 +163,25 @@ def test_quantised_pool_argument_checks(pkv_lib):
     assert app("pkv_append_int8", 4, n=-1) == SHAPE
     assert app("pkv_append_int8", 4, n=0) == OK
     assert _decode(pkv, _layout(pkv, dt=5)) == DTYPE
+
+
+def test_prefill_argument_checks(pkv_lib):
+    """pkv_prefill rejects bad shapes before touching memory: 8-bit or fp32
+    pools, a negative sink count, more than 65534 sequences; no sequences or an
+    empty chunk is a no-op."""
+    lib = pkv_lib.load_library()
+
+    def call(dt=1, num_seqs=4, max_chunk=64, sinks=0, window=16):
+        lay = _layout(pkv_lib, dt=dt)
+        return lib.pkv_prefill(FAKE, FAKE, FAKE, FAKE, num_seqs, 32, max_chunk, FAKE, FAKE,
+                               ctypes.byref(lay), FAKE, 8, FAKE, window, sinks,
+                               ctypes.c_float(0.1), FAKE, None)
+
+    assert call(dt=0) == UNSUP
+    assert call(dt=3) == UNSUP
+    assert call(dt=4) == UNSUP
+    assert call(sinks=-1) == SHAPE
+    assert call(num_seqs=-1) == SHAPE
+    assert call(num_seqs=65535) == UNSUP
+    assert call(num_seqs=0) == OK
+    assert call(max_chunk=0) == OK

@@ -99,6 +99,82 @@ def test_prefill_matches_oracle(pkv_lib, oracle_lib, name, dtype, hq, hkv, d, bs
     assert (err <= tol).all(), f"max err {err.max():.3e}"
 
 
+SINK_CASES = [
+    # name, dtype, hq, hkv, d, bs, prefixes, chunks, window, sinks
+    ("w37_s4", torch.bfloat16, 8, 2, 128, 16, [0, 100, 7], [80, 50, 30], 37, 4),
+    # more sinks than the window, not a whole unit
+    ("w5_s20_long", torch.bfloat16, 4, 4, 128, 16, [0, 200], [300, 260], 5, 20),
+    ("w16_s16_d64", torch.float16, 8, 2, 64, 16, [100], [500], 16, 16),
+    # sinks reaching into the window of the chunk's first rows
+    ("w100_s150_bs32", torch.float16, 8, 2, 128, 32, [400, 10], [300, 200], 100, 150),
+    ("w1_s1", torch.float16, 4, 4, 128, 16, [5, 0], [20, 33], 1, 1),
+    # the sink tile far ahead of the window tiles
+    ("w300_s3_far", torch.bfloat16, 16, 2, 128, 16, [3000], [700], 300, 3),
+    ("w2000_s7_g4", torch.bfloat16, 8, 2, 128, 16, [3000, 1], [300, 700], 2000, 7),
+    ("w64_s130_g8", torch.float16, 16, 2, 128, 16, [900, 129], [200, 64], 64, 130),
+]
+
+
+def _poison_unattended(w, prefixes, chunks, window, sinks):
+    """NaN into every prefix slot no chunk row attends: past the sinks and
+    before the first chunk row's window."""
+    bs = w.spec.block_size
+    bt = w.block_tables.cpu().numpy()
+    slots = []
+    for b, (p, n) in enumerate(zip(prefixes, chunks)):
+        first_lo = max(0, p - window + 1)
+        slots += [oracle.slot_for_position(bt[b], bs, t) for t in range(sinks, first_lo)]
+    if slots:
+        s = np.array(slots, np.int64)
+        blk = torch.from_numpy(s // bs).to("cuda")
+        row = torch.from_numpy(s % bs).to("cuda")
+        w.k_cache[blk, :, row] = float("nan")
+        w.v_cache[blk, :, row] = float("nan")
+
+
+@pytest.mark.parametrize("name,dtype,hq,hkv,d,bs,prefixes,chunks,window,sinks", SINK_CASES,
+                         ids=[c[0] for c in SINK_CASES])
+def test_prefill_with_sinks_matches_oracle(pkv_lib, oracle_lib, name, dtype, hq, hkv, d, bs,
+                                           prefixes, chunks, window, sinks):
+    w, q, k, v, cu, lens = _prefill_case(dtype, hq, hkv, d, bs, prefixes, chunks, window,
+                                         seed=len(name) + 100)
+    _poison_unattended(w, prefixes, chunks, window, sinks)
+    kc, vc = w.k_cache.cpu(), w.v_cache.cpu()
+    bt = w.block_tables.cpu().numpy()
+    lens_h = lens.cpu().numpy()
+    slots = [oracle.slot_for_position(bt[b], bs, lens_h[b] - n + i)
+             for b, n in enumerate(chunks) for i in range(n)]
+    oracle.append(k.cpu(), v.cpu(), np.array(slots, np.int64), kc, vc)
+    ref = oracle.prefill(q.cpu(), cu.cpu().numpy(), kc, vc, bt, lens_h, window, w.scale,
+                         num_sinks=sinks)
+    out = torch.full_like(q, float("nan"))
+    pkv_lib.pkv_prefill(q, k, v, cu, w.k_cache, w.v_cache, w.block_tables, lens, window,
+                        w.scale, max_chunk=max(chunks), out=out, num_sinks=sinks)
+    torch.cuda.synchronize()
+    assert torch.equal(_bits(w.k_cache.cpu()), _bits(kc))
+    assert torch.equal(_bits(w.v_cache.cpu()), _bits(vc))
+    g = out.double().cpu().numpy()
+    assert not np.isnan(g).any()
+    err = np.abs(g - ref)
+    tol = 2e-3 + 0.5 * torch.finfo(dtype).eps * np.abs(ref)
+    assert (err <= tol).all(), f"max err {err.max():.3e}"
+
+
+def test_prefill_last_row_equals_decode_with_sinks(pkv_lib):
+    """The last chunk token attends exactly what a decode of length L with the
+    same window and sinks attends."""
+    w, q, k, v, cu, lens = _prefill_case(torch.bfloat16, 8, 2, 128, 16, [700, 90], [100, 40], 0,
+                                         seed=5)
+    out = pkv_lib.pkv_prefill(q, k, v, cu, w.k_cache, w.v_cache, w.block_tables, lens, 50,
+                              w.scale, max_chunk=100, num_sinks=6)
+    last = cu[1:].long() - 1
+    dec = pkv_lib.pkv_decode(q[last].contiguous(), w.k_cache, w.v_cache, w.block_tables, lens, 50,
+                             w.scale, num_sinks=6)
+    torch.cuda.synchronize()
+    diff = (out[last].double() - dec.double()).abs().max().item()
+    assert diff <= 2e-3 + 0.5 * torch.finfo(torch.bfloat16).eps * dec.double().abs().max().item()
+
+
 def test_prefill_last_row_equals_decode(pkv_lib):
     """The last chunk token attends exactly what a decode of length L attends."""
     w, q, k, v, cu, lens = _prefill_case(torch.bfloat16, 8, 2, 128, 16, [100, 37], [40, 12], 0,

@@ -1,6 +1,6 @@
 """Seeded random sweep of the CUDA path against the oracle: decode over fp32,
 fp16, bf16, FP8 and INT8 pools (separate or fused append), and the chunked
-prefill, on shapes drawn from the supported ranges -- head dims, GQA groups,
+prefill (with windows and sinks), on shapes drawn from the supported ranges -- head dims, GQA groups,
 page sizes, ragged lengths, windows, attention sinks and split sizes.  Every
 output and the whole pool after the append are compared; a failing case
 names its seed."""
@@ -119,13 +119,15 @@ def _prefill_case(seed):
     prefixes = [int(x) for x in r.integers(0, 1500, B)]
     chunks = [int(x) for x in r.integers(1, 400, B)]
     window = 0 if r.random() < 0.5 else int(r.integers(1, 700))
-    return dtype, d, hkv, g, bs, prefixes, chunks, window
+    sinks = 0 if window == 0 else int(r.choice([0, 0, 1, 4, 19, 200]))
+    return dtype, d, hkv, g, bs, prefixes, chunks, window, sinks
 
 
-@pytest.mark.parametrize("seed", range(16))
+@pytest.mark.parametrize("seed", range(24))
 def test_random_prefill(pkv_lib, oracle_lib, seed):
-    dtype, d, hkv, g, bs, prefixes, chunks, window = _prefill_case(seed)
-    what = f"seed {seed}: {dtype} d={d} hkv={hkv} g={g} bs={bs} {prefixes} {chunks} w={window}"
+    dtype, d, hkv, g, bs, prefixes, chunks, window, sinks = _prefill_case(seed)
+    what = (f"seed {seed}: {dtype} d={d} hkv={hkv} g={g} bs={bs} {prefixes} {chunks} "
+            f"w={window} sinks={sinks}")
     lens = [p + n for p, n in zip(prefixes, chunks)]
     spec = config_spec(0, dtype=dtype, num_seqs=len(lens), num_q_heads=hkv * g,
                        num_kv_heads=hkv, head_dim=d, block_size=bs, lens=lens,
@@ -150,10 +152,10 @@ def test_random_prefill(pkv_lib, oracle_lib, seed):
     kc_h, vc_h = w.k_cache.cpu(), w.v_cache.cpu()
     oracle.append(k.cpu(), v.cpu(), slots, kc_h, vc_h)
     ref = oracle.prefill(q.cpu(), cu.cpu().numpy(), kc_h, vc_h, bt, np.array(lens, np.int32),
-                         window, w.scale)
+                         window, w.scale, num_sinks=sinks)
     out = torch.full_like(q, float("nan"))
     pkv_lib.pkv_prefill(q, k, v, cu, w.k_cache, w.v_cache, w.block_tables, L, window, w.scale,
-                        max_chunk=max(chunks), out=out)
+                        max_chunk=max(chunks), out=out, num_sinks=sinks)
     torch.cuda.synchronize()
     assert torch.equal(_bits(w.k_cache.cpu()), _bits(kc_h)), what
     assert torch.equal(_bits(w.v_cache.cpu()), _bits(vc_h)), what
