@@ -76,6 +76,19 @@ typedef struct pkv_cache_layout {
 } pkv_cache_layout;
 
 /*
+ * pkv_stage_copy -- copy `bytes` from src to dst with a kernel on `stream`.
+ *   Not an operation of the pages: it moves a decode step's staged inputs
+ *   from pinned host memory to the device and its output back.  Either side
+ *   may be device memory, managed memory or pinned host memory (the kernel
+ *   uses its device-side address); on a host whose pinned memory the GPU
+ *   reaches over a coherent link this finishes small transfers well before a
+ *   copy-engine copy.  Both addresses 16-byte aligned; any byte count.
+ *   Pageable or unknown host memory: PKV_ERR_UNSUPPORTED (nothing launched).
+ *   The ranges must not overlap.  Asynchronous, like every call here.
+ */
+int pkv_stage_copy(void* dst, const void* src, int64_t bytes, void* stream);
+
+/*
  * pkv_slot_mapping -- slot of each sequence's new token.
  *   ("Build a Paged KV Cache in Pure Python", Step 3, PagedKVCache.append)
  *   slot_mapping[b] = block_tables[b][pos / bs] * bs + pos % bs, pos =

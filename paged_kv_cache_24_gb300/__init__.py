@@ -15,8 +15,11 @@ Public API (thin wrappers over the C ABI of ``libpkv.so``, see include/pkv.h):
   and ``pkv_append_int8(...)`` -- quantising append into FP8 E4M3 (uint8) or
   INT8 (int8) pools, which ``pkv_decode`` reads when given the row scales;
 * ``pkv_prefill(q, k, v, cu_q, k_cache, v_cache, block_tables, context_lens,
-  window, scale, max_chunk)`` -- chunked prefill: append packed chunks and
-  compute their causal (windowed) attention over the paged cache.
+  window, scale, max_chunk, num_sinks=0)`` -- chunked prefill: append packed
+  chunks and compute their causal (windowed, with sinks) attention over the
+  paged cache;
+* ``pkv_stage_copy(dst, src)`` -- a kernel copy between device memory and
+  pinned host memory (DecodeStep's host transfers).
 
 ``DecodeStep`` packages one serving step (slot mapping, append, decode) as a
 CUDA graph fed from a pinned host staging buffer.
@@ -27,12 +30,12 @@ benchmark.
 """
 from ._binding import (CacheLayout, DecodeOptions, PkvError, cache_layout, library_path, load_library,
                        pkv_append, pkv_append_decode, pkv_append_fp8, pkv_append_int8, pkv_decode, pkv_prefill, pkv_decode_plan, pkv_release_workspaces,
-                       pkv_slot_mapping, status_string)
+                       pkv_slot_mapping, pkv_stage_copy, status_string, PKV_ERR_UNSUPPORTED)
 from .step import DecodeStep
 
 __all__ = [
     "DecodeStep", "DecodeOptions", "CacheLayout", "PkvError", "cache_layout", "library_path", "load_library", "pkv_append",
     "pkv_append_decode", "pkv_append_fp8", "pkv_append_int8", "pkv_prefill",
-    "pkv_decode", "pkv_decode_plan", "pkv_release_workspaces", "pkv_slot_mapping",
+    "pkv_decode", "pkv_decode_plan", "pkv_release_workspaces", "pkv_slot_mapping", "pkv_stage_copy", "PKV_ERR_UNSUPPORTED",
     "status_string",
 ]

@@ -16,6 +16,7 @@ import torch
 from . import _build
 
 PKV_OK = 0
+PKV_ERR_UNSUPPORTED = 4
 PKV_FP8_E4M3 = 3
 PKV_INT8 = 4
 _DTYPES = {torch.float32: 0, torch.float16: 1, torch.bfloat16: 2}
@@ -71,6 +72,7 @@ def load_library():
         lay = ctypes.POINTER(CacheLayout)
         sig = {
             "pkv_slot_mapping": [vp, i32, i32, vp, i32, vp, vp],
+            "pkv_stage_copy": [vp, vp, i64, vp],
             "pkv_append": [vp, vp, vp, i64, vp, vp, lay, vp],
             "pkv_decode": [vp, i32, i32, vp, vp, lay, vp, i32, vp, i32, f32, vp, vp],
             "pkv_decode_split": [vp, i32, i32, vp, vp, lay, vp, i32, vp, i32, f32, vp, i32, vp],
@@ -154,6 +156,22 @@ def _on_cuda(*ts) -> None:
     for t in ts:
         if t is not None and t.device.type != "cuda":
             raise ValueError("libpkv operates on CUDA tensors only")
+
+
+def pkv_stage_copy(dst: torch.Tensor, src: torch.Tensor, nbytes: int | None = None,
+                   stream=None) -> int:
+    """Copy the first nbytes (default: all) of src into dst with a kernel; either
+    tensor may live in pinned host memory.  Returns the library's status
+    (PKV_ERR_UNSUPPORTED = 4 when a side is pageable host memory; nothing is
+    launched then); other errors raise."""
+    _require(src.is_contiguous() and dst.is_contiguous(), "src and dst must be contiguous")
+    n = src.numel() * src.element_size() if nbytes is None else int(nbytes)
+    _require(0 <= n <= src.numel() * src.element_size() and n <= dst.numel() * dst.element_size(),
+             "nbytes exceeds a tensor")
+    rc = load_library().pkv_stage_copy(_ptr(dst), _ptr(src), n, _stream(stream))
+    if rc != PKV_ERR_UNSUPPORTED:
+        _check("pkv_stage_copy", rc)
+    return rc
 
 
 def pkv_slot_mapping(block_tables: torch.Tensor, positions: torch.Tensor, block_size: int,

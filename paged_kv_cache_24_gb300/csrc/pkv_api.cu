@@ -11,6 +11,7 @@
 #include "pkv.h"
 #include "pkv_internal.h"
 #include "pkv_prefill.h"
+#include "pkv_stage.h"
 
 namespace {
 
@@ -372,6 +373,33 @@ int pkv_slot_mapping(const int32_t* block_tables, int32_t num_seqs, int32_t max_
   return to_status(pkv::launch_slot_mapping(block_tables, num_seqs, max_blocks_per_seq, positions,
                                             block_size, slot_mapping,
                                             static_cast<cudaStream_t>(stream)));
+}
+
+// The address a kernel uses for p: p itself for device or managed memory, the
+// device-side address of pinned host memory; nullptr when no kernel may touch p
+// (pageable host memory, or no CUDA allocation at all).
+static const void* device_side(const void* p) {
+  cudaPointerAttributes a{};
+  if (cudaPointerGetAttributes(&a, p) != cudaSuccess) {
+    cudaGetLastError();  // not a CUDA pointer: clear the error
+    return nullptr;
+  }
+  if (a.type == cudaMemoryTypeDevice || a.type == cudaMemoryTypeManaged) return p;
+  if (a.type == cudaMemoryTypeHost) return a.devicePointer;
+  return nullptr;
+}
+
+int pkv_stage_copy(void* dst, const void* src, int64_t bytes, void* stream) {
+  if (bytes < 0) return PKV_ERR_SHAPE;
+  if (bytes == 0) return PKV_OK;
+  if (!dst || !src) return PKV_ERR_NULL;
+  if (!aligned16(dst) || !aligned16(src)) return PKV_ERR_ALIGNMENT;
+  const void* d = device_side(dst);
+  const void* s = device_side(src);
+  if (!d || !s) return PKV_ERR_UNSUPPORTED;
+  return to_status(pkv::launch_stage_copy(const_cast<void*>(d), s, bytes,
+                                          sm_count_of_current_device(),
+                                          static_cast<cudaStream_t>(stream)));
 }
 
 int pkv_append(const void* k, const void* v, const int64_t* slot_mapping, int64_t num_tokens,

@@ -8,7 +8,9 @@ launch; ``fused=False`` runs the three separate calls.
 A step's host inputs -- the queries, the new tokens' K and V, their positions,
 the context lengths and (optionally) the block tables -- are packed into one
 pinned staging buffer and reach the device in a single copy; the attention
-output comes back in another.  Between them the graph replays
+output comes back in another.  Both copies are ``pkv_stage_copy`` kernels,
+which read and write the pinned buffers directly (the copy engine where the
+GPU cannot reach them).  Between them the graph replays
 ``pkv_slot_mapping``, ``pkv_append`` and ``pkv_decode`` exactly as the eager
 calls would run them.  The K/V pools stay resident on the device.
 
@@ -28,7 +30,7 @@ import torch
 
 from ._binding import (cache_layout, pkv_append, pkv_append_decode, pkv_append_fp8,
                        pkv_append_int8,
-                       pkv_decode, pkv_slot_mapping)
+                       pkv_decode, pkv_slot_mapping, pkv_stage_copy, PKV_ERR_UNSUPPORTED)
 
 _ALIGN = 256
 
@@ -102,9 +104,16 @@ class DecodeStep:
                     self._enqueue(i)
                 self.graphs.append(g)
 
+    def _copy(self, dst, src, n):
+        # a kernel copy where the GPU reaches the pinned buffer directly (fewer
+        # microseconds of fixed cost than a copy-engine transfer of these
+        # sizes), else the copy engine
+        if pkv_stage_copy(dst, src, n) == PKV_ERR_UNSUPPORTED:
+            dst.view(-1)[:n // dst.element_size()].copy_(
+                src.view(-1)[:n // src.element_size()], non_blocking=True)
+
     def _enqueue(self, i):
-        n = self._staged_bytes
-        self._dev_buf[:n].copy_(self._host_bufs[i][:n], non_blocking=True)
+        self._copy(self._dev_buf, self._host_bufs[i], self._staged_bytes)
         dv = self.device
         if self.fused:
             # the new token sits at position context_lens - 1: one launch
@@ -123,7 +132,7 @@ class DecodeStep:
             pkv_decode(dv["q"], self.k_cache, self.v_cache, dv["block_tables"],
                        dv["context_lens"], self.window, self.scale, out=self.out,
                        k_scale=self.k_scale, v_scale=self.v_scale)
-        self.host_out.copy_(self.out, non_blocking=True)
+        self._copy(self.host_out, self.out, self.d2h_bytes)
 
     def run(self, i: int = 0, wait: bool = True) -> torch.Tensor:
         """Copy staging buffer i in, run the step, copy the output back."""

@@ -185,3 +185,14 @@ def test_prefill_argument_checks(pkv_lib):
     assert call(num_seqs=65535) == UNSUP
     assert call(num_seqs=0) == OK
     assert call(max_chunk=0) == OK
+
+
+def test_stage_copy_argument_checks(pkv_lib):
+    """pkv_stage_copy checks its arguments before any CUDA call."""
+    lib = pkv_lib.load_library()
+    assert lib.pkv_stage_copy(FAKE, FAKE, -1, None) == SHAPE
+    assert lib.pkv_stage_copy(FAKE, FAKE, 0, None) == OK
+    assert lib.pkv_stage_copy(None, FAKE, 64, None) == NULL
+    assert lib.pkv_stage_copy(FAKE, None, 64, None) == NULL
+    assert lib.pkv_stage_copy(FAKE + 8, FAKE, 64, None) == ALIGN
+    assert lib.pkv_stage_copy(FAKE, FAKE + 4, 64, None) == ALIGN
