@@ -3,21 +3,24 @@
 //
 // What is computed: see pkv_prefill.cu ("Building a Streaming Sliding-Window
 // Attention Engine in Pure Python", Step 3, prefill_attention: the query at
-// position p attends keys j <= p with p - j < window, softmax per row).
+// position p attends keys j <= p with p - j < window, softmax per row; with
+// a window, the first num_sinks positions too -- the attention sinks of that
+// page's Extending list).
 //
 // How.  A CTA owns 256 query rows of one (sequence, kv head): (token, GQA
 // head) pairs, so every K/V page it reads serves the whole group.  CTAs take
 // the (sequence, token chunk) items in the order the planner gave them
 // (most key tiles first), the kv heads of one item side by side.  The rows
 // form two tiles of 128 (one per TMEM lane), worked on in ping-pong over
-// tiles of 128 keys:
+// tiles of 128 keys (with sinks: the sink tiles first, then the window's):
 //   warp 9       (load)    TMA of the 16-key K and V units of each key tile
-//                          into two rings of stages (128-byte swizzle);
+//                          into two rings of stages (128-byte swizzle), lane
+//                          i issuing unit i's copies;
 //   warps 10-11  (V prep)  turn each landed V tile into fp16 in place (bf16
 //                          caches) and zero the rows of keys no row of the CTA
 //                          may see, so garbage (even NaN) in unused slots
 //                          cannot leak through a zero weight;
-//   warp 8       (MMA)     one thread issues S_t = Q_t K^T (M 128, N 128, both
+//   warp 8       (MMA)     one thread waits and issues S_t = Q_t K^T (M 128, N 128, both
 //                          operands K-major in shared memory) and
 //                          O_t += P_t V (A = P_t read from TMEM, B = V read
 //                          MN-major from its stage);
