@@ -347,8 +347,10 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
           issue_s(1, 0);
           umma_commit(smem_u32(&k_empty[0]));
         }
+        // V(j) and K(j+1) are waited for by tile 0's softmax warps before
+        // they announce P_0(j): acquiring p_full[0] orders them before the
+        // products below, so this thread waits only for the two P tiles.
         for (int j = 0; j < n_tiles; ++j) {
-          if (!mbar_wait_bounded(smem_u32(&v_ready[j % SV]), (j / SV) & 1, kWaitLimit)) bad = true;
           // V: keys are the K dimension (8-row groups 1 KB apart, 16 keys a
           // step), head dims the N dimension (64-column blocks a tile apart)
           const uint64_t v0 = umma_sdesc_sw128(v_addr(j), kTKeys * 128, 1024);
@@ -366,7 +368,6 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
             if (j + 1 < n_tiles) {
               // S_t(j+1) overwrites P_t(j) after the product above read it (one
               // issuing thread: the tensor pipe takes them in order)
-              if (t == 0) wait_k(j + 1);
               issue_s(t, j + 1);
               if (t == 1) umma_commit(smem_u32(&k_empty[(j + 1) % SK]));
             }
@@ -477,6 +478,12 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
     l_run = l_run * alpha + ((a01.x + a01.y) + (a23.x + a23.y));
     tmem_wait_st();
     tc_fence_before();
+    if (t == 0) {
+      if (!mbar_wait_bounded(smem_u32(&v_ready[j % SV]), (j / SV) & 1, kWaitLimit)) bad = true;
+      if (j + 1 < n_tiles &&
+          !mbar_wait_bounded(smem_u32(&k_full[(j + 1) % SK]), ((j + 1) / SK) & 1, kWaitLimit))
+        bad = true;
+    }
     mbar_arrive(smem_u32(&p_full[t]));
   }
   if (n_tiles > 0) {
