@@ -363,7 +363,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
               umma_f16_ts(tmem + Lay::o_col(t), tmem + Lay::s_col(t) + kk * 8,
                           v0 + static_cast<uint64_t>((kk * 16 * 128) >> 4), kIdO,
                           (j > 0 || kk > 0) ? 1u : 0u);
-            umma_commit(smem_u32(&o_done[t]));
+            if (j + 1 == n_tiles) umma_commit(smem_u32(&o_done[t]));  // O_t final
             if (t == 1) umma_commit(smem_u32(&v_empty[j % SV]));
             if (j + 1 < n_tiles) {
               // S_t(j+1) overwrites P_t(j) after the product above read it (one
@@ -487,7 +487,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
     mbar_arrive(smem_u32(&p_full[t]));
   }
   if (n_tiles > 0) {
-    if (!mbar_wait_bounded(smem_u32(&o_done[t]), (n_tiles - 1) & 1, kWaitLimit)) bad = true;
+    if (!mbar_wait_bounded(smem_u32(&o_done[t]), 0, kWaitLimit)) bad = true;
     tc_fence_after();
   }
 
