@@ -219,20 +219,24 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
         tma_prefetch_desc(&kmap);
         tma_prefetch_desc(&vmap);
       }
-      // page row of virtual unit u (the sink tiles' units, then the window's):
-      // -1 past the range or in the sink tiles' padding, -2 invalid page
-      auto page_row = [&](int u) -> int {
+      // First key position of virtual unit u (the sink tiles' units, then the
+      // window's), -1 past the range or in the sink tiles' padding.
+      auto unit_t0 = [&](int u) -> int {
         if (u >= n_units) return -1;
-        int t0;
         if constexpr (kSinks) {
           const int su = sink_tiles * kTUnits;
           if (u < su && u >= sink_units) return -1;
-          t0 = (u < su ? u : win_u0 + (u - su)) * kUnitTokens;
+          return (u < su ? u : win_u0 + (u - su)) * kUnitTokens;
         } else {
-          t0 = (win_u0 + u) * kUnitTokens;
+          return (win_u0 + u) * kUnitTokens;
         }
-        const int32_t pb = __ldg(p.block_tables + static_cast<int64_t>(b) * p.max_blocks +
-                                 t0 / p.block_size);
+      };
+      auto table_entry = [&](int t0) -> int32_t {
+        return __ldg(p.block_tables + static_cast<int64_t>(b) * p.max_blocks + t0 / p.block_size);
+      };
+      // page row of the unit at t0 with block id pb: -1 past the range, -2 invalid page
+      auto page_y = [&](int t0, int32_t pb) -> int {
+        if (t0 < 0) return -1;
         if (pb < 0 || pb >= p.num_blocks) return -2;
         return (pb * p.num_kv_heads + hkv) * p.block_size + (t0 % p.block_size);
       };
@@ -254,10 +258,17 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
         }
       };
       // lane i < 8 holds the page row of unit i of the tile (-1 elsewhere)
-      int y_next = (lane < kTUnits && n_tiles > 0) ? page_row(lane) : -1;
+      int y_next = -1;
+      if (lane < kTUnits && n_tiles > 0) {
+        const int t0 = unit_t0(lane);
+        y_next = page_y(t0, t0 >= 0 ? table_entry(t0) : -1);
+      }
       for (int j = 0; j < n_tiles; ++j) {
         const int y_cur = y_next;
-        if (j + 1 < n_tiles) y_next = lane < kTUnits ? page_row((j + 1) * kTUnits + lane) : -1;
+        // the next tile's block-table entries: read now, examined only after
+        // this tile's copies are out, so the read's latency overlaps them
+        const int t0n = (lane < kTUnits && j + 1 < n_tiles) ? unit_t0((j + 1) * kTUnits + lane) : -1;
+        const int32_t pb_next = t0n >= 0 ? table_entry(t0n) : -1;
         const int loaded = __popc(__ballot_sync(0xffffffffu, y_cur >= 0));
         if (y_cur == -2) bad = true;
         if (j >= SK &&
@@ -268,6 +279,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
             !mbar_wait_bounded(smem_u32(&v_empty[j % SV]), ((j / SV) - 1) & 1, kWaitLimit))
           bad = true;
         issue(&vmap, smem_u32(&v_full[j % SV]), v_addr(j), y_cur, loaded);
+        y_next = page_y(t0n, pb_next);
       }
       // every copy started has landed (already waited for unless a wait ran out)
       if (lane == 0) {
