@@ -157,7 +157,7 @@ __device__ void merge_and_store(const float* so, const float* sm, const float* s
 // 16-bit pools: TMA-staged pages, tensor-core QK^T and PV.
 
 template <typename T, int D, int NT, bool KV8, bool I8 = false>
-__global__ void __launch_bounds__(kThreads, (KV8 && NT == 1) ? 3 : 2)
+__global__ void __launch_bounds__(kThreads, (KV8 && NT == 1) ? 4 : 2)
 decode16_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
                 const DecodeParams p) {
   using Cfg = Tile16<D, KV8>;

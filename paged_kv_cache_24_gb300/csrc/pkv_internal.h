@@ -17,7 +17,7 @@ constexpr int kDecodeWarps = 4;
 // Ring depth (units in flight per warp) by head_dim, for 16-bit pools.
 constexpr int kStagesD128 = 3;
 constexpr int kStagesD64 = 4;
-constexpr int kStagesFp8 = 4;  // FP8 pools: 4 KB of codes + 128 B of scales per unit
+constexpr int kStagesFp8 = 3;  // 8-bit pools: 4 KB of codes + 128 B of scales per unit
 // Bounded mbarrier wait (polls); a TMA that has not landed by then is treated
 // as an error (output NaN), never as a reason to spin forever.
 constexpr uint32_t kWaitLimit = 1u << 20;
