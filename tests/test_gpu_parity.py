@@ -112,6 +112,19 @@ SMALL = [
 ]
 
 
+# enough (sequence, kv head) items for the launcher to pick two ring stages and
+# three CTAs per SM (at least 16 items per SM: 2432 on 152 SMs)
+_r = np.random.default_rng(41)
+SMALL.append(("many_short_fp16", dict(dtype=torch.float16, num_seqs=640, num_q_heads=8,
+                                      num_kv_heads=4, head_dim=128, block_size=16,
+                                      lens=_r.integers(1, 160, 640).tolist(), explicit_pool=None,
+                                      lens_are_pre_append=False), (0, 32)))
+SMALL.append(("many_short_bf16_bs32", dict(dtype=torch.bfloat16, num_seqs=700, num_q_heads=16,
+                                           num_kv_heads=4, head_dim=128, block_size=32,
+                                           lens=_r.integers(1, 120, 700).tolist(),
+                                           explicit_pool=None, lens_are_pre_append=False), (0,)))
+
+
 @pytest.mark.parametrize("name,over,splits", SMALL, ids=[s[0] for s in SMALL])
 def test_small_cases_all_outputs(pkv_lib, oracle_lib, name, over, splits):
     spec = config_spec(0, **over)
