@@ -158,9 +158,9 @@ int pkv_decode(const void* q, int32_t num_seqs, int32_t num_q_heads,
 
 /*
  * pkv_decode_split -- pkv_decode with an explicit context split.
- *   tokens_per_split: a positive multiple of 16 (each CTA handles at most that
- *   many tokens of one sequence), or 0 to let the library choose (exactly
- *   what pkv_decode does).  The result is the same up to fp32 rounding
+ *   tokens_per_split: a positive multiple of 16 up to 65536 (each CTA handles
+ *   at most that many tokens of one sequence; larger: PKV_ERR_UNSUPPORTED),
+ *   or 0 to let the library choose (exactly what pkv_decode does).  The result is the same up to fp32 rounding
  *   order for every choice.
  */
 int pkv_decode_split(const void* q, int32_t num_seqs, int32_t num_q_heads,
@@ -196,7 +196,7 @@ typedef struct pkv_decode_options {
   int32_t window;           /* <= 0: no window                                        */
   int32_t num_sinks;        /* with window > 0, positions [0, num_sinks) are attended
                                as well (attention sinks); 0: plain window             */
-  int32_t tokens_per_split; /* a multiple of 16 up to 2048, or 0 for the library plan */
+  int32_t tokens_per_split; /* a multiple of 16 up to 65536, or 0 for the library plan */
   const void* k_new;        /* both non-NULL: fused append of position L-1, as in    */
   const void* v_new;        /* pkv_append_decode; both NULL: decode only             */
   const float* k_scale;     /* 8-bit pools: [NB][Hkv][bs] row scales, 16-byte aligned; */

@@ -168,6 +168,7 @@ decode16_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant_
   constexpr int KS = D / 16;        // k-steps of QK^T == m-tiles of PV
   constexpr int DP = D + 4;         // padded row stride of the merge buffer
   constexpr int S = Cfg::kStages;
+  static_assert(S <= 16, "the next chunk's pages are resolved 16 units ahead");
   static_assert(kDecodeWarps * QT * (DP + 2) * 4 <= kDecodeWarps * Cfg::kWarpBytes,
                 "merge buffer must fit in the staging rings");
   static_assert(!KV8 || D == 128, "FP8 pools: head_dim 128");
@@ -205,18 +206,39 @@ decode16_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant_
   }
   __syncthreads();
 
-  // Units of this warp: u = u0 + warp + j * kDecodeWarps.  Lane j resolves
-  // unit j's page through the block table once, up front.
+  // Units of this warp: u = u0 + warp + j * kDecodeWarps.  Their pages are
+  // resolved through the block table 32 at a time, lane l holding unit
+  // 32 c + l of chunk c: y_cur holds the chunk of unit j, y_next the one
+  // after it.  The next chunk's entries are read when a chunk starts and
+  // examined only halfway through it, so the read never stalls the warp.
   const int span = w.u1 - w.u0;
   const int my_n = span > warp ? (span - warp + kDecodeWarps - 1) / kDecodeWarps : 0;
-  int my_y = -1;  // TMA row coordinate of the unit's first token, -1 = bad block id
-  if (lane < my_n) {
-    const int t0 = phys_unit(w.su, w.u0 + warp + lane * kDecodeWarps) * kUnitTokens;
-    const int32_t pb = __ldg(p.block_tables + static_cast<int64_t>(w.b) * p.max_blocks +
-                             t0 / p.block_size);
-    if (pb >= 0 && pb < p.num_blocks)
-      my_y = (pb * p.num_kv_heads + w.hkv) * p.block_size + (t0 % p.block_size);
+  auto unit_t0 = [&](int jj) -> int {  // first token of unit jj, -1 past the warp's units
+    return jj < my_n ? phys_unit(w.su, w.u0 + warp + jj * kDecodeWarps) * kUnitTokens : -1;
+  };
+  auto table_entry = [&](int t0) -> int32_t {
+    return t0 < 0 ? -1
+                  : __ldg(p.block_tables + static_cast<int64_t>(w.b) * p.max_blocks +
+                          t0 / p.block_size);
+  };
+  // TMA row coordinate of the unit's first token, -1 = bad block id or no unit
+  auto row_of = [&](int t0, int32_t pb) -> int {
+    return (t0 >= 0 && pb >= 0 && pb < p.num_blocks)
+               ? (pb * p.num_kv_heads + w.hkv) * p.block_size + (t0 % p.block_size)
+               : -1;
+  };
+  int y_cur, y_next = -1;
+  {
+    const int t0 = unit_t0(lane);
+    y_cur = row_of(t0, table_entry(t0));
   }
+  int t0_ahead = unit_t0(32 + lane);  // the next chunk's entries, read ahead
+  int32_t pb_ahead = table_entry(t0_ahead);
+  // row coordinate of unit jj, jj in the current chunk or the next one
+  auto y_of = [&](int jj, int j) -> int {
+    const int v = (jj >> 5) == (j >> 5) ? y_cur : y_next;
+    return __shfl_sync(0xffffffffu, v, jj & 31);
+  };
 
   auto issue = [&](int stage, int y) {
     const uint32_t bar = smem_u32(&bars[warp][stage]);
@@ -244,7 +266,7 @@ decode16_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant_
 
 #pragma unroll
   for (int j = 0; j < S; ++j) {
-    const int y = __shfl_sync(0xffffffffu, my_y, j);
+    const int y = y_of(j, 0);
     if (lane == 0 && j < my_n) issue(j, y);
   }
 
@@ -306,9 +328,17 @@ decode16_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant_
   }
 
   for (int j = 0; j < my_n; ++j) {
+    if (my_n > 32) {  // (warp-uniform)
+      if ((j & 31) == 16) y_next = row_of(t0_ahead, pb_ahead);  // read 16 units ago
+      if ((j & 31) == 0 && j > 0) {
+        y_cur = y_next;
+        t0_ahead = unit_t0(j + 32 + lane);
+        pb_ahead = table_entry(t0_ahead);
+      }
+    }
     const int stage = j % S;
     const uint32_t parity = (j / S) & 1;
-    const int yj = __shfl_sync(0xffffffffu, my_y, j);
+    const int yj = y_of(j, j);
     const bool ok = mbar_wait_bounded(smem_u32(&bars[warp][stage]), parity, kWaitLimit);
     if (!__all_sync(0xffffffffu, ok)) {
       bad = true;  // the copy never landed; stop using this ring
@@ -569,7 +599,7 @@ decode16_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant_
     fence_proxy_async_smem();  // this lane's reads of the stage precede the refill
     __syncwarp();
     if (j + S < my_n) {
-      const int yn = __shfl_sync(0xffffffffu, my_y, j + S);
+      const int yn = y_of(j + S, j);
       if (lane == 0) issue(stage, yn);
     }
   }

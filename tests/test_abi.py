@@ -63,7 +63,7 @@ def test_decode_argument_checks(pkv_lib):
     assert _decode(pkv, _layout(pkv), q=FAKE + 8) == ALIGN
     assert _decode(pkv, _layout(pkv), lens=FAKE + 2) == ALIGN
     assert _decode(pkv, _layout(pkv), tps=24) == SHAPE          # not a multiple of 16
-    assert _decode(pkv, _layout(pkv), tps=4096) == UNSUP        # more than 2048 per split
+    assert _decode(pkv, _layout(pkv), tps=65536 + 16) == UNSUP  # more than 65536 per split
     assert _decode(pkv, _layout(pkv, nb=1 << 30)) == UNSUP      # TMA rows exceed int32
     # nothing to do: succeeds without touching the device
     assert _decode(pkv, _layout(pkv), B=0, q=0, out=0) == OK
@@ -102,6 +102,11 @@ def test_slot_mapping_argument_checks(pkv_lib):
     ((16, 32, (30000, 8, 16, 128, 2), 2048, 4096), (1024, 5)),
     ((4, 8, (32, 8, 16, 64, 0), 7, 0), (128, 1)),
     ((1, 8, (4096, 8, 16, 128, 1), 2048, 0), (256, 128)),
+    # 32+ items per SM and at most 4096 tokens each: one split per item
+    ((1024, 32, (50000, 8, 16, 128, 1), 130, 0), (2080, 1)),
+    ((1024, 32, (50000, 8, 16, 128, 1), 256, 0), (4096, 1)),
+    ((1024, 32, (50000, 8, 16, 128, 1), 257, 0), (2048, 3)),
+    ((600, 32, (50000, 8, 16, 128, 1), 130, 0), (2048, 2)),
 ])
 def test_plan(pkv_lib, cfg, expect):
     B, hq, lay, mb, window = cfg

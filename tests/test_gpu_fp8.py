@@ -61,6 +61,10 @@ CASES = [
      (0, 32)),
     ("window_sinks", dict(num_seqs=6, num_q_heads=8, num_kv_heads=2,
                           lens=[1, 20, 100, 101, 317, 2000]), 37, 4, (0, 16)),
+    ("long_split", dict(num_seqs=3, num_q_heads=8, num_kv_heads=2, lens=[100, 3000, 6000]),
+     0, 0, (4096, 65536)),
+    ("window_sinks_long_split", dict(num_seqs=2, num_q_heads=8, num_kv_heads=2,
+                                     lens=[2600, 6000]), 2500, 4, (2528,)),
 ]
 
 

@@ -125,6 +125,30 @@ SMALL.append(("many_short_bf16_bs32", dict(dtype=torch.bfloat16, num_seqs=700, n
                                            explicit_pool=None, lens_are_pre_append=False), (0,)))
 
 
+# more work items than SMs and fewer than 16 per SM
+SMALL.append(("mid_grid_fp16", dict(dtype=torch.float16, num_seqs=40, num_q_heads=8,
+                                    num_kv_heads=4, head_dim=128, block_size=16,
+                                    lens=_r.integers(1, 600, 40).tolist(), explicit_pool=None,
+                                    lens_are_pre_append=False), (0, 64)))
+SMALL.append(("mid_grid_bf16_bs64", dict(dtype=torch.bfloat16, num_seqs=20, num_q_heads=16,
+                                         num_kv_heads=8, head_dim=128, block_size=64,
+                                         lens=_r.integers(1, 900, 20).tolist(),
+                                         explicit_pool=None, lens_are_pre_append=False),
+                      (0, 32)))
+
+# splits longer than 32 units per warp: each warp resolves its pages 32 units
+# at a time
+SMALL.append(("long_split_fp16", dict(dtype=torch.float16, num_seqs=5, num_q_heads=4,
+                                      num_kv_heads=4, head_dim=128, block_size=16,
+                                      lens=[1, 700, 2100, 5000, 9000], explicit_pool=None,
+                                      lens_are_pre_append=False), (4096, 65536)))
+SMALL.append(("long_split_bf16_d64_window", dict(dtype=torch.bfloat16, num_seqs=4,
+                                                 num_q_heads=16, num_kv_heads=2, head_dim=64,
+                                                 block_size=32, lens=[2999, 3001, 3003, 7000],
+                                                 window=3000, explicit_pool=None,
+                                                 lens_are_pre_append=False), (0, 3008, 65536)))
+
+
 @pytest.mark.parametrize("name,over,splits", SMALL, ids=[s[0] for s in SMALL])
 def test_small_cases_all_outputs(pkv_lib, oracle_lib, name, over, splits):
     spec = config_spec(0, **over)
@@ -152,6 +176,9 @@ SINKS = [
                          head_dim=128, lens=[3, 17, 21, 400], window=16), 4, (0, 16)),
     ("bf16_s16_aligned", dict(dtype=torch.bfloat16, num_seqs=3, num_q_heads=32, num_kv_heads=2,
                               head_dim=128, lens=[33, 64, 999], window=32), 16, (0, 16)),
+    ("fp16_w2500_s20_long_split", dict(dtype=torch.float16, num_seqs=3, num_q_heads=8,
+                                       num_kv_heads=2, head_dim=128, lens=[2600, 3000, 6000],
+                                       window=2500), 20, (0, 2528, 65536)),
 ]
 
 

@@ -50,7 +50,7 @@ def _decode_case(seed):
             lens[i] = max(1, bs * int(r.integers(1, 6)) + int(r.choice([-1, 0, 1])))
     window = 0 if r.random() < 0.4 else int(r.integers(1, 600))
     sinks = 0 if window == 0 else int(r.choice([0, 1, 4, 17]))
-    tps = int(r.choice([0, 16, 48, 256, 2048]))
+    tps = int(r.choice([0, 16, 48, 256, 2048, 4096, 65536]))
     fused = kind in ("fp32", "fp16", "bf16") and r.random() < 0.5
     over = dict(dtype=DTYPE[kind], num_seqs=B, num_q_heads=hkv * g, num_kv_heads=hkv,
                 head_dim=d, block_size=bs, lens=[int(x) for x in lens], window=window,
