@@ -123,6 +123,30 @@ int encode_pool_map(CUtensorMap* map, const void* pool, const pkv_cache_layout* 
   return r == CUDA_SUCCESS ? PKV_OK : PKV_ERR_CUDA;
 }
 
+// The decode kernels' view of a pool.  16-bit pools with head_dim 128 are
+// seen as a 3-D tensor [2 column halves][NB * Hkv * bs rows][64 columns] (the
+// halves' stride, 128 bytes, is below the rows' 256), so that one box of
+// 64 x 16 x 2 brings a unit's 16 rows in a single copy, in shared memory as
+// two 16 x 64 swizzled tiles one after the other; other pools keep the 2-D
+// view above.
+int encode_decode_map(CUtensorMap* map, const void* pool, const pkv_cache_layout* L) {
+  if (L->head_dim != 128 || (L->dtype != PKV_FLOAT16 && L->dtype != PKV_BFLOAT16))
+    return encode_pool_map(map, pool, L);
+  auto fn = get_encode_fn();
+  if (!fn) return PKV_ERR_CUDA;
+  const cuuint64_t rows = static_cast<cuuint64_t>(L->num_blocks) * L->num_kv_heads * L->block_size;
+  cuuint64_t dims[3] = {64, rows > 0 ? rows : 1, 2};
+  cuuint64_t strides[2] = {256, 128};
+  cuuint32_t box[3] = {64, static_cast<cuuint32_t>(pkv::kUnitTokens), 2};
+  cuuint32_t estr[3] = {1, 1, 1};
+  const CUtensorMapDataType dt =
+      L->dtype == PKV_FLOAT16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+  CUresult r = fn(map, dt, 3, const_cast<void*>(pool), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? PKV_OK : PKV_ERR_CUDA;
+}
+
 // ---- planning -----------------------------------------------------------------
 
 struct Plan {
@@ -282,9 +306,9 @@ int decode_impl(const void* q, const void* k_new, const void* v_new, int32_t num
     e = pkv::launch_decode_f32(layout->head_dim, p, st);
   } else {
     CUtensorMap kmap, vmap;
-    rc = encode_pool_map(&kmap, k_cache, layout);
+    rc = encode_decode_map(&kmap, k_cache, layout);
     if (rc != PKV_OK) return rc;
-    rc = encode_pool_map(&vmap, v_cache, layout);
+    rc = encode_decode_map(&vmap, v_cache, layout);
     if (rc != PKV_OK) return rc;
     e = q8 ? pkv::launch_decode_q8(layout->dtype == PKV_INT8, plan.ntiles, kmap, vmap, p, st)
             : pkv::launch_decode_16bit(layout->dtype, layout->head_dim, plan.ntiles, kmap, vmap,
@@ -325,7 +349,7 @@ int decode_plan(int num_seqs, int num_q_heads, const pkv_cache_layout* layout, i
   return PKV_OK;
 }
 int pool_tensor_map(CUtensorMap* map, const void* pool, const pkv_cache_layout* layout) {
-  return encode_pool_map(map, pool, layout);
+  return encode_decode_map(map, pool, layout);
 }
 int status_of(cudaError_t e) { return to_status(e); }
 }  // namespace pkv

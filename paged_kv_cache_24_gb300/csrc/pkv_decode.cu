@@ -37,6 +37,17 @@
 namespace pkv {
 namespace {
 
+// 3-D tiled load of the box at (x, y, z) into shared memory; completion is
+// signalled as transaction bytes on `bar`.
+__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map, int32_t x,
+                                            int32_t y, int32_t z, uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(bar)
+      : "memory");
+}
+
 constexpr int kThreads = kDecodeWarps * 32;
 constexpr int kBoxBytes = kUnitTokens * 128;  // one TMA box: 16 rows x 128 bytes
 constexpr float kRescaleThreshold = 8.0f;     // log2 units: weights stay <= 2^8
@@ -252,12 +263,13 @@ decode16_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant_
         const uint32_t sdst = scales + stage * 2 * kUnitTokens * 4;
         bulk_load(sdst, p.k_scale + y, kUnitTokens * 4, bar);
         bulk_load(sdst + kUnitTokens * 4, p.v_scale + y, kUnitTokens * 4, bar);
+      } else if constexpr (D == 128) {
+        // the 3-D view: both 64-column halves of the 16 rows in one copy
+        tma_load_3d(kdst, &kmap, 0, y, 0, bar);
+        tma_load_3d(vdst, &vmap, 0, y, 0, bar);
       } else {
-#pragma unroll
-        for (int bx = 0; bx < Cfg::kBoxes; ++bx) {
-          tma_load_2d(kdst + bx * kBoxBytes, &kmap, bx * 64, y, bar);
-          tma_load_2d(vdst + bx * kBoxBytes, &vmap, bx * 64, y, bar);
-        }
+        tma_load_2d(kdst, &kmap, 0, y, bar);
+        tma_load_2d(vdst, &vmap, 0, y, bar);
       }
     } else {
       mbar_arrive(bar);  // nothing to fetch: complete the phase, the unit is flagged bad
