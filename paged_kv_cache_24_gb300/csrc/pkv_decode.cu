@@ -37,6 +37,22 @@
 namespace pkv {
 namespace {
 
+// 4-byte asynchronous copy global -> shared through the load/store path,
+// tracked by commit groups.
+__device__ __forceinline__ void cp_async_4(uint32_t dst, const void* src) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(dst),
+               "l"(reinterpret_cast<uint64_t>(src))
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() {
+  asm volatile("cp.async.commit_group;" ::: "memory");
+}
+// wait until at most N of this thread's commit groups are pending
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
 // 3-D tiled load of the box at (x, y, z) into shared memory; completion is
 // signalled as transaction bytes on `bar`.
 __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map, int32_t x,
@@ -72,7 +88,7 @@ struct Tile16 {
   static constexpr int kRingBytes = kStages * kStageBytes;  // per warp
   static constexpr int kWarpBytes = kRingBytes;             // multiple of 1 KB
   static constexpr int kScaleBytes = KV8 ? kStages * 2 * kUnitTokens * 4 : 0;  // per warp
-  static constexpr int kTxBytes = KV8 ? 2 * kCodeTileBytes + 2 * kUnitTokens * 4 : kStageBytes;
+  static constexpr int kTxBytes = KV8 ? 2 * kCodeTileBytes : kStageBytes;  // TMA bytes per stage
   static constexpr int kSmemBytes = kDecodeWarps * (kWarpBytes + kScaleBytes) + 1024;
   static_assert(kWarpBytes % 1024 == 0, "swizzled tiles need 1 KB alignment");
 };
@@ -260,9 +276,6 @@ decode16_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant_
       if constexpr (KV8) {
         tma_load_2d(kdst, &kmap, 0, y, bar);  // 16 rows x 128 codes
         tma_load_2d(vdst, &vmap, 0, y, bar);
-        const uint32_t sdst = scales + stage * 2 * kUnitTokens * 4;
-        bulk_load(sdst, p.k_scale + y, kUnitTokens * 4, bar);
-        bulk_load(sdst + kUnitTokens * 4, p.v_scale + y, kUnitTokens * 4, bar);
       } else if constexpr (D == 128) {
         // the 3-D view: both 64-column halves of the 16 rows in one copy
         tma_load_3d(kdst, &kmap, 0, y, 0, bar);
@@ -276,10 +289,27 @@ decode16_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant_
     }
   };
 
+  // 8-bit pools: the unit's 2 x 16 row scales come in by 4-byte cp.async
+  // (lane l < 16: K row l, else V row l - 16), not as two more TMA copies:
+  // each copy costs the SM's copy engine about as much to process as a whole
+  // code tile.  Every lane commits one group per unit slot, empty when there
+  // is nothing to fetch, so that the group of unit j is always the S-th
+  // newest when unit j is read.
+  auto issue_scales = [&](int stage, int y) {
+    if constexpr (KV8) {
+      if (y >= 0) {
+        const float* src = (lane < kUnitTokens ? p.k_scale : p.v_scale) + y + (lane & (kUnitTokens - 1));
+        cp_async_4(scales + stage * 2 * kUnitTokens * 4 + lane * 4, src);
+      }
+      cp_async_commit();
+    }
+  };
+
 #pragma unroll
   for (int j = 0; j < S; ++j) {
     const int y = y_of(j, 0);
     if (lane == 0 && j < my_n) issue(j, y);
+    issue_scales(j, j < my_n ? y : -1);
   }
 
   // Q fragments: B operand of S^T = K Q^T.  Lane holds q[n = lane/4] at
@@ -364,6 +394,8 @@ decode16_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant_
     // per-row scales of the unit (FP8 pools; 1 otherwise): K rows g, g+8; V rows g, g+8
     float ksa = 1.f, ksb = 1.f, vsa = 1.f, vsb = 1.f;
     if constexpr (KV8) {
+      cp_async_wait<S - 1>();  // this lane's scale copy of unit j has landed
+      __syncwarp();            // ... and every other lane's
       const uint32_t sc = scales + stage * 2 * kUnitTokens * 4;
       ksa = ld_shared_f32(sc + (g << 2));
       ksb = ld_shared_f32(sc + ((g + 8) << 2));
@@ -610,11 +642,11 @@ decode16_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant_
     // ---- recycle the stage ----
     fence_proxy_async_smem();  // this lane's reads of the stage precede the refill
     __syncwarp();
-    if (j + S < my_n) {
-      const int yn = y_of(j + S, j);
-      if (lane == 0) issue(stage, yn);
-    }
+    const int yn = j + S < my_n ? y_of(j + S, j) : -1;
+    if (lane == 0 && j + S < my_n) issue(stage, yn);
+    issue_scales(stage, yn);
   }
+  if constexpr (KV8) cp_async_wait<0>();  // no copy into shared memory outlives the loop
 
   // ---- per-warp state -> shared memory -> CTA merge ----
 #pragma unroll
