@@ -21,7 +21,9 @@ namespace pkv {
 namespace {
 
 constexpr int kAppendThreads = 256;
-constexpr int kPlanBins = 4096;  // work sizes 0 .. 4095 key tiles (larger ones share the top bin)
+constexpr int kAppendVec = 4;  // 16-byte chunks per thread (a row has 8 or 16)
+constexpr int kPlanBins = 1024;  // work sizes 0 .. 1023 key tiles (larger ones share the top bin)
+constexpr int kPlanCache = 4;    // planner items per thread sized once
 
 struct PlanArgs {
   int32_t* order;
@@ -35,12 +37,11 @@ struct PlanArgs {
 __device__ void plan_items(const int32_t* __restrict__ cu_q,
                            const int32_t* __restrict__ context_lens, int num_seqs,
                            int max_blocks, int block_size, const PlanArgs& pa) {
-  static_assert(kPlanBins % kAppendThreads == 0, "bins per thread");
-  constexpr int kPer = kPlanBins / kAppendThreads;
-  __shared__ int bins[kPlanBins];
+  static_assert(kPlanBins == 4 * kAppendThreads, "four bins per thread");
+  __shared__ __align__(16) int bins[kPlanBins];
   __shared__ int warp_sum[kAppendThreads / 32];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  for (int i = tid; i < kPlanBins; i += kAppendThreads) bins[i] = 0;
+  reinterpret_cast<int4*>(bins)[tid] = make_int4(0, 0, 0, 0);
   __syncthreads();
   const int64_t n_items = static_cast<int64_t>(num_seqs) * pa.chunks_per_seq;
   auto bin_of = [&](int64_t i) {
@@ -51,12 +52,25 @@ __device__ void plan_items(const int32_t* __restrict__ cu_q,
     const int w = it.empty ? 0 : min(it.n_tiles, kPlanBins - 1);
     return kPlanBins - 1 - w;  // the largest work first
   };
-  for (int64_t i = tid; i < n_items; i += kAppendThreads) atomicAdd(&bins[bin_of(i)], 1);
-  __syncthreads();
-  // exclusive scan: thread t owns bins t*kPer .. t*kPer + kPer - 1
-  int local = 0;
+  // the first kPlanCache items of each thread keep their bin in registers (their
+  // reads all go out before the first one is used); any further ones are
+  // sized twice
+  int cached[kPlanCache];
 #pragma unroll
-  for (int k = 0; k < kPer; ++k) local += bins[tid * kPer + k];
+  for (int r = 0; r < kPlanCache; ++r) {
+    const int64_t i = tid + static_cast<int64_t>(r) * kAppendThreads;
+    cached[r] = i < n_items ? bin_of(i) : 0;
+  }
+#pragma unroll
+  for (int r = 0; r < kPlanCache; ++r)
+    if (tid + static_cast<int64_t>(r) * kAppendThreads < n_items) atomicAdd(&bins[cached[r]], 1);
+  for (int64_t i = tid + static_cast<int64_t>(kPlanCache) * kAppendThreads; i < n_items;
+       i += kAppendThreads)
+    atomicAdd(&bins[bin_of(i)], 1);
+  __syncthreads();
+  // exclusive scan: thread t owns bins 4t .. 4t + 3 (one 16-byte access each way)
+  const int4 c4 = reinterpret_cast<const int4*>(bins)[tid];
+  const int local = c4.x + c4.y + c4.z + c4.w;
   int incl = local;
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
@@ -67,20 +81,28 @@ __device__ void plan_items(const int32_t* __restrict__ cu_q,
   __syncthreads();
   int run = incl - local;
   for (int w = 0; w < warp; ++w) run += warp_sum[w];
-#pragma unroll
-  for (int k = 0; k < kPer; ++k) {
-    const int h = bins[tid * kPer + k];
-    bins[tid * kPer + k] = run;
-    run += h;
-  }
+  int4 first;
+  first.x = run;
+  first.y = first.x + c4.x;
+  first.z = first.y + c4.y;
+  first.w = first.z + c4.z;
+  reinterpret_cast<int4*>(bins)[tid] = first;
   __syncthreads();
-  for (int64_t i = tid; i < n_items; i += kAppendThreads)
+#pragma unroll
+  for (int r = 0; r < kPlanCache; ++r) {
+    const int64_t i = tid + static_cast<int64_t>(r) * kAppendThreads;
+    if (i < n_items) pa.order[atomicAdd(&bins[cached[r]], 1)] = static_cast<int32_t>(i);
+  }
+  for (int64_t i = tid + static_cast<int64_t>(kPlanCache) * kAppendThreads; i < n_items;
+       i += kAppendThreads)
     pa.order[atomicAdd(&bins[bin_of(i)], 1)] = static_cast<int32_t>(i);
 }
 
 // The chunk's K/V rows to their slots: token i of sequence b sits at position
-// L_b - n_b + i.  One thread per 16-byte chunk of a (token, kv head) row.
-// Block (0, num_seqs) orders the attention's work items instead.
+// L_b - n_b + i.  One thread per kAppendVec 16-byte chunks of a (token, kv
+// head) row, so that each thread keeps several loads in flight behind its
+// block-table read.  Block (0, num_seqs) orders the attention's work items
+// instead.
 __global__ void __launch_bounds__(kAppendThreads)
 chunk_append_kernel(const uint4* __restrict__ k, const uint4* __restrict__ v,
                     const int32_t* __restrict__ cu_q, const int32_t* __restrict__ context_lens,
@@ -98,21 +120,32 @@ chunk_append_kernel(const uint4* __restrict__ k, const uint4* __restrict__ v,
   const int b = blockIdx.y;
   const int start = cu_q[b];
   const int n = cu_q[b + 1] - start;
-  const int64_t per_tok = static_cast<int64_t>(num_kv_heads) * chunks_per_row;
+  const int vecs_per_row = chunks_per_row / kAppendVec;
+  const int64_t per_tok = static_cast<int64_t>(num_kv_heads) * vecs_per_row;
   const int64_t idx = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
   if (idx >= n * per_tok) return;
   const int i = static_cast<int>(idx / per_tok);
   const int rem = static_cast<int>(idx - i * per_tok);
-  const int h = rem / chunks_per_row, c = rem - h * chunks_per_row;
+  const int h = rem / vecs_per_row, c = (rem - h * vecs_per_row) * kAppendVec;
+  // the rows' loads go out before the block-table read, not after it
+  const int64_t src = (static_cast<int64_t>(start + i) * num_kv_heads + h) * chunks_per_row + c;
+  uint4 kr[kAppendVec], vr[kAppendVec];
+#pragma unroll
+  for (int e = 0; e < kAppendVec; ++e) {
+    kr[e] = __ldg(k + src + e);
+    vr[e] = __ldg(v + src + e);
+  }
   const int64_t p = static_cast<int64_t>(context_lens[b]) - n + i;
   if (p < 0 || p >= static_cast<int64_t>(max_blocks) * block_size) return;
   const int32_t blk = block_tables[static_cast<int64_t>(b) * max_blocks + p / block_size];
   if (blk < 0 || blk >= num_blocks) return;
   const int64_t dst = ((static_cast<int64_t>(blk) * num_kv_heads + h) * block_size +
                        p % block_size) * chunks_per_row + c;
-  const int64_t src = (static_cast<int64_t>(start + i) * num_kv_heads + h) * chunks_per_row + c;
-  k_cache[dst] = __ldg(k + src);
-  v_cache[dst] = __ldg(v + src);
+#pragma unroll
+  for (int e = 0; e < kAppendVec; ++e) {
+    k_cache[dst + e] = kr[e];
+    v_cache[dst + e] = vr[e];
+  }
 }
 
 }  // namespace
@@ -127,7 +160,7 @@ cudaError_t launch_prefill(int dtype, int head_dim, const void* q, const void* k
   if (num_seqs == 0 || max_chunk == 0) return cudaSuccess;
   // 1) the chunk's rows to their slots; the work items' order
   const int cpr = head_dim * 2 / 16;
-  const int64_t per_seq = static_cast<int64_t>(max_chunk) * num_kv_heads * cpr;
+  const int64_t per_seq = static_cast<int64_t>(max_chunk) * num_kv_heads * (cpr / kAppendVec);
   PlanArgs pa;
   pa.order = order;
   pa.tok_per_cta = kPrefillRowsCta >> prefill_heads_log2(num_q_heads / num_kv_heads);
