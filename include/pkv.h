@@ -62,8 +62,9 @@ typedef enum pkv_status {
   PKV_ERR_ALIGNMENT = 5,   /* a data pointer is not 16-byte aligned              */
   PKV_ERR_CUDA = 6,        /* a CUDA runtime call or a kernel launch failed       */
   PKV_ERR_NOMEM = 7,       /* the split-K workspace could not be allocated        */
-  PKV_ERR_SCRATCH = 8      /* pkv_decode_noalloc: the problem needs more split-K
+  PKV_ERR_SCRATCH = 8,     /* pkv_decode_noalloc: the problem needs more split-K
                               scratch than its fixed buffer holds                */
+  PKV_ERR_RANGE = 9        /* pkv_validate_indices: an index is out of range      */
 } pkv_status;
 
 /* Shape of one layer's K (or V) pool. */
@@ -336,6 +337,41 @@ int pkv_decode_noalloc(const void* q, int32_t num_seqs, int32_t num_q_heads,
                        const int32_t* block_tables, int32_t max_blocks_per_seq,
                        const int32_t* context_lens, int32_t window, float scale, void* out,
                        void* stream);
+
+/*
+ * pkv_validate_indices -- debug aid, not part of the hot path: range-check
+ * the indices that the other calls trust.
+ *   The pages check capacity where an index is made: the allocator of "Build
+ *   a Paged KV Cache in Pure Python" (Step 2) raises MemoryError when the pool
+ *   cannot supply a block, and the cache manager of "Building a Streaming
+ *   Sliding-Window Attention Engine in Pure Python" (Step 2) asserts that an
+ *   append fits.  The kernels here cannot raise: a bad block id is skipped and
+ *   the sequence's output is NaN, a slot past the pool is skipped.  This call
+ *   finds such indices before they reach a kernel.
+ *   block_tables [num_seqs][max_blocks_per_seq] int32, context_lens [num_seqs]
+ *   int32 and slot_mapping [num_slots] int64 (NULL when num_slots == 0) are
+ *   copied to the host on `stream`; the call then WAITS for the stream.  It
+ *   checks, in this order:
+ *     1 context_lens[b] in [0, max_blocks_per_seq * block_size];
+ *     2 block_tables[b][j] in [0, num_blocks) for every block the context
+ *       uses, j < ceil(context_lens[b] / block_size) (later entries are never
+ *       read and may hold anything);
+ *     3 slot_mapping[i] < num_blocks * block_size (negative = skipped);
+ *     4 no two tokens share a slot (the order of their writes is undefined).
+ *   Returns PKV_OK, or PKV_ERR_RANGE with the first failure in `error` (if
+ *   not NULL): what = the check's number above, row / col = the index
+ *   (b, j) or (i, earlier i'), value = the offending entry.  NULL arrays
+ *   with non-zero sizes: PKV_ERR_NULL; negative sizes or block_size < 1:
+ *   PKV_ERR_SHAPE; a failed copy: PKV_ERR_CUDA.
+ */
+typedef struct pkv_index_error {
+  int32_t what;  /* 0 = none, else the number of the failed check */
+  int64_t row, col, value;
+} pkv_index_error;
+int pkv_validate_indices(const int32_t* block_tables, int32_t num_seqs,
+                         int32_t max_blocks_per_seq, const int32_t* context_lens,
+                         const int64_t* slot_mapping, int64_t num_slots, int64_t num_blocks,
+                         int32_t block_size, void* stream, pkv_index_error* error);
 
 /* Human-readable name of a pkv_status code (static storage). */
 const char* pkv_status_string(int status);

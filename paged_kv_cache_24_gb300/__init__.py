@@ -19,7 +19,10 @@ Public API (thin wrappers over the C ABI of ``libpkv.so``, see include/pkv.h):
   chunks and compute their causal (windowed, with sinks) attention over the
   paged cache;
 * ``pkv_stage_copy(dst, src)`` -- a kernel copy between device memory and
-  pinned host memory (DecodeStep's host transfers).
+  pinned host memory (DecodeStep's host transfers);
+* ``pkv_validate_indices(block_tables, context_lens, num_blocks, block_size,
+  slot_mapping=None)`` -- debug check of the indices the kernels trust
+  (waits for the stream).
 
 ``DecodeStep`` packages one serving step (slot mapping, append, decode) as a
 CUDA graph fed from a pinned host staging buffer.
@@ -30,12 +33,14 @@ benchmark.
 """
 from ._binding import (CacheLayout, DecodeOptions, PkvError, cache_layout, library_path, load_library,
                        pkv_append, pkv_append_decode, pkv_append_fp8, pkv_append_int8, pkv_decode, pkv_prefill, pkv_decode_plan, pkv_release_workspaces,
-                       pkv_slot_mapping, pkv_stage_copy, status_string, PKV_ERR_UNSUPPORTED)
+                       pkv_slot_mapping, pkv_stage_copy, pkv_validate_indices, status_string,
+                       PKV_ERR_RANGE, PKV_ERR_UNSUPPORTED)
 from .step import DecodeStep
 
 __all__ = [
     "DecodeStep", "DecodeOptions", "CacheLayout", "PkvError", "cache_layout", "library_path", "load_library", "pkv_append",
     "pkv_append_decode", "pkv_append_fp8", "pkv_append_int8", "pkv_prefill",
-    "pkv_decode", "pkv_decode_plan", "pkv_release_workspaces", "pkv_slot_mapping", "pkv_stage_copy", "PKV_ERR_UNSUPPORTED",
+    "pkv_decode", "pkv_decode_plan", "pkv_release_workspaces", "pkv_slot_mapping", "pkv_stage_copy",
+    "pkv_validate_indices", "PKV_ERR_RANGE", "PKV_ERR_UNSUPPORTED",
     "status_string",
 ]

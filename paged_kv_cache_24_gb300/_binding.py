@@ -17,6 +17,7 @@ from . import _build
 
 PKV_OK = 0
 PKV_ERR_UNSUPPORTED = 4
+PKV_ERR_RANGE = 9
 PKV_FP8_E4M3 = 3
 PKV_INT8 = 4
 _DTYPES = {torch.float32: 0, torch.float16: 1, torch.bfloat16: 2}
@@ -46,6 +47,12 @@ class CacheLayout(ctypes.Structure):
     _fields_ = [("num_blocks", ctypes.c_int64), ("num_kv_heads", ctypes.c_int32),
                 ("block_size", ctypes.c_int32), ("head_dim", ctypes.c_int32),
                 ("dtype", ctypes.c_int32)]
+
+
+class IndexErrorInfo(ctypes.Structure):
+    """Mirror of ``pkv_index_error``."""
+    _fields_ = [("what", ctypes.c_int32), ("row", ctypes.c_int64), ("col", ctypes.c_int64),
+                ("value", ctypes.c_int64)]
 
 
 _lock = threading.Lock()
@@ -87,6 +94,8 @@ def load_library():
             "pkv_decode_plan": [i32, i32, lay, i32, i32, i32, i32, i32, ctypes.POINTER(i32),
                                 ctypes.POINTER(i32)],
             "pkv_release_workspaces": [],
+            "pkv_validate_indices": [vp, i32, i32, vp, vp, i64, i64, i32, vp,
+                                     ctypes.POINTER(IndexErrorInfo)],
         }
         for name, args in sig.items():
             fn = getattr(lib, name)
@@ -366,6 +375,37 @@ def pkv_decode_plan(num_seqs: int, num_q_heads: int, layout: CacheLayout, max_bl
         num_seqs, num_q_heads, ctypes.byref(layout), max_blocks, window, num_sinks,
         tokens_per_split, num_sms, ctypes.byref(tps), ctypes.byref(ns)))
     return tps.value, ns.value
+
+
+INDEX_CHECKS = {1: "context_length", 2: "block_table_entry", 3: "slot", 4: "duplicate_slot"}
+
+
+def pkv_validate_indices(block_tables, context_lens, num_blocks: int, block_size: int,
+                         slot_mapping=None, stream=None):
+    """Debug check of the indices the other calls trust (waits for the stream).
+
+    Returns None when every index is in range, else (check, row, col, value)
+    for the first failure: check is "context_length" (row = sequence),
+    "block_table_entry" (row, col = sequence, block), "slot" (row = token) or
+    "duplicate_slot" (row = token, col = the earlier token with that slot).
+    """
+    for t, dt, what in ((block_tables, torch.int32, "block_tables"),
+                        (context_lens, torch.int32, "context_lens")):
+        _require(t.dtype == dt and t.is_contiguous(), f"{what} must be contiguous {dt}")
+    _require(block_tables.dim() == 2 and context_lens.numel() == block_tables.shape[0],
+             "block_tables [B, MB] and context_lens [B]")
+    if slot_mapping is not None:
+        _require(slot_mapping.dtype == torch.int64 and slot_mapping.is_contiguous(),
+                 "slot_mapping must be contiguous int64")
+    err = IndexErrorInfo()
+    rc = load_library().pkv_validate_indices(
+        _ptr(block_tables), block_tables.shape[0], block_tables.shape[1], _ptr(context_lens),
+        _ptr(slot_mapping), 0 if slot_mapping is None else slot_mapping.numel(), num_blocks,
+        block_size, _stream(stream), ctypes.byref(err))
+    if rc == PKV_ERR_RANGE:
+        return INDEX_CHECKS[err.what], err.row, err.col, err.value
+    _check("pkv_validate_indices", rc)
+    return None
 
 
 def pkv_release_workspaces() -> None:

@@ -3,6 +3,7 @@
 // descriptor encoding and kernel dispatch.
 #include <cudaTypedefs.h>
 
+#include <algorithm>
 #include <map>
 #include <mutex>
 #include <utility>
@@ -392,6 +393,7 @@ const char* pkv_status_string(int status) {
     case PKV_ERR_CUDA: return "PKV_ERR_CUDA: a CUDA call or kernel launch failed";
     case PKV_ERR_NOMEM: return "PKV_ERR_NOMEM: workspace allocation failed";
     case PKV_ERR_SCRATCH: return "PKV_ERR_SCRATCH: problem needs more than the fixed no-alloc scratch";
+    case PKV_ERR_RANGE: return "PKV_ERR_RANGE: an index is out of range (pkv_validate_indices)";
     default: return "unknown pkv status";
   }
 }
@@ -578,6 +580,68 @@ int pkv_decode(const void* q, int32_t num_seqs, int32_t num_q_heads, const void*
                float scale, void* out, void* stream) {
   return pkv_decode_split(q, num_seqs, num_q_heads, k_cache, v_cache, layout, block_tables,
                           max_blocks_per_seq, context_lens, window, scale, out, 0, stream);
+}
+
+int pkv_validate_indices(const int32_t* block_tables, int32_t num_seqs,
+                         int32_t max_blocks_per_seq, const int32_t* context_lens,
+                         const int64_t* slot_mapping, int64_t num_slots, int64_t num_blocks,
+                         int32_t block_size, void* stream, pkv_index_error* error) {
+  if (error) *error = pkv_index_error{0, 0, 0, 0};
+  if (num_seqs < 0 || max_blocks_per_seq < 0 || num_slots < 0 || num_blocks < 0 ||
+      block_size < 1)
+    return PKV_ERR_SHAPE;
+  if ((num_seqs > 0 && (!block_tables || !context_lens)) || (num_slots > 0 && !slot_mapping))
+    return PKV_ERR_NULL;
+  auto fail = [&](int what, int64_t row, int64_t col, int64_t value) {
+    if (error) *error = pkv_index_error{what, row, col, value};
+    return PKV_ERR_RANGE;
+  };
+  const cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const size_t n_table = static_cast<size_t>(num_seqs) * static_cast<size_t>(max_blocks_per_seq);
+  std::vector<int32_t> lens(static_cast<size_t>(num_seqs)), table(n_table);
+  std::vector<int64_t> slots(static_cast<size_t>(num_slots));
+  auto fetch = [&](void* dst, const void* src, size_t bytes) {
+    return bytes == 0 || cudaMemcpyAsync(dst, src, bytes, cudaMemcpyDefault, st) == cudaSuccess;
+  };
+  if (!fetch(lens.data(), context_lens, lens.size() * sizeof(int32_t)) ||
+      !fetch(table.data(), block_tables, table.size() * sizeof(int32_t)) ||
+      !fetch(slots.data(), slot_mapping, slots.size() * sizeof(int64_t)) ||
+      ((num_seqs > 0 || num_slots > 0) && cudaStreamSynchronize(st) != cudaSuccess)) {
+    cudaGetLastError();
+    return PKV_ERR_CUDA;
+  }
+  const int64_t max_len = static_cast<int64_t>(max_blocks_per_seq) * block_size;
+  for (int32_t b = 0; b < num_seqs; ++b)
+    if (lens[b] < 0 || lens[b] > max_len) return fail(1, b, 0, lens[b]);
+  for (int32_t b = 0; b < num_seqs; ++b) {
+    const int64_t used = (static_cast<int64_t>(lens[b]) + block_size - 1) / block_size;
+    for (int64_t j = 0; j < used; ++j) {
+      const int32_t e = table[static_cast<size_t>(b) * max_blocks_per_seq + j];
+      if (e < 0 || e >= num_blocks) return fail(2, b, j, e);
+    }
+  }
+  const int64_t pool_slots = num_blocks * block_size;
+  std::vector<std::pair<int64_t, int64_t>> taken;  // (slot, token)
+  taken.reserve(slots.size());
+  for (int64_t i = 0; i < num_slots; ++i) {
+    if (slots[i] >= pool_slots) return fail(3, i, 0, slots[i]);
+    if (slots[i] >= 0) taken.emplace_back(slots[i], i);
+  }
+  std::sort(taken.begin(), taken.end());
+  // the earliest token whose slot an earlier token already holds: in each run
+  // of equal slots (tokens ascending) the run's second token
+  int64_t row = -1, col = -1, value = 0;
+  for (size_t k = 1; k < taken.size(); ++k) {
+    const bool second = taken[k].first == taken[k - 1].first &&
+                        (k == 1 || taken[k - 1].first != taken[k - 2].first);
+    if (second && (row < 0 || taken[k].second < row)) {
+      row = taken[k].second;
+      col = taken[k - 1].second;
+      value = taken[k].first;
+    }
+  }
+  if (row >= 0) return fail(4, row, col, value);
+  return PKV_OK;
 }
 
 int pkv_release_workspaces(void) {

@@ -30,7 +30,7 @@ def test_library_exports_every_declared_symbol(pkv_lib):
 
 
 def test_status_strings(pkv_lib):
-    for code in range(8):
+    for code in range(10):
         assert pkv_lib.status_string(code).startswith("PKV_")
     assert "unknown" in pkv_lib.status_string(99)
 
@@ -201,3 +201,21 @@ def test_stage_copy_argument_checks(pkv_lib):
     assert lib.pkv_stage_copy(FAKE, None, 64, None) == NULL
     assert lib.pkv_stage_copy(FAKE + 8, FAKE, 64, None) == ALIGN
     assert lib.pkv_stage_copy(FAKE, FAKE + 4, 64, None) == ALIGN
+
+
+def test_validate_indices_argument_checks(pkv_lib):
+    """pkv_validate_indices checks sizes and pointers before copying anything."""
+    lib = pkv_lib.load_library()
+    err = pkv_lib._binding.IndexErrorInfo()
+    ref = ctypes.byref(err)
+    assert lib.pkv_validate_indices(None, 0, 0, None, None, 0, 0, 16, None, ref) == OK
+    assert err.what == 0
+    assert lib.pkv_validate_indices(None, 0, 4, None, None, 0, 10, 16, None, None) == OK
+    assert lib.pkv_validate_indices(FAKE, -1, 4, FAKE, None, 0, 10, 16, None, ref) == SHAPE
+    assert lib.pkv_validate_indices(FAKE, 2, -4, FAKE, None, 0, 10, 16, None, ref) == SHAPE
+    assert lib.pkv_validate_indices(FAKE, 2, 4, FAKE, None, -3, 10, 16, None, ref) == SHAPE
+    assert lib.pkv_validate_indices(FAKE, 2, 4, FAKE, None, 0, -1, 16, None, ref) == SHAPE
+    assert lib.pkv_validate_indices(FAKE, 2, 4, FAKE, None, 0, 10, 0, None, ref) == SHAPE
+    assert lib.pkv_validate_indices(None, 2, 4, FAKE, None, 0, 10, 16, None, ref) == NULL
+    assert lib.pkv_validate_indices(FAKE, 2, 4, None, None, 0, 10, 16, None, ref) == NULL
+    assert lib.pkv_validate_indices(None, 0, 4, None, None, 3, 10, 16, None, ref) == NULL
