@@ -23,7 +23,9 @@ import hashlib
 import json
 import math
 import os
+import platform
 import statistics
+import subprocess
 import sys
 import threading
 import time
@@ -210,8 +212,9 @@ class OracleSampler:
         self.q = w.q_steps[0].cpu()
         self.threads = oracle.max_threads()
 
-    def run(self, n_pairs, seed=0):
+    def run(self, n_pairs, seed=0, threads=None):
         spec = self.w.spec
+        threads = self.threads if threads is None else threads
         rng = np.random.default_rng(seed)
         total = spec.num_seqs * spec.num_q_heads
         flat = rng.choice(total, size=min(n_pairs, total), replace=False)
@@ -220,10 +223,10 @@ class OracleSampler:
         if spec.kv_fp8 or spec.kv_int8:
             decode = self.oracle.decode_fp8 if spec.kv_fp8 else self.oracle.decode_int8
             decode(self.q, self.kc, self.vc, self.ks, self.vs, self.bt, self.lens, spec.window,
-                   self.w.scale, pairs=pairs, threads=self.threads)
+                   self.w.scale, pairs=pairs, threads=threads)
         else:
             self.oracle.decode(self.q, self.kc, self.vc, self.bt, self.lens, spec.window,
-                               self.w.scale, pairs=pairs, threads=self.threads)
+                               self.w.scale, pairs=pairs, threads=threads)
         dt = time.perf_counter() - t0
         L = self.lens[pairs[:, 0]].astype(np.int64)
         lo = np.maximum(L - spec.window, 0) if spec.window > 0 else 0
@@ -231,6 +234,12 @@ class OracleSampler:
         row = spec.head_dim + 4 if (spec.kv_fp8 or spec.kv_int8) else spec.head_dim * self.e
         kvb = float(((L - lo) * 2 * row).sum()) / G
         return kvb / dt, dt, len(pairs)
+
+    def one_thread(self, pairs_per_s_all, target_s=3.0):
+        """The same float64 decode on one host thread, sized to about target_s
+        seconds if the threads scaled perfectly: (rate, seconds, pairs)."""
+        n = max(4, int(pairs_per_s_all * target_s / max(1, self.threads)))
+        return self.run(n, seed=1, threads=1)
 
     def rate_for(self, target_s):
         """Grow the sample until it takes about target_s seconds; when even the
@@ -285,7 +294,8 @@ def run_reference(args, workload):
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": {"workload": workload, "sample": desc},
         "cpu_baseline": {"value": gbs, "unit": "GB/s", "cores": sampler.threads,
-                         "kind": "oracle", "sample": desc},
+                         "kind": "oracle", "sample": desc, "cpu_model": host_cpu_model()},
+        "step_ms_percentiles": percentiles_ms([1e3 * t for t in times]),
         "e2e": {"value": gbs, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
@@ -304,6 +314,31 @@ PREFILL = {
                          head_dim=128, block_size=16, chunk=1024, prefix_lo=2048,
                          prefix_hi=6144, seed=11),
 }
+
+
+def host_cpu_model():
+    """The host CPU's model name (lscpu, else /proc/cpuinfo), for the baseline line."""
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.strip().lower().startswith("model name"):
+                return line.split(":", 1)[1].strip()
+    except Exception:
+        pass
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                if line.lower().startswith("model name"):
+                    return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    return platform.machine()
+
+
+def percentiles_ms(times_ms):
+    """p10 / p50 / p90 of per-step times (ms)."""
+    a = np.asarray(times_ms, dtype=np.float64)
+    return {f"p{q}": float(np.percentile(a, q)) for q in (10, 50, 90)}
 
 
 def run_prefill(args, pkv):
@@ -360,7 +395,8 @@ def run_prefill(args, pkv):
             graph.replay()
             ev[s][1].record(gstream)
         torch.cuda.synchronize()
-    ms = sum(a.elapsed_time(b) for a, b in ev) / args.steps
+    times = [a.elapsed_time(b) for a, b in ev]
+    ms = sum(times) / args.steps
     tflops = flops / (ms * 1e-3) / 1e12
     peak = None
     try:
@@ -379,6 +415,7 @@ def run_prefill(args, pkv):
                    "head_dim": d, "block_size": spec.block_size,
                    "l2": "flushed between steps (2x L2 written, then 2x L2 read)"},
         "tokens_per_s": T / (ms * 1e-3),
+        "step_ms_percentiles": percentiles_ms(times),
         "roofline": {"bound": "tensor", "kernel": "prefill (chunk append + attention)",
                      "achieved": tflops, "peak": peak, "unit": "TFLOP/s", "frac": tflops / peak,
                      "peak_kind": peak_kind,
@@ -553,9 +590,13 @@ def main(argv=None):
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         sampler = OracleSampler(w)
         rate, dt, got = sampler.rate_for(10.0)
+        rate1, dt1, got1 = sampler.one_thread(got / dt)
         cpu = {"value": rate / 1e9, "unit": "GB/s", "cores": sampler.threads, "kind": "oracle",
                "sample": f"{got} random (sequence, query head) pairs of step 0; {dt:.1f} s of "
-                         f"float64 decode on the host cores; K/V bytes of the sample / time"}
+                         f"float64 decode on the host cores; K/V bytes of the sample / time",
+               "cpu_model": host_cpu_model(),
+               "one_thread": {"value": rate1 / 1e9, "unit": "GB/s",
+                              "sample": f"{got1} pairs, {dt1:.1f} s on one thread"}}
 
     if rank == 0:
         line = {
@@ -578,6 +619,7 @@ def main(argv=None):
                 "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
             },
             "tokens_per_s": tokens_per_s,
+            "step_ms_percentiles": percentiles_ms(step_ms),
             "pct_of_hbm_peak": 100.0 * value / (world * peak),
             "path": "fused" if fused else "separate",
             "roofline": {"bound": "hbm",
