@@ -531,7 +531,7 @@ int pkv_prefill(const void* q, const void* k, const void* v, const int32_t* cu_q
   CUtensorMap kmap, vmap;
   rc = encode_pool_map(&kmap, k_cache, layout);
   if (rc != PKV_OK) return rc;
-  rc = encode_pool_map(&vmap, v_cache, layout);
+  rc = encode_decode_map(&vmap, v_cache, layout);  // 3-D for head_dim 128: one copy per V unit
   if (rc != PKV_OK) return rc;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   int device = 0;

@@ -79,6 +79,10 @@ struct TcLayout {
   static constexpr int kKBlocks = D / 64;                   // 128-byte column blocks
   static constexpr int kQTileBytes = kKBlocks * kQT * 128;
   static constexpr int kKVTile = kKBlocks * kTKeys * 128;   // K (or V) of one key tile
+  // V tiles are unit-major: unit u (16 keys) at u * kVUnitBytes, its 64-column
+  // blocks 2 KB apart, so one 3-D copy brings a unit's rows (K tiles keep
+  // each 64-column block of all 128 keys together, as the S product needs)
+  static constexpr int kVUnitBytes = kKBlocks * kUnitTokens * 128;
   static constexpr int kKOff = 2 * kQTileBytes;
   static constexpr int kVOff = kKOff + kKStages * kKVTile;
   static constexpr int kSmemBytes = kVOff + kVStages * kKVTile;
@@ -243,7 +247,8 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
       // Lane 0 posts the tile's byte count, then lane i copies unit i (its
       // K or V rows, one box per 64 columns): a copy takes tens of cycles to
       // issue, so the eight units go out side by side.
-      auto issue = [&](const CUtensorMap* map, uint32_t bar, uint32_t dst, int y, int loaded) {
+      auto issue = [&](const CUtensorMap* map, uint32_t bar, uint32_t dst, int y, int loaded,
+                       bool v_tile) {
         if (lane == 0) {
           if (loaded == 0)
             mbar_arrive(bar);
@@ -252,9 +257,19 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
         }
         __syncwarp();
         if (y >= 0) {
+          if (v_tile) {
+            // the V map of a 128-column pool is 3-D: both column blocks of the
+            // unit's 16 rows in one box
+            if constexpr (D == 128)
+              tma_load_3d(dst + lane * Lay::kVUnitBytes, map, 0, y, 0, bar);
+            else
+              tma_load_2d(dst + lane * Lay::kVUnitBytes, map, 0, y, bar);
+          } else {
 #pragma unroll
-          for (int kb = 0; kb < Lay::kKBlocks; ++kb)
-            tma_load_2d(dst + kb * kTKeys * 128 + lane * kUnitTokens * 128, map, kb * 64, y, bar);
+            for (int kb = 0; kb < Lay::kKBlocks; ++kb)
+              tma_load_2d(dst + kb * kTKeys * 128 + lane * kUnitTokens * 128, map, kb * 64, y,
+                          bar);
+          }
         }
       };
       // lane i < 8 holds the page row of unit i of the tile (-1 elsewhere)
@@ -274,11 +289,11 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
         if (j >= SK &&
             !mbar_wait_bounded(smem_u32(&k_empty[j % SK]), ((j / SK) - 1) & 1, kWaitLimit))
           bad = true;
-        issue(&kmap, smem_u32(&k_full[j % SK]), k_addr(j), y_cur, loaded);
+        issue(&kmap, smem_u32(&k_full[j % SK]), k_addr(j), y_cur, loaded, false);
         if (j >= SV &&
             !mbar_wait_bounded(smem_u32(&v_empty[j % SV]), ((j / SV) - 1) & 1, kWaitLimit))
           bad = true;
-        issue(&vmap, smem_u32(&v_full[j % SV]), v_addr(j), y_cur, loaded);
+        issue(&vmap, smem_u32(&v_full[j % SV]), v_addr(j), y_cur, loaded, true);
         y_next = page_y(t0n, pb_next);
       }
       // every copy started has landed (already waited for unless a wait ran out)
@@ -301,7 +316,8 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
         if (kBf16) {
 #pragma unroll 4
           for (int u = ct; u < Lay::kKVTile / 16; u += kPrepThreads) {  // 16-byte chunks
-            const int kp = t0 + ((u & (kTKeys * 8 - 1)) >> 3);
+            // chunk u: unit u / (kVUnitBytes / 16), row (u / 8) % 16 of it
+            const int kp = t0 + (u / (Lay::kVUnitBytes / 16)) * kUnitTokens + ((u >> 3) & 15);
             uint4 x = ld_shared_v4(vt + u * 16);
             if (!whole && (kSinks ? !key_kept(j, kp) : (kp < k_lo || kp > pos1))) {
               x = make_uint4(0u, 0u, 0u, 0u);
@@ -321,7 +337,9 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
             for (int kb = 0; kb < Lay::kKBlocks; ++kb)
 #pragma unroll
               for (int c = 0; c < 8; ++c)
-                st_shared_v4(vt + kb * kTKeys * 128 + r * 128 + c * 16, make_uint4(0u, 0u, 0u, 0u));
+                st_shared_v4(vt + (r >> 4) * Lay::kVUnitBytes + kb * kUnitTokens * 128 +
+                                 (r & 15) * 128 + c * 16,
+                             make_uint4(0u, 0u, 0u, 0u));
           }
         }
         fence_proxy_async_smem();
@@ -363,9 +381,10 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
         // they announce P_0(j): acquiring p_full[0] orders them before the
         // products below, so this thread waits only for the two P tiles.
         for (int j = 0; j < n_tiles; ++j) {
-          // V: keys are the K dimension (8-row groups 1 KB apart, 16 keys a
-          // step), head dims the N dimension (64-column blocks a tile apart)
-          const uint64_t v0 = umma_sdesc_sw128(v_addr(j), kTKeys * 128, 1024);
+          // V: keys are the K dimension (8-row groups 1 KB apart; a step of
+          // 16 keys is one unit), head dims the N dimension (64-column blocks
+          // 2 KB apart inside the unit)
+          const uint64_t v0 = umma_sdesc_sw128(v_addr(j), kUnitTokens * 128, 1024);
 #pragma unroll
           for (int t = 0; t < 2; ++t) {
             if (!mbar_wait_bounded(smem_u32(&p_full[t]), j & 1, kWaitLimit)) bad = true;
@@ -373,7 +392,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
 #pragma unroll
             for (int kk = 0; kk < kTKeys / 16; ++kk)
               umma_f16_ts(tmem + Lay::o_col(t), tmem + Lay::s_col(t) + kk * 8,
-                          v0 + static_cast<uint64_t>((kk * 16 * 128) >> 4), kIdO,
+                          v0 + static_cast<uint64_t>((kk * Lay::kVUnitBytes) >> 4), kIdO,
                           (j > 0 || kk > 0) ? 1u : 0u);
             if (j + 1 == n_tiles) umma_commit(smem_u32(&o_done[t]));  // O_t final
             if (t == 1) umma_commit(smem_u32(&v_empty[j % SV]));

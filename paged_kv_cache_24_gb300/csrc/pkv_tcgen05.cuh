@@ -8,6 +8,17 @@
 
 namespace pkv {
 
+// 3-D tiled load of the box at (x, y, z) into shared memory; completion is
+// signalled as transaction bytes on `bar`.
+__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map, int32_t x,
+                                            int32_t y, int32_t z, uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(bar)
+      : "memory");
+}
+
 // ---- tcgen05 (5th-generation tensor cores, accumulators in TMEM) -----------
 
 // Shared-memory matrix descriptor for a 128-byte-swizzled operand tile whose
