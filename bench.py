@@ -94,17 +94,25 @@ def step_bytes(w):
     B, hq, hkv, d, bs = (spec.num_seqs, spec.num_q_heads, spec.num_kv_heads, spec.head_dim,
                          spec.block_size)
     out = []
+    tables = w.block_tables.cpu().numpy().astype(np.int64)
     for s in range(w.steps):
         L = w.lens_steps[s].cpu().numpy().astype(np.int64)
         lo = np.maximum(L - spec.window, 0) if spec.window > 0 else np.zeros_like(L)
         ctx = int((L - lo).sum())
+        # distinct pool rows the step attends (sequences that share prefix
+        # blocks read those rows once from DRAM at best)
+        t = np.concatenate([np.arange(a, b) for a, b in zip(lo, L)] or [np.zeros(0, np.int64)])
+        seq = np.repeat(np.arange(B), L - lo)
+        rows = tables[seq, t // bs] * bs + t % bs
+        kv_unique = int(np.unique(rows).size) * 2 * hkv * row
         pages = int((((L - 1) // bs) - (lo // bs) + 1).clip(min=0).sum())
         kv = ctx * 2 * hkv * row            # one K row and one V row per (token, kv head)
         qo = 2 * B * hq * d * e
         meta = pages * 4 + B * 4
         append = B * hkv * (d * e + d_row) * 2 + B * 8  # new rows read, pool rows written
         out.append({"kv": kv, "decode": kv + qo + meta, "append": append,
-                    "step": kv + qo + meta + append, "tokens_kvhead": ctx * hkv})
+                    "step": kv + qo + meta + append, "tokens_kvhead": ctx * hkv,
+                    "step_unique": kv_unique + qo + meta + append})
     return out
 
 
@@ -568,6 +576,7 @@ def main(argv=None):
     # the step time: whole loop / K when nothing else ran in it, else the sum of steps
     total_ms = sum(step_ms) if need_flush else loop_ms
     my_bytes = sum(sbytes[s % S]["step"] for s in range(args.steps))
+    my_unique = sum(sbytes[s % S]["step_unique"] for s in range(args.steps))
     dec_key = "step" if fused else "decode"  # the fused launch also does the append
     my_dec_bytes = sum(sbytes[s % S][dec_key] for s in range(args.steps))
 
@@ -620,6 +629,12 @@ def main(argv=None):
             },
             "tokens_per_s": tokens_per_s,
             "step_ms_percentiles": percentiles_ms(step_ms),
+            # the same step counted on distinct pool rows (shared prefix blocks once)
+            # (every rank's workload has the same shape: rank 0's count x ranks)
+            "unique_rows": {"value": world * my_unique / (total_ms_all * 1e-3) / 1e9,
+                            "unit": "GB/s", "bytes_per_step": my_unique / args.steps,
+                            "pct_of_hbm_peak": 100.0 * my_unique / (total_ms_all * 1e-3) / 1e9
+                            / peak},
             "pct_of_hbm_peak": 100.0 * value / (world * peak),
             "path": "fused" if fused else "separate",
             "roofline": {"bound": "hbm",
