@@ -136,6 +136,14 @@ SMALL.append(("mid_grid_bf16_bs64", dict(dtype=torch.bfloat16, num_seqs=20, num_
                                          explicit_pool=None, lens_are_pre_append=False),
                       (0, 32)))
 
+# the largest batch the decode grid takes (65535 sequences), with empty and
+# one-token contexts among them
+SMALL.append(("max_sequences_fp16_d64", dict(dtype=torch.float16, num_seqs=65535, num_q_heads=2,
+                                             num_kv_heads=1, head_dim=64, block_size=16,
+                                             lens=_r.integers(0, 33, 65535).tolist(),
+                                             explicit_pool=None, lens_are_pre_append=False),
+                      (0,)))
+
 # splits longer than 32 units per warp: each warp resolves its pages 32 units
 # at a time
 SMALL.append(("long_split_fp16", dict(dtype=torch.float16, num_seqs=5, num_q_heads=4,

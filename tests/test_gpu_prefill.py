@@ -76,6 +76,10 @@ CASES = [
 _r = np.random.default_rng(29)
 CASES.append(("many_seqs", torch.float16, 8, 2, 128, 16, _r.integers(0, 600, 300).tolist(),
               _r.integers(1, 140, 300).tolist(), 0))
+# the largest batch the prefill takes (65534 sequences): one work item each,
+# prefixes from empty up
+CASES.append(("max_sequences", torch.float16, 2, 1, 64, 16, _r.integers(0, 40, 65534).tolist(),
+              _r.integers(1, 4, 65534).tolist(), 0))
 # more than 1024 work items (16 tokens per CTA at 16 query heads per kv head):
 # the planner sizes the items past its per-thread register cache twice
 CASES.append(("many_items", torch.bfloat16, 16, 1, 128, 16, _r.integers(0, 300, 90).tolist(),

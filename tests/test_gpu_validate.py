@@ -70,3 +70,24 @@ def test_slots_from_the_library_are_valid(pkv_lib):
     nb = w.k_cache.shape[0]
     assert pkv_lib.pkv_validate_indices(w.block_tables, w.lens_steps[0].contiguous(), nb,
                                         w.spec.block_size, slot_mapping=slots) is None
+
+
+def test_flagged_indices_are_the_ones_decode_marks(pkv_lib):
+    """Every sequence the check would flag comes back NaN from the decode, and
+    only those: the check and the kernels agree on what a bad index is."""
+    dt = torch.bfloat16
+    q = torch.randn(4, 8, 128, device="cuda").to(dt)
+    kc = torch.randn(6, 2, 16, 128, device="cuda").to(dt)
+    vc = torch.randn_like(kc)
+    bt = torch.tensor([[0, 1], [2, 99], [3, -5], [4, 5]], dtype=torch.int32, device="cuda")
+    lens = torch.tensor([20, 20, 20, 33], dtype=torch.int32, device="cuda")
+    out = pkv_lib.pkv_decode(q, kc, vc, bt, lens, 0, 0.1)
+    torch.cuda.synchronize()
+    flagged = []
+    for b in range(4):
+        one = pkv_lib.pkv_validate_indices(bt[b:b + 1].contiguous(), lens[b:b + 1].contiguous(),
+                                           6, 16)
+        flagged.append(one is not None)
+        assert flagged[-1] == bool(torch.isnan(out[b].float()).any())
+    assert flagged == [False, True, True, True]
+    assert pkv_lib.pkv_validate_indices(bt, lens, 6, 16) == ("context_length", 3, 0, 33)
