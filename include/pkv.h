@@ -23,6 +23,8 @@
  *   - Pointers named *_cache, q, k, v, out, block_tables, context_lens,
  *     positions and slot_mapping are DEVICE pointers on the current CUDA
  *     device; the caller owns them.  Data pointers must be 16-byte aligned.
+ *     A decode's `out` may also be the device-side address of pinned host
+ *     memory (pkv_device_address): the kernels then write the result there.
  *   - `stream` is a cudaStream_t (NULL = legacy default stream).  Every call
  *     only enqueues work on it and returns without synchronising, except
  *     where stated.
@@ -75,6 +77,17 @@ typedef struct pkv_cache_layout {
   int32_t head_dim;     /* D: 64 or 128                                            */
   int32_t dtype;        /* pkv_dtype of the pool, and of q, k, v and out           */
 } pkv_cache_layout;
+
+/*
+ * pkv_device_address -- the address through which this library's kernels
+ *   reach `p`: p itself for device or managed memory, the mapped device-side
+ *   address for pinned host memory.  Pageable or unknown host memory:
+ *   PKV_ERR_UNSUPPORTED and *device_address = NULL.  Host-only: launches
+ *   nothing and does not synchronise.  Not an operation of the pages: a
+ *   decode's `out` may be such an address of pinned host memory, so that the
+ *   result is written straight to the host (what DecodeStep does).
+ */
+int pkv_device_address(const void* p, void** device_address);
 
 /*
  * pkv_stage_copy -- copy `bytes` from src to dst with a kernel on `stream`.

@@ -20,6 +20,9 @@ Public API (thin wrappers over the C ABI of ``libpkv.so``, see include/pkv.h):
   paged cache;
 * ``pkv_stage_copy(dst, src)`` -- a kernel copy between device memory and
   pinned host memory (DecodeStep's host transfers);
+* ``pkv_device_address(t)`` -- the address the kernels use for a device or
+  pinned host tensor (a decode may write its ``out`` straight to pinned host
+  memory);
 * ``pkv_validate_indices(block_tables, context_lens, num_blocks, block_size,
   slot_mapping=None)`` -- debug check of the indices the kernels trust
   (waits for the stream).
@@ -33,7 +36,8 @@ benchmark.
 """
 from ._binding import (CacheLayout, DecodeOptions, PkvError, cache_layout, library_path, load_library,
                        pkv_append, pkv_append_decode, pkv_append_fp8, pkv_append_int8, pkv_decode, pkv_prefill, pkv_decode_plan, pkv_release_workspaces,
-                       pkv_slot_mapping, pkv_stage_copy, pkv_validate_indices, status_string,
+                       pkv_device_address, pkv_slot_mapping, pkv_stage_copy,
+                       pkv_validate_indices, status_string,
                        PKV_ERR_RANGE, PKV_ERR_UNSUPPORTED)
 from .step import DecodeStep
 
@@ -41,6 +45,6 @@ __all__ = [
     "DecodeStep", "DecodeOptions", "CacheLayout", "PkvError", "cache_layout", "library_path", "load_library", "pkv_append",
     "pkv_append_decode", "pkv_append_fp8", "pkv_append_int8", "pkv_prefill",
     "pkv_decode", "pkv_decode_plan", "pkv_release_workspaces", "pkv_slot_mapping", "pkv_stage_copy",
-    "pkv_validate_indices", "PKV_ERR_RANGE", "PKV_ERR_UNSUPPORTED",
+    "pkv_validate_indices", "pkv_device_address", "PKV_ERR_RANGE", "PKV_ERR_UNSUPPORTED",
     "status_string",
 ]

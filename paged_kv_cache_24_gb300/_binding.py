@@ -96,6 +96,7 @@ def load_library():
             "pkv_release_workspaces": [],
             "pkv_validate_indices": [vp, i32, i32, vp, vp, i64, i64, i32, vp,
                                      ctypes.POINTER(IndexErrorInfo)],
+            "pkv_device_address": [vp, ctypes.POINTER(vp)],
         }
         for name, args in sig.items():
             fn = getattr(lib, name)
@@ -167,6 +168,28 @@ def _on_cuda(*ts) -> None:
             raise ValueError("libpkv operates on CUDA tensors only")
 
 
+def pkv_device_address(t: torch.Tensor) -> int | None:
+    """The address through which the library's kernels reach t's memory (device
+    memory, or pinned host memory), or None for pageable host memory."""
+    addr = ctypes.c_void_p()
+    rc = load_library().pkv_device_address(ctypes.c_void_p(t.data_ptr()), ctypes.byref(addr))
+    if rc == PKV_ERR_UNSUPPORTED:
+        return None
+    _check("pkv_device_address", rc)
+    return addr.value
+
+
+def _out_address(out: torch.Tensor) -> int:
+    """A decode's output: a CUDA tensor, or a pinned host tensor the kernels write
+    directly (the result then needs no copy back)."""
+    if out.device.type == "cuda":
+        return out.data_ptr()
+    _require(out.is_pinned(), "out must be a CUDA tensor or pinned host memory")
+    addr = pkv_device_address(out)
+    _require(addr is not None, "this GPU cannot address the pinned output buffer")
+    return addr
+
+
 def pkv_stage_copy(dst: torch.Tensor, src: torch.Tensor, nbytes: int | None = None,
                    stream=None) -> int:
     """Copy the first nbytes (default: all) of src into dst with a kernel; either
@@ -225,8 +248,9 @@ def pkv_decode(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
                v_scale: torch.Tensor | None = None) -> torch.Tensor:
     """Decode attention of q [B, Hq, D] over the paged context; returns out [B, Hq, D].
     With a window, ``num_sinks`` first positions are attended as well.  8-bit pools
-    (uint8 E4M3 or int8 codes) take their row scales and fp16 q."""
-    _on_cuda(q, k_cache, v_cache, block_tables, context_lens, out, k_scale, v_scale)
+    (uint8 E4M3 or int8 codes) take their row scales and fp16 q.  ``out`` may be a
+    pinned host tensor: the kernels then write the result straight into it."""
+    _on_cuda(q, k_cache, v_cache, block_tables, context_lens, k_scale, v_scale)
     layout = cache_layout(k_cache)
     _require(v_cache.shape == k_cache.shape and v_cache.dtype == k_cache.dtype
              and v_cache.is_contiguous(), "v_cache must match k_cache")
@@ -248,8 +272,8 @@ def pkv_decode(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
                          _ptr(k_scale) or None, _ptr(v_scale) or None)
     _check("pkv_decode", load_library().pkv_decode_ex(
         _ptr(q), B, Hq, _ptr(k_cache), _ptr(v_cache), ctypes.byref(layout),
-        _ptr(block_tables), block_tables.shape[1], _ptr(context_lens), float(scale), _ptr(out),
-        ctypes.byref(opts), _stream(stream)))
+        _ptr(block_tables), block_tables.shape[1], _ptr(context_lens), float(scale),
+        _out_address(out), ctypes.byref(opts), _stream(stream)))
     return out
 
 
@@ -335,8 +359,9 @@ def pkv_append_decode(q: torch.Tensor, k_new: torch.Tensor, v_new: torch.Tensor,
                       out: torch.Tensor | None = None, tokens_per_split: int = 0,
                       stream=None, num_sinks: int = 0) -> torch.Tensor:
     """Append each sequence's new token (at position context_lens[b] - 1) and
-    decode, in one launch; same result as the separate calls."""
-    _on_cuda(q, k_new, v_new, k_cache, v_cache, block_tables, context_lens, out)
+    decode, in one launch; same result as the separate calls.  ``out`` may be a
+    pinned host tensor, as for ``pkv_decode``."""
+    _on_cuda(q, k_new, v_new, k_cache, v_cache, block_tables, context_lens)
     layout = cache_layout(k_cache)
     _require(v_cache.shape == k_cache.shape and v_cache.dtype == k_cache.dtype
              and v_cache.is_contiguous(), "v_cache must match k_cache")
@@ -361,8 +386,8 @@ def pkv_append_decode(q: torch.Tensor, k_new: torch.Tensor, v_new: torch.Tensor,
                          _ptr(v_new), None, None)
     _check("pkv_append_decode", load_library().pkv_decode_ex(
         _ptr(q), B, Hq, _ptr(k_cache), _ptr(v_cache), ctypes.byref(layout), _ptr(block_tables),
-        block_tables.shape[1], _ptr(context_lens), float(scale), _ptr(out), ctypes.byref(opts),
-        _stream(stream)))
+        block_tables.shape[1], _ptr(context_lens), float(scale), _out_address(out),
+        ctypes.byref(opts), _stream(stream)))
     return out
 
 

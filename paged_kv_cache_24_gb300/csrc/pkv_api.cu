@@ -426,6 +426,16 @@ static const void* device_side(const void* p) {
   return nullptr;
 }
 
+int pkv_device_address(const void* p, void** device_address) {
+  if (!device_address) return PKV_ERR_NULL;
+  *device_address = nullptr;
+  if (!p) return PKV_ERR_NULL;
+  const void* d = device_side(p);
+  if (!d) return PKV_ERR_UNSUPPORTED;
+  *device_address = const_cast<void*>(d);
+  return PKV_OK;
+}
+
 int pkv_stage_copy(void* dst, const void* src, int64_t bytes, void* stream) {
   if (bytes < 0) return PKV_ERR_SHAPE;
   if (bytes == 0) return PKV_OK;

@@ -10,8 +10,9 @@ from paged_kv_cache_24_gb300.workloads import config_spec, make_workload
 pytestmark = pytest.mark.gpu
 
 
+@pytest.mark.parametrize("direct_out", [False, True])
 @pytest.mark.parametrize("fused", [True, False])
-def test_decode_step_graph_matches_eager_and_oracle(pkv_lib, oracle_lib, fused):
+def test_decode_step_graph_matches_eager_and_oracle(pkv_lib, oracle_lib, fused, direct_out):
     pkv = pkv_lib
     spec = config_spec(4, num_seqs=24, num_q_heads=16, num_kv_heads=4, steps=3, seed=9)
     w = make_workload(spec, device="cuda")
@@ -19,7 +20,9 @@ def test_decode_step_graph_matches_eager_and_oracle(pkv_lib, oracle_lib, fused):
     kc_h, vc_h = w.k_cache.cpu(), w.v_cache.cpu()
     bt_h = w.block_tables.cpu().numpy()
     step = pkv.DecodeStep(w.k_cache, w.v_cache, spec.num_seqs, spec.num_q_heads, w.max_blocks,
-                          spec.window, w.scale, num_buffers=spec.steps, fused=fused)
+                          spec.window, w.scale, num_buffers=spec.steps, fused=fused,
+                          direct_out=direct_out)
+    assert step.direct_out == direct_out
     for s in range(spec.steps):
         h = step.host[s]
         h["q"].copy_(w.q_steps[s]); h["k"].copy_(w.k_steps[s]); h["v"].copy_(w.v_steps[s])
