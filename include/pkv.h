@@ -335,7 +335,7 @@ int pkv_decode_plan(int32_t num_seqs, int32_t num_q_heads, const pkv_cache_layou
  *   buffer (num_splits from pkv_decode_plan; a problem that needs no split
  *   uses no scratch); otherwise PKV_ERR_SCRATCH and nothing is launched.
  *   8-bit pools (FP8, INT8) need row scales this call does not take:
- *   PKV_ERR_UNSUPPORTED.
+ *   PKV_ERR_UNSUPPORTED (pkv_decode_noalloc_ex takes them).
  *   Set-up: the first call on each device looks up the buffer's device address
  *   (cudaGetSymbolAddress) with that device current; make that first call
  *   before any stream capture.
@@ -350,6 +350,20 @@ int pkv_decode_noalloc(const void* q, int32_t num_seqs, int32_t num_q_heads,
                        const int32_t* block_tables, int32_t max_blocks_per_seq,
                        const int32_t* context_lens, int32_t window, float scale, void* out,
                        void* stream);
+
+/*
+ * pkv_decode_noalloc_ex -- pkv_decode_ex (window, attention sinks, tokens
+ * per split, fused append rows, 8-bit pools with their row scales) with the
+ * fixed scratch buffer of pkv_decode_noalloc instead of an allocated
+ * workspace: the arguments and results of pkv_decode_ex, the limit, set-up
+ * and sharing rules of pkv_decode_noalloc (PKV_ERR_SCRATCH beyond the
+ * buffer).
+ */
+int pkv_decode_noalloc_ex(const void* q, int32_t num_seqs, int32_t num_q_heads, void* k_cache,
+                          void* v_cache, const pkv_cache_layout* layout,
+                          const int32_t* block_tables, int32_t max_blocks_per_seq,
+                          const int32_t* context_lens, float scale, void* out,
+                          const pkv_decode_options* options, void* stream);
 
 /*
  * pkv_validate_indices -- debug aid, not part of the hot path: range-check

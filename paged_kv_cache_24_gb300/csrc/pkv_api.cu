@@ -241,7 +241,8 @@ int decode_impl(const void* q, const void* k_new, const void* v_new, int32_t num
                 const pkv_cache_layout* layout, const int32_t* block_tables,
                 int32_t max_blocks_per_seq, const int32_t* context_lens, int32_t window,
                 int32_t num_sinks, float scale, void* out, int32_t tokens_per_split,
-                void* stream, const float* k_scale = nullptr, const float* v_scale = nullptr) {
+                void* stream, const float* k_scale = nullptr, const float* v_scale = nullptr,
+                bool fixed_scratch = false) {
   int rc = check_decode_args(q, num_seqs, num_q_heads, k_cache, v_cache, layout, block_tables,
                              max_blocks_per_seq, context_lens, out);
   if (rc != PKV_OK) return rc;
@@ -295,8 +296,15 @@ int decode_impl(const void* q, const void* k_new, const void* v_new, int32_t num
   if (plan.num_splits > 1) {
     const size_t rows = static_cast<size_t>(num_seqs) * num_q_heads * plan.num_splits;
     const size_t o_bytes = rows * layout->head_dim * sizeof(float);
+    const size_t need = o_bytes + rows * sizeof(float2);
     void* ws = nullptr;
-    rc = get_workspace(device, st, o_bytes + rows * sizeof(float2), &ws);
+    if (fixed_scratch) {
+      // the buffer in the library image (pkv_noalloc.cu): no allocation
+      if (need > PKV_NOALLOC_SCRATCH_BYTES) return PKV_ERR_SCRATCH;
+      rc = pkv::noalloc_scratch(device, &ws);
+    } else {
+      rc = get_workspace(device, st, need, &ws);
+    }
     if (rc != PKV_OK) return rc;
     p.part_o = static_cast<float*>(ws);
     p.part_ml = reinterpret_cast<float2*>(static_cast<char*>(ws) + o_bytes);
@@ -326,34 +334,7 @@ int decode_impl(const void* q, const void* k_new, const void* v_new, int32_t num
 
 }  // namespace
 
-namespace pkv {
-// Host helpers shared with the fixed-scratch entry point (pkv_noalloc.cu).
-int decode_checks(const void* q, int32_t num_seqs, int32_t num_q_heads, const void* k_cache,
-                  const void* v_cache, const pkv_cache_layout* layout,
-                  const int32_t* block_tables, int32_t max_blocks, const int32_t* context_lens,
-                  const void* out) {
-  return check_decode_args(q, num_seqs, num_q_heads, k_cache, v_cache, layout, block_tables,
-                           max_blocks, context_lens, out);
-}
-int decode_plan(int num_seqs, int num_q_heads, const pkv_cache_layout* layout, int max_blocks,
-                int window, int num_sinks, int* head_chunk, int* num_head_chunks, int* ntiles,
-                int* units_per_split, int* num_splits) {
-  Plan plan;
-  int rc = make_plan(num_seqs, num_q_heads, layout, max_blocks, window, num_sinks, 0,
-                     sm_count_of_current_device(), &plan);
-  if (rc != PKV_OK) return rc;
-  *head_chunk = plan.head_chunk;
-  *num_head_chunks = plan.num_head_chunks;
-  *ntiles = plan.ntiles;
-  *units_per_split = plan.units_per_split;
-  *num_splits = plan.num_splits;
-  return PKV_OK;
-}
-int pool_tensor_map(CUtensorMap* map, const void* pool, const pkv_cache_layout* layout) {
-  return encode_decode_map(map, pool, layout);
-}
-int status_of(cudaError_t e) { return to_status(e); }
-}  // namespace pkv
+
 
 // Quantising append into an 8-bit pool (E4M3 or int8 codes).
 static int append_q8(bool int8, const void* k, const void* v, int32_t in_dtype,
@@ -494,10 +475,12 @@ int pkv_decode_split(const void* q, int32_t num_seqs, int32_t num_q_heads,
                      tokens_per_split, stream);
 }
 
-int pkv_decode_ex(const void* q, int32_t num_seqs, int32_t num_q_heads, void* k_cache,
-                  void* v_cache, const pkv_cache_layout* layout, const int32_t* block_tables,
-                  int32_t max_blocks_per_seq, const int32_t* context_lens, float scale, void* out,
-                  const pkv_decode_options* options, void* stream) {
+static int decode_options_impl(const void* q, int32_t num_seqs, int32_t num_q_heads,
+                               void* k_cache, void* v_cache, const pkv_cache_layout* layout,
+                               const int32_t* block_tables, int32_t max_blocks_per_seq,
+                               const int32_t* context_lens, float scale, void* out,
+                               const pkv_decode_options* options, void* stream,
+                               bool fixed_scratch) {
   if (!options) return PKV_ERR_NULL;
   if (num_seqs > 0 && (options->k_new != nullptr) != (options->v_new != nullptr))
     return PKV_ERR_NULL;
@@ -507,7 +490,39 @@ int pkv_decode_ex(const void* q, int32_t num_seqs, int32_t num_q_heads, void* k_
   return decode_impl(q, options->k_new, options->v_new, num_seqs, num_q_heads, k_cache, v_cache,
                      layout, block_tables, max_blocks_per_seq, context_lens, options->window,
                      options->num_sinks, scale, out, options->tokens_per_split, stream,
-                     options->k_scale, options->v_scale);
+                     options->k_scale, options->v_scale, fixed_scratch);
+}
+
+int pkv_decode_ex(const void* q, int32_t num_seqs, int32_t num_q_heads, void* k_cache,
+                  void* v_cache, const pkv_cache_layout* layout, const int32_t* block_tables,
+                  int32_t max_blocks_per_seq, const int32_t* context_lens, float scale, void* out,
+                  const pkv_decode_options* options, void* stream) {
+  return decode_options_impl(q, num_seqs, num_q_heads, k_cache, v_cache, layout, block_tables,
+                             max_blocks_per_seq, context_lens, scale, out, options, stream,
+                             false);
+}
+
+int pkv_decode_noalloc_ex(const void* q, int32_t num_seqs, int32_t num_q_heads, void* k_cache,
+                          void* v_cache, const pkv_cache_layout* layout,
+                          const int32_t* block_tables, int32_t max_blocks_per_seq,
+                          const int32_t* context_lens, float scale, void* out,
+                          const pkv_decode_options* options, void* stream) {
+  return decode_options_impl(q, num_seqs, num_q_heads, k_cache, v_cache, layout, block_tables,
+                             max_blocks_per_seq, context_lens, scale, out, options, stream,
+                             true);
+}
+
+int pkv_decode_noalloc(const void* q, int32_t num_seqs, int32_t num_q_heads,
+                       const void* k_cache, const void* v_cache, const pkv_cache_layout* layout,
+                       const int32_t* block_tables, int32_t max_blocks_per_seq,
+                       const int32_t* context_lens, int32_t window, float scale, void* out,
+                       void* stream) {
+  // 8-bit pools need row scales, which this form does not take
+  if (layout && (layout->dtype == PKV_FP8_E4M3 || layout->dtype == PKV_INT8))
+    return PKV_ERR_UNSUPPORTED;
+  return decode_impl(q, nullptr, nullptr, num_seqs, num_q_heads, k_cache, v_cache, layout,
+                     block_tables, max_blocks_per_seq, context_lens, window, 0, scale, out, 0,
+                     stream, nullptr, nullptr, true);
 }
 
 int pkv_prefill(const void* q, const void* k, const void* v, const int32_t* cu_q,

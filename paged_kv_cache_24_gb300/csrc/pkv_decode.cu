@@ -892,10 +892,6 @@ cudaError_t launch16(const CUtensorMap& kmap, const CUtensorMap& vmap, const Dec
 
 }  // namespace
 
-size_t decode_16bit_smem_bytes(int head_dim) {
-  return head_dim == 128 ? Tile16<128, false>::kSmemBytes : Tile16<64, false>::kSmemBytes;
-}
-
 cudaError_t launch_decode_q8(bool int8, int ntiles, const CUtensorMap& kmap,
                              const CUtensorMap& vmap, const DecodeParams& p, cudaStream_t stream) {
   if (int8) {

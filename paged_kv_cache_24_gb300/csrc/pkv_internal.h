@@ -137,24 +137,8 @@ cudaError_t launch_slot_mapping(const int32_t* block_tables, int num_seqs, int m
                                 const int64_t* positions, int block_size, int64_t* slots,
                                 cudaStream_t stream);
 
-// Dynamic shared memory the 16-bit decode kernel needs for a head_dim.
-size_t decode_16bit_smem_bytes(int head_dim);
-
-}  // namespace pkv
-
-struct pkv_cache_layout;
-
-namespace pkv {
-
-// Host helpers of the C-ABI layer, reused by the fixed-scratch entry point.
-int decode_checks(const void* q, int32_t num_seqs, int32_t num_q_heads, const void* k_cache,
-                  const void* v_cache, const pkv_cache_layout* layout,
-                  const int32_t* block_tables, int32_t max_blocks, const int32_t* context_lens,
-                  const void* out);
-int decode_plan(int num_seqs, int num_q_heads, const pkv_cache_layout* layout, int max_blocks,
-                int window, int num_sinks, int* head_chunk, int* num_head_chunks, int* ntiles,
-                int* units_per_split, int* num_splits);
-int pool_tensor_map(CUtensorMap* map, const void* pool, const pkv_cache_layout* layout);
-int status_of(cudaError_t e);
+// Device address of the library-resident split-K scratch buffer
+// (PKV_NOALLOC_SCRATCH_BYTES) on `device`, which must be current.
+int noalloc_scratch(int device, void** addr);
 
 }  // namespace pkv

@@ -154,6 +154,20 @@ def test_quantised_pool_argument_checks(pkv_lib):
         assert lib.pkv_decode_noalloc(vp(FAKE), 4, 32, vp(FAKE), vp(FAKE),
                                       ctypes.byref(_layout(pkv, dt=dt)), vp(FAKE), 8, vp(FAKE),
                                       0, ctypes.c_float(0.1), vp(FAKE), None) == UNSUP
+        # the options form takes the scales; without them: NULL, before any CUDA call
+        lib.pkv_decode_noalloc_ex.argtypes = [vp, ctypes.c_int32, ctypes.c_int32, vp, vp,
+                                              ctypes.POINTER(pkv.CacheLayout), vp,
+                                              ctypes.c_int32, vp, ctypes.c_float, vp,
+                                              ctypes.POINTER(pkv.DecodeOptions), vp]
+        opts = pkv.DecodeOptions(0, 0, 0, None, None, None, None)
+        assert lib.pkv_decode_noalloc_ex(vp(FAKE), 4, 32, vp(FAKE), vp(FAKE),
+                                         ctypes.byref(_layout(pkv, dt=dt)), vp(FAKE), 8,
+                                         vp(FAKE), ctypes.c_float(0.1), vp(FAKE),
+                                         ctypes.byref(opts), None) == NULL
+        assert lib.pkv_decode_noalloc_ex(vp(FAKE), 4, 32, vp(FAKE), vp(FAKE),
+                                         ctypes.byref(_layout(pkv, dt=dt)), vp(FAKE), 8,
+                                         vp(FAKE), ctypes.c_float(0.1), vp(FAKE), None,
+                                         None) == NULL
 
     def app(fn, dt, in_dtype=1, ks=FAKE, n=3):
         lay = _layout(pkv, dt=dt)

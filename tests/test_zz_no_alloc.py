@@ -91,3 +91,62 @@ def test_noalloc_rejects_problems_beyond_its_scratch(pkv_lib):
     rc = _call_noalloc(pkv, fn, q, kc, kc, bt, lens, 0, 0.1, out)
     assert rc == PKV_ERR_SCRATCH
     assert "scratch" in pkv.status_string(rc)
+
+
+def _noalloc_ex(pkv):
+    lib = pkv.load_library()
+    fn = lib.pkv_decode_noalloc_ex
+    vp, i32 = ctypes.c_void_p, ctypes.c_int32
+    fn.argtypes = [vp, i32, i32, vp, vp, ctypes.POINTER(pkv.CacheLayout), vp, i32, vp,
+                   ctypes.c_float, vp, ctypes.POINTER(pkv.DecodeOptions), vp]
+    fn.restype = ctypes.c_int
+    return fn
+
+
+@pytest.mark.parametrize("kind", ["sinks_window", "fused_append", "fp8", "int8"])
+def test_noalloc_ex_matches_decode_ex_bit_for_bit(pkv_lib, oracle_lib, kind):
+    """The options form runs the same plan and kernels as pkv_decode_ex, only
+    with the library's scratch: the outputs (and pools) agree bit for bit."""
+    pkv = pkv_lib
+    fn = _noalloc_ex(pkv)
+    q8 = kind in ("fp8", "int8")
+    spec = config_spec(0, dtype=torch.float16, num_seqs=5, num_q_heads=16, num_kv_heads=4,
+                       head_dim=128, block_size=16, lens=[1, 60, 900, 2500, 4100],
+                       explicit_pool=None, lens_are_pre_append=False,
+                       window=700 if kind == "sinks_window" else 0,
+                       num_sinks=5 if kind == "sinks_window" else 0,
+                       kv_fp8=kind == "fp8", kv_int8=kind == "int8")
+    outs, pools = [], []
+    for noalloc in (False, True):
+        w = make_workload(spec, device="cuda", poison=True)
+        lens = w.lens_steps[0].contiguous()
+        fused = kind == "fused_append"
+        if not fused:
+            slots = pkv.pkv_slot_mapping(w.block_tables, w.pos_steps[0].contiguous(), 16)
+            if q8:
+                app = pkv.pkv_append_fp8 if kind == "fp8" else pkv.pkv_append_int8
+                app(w.k_steps[0], w.v_steps[0], slots, w.k_cache, w.v_cache, w.k_scale,
+                    w.v_scale)
+            else:
+                pkv.pkv_append(w.k_steps[0], w.v_steps[0], slots, w.k_cache, w.v_cache)
+        opts = pkv.DecodeOptions(spec.window, spec.num_sinks, 512,
+                                 w.k_steps[0].data_ptr() if fused else None,
+                                 w.v_steps[0].data_ptr() if fused else None,
+                                 w.k_scale.data_ptr() if q8 else None,
+                                 w.v_scale.data_ptr() if q8 else None)
+        out = torch.full_like(w.q_steps[0], float("nan"))
+        layout = pkv.cache_layout(w.k_cache)
+        call = fn if noalloc else pkv.load_library().pkv_decode_ex
+        rc = call(w.q_steps[0].data_ptr(), spec.num_seqs, spec.num_q_heads,
+                  w.k_cache.data_ptr(), w.v_cache.data_ptr(), ctypes.byref(layout),
+                  w.block_tables.data_ptr(), w.block_tables.shape[1], lens.data_ptr(),
+                  ctypes.c_float(w.scale), out.data_ptr(), ctypes.byref(opts),
+                  torch.cuda.current_stream().cuda_stream)
+        assert rc == 0, pkv.status_string(rc)
+        torch.cuda.synchronize()
+        assert torch.isfinite(out.float()).all()
+        outs.append(out.cpu())
+        pools.append((w.k_cache.cpu(), w.v_cache.cpu()))
+    assert torch.equal(outs[0].view(torch.int16), outs[1].view(torch.int16))
+    for a, b in zip(pools[0], pools[1]):
+        assert torch.equal(a.view(torch.uint8), b.view(torch.uint8))
