@@ -11,10 +11,12 @@
 //  * Work item = (sequence, kv head, head chunk, context split).  One CTA of
 //    four warps per item; the split covers a fixed number of 16-token units
 //    so every CTA streams the same number of bytes (flash-decoding split-K).
-//  * Each warp owns a ring of shared-memory stages.  Lane 0 reads the block
-//    table and issues TMA tile loads (cp.async.bulk.tensor, 128-byte swizzle)
-//    of the unit's K and V rows straight from the page; completion arrives on
-//    the stage's mbarrier.  Nothing is gathered through registers.
+//  * Each warp owns a ring of shared-memory stages.  The warp resolves its
+//    units' pages through the block table 32 at a time (one lane per unit),
+//    and lane 0 issues one TMA tile load (cp.async.bulk.tensor, 128-byte
+//    swizzle) for the unit's K rows and one for its V rows straight from the
+//    page; completion arrives on the stage's mbarrier.  Nothing is gathered
+//    through registers.
 //  * 16-bit pools: S^T = K Q^T and O^T += V^T P^T on the tensor cores
 //    (mma.m16n8k16, fp32 accumulate): 16 context tokens form the M side, the
 //    G query heads of the group (padded to 8) the N side, so one page read
@@ -73,8 +75,8 @@ constexpr float kRescaleThreshold = 8.0f;     // log2 units: weights stay <= 2^8
 //    x D, 128-byte swizzled boxes), read by ldmatrix in place.
 //  FP8 pools (KV8): a stage holds the unit's K and V code tiles (16 rows x D
 //    bytes, one swizzled box each); the 2 x 16 row scales sit in a separate
-//    per-warp array.  ldmatrix reads the codes in place and the warp turns
-//    them into fp16 fragments in registers.
+//    per-warp array, filled by per-lane cp.async.  ldmatrix reads the codes
+//    in place and the warp turns them into fp16 fragments in registers.
 // kShallow: two ring stages per warp (16-bit pools, D = 128), so that three
 // CTAs fit on an SM instead of two.
 template <int D, bool KV8, bool kShallow = false>

@@ -245,8 +245,8 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
         return (pb * p.num_kv_heads + hkv) * p.block_size + (t0 % p.block_size);
       };
       // Lane 0 posts the tile's byte count, then lane i copies unit i (its
-      // K or V rows, one box per 64 columns): a copy takes tens of cycles to
-      // issue, so the eight units go out side by side.
+      // K rows one box per 64 columns, its V rows in one box): a copy takes
+      // tens of cycles to issue, so the eight units go out side by side.
       auto issue = [&](const CUtensorMap* map, uint32_t bar, uint32_t dst, int y, int loaded,
                        bool v_tile) {
         if (lane == 0) {
