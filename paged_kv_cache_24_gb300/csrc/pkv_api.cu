@@ -200,12 +200,15 @@ int make_plan(int num_seqs, int num_q_heads, const pkv_cache_layout* L, int max_
     const int64_t target = static_cast<int64_t>(num_sms) * 4;
     ups = max_ups;
     while (ups > 8 && pairs * ((max_units + ups - 1) / ups) < target) ups /= 2;
-    // With 32 or more work items per SM the items alone balance the SMs:
-    // when none can exceed 4096 tokens, one split each needs no combine
-    // pass (a serving batch of 8192 items of up to 2080 tokens: 5 % less
-    // time than 2048-token splits).
-    if (pairs >= 32 * static_cast<int64_t>(num_sms) && max_units > ups &&
-        max_units <= 2 * max_ups)
+    // One split per item, with no combine pass, when no item can exceed 257
+    // units (4096 tokens at any alignment) and the items either balance the
+    // SMs on their own (32 or more per SM: a serving batch of 8192 items of
+    // up to 2080 tokens, 5 % less time than 2048-token splits) or are too
+    // few to fill them anyway (at most one per SM: 128 windows of 4096
+    // tokens, 4 % less time than 64-unit splits).
+    const int64_t sms = num_sms;
+    if (max_units > ups && max_units <= 2 * max_ups + 1 &&
+        (pairs >= 32 * sms || pairs <= sms))
       ups = static_cast<int>(max_units);
   }
   int64_t ns = (max_units + ups - 1) / ups;

@@ -99,13 +99,16 @@ def test_slot_mapping_argument_checks(pkv_lib):
     # (num_seqs, hq, layout args, max_blocks, window) -> (tokens_per_split, num_splits)
     ((64, 32, (10000, 32, 16, 128, 1), 256, 0), (2048, 2)),
     ((256, 32, (44000, 8, 32, 128, 2), 256, 0), (2048, 4)),
-    ((16, 32, (30000, 8, 16, 128, 2), 2048, 4096), (1024, 5)),
+    # 128 items (under one per SM), windows of 4096 tokens: one split each
+    ((16, 32, (30000, 8, 16, 128, 2), 2048, 4096), (4112, 1)),
+    ((16, 32, (30000, 8, 16, 128, 2), 2048, 4097), (1024, 5)),
     ((4, 8, (32, 8, 16, 64, 0), 7, 0), (128, 1)),
     ((1, 8, (4096, 8, 16, 128, 1), 2048, 0), (256, 128)),
-    # 32+ items per SM and at most 4096 tokens each: one split per item
+    # 32+ items per SM and at most 257 units each: one split per item
     ((1024, 32, (50000, 8, 16, 128, 1), 130, 0), (2080, 1)),
     ((1024, 32, (50000, 8, 16, 128, 1), 256, 0), (4096, 1)),
-    ((1024, 32, (50000, 8, 16, 128, 1), 257, 0), (2048, 3)),
+    ((1024, 32, (50000, 8, 16, 128, 1), 257, 0), (4112, 1)),
+    ((1024, 32, (50000, 8, 16, 128, 1), 258, 0), (2048, 3)),
     ((600, 32, (50000, 8, 16, 128, 1), 130, 0), (2048, 2)),
 ])
 def test_plan(pkv_lib, cfg, expect):
