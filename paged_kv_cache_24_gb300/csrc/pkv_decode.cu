@@ -78,8 +78,8 @@ constexpr float kRescaleThreshold = 8.0f;     // log2 units: weights stay <= 2^8
 //    per-warp array, filled by per-lane cp.async.  ldmatrix reads the codes
 //    in place and the warp turns them into fp16 fragments in registers.
 // kShallow: two ring stages per warp (16-bit pools, D = 128), so that three
-// CTAs fit on an SM instead of two.
-template <int D, bool KV8, bool kShallow = false>
+// CTAs fit on an SM instead of two.  W: warps per CTA (each with its ring).
+template <int D, bool KV8, bool kShallow = false, int W = kDecodeWarps>
 struct Tile16 {
   static constexpr int kBoxes = D / 64;                     // 64 16-bit columns per box
   static constexpr int kTileBytes = kBoxes * kBoxBytes;     // fp16 K (or V) rows of one unit
@@ -91,7 +91,7 @@ struct Tile16 {
   static constexpr int kWarpBytes = kRingBytes;             // multiple of 1 KB
   static constexpr int kScaleBytes = KV8 ? kStages * 2 * kUnitTokens * 4 : 0;  // per warp
   static constexpr int kTxBytes = KV8 ? 2 * kCodeTileBytes : kStageBytes;  // TMA bytes per stage
-  static constexpr int kSmemBytes = kDecodeWarps * (kWarpBytes + kScaleBytes) + 1024;
+  static constexpr int kSmemBytes = W * (kWarpBytes + kScaleBytes) + 1024;
   static_assert(kWarpBytes % 1024 == 0, "swizzled tiles need 1 KB alignment");
 };
 
@@ -157,7 +157,7 @@ __device__ void write_trivial_rows(const DecodeParams& p, const WorkItem& w) {
 // Merge the per-warp softmax states held in shared memory and store either
 // the final rows (single split) or this split's unnormalised partial.
 //   so[w][q][DP] partial O, sm[w][q] running max (log2 units), sl[w][q] sum.
-template <typename T, int D, int QT, int DP>
+template <typename T, int D, int QT, int DP, int W = kDecodeWarps>
 __device__ void merge_and_store(const float* so, const float* sm, const float* sl,
                                 const DecodeParams& p, const WorkItem& w, bool bad) {
   const float nanf_ = __int_as_float(0x7fc00000);
@@ -165,10 +165,10 @@ __device__ void merge_and_store(const float* so, const float* sm, const float* s
     const int qi = i / D, d = i - qi * D;
     float M = -INFINITY;
 #pragma unroll
-    for (int k = 0; k < kDecodeWarps; ++k) M = fmaxf(M, sm[k * QT + qi]);
+    for (int k = 0; k < W; ++k) M = fmaxf(M, sm[k * QT + qi]);
     float acc = 0.f, lsum = 0.f;
 #pragma unroll
-    for (int k = 0; k < kDecodeWarps; ++k) {
+    for (int k = 0; k < W; ++k) {
       const float mk = sm[k * QT + qi];
       const float f = (mk == -INFINITY) ? 0.f : ex2(mk - M);
       acc = fmaf(f, so[(k * QT + qi) * DP + d], acc);
@@ -188,22 +188,24 @@ __device__ void merge_and_store(const float* so, const float* sm, const float* s
 // ---------------------------------------------------------------------------
 // 16-bit pools: TMA-staged pages, tensor-core QK^T and PV.
 
-template <typename T, int D, int NT, bool KV8, bool I8 = false, bool kShallow = false>
-__global__ void __launch_bounds__(kThreads, (KV8 && NT == 1) ? 4 : (kShallow ? 3 : 2))
+template <typename T, int D, int NT, bool KV8, bool I8 = false, bool kShallow = false,
+          int W = kDecodeWarps>
+__global__ void __launch_bounds__(W * 32, W > kDecodeWarps ? 1
+                                             : ((KV8 && NT == 1) ? 4 : (kShallow ? 3 : 2)))
 decode16_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
                 const DecodeParams p) {
-  using Cfg = Tile16<D, KV8, kShallow>;
+  using Cfg = Tile16<D, KV8, kShallow, W>;
   constexpr int QT = 8 * NT;        // query columns per CTA (padded group)
   constexpr int KS = D / 16;        // k-steps of QK^T == m-tiles of PV
   constexpr int DP = D + 4;         // padded row stride of the merge buffer
   constexpr int S = Cfg::kStages;
   static_assert(S <= 16, "the next chunk's pages are resolved 16 units ahead");
-  static_assert(kDecodeWarps * QT * (DP + 2) * 4 <= kDecodeWarps * Cfg::kWarpBytes,
+  static_assert(W * QT * (DP + 2) * 4 <= W * Cfg::kWarpBytes,
                 "merge buffer must fit in the staging rings");
   static_assert(!KV8 || D == 128, "FP8 pools: head_dim 128");
 
   extern __shared__ uint8_t smem_raw[];
-  __shared__ __align__(8) uint64_t bars[kDecodeWarps][S];
+  __shared__ __align__(8) uint64_t bars[W][S];
   __shared__ int s_bad;
 
   const int lane = threadIdx.x & 31;
@@ -221,7 +223,7 @@ decode16_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant_
   const uint32_t base_addr = (raw_addr + 1023u) & ~1023u;  // 128B-swizzle tiles need 1 KB alignment
   uint8_t* base = smem_raw + (base_addr - raw_addr);
   const uint32_t ring = base_addr + warp * Cfg::kWarpBytes;
-  const uint32_t scales = base_addr + kDecodeWarps * Cfg::kWarpBytes + warp * Cfg::kScaleBytes;
+  const uint32_t scales = base_addr + W * Cfg::kWarpBytes + warp * Cfg::kScaleBytes;
 
   if (threadIdx.x == 0) s_bad = 0;
   if (lane == 0) {
@@ -235,15 +237,15 @@ decode16_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant_
   }
   __syncthreads();
 
-  // Units of this warp: u = u0 + warp + j * kDecodeWarps.  Their pages are
+  // Units of this warp: u = u0 + warp + j * W.  Their pages are
   // resolved through the block table 32 at a time, lane l holding unit
   // 32 c + l of chunk c: y_cur holds the chunk of unit j, y_next the one
   // after it.  The next chunk's entries are read when a chunk starts and
   // examined only halfway through it, so the read never stalls the warp.
   const int span = w.u1 - w.u0;
-  const int my_n = span > warp ? (span - warp + kDecodeWarps - 1) / kDecodeWarps : 0;
+  const int my_n = span > warp ? (span - warp + W - 1) / W : 0;
   auto unit_t0 = [&](int jj) -> int {  // first token of unit jj, -1 past the warp's units
-    return jj < my_n ? phys_unit(w.su, w.u0 + warp + jj * kDecodeWarps) * kUnitTokens : -1;
+    return jj < my_n ? phys_unit(w.su, w.u0 + warp + jj * W) * kUnitTokens : -1;
   };
   auto table_entry = [&](int t0) -> int32_t {
     return t0 < 0 ? -1
@@ -362,8 +364,8 @@ decode16_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant_
   const int v_new = w.su.n_sink_u + t_new / kUnitTokens - w.su.win_u0;
   const int rel_new = v_new - w.u0 - warp;
   const bool own_new = p.k_new != nullptr && t_new >= 0 && rel_new >= 0 && v_new < w.u1 &&
-                       rel_new % kDecodeWarps == 0;
-  const int j_new = own_new ? rel_new / kDecodeWarps : -1;
+                       rel_new % W == 0;
+  const int j_new = own_new ? rel_new / W : -1;
   uint4 new_row = make_uint4(0u, 0u, 0u, 0u);
   if (own_new && lane < 2 * CPR) {
     const T* src = static_cast<const T*>(lane < CPR ? p.k_new : p.v_new) +
@@ -392,7 +394,7 @@ decode16_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant_
 
     const uint32_t kt = ring + stage * Cfg::kStageBytes;
     const uint32_t vt = kt + Cfg::kStageBytes / 2;
-    const int t0 = phys_unit(w.su, w.u0 + warp + j * kDecodeWarps) * kUnitTokens;
+    const int t0 = phys_unit(w.su, w.u0 + warp + j * W) * kUnitTokens;
     // per-row scales of the unit (FP8 pools; 1 otherwise): K rows g, g+8; V rows g, g+8
     float ksa = 1.f, ksb = 1.f, vsa = 1.f, vsb = 1.f;
     if constexpr (KV8) {
@@ -665,8 +667,8 @@ decode16_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant_
   __syncthreads();  // every warp is done with its ring; reuse it for the merge
 
   float* so = reinterpret_cast<float*>(base);
-  float* sm = so + kDecodeWarps * QT * DP;
-  float* sl = sm + kDecodeWarps * QT;
+  float* sm = so + W * QT * DP;
+  float* sl = sm + W * QT;
 #pragma unroll
   for (int mt = 0; mt < KS; ++mt)
 #pragma unroll
@@ -687,7 +689,7 @@ decode16_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant_
       }
   }
   __syncthreads();
-  merge_and_store<T, D, QT, DP>(so, sm, sl, p, w, s_bad != 0);
+  merge_and_store<T, D, QT, DP, W>(so, sm, sl, p, w, s_bad != 0);
 }
 
 // ---------------------------------------------------------------------------
@@ -872,11 +874,12 @@ combine_kernel(const DecodeParams p) {
   for (int i = 0; i < PER; ++i) out[i] = from_f32<T>(acc[i] / lsum);
 }
 
-template <typename T, int D, int NT, bool KV8 = false, bool I8 = false, bool kShallow = false>
+template <typename T, int D, int NT, bool KV8 = false, bool I8 = false, bool kShallow = false,
+          int W = kDecodeWarps>
 cudaError_t launch16(const CUtensorMap& kmap, const CUtensorMap& vmap, const DecodeParams& p,
                      cudaStream_t stream) {
-  auto kern = decode16_kernel<T, D, NT, KV8, I8, kShallow>;
-  const int smem = Tile16<D, KV8, kShallow>::kSmemBytes;
+  auto kern = decode16_kernel<T, D, NT, KV8, I8, kShallow, W>;
+  const int smem = Tile16<D, KV8, kShallow, W>::kSmemBytes;
   // the shared-memory opt-in is per device; set it once for each
   static std::atomic<uint64_t> configured{0};
   int dev = 0;
@@ -889,7 +892,7 @@ cudaError_t launch16(const CUtensorMap& kmap, const CUtensorMap& vmap, const Dec
     configured.fetch_or(bit, std::memory_order_acq_rel);
   }
   dim3 grid(p.num_splits, p.num_kv_heads * p.num_head_chunks, p.num_seqs);
-  return launch_pdl(kern, grid, dim3(kThreads), smem, stream, kmap, vmap, p);
+  return launch_pdl(kern, grid, dim3(W * 32), smem, stream, kmap, vmap, p);
 }
 
 }  // namespace
@@ -918,11 +921,16 @@ cudaError_t launch_decode_16bit(int dtype, int head_dim, int ntiles, const CUten
     sms = 148;
   const int64_t items = static_cast<int64_t>(p.num_seqs) * p.num_kv_heads * p.num_head_chunks;
   const bool shallow = head_dim == 128 && ntiles == 1 && items >= 16 * static_cast<int64_t>(sms);
+  // A grid of at most one CTA per SM (a window per item, one split each):
+  // eight warps per CTA, so that each SM runs more than four warps' chains.
+  const bool wide = head_dim == 128 && ntiles == 1 &&
+                    items * p.num_splits <= static_cast<int64_t>(sms);
   // dtype: 1 = fp16, 2 = bf16
 #define PKV_LAUNCH16(T, D, NT) return launch16<T, D, NT>(kmap, vmap, p, stream)
   if (dtype == 1) {
     if (head_dim == 128) {
       if (ntiles == 1 && shallow) return launch16<__half, 128, 1, false, false, true>(kmap, vmap, p, stream);
+      if (wide) return launch16<__half, 128, 1, false, false, false, 8>(kmap, vmap, p, stream);
       if (ntiles == 1) PKV_LAUNCH16(__half, 128, 1);
       PKV_LAUNCH16(__half, 128, 2);
     }
@@ -932,6 +940,7 @@ cudaError_t launch_decode_16bit(int dtype, int head_dim, int ntiles, const CUten
   if (head_dim == 128) {
     if (ntiles == 1 && shallow)
       return launch16<__nv_bfloat16, 128, 1, false, false, true>(kmap, vmap, p, stream);
+    if (wide) return launch16<__nv_bfloat16, 128, 1, false, false, false, 8>(kmap, vmap, p, stream);
     if (ntiles == 1) PKV_LAUNCH16(__nv_bfloat16, 128, 1);
     PKV_LAUNCH16(__nv_bfloat16, 128, 2);
   }
