@@ -23,8 +23,9 @@
  *   - Pointers named *_cache, q, k, v, out, block_tables, context_lens,
  *     positions and slot_mapping are DEVICE pointers on the current CUDA
  *     device; the caller owns them.  Data pointers must be 16-byte aligned.
- *     A decode's `out` may also be the device-side address of pinned host
- *     memory (pkv_device_address): the kernels then write the result there.
+ *     A decode's q, k_new, v_new and out may also be device-side addresses
+ *     of pinned host memory (pkv_device_address): the kernels then read or
+ *     write them there, over the host link.
  *   - `stream` is a cudaStream_t (NULL = legacy default stream).  Every call
  *     only enqueues work on it and returns without synchronising, except
  *     where stated.
@@ -84,8 +85,9 @@ typedef struct pkv_cache_layout {
  *   address for pinned host memory.  Pageable or unknown host memory:
  *   PKV_ERR_UNSUPPORTED and *device_address = NULL.  Host-only: launches
  *   nothing and does not synchronise.  Not an operation of the pages: a
- *   decode's `out` may be such an address of pinned host memory, so that the
- *   result is written straight to the host (what DecodeStep does).
+ *   decode's q, k_new, v_new and out may be such addresses of pinned host
+ *   memory, read or written by the kernels over the host link (DecodeStep
+ *   reads a step's queries and new rows that way).
  */
 int pkv_device_address(const void* p, void** device_address);
 

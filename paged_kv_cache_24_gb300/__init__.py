@@ -21,8 +21,8 @@ Public API (thin wrappers over the C ABI of ``libpkv.so``, see include/pkv.h):
 * ``pkv_stage_copy(dst, src)`` -- a kernel copy between device memory and
   pinned host memory (DecodeStep's host transfers);
 * ``pkv_device_address(t)`` -- the address the kernels use for a device or
-  pinned host tensor (a decode may write its ``out`` straight to pinned host
-  memory);
+  pinned host tensor (a decode may read q and the new K/V from, and write
+  ``out`` to, pinned host memory);
 * ``pkv_validate_indices(block_tables, context_lens, num_blocks, block_size,
   slot_mapping=None)`` -- debug check of the indices the kernels trust
   (waits for the stream).

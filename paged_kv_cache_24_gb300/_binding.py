@@ -179,14 +179,14 @@ def pkv_device_address(t: torch.Tensor) -> int | None:
     return addr.value
 
 
-def _out_address(out: torch.Tensor) -> int:
-    """A decode's output: a CUDA tensor, or a pinned host tensor the kernels write
-    directly (the result then needs no copy back)."""
-    if out.device.type == "cuda":
-        return out.data_ptr()
-    _require(out.is_pinned(), "out must be a CUDA tensor or pinned host memory")
-    addr = pkv_device_address(out)
-    _require(addr is not None, "this GPU cannot address the pinned output buffer")
+def _address(t: torch.Tensor, what: str) -> int:
+    """A decode's q, new K/V or output: a CUDA tensor, or a pinned host tensor
+    the kernels read or write directly over the host link."""
+    if t.device.type == "cuda":
+        return t.data_ptr()
+    _require(t.is_pinned(), f"{what} must be a CUDA tensor or pinned host memory")
+    addr = pkv_device_address(t)
+    _require(addr is not None, f"this GPU cannot address the pinned {what} buffer")
     return addr
 
 
@@ -248,9 +248,10 @@ def pkv_decode(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
                v_scale: torch.Tensor | None = None) -> torch.Tensor:
     """Decode attention of q [B, Hq, D] over the paged context; returns out [B, Hq, D].
     With a window, ``num_sinks`` first positions are attended as well.  8-bit pools
-    (uint8 E4M3 or int8 codes) take their row scales and fp16 q.  ``out`` may be a
-    pinned host tensor: the kernels then write the result straight into it."""
-    _on_cuda(q, k_cache, v_cache, block_tables, context_lens, k_scale, v_scale)
+    (uint8 E4M3 or int8 codes) take their row scales and fp16 q.  ``q`` and ``out``
+    may be pinned host tensors: the kernels then read or write them straight
+    over the host link."""
+    _on_cuda(k_cache, v_cache, block_tables, context_lens, k_scale, v_scale)
     layout = cache_layout(k_cache)
     _require(v_cache.shape == k_cache.shape and v_cache.dtype == k_cache.dtype
              and v_cache.is_contiguous(), "v_cache must match k_cache")
@@ -265,15 +266,15 @@ def pkv_decode(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
     _require(context_lens.dtype == torch.int32 and context_lens.numel() == B
              and context_lens.is_contiguous(), "context_lens must be int32 [B]")
     if out is None:
-        out = torch.empty_like(q)
+        out = torch.empty_like(q, device=k_cache.device)
     _require(out.shape == q.shape and out.dtype == q.dtype and out.is_contiguous(),
              "out must be contiguous and shaped like q")
     opts = DecodeOptions(int(window), int(num_sinks), int(tokens_per_split), None, None,
                          _ptr(k_scale) or None, _ptr(v_scale) or None)
     _check("pkv_decode", load_library().pkv_decode_ex(
-        _ptr(q), B, Hq, _ptr(k_cache), _ptr(v_cache), ctypes.byref(layout),
+        _address(q, "q"), B, Hq, _ptr(k_cache), _ptr(v_cache), ctypes.byref(layout),
         _ptr(block_tables), block_tables.shape[1], _ptr(context_lens), float(scale),
-        _out_address(out), ctypes.byref(opts), _stream(stream)))
+        _address(out, "out"), ctypes.byref(opts), _stream(stream)))
     return out
 
 
@@ -359,9 +360,9 @@ def pkv_append_decode(q: torch.Tensor, k_new: torch.Tensor, v_new: torch.Tensor,
                       out: torch.Tensor | None = None, tokens_per_split: int = 0,
                       stream=None, num_sinks: int = 0) -> torch.Tensor:
     """Append each sequence's new token (at position context_lens[b] - 1) and
-    decode, in one launch; same result as the separate calls.  ``out`` may be a
-    pinned host tensor, as for ``pkv_decode``."""
-    _on_cuda(q, k_new, v_new, k_cache, v_cache, block_tables, context_lens)
+    decode, in one launch; same result as the separate calls.  ``q``, ``k_new``,
+    ``v_new`` and ``out`` may be pinned host tensors, as for ``pkv_decode``."""
+    _on_cuda(k_cache, v_cache, block_tables, context_lens)
     layout = cache_layout(k_cache)
     _require(v_cache.shape == k_cache.shape and v_cache.dtype == k_cache.dtype
              and v_cache.is_contiguous(), "v_cache must match k_cache")
@@ -379,15 +380,15 @@ def pkv_append_decode(q: torch.Tensor, k_new: torch.Tensor, v_new: torch.Tensor,
     _require(context_lens.dtype == torch.int32 and context_lens.numel() == B
              and context_lens.is_contiguous(), "context_lens must be int32 [B]")
     if out is None:
-        out = torch.empty_like(q)
+        out = torch.empty_like(q, device=k_cache.device)
     _require(out.shape == q.shape and out.dtype == q.dtype and out.is_contiguous(),
              "out must be contiguous and shaped like q")
-    opts = DecodeOptions(int(window), int(num_sinks), int(tokens_per_split), _ptr(k_new),
-                         _ptr(v_new), None, None)
+    opts = DecodeOptions(int(window), int(num_sinks), int(tokens_per_split),
+                         _address(k_new, "k_new"), _address(v_new, "v_new"), None, None)
     _check("pkv_append_decode", load_library().pkv_decode_ex(
-        _ptr(q), B, Hq, _ptr(k_cache), _ptr(v_cache), ctypes.byref(layout), _ptr(block_tables),
-        block_tables.shape[1], _ptr(context_lens), float(scale), _out_address(out),
-        ctypes.byref(opts), _stream(stream)))
+        _address(q, "q"), B, Hq, _ptr(k_cache), _ptr(v_cache), ctypes.byref(layout),
+        _ptr(block_tables), block_tables.shape[1], _ptr(context_lens), float(scale),
+        _address(out, "out"), ctypes.byref(opts), _stream(stream)))
     return out
 
 

@@ -7,11 +7,14 @@ launch; ``fused=False`` runs the three separate calls.
 
 A step's host inputs -- the queries, the new tokens' K and V, their positions,
 the context lengths and (optionally) the block tables -- are packed into one
-pinned staging buffer and reach the device in a single copy, a
+pinned staging buffer.  On the fused path the decode kernels read the
+queries and the new K/V straight from it over the host link, and the rest
+(positions, lengths, block tables) reaches the device first in a single
 ``pkv_stage_copy`` kernel that reads the pinned buffer directly (the copy
-engine where the GPU cannot reach it); the attention output comes back in a
-second one (or, with ``direct_out=True``, the decode kernels write it straight
-into the pinned host buffer).  The graph replays
+engine where the GPU cannot reach it); with ``direct_in=False``, or on the
+separate-call path, everything is copied in that way.  The attention output
+comes back in a second copy (or, with ``direct_out=True``, the decode kernels
+write it straight into the pinned host buffer).  The graph replays
 ``pkv_slot_mapping``, ``pkv_append`` and ``pkv_decode`` exactly as the eager
 calls would run them.  The K/V pools stay resident on the device.
 
@@ -41,7 +44,8 @@ class DecodeStep:
                  num_q_heads: int, max_blocks: int, window: int, scale: float,
                  copy_block_tables: bool = True, num_buffers: int = 1, use_graph: bool = True,
                  fused: bool = True, k_scale: torch.Tensor | None = None,
-                 v_scale: torch.Tensor | None = None, direct_out: bool = False):
+                 v_scale: torch.Tensor | None = None, direct_out: bool = False,
+                 direct_in: bool = True):
         layout = cache_layout(k_cache)
         self.k_cache, self.v_cache = k_cache, v_cache
         self.window, self.scale = int(window), float(scale)
@@ -78,6 +82,14 @@ class DecodeStep:
 
         self._host_bufs = [torch.empty(cur, dtype=torch.uint8).pin_memory()
                            for _ in range(num_buffers)]
+        # direct_in (the fused path): the decode kernels read the queries and
+        # the new K/V straight from the pinned buffer over the host link; only
+        # the positions, lengths and block tables are copied in first.
+        # Measured on the MHA step: 0.3511 ms against 0.3658 with everything
+        # copied in first (the copy of 1.5 MB no longer precedes the decode).
+        self.direct_in = (direct_in and fused and
+                          all(pkv_device_address(b) is not None for b in self._host_bufs))
+        self._stage_start = offsets["positions"][0] if self.direct_in else 0
         self.host = [views(b) for b in self._host_bufs]   # fill these, then run(i)
         self._dev_buf = torch.empty(cur, dtype=torch.uint8, device=dev)
         self.device = views(self._dev_buf)
@@ -120,12 +132,14 @@ class DecodeStep:
                 src.view(-1)[:n // src.element_size()], non_blocking=True)
 
     def _enqueue(self, i):
-        self._copy(self._dev_buf, self._host_bufs[i], self._staged_bytes)
+        a = self._stage_start
+        self._copy(self._dev_buf[a:], self._host_bufs[i][a:], self._staged_bytes - a)
         dv = self.device
+        src = self.host[i] if self.direct_in else dv
         out = self.host_out if self.direct_out else self.out
         if self.fused:
             # the new token sits at position context_lens - 1: one launch
-            pkv_append_decode(dv["q"], dv["k"], dv["v"], self.k_cache, self.v_cache,
+            pkv_append_decode(src["q"], src["k"], src["v"], self.k_cache, self.v_cache,
                               dv["block_tables"], dv["context_lens"], self.window, self.scale,
                               out=out)
         else:

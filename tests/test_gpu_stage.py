@@ -42,8 +42,9 @@ def test_device_address(pkv_lib):
 
 @pytest.mark.parametrize("fused", [False, True])
 def test_decode_into_pinned_host_output(pkv_lib, fused):
-    """The decode kernels write a pinned host `out` directly: the same bits as a
-    device `out`, for single-split and split sequences alike."""
+    """The decode kernels write a pinned host `out` directly (and, fused, read the
+    queries and new rows from pinned memory): the same bits as device tensors,
+    for single-split and split sequences alike."""
     from paged_kv_cache_24_gb300.workloads import config_spec, make_workload
     spec = config_spec(0, dtype=torch.bfloat16, num_seqs=6, num_q_heads=8, num_kv_heads=2,
                        head_dim=128, block_size=16, lens=[1, 30, 500, 2100, 4000, 0],
@@ -55,9 +56,12 @@ def test_decode_into_pinned_host_output(pkv_lib, fused):
         out = (torch.full_like(w.q_steps[0], float("nan"), device="cpu").pin_memory() if host
                else torch.full_like(w.q_steps[0], float("nan")))
         if fused:
-            pkv_lib.pkv_append_decode(w.q_steps[0], w.k_steps[0], w.v_steps[0], w.k_cache,
-                                      w.v_cache, w.block_tables, lens, 0, w.scale, out=out,
-                                      tokens_per_split=512)
+            # with host output, the queries and new rows come from pinned memory too
+            q, kn, vn = ((t.cpu().pin_memory() for t in (w.q_steps[0], w.k_steps[0],
+                                                          w.v_steps[0]))
+                         if host else (w.q_steps[0], w.k_steps[0], w.v_steps[0]))
+            pkv_lib.pkv_append_decode(q, kn, vn, w.k_cache, w.v_cache, w.block_tables, lens, 0,
+                                      w.scale, out=out, tokens_per_split=512)
         else:
             slots = pkv_lib.pkv_slot_mapping(w.block_tables, w.pos_steps[0].contiguous(),
                                              spec.block_size)

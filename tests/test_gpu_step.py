@@ -10,9 +10,11 @@ from paged_kv_cache_24_gb300.workloads import config_spec, make_workload
 pytestmark = pytest.mark.gpu
 
 
+@pytest.mark.parametrize("direct_in", [True, False])
 @pytest.mark.parametrize("direct_out", [False, True])
 @pytest.mark.parametrize("fused", [True, False])
-def test_decode_step_graph_matches_eager_and_oracle(pkv_lib, oracle_lib, fused, direct_out):
+def test_decode_step_graph_matches_eager_and_oracle(pkv_lib, oracle_lib, fused, direct_out,
+                                                    direct_in):
     pkv = pkv_lib
     spec = config_spec(4, num_seqs=24, num_q_heads=16, num_kv_heads=4, steps=3, seed=9)
     w = make_workload(spec, device="cuda")
@@ -21,8 +23,9 @@ def test_decode_step_graph_matches_eager_and_oracle(pkv_lib, oracle_lib, fused, 
     bt_h = w.block_tables.cpu().numpy()
     step = pkv.DecodeStep(w.k_cache, w.v_cache, spec.num_seqs, spec.num_q_heads, w.max_blocks,
                           spec.window, w.scale, num_buffers=spec.steps, fused=fused,
-                          direct_out=direct_out)
+                          direct_out=direct_out, direct_in=direct_in)
     assert step.direct_out == direct_out
+    assert step.direct_in == (direct_in and fused)
     for s in range(spec.steps):
         h = step.host[s]
         h["q"].copy_(w.q_steps[s]); h["k"].copy_(w.k_steps[s]); h["v"].copy_(w.v_steps[s])
