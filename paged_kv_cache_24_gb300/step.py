@@ -12,9 +12,9 @@ queries and the new K/V straight from it over the host link, and the rest
 (positions, lengths, block tables) reaches the device first in a single
 ``pkv_stage_copy`` kernel that reads the pinned buffer directly (the copy
 engine where the GPU cannot reach it); with ``direct_in=False``, or on the
-separate-call path, everything is copied in that way.  The attention output
-comes back in a second copy (or, with ``direct_out=True``, the decode kernels
-write it straight into the pinned host buffer).  The graph replays
+separate-call path, everything is copied in that way.  The decode kernels
+write the attention output straight into a pinned host buffer (with
+``direct_out=False`` it comes back in a second copy).  The graph replays
 ``pkv_slot_mapping``, ``pkv_append`` and ``pkv_decode`` exactly as the eager
 calls would run them.  The K/V pools stay resident on the device.
 
@@ -44,7 +44,7 @@ class DecodeStep:
                  num_q_heads: int, max_blocks: int, window: int, scale: float,
                  copy_block_tables: bool = True, num_buffers: int = 1, use_graph: bool = True,
                  fused: bool = True, k_scale: torch.Tensor | None = None,
-                 v_scale: torch.Tensor | None = None, direct_out: bool = False,
+                 v_scale: torch.Tensor | None = None, direct_out: bool = True,
                  direct_in: bool = True):
         layout = cache_layout(k_cache)
         self.k_cache, self.v_cache = k_cache, v_cache
@@ -98,9 +98,8 @@ class DecodeStep:
         self.host_out = torch.empty((B, hq, d), dtype=dt).pin_memory()
         # direct_out: the decode writes the result straight into the pinned
         # buffer where the GPU can address it, instead of a copy back after it.
-        # Measured on the MHA step: 0.3632 ms vs 0.3622 with the copy (the
-        # copy back is not on the step's critical path; the kernels' stores
-        # over the host link slow their tails slightly), so it is off by default.
+        # Measured end to end: the serving mix (8 MB of output a step) 0.3030
+        # -> 0.2566 ms, the MHA step (512 KB) 0.3567 -> 0.3574 ms.
         self.direct_out = direct_out and pkv_device_address(self.host_out) is not None
         self.h2d_bytes = self._staged_bytes
         self.d2h_bytes = self.host_out.numel() * self.host_out.element_size()
