@@ -224,8 +224,9 @@ def pkv_slot_mapping(block_tables: torch.Tensor, positions: torch.Tensor, block_
 
 def pkv_append(k: torch.Tensor, v: torch.Tensor, slot_mapping: torch.Tensor,
                k_cache: torch.Tensor, v_cache: torch.Tensor, stream=None) -> None:
-    """Write k[i], v[i] ([T, Hkv, D]) into cache slot slot_mapping[i] (int64, <0 skips)."""
-    _on_cuda(k, v, slot_mapping, k_cache, v_cache)
+    """Write k[i], v[i] ([T, Hkv, D]) into cache slot slot_mapping[i] (int64, <0 skips).
+    k and v may be pinned host tensors (read by the kernel over the host link)."""
+    _on_cuda(slot_mapping, k_cache, v_cache)
     layout = cache_layout(k_cache)
     _require(v_cache.shape == k_cache.shape and v_cache.dtype == k_cache.dtype
              and v_cache.is_contiguous(), "v_cache must match k_cache")
@@ -237,7 +238,7 @@ def pkv_append(k: torch.Tensor, v: torch.Tensor, slot_mapping: torch.Tensor,
     _require(slot_mapping.dtype == torch.int64 and slot_mapping.numel() == T
              and slot_mapping.is_contiguous(), "slot_mapping must be int64 [T]")
     _check("pkv_append", load_library().pkv_append(
-        _ptr(k), _ptr(v), _ptr(slot_mapping), T, _ptr(k_cache), _ptr(v_cache),
+        _address(k, "k"), _address(v, "v"), _ptr(slot_mapping), T, _ptr(k_cache), _ptr(v_cache),
         ctypes.byref(layout), _stream(stream)))
 
 
@@ -280,7 +281,7 @@ def pkv_decode(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
 
 def _append_q8(fn: str, code_dtype, k, v, slot_mapping, k_cache, v_cache, k_scale, v_scale,
                stream) -> None:
-    _on_cuda(k, v, slot_mapping, k_cache, v_cache, k_scale, v_scale)
+    _on_cuda(slot_mapping, k_cache, v_cache, k_scale, v_scale)
     layout = cache_layout(k_cache)
     _require(k_cache.dtype == code_dtype, f"{fn} writes {code_dtype} pools")
     _require(v_cache.shape == k_cache.shape and v_cache.dtype == code_dtype
@@ -294,8 +295,9 @@ def _append_q8(fn: str, code_dtype, k, v, slot_mapping, k_cache, v_cache, k_scal
     _require(slot_mapping.dtype == torch.int64 and slot_mapping.numel() == T
              and slot_mapping.is_contiguous(), "slot_mapping must be int64 [T]")
     _check(fn, getattr(load_library(), fn)(
-        _ptr(k), _ptr(v), _DTYPES[k.dtype], _ptr(slot_mapping), T, _ptr(k_cache), _ptr(v_cache),
-        _ptr(k_scale), _ptr(v_scale), ctypes.byref(layout), _stream(stream)))
+        _address(k, "k"), _address(v, "v"), _DTYPES[k.dtype], _ptr(slot_mapping), T,
+        _ptr(k_cache), _ptr(v_cache), _ptr(k_scale), _ptr(v_scale), ctypes.byref(layout),
+        _stream(stream)))
 
 
 def pkv_append_fp8(k: torch.Tensor, v: torch.Tensor, slot_mapping: torch.Tensor,

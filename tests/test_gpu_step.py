@@ -25,7 +25,7 @@ def test_decode_step_graph_matches_eager_and_oracle(pkv_lib, oracle_lib, fused, 
                           spec.window, w.scale, num_buffers=spec.steps, fused=fused,
                           direct_out=direct_out, direct_in=direct_in)
     assert step.direct_out == direct_out
-    assert step.direct_in == (direct_in and fused)
+    assert step.direct_in == direct_in
     for s in range(spec.steps):
         h = step.host[s]
         h["q"].copy_(w.q_steps[s]); h["k"].copy_(w.k_steps[s]); h["v"].copy_(w.v_steps[s])
