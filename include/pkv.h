@@ -240,13 +240,14 @@ typedef struct pkv_decode_options {
  *   is ignored without a window and must not be negative.
  *   out [T][num_q_heads][head_dim].
  *   Limits: head_dim 64 or 128; num_seqs <= 65534.  The P.V product runs in
- *   fp16: with a bf16 cache, V values beyond the fp16 range (|v| > 65504) are
- *   an error.  Uses the stream's workspace (as pkv_decode's split-K) for the
- *   order of its work items, 4 bytes per (sequence, token chunk); may return
+ *   fp16: with a bf16 cache, a V value beyond the fp16 range (|v| > 65504)
+ *   makes the rows of the work items that read it non-finite (inf or NaN).
+ *   Uses the stream's workspace (as pkv_decode's split-K) for the order of
+ *   its work items, 4 bytes per (sequence, token chunk); may return
  *   PKV_ERR_NOMEM when that has to grow.
- *   In-kernel errors (bad block id, L_b < n_b, V out of range) make the rows
- *   of the affected work item NaN: up to 256 (token, query head) rows of one
- *   sequence and kv head.
+ *   In-kernel errors (bad block id, L_b < n_b) make the rows of the affected
+ *   work item NaN: up to 256 (token, query head) rows of one sequence and kv
+ *   head.
  */
 int pkv_prefill(const void* q, const void* k, const void* v, const int32_t* cu_q,
                 int32_t num_seqs, int32_t num_q_heads, int32_t max_chunk, void* k_cache,

@@ -97,13 +97,12 @@ __device__ __forceinline__ uint32_t sw128(int row, int chunk) {
   return static_cast<uint32_t>(row * 128 + (((chunk & 7) ^ (row & 7)) << 4));
 }
 
-// two bf16 (low half first) -> two fp16; `amax` keeps the largest magnitudes
-// (an infinity there means a value beyond the fp16 range)
-__device__ __forceinline__ uint32_t bf16x2_to_f16x2(uint32_t w, __half2& amax) {
+// two bf16 (low half first) -> two fp16, rounded to nearest; a value beyond
+// the fp16 range becomes an infinity, which the P.V product then carries
+// into every output row of the CTA (as inf or NaN): no separate range test
+__device__ __forceinline__ uint32_t bf16x2_to_f16x2(uint32_t w) {
   const float lo = __uint_as_float(w << 16), hi = __uint_as_float(w & 0xffff0000u);
-  const uint32_t h = Mma<__half>::pack(lo, hi);
-  amax = __hmax2(amax, __habs2(*reinterpret_cast<const __half2*>(&h)));
-  return h;
+  return Mma<__half>::pack(lo, hi);
 }
 
 // kSinks: the key range has a sink section (window > 0, num_sinks > 0); the
@@ -306,7 +305,6 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
     } else if (warp >= kPrepWarp0) {
       // ============ V prep: fp16 in place (bf16 caches), unseen keys zeroed ============
       const int ct = tid - kPrepWarp0 * 32;
-      __half2 amax = __float2half2_rn(0.f);
       for (int j = 0; j < n_tiles; ++j) {
         if (!mbar_wait_bounded(smem_u32(&v_full[j % SV]), (j / SV) & 1, kWaitLimit)) bad = true;
         const int t0 = tile_t0(j);
@@ -322,10 +320,10 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
             if (!whole && (kSinks ? !key_kept(j, kp) : (kp < k_lo || kp > pos1))) {
               x = make_uint4(0u, 0u, 0u, 0u);
             } else {
-              x.x = bf16x2_to_f16x2(x.x, amax);
-              x.y = bf16x2_to_f16x2(x.y, amax);
-              x.z = bf16x2_to_f16x2(x.z, amax);
-              x.w = bf16x2_to_f16x2(x.w, amax);
+              x.x = bf16x2_to_f16x2(x.x);
+              x.y = bf16x2_to_f16x2(x.y);
+              x.z = bf16x2_to_f16x2(x.z);
+              x.w = bf16x2_to_f16x2(x.w);
             }
             st_shared_v4(vt + u * 16, x);
           }
@@ -345,8 +343,6 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
         fence_proxy_async_smem();
         mbar_arrive(smem_u32(&v_ready[j % SV]));
       }
-      // a bf16 value beyond the fp16 range cannot take part in the fp16 product
-      if (__hisinf(__low2half(amax)) || __hisinf(__high2half(amax))) bad = true;
     } else {
       // ============ MMA warp: one thread waits and issues ============
       // (the role uses no warp-collective instruction; the other lanes wait

@@ -217,3 +217,25 @@ def test_prefill_nonpositive_scale(pkv_lib, oracle_lib, scale):
     g = out.double().cpu().numpy()
     err = np.abs(g - ref)
     assert (err <= 2e-3 + 0.5 * torch.finfo(torch.bfloat16).eps * np.abs(ref)).all(), err.max()
+
+
+def test_prefill_bf16_value_beyond_fp16_range(pkv_lib):
+    """The P.V product runs in fp16: a bf16 V value beyond the fp16 range makes
+    the rows of the work items that read it non-finite (never silently wrong),
+    and leaves every other row as it was."""
+    dtype = torch.bfloat16
+    w, q, k, v, cu, lens = _prefill_case(dtype, 4, 2, 128, 16, [30, 30], [10, 10], 0, seed=5)
+    ref = pkv_lib.pkv_prefill(q, k, v, cu, w.k_cache.clone(), w.v_cache.clone(),
+                              w.block_tables, lens, 0, w.scale, max_chunk=10)
+    bt = w.block_tables.cpu().numpy()
+    s = oracle.slot_for_position(bt[0], 16, 5)       # a prefix key of sequence 0
+    w.v_cache[s // 16, 0, s % 16, 3] = 1.0e6            # kv head 0; fp16 tops out at 65504
+    out = pkv_lib.pkv_prefill(q, k, v, cu, w.k_cache, w.v_cache, w.block_tables, lens, 0,
+                              w.scale, max_chunk=10)
+    torch.cuda.synchronize()
+    o, r = out.float().cpu(), ref.float().cpu()
+    # sequence 0's tokens 0..9, query heads 0 and 1 (kv head 0): non-finite
+    assert not torch.isfinite(o[:10, :2]).all()
+    # the other kv head of sequence 0 and all of sequence 1: unchanged
+    assert torch.equal(o[:10, 2:], r[:10, 2:])
+    assert torch.equal(o[10:], r[10:])
