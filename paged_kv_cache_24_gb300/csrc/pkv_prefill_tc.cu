@@ -311,13 +311,23 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
         const uint32_t vt = v_addr(j);
         // a window tile wholly inside [k_lo, pos1] keeps every key
         const bool whole = j >= sink_tiles && t0 >= k_lo && t0 + kTKeys - 1 <= pos1;
-        if (kBf16) {
+        if (kBf16 && whole) {
 #pragma unroll 4
           for (int u = ct; u < Lay::kKVTile / 16; u += kPrepThreads) {  // 16-byte chunks
+            uint4 x = ld_shared_v4(vt + u * 16);
+            x.x = bf16x2_to_f16x2(x.x);
+            x.y = bf16x2_to_f16x2(x.y);
+            x.z = bf16x2_to_f16x2(x.z);
+            x.w = bf16x2_to_f16x2(x.w);
+            st_shared_v4(vt + u * 16, x);
+          }
+        } else if (kBf16) {
+#pragma unroll 4
+          for (int u = ct; u < Lay::kKVTile / 16; u += kPrepThreads) {
             // chunk u: unit u / (kVUnitBytes / 16), row (u / 8) % 16 of it
             const int kp = t0 + (u / (Lay::kVUnitBytes / 16)) * kUnitTokens + ((u >> 3) & 15);
             uint4 x = ld_shared_v4(vt + u * 16);
-            if (!whole && (kSinks ? !key_kept(j, kp) : (kp < k_lo || kp > pos1))) {
+            if (kSinks ? !key_kept(j, kp) : (kp < k_lo || kp > pos1)) {
               x = make_uint4(0u, 0u, 0u, 0u);
             } else {
               x.x = bf16x2_to_f16x2(x.x);
