@@ -192,24 +192,40 @@ int make_plan(int num_seqs, int num_q_heads, const pkv_cache_layout* L, int max_
     ups = tokens_per_split / pkv::kUnitTokens;
     if (ups > cap_ups) return PKV_ERR_UNSUPPORTED;
   } else {
-    // Long splits cost the least per byte (each CTA pays its pipeline fill
-    // and merge once): start at 2048 tokens and halve (down to 128) only
-    // while the grid would give the SMs fewer than 4 CTAs each.
     if (num_sms <= 0) num_sms = 148;
-    const int64_t pairs = static_cast<int64_t>(num_seqs) * L->num_kv_heads * plan->num_head_chunks;
-    const int64_t target = static_cast<int64_t>(num_sms) * 4;
-    ups = max_ups;
-    while (ups > 8 && pairs * ((max_units + ups - 1) / ups) < target) ups /= 2;
-    // One split per item, with no combine pass, when no item can exceed 257
-    // units (4096 tokens at any alignment) and the items either balance the
-    // SMs on their own (32 or more per SM: a serving batch of 8192 items of
-    // up to 2080 tokens, 5 % less time than 2048-token splits) or are too
-    // few to fill them anyway (at most one per SM: 128 windows of 4096
-    // tokens, 4 % less time than 64-unit splits).
     const int64_t sms = num_sms;
-    if (max_units > ups && max_units <= 2 * max_ups + 1 &&
-        (pairs >= 32 * sms || pairs <= sms))
-      ups = static_cast<int>(max_units);
+    const int64_t pairs = static_cast<int64_t>(num_seqs) * L->num_kv_heads * plan->num_head_chunks;
+    // 16-bit pools at head_dim 128 with at most 8 query heads per CTA have a
+    // twelve-warp kernel for grids of at most one CTA per SM
+    const bool wide_kernel = L->head_dim == 128 && plan->ntiles == 1 &&
+                             (L->dtype == PKV_FLOAT16 || L->dtype == PKV_BFLOAT16);
+    if (wide_kernel && pairs <= sms) {
+      // Fewer items than SMs: split each item into as many pieces as fit one
+      // wave of one CTA per SM.  Measured on 4096-token contexts (32 query /
+      // 8 kv heads, fp16), 1 / 4 / 12 sequences: 20.3 / 24.4 / 40.7 µs,
+      // against 23.0 / 35.3 / 70.1 with the 128-token splits of the rule
+      // below and 26.7 / 26.7 / 40.7 with one split per item.
+      const int64_t ns_target = sms / pairs;
+      int64_t u = (max_units + ns_target - 1) / ns_target;
+      if (u < 1) u = 1;
+      if (u > cap_ups) u = cap_ups;
+      ups = static_cast<int>(u);
+    } else {
+      // Long splits cost the least per byte (each CTA pays its pipeline fill
+      // and merge once): start at 2048 tokens and halve (down to 128) only
+      // while the grid would give the SMs fewer than 4 CTAs each.
+      const int64_t target = sms * 4;
+      ups = max_ups;
+      while (ups > 8 && pairs * ((max_units + ups - 1) / ups) < target) ups /= 2;
+      // One split per item, with no combine pass, when no item can exceed
+      // 257 units (4096 tokens at any alignment) and the items either balance
+      // the SMs on their own (32 or more per SM: a serving batch of 8192
+      // items of up to 2080 tokens, 5 % less time than 2048-token splits) or
+      // fill at least four fifths of them one item each.
+      if (max_units > ups && max_units <= 2 * max_ups + 1 &&
+          (pairs >= 32 * sms || (pairs <= sms && 5 * pairs >= 4 * sms)))
+        ups = static_cast<int>(max_units);
+    }
   }
   int64_t ns = (max_units + ups - 1) / ups;
   if (ns < 1) ns = 1;

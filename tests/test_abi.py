@@ -99,11 +99,18 @@ def test_slot_mapping_argument_checks(pkv_lib):
     # (num_seqs, hq, layout args, max_blocks, window) -> (tokens_per_split, num_splits)
     ((64, 32, (10000, 32, 16, 128, 1), 256, 0), (2048, 2)),
     ((256, 32, (44000, 8, 32, 128, 2), 256, 0), (2048, 4)),
-    # 128 items (under one per SM), windows of 4096 tokens: one split each
+    # fewer items than SMs (16-bit, head_dim 128): one wave of at most one
+    # CTA per SM -- 128 or 96 windows one split each, a single 4096-token
+    # sequence's 8 items in 19 pieces each
     ((16, 32, (30000, 8, 16, 128, 2), 2048, 4096), (4112, 1)),
-    ((16, 32, (30000, 8, 16, 128, 2), 2048, 4097), (1024, 5)),
+    ((12, 32, (30000, 8, 16, 128, 2), 2048, 4096), (4112, 1)),
+    ((1, 32, (4096, 8, 16, 128, 1), 256, 0), (224, 19)),
+    ((4, 32, (4096, 8, 16, 128, 1), 256, 0), (1024, 4)),
+    # the same few items at head_dim 64 keep the 4-CTAs-per-SM splits
+    ((1, 32, (4096, 8, 16, 64, 1), 256, 0), (128, 32)),
+    ((16, 32, (30000, 8, 16, 128, 2), 2048, 4097), (4128, 1)),
     ((4, 8, (32, 8, 16, 64, 0), 7, 0), (128, 1)),
-    ((1, 8, (4096, 8, 16, 128, 1), 2048, 0), (256, 128)),
+    ((1, 8, (4096, 8, 16, 128, 1), 2048, 0), (1728, 19)),
     # 32+ items per SM and at most 257 units each: one split per item
     ((1024, 32, (50000, 8, 16, 128, 1), 130, 0), (2080, 1)),
     ((1024, 32, (50000, 8, 16, 128, 1), 256, 0), (4096, 1)),
