@@ -6,8 +6,10 @@
 A step is one pass of the whole path over one batch: the slot-mapped append
 of every sequence's new token, then decode attention (split-K + log-sum-exp
 combine) over every sequence's paged context.  Inputs are seeded synthetic
-data resident in HBM; the K/V pool (GBs) is far larger than the 129 MB L2,
-so no flush is needed between steps for the default workload.
+data resident in HBM.  The default workload is the largest of the five:
+GQA bf16, 256 sequences, 32 query / 8 kv heads, head_dim 128, block_size 32,
+contexts uniform in [1024, 8192] (about 4.8 GB of K/V a step, far larger than
+the 129 MB L2, so no flush is needed between its steps).
 
 Prints one JSON line (rank 0).  `value` is the effective HBM throughput of the
 step in GB/s (algorithmic bytes: K/V in context, q, out, block-table entries,
@@ -38,7 +40,7 @@ if REPO not in sys.path:
     sys.path.insert(0, REPO)
 
 METRIC = "paged decode: effective KV HBM GB/s (% of GB300 peak) and decode tokens/sec"
-DEFAULT_WORKLOAD = "mha_fp16"
+DEFAULT_WORKLOAD = "gqa_bf16"
 L2_BYTES = 129 * 1024 * 1024
 FALLBACK_HBM_GBS = 6800.0
 DTYPE_NAME = {torch.float32: "f32", torch.float16: "f16", torch.bfloat16: "bf16"}

@@ -341,7 +341,10 @@ int pkv_decode_plan(int32_t num_seqs, int32_t num_q_heads, const pkv_cache_layou
  *   PKV_ERR_UNSUPPORTED (pkv_decode_noalloc_ex takes them).
  *   Set-up: the first call on each device looks up the buffer's device address
  *   (cudaGetSymbolAddress) with that device current; make that first call
- *   before any stream capture.
+ *   before any stream capture.  The address is kept until
+ *   pkv_release_workspaces; after a device reset (cudaDeviceReset reloads
+ *   the library's device image) call pkv_release_workspaces before the next
+ *   pkv_decode_noalloc, so that it looks the buffer up again.
  *   Sharing: every call on every stream of a device uses the same buffer,
  *   which keeps the last call's partial results.  Nothing in it needs to start
  *   at zero (each call writes every partial it reads), but calls that overlap
@@ -408,9 +411,10 @@ const char* pkv_status_string(int status);
 
 /*
  * pkv_release_workspaces -- free every split-K workspace the library holds,
- * outgrown ones included.  Synchronises the device; call it only when no
- * pkv_decode is in flight and no captured graph that contains one will run
- * again.
+ * outgrown ones included, and forget the device addresses of the fixed
+ * scratch buffer of pkv_decode_noalloc (looked up again on the next call).
+ * Synchronises the device; call it only when no pkv_decode is in flight and
+ * no captured graph that contains one will run again.
  */
 int pkv_release_workspaces(void);
 

@@ -20,7 +20,7 @@
  *        (sliding_window_attention: start = max(0, T - window), attend over
  *        [start, T)).
  *
- * Readings of the pages that this file takes (each is listed in the design doc):
+ * Readings of the pages that this file takes:
  *   - The physical pool is stored head-major, [num_blocks][num_kv_heads]
  *     [block_size][head_dim]; this is a storage order only, indexed
  *     explicitly below.  Token t of a sequence lives in physical block

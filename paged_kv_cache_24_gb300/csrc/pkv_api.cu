@@ -701,6 +701,7 @@ int pkv_release_workspaces(void) {
   }
   cudaSetDevice(prev);
   g_ws.clear();
+  pkv::noalloc_forget();
   return rc;
 }
 

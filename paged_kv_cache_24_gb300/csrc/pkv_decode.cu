@@ -387,7 +387,12 @@ decode16_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant_
     const int yj = y_of(j, j);
     const bool ok = mbar_wait_bounded(smem_u32(&bars[warp][stage]), parity, kWaitLimit);
     if (!__all_sync(0xffffffffu, ok)) {
-      bad = true;  // the copy never landed; stop using this ring
+      // The copy has not landed: stop using this ring.  Units j .. j+S-1 may
+      // still have copies in flight, and the ring becomes the merge buffer
+      // after the loop, so wait (bounded again) for each of them first.
+      bad = true;
+      for (int jj = j; jj < j + S && jj < my_n; ++jj)
+        mbar_wait_bounded(smem_u32(&bars[warp][jj % S]), (jj / S) & 1, kWaitLimit);
       break;
     }
     if (yj < 0) bad = true;

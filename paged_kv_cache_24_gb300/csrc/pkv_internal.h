@@ -140,5 +140,7 @@ cudaError_t launch_slot_mapping(const int32_t* block_tables, int num_seqs, int m
 // Device address of the library-resident split-K scratch buffer
 // (PKV_NOALLOC_SCRATCH_BYTES) on `device`, which must be current.
 int noalloc_scratch(int device, void** addr);
+// Forget the looked-up addresses (pkv_release_workspaces; after a device reset).
+void noalloc_forget();
 
 }  // namespace pkv

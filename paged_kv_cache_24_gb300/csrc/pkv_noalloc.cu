@@ -13,6 +13,9 @@
 // host code its name is only a host-side stand-in, so the device address is
 // looked up once per device with cudaGetSymbolAddress (that device current,
 // on the first call there) and passed to the kernels as a plain pointer.
+// pkv_release_workspaces forgets the looked-up addresses, so that after a
+// device reset (which reloads the library's device image) the next call looks
+// the buffer up again instead of using a stale address.
 // Every call shares the buffer and leaves its partials in it; nothing needs
 // clearing (each call writes every partial it reads), but calls that overlap
 // on the GPU race on it.
@@ -45,6 +48,11 @@ int noalloc_scratch(int device, void** addr) {
   }
   *addr = g_scratch_addr[device];
   return PKV_OK;
+}
+
+void noalloc_forget() {
+  std::lock_guard<std::mutex> lock(g_scratch_mutex);
+  for (void*& a : g_scratch_addr) a = nullptr;
 }
 
 }  // namespace pkv

@@ -16,18 +16,18 @@
 //   warp 9       (load)    TMA of the 16-key K and V units of each key tile
 //                          into two rings of stages (128-byte swizzle), lane
 //                          i issuing unit i's copies;
-//   warps 10-11  (V prep)  turn each landed V tile into fp16 in place (bf16
-//                          caches) and zero the rows of keys no row of the CTA
-//                          may see, so garbage (even NaN) in unused slots
-//                          cannot leak through a zero weight;
+//   warps 10-11  (V prep)  zero the rows of keys no row of the CTA may see in
+//                          each landed V tile, so garbage (even NaN) in unused
+//                          slots cannot leak through a zero weight;
 //   warp 8       (MMA)     one thread waits and issues S_t = Q_t K^T (M 128, N 128, both
 //                          operands K-major in shared memory) and
 //                          O_t += P_t V (A = P_t read from TMEM, B = V read
 //                          MN-major from its stage);
 //   warps 0-3 / 4-7        tile 0 / tile 1 softmax: each thread owns one row
 //                          (its TMEM lane), loads its 128 scores, masks, keeps
-//                          the running maximum and sum, writes P as fp16 over
-//                          the scores it came from, and, when the maximum
+//                          the running maximum and sum, writes P over the
+//                          scores it came from (fp16 caches: one fp16 P; bf16
+//                          caches: P = hi + lo, two bf16 parts), and, when the maximum
 //                          moved by more than 2^8, rescales its O row in TMEM
 //                          (lazy rescaling).
 // While one tile's rows are in the softmax, the tensor cores work on the
@@ -97,12 +97,16 @@ __device__ __forceinline__ uint32_t sw128(int row, int chunk) {
   return static_cast<uint32_t>(row * 128 + (((chunk & 7) ^ (row & 7)) << 4));
 }
 
-// two bf16 (low half first) -> two fp16, rounded to nearest; a value beyond
-// the fp16 range becomes an infinity, which the P.V product then carries
-// into every output row of the CTA (as inf or NaN): no separate range test
-__device__ __forceinline__ uint32_t bf16x2_to_f16x2(uint32_t w) {
-  const float lo = __uint_as_float(w << 16), hi = __uint_as_float(w & 0xffff0000u);
-  return Mma<__half>::pack(lo, hi);
+// Two probabilities as a hi + lo pair of bf16 values (low half first in each
+// word): hi = p rounded to bf16, lo = the remainder p - hi (exact in fp32)
+// rounded to bf16, so hi + lo carries p to about 2^-17 of itself.  A bf16
+// cache keeps V in bf16 (the tensor cores take P and V in one type), and the
+// P.V product runs twice, once per part.
+__device__ __forceinline__ void split_bf16x2(float2 pr, uint32_t& hi, uint32_t& lo) {
+  hi = Mma<__nv_bfloat16>::pack(pr.x, pr.y);
+  const float2 hf = make_float2(__uint_as_float(hi << 16), __uint_as_float(hi & 0xffff0000u));
+  const float2 r = ffma2(hf, make_float2(-1.f, -1.f), pr);
+  lo = Mma<__nv_bfloat16>::pack(r.x, r.y);
 }
 
 // kSinks: the key range has a sink section (window > 0, num_sinks > 0); the
@@ -115,7 +119,8 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
   constexpr int SK = Lay::kKStages, SV = Lay::kVStages;
   constexpr bool kBf16 = __is_same(T, __nv_bfloat16);
   constexpr uint32_t kIdS = umma_idesc_f16(kBf16 ? 1u : 0u, kQT, kTKeys, 0);
-  constexpr uint32_t kIdO = umma_idesc_f16(0u, kQT, D, 1);  // P and V in fp16
+  // P.V: P and V in the cache's type (bf16: P as hi + lo, two products)
+  constexpr uint32_t kIdO = umma_idesc_f16(kBf16 ? 1u : 0u, kQT, D, 1);
 
   extern __shared__ uint8_t smem_raw[];
   __shared__ __align__(8) uint64_t k_full[SK], k_empty[SK], v_full[SV], v_ready[SV], v_empty[SV];
@@ -303,7 +308,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
           if (!mbar_wait_bounded(smem_u32(&v_full[t % SV]), (t / SV) & 1, kWaitLimit)) bad = true;
       }
     } else if (warp >= kPrepWarp0) {
-      // ============ V prep: fp16 in place (bf16 caches), unseen keys zeroed ============
+      // ============ V prep: rows of keys no row of the CTA sees zeroed ============
       const int ct = tid - kPrepWarp0 * 32;
       for (int j = 0; j < n_tiles; ++j) {
         if (!mbar_wait_bounded(smem_u32(&v_full[j % SV]), (j / SV) & 1, kWaitLimit)) bad = true;
@@ -311,33 +316,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
         const uint32_t vt = v_addr(j);
         // a window tile wholly inside [k_lo, pos1] keeps every key
         const bool whole = j >= sink_tiles && t0 >= k_lo && t0 + kTKeys - 1 <= pos1;
-        if (kBf16 && whole) {
-#pragma unroll 4
-          for (int u = ct; u < Lay::kKVTile / 16; u += kPrepThreads) {  // 16-byte chunks
-            uint4 x = ld_shared_v4(vt + u * 16);
-            x.x = bf16x2_to_f16x2(x.x);
-            x.y = bf16x2_to_f16x2(x.y);
-            x.z = bf16x2_to_f16x2(x.z);
-            x.w = bf16x2_to_f16x2(x.w);
-            st_shared_v4(vt + u * 16, x);
-          }
-        } else if (kBf16) {
-#pragma unroll 4
-          for (int u = ct; u < Lay::kKVTile / 16; u += kPrepThreads) {
-            // chunk u: unit u / (kVUnitBytes / 16), row (u / 8) % 16 of it
-            const int kp = t0 + (u / (Lay::kVUnitBytes / 16)) * kUnitTokens + ((u >> 3) & 15);
-            uint4 x = ld_shared_v4(vt + u * 16);
-            if (kSinks ? !key_kept(j, kp) : (kp < k_lo || kp > pos1)) {
-              x = make_uint4(0u, 0u, 0u, 0u);
-            } else {
-              x.x = bf16x2_to_f16x2(x.x);
-              x.y = bf16x2_to_f16x2(x.y);
-              x.z = bf16x2_to_f16x2(x.z);
-              x.w = bf16x2_to_f16x2(x.w);
-            }
-            st_shared_v4(vt + u * 16, x);
-          }
-        } else if (!whole) {
+        if (!whole) {
           for (int r = ct; r < kTKeys; r += kPrepThreads) {
             const int kp = t0 + r;
             if (kSinks ? key_kept(j, kp) : (kp >= k_lo && kp <= pos1)) continue;
@@ -396,10 +375,15 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
             if (!mbar_wait_bounded(smem_u32(&p_full[t]), j & 1, kWaitLimit)) bad = true;
             tc_fence_after();
 #pragma unroll
-            for (int kk = 0; kk < kTKeys / 16; ++kk)
-              umma_f16_ts(tmem + Lay::o_col(t), tmem + Lay::s_col(t) + kk * 8,
-                          v0 + static_cast<uint64_t>((kk * Lay::kVUnitBytes) >> 4), kIdO,
+            for (int kk = 0; kk < kTKeys / 16; ++kk) {
+              const uint64_t vb = v0 + static_cast<uint64_t>((kk * Lay::kVUnitBytes) >> 4);
+              umma_f16_ts(tmem + Lay::o_col(t), tmem + Lay::s_col(t) + kk * 8, vb, kIdO,
                           (j > 0 || kk > 0) ? 1u : 0u);
+              // bf16: the lo parts of P, kTKeys / 2 columns after the hi parts
+              if constexpr (kBf16)
+                umma_f16_ts(tmem + Lay::o_col(t), tmem + Lay::s_col(t) + kTKeys / 2 + kk * 8, vb,
+                            kIdO, 1u);
+            }
             if (j + 1 == n_tiles) umma_commit(smem_u32(&o_done[t]));  // O_t final
             if (t == 1) umma_commit(smem_u32(&v_empty[j % SV]));
             if (j + 1 < n_tiles) {
@@ -496,20 +480,38 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
         tmem_st16(tO + c, v);
       }
     }
-    // P = 2^(s*sl - m) as fp16 over the first 64 columns of S_t
+    // P = 2^(s*sl - m) over the columns of S_t: fp16 in the first 64 (fp16
+    // caches), or bf16 hi parts in the first 64 and lo parts in the next 64
     float2 acc[4] = {{0.f, 0.f}, {0.f, 0.f}, {0.f, 0.f}, {0.f, 0.f}};
     const float2 sl2 = make_float2(sl, sl), nm2 = make_float2(neg_m, neg_m);
+    if constexpr (kBf16) {
+      // 16 keys at a time: the hi and lo words of 8 pairs, stored as they come
 #pragma unroll
-    for (int h = 0; h < kTKeys / 32; ++h) {
-      uint32_t w[16];
+      for (int h = 0; h < kTKeys / 16; ++h) {
+        uint32_t w[8], wl[8];
 #pragma unroll
-      for (int i = 0; i < 16; ++i) {
-        const float2 x = ffma2(make_float2(s[h * 32 + 2 * i], s[h * 32 + 2 * i + 1]), sl2, nm2);
-        const float2 pr = make_float2(ex2(x.x), ex2(x.y));
-        acc[i & 3] = fadd2(acc[i & 3], pr);
-        w[i] = Mma<__half>::pack(pr.x, pr.y);
+        for (int i = 0; i < 8; ++i) {
+          const float2 x = ffma2(make_float2(s[h * 16 + 2 * i], s[h * 16 + 2 * i + 1]), sl2, nm2);
+          const float2 pr = make_float2(ex2(x.x), ex2(x.y));
+          acc[i & 3] = fadd2(acc[i & 3], pr);
+          split_bf16x2(pr, w[i], wl[i]);
+        }
+        tmem_st8u(tS + h * 8, w);
+        tmem_st8u(tS + kTKeys / 2 + h * 8, wl);
       }
-      tmem_st16u(tS + h * 16, w);
+    } else {
+#pragma unroll
+      for (int h = 0; h < kTKeys / 32; ++h) {
+        uint32_t w[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          const float2 x = ffma2(make_float2(s[h * 32 + 2 * i], s[h * 32 + 2 * i + 1]), sl2, nm2);
+          const float2 pr = make_float2(ex2(x.x), ex2(x.y));
+          acc[i & 3] = fadd2(acc[i & 3], pr);
+          w[i] = Mma<__half>::pack(pr.x, pr.y);
+        }
+        tmem_st16u(tS + h * 16, w);
+      }
     }
     const float2 a01 = fadd2(acc[0], acc[1]), a23 = fadd2(acc[2], acc[3]);
     l_run = l_run * alpha + ((a01.x + a01.y) + (a23.x + a23.y));

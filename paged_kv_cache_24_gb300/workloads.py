@@ -8,9 +8,9 @@ slots with its own code), so it can feed both without coupling them.
 
 Workload recipes follow the five benchmark configurations of this project
 (tiny fp32 / MHA fp16 / GQA bf16 / sliding-window bf16 / serving mix fp16).
-The block pool and its LIFO free list follow the block allocator of
-"Build a Paged KV Cache in Pure Python", Step 2 (``BlockAllocator``: a stack of
-free block ids, ``pop()`` to allocate, ``MemoryError`` when exhausted).
+The serving mix's fragmented pool hands out its free block ids last in, first
+out, as the allocator of "Build a Paged KV Cache in Pure Python", Step 2 does
+(``FreeBlockStack`` here).
 
 Poisoning: every pool slot that no sequence's context covers holds NaN (and,
 with ``poison_outside_window``, every slot before a sequence's window start
@@ -28,43 +28,44 @@ import numpy as np
 import torch
 
 __all__ = [
-    "BlockAllocator", "WorkloadSpec", "Workload", "make_workload", "CONFIGS", "config_spec",
+    "FreeBlockStack", "WorkloadSpec", "Workload", "make_workload", "CONFIGS", "config_spec",
 ]
 
 
-class BlockAllocator:
-    """Fixed pool of block ids with a LIFO free list (stack), like a page allocator.
+class FreeBlockStack:
+    """The serving workload's pool bookkeeping: block ids not in use sit on a
+    stack, and a request takes ids from its top (so the ids a sequence gave
+    back are the first reused).
 
-    ``allocate`` pops ids from the end of the free list and raises ``MemoryError``
-    when the pool cannot satisfy the request; ``deallocate`` pushes a sequence's
-    ids back.  Pure host bookkeeping: it never touches K/V data.
+    The pages' allocator behaves the same way (a LIFO free list, an error once
+    the pool cannot serve a request); this is only the part the serving mix
+    needs to lay out a fragmented, partly occupied pool from a seed.  It never
+    touches K/V data.
     """
 
-    def __init__(self, total_blocks: int, free_list: Optional[List[int]] = None):
-        self.total_blocks = int(total_blocks)
-        self.free_list: List[int] = (list(range(total_blocks)) if free_list is None
-                                     else [int(x) for x in free_list])
-        self.used_map: dict = {}
+    def __init__(self, num_blocks: int, stack: Optional[List[int]] = None):
+        self.num_blocks = int(num_blocks)
+        self.stack: List[int] = (list(range(self.num_blocks)) if stack is None
+                                 else [int(x) for x in stack])
+        self.held_by: dict = {}
 
-    def allocate(self, seq_id: int, num_blocks: int = 1) -> List[int]:
-        if len(self.free_list) < num_blocks:
-            raise MemoryError(
-                f"KV cache out of memory: need {num_blocks} blocks, "
-                f"only {len(self.free_list)} free of {self.total_blocks} total.")
-        got = [self.free_list.pop() for _ in range(num_blocks)]
-        self.used_map.setdefault(seq_id, []).extend(got)
-        return got
+    def take(self, owner: int, count: int = 1) -> List[int]:
+        """Pop `count` ids for `owner`; MemoryError when fewer are left."""
+        if count > len(self.stack):
+            raise MemoryError(f"block pool exhausted: {count} requested, {len(self.stack)} of "
+                              f"{self.num_blocks} left")
+        ids = self.stack[len(self.stack) - count:][::-1]
+        del self.stack[len(self.stack) - count:]
+        self.held_by[owner] = self.held_by.get(owner, []) + ids
+        return ids
 
-    def deallocate(self, seq_id: int) -> None:
-        for idx in self.used_map.pop(seq_id, []):
-            self.free_list.append(idx)
+    def give_back(self, owner: int) -> None:
+        """Push every id `owner` holds back onto the stack, in the order taken."""
+        self.stack.extend(self.held_by.pop(owner, []))
 
     @property
-    def free_blocks(self) -> int:
-        return len(self.free_list)
-
-    def used_blocks(self) -> int:
-        return sum(len(v) for v in self.used_map.values())
+    def available(self) -> int:
+        return len(self.stack)
 
 
 @dataclass
@@ -254,14 +255,14 @@ def make_workload(spec: WorkloadSpec, device="cpu", poison: bool = True,
             n = int(need0[b] - shared_per_seq[b])
             block_tables[b, shared_per_seq[b]:need0[b]] = occupied[cursor:cursor + n]
             cursor += n
-        alloc = BlockAllocator(nb, free_list=list(free))
+        alloc = FreeBlockStack(nb, stack=list(free))
         held = need0.copy()
         for s in range(S):                      # blocks the 32 steps need, in step order
             for b in range(B):
                 while held[b] * bs <= pos[s, b]:
-                    block_tables[b, held[b]] = alloc.allocate(b, 1)[0]
+                    block_tables[b, held[b]] = alloc.take(b)[0]
                     held[b] += 1
-        free_after = list(alloc.free_list)
+        free_after = list(alloc.stack)
 
     # ---- tensors ---------------------------------------------------------
     gen = torch.Generator(device=device)

@@ -68,17 +68,6 @@ def gpu_step(pkv, w, s, tokens_per_split=0, stream=None):
     return slots, out
 
 
-def sample_pairs(w, n, seed=0):
-    rng = np.random.default_rng(seed)
-    B, H = w.spec.num_seqs, w.spec.num_q_heads
-    lens = w.lens_steps[0].cpu().numpy()
-    picks = {(int(np.argmax(lens)), h) for h in range(H)} | {(int(np.argmin(lens)), h)
-                                                              for h in range(H)}
-    while len(picks) < n:
-        picks.add((int(rng.integers(B)), int(rng.integers(H))))
-    return np.array(sorted(picks), dtype=np.int32)
-
-
 # ---------------------------------------------------------------------------
 # small and mid-size cases: every output compared
 
@@ -293,7 +282,9 @@ def test_nondefault_stream(pkv_lib, oracle_lib):
 
 
 # ---------------------------------------------------------------------------
-# benchmark-size workloads: whole pool bit-exact after the append, sampled outputs
+# benchmark-size workloads: whole pool bit-exact after the append, and every
+# output compared with the oracle (at these sizes the float64 oracle takes
+# seconds on the host cores)
 
 
 @pytest.mark.parametrize("idx", [0, 1, 2, 3])
@@ -301,32 +292,49 @@ def test_benchmark_workload(pkv_lib, oracle_lib, idx):
     spec = config_spec(idx)
     w = make_workload(spec, device="cuda", poison_outside_window=True)
     mirror = HostMirror(w)
-    pairs = None if idx == 0 else sample_pairs(w, 96, seed=idx)
-    o_slots, ref = mirror.step(0, pairs=pairs)
+    o_slots, ref = mirror.step(0)
     g_slots, out = gpu_step(pkv_lib, w, 0)
     torch.cuda.synchronize()
     assert np.array_equal(g_slots.cpu().numpy(), o_slots)
     assert torch.equal(_bits(w.k_cache.cpu()), _bits(mirror.kc))
     assert torch.equal(_bits(w.v_cache.cpu()), _bits(mirror.vc))
-    got = out if pairs is None else out[torch.from_numpy(pairs[:, 0]).long(),
-                                        torch.from_numpy(pairs[:, 1]).long()]
-    check_close(got, ref, spec.dtype, plain=(idx > 0))
-    assert torch.isfinite(out.float()).all()
+    # the long-context workloads' outputs are far below 1: the plain bound holds
+    check_close(out, ref, spec.dtype, plain=(idx > 0))
+
+
+def test_fused_benchmark_workload_all_outputs(pkv_lib, oracle_lib):
+    """The benchmark's own launch (fused append + decode, the library's plan)
+    on the GQA workload: the whole pool bit-exact and every output within the
+    plain 2e-3 of the oracle."""
+    spec = config_spec(2)
+    w = make_workload(spec, device="cuda", poison_outside_window=True)
+    mirror = HostMirror(w)
+    _, ref = mirror.step(0)
+    out = pkv_lib.pkv_append_decode(w.q_steps[0], w.k_steps[0], w.v_steps[0], w.k_cache,
+                                    w.v_cache, w.block_tables, w.lens_steps[0].contiguous(),
+                                    spec.window, w.scale)
+    torch.cuda.synchronize()
+    assert torch.equal(_bits(w.k_cache.cpu()), _bits(mirror.kc))
+    assert torch.equal(_bits(w.v_cache.cpu()), _bits(mirror.vc))
+    check_close(out, ref, spec.dtype, plain=True)
 
 
 def test_serving_mix_32_steps(pkv_lib, oracle_lib):
+    """All 32 append + decode steps of the serving mix; every output of 8
+    steps spread over the run (first, last and six between) compared with the
+    oracle, and the whole pool bit-exact at the end."""
     spec = config_spec(4)
     w = make_workload(spec, device="cuda")
     mirror = HostMirror(w)
-    pairs = sample_pairs(w, 64, seed=4)
+    checked = {0, 4, 9, 13, 18, 22, 27, spec.steps - 1}
     for s in range(spec.steps):
-        check = s in (0, 13, spec.steps - 1)
-        o_slots, ref = mirror.step(s, pairs=pairs if check else np.zeros((0, 2), np.int32))
+        check = s in checked
+        o_slots, ref = mirror.step(s, pairs=None if check else np.zeros((0, 2), np.int32))
         g_slots, out = gpu_step(pkv_lib, w, s)
         assert np.array_equal(g_slots.cpu().numpy(), o_slots)
         if check:
-            got = out[torch.from_numpy(pairs[:, 0]).long(), torch.from_numpy(pairs[:, 1]).long()]
-            check_close(got, ref, spec.dtype, plain=True)
+            torch.cuda.synchronize()
+            check_close(out, ref, spec.dtype, plain=True)
     torch.cuda.synchronize()
     assert torch.equal(_bits(w.k_cache.cpu()), _bits(mirror.kc))
     assert torch.equal(_bits(w.v_cache.cpu()), _bits(mirror.vc))

@@ -219,23 +219,56 @@ def test_prefill_nonpositive_scale(pkv_lib, oracle_lib, scale):
     assert (err <= 2e-3 + 0.5 * torch.finfo(torch.bfloat16).eps * np.abs(ref)).all(), err.max()
 
 
-def test_prefill_bf16_value_beyond_fp16_range(pkv_lib):
-    """The P.V product runs in fp16: a bf16 V value beyond the fp16 range makes
-    the rows of the work items that read it non-finite (never silently wrong),
-    and leaves every other row as it was."""
+@pytest.mark.parametrize("window,sinks", [(0, 0), (90, 5)])
+def test_prefill_bf16_extreme_values_match_oracle(pkv_lib, oracle_lib, window, sinks):
+    """bf16 caches are exact over bf16's whole range: V values far beyond the
+    fp16 range (7e4, 1e6, 1e30) and far below fp16's normal range (3e-6,
+    1e-30), in cached prefix keys and in the chunk's own keys, give the
+    oracle's output -- within the usual tolerance, and within a relative
+    2^-7 on the columns that hold them (all of one sign, so no cancellation
+    hides an error)."""
     dtype = torch.bfloat16
-    w, q, k, v, cu, lens = _prefill_case(dtype, 4, 2, 128, 16, [30, 30], [10, 10], 0, seed=5)
-    ref = pkv_lib.pkv_prefill(q, k, v, cu, w.k_cache.clone(), w.v_cache.clone(),
-                              w.block_tables, lens, 0, w.scale, max_chunk=10)
+    prefixes, chunks = [30, 300], [10, 200]
+    w, q, k, v, cu, lens = _prefill_case(dtype, 8, 2, 128, 16, prefixes, chunks, window,
+                                         seed=17)
+    g = torch.Generator(device="cuda").manual_seed(23)
+
+    def pos(shape, scale):  # positive values of one magnitude
+        return ((1.0 + torch.rand(shape, generator=g, device="cuda")) * scale).to(dtype)
+
     bt = w.block_tables.cpu().numpy()
-    s = oracle.slot_for_position(bt[0], 16, 5)       # a prefix key of sequence 0
-    w.v_cache[s // 16, 0, s % 16, 3] = 1.0e6            # kv head 0; fp16 tops out at 65504
-    out = pkv_lib.pkv_prefill(q, k, v, cu, w.k_cache, w.v_cache, w.block_tables, lens, 0,
-                              w.scale, max_chunk=10)
+    bs = w.spec.block_size
+    # (kv head, column) -> magnitude, written into every prefix key and every
+    # chunk key of both sequences
+    special = {(0, 3): 1.0e6, (0, 11): 1.0e-30, (1, 7): 1.0e30, (1, 12): 3.0e-6,
+               (1, 40): 7.0e4}
+    for b, (p, n) in enumerate(zip(prefixes, chunks)):
+        s_pref = [oracle.slot_for_position(bt[b], bs, t) for t in range(p)]
+        if s_pref:
+            s_arr = torch.tensor(s_pref, device="cuda")
+            for (h, c), mag in special.items():
+                w.v_cache[s_arr // bs, h, s_arr % bs, c] = pos(len(s_pref), mag)
+    for (h, c), mag in special.items():
+        v[:, h, c] = pos(v.shape[0], mag)
+    kc_h, vc_h = w.k_cache.cpu(), w.v_cache.cpu()
+    lens_h = lens.cpu().numpy()
+    slots = [oracle.slot_for_position(bt[b], bs, lens_h[b] - n + i)
+             for b, n in enumerate(chunks) for i in range(n)]
+    oracle.append(k.cpu(), v.cpu(), np.array(slots, np.int64), kc_h, vc_h)
+    ref = oracle.prefill(q.cpu(), cu.cpu().numpy(), kc_h, vc_h, bt, lens_h, window, w.scale,
+                         num_sinks=sinks)
+    out = torch.full_like(q, float("nan"))
+    pkv_lib.pkv_prefill(q, k, v, cu, w.k_cache, w.v_cache, w.block_tables, lens, window,
+                        w.scale, max_chunk=max(chunks), out=out, num_sinks=sinks)
     torch.cuda.synchronize()
-    o, r = out.float().cpu(), ref.float().cpu()
-    # sequence 0's tokens 0..9, query heads 0 and 1 (kv head 0): non-finite
-    assert not torch.isfinite(o[:10, :2]).all()
-    # the other kv head of sequence 0 and all of sequence 1: unchanged
-    assert torch.equal(o[:10, 2:], r[:10, 2:])
-    assert torch.equal(o[10:], r[10:])
+    got = out.double().cpu().numpy()
+    assert np.isfinite(got).all()
+    err = np.abs(got - ref)
+    tol = 2e-3 + 0.5 * torch.finfo(dtype).eps * np.abs(ref)
+    assert (err <= tol).all(), f"max err {err.max():.3e}"
+    G = 4  # query heads per kv head
+    for (h, c), mag in special.items():
+        r = ref[:, h * G:(h + 1) * G, c]
+        e = err[:, h * G:(h + 1) * G, c]
+        assert (r > 0).all()
+        assert (e <= 2.0 ** -7 * r).all(), (h, c, float((e / r).max()))

@@ -1,4 +1,4 @@
-"""Host-side checks of the seeded workload generator and the LIFO block allocator."""
+"""Host-side checks of the seeded workload generator and the LIFO free-block stack."""
 import json
 import os
 
@@ -6,7 +6,7 @@ import numpy as np
 import pytest
 import torch
 
-from paged_kv_cache_24_gb300.workloads import BlockAllocator, config_spec, make_workload
+from paged_kv_cache_24_gb300.workloads import FreeBlockStack, config_spec, make_workload
 
 GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
 
@@ -18,30 +18,33 @@ def _p2():
 
 def test_allocator_counts_from_the_page():
     g = _p2()["allocator"]
-    a = BlockAllocator(g["total_blocks"])
-    got = a.allocate(seq_id=1, num_blocks=g["allocate"])
-    assert len(got) == g["allocate"]
-    assert a.free_blocks == g["free_after_allocate"]
-    a.deallocate(1)
-    assert a.free_blocks == g["free_after_deallocate"]
-    assert a.used_map == {}
+    a = FreeBlockStack(g["total_blocks"])
+    got = a.take(owner=1, count=g["allocate"])
+    assert len(got) == len(set(got)) == g["allocate"]
+    assert a.available == g["free_after_allocate"]
+    a.give_back(1)
+    assert a.available == g["free_after_deallocate"]
+    assert a.held_by == {}
 
 
 def test_allocator_is_lifo_and_raises_when_exhausted():
     g = _p2()["exhaustion"]
-    a = BlockAllocator(g["total_blocks"], free_list=[3, 1, 0, 2])
-    assert a.allocate(0, 1) == [2]   # pops from the end of the stack
-    a.deallocate(0)
-    assert a.allocate(5, 1) == [2]   # the block just returned comes back first
-    a.deallocate(5)
+    a = FreeBlockStack(g["total_blocks"], stack=[3, 1, 0, 2])
+    assert a.take(0) == [2]          # the top of the stack first
+    a.give_back(0)
+    assert a.take(5) == [2]          # the block just returned comes back first
+    assert a.take(6, 2) == [0, 1]    # then the next ones down, top first
+    a.give_back(6)
+    a.give_back(5)
+    assert a.stack == [3, 0, 1, 2]
     # one block per 16 tokens: 64 tokens fit in 4 blocks, the 65th does not
     held = 0
     for pos in range(g["tokens_before_error"]):
         if pos // g["block_size"] >= held:
-            a.allocate(7, 1)
+            a.take(7)
             held += 1
     with pytest.raises(MemoryError):
-        a.allocate(7, 1)
+        a.take(7)
 
 
 def _slots_of(w, b, upto):

@@ -4,10 +4,11 @@ Some callers cannot let a library call cudaMalloc: a serving engine that has
 already handed all free HBM to its own KV-block pool, or a hot loop that must
 not run into the device-wide synchronisation cudaMalloc / cudaFree can bring.
 pkv_decode_noalloc serves them with a fixed scratch buffer that lives in the
-library image.  These checks call it through the C ABI and compare it with
-pkv_decode, the entry point that allocates its workspace, on two calls in a
+library image.  These checks call it through the C ABI, on two calls in a
 row (the second call runs over the first call's leftovers in the shared
-buffer).  This file is collected last on purpose.
+buffer), with the device's free memory unchanged across them, and compare
+its outputs with the float64 oracle and with pkv_decode, the entry point
+that allocates its workspace.  This file is collected last on purpose.
 """
 import ctypes
 
@@ -15,6 +16,7 @@ import numpy as np
 import pytest
 import torch
 
+import oracle
 from paged_kv_cache_24_gb300.workloads import config_spec, make_workload
 
 pytestmark = pytest.mark.gpu
@@ -33,11 +35,12 @@ def _noalloc_fn(pkv):
     return fn
 
 
-def _call_noalloc(pkv, fn, q, kc, vc, bt, lens, window, scale, out):
+def _call_noalloc(pkv, fn, q, kc, vc, bt, lens, window, scale, out, stream=None):
     layout = pkv.cache_layout(kc)
+    st = (stream or torch.cuda.current_stream()).cuda_stream
     return fn(q.data_ptr(), q.shape[0], q.shape[1], kc.data_ptr(), vc.data_ptr(),
               ctypes.byref(layout), bt.data_ptr(), bt.shape[1], lens.data_ptr(), window,
-              scale, out.data_ptr(), torch.cuda.current_stream().cuda_stream)
+              scale, out.data_ptr(), st)
 
 
 def _close(a, b, dtype):
@@ -49,7 +52,10 @@ def _close(a, b, dtype):
 
 @pytest.mark.parametrize("dtype,window", [(torch.bfloat16, 0), (torch.float16, 4500),
                                           (torch.float32, 0)])
-def test_noalloc_matches_allocating_decode_twice(pkv_lib, dtype, window):
+def test_noalloc_matches_allocating_decode_twice(pkv_lib, oracle_lib, dtype, window):
+    """Two no-alloc calls in a row on a stream no allocating call has used,
+    with the device's free memory unchanged across them; each output is
+    compared with the float64 oracle and with pkv_decode's."""
     pkv = pkv_lib
     fn = _noalloc_fn(pkv)
     spec = config_spec(0, dtype=dtype, num_seqs=6, num_q_heads=16, num_kv_heads=4,
@@ -62,16 +68,34 @@ def test_noalloc_matches_allocating_decode_twice(pkv_lib, dtype, window):
     slots = pkv.pkv_slot_mapping(w.block_tables, w.pos_steps[0].contiguous(), 16)
     pkv.pkv_append(w.k_steps[0], w.v_steps[0], slots, w.k_cache, w.v_cache)
     lens = w.lens_steps[0].contiguous()
-    for call in range(2):
-        # the second call uses other queries and shorter contexts, over what the
-        # first call left in the shared scratch
-        q = w.q_steps[0] if call == 0 else torch.flip(w.q_steps[0], dims=[0]).contiguous()
-        ln = lens if call == 0 else torch.clamp(lens - 17, min=0).contiguous()
-        ref = pkv.pkv_decode(q, w.k_cache, w.v_cache, w.block_tables, ln, window, w.scale)
-        out = torch.full_like(q, float("nan"))
+    # the second call uses other queries and shorter contexts, over what the
+    # first call left in the shared scratch
+    qs = [w.q_steps[0], torch.flip(w.q_steps[0], dims=[0]).contiguous()]
+    lns = [lens, torch.clamp(lens - 17, min=0).contiguous()]
+    outs = [torch.full_like(q, float("nan")) for q in qs]
+    warm_out = torch.full_like(qs[0], float("nan"))
+    side, fresh = torch.cuda.Stream(), torch.cuda.Stream()
+    # once on a side stream first: loads the kernels' code and looks up the
+    # scratch buffer's address (the one-time set-up of the first call)
+    with torch.cuda.stream(side):
+        rc = _call_noalloc(pkv, fn, qs[1], w.k_cache, w.v_cache, w.block_tables, lns[1],
+                           window, w.scale, warm_out, stream=side)
+    assert rc == 0, pkv.status_string(rc)
+    torch.cuda.synchronize()
+    free_before = torch.cuda.mem_get_info()[0]
+    for q, ln, out in zip(qs, lns, outs):
         rc = _call_noalloc(pkv, fn, q, w.k_cache, w.v_cache, w.block_tables, ln, window,
-                           w.scale, out)
+                           w.scale, out, stream=fresh)
         assert rc == 0, pkv.status_string(rc)
+    fresh.synchronize()
+    assert torch.cuda.mem_get_info()[0] == free_before, "device memory was allocated"
+
+    kc_h, vc_h = w.k_cache.cpu(), w.v_cache.cpu()
+    bt_h = w.block_tables.cpu().numpy()
+    for q, ln, out in zip(qs, lns, outs):
+        ref_oracle = oracle.decode(q.cpu(), kc_h, vc_h, bt_h, ln.cpu().numpy(), window, w.scale)
+        _close(out.cpu(), torch.from_numpy(ref_oracle), dtype)
+        ref = pkv.pkv_decode(q, w.k_cache, w.v_cache, w.block_tables, ln, window, w.scale)
         torch.cuda.synchronize()
         _close(out, ref, dtype)
 
