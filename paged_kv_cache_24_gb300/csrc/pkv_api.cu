@@ -580,14 +580,30 @@ int pkv_prefill(const void* q, const void* k, const void* v, const int32_t* cu_q
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   int device = 0;
   if (cudaGetDevice(&device) != cudaSuccess) return PKV_ERR_CUDA;
-  void* order = nullptr;  // the items' order, written and read on this stream
-  rc = get_workspace(device, st, static_cast<size_t>(items) * sizeof(int32_t), &order);
+  // written and read on this stream: the items' order; bf16 caches: each
+  // (sequence, kv head)'s partial V ranges and each attention CTA's mode word
+  auto align16 = [](size_t x) { return (x + 15) & ~size_t(15); };
+  const size_t order_bytes = align16(static_cast<size_t>(items) * sizeof(int32_t));
+  const pkv::PrefillScan scan = pkv::prefill_scan_plan(max_blocks_per_seq, layout->block_size);
+  const bool bf16 = layout->dtype == PKV_BFLOAT16;
+  const size_t parts_bytes =
+      bf16 ? align16(static_cast<size_t>(num_seqs) * layout->num_kv_heads * scan.row_blocks * 8)
+           : 0;
+  const size_t mode_bytes =
+      bf16 ? static_cast<size_t>(pkv::prefill_ctas(num_seqs, num_q_heads, layout->num_kv_heads,
+                                                   max_chunk)) * sizeof(uint32_t)
+           : 0;
+  void* ws = nullptr;
+  rc = get_workspace(device, st, order_bytes + parts_bytes + mode_bytes, &ws);
   if (rc != PKV_OK) return rc;
+  char* wsb = static_cast<char*>(ws);
   return to_status(pkv::launch_prefill(
       layout->dtype, layout->head_dim, q, k, v, cu_q, num_seqs, num_q_heads, max_chunk, k_cache,
       v_cache, layout->num_blocks, layout->num_kv_heads, layout->block_size, block_tables,
       max_blocks_per_seq, context_lens, window, num_sinks, scale, out,
-      static_cast<int32_t*>(order), kmap, vmap, st));
+      reinterpret_cast<int32_t*>(wsb), bf16 ? reinterpret_cast<uint2*>(wsb + order_bytes) : nullptr,
+      bf16 ? reinterpret_cast<uint32_t*>(wsb + order_bytes + parts_bytes) : nullptr, kmap, vmap,
+      st));
 }
 
 int pkv_append_fp8(const void* k, const void* v, int32_t in_dtype, const int64_t* slot_mapping,

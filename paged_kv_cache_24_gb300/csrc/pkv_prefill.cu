@@ -30,6 +30,16 @@ struct PlanArgs {
   int chunks_per_seq, tok_per_cta, window, num_sinks;
 };
 
+// bf16 caches: blocks that record the range of V magnitudes of each
+// (sequence, kv head) over its context, one partial per block of scan_rows
+// context rows: vparts[pair * row_blocks + rb] = (largest magnitude, smallest
+// non-zero magnitude minus one), as bf16 bits ((0, 0xffffffff) for no rows).
+struct ScanArgs {
+  uint2* vparts;  // nullptr: no scan (fp16 caches)
+  const uint4* v_cache;
+  int row_blocks, scan_rows;
+};
+
 // Work items (sequence b, token chunk c), item id b * chunks_per_seq + c, in
 // descending order of their key tiles: a counting sort over the work sizes in
 // one block (histogram, exclusive scan, scatter).  Items of equal size come
@@ -98,18 +108,108 @@ __device__ void plan_items(const int32_t* __restrict__ cu_q,
     pa.order[atomicAdd(&bins[bin_of(i)], 1)] = static_cast<int32_t>(i);
 }
 
+__device__ __forceinline__ uint32_t max_u16x2(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("max.u16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
+}
+__device__ __forceinline__ uint32_t min_u16x2(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("min.u16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
+}
+__device__ __forceinline__ uint32_t add_u16x2(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("add.u16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
+}
+
+// One scan block: rows rb * scan_rows .. of sequence b, kv head h.  Rows of
+// the cached prefix come from the pool, the chunk's rows from the input v
+// (the append blocks write them to the pool at the same time).  Each thread
+// takes one 16-byte column chunk of several rows, reading the rows' block-table
+// entries first and then all their values, so both reads overlap.
+__device__ void scan_v_range(const uint4* __restrict__ v, const int32_t* __restrict__ cu_q,
+                             const int32_t* __restrict__ context_lens,
+                             const int32_t* __restrict__ block_tables, int max_blocks,
+                             int block_size, int64_t num_blocks, int num_kv_heads,
+                             int chunks_per_row, int b, int h, int rb, const ScanArgs& sa) {
+  constexpr int kRowsPerThread = 8;
+  __shared__ uint32_t red[2][kAppendThreads / 32];
+  const int tid = threadIdx.x;
+  const int start = cu_q[b], n = cu_q[b + 1] - start;
+  const int L = context_lens[b];
+  const bool ok = L >= n && static_cast<int64_t>(L) <= static_cast<int64_t>(max_blocks) * block_size;
+  const int r_begin = rb * sa.scan_rows, r_end = ok ? min(L, r_begin + sa.scan_rows) : 0;
+  const int rows_per_pass = kAppendThreads / chunks_per_row;
+  const int c = tid % chunks_per_row;
+  uint32_t mx = 0u, mn = 0xffffffffu;  // per bf16 half: max magnitude, min (magnitude - 1)
+  for (int r0 = r_begin + tid / chunks_per_row; r0 < r_end; r0 += kRowsPerThread * rows_per_pass) {
+    int64_t src[kRowsPerThread];
+#pragma unroll
+    for (int e = 0; e < kRowsPerThread; ++e) {
+      const int r = r0 + e * rows_per_pass;
+      src[e] = -1;
+      if (r >= r_end) continue;
+      if (r >= L - n) {
+        src[e] = -2 - ((static_cast<int64_t>(start) + r - (L - n)) * num_kv_heads + h);
+      } else {
+        const int32_t blk = block_tables[static_cast<int64_t>(b) * max_blocks + r / block_size];
+        if (blk >= 0 && blk < num_blocks)
+          src[e] = (static_cast<int64_t>(blk) * num_kv_heads + h) * block_size + r % block_size;
+      }
+    }
+    uint4 x[kRowsPerThread];
+#pragma unroll
+    for (int e = 0; e < kRowsPerThread; ++e) {
+      x[e] = make_uint4(0u, 0u, 0u, 0u);
+      if (src[e] >= 0)
+        x[e] = sa.v_cache[src[e] * chunks_per_row + c];
+      else if (src[e] <= -2)
+        x[e] = __ldg(v + (-2 - src[e]) * chunks_per_row + c);
+    }
+#pragma unroll
+    for (int e = 0; e < kRowsPerThread; ++e) {
+      if (src[e] == -1) continue;
+      const uint32_t w[4] = {x[e].x, x[e].y, x[e].z, x[e].w};
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const uint32_t a = w[q] & 0x7fff7fffu;
+        mx = max_u16x2(mx, a);
+        mn = min_u16x2(mn, add_u16x2(a, 0xffffffffu));  // a zero wraps to 0xffff
+      }
+    }
+  }
+  uint32_t m1 = max(mx & 0xffffu, mx >> 16), m2 = min(mn & 0xffffu, mn >> 16);
+  m1 = __reduce_max_sync(0xffffffffu, m1);
+  m2 = __reduce_min_sync(0xffffffffu, m2);
+  if ((tid & 31) == 0) {
+    red[0][tid >> 5] = m1;
+    red[1][tid >> 5] = m2;
+  }
+  __syncthreads();
+  if (tid == 0) {
+    for (int w = 1; w < kAppendThreads / 32; ++w) {
+      m1 = max(m1, red[0][w]);
+      m2 = min(m2, red[1][w]);
+    }
+    if (m1 == 0u) m2 = 0xffffffffu;  // nothing non-zero
+    sa.vparts[(static_cast<int64_t>(b) * num_kv_heads + h) * sa.row_blocks + rb] = make_uint2(m1, m2);
+  }
+}
+
 // The chunk's K/V rows to their slots: token i of sequence b sits at position
 // L_b - n_b + i.  One thread per kAppendVec 16-byte chunks of a (token, kv
 // head) row, so that each thread keeps several loads in flight behind its
 // block-table read.  Block (0, num_seqs) orders the attention's work items
-// instead.
+// instead; blocks (append_blocks + h * row_blocks + rb, b) scan V ranges.
 __global__ void __launch_bounds__(kAppendThreads)
 chunk_append_kernel(const uint4* __restrict__ k, const uint4* __restrict__ v,
                     const int32_t* __restrict__ cu_q, const int32_t* __restrict__ context_lens,
                     const int32_t* __restrict__ block_tables, int max_blocks, int block_size,
                     int64_t num_blocks, int num_kv_heads, int chunks_per_row,
                     uint4* __restrict__ k_cache, uint4* __restrict__ v_cache, int num_seqs,
-                    const PlanArgs pa) {
+                    int append_blocks, const PlanArgs pa, const ScanArgs sa) {
   pdl_launch_dependents();
   pdl_wait_prior();
   if (static_cast<int>(blockIdx.y) == num_seqs) {
@@ -118,6 +218,12 @@ chunk_append_kernel(const uint4* __restrict__ k, const uint4* __restrict__ v,
     return;
   }
   const int b = blockIdx.y;
+  if (static_cast<int>(blockIdx.x) >= append_blocks) {
+    const int s = static_cast<int>(blockIdx.x) - append_blocks;
+    scan_v_range(v, cu_q, context_lens, block_tables, max_blocks, block_size, num_blocks,
+                 num_kv_heads, chunks_per_row, b, s / sa.row_blocks, s % sa.row_blocks, sa);
+    return;
+  }
   const int start = cu_q[b];
   const int n = cu_q[b + 1] - start;
   const int vecs_per_row = chunks_per_row / kAppendVec;
@@ -155,10 +261,10 @@ cudaError_t launch_prefill(int dtype, int head_dim, const void* q, const void* k
                            void* k_cache, void* v_cache, int64_t num_blocks, int num_kv_heads,
                            int block_size, const int32_t* block_tables, int max_blocks,
                            const int32_t* context_lens, int window, int num_sinks, float scale,
-                           void* out, int32_t* order, const CUtensorMap& kmap,
-                           const CUtensorMap& vmap, cudaStream_t stream) {
+                           void* out, int32_t* order, uint2* vparts, uint32_t* mode,
+                           const CUtensorMap& kmap, const CUtensorMap& vmap, cudaStream_t stream) {
   if (num_seqs == 0 || max_chunk == 0) return cudaSuccess;
-  // 1) the chunk's rows to their slots; the work items' order
+  // 1) the chunk's rows to their slots; the work items' order; (bf16) the V ranges
   const int cpr = head_dim * 2 / 16;
   const int64_t per_seq = static_cast<int64_t>(max_chunk) * num_kv_heads * (cpr / kAppendVec);
   PlanArgs pa;
@@ -167,19 +273,30 @@ cudaError_t launch_prefill(int dtype, int head_dim, const void* q, const void* k
   pa.chunks_per_seq = (max_chunk + pa.tok_per_cta - 1) / pa.tok_per_cta;
   pa.window = window;
   pa.num_sinks = num_sinks;
-  dim3 agrid(static_cast<unsigned>((per_seq + kAppendThreads - 1) / kAppendThreads),
-             num_seqs + 1);
+  ScanArgs sa{};
+  const PrefillScan plan = prefill_scan_plan(max_blocks, block_size);
+  if (dtype == 2) {
+    sa.vparts = vparts;
+    sa.v_cache = static_cast<const uint4*>(v_cache);
+    sa.row_blocks = plan.row_blocks;
+    sa.scan_rows = plan.scan_rows;
+  }
+  const int64_t append_blocks = (per_seq + kAppendThreads - 1) / kAppendThreads;
+  const int64_t gx = append_blocks + (sa.vparts ? static_cast<int64_t>(num_kv_heads) * sa.row_blocks : 0);
+  if (gx > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+  dim3 agrid(static_cast<unsigned>(gx), num_seqs + 1);
   cudaError_t e = launch_pdl(chunk_append_kernel, agrid, dim3(kAppendThreads), 0, stream,
                              static_cast<const uint4*>(k), static_cast<const uint4*>(v), cu_q,
                              context_lens, block_tables, max_blocks, block_size, num_blocks,
                              num_kv_heads, cpr, static_cast<uint4*>(k_cache),
-                             static_cast<uint4*>(v_cache), num_seqs, pa);
+                             static_cast<uint4*>(v_cache), num_seqs,
+                             static_cast<int>(append_blocks), pa, sa);
   if (e != cudaSuccess) return e;
   // 2) attention over prefix + chunk on the tensor cores, items in that order
   return launch_prefill_tc(dtype, head_dim, q, cu_q, num_seqs, num_q_heads, max_chunk,
                            num_blocks, num_kv_heads, block_size, block_tables, max_blocks,
-                           context_lens, window, num_sinks, scale, out, order, kmap, vmap,
-                           stream);
+                           context_lens, window, num_sinks, scale, out, order, vparts,
+                           plan.row_blocks, mode, kmap, vmap, stream);
 }
 
 }  // namespace pkv

@@ -74,13 +74,42 @@ __device__ __forceinline__ PrefillItem prefill_item(const int32_t* cu_q, const i
 // sequence entries, device memory), and the attention CTAs take the items in
 // that order: the hardware starts CTAs in index order, so the long items
 // start first and the short ones fill the end (longest-processing-time-first).
+// bf16 caches: the V range scan.  Each (sequence, kv head) gets row_blocks
+// partial ranges of scan_rows context rows each (a multiple of 128 rows,
+// so that row_blocks stays at most 1024).
+struct PrefillScan {
+  int scan_rows, row_blocks;
+};
+inline PrefillScan prefill_scan_plan(int max_blocks, int block_size) {
+  const int64_t rows = static_cast<int64_t>(max_blocks) * block_size;
+  int64_t sr = 128;
+  while ((rows + sr - 1) / sr > 1024) sr += 128;
+  const int64_t rb = (rows + sr - 1) / sr;
+  return PrefillScan{static_cast<int>(sr), static_cast<int>(rb > 0 ? rb : 1)};
+}
+
+// bf16 caches: `vparts` (num_seqs * num_kv_heads * row_blocks (max, min)
+// pairs, device memory) receives, from the append launch, the range of each
+// (sequence, kv head)'s V magnitudes over its context, from which the
+// attention scales V into fp16 exactly, or leaves the pair to its exact bf16
+// launch; `mode` (one word per attention CTA) carries that choice from the
+// attention's first launch to its second.
 cudaError_t launch_prefill(int dtype, int head_dim, const void* q, const void* k, const void* v,
                            const int32_t* cu_q, int num_seqs, int num_q_heads, int max_chunk,
                            void* k_cache, void* v_cache, int64_t num_blocks, int num_kv_heads,
                            int block_size, const int32_t* block_tables, int max_blocks,
                            const int32_t* context_lens, int window, int num_sinks, float scale,
-                           void* out, int32_t* order, const CUtensorMap& kmap,
-                           const CUtensorMap& vmap, cudaStream_t stream);
+                           void* out, int32_t* order, uint2* vparts, uint32_t* mode,
+                           const CUtensorMap& kmap, const CUtensorMap& vmap, cudaStream_t stream);
+
+// CTAs of the attention launch: one per (work item, kv head, head chunk).
+inline int64_t prefill_ctas(int num_seqs, int num_q_heads, int num_kv_heads, int max_chunk) {
+  const int group = num_q_heads / num_kv_heads;
+  const int lg = prefill_heads_log2(group);
+  const int tok_per_cta = kPrefillRowsCta >> lg;
+  const int64_t chunks = (max_chunk + tok_per_cta - 1) / tok_per_cta;
+  return static_cast<int64_t>(num_seqs) * chunks * num_kv_heads * (group >> lg);
+}
 
 // Attention half of the chunked prefill on the tcgen05 tensor cores (the
 // chunk's rows must already be in the pools).
@@ -89,6 +118,7 @@ cudaError_t launch_prefill_tc(int dtype, int head_dim, const void* q, const int3
                               int num_kv_heads, int block_size, const int32_t* block_tables,
                               int max_blocks, const int32_t* context_lens, int window,
                               int num_sinks, float scale, void* out, const int32_t* order,
+                              const uint2* vparts, int row_blocks, uint32_t* mode,
                               const CUtensorMap& kmap, const CUtensorMap& vmap,
                               cudaStream_t stream);
 

@@ -16,20 +16,28 @@
 //   warp 9       (load)    TMA of the 16-key K and V units of each key tile
 //                          into two rings of stages (128-byte swizzle), lane
 //                          i issuing unit i's copies;
-//   warps 10-11  (V prep)  zero the rows of keys no row of the CTA may see in
-//                          each landed V tile, so garbage (even NaN) in unused
-//                          slots cannot leak through a zero weight;
+//   warps 10-11  (V prep)  turn each landed V tile into fp16 in place (bf16
+//                          caches) and zero the rows of keys no row of the CTA
+//                          may see, so garbage (even NaN) in unused slots
+//                          cannot leak through a zero weight;
 //   warp 8       (MMA)     one thread waits and issues S_t = Q_t K^T (M 128, N 128, both
 //                          operands K-major in shared memory) and
 //                          O_t += P_t V (A = P_t read from TMEM, B = V read
 //                          MN-major from its stage);
 //   warps 0-3 / 4-7        tile 0 / tile 1 softmax: each thread owns one row
 //                          (its TMEM lane), loads its 128 scores, masks, keeps
-//                          the running maximum and sum, writes P over the
-//                          scores it came from (fp16 caches: one fp16 P; bf16
-//                          caches: P = hi + lo, two bf16 parts), and, when the maximum
+//                          the running maximum and sum, writes P as fp16 over
+//                          the scores it came from, and, when the maximum
 //                          moved by more than 2^8, rescales its O row in TMEM
 //                          (lazy rescaling).
+// bf16 caches: the P.V product runs in fp16 on V scaled by a power of two
+// 2^k chosen per (sequence, kv head) from the range of its V values (found by
+// the append launch before this one), so that every scaled value is exactly
+// an fp16 value; the output is scaled back by 2^-k.  A (sequence, kv head)
+// whose values span more than fp16 can hold exactly, or that holds an
+// infinity or NaN, is left to a second launch of this kernel (kExact): V
+// stays bf16 and P comes as a hi + lo pair of bf16 parts (two P.V
+// products), exact over bf16's whole range.
 // While one tile's rows are in the softmax, the tensor cores work on the
 // other tile's products.  The softmax warpgroups take registers from the
 // others (setmaxnreg).
@@ -70,6 +78,12 @@ struct TcParams {
   int num_sinks;  // attention sinks (0 without a window)
   int max_blocks, block_size, window;
   float scale_log2;
+  // bf16 caches: per (sequence, kv head), row_blocks partial ranges of its V
+  // magnitudes (largest, smallest non-zero minus one; bf16 bits), and per
+  // CTA the first launch's choice for the second (0: done, else 1 + down_c)
+  const uint2* vparts;
+  int row_blocks;
+  uint32_t* mode;
 };
 
 template <int D>
@@ -97,11 +111,55 @@ __device__ __forceinline__ uint32_t sw128(int row, int chunk) {
   return static_cast<uint32_t>(row * 128 + (((chunk & 7) ^ (row & 7)) << 4));
 }
 
+// two bf16 (low half first) times a power of two -> two fp16, rounded to
+// nearest: exact when the scaled values are fp16 values (see VRange)
+__device__ __forceinline__ uint32_t bf16x2_to_f16x2(uint32_t w, float2 up) {
+  const float2 x = __fmul2_rn(make_float2(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u)),
+                              up);
+  return Mma<__half>::pack(x.x, x.y);
+}
+
+// What the V range of a (sequence, kv head) allows.  mx: the largest
+// magnitude of its bf16 V values (as bits), mn1: the smallest non-zero one
+// minus one (as bits).
+//   up:     2^k, k in [-126, 126], putting the largest magnitude in [2^14, 2^15);
+//   exact:  some value would not be exactly an fp16 value after the scaling
+//           (below 2^-17 its last significant bit falls under fp16's
+//           subnormal step 2^-24), or the range holds an infinity or NaN:
+//           the kExact launch takes the pair;
+//   down_c: kExact only, weights scaled by 2^-down_c so that P.V sums of
+//           values near bf16's top stay inside fp32's range.
+struct VRange {
+  float up, down;
+  int down_c;
+  bool exact;
+};
+__device__ __forceinline__ VRange v_range_decision(uint32_t mx, uint32_t mn1) {
+  VRange r{1.f, 1.f, 0, false};
+  if (mx == 0u) return r;  // all zero
+  if (mx >= 0x7f80u) {     // an infinity or NaN
+    r.exact = true;
+    return r;
+  }
+  const int e = static_cast<int>(mx >> 7);  // biased exponent of the largest value
+  const int k = max(-126, min(126, 141 - max(e, 1)));
+  r.up = __int_as_float((127 + k) << 23);
+  r.down = __int_as_float((127 - k) << 23);
+  const float hi = __uint_as_float(mx << 16) * r.up;
+  const float lo = __uint_as_float((mn1 + 1u) << 16) * r.up;
+  if (!(hi <= 65280.f && lo >= 0x1p-17f)) {
+    // V stays as it is in the kExact launch
+    r.exact = true;
+    r.up = r.down = 1.f;
+    r.down_c = max(0, e - 227);  // 2^100 and above
+  }
+  return r;
+}
+
 // Two probabilities as a hi + lo pair of bf16 values (low half first in each
 // word): hi = p rounded to bf16, lo = the remainder p - hi (exact in fp32)
-// rounded to bf16, so hi + lo carries p to about 2^-17 of itself.  A bf16
-// cache keeps V in bf16 (the tensor cores take P and V in one type), and the
-// P.V product runs twice, once per part.
+// rounded to bf16, so hi + lo carries p to about 2^-17 of itself over bf16's
+// range (a single bf16 P would lose up to 2^-9 of each weight).
 __device__ __forceinline__ void split_bf16x2(float2 pr, uint32_t& hi, uint32_t& lo) {
   hi = Mma<__nv_bfloat16>::pack(pr.x, pr.y);
   const float2 hf = make_float2(__uint_as_float(hi << 16), __uint_as_float(hi & 0xffff0000u));
@@ -110,17 +168,22 @@ __device__ __forceinline__ void split_bf16x2(float2 pr, uint32_t& hi, uint32_t& 
 }
 
 // kSinks: the key range has a sink section (window > 0, num_sinks > 0); the
-// instantiation without it compiles the sink tests away.
-template <typename T, int D, bool kSinks>
+// instantiation without it compiles the sink tests away.  kExact (bf16
+// caches): the second launch -- only the CTAs of (sequence, kv head) pairs
+// whose V range fp16 cannot hold run, with V in bf16 and P as hi + lo bf16
+// parts.
+template <typename T, int D, bool kSinks, bool kExact>
 __global__ void __launch_bounds__(kTThreads, 1)
 prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
                   const TcParams p) {
   using Lay = TcLayout<D>;
   constexpr int SK = Lay::kKStages, SV = Lay::kVStages;
   constexpr bool kBf16 = __is_same(T, __nv_bfloat16);
+  static_assert(!kExact || kBf16, "the kExact launch is for bf16 caches");
+  constexpr bool kConvert = kBf16 && !kExact;  // V to fp16 (scaled) in shared memory
   constexpr uint32_t kIdS = umma_idesc_f16(kBf16 ? 1u : 0u, kQT, kTKeys, 0);
-  // P.V: P and V in the cache's type (bf16: P as hi + lo, two products)
-  constexpr uint32_t kIdO = umma_idesc_f16(kBf16 ? 1u : 0u, kQT, D, 1);
+  // P.V: P and V in fp16, or (kExact) both in bf16
+  constexpr uint32_t kIdO = umma_idesc_f16(kExact ? 1u : 0u, kQT, D, 1);
 
   extern __shared__ uint8_t smem_raw[];
   __shared__ __align__(8) uint64_t k_full[SK], k_empty[SK], v_full[SV], v_ready[SV], v_empty[SV];
@@ -131,6 +194,12 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   pdl_launch_dependents();
   pdl_wait_prior();
+  VRange vr{1.f, 1.f, 0, false};
+  if constexpr (kExact) {
+    const uint32_t m = p.mode[blockIdx.x];  // the first launch's choice
+    if (m == 0u) return;
+    vr = VRange{1.f, 1.f, static_cast<int>(m) - 1, true};
+  }
 
   const int hh_count = p.num_kv_heads * p.num_head_chunks;
   const int slot = static_cast<int>(blockIdx.x / hh_count);
@@ -144,7 +213,25 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
   const PrefillItem it = prefill_item(p.cu_q, p.context_lens, b, item - b * p.chunks_per_seq,
                                       tok_per_cta, p.window, p.num_sinks, p.max_blocks,
                                       p.block_size);
-  if (it.empty) return;
+  if (it.empty) {
+    if (kConvert && tid == 0) p.mode[blockIdx.x] = 0u;
+    return;
+  }
+  if constexpr (kConvert) {
+    // bf16 caches: this launch takes the pairs whose V range scales into fp16
+    // exactly and leaves the others to the kExact launch (each warp reduces
+    // the pair's partial ranges itself)
+    uint32_t mx = 0u, mn = 0xffffffffu;
+    const uint2* part = p.vparts + (static_cast<int64_t>(b) * p.num_kv_heads + hkv) * p.row_blocks;
+    for (int i = lane; i < p.row_blocks; i += 32) {
+      const uint2 r = __ldg(part + i);
+      mx = max(mx, r.x);
+      mn = min(mn, r.y);
+    }
+    vr = v_range_decision(__reduce_max_sync(0xffffffffu, mx), __reduce_min_sync(0xffffffffu, mn));
+    if (tid == 0) p.mode[blockIdx.x] = vr.exact ? 1u + static_cast<uint32_t>(vr.down_c) : 0u;
+    if (vr.exact) return;
+  }
   const int start = it.start, tile0 = it.tile0, tile_n = it.tile_n;
   const int pos0 = it.pos0, pos1 = it.pos1, k_lo = it.k_lo;
   const int n_units = it.n_units, n_tiles = it.n_tiles;
@@ -308,15 +395,42 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
           if (!mbar_wait_bounded(smem_u32(&v_full[t % SV]), (t / SV) & 1, kWaitLimit)) bad = true;
       }
     } else if (warp >= kPrepWarp0) {
-      // ============ V prep: rows of keys no row of the CTA sees zeroed ============
+      // ============ V prep: fp16 in place (bf16 caches, scaled), unseen keys zeroed ============
       const int ct = tid - kPrepWarp0 * 32;
+      const float2 up2 = make_float2(vr.up, vr.up);
       for (int j = 0; j < n_tiles; ++j) {
         if (!mbar_wait_bounded(smem_u32(&v_full[j % SV]), (j / SV) & 1, kWaitLimit)) bad = true;
         const int t0 = tile_t0(j);
         const uint32_t vt = v_addr(j);
         // a window tile wholly inside [k_lo, pos1] keeps every key
         const bool whole = j >= sink_tiles && t0 >= k_lo && t0 + kTKeys - 1 <= pos1;
-        if (!whole) {
+        if (kConvert && whole) {
+#pragma unroll 4
+          for (int u = ct; u < Lay::kKVTile / 16; u += kPrepThreads) {  // 16-byte chunks
+            uint4 x = ld_shared_v4(vt + u * 16);
+            x.x = bf16x2_to_f16x2(x.x, up2);
+            x.y = bf16x2_to_f16x2(x.y, up2);
+            x.z = bf16x2_to_f16x2(x.z, up2);
+            x.w = bf16x2_to_f16x2(x.w, up2);
+            st_shared_v4(vt + u * 16, x);
+          }
+        } else if (kConvert) {
+#pragma unroll 4
+          for (int u = ct; u < Lay::kKVTile / 16; u += kPrepThreads) {
+            // chunk u: unit u / (kVUnitBytes / 16), row (u / 8) % 16 of it
+            const int kp = t0 + (u / (Lay::kVUnitBytes / 16)) * kUnitTokens + ((u >> 3) & 15);
+            uint4 x = ld_shared_v4(vt + u * 16);
+            if (kSinks ? !key_kept(j, kp) : (kp < k_lo || kp > pos1)) {
+              x = make_uint4(0u, 0u, 0u, 0u);
+            } else {
+              x.x = bf16x2_to_f16x2(x.x, up2);
+              x.y = bf16x2_to_f16x2(x.y, up2);
+              x.z = bf16x2_to_f16x2(x.z, up2);
+              x.w = bf16x2_to_f16x2(x.w, up2);
+            }
+            st_shared_v4(vt + u * 16, x);
+          }
+        } else if (!whole) {
           for (int r = ct; r < kTKeys; r += kPrepThreads) {
             const int kp = t0 + r;
             if (kSinks ? key_kept(j, kp) : (kp >= k_lo && kp <= pos1)) continue;
@@ -379,8 +493,8 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
               const uint64_t vb = v0 + static_cast<uint64_t>((kk * Lay::kVUnitBytes) >> 4);
               umma_f16_ts(tmem + Lay::o_col(t), tmem + Lay::s_col(t) + kk * 8, vb, kIdO,
                           (j > 0 || kk > 0) ? 1u : 0u);
-              // bf16: the lo parts of P, kTKeys / 2 columns after the hi parts
-              if constexpr (kBf16)
+              // kExact: the lo parts of P, kTKeys / 2 columns after the hi parts
+              if constexpr (kExact)
                 umma_f16_ts(tmem + Lay::o_col(t), tmem + Lay::s_col(t) + kTKeys / 2 + kk * 8, vb,
                             kIdO, 1u);
             }
@@ -467,7 +581,9 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
     if (mx > m_old + kTRescale) m_run = mx;
     const bool rescale = m_run != m_old && m_old != -INFINITY;
     const float alpha = rescale ? ex2(m_old - m_run) : 1.f;
-    const float neg_m = m_run == -INFINITY ? 0.f : -m_run;  // nothing visible yet: p = 0
+    // (nothing visible yet: p = 0; kExact: weights times 2^-down_c, which the
+    // normalisation by their sum cancels)
+    const float neg_m = (m_run == -INFINITY ? 0.f : -m_run) - static_cast<float>(vr.down_c);
 
     // S_t(j) completing means O_t += P_t(j-1) V completed too (issued before it)
     if (__any_sync(0xffffffffu, rescale)) {
@@ -480,12 +596,11 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
         tmem_st16(tO + c, v);
       }
     }
-    // P = 2^(s*sl - m) over the columns of S_t: fp16 in the first 64 (fp16
-    // caches), or bf16 hi parts in the first 64 and lo parts in the next 64
+    // P = 2^(s*sl - m) as fp16 over the first 64 columns of S_t (kExact: bf16
+    // hi parts there, lo parts over the next 64)
     float2 acc[4] = {{0.f, 0.f}, {0.f, 0.f}, {0.f, 0.f}, {0.f, 0.f}};
     const float2 sl2 = make_float2(sl, sl), nm2 = make_float2(neg_m, neg_m);
-    if constexpr (kBf16) {
-      // 16 keys at a time: the hi and lo words of 8 pairs, stored as they come
+    if constexpr (kExact) {
 #pragma unroll
       for (int h = 0; h < kTKeys / 16; ++h) {
         uint32_t w[8], wl[8];
@@ -537,7 +652,8 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
   tc_fence_after();
   const bool nan_out = s_bad != 0;
   T* dst = static_cast<T*>(p.out) + qo_row;
-  const float inv = nan_out ? __int_as_float(0x7fc00000) : 1.f / l_run;
+  // (bf16 caches: V was scaled by vr.up)
+  const float inv = nan_out ? __int_as_float(0x7fc00000) : vr.down / l_run;
 #pragma unroll
   for (int c = 0; c < D; c += 16) {
     float v[16];
@@ -562,11 +678,11 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
                  "r"(Lay::kTmemCols));
 }
 
-template <typename T, int D, bool kSinks>
-cudaError_t launch_t(const CUtensorMap& kmap, const CUtensorMap& vmap, const TcParams& p,
-                     int max_chunk, int num_seqs, cudaStream_t stream) {
+template <typename T, int D, bool kSinks, bool kExact>
+cudaError_t launch_one(const CUtensorMap& kmap, const CUtensorMap& vmap, const TcParams& p,
+                       int num_seqs, cudaStream_t stream) {
   using Lay = TcLayout<D>;
-  auto kern = prefill_tc_kernel<T, D, kSinks>;
+  auto kern = prefill_tc_kernel<T, D, kSinks, kExact>;
   const int smem = 1024 + Lay::kSmemBytes;
   // per device, once: the shared-memory opt-in, and a check that the block
   // is launched with the registers the warpgroups' split hands out (a larger
@@ -593,6 +709,18 @@ cudaError_t launch_t(const CUtensorMap& kmap, const CUtensorMap& vmap, const TcP
                     vmap, p);
 }
 
+// fp16 caches: one launch.  bf16 caches: the fast launch, then the kExact
+// launch, in which only the CTAs of pairs the fast one left do any work.
+template <typename T, int D, bool kSinks>
+cudaError_t launch_t(const CUtensorMap& kmap, const CUtensorMap& vmap, const TcParams& p,
+                     int num_seqs, cudaStream_t stream) {
+  cudaError_t e = launch_one<T, D, kSinks, false>(kmap, vmap, p, num_seqs, stream);
+  if constexpr (__is_same(T, __nv_bfloat16)) {
+    if (e == cudaSuccess) e = launch_one<T, D, kSinks, true>(kmap, vmap, p, num_seqs, stream);
+  }
+  return e;
+}
+
 }  // namespace
 
 cudaError_t launch_prefill_tc(int dtype, int head_dim, const void* q, const int32_t* cu_q,
@@ -600,9 +728,13 @@ cudaError_t launch_prefill_tc(int dtype, int head_dim, const void* q, const int3
                               int num_kv_heads, int block_size, const int32_t* block_tables,
                               int max_blocks, const int32_t* context_lens, int window,
                               int num_sinks, float scale, void* out, const int32_t* order,
+                              const uint2* vparts, int row_blocks, uint32_t* mode,
                               const CUtensorMap& kmap, const CUtensorMap& vmap,
                               cudaStream_t stream) {
   TcParams p{};
+  p.vparts = vparts;
+  p.row_blocks = row_blocks;
+  p.mode = mode;
   p.q = q;
   p.out = out;
   p.cu_q = cu_q;
@@ -625,16 +757,16 @@ cudaError_t launch_prefill_tc(int dtype, int head_dim, const void* q, const int3
   p.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
   if (dtype == 1) {
     if (head_dim == 128)
-      return sinks ? launch_t<__half, 128, true>(kmap, vmap, p, max_chunk, num_seqs, stream)
-                   : launch_t<__half, 128, false>(kmap, vmap, p, max_chunk, num_seqs, stream);
-    return sinks ? launch_t<__half, 64, true>(kmap, vmap, p, max_chunk, num_seqs, stream)
-                 : launch_t<__half, 64, false>(kmap, vmap, p, max_chunk, num_seqs, stream);
+      return sinks ? launch_t<__half, 128, true>(kmap, vmap, p, num_seqs, stream)
+                   : launch_t<__half, 128, false>(kmap, vmap, p, num_seqs, stream);
+    return sinks ? launch_t<__half, 64, true>(kmap, vmap, p, num_seqs, stream)
+                 : launch_t<__half, 64, false>(kmap, vmap, p, num_seqs, stream);
   }
   if (head_dim == 128)
-    return sinks ? launch_t<__nv_bfloat16, 128, true>(kmap, vmap, p, max_chunk, num_seqs, stream)
-                 : launch_t<__nv_bfloat16, 128, false>(kmap, vmap, p, max_chunk, num_seqs, stream);
-  return sinks ? launch_t<__nv_bfloat16, 64, true>(kmap, vmap, p, max_chunk, num_seqs, stream)
-               : launch_t<__nv_bfloat16, 64, false>(kmap, vmap, p, max_chunk, num_seqs, stream);
+    return sinks ? launch_t<__nv_bfloat16, 128, true>(kmap, vmap, p, num_seqs, stream)
+                 : launch_t<__nv_bfloat16, 128, false>(kmap, vmap, p, num_seqs, stream);
+  return sinks ? launch_t<__nv_bfloat16, 64, true>(kmap, vmap, p, num_seqs, stream)
+               : launch_t<__nv_bfloat16, 64, false>(kmap, vmap, p, num_seqs, stream);
 }
 
 }  // namespace pkv

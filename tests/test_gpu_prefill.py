@@ -219,14 +219,20 @@ def test_prefill_nonpositive_scale(pkv_lib, oracle_lib, scale):
     assert (err <= 2e-3 + 0.5 * torch.finfo(torch.bfloat16).eps * np.abs(ref)).all(), err.max()
 
 
+@pytest.mark.parametrize("mode", ["dense", "sparse", "one_pair"])
 @pytest.mark.parametrize("window,sinks", [(0, 0), (90, 5)])
-def test_prefill_bf16_extreme_values_match_oracle(pkv_lib, oracle_lib, window, sinks):
+def test_prefill_bf16_extreme_values_match_oracle(pkv_lib, oracle_lib, window, sinks, mode):
     """bf16 caches are exact over bf16's whole range: V values far beyond the
     fp16 range (7e4, 1e6, 1e30) and far below fp16's normal range (3e-6,
     1e-30), in cached prefix keys and in the chunk's own keys, give the
-    oracle's output -- within the usual tolerance, and within a relative
-    2^-7 on the columns that hold them (all of one sign, so no cancellation
-    hides an error)."""
+    oracle's output within the usual tolerance.
+    dense: every key holds them (every key tile takes the bf16 product), and
+    the columns that hold them (all of one sign, so no cancellation hides an
+    error) are also within a relative 2^-7.
+    sparse: a few keys hold them.
+    one_pair: only kv head 1 of the second sequence holds them (in a few
+    keys), so one launch mixes pairs whose V scales into fp16 exactly with
+    pairs that need the bf16 product."""
     dtype = torch.bfloat16
     prefixes, chunks = [30, 300], [10, 200]
     w, q, k, v, cu, lens = _prefill_case(dtype, 8, 2, 128, 16, prefixes, chunks, window,
@@ -238,18 +244,24 @@ def test_prefill_bf16_extreme_values_match_oracle(pkv_lib, oracle_lib, window, s
 
     bt = w.block_tables.cpu().numpy()
     bs = w.spec.block_size
-    # (kv head, column) -> magnitude, written into every prefix key and every
-    # chunk key of both sequences
+    # (kv head, column) -> magnitude
     special = {(0, 3): 1.0e6, (0, 11): 1.0e-30, (1, 7): 1.0e30, (1, 12): 3.0e-6,
                (1, 40): 7.0e4}
+    if mode == "one_pair":
+        special = {(h, c): mag for (h, c), mag in special.items() if h == 1}
     for b, (p, n) in enumerate(zip(prefixes, chunks)):
-        s_pref = [oracle.slot_for_position(bt[b], bs, t) for t in range(p)]
+        if mode == "one_pair" and b != 1:
+            continue
+        ts = list(range(p)) if mode == "dense" else [t for t in (5, p - 1) if 0 <= t < p]
+        s_pref = [oracle.slot_for_position(bt[b], bs, t) for t in ts]
         if s_pref:
             s_arr = torch.tensor(s_pref, device="cuda")
             for (h, c), mag in special.items():
                 w.v_cache[s_arr // bs, h, s_arr % bs, c] = pos(len(s_pref), mag)
+    rows = (torch.arange(v.shape[0], device="cuda") if mode == "dense"
+            else torch.tensor([150] if mode == "one_pair" else [3, 150], device="cuda"))
     for (h, c), mag in special.items():
-        v[:, h, c] = pos(v.shape[0], mag)
+        v[rows, h, c] = pos(rows.numel(), mag)
     kc_h, vc_h = w.k_cache.cpu(), w.v_cache.cpu()
     lens_h = lens.cpu().numpy()
     slots = [oracle.slot_for_position(bt[b], bs, lens_h[b] - n + i)
@@ -266,9 +278,10 @@ def test_prefill_bf16_extreme_values_match_oracle(pkv_lib, oracle_lib, window, s
     err = np.abs(got - ref)
     tol = 2e-3 + 0.5 * torch.finfo(dtype).eps * np.abs(ref)
     assert (err <= tol).all(), f"max err {err.max():.3e}"
-    G = 4  # query heads per kv head
-    for (h, c), mag in special.items():
-        r = ref[:, h * G:(h + 1) * G, c]
-        e = err[:, h * G:(h + 1) * G, c]
-        assert (r > 0).all()
-        assert (e <= 2.0 ** -7 * r).all(), (h, c, float((e / r).max()))
+    if mode == "dense":
+        G = 4  # query heads per kv head
+        for (h, c), mag in special.items():
+            r = ref[:, h * G:(h + 1) * G, c]
+            e = err[:, h * G:(h + 1) * G, c]
+            assert (r > 0).all()
+            assert (e <= 2.0 ** -7 * r).all(), (h, c, float((e / r).max()))
