@@ -351,10 +351,11 @@ def percentiles_ms(times_ms):
     return {f"p{q}": float(np.percentile(a, q)) for q in (10, 50, 90)}
 
 
-def run_prefill(args, pkv):
+def measure_prefill(pkv, workload, steps, warmup):
+    """Time `pkv_prefill` on a prefill workload; returns the JSON line's dict."""
     from paged_kv_cache_24_gb300.workloads import config_spec, make_workload
 
-    c = PREFILL[args.workload]
+    c = PREFILL[workload]
     rng = np.random.default_rng(c["seed"])
     B, chunk = c["num_seqs"], c["chunk"]
     prefix = rng.integers(c["prefix_lo"], c["prefix_hi"] + 1, B)
@@ -388,7 +389,7 @@ def run_prefill(args, pkv):
     gstream = torch.cuda.Stream()
     gstream.wait_stream(torch.cuda.current_stream())
     with torch.cuda.stream(gstream):
-        for _ in range(args.warmup):
+        for _ in range(warmup):
             step()
     gstream.synchronize()
     graph = torch.cuda.CUDAGraph()
@@ -396,9 +397,9 @@ def run_prefill(args, pkv):
         step()
     torch.cuda.synchronize()
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-          for _ in range(args.steps)]
+          for _ in range(steps)]
     with ClockSampler(0) as clocks, torch.cuda.stream(gstream):
-        for s in range(args.steps):
+        for s in range(steps):
             flush_buf.add_(1)
             clean_buf.amax()
             ev[s][0].record(gstream)
@@ -406,7 +407,7 @@ def run_prefill(args, pkv):
             ev[s][1].record(gstream)
         torch.cuda.synchronize()
     times = [a.elapsed_time(b) for a, b in ev]
-    ms = sum(times) / args.steps
+    ms = sum(times) / steps
     tflops = flops / (ms * 1e-3) / 1e12
     peak = None
     try:
@@ -415,12 +416,15 @@ def run_prefill(args, pkv):
         peak_kind = "measured"
     except Exception:
         peak, peak_kind = 1900.0, "fallback"
-    print(json.dumps({
+    # launches a step: the chunk append, the attention (bf16: and its exact
+    # second launch)
+    per_step = 3 if spec.dtype == torch.bfloat16 else 2
+    return {
         "metric": "paged chunked prefill: attention TFLOP/s", "value": tflops,
-        "unit": "TFLOP/s", "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
+        "unit": "TFLOP/s", "n_gpus": 1, "steps": steps, "warmup": warmup,
         "ms_per_step": ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": DTYPE_NAME[spec.dtype], "data": "synthetic",
-        "config": {"workload": args.workload, "num_seqs": B, "chunk": chunk,
+        "config": {"workload": workload, "num_seqs": B, "chunk": chunk,
                    "mean_prefix": float(prefix.mean()), "num_q_heads": hq, "num_kv_heads": hkv,
                    "head_dim": d, "block_size": spec.block_size,
                    "l2": "flushed between steps (2x L2 written, then 2x L2 read)"},
@@ -429,8 +433,12 @@ def run_prefill(args, pkv):
         "roofline": {"bound": "tensor", "kernel": "prefill (chunk append + attention)",
                      "achieved": tflops, "peak": peak, "unit": "TFLOP/s", "frac": tflops / peak,
                      "peak_kind": peak_kind,
-                     "traffic": recorded_traffic(args.workload, "prefill")},
-        "gpu_launches": 2 * args.steps, "clocks": clocks.summary()}), flush=True)
+                     "traffic": recorded_traffic(workload, "prefill")},
+        "gpu_launches": per_step * steps, "clocks": clocks.summary()}
+
+
+def run_prefill(args, pkv):
+    print(json.dumps(measure_prefill(pkv, args.workload, args.steps, args.warmup)), flush=True)
     return 0
 
 
@@ -453,6 +461,9 @@ def main(argv=None):
                     help="--impl reference: host time of all warm-up and timed steps")
     ap.add_argument("--num-seqs", type=int, default=0,
                     help="profiling only: shrink the workload's batch (not a bench line)")
+    ap.add_argument("--no-extra-workloads", dest="extra_workloads", action="store_false",
+                    help="time only the chosen workload (by default the line also carries "
+                         "every other workload's value, roofline and clocks)")
     args = ap.parse_args(argv)
     args.warmup = max(args.warmup, 3)
 
@@ -460,8 +471,6 @@ def main(argv=None):
         return run_reference(args, args.workload)
 
     import paged_kv_cache_24_gb300 as pkv
-    from paged_kv_cache_24_gb300.workloads import CONFIGS, config_spec, make_workload
-
     rank, world, local_rank = dist_env()
     torch.cuda.set_device(local_rank)
     if args.workload in PREFILL:
@@ -474,12 +483,93 @@ def main(argv=None):
 
     over = {"num_seqs": args.num_seqs} if args.num_seqs > 0 else {}
     spec = rank_spec(args.workload, rank, args.num_seqs)
+    m = measure_decode(pkv, spec, args.steps, args.warmup, args.path, pg, world, local_rank,
+                       traffic_key=None if over else args.workload)
+    w, sbytes, S = m["w"], m["sbytes"], m["w"].steps
+    total_ms_all, bytes_all = m["total_ms"], m["bytes"]
+    ms_per_step = total_ms_all / args.steps
+    value = bytes_all / (total_ms_all * 1e-3) / 1e9
+    tokens_per_s = world * spec.num_seqs * args.steps / (total_ms_all * 1e-3)
+    peak, peak_kind = hbm_peak()
+
+    # ---- end to end through the public API, host buffers ----
+    e2e = None
+    if not args.no_e2e:
+        e2e = run_e2e(pkv, w, spec, args, sbytes, pg, world)
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        sampler = OracleSampler(w)
+        rate, dt, got = sampler.rate_for(10.0)
+        rate1, dt1, got1 = sampler.one_thread(got / dt)
+        cpu = {"value": rate / 1e9, "unit": "GB/s", "cores": sampler.threads, "kind": "oracle",
+               "sample": f"{got} random (sequence, query head) pairs of step 0; {dt:.1f} s of "
+                         f"float64 decode on the host cores; K/V bytes of the sample / time",
+               "cpu_model": host_cpu_model(),
+               "one_thread": {"value": rate1 / 1e9, "unit": "GB/s",
+                              "sample": f"{got1} pairs, {dt1:.1f} s on one thread"}}
+
+    line = None
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": ("e4m3+f16" if spec.kv_fp8 else "i8+f16" if spec.kv_int8
+                      else DTYPE_NAME[spec.dtype]), "data": "synthetic",
+            "config": {
+                "workload": args.workload + ("" if not over else "-reduced"),
+                "num_seqs": spec.num_seqs,
+                "num_q_heads": spec.num_q_heads, "num_kv_heads": spec.num_kv_heads,
+                "head_dim": spec.head_dim, "block_size": spec.block_size,
+                "window": spec.window, "steps_in_workload": S,
+                "mean_context": float(w.lens_steps.float().mean()),
+                "num_blocks": w.num_blocks,
+                "tokens_per_split": m["plan"][0], "num_splits": m["plan"][1],
+                "l2": m["l2"],
+                "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+            },
+            "tokens_per_s": tokens_per_s,
+            "step_ms_percentiles": percentiles_ms(m["step_ms"]),
+            # the same step counted on distinct pool rows (shared prefix blocks once)
+            # (every rank's workload has the same shape: rank 0's count x ranks)
+            "unique_rows": {"value": world * m["unique"] / (total_ms_all * 1e-3) / 1e9,
+                            "unit": "GB/s", "bytes_per_step": m["unique"] / args.steps,
+                            "pct_of_hbm_peak": 100.0 * m["unique"] / (total_ms_all * 1e-3) / 1e9
+                            / peak},
+            "pct_of_hbm_peak": 100.0 * value / (world * peak),
+            "path": m["path"],
+            "roofline": m["roofline"],
+            "gpu_launches": m["gpu_launches"],
+            "clocks": m["clocks"],
+            "e2e": e2e,
+            "cpu_baseline": cpu,
+        }
+    del m, w
+    torch.cuda.empty_cache()
+    if rank == 0 and world == 1 and args.extra_workloads and not over:
+        line["workloads"] = measure_other_workloads(pkv, args)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if pg:
+        pg.destroy_process_group()
+    return 0
+
+
+def measure_decode(pkv, spec, steps, warmup, path, pg=None, world=1, local_rank=0,
+                   traffic_key=None):
+    """Time `steps` decode steps (append + decode) of workload `spec`: CUDA
+    graphs of the C-ABI calls replayed on one stream, CUDA events around each
+    step and around the decode launch.  Returns the measured times, bytes and
+    the roofline record (its `traffic` from the committed record for
+    `traffic_key`); `w` is the workload (for the end-to-end and CPU legs)."""
+    from paged_kv_cache_24_gb300.workloads import make_workload
+
     w = make_workload(spec, device="cuda", poison=True)
     S = w.steps
     bs = spec.block_size
     sbytes = step_bytes(w)
 
-    stream = torch.cuda.current_stream()
     slots = [pkv.pkv_slot_mapping(w.block_tables, w.pos_steps[s].contiguous(), bs)
              for s in range(S)]
     lens = [w.lens_steps[s].contiguous() for s in range(S)]
@@ -488,7 +578,7 @@ def main(argv=None):
                                w.max_blocks, spec.window)
     # FP8 pools append through the quantising kernel (no fused form)
     q8 = spec.kv_fp8 or spec.kv_int8
-    fused = args.path == "fused" and not q8
+    fused = path == "fused" and not q8
     launches_per_step = (1 if fused else 2) + (1 if plan[1] > 1 else 0)
 
     def do_append(i):
@@ -530,7 +620,7 @@ def main(argv=None):
     gstream = torch.cuda.Stream()
     gstream.wait_stream(torch.cuda.current_stream())
     with torch.cuda.stream(gstream):
-        for s in range(args.warmup):
+        for s in range(warmup):
             step(s)
     gstream.synchronize()
     g_app, g_dec = [], []
@@ -547,9 +637,9 @@ def main(argv=None):
     torch.cuda.synchronize()
     stream = gstream
 
-    # ---- timed region: exactly K steps ----
+    # ---- timed region: exactly `steps` steps ----
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
-           torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+           torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
     if pg:
         pg.barrier()
     torch.cuda.synchronize()
@@ -557,7 +647,7 @@ def main(argv=None):
     t_end = torch.cuda.Event(enable_timing=True)
     with ClockSampler(local_rank) as clocks, torch.cuda.stream(gstream):
         t_start.record(stream)
-        for s in range(args.steps):
+        for s in range(steps):
             if need_flush:
                 flush_buf.add_(1)  # evict the previous step's working set from L2
                 clean_buf.amax()
@@ -572,90 +662,79 @@ def main(argv=None):
         torch.cuda.synchronize()
     if pg:
         pg.barrier()
-    step_ms = [ev[s][0].elapsed_time(ev[s][2]) for s in range(args.steps)]
-    dec_ms = [ev[s][1].elapsed_time(ev[s][2]) for s in range(args.steps)]
+    step_ms = [ev[s][0].elapsed_time(ev[s][2]) for s in range(steps)]
+    dec_ms = [ev[s][1].elapsed_time(ev[s][2]) for s in range(steps)]
     loop_ms = t_start.elapsed_time(t_end)
     # the step time: whole loop / K when nothing else ran in it, else the sum of steps
     total_ms = sum(step_ms) if need_flush else loop_ms
-    my_bytes = sum(sbytes[s % S]["step"] for s in range(args.steps))
-    my_unique = sum(sbytes[s % S]["step_unique"] for s in range(args.steps))
+    my_bytes = sum(sbytes[s % S]["step"] for s in range(steps))
+    my_unique = sum(sbytes[s % S]["step_unique"] for s in range(steps))
     dec_key = "step" if fused else "decode"  # the fused launch also does the append
-    my_dec_bytes = sum(sbytes[s % S][dec_key] for s in range(args.steps))
-
+    my_dec_bytes = sum(sbytes[s % S][dec_key] for s in range(steps))
     total_ms_all, bytes_all = reduce_over_ranks(pg, total_ms, my_bytes)
-    ms_per_step = total_ms_all / args.steps
-    value = bytes_all / (total_ms_all * 1e-3) / 1e9
-    tokens_per_s = world * spec.num_seqs * args.steps / (total_ms_all * 1e-3)
 
     peak, peak_kind = hbm_peak()
-    dec_avg_ms = sum(dec_ms) / args.steps
-    achieved = (my_dec_bytes / args.steps) / (dec_avg_ms * 1e-3) / 1e9
-    traffic = recorded_traffic(args.workload)
+    dec_avg_ms = sum(dec_ms) / steps
+    achieved = (my_dec_bytes / steps) / (dec_avg_ms * 1e-3) / 1e9
+    return {
+        "w": w, "sbytes": sbytes, "plan": plan, "total_ms": total_ms_all, "bytes": bytes_all,
+        "unique": my_unique, "step_ms": step_ms, "path": "fused" if fused else "separate",
+        "l2": ("flushed between steps (2x L2 written, then 2x L2 read)" if need_flush else
+               f"inputs larger than L2 ({kv_per_step / 1e9:.2f} GB of K/V per step)"),
+        "roofline": {"bound": "hbm",
+                     "kernel": ("fused append + decode (split-K) + LSE combine" if fused
+                                else "decode (split-K decode + LSE combine)"),
+                     "achieved": achieved, "peak": peak, "unit": "GB/s",
+                     "frac": achieved / peak, "peak_kind": peak_kind,
+                     "traffic": recorded_traffic(traffic_key) if traffic_key else None,
+                     "algorithmic_bytes_per_launch": my_dec_bytes / steps,
+                     "launch_ms": dec_avg_ms},
+        "gpu_launches": launches_per_step * steps,
+        "clocks": clocks.summary(),
+    }
 
-    # ---- end to end through the public API, host buffers ----
-    e2e = None
-    if not args.no_e2e:
-        e2e = run_e2e(pkv, w, spec, args, sbytes, pg, world)
 
-    cpu = None
-    if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        sampler = OracleSampler(w)
-        rate, dt, got = sampler.rate_for(10.0)
-        rate1, dt1, got1 = sampler.one_thread(got / dt)
-        cpu = {"value": rate / 1e9, "unit": "GB/s", "cores": sampler.threads, "kind": "oracle",
-               "sample": f"{got} random (sequence, query head) pairs of step 0; {dt:.1f} s of "
-                         f"float64 decode on the host cores; K/V bytes of the sample / time",
-               "cpu_model": host_cpu_model(),
-               "one_thread": {"value": rate1 / 1e9, "unit": "GB/s",
-                              "sample": f"{got1} pairs, {dt1:.1f} s on one thread"}}
+# the other workloads, timed after the headline in the same run
+OTHER_WORKLOADS = ["tiny_fp32", "mha_fp16", "sliding_bf16", "serving_fp16", "mha_fp8",
+                   "gqa_fp8", "mha_int8", "gqa_int8", "prefill_bf16", "prefill_fp16"]
 
-    if rank == 0:
-        line = {
-            "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world,
-            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
-            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-            "dtype": ("e4m3+f16" if spec.kv_fp8 else "i8+f16" if spec.kv_int8
-                      else DTYPE_NAME[spec.dtype]), "data": "synthetic",
-            "config": {
-                "workload": args.workload + ("" if not over else "-reduced"),
-                "num_seqs": spec.num_seqs,
-                "num_q_heads": spec.num_q_heads, "num_kv_heads": spec.num_kv_heads,
-                "head_dim": spec.head_dim, "block_size": spec.block_size,
-                "window": spec.window, "steps_in_workload": S,
-                "mean_context": float(w.lens_steps.float().mean()),
-                "num_blocks": w.num_blocks,
-                "tokens_per_split": plan[0], "num_splits": plan[1],
-                "l2": ("flushed between steps (2x L2 written, then 2x L2 read)" if need_flush else
-                       f"inputs larger than L2 ({kv_per_step / 1e9:.2f} GB of K/V per step)"),
-                "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
-            },
-            "tokens_per_s": tokens_per_s,
-            "step_ms_percentiles": percentiles_ms(step_ms),
-            # the same step counted on distinct pool rows (shared prefix blocks once)
-            # (every rank's workload has the same shape: rank 0's count x ranks)
-            "unique_rows": {"value": world * my_unique / (total_ms_all * 1e-3) / 1e9,
-                            "unit": "GB/s", "bytes_per_step": my_unique / args.steps,
-                            "pct_of_hbm_peak": 100.0 * my_unique / (total_ms_all * 1e-3) / 1e9
-                            / peak},
-            "pct_of_hbm_peak": 100.0 * value / (world * peak),
-            "path": "fused" if fused else "separate",
-            "roofline": {"bound": "hbm",
-                         "kernel": ("fused append + decode (split-K) + LSE combine" if fused
-                                    else "decode (split-K decode + LSE combine)"),
-                         "achieved": achieved, "peak": peak, "unit": "GB/s",
-                         "frac": achieved / peak, "peak_kind": peak_kind,
-                         "traffic": traffic,
-                         "algorithmic_bytes_per_launch": my_dec_bytes / args.steps,
-                         "launch_ms": dec_avg_ms},
-            "gpu_launches": launches_per_step * args.steps,
-            "clocks": clocks.summary(),
-            "e2e": e2e,
-            "cpu_baseline": cpu,
-        }
-        print(json.dumps(line), flush=True)
-    if pg:
-        pg.destroy_process_group()
-    return 0
+
+def measure_other_workloads(pkv, args):
+    """Each other workload's line (its value, roofline and clocks), timed in
+    this run after the headline: at most 200 steps (serving: its 32) after
+    `args.warmup` warm-up steps each."""
+    from paged_kv_cache_24_gb300.workloads import CONFIGS, config_spec
+
+    res = {}
+    for name in OTHER_WORKLOADS:
+        if name == args.workload:
+            continue
+        steps = min(args.steps, 200)
+        if name in PREFILL:
+            d = measure_prefill(pkv, name, min(args.steps, 20), args.warmup)
+            res[name] = {"metric": d["metric"], "value": d["value"], "unit": d["unit"],
+                         "steps": d["steps"], "ms_per_step": d["ms_per_step"],
+                         "dtype": d["dtype"], "roofline": d["roofline"], "clocks": d["clocks"],
+                         "config": d["config"]}
+        else:
+            spec = config_spec(CONFIGS[name])
+            if spec.steps > 1:
+                steps = max(steps, spec.steps)
+            m = measure_decode(pkv, spec, steps, args.warmup, args.path, traffic_key=name)
+            value = m["bytes"] / (m["total_ms"] * 1e-3) / 1e9
+            res[name] = {"metric": METRIC, "value": value, "unit": "GB/s", "steps": steps,
+                         "ms_per_step": m["total_ms"] / steps,
+                         "tokens_per_s": spec.num_seqs * steps / (m["total_ms"] * 1e-3),
+                         "dtype": ("e4m3+f16" if spec.kv_fp8 else "i8+f16" if spec.kv_int8
+                                   else DTYPE_NAME[spec.dtype]),
+                         "path": m["path"], "roofline": m["roofline"], "clocks": m["clocks"],
+                         "unique_rows_gbs": m["unique"] / (m["total_ms"] * 1e-3) / 1e9,
+                         "config": {"num_seqs": spec.num_seqs, "window": spec.window,
+                                    "tokens_per_split": m["plan"][0],
+                                    "num_splits": m["plan"][1], "l2": m["l2"]}}
+            del m
+        torch.cuda.empty_cache()
+    return res
 
 
 def run_e2e(pkv, w, spec, args, sbytes, pg, world):
