@@ -219,13 +219,16 @@ def test_prefill_nonpositive_scale(pkv_lib, oracle_lib, scale):
     assert (err <= 2e-3 + 0.5 * torch.finfo(torch.bfloat16).eps * np.abs(ref)).all(), err.max()
 
 
+@pytest.mark.parametrize("d", [128, 64])
 @pytest.mark.parametrize("mode", ["dense", "sparse", "one_pair"])
 @pytest.mark.parametrize("window,sinks", [(0, 0), (90, 5)])
-def test_prefill_bf16_extreme_values_match_oracle(pkv_lib, oracle_lib, window, sinks, mode):
+def test_prefill_bf16_extreme_values_match_oracle(pkv_lib, oracle_lib, window, sinks, mode, d):
     """bf16 caches are exact over bf16's whole range: V values far beyond the
-    fp16 range (7e4, 1e6, 1e30) and far below fp16's normal range (3e-6,
-    1e-30), in cached prefix keys and in the chunk's own keys, give the
-    oracle's output within the usual tolerance.
+    fp16 range (7e4, 1e6, 1e30, 1e35 -- the last past 2^100, where the sums
+    of weights times values need the weights scaled down to stay finite in
+    fp32) and far below fp16's normal range (3e-6, 1e-30), in cached prefix
+    keys and in the chunk's own keys, give the oracle's output within the
+    usual tolerance.
     dense: every key holds them (every key tile takes the bf16 product), and
     the columns that hold them (all of one sign, so no cancellation hides an
     error) are also within a relative 2^-7.
@@ -235,7 +238,7 @@ def test_prefill_bf16_extreme_values_match_oracle(pkv_lib, oracle_lib, window, s
     pairs that need the bf16 product."""
     dtype = torch.bfloat16
     prefixes, chunks = [30, 300], [10, 200]
-    w, q, k, v, cu, lens = _prefill_case(dtype, 8, 2, 128, 16, prefixes, chunks, window,
+    w, q, k, v, cu, lens = _prefill_case(dtype, 8, 2, d, 16, prefixes, chunks, window,
                                          seed=17)
     g = torch.Generator(device="cuda").manual_seed(23)
 
@@ -245,8 +248,8 @@ def test_prefill_bf16_extreme_values_match_oracle(pkv_lib, oracle_lib, window, s
     bt = w.block_tables.cpu().numpy()
     bs = w.spec.block_size
     # (kv head, column) -> magnitude
-    special = {(0, 3): 1.0e6, (0, 11): 1.0e-30, (1, 7): 1.0e30, (1, 12): 3.0e-6,
-               (1, 40): 7.0e4}
+    special = {(0, 3): 1.0e6, (0, 11): 1.0e-30, (0, 20): 1.0e35, (1, 7): 1.0e30,
+               (1, 12): 3.0e-6, (1, 40): 7.0e4}
     if mode == "one_pair":
         special = {(h, c): mag for (h, c), mag in special.items() if h == 1}
     for b, (p, n) in enumerate(zip(prefixes, chunks)):
@@ -285,3 +288,28 @@ def test_prefill_bf16_extreme_values_match_oracle(pkv_lib, oracle_lib, window, s
             e = err[:, h * G:(h + 1) * G, c]
             assert (r > 0).all()
             assert (e <= 2.0 ** -7 * r).all(), (h, c, float((e / r).max()))
+
+
+@pytest.mark.parametrize("dtype", [torch.float16, torch.bfloat16])
+def test_prefill_invalid_indices_give_nan_rows_only(pkv_lib, dtype):
+    """A block id outside the pool in a sequence's table, or a length the
+    table cannot hold, makes that sequence's rows NaN (never a trap, never a
+    read outside the pool); the other sequences' rows are exactly those of a
+    run without the bad sequences (bf16: the V-range scan skips the bad
+    rows too)."""
+    prefixes, chunks = [40, 70, 20], [10, 30, 25]
+    w, q, k, v, cu, lens = _prefill_case(dtype, 8, 2, 128, 16, prefixes, chunks, 0, seed=9)
+    good = pkv_lib.pkv_prefill(q, k, v, cu, w.k_cache.clone(), w.v_cache.clone(),
+                               w.block_tables, lens, 0, w.scale, max_chunk=max(chunks))
+    bt = w.block_tables.clone()
+    bt[0, 1] = w.num_blocks + 7          # a prefix block of sequence 0 past the pool
+    bad_lens = lens.clone()
+    bad_lens[2] = bt.shape[1] * w.spec.block_size + 1   # longer than sequence 2's table
+    out = pkv_lib.pkv_prefill(q, k, v, cu, w.k_cache, w.v_cache, bt, bad_lens, 0, w.scale,
+                              max_chunk=max(chunks))
+    torch.cuda.synchronize()
+    o, r = out.float().cpu(), good.float().cpu()
+    c = cu.cpu().tolist()
+    assert torch.isnan(o[c[0]:c[1]]).all()
+    assert torch.isnan(o[c[2]:c[3]]).all()
+    assert torch.equal(o[c[1]:c[2]], r[c[1]:c[2]])
