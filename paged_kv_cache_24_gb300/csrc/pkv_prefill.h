@@ -75,15 +75,18 @@ __device__ __forceinline__ PrefillItem prefill_item(const int32_t* cu_q, const i
 // that order: the hardware starts CTAs in index order, so the long items
 // start first and the short ones fill the end (longest-processing-time-first).
 // bf16 caches: the V range scan.  Each (sequence, kv head) gets row_blocks
-// partial ranges of scan_rows context rows each (a multiple of 128 rows,
-// so that row_blocks stays at most 1024).
+// partial ranges of scan_rows context rows each: scan_rows a multiple of 128,
+// at least 128, chosen so that row_blocks stays at most kPrefillScanParts (the
+// attention's warps read a pair's partials two per lane, and the partials of
+// a large batch stay a small buffer).
+constexpr int kPrefillScanParts = 64;
 struct PrefillScan {
   int scan_rows, row_blocks;
 };
 inline PrefillScan prefill_scan_plan(int max_blocks, int block_size) {
   const int64_t rows = static_cast<int64_t>(max_blocks) * block_size;
-  int64_t sr = 128;
-  while ((rows + sr - 1) / sr > 1024) sr += 128;
+  const int64_t per = (rows + kPrefillScanParts - 1) / kPrefillScanParts;
+  const int64_t sr = per <= 128 ? 128 : (per + 127) / 128 * 128;
   const int64_t rb = (rows + sr - 1) / sr;
   return PrefillScan{static_cast<int>(sr), static_cast<int>(rb > 0 ? rb : 1)};
 }

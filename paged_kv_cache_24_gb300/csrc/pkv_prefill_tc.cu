@@ -210,6 +210,16 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
   const int chunk = hh - hkv * p.num_head_chunks;
   const int lg = p.head_chunk_log2, gc = 1 << lg;
   const int tok_per_cta = kRowsCta >> lg;
+  // bf16 caches: the pair's partial V ranges (at most two per lane), read
+  // alongside the work item's own loads
+  static_assert(kPrefillScanParts <= 64, "two partials per lane");
+  uint2 part_r[2] = {make_uint2(0u, 0xffffffffu), make_uint2(0u, 0xffffffffu)};
+  if constexpr (kConvert) {
+    const uint2* part = p.vparts + (static_cast<int64_t>(b) * p.num_kv_heads + hkv) * p.row_blocks;
+#pragma unroll
+    for (int q = 0; q < 2; ++q)
+      if (lane + 32 * q < p.row_blocks) part_r[q] = __ldg(part + lane + 32 * q);
+  }
   const PrefillItem it = prefill_item(p.cu_q, p.context_lens, b, item - b * p.chunks_per_seq,
                                       tok_per_cta, p.window, p.num_sinks, p.max_blocks,
                                       p.block_size);
@@ -221,13 +231,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
     // bf16 caches: this launch takes the pairs whose V range scales into fp16
     // exactly and leaves the others to the kExact launch (each warp reduces
     // the pair's partial ranges itself)
-    uint32_t mx = 0u, mn = 0xffffffffu;
-    const uint2* part = p.vparts + (static_cast<int64_t>(b) * p.num_kv_heads + hkv) * p.row_blocks;
-    for (int i = lane; i < p.row_blocks; i += 32) {
-      const uint2 r = __ldg(part + i);
-      mx = max(mx, r.x);
-      mn = min(mn, r.y);
-    }
+    const uint32_t mx = max(part_r[0].x, part_r[1].x), mn = min(part_r[0].y, part_r[1].y);
     vr = v_range_decision(__reduce_max_sync(0xffffffffu, mx), __reduce_min_sync(0xffffffffu, mn));
     if (tid == 0) p.mode[blockIdx.x] = vr.exact ? 1u + static_cast<uint32_t>(vr.down_c) : 0u;
     if (vr.exact) return;

@@ -313,3 +313,28 @@ def test_prefill_invalid_indices_give_nan_rows_only(pkv_lib, dtype):
     assert torch.isnan(o[c[0]:c[1]]).all()
     assert torch.isnan(o[c[2]:c[3]]).all()
     assert torch.equal(o[c[1]:c[2]], r[c[1]:c[2]])
+
+
+def test_prefill_bf16_long_table_scan_sees_every_row(pkv_lib, oracle_lib):
+    """A block table longer than 64 row blocks of 128 (here 10,040 tokens)
+    is scanned in longer blocks; a single V value of 1e30 near its end must
+    still be found (else it would be converted to fp16, an infinity), and the
+    output matches the oracle."""
+    dtype = torch.bfloat16
+    prefixes, chunks = [10000], [40]
+    w, q, k, v, cu, lens = _prefill_case(dtype, 8, 2, 128, 16, prefixes, chunks, 0, seed=31)
+    bt = w.block_tables.cpu().numpy()
+    s = oracle.slot_for_position(bt[0], 16, 9500)
+    w.v_cache[s // 16, 1, s % 16, 5] = 1.0e30
+    kc_h, vc_h = w.k_cache.cpu(), w.v_cache.cpu()
+    lens_h = lens.cpu().numpy()
+    slots = [oracle.slot_for_position(bt[0], 16, lens_h[0] - 40 + i) for i in range(40)]
+    oracle.append(k.cpu(), v.cpu(), np.array(slots, np.int64), kc_h, vc_h)
+    ref = oracle.prefill(q.cpu(), cu.cpu().numpy(), kc_h, vc_h, bt, lens_h, 0, w.scale)
+    out = pkv_lib.pkv_prefill(q, k, v, cu, w.k_cache, w.v_cache, w.block_tables, lens, 0,
+                              w.scale, max_chunk=40)
+    torch.cuda.synchronize()
+    got = out.double().cpu().numpy()
+    assert np.isfinite(got).all()
+    err = np.abs(got - ref)
+    assert (err <= 2e-3 + 0.5 * torch.finfo(dtype).eps * np.abs(ref)).all(), err.max()
