@@ -160,3 +160,78 @@ def test_random_prefill(pkv_lib, oracle_lib, seed):
     assert torch.equal(_bits(w.k_cache.cpu()), _bits(kc_h)), what
     assert torch.equal(_bits(w.v_cache.cpu()), _bits(vc_h)), what
     _close(out, ref, dtype, what)
+
+
+@pytest.mark.parametrize("seed", range(12))
+def test_random_prefill_bf16_wide_range(pkv_lib, oracle_lib, seed):
+    """bf16 prefills whose (sequence, kv head) pairs each hold V at their own
+    scale, 10^-30 .. 10^30 (some pairs also one value 10^12 times larger than
+    the rest), in random shapes: the outputs match the oracle's relative to
+    each pair's scale -- through both the scaled-fp16 product and the exact
+    bf16 one (the outlier is capped at 1e37, inside bf16's range)."""
+    _, d, hkv, g, bs, prefixes, chunks, window, sinks = _prefill_case(seed + 100)
+    dtype = torch.bfloat16
+    r = np.random.default_rng(7000 + seed)
+    what = (f"seed {seed}: d={d} hkv={hkv} g={g} bs={bs} {prefixes} {chunks} "
+            f"w={window} sinks={sinks}")
+    lens = [p + n for p, n in zip(prefixes, chunks)]
+    B = len(lens)
+    spec = config_spec(0, dtype=dtype, num_seqs=B, num_q_heads=hkv * g, num_kv_heads=hkv,
+                       head_dim=d, block_size=bs, lens=lens, explicit_pool=None,
+                       lens_are_pre_append=False, window=0, seed=8000 + seed)
+    w = make_workload(spec, device="cuda")
+    bt = w.block_tables.cpu().numpy()
+    gen = torch.Generator(device="cuda").manual_seed(9000 + seed)
+    T = sum(chunks)
+    q = torch.randn(T, hkv * g, d, generator=gen, device="cuda").to(dtype)
+    k = torch.randn(T, hkv, d, generator=gen, device="cuda").to(dtype)
+    v = torch.randn(T, hkv, d, generator=gen, device="cuda").to(dtype)
+    starts = np.concatenate([[0], np.cumsum(chunks)])
+    scale = np.ones((B, hkv))
+    for b in range(B):
+        prefix_slots = np.array([oracle.slot_for_position(bt[b], bs, t)
+                                 for t in range(prefixes[b])], np.int64)
+        for h in range(hkv):
+            s = 10.0 ** int(r.integers(-30, 31))
+            scale[b, h] = s
+            if prefix_slots.size:
+                blk = torch.from_numpy(prefix_slots // bs).to("cuda")
+                row = torch.from_numpy(prefix_slots % bs).to("cuda")
+                w.v_cache[blk, h, row] = (w.v_cache[blk, h, row].double() * s).to(dtype)
+            v[starts[b]:starts[b + 1], h] = (v[starts[b]:starts[b + 1], h].double() * s).to(dtype)
+            if r.random() < 0.3:  # one value far above the pair's others (finite in bf16)
+                t = int(r.integers(0, lens[b]))
+                c = int(r.integers(0, d))
+                big = min(1.0e12 * s, 1.0e37)
+                if t < prefixes[b]:
+                    sl = oracle.slot_for_position(bt[b], bs, t)
+                    w.v_cache[sl // bs, h, sl % bs, c] = big
+                else:
+                    v[starts[b] + t - prefixes[b], h, c] = big
+    # the chunk's own slots start as NaN: the prefill must write them first
+    slots = np.array([oracle.slot_for_position(bt[b], bs, t)
+                      for b, (p, L) in enumerate(zip(prefixes, lens)) for t in range(p, L)],
+                     np.int64)
+    w.k_cache[torch.from_numpy(slots // bs).to("cuda"), :,
+              torch.from_numpy(slots % bs).to("cuda")] = float("nan")
+    w.v_cache[torch.from_numpy(slots // bs).to("cuda"), :,
+              torch.from_numpy(slots % bs).to("cuda")] = float("nan")
+    cu = torch.tensor(starts, dtype=torch.int32, device="cuda")
+    L = torch.tensor(lens, dtype=torch.int32, device="cuda")
+    kc_h, vc_h = w.k_cache.cpu(), w.v_cache.cpu()
+    oracle.append(k.cpu(), v.cpu(), slots, kc_h, vc_h)
+    ref = oracle.prefill(q.cpu(), cu.cpu().numpy(), kc_h, vc_h, bt, np.array(lens, np.int32),
+                         window, w.scale, num_sinks=sinks)
+    out = torch.full_like(q, float("nan"))
+    pkv_lib.pkv_prefill(q, k, v, cu, w.k_cache, w.v_cache, w.block_tables, L, window, w.scale,
+                        max_chunk=max(chunks), out=out, num_sinks=sinks)
+    torch.cuda.synchronize()
+    got = out.double().cpu().numpy()
+    assert np.isfinite(got).all(), what
+    # every output row of sequence b, query head hq is in units of its pair's scale
+    row_scale = np.repeat(np.repeat(scale, g, axis=1)[:, None, :], 1, axis=1)
+    tok_b = np.repeat(np.arange(B), chunks)
+    s = row_scale[tok_b][:, 0, :, None]          # [T, Hq, 1]
+    err = np.abs(got - ref) / s
+    tol = 2e-3 + 0.5 * torch.finfo(dtype).eps * np.abs(ref) / s
+    assert (err <= tol).all(), f"{what}: max scaled err {err.max():.3e}"
