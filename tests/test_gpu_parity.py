@@ -338,3 +338,45 @@ def test_serving_mix_32_steps(pkv_lib, oracle_lib):
     torch.cuda.synchronize()
     assert torch.equal(_bits(w.k_cache.cpu()), _bits(mirror.kc))
     assert torch.equal(_bits(w.v_cache.cpu()), _bits(mirror.vc))
+
+
+@pytest.mark.parametrize("tps", [0, 64])
+def test_decode_bf16_wide_range(pkv_lib, oracle_lib, tps):
+    """bf16 pools whose (sequence, kv head) pairs each hold V at their own
+    scale, 10^-30 .. 10^30, some with one value 10^12 above the rest (capped
+    inside bf16's range): every output matches the oracle relative to its
+    pair's scale (V stays bf16 in the decode's products; P is carried as hi +
+    lo parts), with and without split contexts."""
+    dtype = torch.bfloat16
+    B, hq, hkv, d = 6, 16, 4, 128
+    spec = config_spec(0, dtype=dtype, num_seqs=B, num_q_heads=hq, num_kv_heads=hkv,
+                       head_dim=d, block_size=16, lens=[1, 17, 300, 777, 1500, 2100],
+                       explicit_pool=None, lens_are_pre_append=False, seed=77)
+    w = make_workload(spec, device="cuda", poison_outside_window=True)
+    r = np.random.default_rng(78)
+    bt = w.block_tables.cpu().numpy()
+    lens = w.lens_steps[0].cpu().numpy()
+    scale = np.ones((B, hkv))
+    for b in range(B):
+        sl = np.array([oracle.slot_for_position(bt[b], 16, t) for t in range(lens[b] - 1)],
+                      np.int64)
+        for h in range(hkv):
+            s = 10.0 ** int(r.integers(-30, 31))
+            scale[b, h] = s
+            if sl.size:
+                blk, row = torch.from_numpy(sl // 16).cuda(), torch.from_numpy(sl % 16).cuda()
+                w.v_cache[blk, h, row] = (w.v_cache[blk, h, row].double() * s).to(dtype)
+            w.v_steps[0][b, h] = (w.v_steps[0][b, h].double() * s).to(dtype)
+            if sl.size and r.random() < 0.4:
+                t = int(r.integers(0, sl.size))
+                w.v_cache[sl[t] // 16, h, sl[t] % 16, int(r.integers(0, d))] = min(1e12 * s, 1e37)
+    mirror = HostMirror(w)
+    _, ref = mirror.step(0)
+    _, out = gpu_step(pkv_lib, w, 0, tokens_per_split=tps)
+    torch.cuda.synchronize()
+    got = out.double().cpu().numpy()
+    assert np.isfinite(got).all()
+    s = np.repeat(scale, hq // hkv, axis=1)[:, :, None]     # [B, Hq, 1]
+    err = np.abs(got - ref) / s
+    tol = 2e-3 + 0.5 * torch.finfo(dtype).eps * np.abs(ref) / s
+    assert (err <= tol).all(), f"max scaled err {err.max():.3e}"
