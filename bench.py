@@ -560,7 +560,7 @@ def measure_decode(pkv, spec, steps, warmup, path, pg=None, world=1, local_rank=
                    traffic_key=None):
     """Time `steps` decode steps (append + decode) of workload `spec`: CUDA
     graphs of the C-ABI calls replayed on one stream, CUDA events around each
-    step and around the decode launch.  Returns the measured times, bytes and
+    step and (separate path) around its decode launch.  Returns the measured times, bytes and
     the roofline record (its `traffic` from the committed record for
     `traffic_key`); `w` is the workload (for the end-to-end and CPU legs)."""
     from paged_kv_cache_24_gb300.workloads import make_workload
@@ -654,8 +654,11 @@ def measure_decode(pkv, spec, steps, warmup, path, pg=None, world=1, local_rank=
             i = s % S
             ev[s][0].record(stream)
             if not fused:
+                # the decode launch's own start (with the fused call the step
+                # is that launch: a second event here would only add its own
+                # cost, ~2 us of GPU time, to every step)
                 g_app[i].replay()
-            ev[s][1].record(stream)
+                ev[s][1].record(stream)
             g_dec[i].replay()
             ev[s][2].record(stream)
         t_end.record(stream)
@@ -663,7 +666,7 @@ def measure_decode(pkv, spec, steps, warmup, path, pg=None, world=1, local_rank=
     if pg:
         pg.barrier()
     step_ms = [ev[s][0].elapsed_time(ev[s][2]) for s in range(steps)]
-    dec_ms = [ev[s][1].elapsed_time(ev[s][2]) for s in range(steps)]
+    dec_ms = step_ms if fused else [ev[s][1].elapsed_time(ev[s][2]) for s in range(steps)]
     loop_ms = t_start.elapsed_time(t_end)
     # the step time: whole loop / K when nothing else ran in it, else the sum of steps
     total_ms = sum(step_ms) if need_flush else loop_ms
