@@ -351,8 +351,11 @@ def percentiles_ms(times_ms):
     return {f"p{q}": float(np.percentile(a, q)) for q in (10, 50, 90)}
 
 
-def measure_prefill(pkv, workload, steps, warmup):
-    """Time `pkv_prefill` on a prefill workload; returns the JSON line's dict."""
+def prefill_inputs(workload):
+    """The seeded inputs of a prefill workload on the device: the workload
+    (pools holding every sequence's cached prefix), the packed chunk's q, k
+    and v, the chunk offsets cu, the lengths L after the chunk, the chunk
+    length and the prefixes."""
     from paged_kv_cache_24_gb300.workloads import config_spec, make_workload
 
     c = PREFILL[workload]
@@ -372,6 +375,15 @@ def measure_prefill(pkv, workload, steps, warmup):
     v = torch.randn(T, hkv, d, generator=g, device="cuda").to(spec.dtype)
     cu = torch.arange(0, T + 1, chunk, dtype=torch.int32, device="cuda")
     L = torch.tensor(lens, dtype=torch.int32, device="cuda")
+    return w, q, k, v, cu, L, chunk, prefix
+
+
+def measure_prefill(pkv, workload, steps, warmup):
+    """Time `pkv_prefill` on a prefill workload; returns the JSON line's dict."""
+    w, q, k, v, cu, L, chunk, prefix = prefill_inputs(workload)
+    spec = w.spec
+    B, T = spec.num_seqs, q.shape[0]
+    hq, hkv, d = spec.num_q_heads, spec.num_kv_heads, spec.head_dim
     out = torch.empty_like(q)
     # algorithmic flops: every (query row, attended key) pair costs 2 D (QK) + 2 D (PV)
     flops = float(sum(int(chunk) * int(p) + chunk * (chunk + 1) // 2 for p in prefix)) * hq * 4 * d

@@ -338,3 +338,49 @@ def test_prefill_bf16_long_table_scan_sees_every_row(pkv_lib, oracle_lib):
     assert np.isfinite(got).all()
     err = np.abs(got - ref)
     assert (err <= 2e-3 + 0.5 * torch.finfo(dtype).eps * np.abs(ref)).all(), err.max()
+
+
+@pytest.mark.parametrize("workload", ["prefill_bf16", "prefill_fp16"])
+def test_prefill_benchmark_workload_sampled(pkv_lib, oracle_lib, workload):
+    """The bench's prefill workloads at their full size (4 sequences, a
+    1024-token chunk each after a 2048-6144-token cached prefix, 32 query / 8
+    kv heads, head_dim 128, block size 16), in the call the bench times: the
+    pools after the chunk's append equal the oracle's bit for bit, and sampled
+    rows -- every query head of each sequence's first and last chunk token and
+    of 30 random ones -- match the float64 oracle.  Without a window, the row
+    of the token at position p attends keys 0 .. p ("Building a Streaming
+    Sliding-Window Attention Engine in Pure Python", Step 3,
+    prefill_attention, read row-wise): the oracle's decode of that query with
+    context length p + 1."""
+    import bench
+
+    w, q, k, v, cu, L, chunk, _ = bench.prefill_inputs(workload)
+    spec = w.spec
+    bs, dtype = spec.block_size, spec.dtype
+    kc_h, vc_h = w.k_cache.cpu(), w.v_cache.cpu()
+    bt = w.block_tables.cpu().numpy()
+    lens, cu_h = L.cpu().numpy(), cu.cpu().numpy()
+    out = torch.full_like(q, float("nan"))
+    pkv_lib.pkv_prefill(q, k, v, cu, w.k_cache, w.v_cache, w.block_tables, L, 0, w.scale,
+                        max_chunk=chunk, out=out)
+    torch.cuda.synchronize()
+    slots = [oracle.slot_for_position(bt[b], bs, int(lens[b]) - chunk + i)
+             for b in range(spec.num_seqs) for i in range(chunk)]
+    oracle.append(k.cpu(), v.cpu(), np.array(slots, np.int64), kc_h, vc_h)
+    assert torch.equal(_bits(w.k_cache.cpu()), _bits(kc_h))
+    assert torch.equal(_bits(w.v_cache.cpu()), _bits(vc_h))
+
+    r = np.random.default_rng(41)
+    toks = []
+    for b in range(spec.num_seqs):
+        sel = {0, chunk - 1} | set(r.choice(chunk, 30, replace=False).tolist())
+        toks += [(b, i) for i in sorted(sel)]
+    rows = torch.tensor([int(cu_h[b]) + i for b, i in toks], device=q.device)
+    ctx = np.array([int(lens[b]) - chunk + i + 1 for b, i in toks], np.int32)
+    ref = oracle.decode(q[rows].cpu(), kc_h, vc_h, np.stack([bt[b] for b, _ in toks]), ctx, 0,
+                        w.scale)
+    g = out[rows].double().cpu().numpy()
+    assert np.isfinite(g).all()
+    err = np.abs(g - ref)
+    tol = 2e-3 + 0.5 * torch.finfo(dtype).eps * np.abs(ref)
+    assert (err <= tol).all(), f"max err {err.max():.3e}"
