@@ -4,6 +4,8 @@ prefill (with windows and sinks), on shapes drawn from the supported ranges -- h
 page sizes, ragged lengths, windows, attention sinks and split sizes.  Every
 output and the whole pool after the append are compared; a failing case
 names its seed."""
+import os
+
 import numpy as np
 import pytest
 import torch
@@ -14,6 +16,10 @@ from paged_kv_cache_24_gb300.workloads import config_spec, make_workload
 pytestmark = pytest.mark.gpu
 
 BASE_TOL = {torch.float32: 1e-5, torch.float16: 2e-3, torch.bfloat16: 2e-3}
+# seeds per sweep; a longer sweep sets these (e.g. PKV_RANDOM_DECODE_SEEDS=5000)
+N_DECODE = int(os.environ.get("PKV_RANDOM_DECODE_SEEDS", "30"))
+N_PREFILL = int(os.environ.get("PKV_RANDOM_PREFILL_SEEDS", "24"))
+N_WIDE = int(os.environ.get("PKV_RANDOM_WIDE_SEEDS", "12"))
 KINDS = ("fp32", "fp16", "bf16", "fp8", "int8")
 DTYPE = {"fp32": torch.float32, "fp16": torch.float16, "bf16": torch.bfloat16,
          "fp8": torch.float16, "int8": torch.float16}
@@ -59,7 +65,7 @@ def _decode_case(seed):
     return kind, over, tps, fused
 
 
-@pytest.mark.parametrize("seed", range(30))
+@pytest.mark.parametrize("seed", range(N_DECODE))
 def test_random_decode(pkv_lib, oracle_lib, seed):
     kind, over, tps, fused = _decode_case(seed)
     what = f"seed {seed}: {kind} {over} tps={tps} fused={fused}"
@@ -123,7 +129,7 @@ def _prefill_case(seed):
     return dtype, d, hkv, g, bs, prefixes, chunks, window, sinks
 
 
-@pytest.mark.parametrize("seed", range(24))
+@pytest.mark.parametrize("seed", range(N_PREFILL))
 def test_random_prefill(pkv_lib, oracle_lib, seed):
     dtype, d, hkv, g, bs, prefixes, chunks, window, sinks = _prefill_case(seed)
     what = (f"seed {seed}: {dtype} d={d} hkv={hkv} g={g} bs={bs} {prefixes} {chunks} "
@@ -162,7 +168,7 @@ def test_random_prefill(pkv_lib, oracle_lib, seed):
     _close(out, ref, dtype, what)
 
 
-@pytest.mark.parametrize("seed", range(12))
+@pytest.mark.parametrize("seed", range(N_WIDE))
 def test_random_prefill_bf16_wide_range(pkv_lib, oracle_lib, seed):
     """bf16 prefills whose (sequence, kv head) pairs each hold V at their own
     scale, 10^-30 .. 10^30 (some pairs also one value 10^12 times larger than
