@@ -11,9 +11,11 @@ pinned staging buffer.  The kernels read the queries and the new K/V
 straight from it over the host link, and the rest (positions, lengths, block
 tables) reaches the device first in a single ``pkv_stage_copy`` kernel that
 reads the pinned buffer directly (the copy engine where the GPU cannot reach
-it); with ``direct_in=False`` everything is copied in that way.  The decode kernels
-write the attention output straight into a pinned host buffer (with
-``direct_out=False`` it comes back in a second copy).  The graph replays
+it); with ``direct_in=False`` everything is copied in that way.  The
+attention output comes back in a second copy of that kind, or, with
+``direct_out=True``, the decode kernels write it straight into a pinned host
+buffer (the default when every context is planned as one split, so that no
+combine pass writes the rows at the end).  The graph replays
 ``pkv_slot_mapping``, ``pkv_append`` and ``pkv_decode`` exactly as the eager
 calls would run them.  The K/V pools stay resident on the device.
 
@@ -32,8 +34,8 @@ from __future__ import annotations
 import torch
 
 from ._binding import (cache_layout, pkv_append, pkv_append_decode, pkv_append_fp8,
-                       pkv_append_int8, pkv_decode, pkv_device_address, pkv_slot_mapping,
-                       pkv_stage_copy, PKV_ERR_UNSUPPORTED)
+                       pkv_append_int8, pkv_decode, pkv_decode_plan, pkv_device_address,
+                       pkv_slot_mapping, pkv_stage_copy, PKV_ERR_UNSUPPORTED)
 
 _ALIGN = 256
 
@@ -43,7 +45,7 @@ class DecodeStep:
                  num_q_heads: int, max_blocks: int, window: int, scale: float,
                  copy_block_tables: bool = True, num_buffers: int = 1, use_graph: bool = True,
                  fused: bool = True, k_scale: torch.Tensor | None = None,
-                 v_scale: torch.Tensor | None = None, direct_out: bool = True,
+                 v_scale: torch.Tensor | None = None, direct_out: bool | None = None,
                  direct_in: bool = True):
         layout = cache_layout(k_cache)
         self.k_cache, self.v_cache = k_cache, v_cache
@@ -98,12 +100,23 @@ class DecodeStep:
         self.host_out = torch.empty((B, hq, d), dtype=dt).pin_memory()
         # direct_out: the decode writes the result straight into the pinned
         # buffer where the GPU can address it, instead of a copy back after it.
-        # Measured end to end: the serving mix (8 MB of output a step) 0.3030
-        # -> 0.2566 ms, the MHA step (512 KB) 0.3567 -> 0.3574 ms.
+        # By default only when the plan gives every context one split: then
+        # the decode's CTAs write their rows over the host link while the
+        # launch runs (the serving mix, 8 MB of output a step: 0.3030 ->
+        # 0.2566 ms a step end to end); with a combine pass, that pass would
+        # write every row over the link at the end, and the copy back is
+        # faster (device time a step: the GQA step 0.704 against 0.728 ms,
+        # the MHA step 0.3367 against 0.3382).
+        if direct_out is None:
+            direct_out = pkv_decode_plan(num_seqs, num_q_heads, layout, max_blocks,
+                                         self.window)[1] == 1
         self.direct_out = direct_out and pkv_device_address(self.host_out) is not None
         self.h2d_bytes = self._staged_bytes
         self.d2h_bytes = self.host_out.numel() * self.host_out.element_size()
         self.stream = torch.cuda.Stream(device=dev)
+        # ordering with the caller's stream, recorded afresh on every run
+        self._caller_done = torch.cuda.Event()
+        self._step_done = torch.cuda.Event()
         self.graphs = None
         if use_graph:
             # an eager pass with empty contexts and no writes sizes the decode
@@ -159,7 +172,9 @@ class DecodeStep:
     def run(self, i: int = 0, wait: bool = True) -> torch.Tensor:
         """Copy staging buffer i in, run the step, copy the output back."""
         caller = torch.cuda.current_stream(self.stream.device)
-        self.stream.wait_stream(caller)   # after whatever the caller queued on the pools
+        # after whatever the caller queued on the pools
+        self._caller_done.record(caller)
+        self.stream.wait_event(self._caller_done)
         with torch.cuda.stream(self.stream):
             if self.graphs is not None:
                 self.graphs[i].replay()
@@ -168,5 +183,6 @@ class DecodeStep:
         if wait:
             self.stream.synchronize()
         else:
-            caller.wait_stream(self.stream)
+            self._step_done.record(self.stream)
+            caller.wait_event(self._step_done)
         return self.host_out
