@@ -748,33 +748,57 @@ decode_f32_kernel(const DecodeParams p) {
   const float* kc = static_cast<const float*>(p.k_cache);
   const float* vc = static_cast<const float*>(p.v_cache);
 
+  // Rows of a unit come in batches of kBatch warp steps, all their loads
+  // issued before any of them is used (one round trip to memory per batch,
+  // not per row); the next unit's block-table entry is read while the
+  // current unit's rows are in flight.
+  constexpr int kSteps = kUnitTokens / RPW;
+  constexpr int kBatch = D == 128 ? 4 : (kSteps < 8 ? kSteps : 8);  // (D 128: no spills)
+  auto page_of = [&](int u) -> int32_t {
+    return u < w.u1 ? __ldg(p.block_tables + static_cast<int64_t>(w.b) * p.max_blocks +
+                            phys_unit(w.su, u) * kUnitTokens / p.block_size)
+                    : -1;
+  };
+  int32_t pb_next = page_of(w.u0 + warp);
   for (int u = w.u0 + warp; u < w.u1; u += kDecodeWarps) {
     const int t0 = phys_unit(w.su, u) * kUnitTokens;
-    const int32_t pb = __ldg(p.block_tables + static_cast<int64_t>(w.b) * p.max_blocks +
-                             t0 / p.block_size);
+    const int32_t pb = pb_next;
+    pb_next = page_of(u + kDecodeWarps);
     if (pb < 0 || pb >= p.num_blocks) {
       bad = true;
       continue;
     }
     const int64_t tile = ((static_cast<int64_t>(pb) * p.num_kv_heads + w.hkv) * p.block_size +
                           (t0 % p.block_size)) * D;
-    for (int r = sub; r < kUnitTokens; r += RPW) {
-      const int t = t0 + r;
-      const bool valid = attended(w.su, w.L, t);
-      float4 k4 = make_float4(0.f, 0.f, 0.f, 0.f), v4 = k4;
-      if (valid && p.k_new != nullptr && t == w.L - 1) {
-        // fused append: attend to the new token and store it to its slot
-        const int64_t src = (static_cast<int64_t>(w.b) * p.num_kv_heads + w.hkv) * D;
-        k4 = __ldg(reinterpret_cast<const float4*>(static_cast<const float*>(p.k_new) + src) + li);
-        v4 = __ldg(reinterpret_cast<const float4*>(static_cast<const float*>(p.v_new) + src) + li);
-        if (w.h0 == w.hkv * p.group) {
-          reinterpret_cast<float4*>(static_cast<float*>(p.k_dst) + tile + r * D)[li] = k4;
-          reinterpret_cast<float4*>(static_cast<float*>(p.v_dst) + tile + r * D)[li] = v4;
+    for (int s0 = 0; s0 < kSteps; s0 += kBatch) {
+      float4 kb[kBatch], vb[kBatch];
+      bool vok[kBatch];
+#pragma unroll
+      for (int i = 0; i < kBatch; ++i) {
+        const int r = sub + (s0 + i) * RPW;
+        const int t = t0 + r;
+        const bool valid = attended(w.su, w.L, t);
+        vok[i] = valid;
+        kb[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+        vb[i] = kb[i];
+        if (valid && p.k_new != nullptr && t == w.L - 1) {
+          // fused append: attend to the new token and store it to its slot
+          const int64_t src = (static_cast<int64_t>(w.b) * p.num_kv_heads + w.hkv) * D;
+          kb[i] = __ldg(reinterpret_cast<const float4*>(static_cast<const float*>(p.k_new) + src) + li);
+          vb[i] = __ldg(reinterpret_cast<const float4*>(static_cast<const float*>(p.v_new) + src) + li);
+          if (w.h0 == w.hkv * p.group) {
+            reinterpret_cast<float4*>(static_cast<float*>(p.k_dst) + tile + r * D)[li] = kb[i];
+            reinterpret_cast<float4*>(static_cast<float*>(p.v_dst) + tile + r * D)[li] = vb[i];
+          }
+        } else if (valid) {
+          kb[i] = __ldg(reinterpret_cast<const float4*>(kc + tile + r * D) + li);
+          vb[i] = __ldg(reinterpret_cast<const float4*>(vc + tile + r * D) + li);
         }
-      } else if (valid) {
-        k4 = __ldg(reinterpret_cast<const float4*>(kc + tile + r * D) + li);
-        v4 = __ldg(reinterpret_cast<const float4*>(vc + tile + r * D) + li);
       }
+#pragma unroll
+      for (int i = 0; i < kBatch; ++i) {
+      const bool valid = vok[i];
+      const float4 k4 = kb[i], v4 = vb[i];
 #pragma unroll
       for (int qi = 0; qi < QT; ++qi) {
         float part = qv[qi].x * k4.x + qv[qi].y * k4.y + qv[qi].z * k4.z + qv[qi].w * k4.w;
@@ -792,6 +816,7 @@ decode_f32_kernel(const DecodeParams p) {
           acc[qi].z = acc[qi].z * alpha + pw * v4.z;
           acc[qi].w = acc[qi].w * alpha + pw * v4.w;
         }
+      }
       }
     }
   }
