@@ -384,3 +384,40 @@ def test_prefill_benchmark_workload_sampled(pkv_lib, oracle_lib, workload):
     err = np.abs(g - ref)
     tol = 2e-3 + 0.5 * torch.finfo(dtype).eps * np.abs(ref)
     assert (err <= tol).all(), f"max err {err.max():.3e}"
+
+
+def test_prefill_two_streams_concurrently(pkv_lib, oracle_lib):
+    """Two prefills at the same time on two streams (each stream has its own
+    workspace: work order, counters, V ranges), launched interleaved for
+    several rounds without synchronisation between the streams: every
+    round's rows match the oracle and the pools end bit for bit as its."""
+    cases = [(torch.float16, [300, 40, 0], [200, 77, 130], 0, 51),
+             (torch.bfloat16, [1000, 5], [64, 300], 0, 52)]
+    prepared = []
+    for dtype, prefixes, chunks, window, seed in cases:
+        w, q, k, v, cu, lens = _prefill_case(dtype, 8, 2, 128, 16, prefixes, chunks, window, seed)
+        ref, kc_h, vc_h = _oracle_prefill(w, q, k, v, cu, lens, chunks, window)
+        prepared.append((w, q, k, v, cu, lens, chunks, window, ref, kc_h, vc_h, dtype))
+    streams = [torch.cuda.Stream(), torch.cuda.Stream()]
+    for st in streams:
+        st.wait_stream(torch.cuda.current_stream())
+    outs = []
+    for _ in range(3):
+        for i, st in enumerate(streams):
+            w, q, k, v, cu, lens, chunks, window = prepared[i][:8]
+            with torch.cuda.stream(st):
+                # the same chunk again: its append rewrites the same rows
+                outs.append((i, pkv_lib.pkv_prefill(q, k, v, cu, w.k_cache, w.v_cache,
+                                                    w.block_tables, lens, window, w.scale,
+                                                    max_chunk=max(chunks), stream=st)))
+    torch.cuda.synchronize()
+    for i, out in outs:
+        ref, dtype = prepared[i][8], prepared[i][11]
+        g = out.double().cpu().numpy()
+        assert np.isfinite(g).all()
+        err = np.abs(g - ref)
+        assert (err <= 2e-3 + 0.5 * torch.finfo(dtype).eps * np.abs(ref)).all(), err.max()
+    for p_ in prepared:
+        w, kc_h, vc_h = p_[0], p_[9], p_[10]
+        assert torch.equal(_bits(w.k_cache.cpu()), _bits(kc_h))
+        assert torch.equal(_bits(w.v_cache.cpu()), _bits(vc_h))
