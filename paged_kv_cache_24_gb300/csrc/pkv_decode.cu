@@ -797,26 +797,26 @@ decode_f32_kernel(const DecodeParams p) {
       }
 #pragma unroll
       for (int i = 0; i < kBatch; ++i) {
-      const bool valid = vok[i];
-      const float4 k4 = kb[i], v4 = vb[i];
+        const bool valid = vok[i];
+        const float4 k4 = kb[i], v4 = vb[i];
 #pragma unroll
-      for (int qi = 0; qi < QT; ++qi) {
-        float part = qv[qi].x * k4.x + qv[qi].y * k4.y + qv[qi].z * k4.z + qv[qi].w * k4.w;
+        for (int qi = 0; qi < QT; ++qi) {
+          float part = qv[qi].x * k4.x + qv[qi].y * k4.y + qv[qi].z * k4.z + qv[qi].w * k4.w;
 #pragma unroll
-        for (int off = 1; off < LPR; off <<= 1) part += __shfl_xor_sync(0xffffffffu, part, off);
-        if (valid) {
-          const float sc = part * p.scale_log2;
-          const float mnew = fmaxf(m[qi], sc);
-          const float alpha = ex2(m[qi] - mnew);
-          const float pw = ex2(sc - mnew);
-          m[qi] = mnew;
-          l[qi] = l[qi] * alpha + pw;
-          acc[qi].x = acc[qi].x * alpha + pw * v4.x;
-          acc[qi].y = acc[qi].y * alpha + pw * v4.y;
-          acc[qi].z = acc[qi].z * alpha + pw * v4.z;
-          acc[qi].w = acc[qi].w * alpha + pw * v4.w;
+          for (int off = 1; off < LPR; off <<= 1) part += __shfl_xor_sync(0xffffffffu, part, off);
+          if (valid) {
+            const float sc = part * p.scale_log2;
+            const float mnew = fmaxf(m[qi], sc);
+            const float alpha = ex2(m[qi] - mnew);
+            const float pw = ex2(sc - mnew);
+            m[qi] = mnew;
+            l[qi] = l[qi] * alpha + pw;
+            acc[qi].x = acc[qi].x * alpha + pw * v4.x;
+            acc[qi].y = acc[qi].y * alpha + pw * v4.y;
+            acc[qi].z = acc[qi].z * alpha + pw * v4.z;
+            acc[qi].w = acc[qi].w * alpha + pw * v4.w;
+          }
         }
-      }
       }
     }
   }
