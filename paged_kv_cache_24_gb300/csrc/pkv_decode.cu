@@ -700,16 +700,20 @@ decode16_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant_
 // ---------------------------------------------------------------------------
 // fp32 pools: CUDA-core path with the same work split.
 
+// fp32 pools: warps per CTA (each a unit at a time; short contexts need
+// more of them side by side to hide the memory latency)
+constexpr int kF32Warps = 8;
+
 template <int D>
-__global__ void __launch_bounds__(kThreads)
+__global__ void __launch_bounds__(kF32Warps * 32)
 decode_f32_kernel(const DecodeParams p) {
   constexpr int QT = 8;          // query heads per CTA
   constexpr int LPR = D / 4;     // lanes per context row (one float4 each)
   constexpr int RPW = 32 / LPR;  // rows per warp step
   constexpr int DP = D + 4;
-  __shared__ float so[kDecodeWarps * QT * DP];
-  __shared__ float sm[kDecodeWarps * QT];
-  __shared__ float sl[kDecodeWarps * QT];
+  __shared__ float so[kF32Warps * QT * DP];
+  __shared__ float sm[kF32Warps * QT];
+  __shared__ float sl[kF32Warps * QT];
   __shared__ int s_bad;
 
   const int lane = threadIdx.x & 31;
@@ -760,10 +764,10 @@ decode_f32_kernel(const DecodeParams p) {
                     : -1;
   };
   int32_t pb_next = page_of(w.u0 + warp);
-  for (int u = w.u0 + warp; u < w.u1; u += kDecodeWarps) {
+  for (int u = w.u0 + warp; u < w.u1; u += kF32Warps) {
     const int t0 = phys_unit(w.su, u) * kUnitTokens;
     const int32_t pb = pb_next;
-    pb_next = page_of(u + kDecodeWarps);
+    pb_next = page_of(u + kF32Warps);
     if (pb < 0 || pb >= p.num_blocks) {
       bad = true;
       continue;
@@ -858,7 +862,7 @@ decode_f32_kernel(const DecodeParams p) {
     }
   }
   __syncthreads();
-  merge_and_store<float, D, QT, DP>(so, sm, sl, p, w, s_bad != 0);
+  merge_and_store<float, D, QT, DP, kF32Warps>(so, sm, sl, p, w, s_bad != 0);
 }
 
 // ---------------------------------------------------------------------------
@@ -983,8 +987,8 @@ cudaError_t launch_decode_16bit(int dtype, int head_dim, int ntiles, const CUten
 cudaError_t launch_decode_f32(int head_dim, const DecodeParams& p, cudaStream_t stream) {
   dim3 grid(p.num_splits, p.num_kv_heads * p.num_head_chunks, p.num_seqs);
   if (head_dim == 128)
-    return launch_pdl(decode_f32_kernel<128>, grid, dim3(kThreads), 0, stream, p);
-  return launch_pdl(decode_f32_kernel<64>, grid, dim3(kThreads), 0, stream, p);
+    return launch_pdl(decode_f32_kernel<128>, grid, dim3(kF32Warps * 32), 0, stream, p);
+  return launch_pdl(decode_f32_kernel<64>, grid, dim3(kF32Warps * 32), 0, stream, p);
 }
 
 cudaError_t launch_combine(int dtype, int head_dim, const DecodeParams& p, cudaStream_t stream) {
