@@ -704,10 +704,11 @@ decode16_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant_
 // more of them side by side to hide the memory latency)
 constexpr int kF32Warps = 8;
 
-template <int D>
+// QT: query heads a CTA computes (1, 2, 4 or 8: the plan's head chunk
+// rounded up), so that an MHA pool does no work for seven empty heads.
+template <int D, int QT>
 __global__ void __launch_bounds__(kF32Warps * 32)
 decode_f32_kernel(const DecodeParams p) {
-  constexpr int QT = 8;          // query heads per CTA
   constexpr int LPR = D / 4;     // lanes per context row (one float4 each)
   constexpr int RPW = 32 / LPR;  // rows per warp step
   constexpr int DP = D + 4;
@@ -984,11 +985,20 @@ cudaError_t launch_decode_16bit(int dtype, int head_dim, int ntiles, const CUten
 #undef PKV_LAUNCH16
 }
 
+template <int D>
+cudaError_t launch_f32_d(const DecodeParams& p, dim3 grid, cudaStream_t stream) {
+  const dim3 block(kF32Warps * 32);
+  if (p.head_chunk <= 1) return launch_pdl(decode_f32_kernel<D, 1>, grid, block, 0, stream, p);
+  if (p.head_chunk <= 2) return launch_pdl(decode_f32_kernel<D, 2>, grid, block, 0, stream, p);
+  if (p.head_chunk <= 4) return launch_pdl(decode_f32_kernel<D, 4>, grid, block, 0, stream, p);
+  return launch_pdl(decode_f32_kernel<D, 8>, grid, block, 0, stream, p);
+}
+
 cudaError_t launch_decode_f32(int head_dim, const DecodeParams& p, cudaStream_t stream) {
   dim3 grid(p.num_splits, p.num_kv_heads * p.num_head_chunks, p.num_seqs);
-  if (head_dim == 128)
-    return launch_pdl(decode_f32_kernel<128>, grid, dim3(kF32Warps * 32), 0, stream, p);
-  return launch_pdl(decode_f32_kernel<64>, grid, dim3(kF32Warps * 32), 0, stream, p);
+  if (p.head_chunk > 8) return cudaErrorInvalidConfiguration;  // the plan caps fp32 at 8
+  if (head_dim == 128) return launch_f32_d<128>(p, grid, stream);
+  return launch_f32_d<64>(p, grid, stream);
 }
 
 cudaError_t launch_combine(int dtype, int head_dim, const DecodeParams& p, cudaStream_t stream) {
